@@ -1,0 +1,393 @@
+"""Benchmark of the KDA hot path on GB300.
+
+One step = one pass of the whole path over one batch: the chunk table,
+forward (saving for the backward) and backward of the 300M-shape layer call
+(B=16, T=2048, H=8, dk=32, dv=64, bf16 inputs, fp32 state), i.e.
+kda_fwd + kda_bwd through the C ABI.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
+on the launch stream; between steps a 512 MiB buffer is written so that the
+L2 (129 MB on GB300) is flushed before every timed step.  Under torchrun each
+rank runs its own batch (weak scaling, no collective on the data path); the
+reported time is the max over ranks.
+
+--impl reference times the plain CPU oracle (the only other implementation
+of the method here) on the host cores, one full workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from kimi_delta_attention_bwd_gb300.inputs import BASE_SEED, WORKLOADS, make_inputs, numpy_f64  # noqa: E402
+
+METRIC = "KDA fwd and fwd+bwd tokens/s on 1 GB300 at 300M shape; % of roofline"
+STEP_WORKLOAD = 3   # fwd+bwd training step at the 300M layer shape
+FWD_WORKLOAD = 1    # forward only at the same shape
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def algorithmic_bytes(w, kernel: str) -> float:
+    """Algorithmic bytes one launch of `kernel` must move for workload w: each
+    input it needs read once, each output it produces written once (bf16 io,
+    fp32 parameters); per-chunk states and workspace are not counted."""
+    e = 2 if w.dtype == "bf16" else 4
+    th = w.B * w.T * w.H  # token-heads
+    dk, dv = w.dk, w.dv
+    inputs_fwd = e * (3 * dk + dv + 1)         # q, k, f, v, b
+    per = {
+        "fwd_intra": inputs_fwd,
+        "fwd_scan": e * dv,                     # o
+        "bwd_scan": e * dv,                     # dO
+        "bwd_intra": inputs_fwd + e * dv + e * (3 * dk + dv + 1),  # + dO, writes dq, dk, df, dv, db
+    }
+    return float(per.get(kernel, 0)) * th
+
+
+def step_bytes(w, backward=True) -> float:
+    e = 2 if w.dtype == "bf16" else 4
+    th = w.B * w.T * w.H
+    fwd = e * (3 * w.dk + 2 * w.dv + 1)
+    bwd = e * (3 * w.dk + 2 * w.dv + 1) + e * (3 * w.dk + w.dv + 1)
+    return float(th * (fwd + (bwd if backward else 0)))
+
+
+def source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "kimi_delta_attention_bwd_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when absent or taken on different kernel sources."""
+    p = os.path.join(PROFILES, "ncu_traffic.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    e = d.get(kernel)
+    if not e or e.get("source_sha") != source_sha():
+        return None
+    return e.get("bytes_per_launch")
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            m = json.load(fh)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------- oracle arm
+def cpu_oracle_step(x, w):
+    from oracle import oracle
+    oracle.forward(x)
+    if w.backward:
+        oracle.backward(x, x["dO"], x.get("dh_final"))
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    w = WORKLOADS[STEP_WORKLOAD]
+    x = numpy_f64(make_inputs(w))
+    cores = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        cpu_oracle_step(x, w)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cpu_oracle_step(x, w)
+    el = time.perf_counter() - t0
+    ms = 1e3 * el / max(1, args.steps)
+    val = w.tokens / (ms / 1e3)
+    line = {"metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, shapes of the 300M KDA layer)",
+            "impl": "reference",
+            "config": {"workload": w.name, "global_batch": w.B, "seq_len": w.T, "heads": w.H, "dk": w.dk,
+                       "dv": w.dv, "parallelism": "single process, host cores"},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"each step = the full workload ({w.B}x{w.T} tokens x {w.H} heads, "
+                                       "forward + backward) on the CPU oracle, threaded over (row, head)"},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def cpu_baseline(min_seconds=10.0, max_reps=20):
+    """The oracle as it stands on the host cores: full workload steps
+    repeated until at least `min_seconds` have elapsed."""
+    w = WORKLOADS[STEP_WORKLOAD]
+    x = numpy_f64(make_inputs(w))
+    cpu_oracle_step(x, w)  # first touch of the output pages
+    reps = 0
+    t0 = time.perf_counter()
+    while reps < max_reps:
+        cpu_oracle_step(x, w)
+        reps += 1
+        if time.perf_counter() - t0 >= min_seconds:
+            break
+    el = time.perf_counter() - t0
+    return {"value": reps * w.tokens / el, "unit": "tokens/s", "cores": os.cpu_count() or 1, "kind": "oracle",
+            "sample": f"{reps} full workload steps ({w.B}x{w.T} tokens x {w.H} heads, fwd+bwd) in {el:.1f} s, "
+                      "threaded over (row, head) units"}
+
+
+# --------------------------------------------------------------- GPU arm
+def make_step(w, inp, dev):
+    from kimi_delta_attention_bwd_gb300 import _lib, kda_backward, kda_forward
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    prob = _lib.make_problem(w.B, w.T, w.H, w.dk, w.dv, w.torch_dtype, d["scale"], d.get("cu_seqlens"), None)
+    ws = _lib.alloc_workspace(prob, w.backward, dev)
+    o = torch.empty(w.B, w.T, w.H, w.dv, dtype=w.torch_dtype, device=dev)
+    grads = None
+    if w.backward:
+        grads = {"dq": torch.empty_like(d["q"]), "dk": torch.empty_like(d["k"]), "dv": torch.empty_like(d["v"]),
+                 "df": torch.empty_like(d["f"]), "db": torch.empty_like(d["b"]),
+                 "dA_log": torch.empty(w.H, device=dev), "ddt_bias": torch.empty(w.H, w.dk, device=dev),
+                 "dh0": None}
+
+    def step():
+        _, _, ctx = kda_forward(d["q"], d["k"], d["v"], d["f"], d["b"], d["A_log"], d["dt_bias"],
+                                scale=d["scale"], h0=d.get("h0"), cu_seqlens=d.get("cu_seqlens"),
+                                save_for_backward=w.backward, workspace=ws, out=o, want_final_state=False)
+        if w.backward:
+            kda_backward(ctx, d["dO"], d.get("dh_final"), grads=grads)
+    return step, d, grads
+
+
+def time_steps(step, steps, warmup, flush, world, stream):
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return sum(a.elapsed_time(b) for a, b in evs) / steps
+
+
+def run_ours(args, rank, world, local):
+    from kimi_delta_attention_bwd_gb300 import _lib
+    from kimi_delta_attention_bwd_gb300.build import build
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
+        return 1
+    build()
+    _lib.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    hbm, tflops, peak_kind = peaks()
+
+    # forward-only number at the same shape
+    wf = WORKLOADS[FWD_WORKLOAD]
+    fstep, _, _ = make_step(wf, make_inputs(wf, seed=BASE_SEED + FWD_WORKLOAD + 1000 * rank), dev)
+    fwd_ms = max_over_ranks(time_steps(fstep, args.steps, args.warmup, flush, world, stream), world, dev)
+    del fstep
+    torch.cuda.empty_cache()
+
+    # the training step (timed region with per-kernel event brackets and clock sampling)
+    w = WORKLOADS[STEP_WORKLOAD]
+    step, d, grads = make_step(w, make_inputs(w, seed=BASE_SEED + STEP_WORKLOAD + 1000 * rank), dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    _lib.prof_start()
+    ms = time_steps(step, args.steps, 0, flush, world, stream)
+    prof = _lib.prof_stop()
+    clk = clocks.stop()
+    ms = max_over_ranks(ms, world, dev)
+    value = world * w.tokens / (ms / 1e3)
+    launches = int(sum(c for _, c in prof.values()))
+    dom = max(prof, key=lambda k: prof[k][0])
+    dom_ms = prof[dom][0] / max(1, prof[dom][1])
+    ab = algorithmic_bytes(w, dom)
+    achieved = ab / (dom_ms / 1e3) / 1e9
+    traffic = ncu_traffic(dom)
+
+    # end to end through the public API with host buffers
+    from kimi_delta_attention_bwd_gb300 import kda_backward, kda_forward
+    host = {k: d[k].cpu().pin_memory() for k in ("q", "k", "v", "f", "b", "dO", "A_log", "dt_bias")}
+    dev_in = {k: torch.empty_like(d[k]) for k in host}
+    outs_host = {k: torch.empty(grads[k].shape, dtype=grads[k].dtype).pin_memory()
+                 for k in ("dq", "dk", "dv", "df", "db", "dA_log", "ddt_bias")}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs_host.values())
+    from kimi_delta_attention_bwd_gb300 import _lib as L
+    prob = L.make_problem(w.B, w.T, w.H, w.dk, w.dv, w.torch_dtype, d["scale"], None, None)
+    ws = L.alloc_workspace(prob, True, dev)
+
+    def e2e_step():
+        for k in host:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        _, _, ctx = kda_forward(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["f"], dev_in["b"], dev_in["A_log"],
+                                dev_in["dt_bias"], scale=d["scale"], workspace=ws, want_final_state=False)
+        g = kda_backward(ctx, dev_in["dO"], None, want_dh0=False)
+        for k in outs_host:
+            outs_host[k].copy_(g[k], non_blocking=True)
+    e2e_ms = max_over_ranks(time_steps(e2e_step, args.steps, args.warmup, flush, world, stream), world, dev)
+
+    cpu = cpu_baseline() if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, shapes of the 300M KDA layer)",
+            "config": {"workload": w.name, "global_batch": w.B * world, "seq_len": w.T, "heads": w.H,
+                       "dk": w.dk, "dv": w.dv, "parallelism": f"dp{world} (independent batches per GPU)",
+                       "l2": "flushed between timed steps (512 MiB write)"},
+            "fwd": {"value": world * wf.tokens / (fwd_ms / 1e3), "unit": "tokens/s", "ms_per_step": fwd_ms,
+                    "workload": wf.name},
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": traffic, "peak_kind": peak_kind,
+                         "algorithmic_bytes_per_launch": ab, "launch_ms": dom_ms},
+            "step_roofline": {"bound": "hbm", "algorithmic_bytes": step_bytes(w),
+                              "achieved": step_bytes(w) / (ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                              "frac": step_bytes(w) / (ms / 1e3) / 1e9 / hbm},
+            "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items() if v[1]},
+            "gpu_launches": launches,
+            "clocks": clk,
+            "e2e": {"value": world * w.tokens / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+    if args.impl == "reference":
+        # rank 0 alone times the oracle; the other ranks exit without work
+        return run_reference(args, int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")))
+    rank, world, local = dist_setup(args.gpus)
+    rc = run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

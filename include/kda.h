@@ -1,0 +1,140 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention library.
+ *
+ * Operation (per document and per head, tokens in order):
+ *   q^ = q / sqrt(sum q^2 + 1e-6)          k^ likewise   (over the key dim dk)
+ *   g  = -exp(A_log[h]) * softplus(f + dt_bias[h, :])    per key channel
+ *   beta = sigmoid(b)                                    per token and head
+ *   S_t = (I - beta_t k^_t k^_t^T) Diag(exp g_t) S_{t-1} + beta_t k^_t v_t^T
+ *   o_t = scale * S_t^T q^_t
+ * with S (dk x dv, fp32) reset to the document's initial state at every
+ * document start.  Sources: "Pure KDA 300M" guide (Primus, ROCm docs),
+ * Overview (softplus decay gate with learnable A_log and dt_bias, delta-rule
+ * recurrence) and "Configs and tools" (one beta per value head); openkimi
+ * README, "What is implemented" (fused Q/K norm, decay gate and beta; fp32
+ * recurrent state); torchtitan PR "[kimi k3] Support sample packing in KDA"
+ * (state reset at cu_seqlens document boundaries).
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *    library never allocates device memory; scratch lives in the caller's
+ *    workspace.  Host pointers are named *_host.
+ *  - Calls are asynchronous on the given stream; nothing synchronises the
+ *    device except kda_device_status() and kda_prof_stop().
+ *  - Arguments are validated on the host before any launch; a failed check
+ *    returns its status and launches nothing.  An invalid cu_seqlens array
+ *    that only exists on the device is caught by the device (no work is done,
+ *    outputs are left unwritten) and reported by kda_device_status().
+ *  - Layouts are contiguous, token-major, over Ntok = B*T flattened tokens:
+ *      q, k, f, dq, dk, df : [B, T, H, dk]
+ *      v, o, dO, dv        : [B, T, H, dv]
+ *      b, db               : [B, T, H]
+ *      A_log, dA_log       : [H] fp32       dt_bias, ddt_bias : [H, dk] fp32
+ *      h0, h_final, dh_final, dh0 : [n_docs, H, dk, dv] fp32
+ *  - Alignment: every tensor pointer 16-byte aligned; workspace 256-byte.
+ *  - Gradient outputs are overwritten, never accumulated.
+ */
+#ifndef KDA_GB300_H
+#define KDA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = -1,  /* null pointer, non-positive size, bad dtype */
+    KDA_ERR_UNSUPPORTED = -2,  /* (dk, dv) pair not compiled in */
+    KDA_ERR_ALIGNMENT = -3,    /* a pointer violates the alignment rule */
+    KDA_ERR_BAD_SEQLENS = -4,  /* cu_seqlens not 0 = c0 <= c1 <= ... = B*T */
+    KDA_ERR_WORKSPACE = -5,    /* workspace missing or smaller than kda_workspace_size() */
+    KDA_ERR_CUDA = -6,         /* a CUDA runtime call failed (launch error) */
+    KDA_ERR_DEVICE = -7        /* the device flagged an error (see kda_device_status) */
+} kda_status;
+
+typedef enum kda_dtype { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
+
+/* Problem description shared by every call.
+ *  B, T      : rows and tokens per row; the token axis is flattened to B*T.
+ *  H         : heads; dk / dv : key / value head dims.  Supported (dk, dv):
+ *              (32, 64), (64, 64), (64, 128), (128, 128).
+ *  dtype     : kda_dtype of q, k, v, f, b, o, dO and dq, dk, dv, df, db.
+ *  scale     : output scale; <= 0 selects 1/sqrt(dk).
+ *  n_docs    : number of documents when cu_seqlens is given (>= 1).
+ *  cu_seqlens: DEVICE int32 [n_docs + 1] document offsets into the flattened
+ *              token axis, or NULL for equal-length rows (n_docs = B,
+ *              documents are the rows).  Zero-length documents are allowed:
+ *              their final state is their initial state.
+ *  cu_seqlens_host : optional HOST copy of cu_seqlens; when given it is
+ *              validated on the host (KDA_ERR_BAD_SEQLENS before any launch).
+ */
+typedef struct kda_problem {
+    int32_t B, T, H, dk, dv;
+    int32_t dtype;
+    float scale;
+    int32_t n_docs;
+    const int32_t* cu_seqlens;
+    const int32_t* cu_seqlens_host;
+} kda_problem;
+
+/* Bytes of device workspace kda_fwd / kda_bwd need for this problem
+ * (for_backward = 0: forward only; 1: forward that saves for the backward,
+ * and the backward).  Returns 0 for an invalid problem. */
+KDA_API size_t kda_workspace_size(const kda_problem* p, int for_backward);
+
+/* Forward.  Writes o and, when non-NULL, h_final.  h0 may be NULL (zero
+ * initial state).  With save_for_backward = 1 the workspace (sized with
+ * for_backward = 1) keeps what kda_bwd needs; it must then be passed to
+ * kda_bwd unmodified, with the same inputs.  Streams: stream 0 is the legacy
+ * default stream. */
+KDA_API kda_status kda_fwd(const kda_problem* p,
+                   const void* q, const void* k, const void* v, const void* f, const void* b,
+                   const float* A_log, const float* dt_bias, const float* h0,
+                   void* o, float* h_final,
+                   int save_for_backward, void* workspace, size_t workspace_bytes,
+                   cudaStream_t stream);
+
+/* Backward of the loss sum(o * dO) + sum(h_final * dh_final).  Requires the
+ * workspace filled by kda_fwd(save_for_backward = 1) on the same inputs.
+ * dh_final may be NULL (zero); dh0 may be NULL (not returned).  Writes dq,
+ * dk, dv, df, db (dtype), dA_log [H] and ddt_bias [H, dk] (fp32, summed over
+ * all tokens in a fixed order: deterministic). */
+KDA_API kda_status kda_bwd(const kda_problem* p,
+                   const void* q, const void* k, const void* v, const void* f, const void* b,
+                   const float* A_log, const float* dt_bias, const float* h0,
+                   const void* dO, const float* dh_final,
+                   void* dq, void* dk, void* dv, void* df, void* db,
+                   float* dA_log, float* ddt_bias, float* dh0,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Synchronises `stream` and reads the device-side error word kept in the
+ * workspace (KDA_OK, or the status the device flagged, e.g.
+ * KDA_ERR_BAD_SEQLENS for offsets that were only on the device). */
+KDA_API kda_status kda_device_status(const void* workspace, cudaStream_t stream);
+
+/* Human-readable text for a status. */
+KDA_API const char* kda_strerror(kda_status s);
+
+/* Per-kernel timing.  kda_prof_start() arms CUDA-event brackets around every
+ * kernel the library launches afterwards (on the launch stream); kda_prof_stop()
+ * synchronises those events and returns, for each kernel id i < n, the summed
+ * milliseconds and the launch count, then disarms.  Not thread-safe; for
+ * benchmarks.  kda_prof_kernel_name(i) names kernel id i (NULL past the end). */
+KDA_API kda_status kda_prof_start(void);
+KDA_API kda_status kda_prof_stop(double* total_ms, int64_t* launches, int n);
+KDA_API const char* kda_prof_kernel_name(int i);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KDA_GB300_H */

@@ -1,0 +1,99 @@
+"""Kimi Delta Attention (KDA) chunked gated delta rule on GB300 (sm_103a).
+
+Public API (PyTorch tensors on the CUDA device; the work runs in
+libkda_gb300.so through its C ABI, include/kda.h):
+
+  o, h_final, ctx = kda_forward(q, k, v, f, b, A_log, dt_bias, ...)
+  grads = kda_backward(ctx, dO, dh_final=None)
+
+Layouts: q, k, f [B, T, H, dk]; v [B, T, H, dv]; b [B, T, H] (bf16 or fp32);
+A_log [H], dt_bias [H, dk] fp32; optional cu_seqlens int32 [n_docs + 1] over
+the flattened B*T tokens; states [n_docs, H, dk, dv] fp32.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _lib
+from ._lib import KdaError, kda_device_status, kda_strerror_text  # noqa: F401
+
+__all__ = ["kda_forward", "kda_backward", "KdaContext", "KdaError", "kda_device_status"]
+
+
+@dataclass
+class KdaContext:
+    problem: object
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    f: torch.Tensor
+    b: torch.Tensor
+    A_log: torch.Tensor
+    dt_bias: torch.Tensor
+    h0: Optional[torch.Tensor]
+    cu_seqlens: Optional[torch.Tensor]
+    cu_seqlens_host: object
+    workspace: torch.Tensor
+    n_docs: int
+
+
+def _check(t, name, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def kda_forward(q, k, v, f, b, A_log, dt_bias, scale: Optional[float] = None, h0=None,
+                cu_seqlens=None, cu_seqlens_host=None, save_for_backward: bool = True,
+                workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                want_final_state: bool = True):
+    """Forward pass.  Returns (o, h_final or None, ctx); ctx feeds kda_backward
+    when save_for_backward is set."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (f, "f"), (b, "b")):
+        _check(t, n, q.dtype)
+    _check(A_log, "A_log", torch.float32)
+    _check(dt_bias, "dt_bias", torch.float32)
+    if cu_seqlens is not None:
+        _check(cu_seqlens, "cu_seqlens", torch.int32)
+    n_docs = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if h0 is not None:
+        _check(h0, "h0", torch.float32)
+    prob = _lib.make_problem(B, T, H, dk, dv, q.dtype, scale, cu_seqlens, cu_seqlens_host)
+    if workspace is None:
+        workspace = _lib.alloc_workspace(prob, save_for_backward, q.device)
+    o = out if out is not None else torch.empty(B, T, H, dv, dtype=q.dtype, device=q.device)
+    hf = torch.empty(n_docs, H, dk, dv, dtype=torch.float32, device=q.device) if want_final_state else None
+    _lib.kda_fwd(prob, q, k, v, f, b, A_log, dt_bias, h0, o, hf, save_for_backward, workspace)
+    ctx = KdaContext(prob, q, k, v, f, b, A_log, dt_bias, h0, cu_seqlens, cu_seqlens_host, workspace, n_docs)
+    return o, hf, ctx
+
+
+def kda_backward(ctx: KdaContext, dO, dh_final=None, want_dh0: bool = True, grads: Optional[dict] = None):
+    """Backward of sum(o * dO) + sum(h_final * dh_final).  Returns a dict with
+    dq, dk, dv, df, db (io dtype), dA_log, ddt_bias, dh0 (fp32)."""
+    _check(dO, "dO", ctx.q.dtype)
+    if dh_final is not None:
+        _check(dh_final, "dh_final", torch.float32)
+    q = ctx.q
+    B, T, H, dk = q.shape
+    dv = ctx.v.shape[-1]
+    if grads is None:
+        grads = {
+            "dq": torch.empty_like(q), "dk": torch.empty_like(ctx.k), "dv": torch.empty_like(ctx.v),
+            "df": torch.empty_like(ctx.f), "db": torch.empty_like(ctx.b),
+            "dA_log": torch.empty(H, dtype=torch.float32, device=q.device),
+            "ddt_bias": torch.empty(H, dk, dtype=torch.float32, device=q.device),
+            "dh0": torch.empty(ctx.n_docs, H, dk, dv, dtype=torch.float32, device=q.device) if want_dh0 else None,
+        }
+    _lib.kda_bwd(ctx.problem, ctx.q, ctx.k, ctx.v, ctx.f, ctx.b, ctx.A_log, ctx.dt_bias, ctx.h0, dO, dh_final,
+                 grads["dq"], grads["dk"], grads["dv"], grads["df"], grads["db"], grads["dA_log"],
+                 grads["ddt_bias"], grads.get("dh0"), ctx.workspace)
+    return grads

@@ -1,0 +1,362 @@
+// C ABI of the KDA library: argument validation, workspace layout, the
+// varlen chunk table, launch order and per-kernel timing.
+#include "../../include/kda.h"
+#include "kda_internal.cuh"
+
+#include <stdio.h>
+#include <string.h>
+
+namespace kda {
+
+// ------------------------------------------------------------ chunk table
+// One CTA builds the chunk table from the document offsets: document i of
+// length L_i owns ceil(L_i / C) chunks, the last one partial.  Chunks always
+// start at a document start, so a state never crosses a document boundary
+// (torchtitan PR "[kimi k3] Support sample packing in KDA", Verification).
+// Equal-length rows use the same table with offsets b * T.
+__global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* cu, Dims d, Ws w) {
+  __shared__ int s_bad;
+  __shared__ int s_carry;
+  __shared__ int s_wsum[32];
+  const int tid = threadIdx.x, n = d.n_docs;
+  auto off = [&](int i) -> int { return cu ? cu[i] : i * d.T; };
+  if (tid == 0) {
+    s_bad = (off(0) != 0 || off(n) != d.Ntok) ? 1 : 0;
+    s_carry = 0;
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += blockDim.x)
+    if (off(i + 1) < off(i)) atomicOr(&s_bad, 1);
+  __syncthreads();
+  if (!s_bad) {
+    for (int base = 0; base < n; base += blockDim.x) {
+      int i = base + tid;
+      int nc = i < n ? (off(i + 1) - off(i) + C - 1) / C : 0;
+      int x = nc;  // inclusive scan over the block
+      const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) s_wsum[warp] = x;
+      __syncthreads();
+      if (warp == 0) {
+        int y = lane < (int)(blockDim.x >> 5) ? s_wsum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          int z = __shfl_up_sync(0xffffffffu, y, o);
+          if (lane >= o) y += z;
+        }
+        s_wsum[lane] = y;
+      }
+      __syncthreads();
+      int incl = x + (warp > 0 ? s_wsum[warp - 1] : 0);
+      if (i < n) w.doc_chunk0[i] = s_carry + incl - nc;
+      int total = s_wsum[(blockDim.x >> 5) - 1];
+      __syncthreads();
+      if (tid == 0) s_carry += total;
+      __syncthreads();
+    }
+    if (tid == 0 && s_carry > d.nc_max) s_bad = 1;  // cannot happen for valid offsets
+    __syncthreads();
+  }
+  if (s_bad) {
+    if (tid == 0) { *w.err = KDA_ERR_BAD_SEQLENS; *w.n_chunks = 0; *w.tag = 0; }
+    for (int j = tid; j < d.nc_max; j += blockDim.x) w.chunk_len[j] = 0;
+    return;
+  }
+  if (tid == 0) {
+    w.doc_chunk0[n] = s_carry;
+    *w.n_chunks = s_carry;
+    *w.err = KDA_OK;
+    *w.tag = d.save ? d.tag : 0;
+  }
+  for (int i = tid; i < n; i += blockDim.x) {
+    int a = off(i), L = off(i + 1) - a, c0 = w.doc_chunk0[i];
+    for (int c = 0; c * C < L; c++) {
+      w.chunk_tok0[c0 + c] = a + c * C;
+      w.chunk_len[c0 + c] = min(C, L - c * C);
+      w.chunk_doc[c0 + c] = i;
+    }
+  }
+  for (int j = s_carry + tid; j < d.nc_max; j += blockDim.x) w.chunk_len[j] = 0;
+}
+
+cudaError_t launch_chunk_table(const int32_t* cu, const Dims& d, const Ws& w, cudaStream_t st) {
+  prof_begin(K_TABLE, st);
+  chunk_table_kernel<<<1, 1024, 0, st>>>(cu, d, w);
+  prof_end(K_TABLE, st);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ timing
+namespace {
+constexpr int MAX_EV = 8192;
+struct Prof {
+  bool on = false;
+  int n = 0;
+  cudaEvent_t ev[MAX_EV][2];
+  int kid[MAX_EV];
+  bool created = false;
+};
+Prof g_prof;
+int g_open = -1;
+}  // namespace
+
+void prof_begin(int kid, cudaStream_t st) {
+  if (!g_prof.on || g_prof.n >= MAX_EV) { g_open = -1; return; }
+  g_open = g_prof.n++;
+  g_prof.kid[g_open] = kid;
+  cudaEventRecord(g_prof.ev[g_open][0], st);
+}
+void prof_end(int kid, cudaStream_t st) {
+  (void)kid;
+  if (g_open < 0) return;
+  cudaEventRecord(g_prof.ev[g_open][1], st);
+  g_open = -1;
+}
+
+// ------------------------------------------------------------ layout
+static size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct Layout {
+  size_t total;
+  size_t off_err, off_nch, off_dc0, off_ct0, off_cl, off_cd;
+  size_t off_W, off_U, off_P, off_QG, off_KD, off_gam, off_Sent;
+  size_t off_dE, off_dSn, off_pA, off_pdt, off_scr;
+};
+
+static Layout layout(const Dims& d, int for_bwd) {
+  Layout L;
+  size_t o = 0;
+  const size_t nch = (size_t)d.nc_max * d.H;
+  auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes); return r; };
+  L.off_err = take(8);  // error word, then the saved-problem tag
+  L.off_nch = take(4);
+  L.off_dc0 = take(4 * (size_t)(d.n_docs + 1));
+  L.off_ct0 = take(4 * (size_t)d.nc_max);
+  L.off_cl = take(4 * (size_t)d.nc_max);
+  L.off_cd = take(4 * (size_t)d.nc_max);
+  L.off_W = take(4 * nch * C * d.dk);
+  L.off_U = take(4 * nch * C * d.dv);
+  L.off_P = take(4 * nch * C * C);
+  L.off_QG = take(4 * nch * C * d.dk);
+  L.off_KD = take(4 * nch * C * d.dk);
+  L.off_gam = take(4 * nch * d.dk);
+  if (for_bwd) {
+    L.off_Sent = take(4 * nch * d.dk * d.dv);
+    L.off_dE = take(4 * nch * C * d.dv);
+    L.off_dSn = take(4 * nch * d.dk * d.dv);
+    L.off_pA = take(4 * nch);
+    L.off_pdt = take(4 * nch * d.dk);
+    L.off_scr = take(4 * nch * (size_t)bwd_scratch_floats(d.dk, d.dv));
+  } else {
+    L.off_Sent = L.off_dE = L.off_dSn = L.off_pA = L.off_pdt = L.off_scr = 0;
+  }
+  L.total = o;
+  return L;
+}
+
+static Ws bind(void* ws, const Layout& L, const Dims& d, int for_bwd) {
+  char* p = (char*)ws;
+  Ws w;
+  w.err = (int32_t*)(p + L.off_err);
+  w.tag = (int32_t*)(p + L.off_err + 4);
+  w.n_chunks = (int32_t*)(p + L.off_nch);
+  w.doc_chunk0 = (int32_t*)(p + L.off_dc0);
+  w.chunk_tok0 = (int32_t*)(p + L.off_ct0);
+  w.chunk_len = (int32_t*)(p + L.off_cl);
+  w.chunk_doc = (int32_t*)(p + L.off_cd);
+  w.W = (float*)(p + L.off_W);
+  w.U = (float*)(p + L.off_U);
+  w.P = (float*)(p + L.off_P);
+  w.QG = (float*)(p + L.off_QG);
+  w.KD = (float*)(p + L.off_KD);
+  w.gam = (float*)(p + L.off_gam);
+  w.Sent = for_bwd ? (float*)(p + L.off_Sent) : nullptr;
+  w.dE = for_bwd ? (float*)(p + L.off_dE) : nullptr;
+  w.dSn = for_bwd ? (float*)(p + L.off_dSn) : nullptr;
+  w.pA = for_bwd ? (float*)(p + L.off_pA) : nullptr;
+  w.pdt = for_bwd ? (float*)(p + L.off_pdt) : nullptr;
+  w.scr = for_bwd ? (float*)(p + L.off_scr) : nullptr;
+  w.scr_per_ch = bwd_scratch_floats(d.dk, d.dv);
+  return w;
+}
+
+static bool supported(int dk, int dv) {
+  return (dk == 32 && dv == 64) || (dk == 64 && dv == 64) || (dk == 64 && dv == 128) || (dk == 128 && dv == 128);
+}
+
+static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Validates the problem and fills the dims.  Pure host code: no CUDA call.
+static kda_status check_problem(const kda_problem* p, Dims* d) {
+  if (!p) return KDA_ERR_INVALID_ARG;
+  if (p->B <= 0 || p->T <= 0 || p->H <= 0 || p->dk <= 0 || p->dv <= 0) return KDA_ERR_INVALID_ARG;
+  if (p->dtype != KDA_BF16 && p->dtype != KDA_F32) return KDA_ERR_INVALID_ARG;
+  if (!supported(p->dk, p->dv)) return KDA_ERR_UNSUPPORTED;
+  const int64_t ntok = (int64_t)p->B * p->T;
+  if (ntok > (int64_t)1 << 30 || p->H > 4096) return KDA_ERR_INVALID_ARG;
+  int n_docs = p->B;
+  if (p->cu_seqlens) {
+    if (p->n_docs <= 0 || p->n_docs > (1 << 24)) return KDA_ERR_INVALID_ARG;
+    if (!aligned(p->cu_seqlens, 4)) return KDA_ERR_ALIGNMENT;
+    n_docs = p->n_docs;
+    if (p->cu_seqlens_host) {
+      const int32_t* c = p->cu_seqlens_host;
+      if (c[0] != 0 || (int64_t)c[n_docs] != ntok) return KDA_ERR_BAD_SEQLENS;
+      for (int i = 0; i < n_docs; i++)
+        if (c[i + 1] < c[i]) return KDA_ERR_BAD_SEQLENS;
+    }
+  } else if (p->cu_seqlens_host) {
+    return KDA_ERR_INVALID_ARG;
+  }
+  d->B = p->B;
+  d->T = p->T;
+  d->Ntok = (int)ntok;
+  d->H = p->H;
+  d->dk = p->dk;
+  d->dv = p->dv;
+  d->n_docs = n_docs;
+  d->scale = p->scale > 0.f ? p->scale : 1.0f / sqrtf((float)p->dk);
+  // upper bound on sum_i ceil(L_i / C) over any valid offsets
+  int64_t ncm = p->cu_seqlens ? (ntok + (int64_t)(C - 1) * n_docs) / C
+                              : (int64_t)p->B * ((p->T + C - 1) / C);
+  if (ncm < 1) ncm = 1;
+  if (ncm > (int64_t)1 << 30) return KDA_ERR_INVALID_ARG;
+  d->nc_max = (int)ncm;
+  uint32_t hsh = 2166136261u;  // FNV-1a over the sizes that fix the layout
+  const int32_t vals[8] = {p->B, p->T, p->H, p->dk, p->dv, p->dtype, n_docs, 0x4b4441};
+  for (int i = 0; i < 8; i++) { hsh ^= (uint32_t)vals[i]; hsh *= 16777619u; }
+  d->tag = (int32_t)(hsh | 1u);
+  d->save = 0;
+  return KDA_OK;
+}
+
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" {
+
+size_t kda_workspace_size(const kda_problem* p, int for_backward) {
+  Dims d;
+  if (check_problem(p, &d) != KDA_OK) return 0;
+  return layout(d, for_backward ? 1 : 0).total;
+}
+
+static kda_status status_of(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+kda_status kda_fwd(const kda_problem* p, const void* q, const void* k, const void* v, const void* f,
+                   const void* b, const float* A_log, const float* dt_bias, const float* h0, void* o,
+                   float* h_final, int save_for_backward, void* workspace, size_t workspace_bytes,
+                   cudaStream_t stream) {
+  Dims d;
+  kda_status s = check_problem(p, &d);
+  if (s != KDA_OK) return s;
+  if (!q || !k || !v || !f || !b || !A_log || !dt_bias || !o) return KDA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, f, b, A_log, dt_bias, o};
+  for (const void* x : ptrs)
+    if (!aligned(x, 16)) return KDA_ERR_ALIGNMENT;
+  if ((h0 && !aligned(h0, 16)) || (h_final && !aligned(h_final, 16))) return KDA_ERR_ALIGNMENT;
+  if (!workspace) return KDA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return KDA_ERR_ALIGNMENT;
+  const int fb = save_for_backward ? 1 : 0;
+  Layout L = layout(d, fb);
+  if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
+  Ws w = bind(workspace, L, d, fb);
+  d.save = fb;
+  FwdIO io{q, k, v, f, b, A_log, dt_bias, h0, o, h_final, fb};
+  cudaError_t e = launch_chunk_table(p->cu_seqlens, d, w, stream);
+  if (e == cudaSuccess) e = launch_fwd_intra(p->dtype, d, io, w, stream);
+  if (e == cudaSuccess) e = launch_fwd_scan(p->dtype, d, io, w, stream);
+  return status_of(e);
+}
+
+kda_status kda_bwd(const kda_problem* p, const void* q, const void* k, const void* v, const void* f,
+                   const void* b, const float* A_log, const float* dt_bias, const float* h0,
+                   const void* dO, const float* dh_final, void* dq, void* dk, void* dv, void* df,
+                   void* db, float* dA_log, float* ddt_bias, float* dh0, void* workspace,
+                   size_t workspace_bytes, cudaStream_t stream) {
+  (void)h0;  // the entry states were saved by kda_fwd
+  Dims d;
+  kda_status s = check_problem(p, &d);
+  if (s != KDA_OK) return s;
+  if (!q || !k || !v || !f || !b || !A_log || !dt_bias || !dO || !dq || !dk || !dv || !df || !db ||
+      !dA_log || !ddt_bias)
+    return KDA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, f, b, A_log, dt_bias, dO, dq, dk, dv, df, db, dA_log, ddt_bias};
+  for (const void* x : ptrs)
+    if (!aligned(x, 16)) return KDA_ERR_ALIGNMENT;
+  if ((dh_final && !aligned(dh_final, 16)) || (dh0 && !aligned(dh0, 16))) return KDA_ERR_ALIGNMENT;
+  if (!workspace) return KDA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return KDA_ERR_ALIGNMENT;
+  Layout L = layout(d, 1);
+  if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
+  Ws w = bind(workspace, L, d, 1);
+  BwdIO io{q, k, v, f, b, A_log, dt_bias, dO, dh_final, dq, dk, dv, df, db, dA_log, ddt_bias, dh0};
+  cudaError_t e = launch_bwd_scan(p->dtype, d, io, w, stream);
+  if (e == cudaSuccess) e = launch_bwd_intra(p->dtype, d, io, w, stream);
+  if (e == cudaSuccess) e = launch_bwd_reduce(d, io, w, stream);
+  return status_of(e);
+}
+
+kda_status kda_device_status(const void* workspace, cudaStream_t stream) {
+  if (!workspace) return KDA_ERR_WORKSPACE;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return KDA_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return KDA_ERR_CUDA;
+  return (kda_status)v;
+}
+
+const char* kda_strerror(kda_status s) {
+  switch (s) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_INVALID_ARG: return "invalid argument (null pointer, size or dtype)";
+    case KDA_ERR_UNSUPPORTED: return "unsupported (dk, dv): supported are (32,64), (64,64), (64,128), (128,128)";
+    case KDA_ERR_ALIGNMENT: return "misaligned pointer (tensors need 16-byte, workspace 256-byte alignment)";
+    case KDA_ERR_BAD_SEQLENS: return "cu_seqlens must start at 0, be non-decreasing and end at B*T";
+    case KDA_ERR_WORKSPACE: return "workspace missing or smaller than kda_workspace_size()";
+    case KDA_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+    case KDA_ERR_DEVICE: return "the device flagged an error";
+  }
+  return "unknown status";
+}
+
+static const char* const k_names[K_COUNT] = {"chunk_table", "fwd_intra", "fwd_scan",
+                                             "bwd_scan", "bwd_intra", "bwd_reduce"};
+
+const char* kda_prof_kernel_name(int i) { return (i >= 0 && i < K_COUNT) ? k_names[i] : nullptr; }
+
+kda_status kda_prof_start(void) {
+  if (!g_prof.created) {
+    for (int i = 0; i < MAX_EV; i++)
+      for (int j = 0; j < 2; j++)
+        if (cudaEventCreate(&g_prof.ev[i][j]) != cudaSuccess) return KDA_ERR_CUDA;
+    g_prof.created = true;
+  }
+  g_prof.n = 0;
+  g_prof.on = true;
+  return KDA_OK;
+}
+
+kda_status kda_prof_stop(double* total_ms, int64_t* launches, int n) {
+  if (!g_prof.created) return KDA_ERR_INVALID_ARG;
+  g_prof.on = false;
+  for (int i = 0; i < n; i++) { if (total_ms) total_ms[i] = 0; if (launches) launches[i] = 0; }
+  for (int e = 0; e < g_prof.n; e++) {
+    if (cudaEventSynchronize(g_prof.ev[e][1]) != cudaSuccess) return KDA_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, g_prof.ev[e][0], g_prof.ev[e][1]) != cudaSuccess) return KDA_ERR_CUDA;
+    int kid = g_prof.kid[e];
+    if (kid < n) {
+      if (total_ms) total_ms[kid] += ms;
+      if (launches) launches[kid] += 1;
+    }
+  }
+  g_prof.n = 0;
+  return KDA_OK;
+}
+
+}  // extern "C"

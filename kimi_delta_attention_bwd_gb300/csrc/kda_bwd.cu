@@ -1,0 +1,445 @@
+// Backward kernels of the KDA chunked gated delta rule.
+//
+// With E = U - W S, O = QG S + P E and S' = Diag(gamma) S + KD^T E per chunk
+// (QG and P carry the output scale), the reverse pass is
+//   dE = P^T dO + KD dS'                 (per chunk, from the state gradient)
+//   dS = Diag(gamma) dS' + QG^T dO - W^T dE
+// carried backwards over a document's chunks (bwd_scan), followed by the
+// local gradients of every chunk through T = (I + A)^-1, the decay ratios,
+// the cumulative gate, the softplus gate, the sigmoid and the L2 norms
+// (bwd_intra), and a fixed-order reduction of the per-head parameter
+// gradients (bwd_reduce).  Derivation: reverse-mode differentiation of the
+// recurrence of the "Pure KDA 300M" guide (Overview), chunked as in the
+// forward kernels.
+#include "kda_internal.cuh"
+
+namespace kda {
+
+constexpr int NT = 16;  // dv columns per scan CTA
+
+template <typename TI, int DK, int DV>
+__global__ void __launch_bounds__(256) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
+  const int doc = blockIdx.x, h = blockIdx.y, c0col = blockIdx.z * NT, tid = threadIdx.x;
+  if (!saved_ok(d, w.tag, w.err)) return;
+  const int H = d.H;
+  extern __shared__ float sm[];
+  float* dS = sm;              // [DK][NT]
+  float* dEt = dS + DK * NT;   // [C][NT]
+  float* dOt = dEt + C * NT;   // [C][NT]
+  float* Wt = dOt + C * NT;    // [C][DK]
+  float* QGt = Wt + C * DK;    // [C][DK]
+  float* KDt = QGt + C * DK;   // [C][DK]
+  float* Pt = KDt + C * DK;    // [C][C]
+  float* gm = Pt + C * C;      // [DK]
+  const TI* dO = (const TI*)io.dO;
+
+  for (int idx = tid; idx < DK * NT; idx += blockDim.x) {
+    int i = idx / NT, jj = idx % NT;
+    dS[idx] = io.dh_final ? io.dh_final[(((int64_t)doc * H + h) * DK + i) * DV + c0col + jj] : 0.f;
+  }
+  const int cb = w.doc_chunk0[doc], ce = w.doc_chunk0[doc + 1];
+  __syncthreads();
+  for (int c = ce - 1; c >= cb; c--) {
+    const int64_t ch = (int64_t)c * H + h;
+    const int L = w.chunk_len[c], t0 = w.chunk_tok0[c];
+    for (int idx = tid; idx < DK * NT; idx += blockDim.x) {
+      int i = idx / NT, jj = idx % NT;
+      w.dSn[(ch * DK + i) * DV + c0col + jj] = dS[idx];
+    }
+    for (int idx = tid; idx < C * DK; idx += blockDim.x) {
+      Wt[idx] = w.W[ch * C * DK + idx];
+      QGt[idx] = w.QG[ch * C * DK + idx];
+      KDt[idx] = w.KD[ch * C * DK + idx];
+    }
+    for (int idx = tid; idx < C * C; idx += blockDim.x) Pt[idx] = w.P[ch * C * C + idx];
+    for (int i = tid; i < DK; i += blockDim.x) gm[i] = w.gam[ch * DK + i];
+    for (int idx = tid; idx < C * NT; idx += blockDim.x) {
+      int r = idx / NT, jj = idx % NT;
+      dOt[idx] = r < L ? ldf(dO + ((int64_t)(t0 + r) * H + h) * DV + c0col + jj) : 0.f;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < C * NT; idx += blockDim.x) {
+      int s = idx / NT, jj = idx % NT;
+      float acc = 0.f;
+      for (int r = s; r < C; r++) acc += Pt[r * C + s] * dOt[r * NT + jj];
+      for (int i = 0; i < DK; i++) acc += KDt[s * DK + i] * dS[i * NT + jj];
+      dEt[idx] = acc;
+      w.dE[(ch * C + s) * DV + c0col + jj] = acc;
+    }
+    __syncthreads();
+    float nv[(DK * NT + 255) / 256];
+#pragma unroll
+    for (int u = 0; u < (DK * NT + 255) / 256; u++) {
+      int idx = tid + u * 256;
+      if (idx < DK * NT) {
+        int i = idx / NT, jj = idx % NT;
+        float acc = gm[i] * dS[idx];
+        for (int r = 0; r < C; r++) acc += QGt[r * DK + i] * dOt[r * NT + jj] - Wt[r * DK + i] * dEt[r * NT + jj];
+        nv[u] = acc;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < (DK * NT + 255) / 256; u++) {
+      int idx = tid + u * 256;
+      if (idx < DK * NT) dS[idx] = nv[u];
+    }
+    __syncthreads();
+  }
+  if (io.dh0)
+    for (int idx = tid; idx < DK * NT; idx += blockDim.x) {
+      int i = idx / NT, jj = idx % NT;
+      io.dh0[(((int64_t)doc * H + h) * DK + i) * DV + c0col + jj] = dS[idx];
+    }
+}
+
+__device__ __forceinline__ float block_sum(float x, float* red) {
+  x = warp_sum(x);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  __syncthreads();
+  if (lane == 0) red[warp] = x;
+  __syncthreads();
+  float r = 0.f;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nw; i++) r += red[i];
+    red[0] = r;
+  }
+  __syncthreads();
+  return red[0];
+}
+
+// One CTA per (chunk, head): all local gradients of the chunk.
+template <typename TI, int DK, int DV>
+__global__ void __launch_bounds__(256) bwd_intra_kernel(Dims d, BwdIO io, Ws w) {
+  const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  if (!saved_ok(d, w.tag, w.err)) return;
+  if (j >= *w.n_chunks) return;
+  const int L = w.chunk_len[j];
+  if (L <= 0) return;
+  const int t0 = w.chunk_tok0[j];
+  const int H = d.H;
+  const int64_t ch = (int64_t)j * H + h;
+  const float scale = d.scale;
+
+  extern __shared__ float sm[];
+  float* qh = sm;               // [C][DK]
+  float* kh = qh + C * DK;      // [C][DK]
+  float* G = kh + C * DK;       // [C][DK]
+  float* Ap = G + C * DK;       // [C][C] unscaled strict-lower K^K^T with ratios
+  float* Pp = Ap + C * C;       // [C][C] unscaled inclusive-lower Q^K^T with ratios
+  float* Tm = Pp + C * C;       // [C][C]
+  float* dAm = Tm + C * C;      // [C][C]
+  float* dPm = dAm + C * C;     // [C][C]
+  float* bet = dPm + C * C;     // [C]
+  float* nq = bet + C;          // [C]
+  float* nk = nq + C;           // [C]
+  float* dbet = nk + C;         // [C]
+  float* dgam = dbet + C;       // [DK]
+  float* red = dgam + DK;       // [32]
+
+  float* scr = w.scr + ch * w.scr_per_ch;
+  float* E = scr;               // [C][DV]
+  float* YU = E + C * DV;       // [C][DV]
+  float* dQG = YU + C * DV;     // [C][DK]  gradient of Q^ * Gamma (unscaled)
+  float* dKd = dQG + C * DK;    // [C][DK]
+  float* dW = dKd + C * DK;     // [C][DK]
+  float* YW = dW + C * DK;      // [C][DK]
+  float* dqh = YW + C * DK;     // [C][DK]
+  float* dkh = dqh + C * DK;    // [C][DK]
+  float* dG = dkh + C * DK;     // [C][DK]
+
+  const TI* q = (const TI*)io.q;
+  const TI* k = (const TI*)io.k;
+  const TI* f = (const TI*)io.f;
+  const TI* v = (const TI*)io.v;
+  const TI* b = (const TI*)io.b;
+  const TI* dO = (const TI*)io.dO;
+  const float a = expf(io.A_log[h]);
+  const float* Sg = w.Sent + ch * DK * DV;
+  const float* dSg = w.dSn + ch * DK * DV;
+  const float* dEg = w.dE + ch * C * DV;
+  const float* Wg = w.W + ch * C * DK;
+  const float* Ug = w.U + ch * C * DV;
+
+  // ---- prologue (same arithmetic as the forward)
+  for (int idx = tid; idx < C * DK; idx += blockDim.x) {
+    int r = idx / DK, i = idx % DK;
+    float qv = 0.f, kv = 0.f, gv = 0.f;
+    if (r < L) {
+      int64_t off = ((int64_t)(t0 + r) * H + h) * DK + i;
+      qv = ldf(q + off);
+      kv = ldf(k + off);
+      gv = -a * softplus_f(ldf(f + off) + io.dt_bias[h * DK + i]);
+    }
+    qh[idx] = qv; kh[idx] = kv; G[idx] = gv;
+  }
+  for (int r = tid; r < C; r += blockDim.x) {
+    bet[r] = r < L ? sigmoid_f(ldf(b + (int64_t)(t0 + r) * H + h)) : 0.f;
+    dbet[r] = 0.f;
+  }
+  __syncthreads();
+  const int warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+  for (int r = warp; r < C; r += nw) {
+    float sq = 0.f, sk = 0.f;
+    for (int i = lane; i < DK; i += 32) { sq += qh[r * DK + i] * qh[r * DK + i]; sk += kh[r * DK + i] * kh[r * DK + i]; }
+    sq = warp_sum(sq); sk = warp_sum(sk);
+    float nqr = sqrtf(sq + L2_EPS), nkr = sqrtf(sk + L2_EPS);
+    float iq = 1.0f / nqr, ik = 1.0f / nkr;
+    for (int i = lane; i < DK; i += 32) { qh[r * DK + i] *= iq; kh[r * DK + i] *= ik; }
+    if (lane == 0) { nq[r] = nqr; nk[r] = nkr; }
+  }
+  for (int i = tid; i < DK; i += blockDim.x) {
+    float acc = 0.f;
+    for (int r = 0; r < C; r++) { acc += G[r * DK + i]; G[r * DK + i] = acc; }
+  }
+  __syncthreads();
+
+  // ---- intra-chunk factors (same arithmetic as the forward)
+  for (int idx = tid; idx < C * C; idx += blockDim.x) {
+    int r = idx / C, s = idx % C;
+    float accA = 0.f, accP = 0.f;
+    if (s <= r) {
+      for (int i = 0; i < DK; i++) {
+        float e = expf(G[r * DK + i] - G[s * DK + i]);
+        float ks = kh[s * DK + i] * e;
+        accP += qh[r * DK + i] * ks;
+        accA += kh[r * DK + i] * ks;
+      }
+    }
+    Ap[idx] = s < r ? accA : 0.f;
+    dAm[idx] = s < r ? bet[r] * accA : 0.f;   // A = diag(beta) Ap, used for the solve
+    Pp[idx] = accP;
+    Tm[idx] = (r == s) ? 1.f : 0.f;
+  }
+  __syncthreads();
+  for (int r = 1; r < C; r++) {
+    for (int c = tid; c < r; c += blockDim.x) {
+      float acc = 0.f;
+      for (int s = c; s < r; s++) acc += dAm[r * C + s] * Tm[s * C + c];
+      Tm[r * C + c] = -acc;
+    }
+    __syncthreads();
+  }
+
+  // ---- E = U - W S,  dQG = scale dO S^T,  dW = -dE S^T,  dgamma
+  for (int idx = tid; idx < C * DV; idx += blockDim.x) {
+    int r = idx / DV, jj = idx % DV;
+    float acc = Ug[idx];
+    for (int i = 0; i < DK; i++) acc -= Wg[r * DK + i] * Sg[i * DV + jj];
+    E[idx] = acc;
+  }
+  for (int idx = tid; idx < C * DK; idx += blockDim.x) {
+    int r = idx / DK, i = idx % DK;
+    float a1 = 0.f, a2 = 0.f;
+    if (r < L)
+      for (int jj = 0; jj < DV; jj++) a1 += ldf(dO + ((int64_t)(t0 + r) * H + h) * DV + jj) * Sg[i * DV + jj];
+    for (int jj = 0; jj < DV; jj++) a2 += dEg[r * DV + jj] * Sg[i * DV + jj];
+    dQG[idx] = scale * a1;
+    dW[idx] = -a2;
+  }
+  for (int i = tid; i < DK; i += blockDim.x) {
+    float acc = 0.f;
+    for (int jj = 0; jj < DV; jj++) acc += dSg[i * DV + jj] * Sg[i * DV + jj];
+    dgam[i] = acc;
+  }
+  __syncthreads();
+
+  // ---- dP = scale dO E^T (inclusive lower), dKd = E dS'^T,  YU = T^T dE,  YW = T^T dW
+  for (int idx = tid; idx < C * C; idx += blockDim.x) {
+    int r = idx / C, s = idx % C;
+    float acc = 0.f;
+    if (s <= r && r < L)
+      for (int jj = 0; jj < DV; jj++) acc += ldf(dO + ((int64_t)(t0 + r) * H + h) * DV + jj) * E[s * DV + jj];
+    dPm[idx] = scale * acc;
+  }
+  for (int idx = tid; idx < C * DK; idx += blockDim.x) {
+    int r = idx / DK, i = idx % DK;
+    float acc = 0.f;
+    for (int jj = 0; jj < DV; jj++) acc += E[r * DV + jj] * dSg[i * DV + jj];
+    dKd[idx] = acc;
+    float acc2 = 0.f;
+    for (int rr = r; rr < C; rr++) acc2 += Tm[rr * C + r] * dW[rr * DK + i];
+    YW[idx] = acc2;
+  }
+  for (int idx = tid; idx < C * DV; idx += blockDim.x) {
+    int s = idx / DV, jj = idx % DV;
+    float acc = 0.f;
+    for (int r = s; r < C; r++) acc += Tm[r * C + s] * dEg[r * DV + jj];
+    YU[idx] = acc;
+  }
+  __syncthreads();
+
+  // ---- dv = beta YU;  dbeta from U and W;  dA = -(YU U^T + YW W^T) strict lower
+  TI* dvo = (TI*)io.dv;
+  for (int idx = tid; idx < C * DV; idx += blockDim.x) {
+    int r = idx / DV, jj = idx % DV;
+    if (r < L) stf(dvo + ((int64_t)(t0 + r) * H + h) * DV + jj, bet[r] * YU[idx]);
+  }
+  for (int r = warp; r < L; r += nw) {
+    float acc = 0.f;
+    for (int jj = lane; jj < DV; jj += 32) acc += YU[r * DV + jj] * ldf(v + ((int64_t)(t0 + r) * H + h) * DV + jj);
+    for (int i = lane; i < DK; i += 32) acc += YW[r * DK + i] * kh[r * DK + i] * expf(G[r * DK + i]);
+    acc = warp_sum(acc);
+    if (lane == 0) dbet[r] += acc;
+  }
+  for (int idx = tid; idx < C * C; idx += blockDim.x) {
+    int r = idx / C, s = idx % C;
+    float acc = 0.f;
+    if (s < r) {
+      for (int jj = 0; jj < DV; jj++) acc += YU[r * DV + jj] * Ug[s * DV + jj];
+      for (int i = 0; i < DK; i++) acc += YW[r * DK + i] * Wg[s * DK + i];
+    }
+    dAm[idx] = -acc;
+  }
+  __syncthreads();
+  for (int r = warp; r < L; r += nw) {
+    float acc = 0.f;
+    for (int s = lane; s < r; s += 32) acc += dAm[r * C + s] * Ap[r * C + s];
+    acc = warp_sum(acc);
+    if (lane == 0) dbet[r] += acc;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < C * C; idx += blockDim.x) dAm[idx] *= bet[idx / C];  // gradient of Ap
+  __syncthreads();
+
+  // ---- pairwise decay-ratio terms and the elementwise ones -> dqh, dkh, dG
+  for (int idx = tid; idx < C * DK; idx += blockDim.x) {
+    int r = idx / DK, i = idx % DK;
+    float Gr = G[idx];
+    float prow = 0.f, arow = 0.f, col = 0.f;
+    for (int s = 0; s <= r; s++) {
+      float e = expf(Gr - G[s * DK + i]);
+      prow += dPm[r * C + s] * kh[s * DK + i] * e;
+      arow += dAm[r * C + s] * kh[s * DK + i] * e;   // dAm is 0 on the diagonal
+    }
+    for (int rr = r; rr < C; rr++) {
+      float e = expf(G[rr * DK + i] - Gr);
+      col += dPm[rr * C + r] * qh[rr * DK + i] * e + dAm[rr * C + r] * kh[rr * DK + i] * e;
+    }
+    float Gam = expf(Gr);
+    float KDr = kh[idx] * expf(G[(L - 1) * DK + i] - Gr);
+    float dkg = bet[r] * YW[idx];  // gradient of K^ * Gamma
+    dqh[idx] = prow + dQG[idx] * Gam;
+    dkh[idx] = arow + col + dkg * Gam + dKd[idx] * expf(G[(L - 1) * DK + i] - Gr);
+    dG[idx] = qh[idx] * prow + kh[idx] * arow - kh[idx] * col + dQG[idx] * qh[idx] * Gam
+              + dkg * kh[idx] * Gam - dKd[idx] * KDr;
+  }
+  __syncthreads();
+
+  // ---- per channel: G_last terms, reverse cumsum -> dg, gate backward, partials
+  TI* dfo = (TI*)io.df;
+  float pA_local = 0.f;
+  for (int i = tid; i < DK; i += blockDim.x) {
+    float Glast = G[(L - 1) * DK + i];
+    float extra = dgam[i] * expf(Glast);
+    for (int r = 0; r < L; r++) extra += dKd[r * DK + i] * kh[r * DK + i] * expf(Glast - G[r * DK + i]);
+    float acc = extra;  // dG at row L-1 gets the G_last terms
+    float pdt = 0.f;
+    for (int r = L - 1; r >= 0; r--) {
+      acc += dG[r * DK + i];
+      int64_t off = ((int64_t)(t0 + r) * H + h) * DK + i;
+      float x = ldf(f + off) + io.dt_bias[h * DK + i];
+      float g = -a * softplus_f(x);
+      float dx = acc * (-a) * sigmoid_f(x);
+      stf(dfo + off, dx);
+      pdt += dx;
+      pA_local += acc * g;
+    }
+    w.pdt[ch * DK + i] = pdt;
+  }
+  float tot = block_sum(pA_local, red);
+  if (tid == 0) w.pA[ch] = tot;
+
+  // ---- L2-norm backward and db
+  TI* dqo = (TI*)io.dq;
+  TI* dko = (TI*)io.dk;
+  TI* dbo = (TI*)io.db;
+  for (int r = warp; r < L; r += nw) {
+    float pq = 0.f, pk = 0.f;
+    for (int i = lane; i < DK; i += 32) { pq += qh[r * DK + i] * dqh[r * DK + i]; pk += kh[r * DK + i] * dkh[r * DK + i]; }
+    pq = warp_sum(pq); pk = warp_sum(pk);
+    for (int i = lane; i < DK; i += 32) {
+      int64_t off = ((int64_t)(t0 + r) * H + h) * DK + i;
+      stf(dqo + off, (dqh[r * DK + i] - qh[r * DK + i] * pq) / nq[r]);
+      stf(dko + off, (dkh[r * DK + i] - kh[r * DK + i] * pk) / nk[r]);
+    }
+    if (lane == 0) stf(dbo + (int64_t)(t0 + r) * H + h, dbet[r] * bet[r] * (1.f - bet[r]));
+  }
+}
+
+// dA_log[h] and ddt_bias[h, :] summed over chunks in a fixed order.
+__global__ void __launch_bounds__(256) bwd_reduce_kernel(Dims d, BwdIO io, Ws w) {
+  const int h = blockIdx.x, tid = threadIdx.x, H = d.H, dk = d.dk;
+  const int nc = *w.n_chunks;
+  __shared__ float red[256];
+  if (!saved_ok(d, w.tag, w.err)) return;
+  float acc = 0.f;
+  for (int c = tid; c < nc; c += blockDim.x) acc += w.pA[(int64_t)c * H + h];
+  red[tid] = acc;
+  __syncthreads();
+  for (int s = 128; s > 0; s >>= 1) {
+    if (tid < s) red[tid] += red[tid + s];
+    __syncthreads();
+  }
+  if (tid == 0) io.dA_log[h] = red[0];
+  for (int i = tid; i < dk; i += blockDim.x) {
+    float s = 0.f;
+    for (int c = 0; c < nc; c++) s += w.pdt[((int64_t)c * H + h) * dk + i];
+    io.ddt_bias[h * dk + i] = s;
+  }
+}
+
+template <typename TI, int DK, int DV>
+static cudaError_t bwd_scan_launch(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st) {
+  size_t smem = sizeof(float) * (DK * NT + 2 * C * NT + 3 * C * DK + C * C + DK);
+  cudaError_t e = cudaFuncSetAttribute(bwd_scan_kernel<TI, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(d.n_docs, d.H, DV / NT);
+  prof_begin(K_BWD_SCAN, st);
+  bwd_scan_kernel<TI, DK, DV><<<grid, 256, smem, st>>>(d, io, w);
+  prof_end(K_BWD_SCAN, st);
+  return cudaGetLastError();
+}
+
+template <typename TI, int DK, int DV>
+static cudaError_t bwd_intra_launch(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st) {
+  size_t smem = sizeof(float) * (3 * C * DK + 5 * C * C + 4 * C + DK + 32);
+  cudaError_t e = cudaFuncSetAttribute(bwd_intra_kernel<TI, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(d.nc_max, d.H);
+  prof_begin(K_BWD_INTRA, st);
+  bwd_intra_kernel<TI, DK, DV><<<grid, 256, smem, st>>>(d, io, w);
+  prof_end(K_BWD_INTRA, st);
+  return cudaGetLastError();
+}
+
+#define KDA_DISPATCH(FN, ...)                                                              \
+  do {                                                                                     \
+    if (dtype == 0) {                                                                      \
+      if (d.dk == 32 && d.dv == 64) return FN<__nv_bfloat16, 32, 64>(__VA_ARGS__);         \
+      if (d.dk == 64 && d.dv == 64) return FN<__nv_bfloat16, 64, 64>(__VA_ARGS__);         \
+      if (d.dk == 64 && d.dv == 128) return FN<__nv_bfloat16, 64, 128>(__VA_ARGS__);       \
+      if (d.dk == 128 && d.dv == 128) return FN<__nv_bfloat16, 128, 128>(__VA_ARGS__);     \
+    } else {                                                                               \
+      if (d.dk == 32 && d.dv == 64) return FN<float, 32, 64>(__VA_ARGS__);                 \
+      if (d.dk == 64 && d.dv == 64) return FN<float, 64, 64>(__VA_ARGS__);                 \
+      if (d.dk == 64 && d.dv == 128) return FN<float, 64, 128>(__VA_ARGS__);               \
+      if (d.dk == 128 && d.dv == 128) return FN<float, 128, 128>(__VA_ARGS__);             \
+    }                                                                                      \
+    return cudaErrorInvalidValue;                                                          \
+  } while (0)
+
+cudaError_t launch_bwd_scan(int dtype, const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st) {
+  KDA_DISPATCH(bwd_scan_launch, d, io, w, st);
+}
+cudaError_t launch_bwd_intra(int dtype, const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st) {
+  KDA_DISPATCH(bwd_intra_launch, d, io, w, st);
+}
+cudaError_t launch_bwd_reduce(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st) {
+  prof_begin(K_BWD_REDUCE, st);
+  bwd_reduce_kernel<<<d.H, 256, 0, st>>>(d, io, w);
+  prof_end(K_BWD_REDUCE, st);
+  return cudaGetLastError();
+}
+
+}  // namespace kda

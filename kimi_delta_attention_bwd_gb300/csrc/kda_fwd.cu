@@ -1,0 +1,261 @@
+// Forward kernels of the KDA chunked gated delta rule.
+//
+// Chunk algebra (per document, head and 64-token chunk with entry state S;
+// G = in-chunk inclusive cumulative log-decay, Gamma = exp(G)):
+//   A  = strict_lower( diag(beta) (K^ K^T with ratios exp(G_r - G_s)) )
+//   T  = (I + A)^-1,  W = T diag(beta) (K^ * Gamma),  U = T diag(beta) V
+//   E  = U - W S                    (the per-token corrections e_r)
+//   O  = scale (Q^ * Gamma) S + scale inclusive_lower(Q^ K^T ratios) E
+//   S' = Diag(Gamma_last) S + (K^ * exp(G_last - G))^T E
+// This is the recurrence of the "Pure KDA 300M" guide (Overview) and of the
+// openkimi KDA oracle unrolled over one chunk; every decay ratio used is
+// exp of a non-positive number, so nothing can overflow.
+#include "kda_internal.cuh"
+
+namespace kda {
+
+// One CTA per (chunk, head): the gate/norm prologue and the intra-chunk
+// factors W, U, P, QG, KD, gamma, written to the workspace.
+template <typename TI, int DK, int DV>
+__global__ void __launch_bounds__(256) fwd_intra_kernel(Dims d, FwdIO io, Ws w) {
+  const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  if (j >= *w.n_chunks) return;
+  const int L = w.chunk_len[j];
+  if (L <= 0) return;
+  const int t0 = w.chunk_tok0[j];
+  const int H = d.H;
+  const int64_t ch = (int64_t)j * H + h;
+
+  extern __shared__ float sm[];
+  float* qh = sm;               // [C][DK]
+  float* kh = qh + C * DK;      // [C][DK]
+  float* G = kh + C * DK;       // [C][DK]
+  float* vv = G + C * DK;       // [C][DV]
+  float* Am = vv + C * DV;      // [C][C]
+  float* Tm = Am + C * C;       // [C][C]
+  float* bet = Tm + C * C;      // [C]
+
+  const TI* q = (const TI*)io.q;
+  const TI* k = (const TI*)io.k;
+  const TI* f = (const TI*)io.f;
+  const TI* v = (const TI*)io.v;
+  const TI* b = (const TI*)io.b;
+  const float a = expf(io.A_log[h]);
+
+  for (int idx = tid; idx < C * DK; idx += blockDim.x) {
+    int r = idx / DK, i = idx % DK;
+    float qv = 0.f, kv = 0.f, gv = 0.f;
+    if (r < L) {
+      int64_t off = ((int64_t)(t0 + r) * H + h) * DK + i;
+      qv = ldf(q + off);
+      kv = ldf(k + off);
+      gv = -a * softplus_f(ldf(f + off) + io.dt_bias[h * DK + i]);
+    }
+    qh[idx] = qv; kh[idx] = kv; G[idx] = gv;
+  }
+  for (int idx = tid; idx < C * DV; idx += blockDim.x) {
+    int r = idx / DV, jj = idx % DV;
+    vv[idx] = r < L ? ldf(v + ((int64_t)(t0 + r) * H + h) * DV + jj) : 0.f;
+  }
+  for (int r = tid; r < C; r += blockDim.x)
+    bet[r] = r < L ? sigmoid_f(ldf(b + (int64_t)(t0 + r) * H + h)) : 0.f;
+  __syncthreads();
+
+  // L2 norms (one warp per row) and the in-chunk cumulative log-decay.
+  const int warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+  for (int r = warp; r < C; r += nw) {
+    float sq = 0.f, sk = 0.f;
+    for (int i = lane; i < DK; i += 32) { sq += qh[r * DK + i] * qh[r * DK + i]; sk += kh[r * DK + i] * kh[r * DK + i]; }
+    sq = warp_sum(sq); sk = warp_sum(sk);
+    float iq = 1.0f / sqrtf(sq + L2_EPS), ik = 1.0f / sqrtf(sk + L2_EPS);
+    for (int i = lane; i < DK; i += 32) { qh[r * DK + i] *= iq; kh[r * DK + i] *= ik; }
+  }
+  for (int i = tid; i < DK; i += blockDim.x) {
+    float acc = 0.f;
+    for (int r = 0; r < C; r++) { acc += G[r * DK + i]; G[r * DK + i] = acc; }
+  }
+  __syncthreads();
+
+  // A (strict lower, beta-scaled) and P (inclusive lower, scale-scaled).
+  float* Pg = w.P + ch * C * C;
+  for (int idx = tid; idx < C * C; idx += blockDim.x) {
+    int r = idx / C, s = idx % C;
+    float accA = 0.f, accP = 0.f;
+    if (s <= r) {
+      for (int i = 0; i < DK; i++) {
+        float e = expf(G[r * DK + i] - G[s * DK + i]);
+        float ks = kh[s * DK + i] * e;
+        accP += qh[r * DK + i] * ks;
+        accA += kh[r * DK + i] * ks;
+      }
+    }
+    Am[idx] = s < r ? bet[r] * accA : 0.f;
+    Pg[idx] = d.scale * accP;
+    Tm[idx] = (r == s) ? 1.f : 0.f;
+  }
+  __syncthreads();
+
+  // T = (I + A)^-1 by forward substitution, one row per step.
+  for (int r = 1; r < C; r++) {
+    for (int c = tid; c < r; c += blockDim.x) {
+      float acc = 0.f;
+      for (int s = c; s < r; s++) acc += Am[r * C + s] * Tm[s * C + c];
+      Tm[r * C + c] = -acc;
+    }
+    __syncthreads();
+  }
+
+  float* Wg = w.W + ch * C * DK;
+  float* QGg = w.QG + ch * C * DK;
+  float* KDg = w.KD + ch * C * DK;
+  const float* Glast = G + (L - 1) * DK;
+  for (int idx = tid; idx < C * DK; idx += blockDim.x) {
+    int r = idx / DK, i = idx % DK;
+    float acc = 0.f;
+    for (int s = 0; s <= r; s++) acc += Tm[r * C + s] * bet[s] * kh[s * DK + i] * expf(G[s * DK + i]);
+    Wg[idx] = acc;
+    float Gr = G[idx];
+    QGg[idx] = d.scale * qh[idx] * expf(Gr);
+    KDg[idx] = kh[idx] * expf(Glast[i] - Gr);
+  }
+  float* Ug = w.U + ch * C * DV;
+  for (int idx = tid; idx < C * DV; idx += blockDim.x) {
+    int r = idx / DV, jj = idx % DV;
+    float acc = 0.f;
+    for (int s = 0; s <= r; s++) acc += Tm[r * C + s] * bet[s] * vv[s * DV + jj];
+    Ug[idx] = acc;
+  }
+  for (int i = tid; i < DK; i += blockDim.x) w.gam[ch * DK + i] = expf(Glast[i]);
+}
+
+constexpr int NT = 16;  // dv columns per scan CTA
+
+// One CTA per (document, head, 16 value columns): walks the document's
+// chunks in order carrying the fp32 state slice S[:, cols].
+template <typename TI, int DK, int DV>
+__global__ void __launch_bounds__(256) fwd_scan_kernel(Dims d, FwdIO io, Ws w) {
+  const int doc = blockIdx.x, h = blockIdx.y, c0col = blockIdx.z * NT, tid = threadIdx.x;
+  if (*w.err != 0) return;
+  const int H = d.H;
+  extern __shared__ float sm[];
+  float* S = sm;               // [DK][NT]
+  float* E = S + DK * NT;      // [C][NT]
+  float* Wt = E + C * NT;      // [C][DK]
+  float* QGt = Wt + C * DK;    // [C][DK]
+  float* KDt = QGt + C * DK;   // [C][DK]
+  float* Pt = KDt + C * DK;    // [C][C]
+  float* gm = Pt + C * C;      // [DK]
+  TI* o = (TI*)io.o;
+
+  for (int idx = tid; idx < DK * NT; idx += blockDim.x) {
+    int i = idx / NT, jj = idx % NT;
+    S[idx] = io.h0 ? io.h0[(((int64_t)doc * H + h) * DK + i) * DV + c0col + jj] : 0.f;
+  }
+  const int cb = w.doc_chunk0[doc], ce = w.doc_chunk0[doc + 1];
+  __syncthreads();
+  for (int c = cb; c < ce; c++) {
+    const int64_t ch = (int64_t)c * H + h;
+    const int L = w.chunk_len[c], t0 = w.chunk_tok0[c];
+    if (io.save)
+      for (int idx = tid; idx < DK * NT; idx += blockDim.x) {
+        int i = idx / NT, jj = idx % NT;
+        w.Sent[(ch * DK + i) * DV + c0col + jj] = S[idx];
+      }
+    for (int idx = tid; idx < C * DK; idx += blockDim.x) {
+      Wt[idx] = w.W[ch * C * DK + idx];
+      QGt[idx] = w.QG[ch * C * DK + idx];
+      KDt[idx] = w.KD[ch * C * DK + idx];
+    }
+    for (int idx = tid; idx < C * C; idx += blockDim.x) Pt[idx] = w.P[ch * C * C + idx];
+    for (int i = tid; i < DK; i += blockDim.x) gm[i] = w.gam[ch * DK + i];
+    __syncthreads();
+    for (int idx = tid; idx < C * NT; idx += blockDim.x) {
+      int r = idx / NT, jj = idx % NT;
+      float acc = w.U[(ch * C + r) * DV + c0col + jj];
+      for (int i = 0; i < DK; i++) acc -= Wt[r * DK + i] * S[i * NT + jj];
+      E[idx] = acc;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < C * NT; idx += blockDim.x) {
+      int r = idx / NT, jj = idx % NT;
+      if (r < L) {
+        float acc = 0.f;
+        for (int i = 0; i < DK; i++) acc += QGt[r * DK + i] * S[i * NT + jj];
+        for (int s = 0; s <= r; s++) acc += Pt[r * C + s] * E[s * NT + jj];
+        stf(o + ((int64_t)(t0 + r) * H + h) * DV + c0col + jj, acc);
+      }
+    }
+    float nv[(DK * NT + 255) / 256];
+#pragma unroll
+    for (int u = 0; u < (DK * NT + 255) / 256; u++) {
+      int idx = tid + u * 256;
+      if (idx < DK * NT) {
+        int i = idx / NT, jj = idx % NT;
+        float acc = gm[i] * S[idx];
+        for (int r = 0; r < C; r++) acc += KDt[r * DK + i] * E[r * NT + jj];
+        nv[u] = acc;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < (DK * NT + 255) / 256; u++) {
+      int idx = tid + u * 256;
+      if (idx < DK * NT) S[idx] = nv[u];
+    }
+    __syncthreads();
+  }
+  if (io.h_final)
+    for (int idx = tid; idx < DK * NT; idx += blockDim.x) {
+      int i = idx / NT, jj = idx % NT;
+      io.h_final[(((int64_t)doc * H + h) * DK + i) * DV + c0col + jj] = S[idx];
+    }
+}
+
+template <typename TI, int DK, int DV>
+static cudaError_t fwd_intra_launch(const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st) {
+  size_t smem = sizeof(float) * (3 * C * DK + C * DV + 2 * C * C + C);
+  cudaError_t e = cudaFuncSetAttribute(fwd_intra_kernel<TI, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(d.nc_max, d.H);
+  prof_begin(K_FWD_INTRA, st);
+  fwd_intra_kernel<TI, DK, DV><<<grid, 256, smem, st>>>(d, io, w);
+  prof_end(K_FWD_INTRA, st);
+  return cudaGetLastError();
+}
+
+template <typename TI, int DK, int DV>
+static cudaError_t fwd_scan_launch(const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st) {
+  size_t smem = sizeof(float) * (DK * NT + C * NT + 3 * C * DK + C * C + DK);
+  cudaError_t e = cudaFuncSetAttribute(fwd_scan_kernel<TI, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(d.n_docs, d.H, DV / NT);
+  prof_begin(K_FWD_SCAN, st);
+  fwd_scan_kernel<TI, DK, DV><<<grid, 256, smem, st>>>(d, io, w);
+  prof_end(K_FWD_SCAN, st);
+  return cudaGetLastError();
+}
+
+#define KDA_DISPATCH(FN, ...)                                                              \
+  do {                                                                                     \
+    if (dtype == 0) {                                                                      \
+      if (d.dk == 32 && d.dv == 64) return FN<__nv_bfloat16, 32, 64>(__VA_ARGS__);         \
+      if (d.dk == 64 && d.dv == 64) return FN<__nv_bfloat16, 64, 64>(__VA_ARGS__);         \
+      if (d.dk == 64 && d.dv == 128) return FN<__nv_bfloat16, 64, 128>(__VA_ARGS__);       \
+      if (d.dk == 128 && d.dv == 128) return FN<__nv_bfloat16, 128, 128>(__VA_ARGS__);     \
+    } else {                                                                               \
+      if (d.dk == 32 && d.dv == 64) return FN<float, 32, 64>(__VA_ARGS__);                 \
+      if (d.dk == 64 && d.dv == 64) return FN<float, 64, 64>(__VA_ARGS__);                 \
+      if (d.dk == 64 && d.dv == 128) return FN<float, 64, 128>(__VA_ARGS__);               \
+      if (d.dk == 128 && d.dv == 128) return FN<float, 128, 128>(__VA_ARGS__);             \
+    }                                                                                      \
+    return cudaErrorInvalidValue;                                                          \
+  } while (0)
+
+cudaError_t launch_fwd_intra(int dtype, const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st) {
+  KDA_DISPATCH(fwd_intra_launch, d, io, w, st);
+}
+cudaError_t launch_fwd_scan(int dtype, const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st) {
+  KDA_DISPATCH(fwd_scan_launch, d, io, w, st);
+}
+
+}  // namespace kda

@@ -1,0 +1,120 @@
+// Internal declarations shared by the CUDA translation units of the KDA
+// library (not part of the C ABI).
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+namespace kda {
+
+constexpr int C = 64;          // chunk length (tokens)
+constexpr float L2_EPS = 1e-6f; // q/k L2-norm epsilon
+
+// Kernel ids for the per-kernel timing brackets.
+enum KernelId {
+  K_TABLE = 0,
+  K_FWD_INTRA,
+  K_FWD_SCAN,
+  K_BWD_SCAN,
+  K_BWD_INTRA,
+  K_BWD_REDUCE,
+  K_COUNT
+};
+
+// Device-side view of the caller's workspace.  Offsets are fixed by
+// layout_workspace() from the problem sizes; the error word sits at byte 0.
+struct Ws {
+  int32_t* err;         // [1]  device error word (kda_status value)
+  int32_t* tag;         // [1]  problem tag of the forward that saved this workspace
+  int32_t* n_chunks;    // [1]
+  int32_t* doc_chunk0;  // [n_docs + 1] first chunk of each document
+  int32_t* chunk_tok0;  // [nc_max] first flattened token of each chunk
+  int32_t* chunk_len;   // [nc_max] tokens in the chunk (1..C), 0 = unused
+  int32_t* chunk_doc;   // [nc_max]
+  // forward intermediates, per chunk-head ch = chunk * H + h
+  float* W;    // [ch][C][dk]  T diag(beta) (K^ * Gamma)
+  float* U;    // [ch][C][dv]  T diag(beta) V
+  float* P;    // [ch][C][C]   scale * inclusive-lower (Q^ K^T with decay ratios)
+  float* QG;   // [ch][C][dk]  scale * Q^ * Gamma
+  float* KD;   // [ch][C][dk]  K^ * exp(G_last - G)
+  float* gam;  // [ch][dk]     exp(G_last)
+  float* Sent; // [ch][dk][dv] state entering the chunk (saved for backward)
+  // backward
+  float* dE;   // [ch][C][dv]  gradient of E = U - W S
+  float* dSn;  // [ch][dk][dv] gradient of the state leaving the chunk
+  float* pA;   // [ch]         per chunk-head partial of dA_log
+  float* pdt;  // [ch][dk]     per chunk-head partial of ddt_bias
+  float* scr;  // [ch][scr_per_ch] backward scratch
+  int64_t scr_per_ch;
+};
+
+struct Dims {
+  int Ntok, H, dk, dv, n_docs, nc_max, B, T;
+  float scale;
+  int32_t tag;   // nonzero hash of the problem; the forward stores it when saving
+  int32_t save;  // forward saves for the backward
+};
+
+// Backward kernels refuse a workspace that no saving forward of the same
+// problem filled (flagging KDA_ERR_WORKSPACE instead of reading garbage).
+__device__ __forceinline__ bool saved_ok(const Dims& d, const int32_t* tag, int32_t* err) {
+  if (*tag != d.tag) {
+    *err = -5;
+    return false;
+  }
+  return *err == 0;
+}
+
+struct FwdIO {
+  const void *q, *k, *v, *f, *b;
+  const float *A_log, *dt_bias, *h0;
+  void* o;
+  float* h_final;
+  int save;
+};
+
+struct BwdIO {
+  const void *q, *k, *v, *f, *b;
+  const float *A_log, *dt_bias;
+  const void* dO;
+  const float* dh_final;
+  void *dq, *dk, *dv, *df, *db;
+  float *dA_log, *ddt_bias, *dh0;
+};
+
+// Launch wrappers (return cudaGetLastError of their launches).
+cudaError_t launch_chunk_table(const int32_t* cu, const Dims& d, const Ws& w, cudaStream_t st);
+cudaError_t launch_fwd_intra(int dtype, const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st);
+cudaError_t launch_fwd_scan(int dtype, const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st);
+cudaError_t launch_bwd_scan(int dtype, const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st);
+cudaError_t launch_bwd_intra(int dtype, const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st);
+cudaError_t launch_bwd_reduce(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st);
+
+// Timing brackets (no-ops unless kda_prof_start() armed them).
+void prof_begin(int kid, cudaStream_t st);
+void prof_end(int kid, cudaStream_t st);
+
+// Bytes of backward scratch per chunk-head.
+inline int64_t bwd_scratch_floats(int dk, int dv) {
+  return (int64_t)C * dv * 2 + (int64_t)C * dk * 8;
+}
+
+// ------------------------------------------------------------ device helpers
+__device__ __forceinline__ float ldf(const float* p) { return *p; }
+__device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void stf(float* p, float x) { *p = x; }
+__device__ __forceinline__ void stf(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float softplus_f(float x) {
+  return fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x)));
+}
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+}  // namespace kda

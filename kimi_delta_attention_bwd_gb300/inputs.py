@@ -64,6 +64,11 @@ WORKLOADS = [
 ]
 
 
+def custom(B, T, H, dk, dv, dtype="bf16", h0=False, dh_final=False, name="custom") -> KdaWorkload:
+    """An ad-hoc workload (edge cases and small parity cases)."""
+    return KdaWorkload(99, name, B, T, H, dk, dv, dtype, True, None, h0, dh_final)
+
+
 def doc_lengths_docs600(total: int, rng: np.random.RandomState) -> list[int]:
     """Log-normal document lengths, median 600 tokens, sigma 1.0 (a reading),
     clipped to [1, 8192], with at least 5% of documents forced to one token.
@@ -106,11 +111,13 @@ def cu_from_lengths(lens) -> np.ndarray:
     return cu
 
 
-def make_inputs(w: KdaWorkload | int, seed: Optional[int] = None, with_grad_inputs: Optional[bool] = None):
+def make_inputs(w: KdaWorkload | int, seed: Optional[int] = None, with_grad_inputs: Optional[bool] = None,
+                lengths=None):
     """Draw the inputs of one workload.  Returns a dict of CPU tensors:
     q, k, f [B,T,H,dk]; v [B,T,H,dv]; b [B,T,H] in the io dtype;
     A_log [H], dt_bias [H,dk] float32; cu_seqlens int32 [n+1] or None
-    (None means equal-length rows); h0 [n,H,dk,dv] float32 or None;
+    (None means equal-length rows; explicit `lengths` override the workload's
+    own document draw); h0 [n,H,dk,dv] float32 or None;
     dO [B,T,H,dv] (io dtype) and dh_final float32 or None when the workload
     has a backward; scale (python float)."""
     if isinstance(w, int):
@@ -138,7 +145,12 @@ def make_inputs(w: KdaWorkload | int, seed: Optional[int] = None, with_grad_inpu
     ud = torch.rand(H, dk, generator=gen, dtype=torch.float64)
     dtv = torch.exp(math.log(1e-3) + ud * (math.log(1e-1) - math.log(1e-3)))
     out["dt_bias"] = (dtv + torch.log(-torch.expm1(-dtv))).to(torch.float32)
-    if w.varlen is None:
+    if lengths is not None:
+        if sum(lengths) != B * T:
+            raise ValueError("lengths must sum to B*T")
+        cu = cu_from_lengths(lengths)
+        n_seqs = len(cu) - 1
+    elif w.varlen is None:
         cu = None
         n_seqs = B
     elif w.varlen == "docs600":

@@ -1,0 +1,102 @@
+"""Shared helpers of the parity tests: run the CUDA path and the oracle on the
+same seeded inputs and compare them with the tolerances of the KDA spec."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from kimi_delta_attention_bwd_gb300.inputs import numpy_f64
+
+# Tolerances: max|err| / rms(ref) for the outputs and every gradient, and
+# relative Frobenius error for the fp32 states (final state and its
+# gradient dS0).
+TOL_IO = 1e-2
+TOL_STATE = 2e-3
+
+
+def rel_max(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rms = np.sqrt(np.mean(ref * ref)) if ref.size else 0.0
+    if rms == 0.0:
+        return float(np.abs(got).max()) if got.size else 0.0
+    return float(np.abs(got - ref).max() / rms)
+
+
+def rel_fro(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    n = np.linalg.norm(ref)
+    if n == 0.0:
+        return float(np.linalg.norm(got))
+    return float(np.linalg.norm(got - ref) / n)
+
+
+def to_dev(inp, device="cuda"):
+    out = {}
+    for k, v in inp.items():
+        out[k] = v.to(device) if isinstance(v, torch.Tensor) else v
+    return out
+
+
+def run_gpu(inp, backward: bool, device="cuda"):
+    """Runs kda_forward (and kda_backward) through the C ABI; returns float64
+    numpy arrays in the flattened [Ntok, H, d] layout."""
+    from kimi_delta_attention_bwd_gb300 import kda_forward, kda_backward
+    d = to_dev(inp, device)
+    cu_host = None if inp.get("cu_seqlens") is None else inp["cu_seqlens"].numpy()
+    o, hf, ctx = kda_forward(d["q"], d["k"], d["v"], d["f"], d["b"], d["A_log"], d["dt_bias"],
+                             scale=d["scale"], h0=d.get("h0"), cu_seqlens=d.get("cu_seqlens"),
+                             cu_seqlens_host=cu_host, save_for_backward=backward)
+    B, T, H = inp["q"].shape[:3]
+    res = {"o": o, "h_final": hf}
+    if backward:
+        g = kda_backward(ctx, d["dO"], d.get("dh_final"))
+        res.update(g)
+    torch.cuda.synchronize()
+    out = {}
+    for k, v in res.items():
+        if v is None:
+            continue
+        v = v.detach().to(torch.float64).cpu().numpy()
+        if k in ("o", "dq", "dk", "dv", "df", "db") and v.ndim >= 3:
+            v = v.reshape(B * T, H, *v.shape[3:]) if v.ndim == 4 else v.reshape(B * T, H)
+        out[k] = v
+    return out
+
+
+def run_oracle(inp, backward: bool, units=None, threads=None):
+    from oracle import oracle
+    x = numpy_f64(inp)
+    o, hf = oracle.forward(x, units=units, threads=threads)
+    res = {"o": o, "h_final": hf}
+    if backward:
+        g = oracle.backward(x, x["dO"], x.get("dh_final"), units=units, threads=threads)
+        res.update(g)
+    return res
+
+
+def compare(gpu, ref, backward: bool, rows=None, states=None, params_heads=None, tol_io=TOL_IO,
+            tol_state=TOL_STATE):
+    """Returns {name: error} and asserts every error is within tolerance.
+    rows/states: index arrays restricting the comparison to sampled units."""
+    errs = {}
+    sel = (lambda a: a) if rows is None else (lambda a: a[rows])
+    sst = (lambda a: a) if states is None else (lambda a: a[states])
+    errs["o"] = rel_max(sel(gpu["o"]), sel(ref["o"]))
+    errs["h_final"] = rel_fro(sst(gpu["h_final"]), sst(ref["h_final"]))
+    if backward:
+        for n in ("dq", "dk", "dv", "df", "db"):
+            errs[n] = rel_max(sel(gpu[n]), sel(ref[n]))
+        if "dh0" in gpu:
+            errs["dh0"] = rel_fro(sst(gpu["dh0"]), sst(ref["dh0"]))
+        ph = slice(None) if params_heads is None else params_heads
+        errs["dA_log"] = rel_max(gpu["dA_log"][ph], ref["dA_log"][ph])
+        errs["ddt_bias"] = rel_max(gpu["ddt_bias"][ph], ref["ddt_bias"][ph])
+    bad = {}
+    for n, e in errs.items():
+        lim = tol_state if n in ("h_final", "dh0") else tol_io
+        if not (e <= lim):
+            bad[n] = (e, lim)
+    assert not bad, f"parity failures {bad}; all errors {errs}"
+    return errs
