@@ -134,7 +134,8 @@ __global__ void __launch_bounds__(256) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   float* nq = bet + C;          // [C]
   float* nk = nq + C;           // [C]
   float* dbet = nk + C;         // [C]
-  float* dgam = dbet + C;       // [DK]
+  float* omb = dbet + C;        // [C]  1 - beta, as sigmoid(-b) (exact near beta = 1)
+  float* dgam = omb + C;        // [DK]
   float* red = dgam + DK;       // [32]
 
   float* scr = w.scr + ch * w.scr_per_ch;
@@ -174,7 +175,9 @@ __global__ void __launch_bounds__(256) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
     qh[idx] = qv; kh[idx] = kv; G[idx] = gv;
   }
   for (int r = tid; r < C; r += blockDim.x) {
-    bet[r] = r < L ? sigmoid_f(ldf(b + (int64_t)(t0 + r) * H + h)) : 0.f;
+    float br = r < L ? ldf(b + (int64_t)(t0 + r) * H + h) : 0.f;
+    bet[r] = r < L ? sigmoid_f(br) : 0.f;
+    omb[r] = sigmoid_f(-br);
     dbet[r] = 0.f;
   }
   __syncthreads();
@@ -363,7 +366,7 @@ __global__ void __launch_bounds__(256) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
       stf(dqo + off, (dqh[r * DK + i] - qh[r * DK + i] * pq) / nq[r]);
       stf(dko + off, (dkh[r * DK + i] - kh[r * DK + i] * pk) / nk[r]);
     }
-    if (lane == 0) stf(dbo + (int64_t)(t0 + r) * H + h, dbet[r] * bet[r] * (1.f - bet[r]));
+    if (lane == 0) stf(dbo + (int64_t)(t0 + r) * H + h, dbet[r] * bet[r] * omb[r]);
   }
 }
 
@@ -403,7 +406,7 @@ static cudaError_t bwd_scan_launch(const Dims& d, const BwdIO& io, const Ws& w, 
 
 template <typename TI, int DK, int DV>
 static cudaError_t bwd_intra_launch(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st) {
-  size_t smem = sizeof(float) * (3 * C * DK + 5 * C * C + 4 * C + DK + 32);
+  size_t smem = sizeof(float) * (3 * C * DK + 5 * C * C + 5 * C + DK + 32);
   cudaError_t e = cudaFuncSetAttribute(bwd_intra_kernel<TI, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(d.nc_max, d.H);

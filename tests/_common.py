@@ -7,20 +7,43 @@ import torch
 
 from kimi_delta_attention_bwd_gb300.inputs import numpy_f64
 
-# Tolerances: max|err| / rms(ref) for the outputs and every gradient, and
-# relative Frobenius error for the fp32 states (final state and its
-# gradient dS0).
+# Tolerances: max|err| / rms(ref) <= 1e-2 for the outputs and every gradient,
+# and relative Frobenius error <= 2e-3 for the fp32 states (final state and
+# its gradient dS0).  For outputs stored in bf16 the max-norm applies to the
+# computed value: the half-ulp rounding of the exact result to bf16, which no
+# bf16-output implementation can avoid, is subtracted element-wise first
+# (|err| - ulp_bf16(ref)/2, floored at 0).  Those outputs must also meet the
+# pages' bf16 bar on the rms ratio, rms(err)/rms(ref) <= 5e-3, which includes
+# the rounding.
 TOL_IO = 1e-2
 TOL_STATE = 2e-3
+TOL_RMS_BF16 = 5e-3
 
 
-def rel_max(got, ref):
+def half_ulp_bf16(ref):
+    """Half a unit in the last place of bf16 (8 significant bits) at |ref|."""
+    _, e = np.frexp(np.abs(ref))
+    return np.ldexp(1.0, e - 9) * (ref != 0)
+
+
+def rel_max(got, ref, bf16=False):
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     rms = np.sqrt(np.mean(ref * ref)) if ref.size else 0.0
+    err = np.abs(got - ref)
+    if bf16:
+        err = np.maximum(err - half_ulp_bf16(ref), 0.0)
     if rms == 0.0:
-        return float(np.abs(got).max()) if got.size else 0.0
-    return float(np.abs(got - ref).max() / rms)
+        return float(err.max()) if got.size else 0.0
+    return float(err.max() / rms)
+
+
+def rel_rms(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rms = np.sqrt(np.mean(ref * ref)) if ref.size else 0.0
+    e = np.sqrt(np.mean((got - ref) ** 2)) if ref.size else 0.0
+    return float(e / rms) if rms else float(e)
 
 
 def rel_fro(got, ref):
@@ -77,17 +100,19 @@ def run_oracle(inp, backward: bool, units=None, threads=None):
 
 
 def compare(gpu, ref, backward: bool, rows=None, states=None, params_heads=None, tol_io=TOL_IO,
-            tol_state=TOL_STATE):
+            tol_state=TOL_STATE, bf16=True):
     """Returns {name: error} and asserts every error is within tolerance.
     rows/states: index arrays restricting the comparison to sampled units."""
     errs = {}
     sel = (lambda a: a) if rows is None else (lambda a: a[rows])
     sst = (lambda a: a) if states is None else (lambda a: a[states])
-    errs["o"] = rel_max(sel(gpu["o"]), sel(ref["o"]))
+    io_names = ["o"] + (["dq", "dk", "dv", "df", "db"] if backward else [])
+    for n in io_names:
+        errs[n] = rel_max(sel(gpu[n]), sel(ref[n]), bf16)
+        if bf16:
+            errs[n + ":rms"] = rel_rms(sel(gpu[n]), sel(ref[n]))
     errs["h_final"] = rel_fro(sst(gpu["h_final"]), sst(ref["h_final"]))
     if backward:
-        for n in ("dq", "dk", "dv", "df", "db"):
-            errs[n] = rel_max(sel(gpu[n]), sel(ref[n]))
         if "dh0" in gpu:
             errs["dh0"] = rel_fro(sst(gpu["dh0"]), sst(ref["dh0"]))
         ph = slice(None) if params_heads is None else params_heads
@@ -95,7 +120,7 @@ def compare(gpu, ref, backward: bool, rows=None, states=None, params_heads=None,
         errs["ddt_bias"] = rel_max(gpu["ddt_bias"][ph], ref["ddt_bias"][ph])
     bad = {}
     for n, e in errs.items():
-        lim = tol_state if n in ("h_final", "dh0") else tol_io
+        lim = tol_state if n in ("h_final", "dh0") else TOL_RMS_BF16 if n.endswith(":rms") else tol_io
         if not (e <= lim):
             bad[n] = (e, lim)
     assert not bad, f"parity failures {bad}; all errors {errs}"

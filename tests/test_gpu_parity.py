@@ -3,9 +3,11 @@ same seeded inputs, at every workload's full size, plus the segmentation
 identity and the edge cases (partial chunks, one-token and empty documents,
 saturated beta, extreme gates, initial states, every compiled head shape).
 
-Tolerances (KDA spec): max|err|/rms(ref) <= 1e-2 for outputs and gradients,
-relative Frobenius error <= 2e-3 for the fp32 final state and dS0; the
-cu_seqlens segmentation itself is bit-exact.
+Tolerances (KDA spec): max|err|/rms(ref) <= 1e-2 for outputs and gradients
+(for bf16-stored outputs, after subtracting the half-ulp bf16 rounding of the
+exact value, with rms(err)/rms(ref) <= 5e-3 as well), relative Frobenius
+error <= 2e-3 for the fp32 final state and dS0; the cu_seqlens segmentation
+itself is bit-exact.
 """
 import json
 import os
@@ -31,7 +33,7 @@ def test_workload_full_size(wi):
     inp = make_inputs(w)
     gpu = run_gpu(inp, w.backward)
     ref = run_oracle(inp, w.backward)
-    _report(w.name, compare(gpu, ref, w.backward))
+    _report(w.name, compare(gpu, ref, w.backward, bf16=w.dtype == "bf16"))
 
 
 def test_workload4_sampled_heads():
@@ -103,7 +105,7 @@ def test_edge_shapes(name, dtype):
     inp = make_inputs(w, seed=11, lengths=e["lens"])
     gpu = run_gpu(inp, True)
     ref = run_oracle(inp, True)
-    _report(f"{name}/{dtype}", compare(gpu, ref, True))
+    _report(f"{name}/{dtype}", compare(gpu, ref, True, bf16=dtype == "bf16"))
 
 
 @pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 128)])
@@ -133,7 +135,7 @@ def test_degenerate_gates(mode):
     for n, v in gpu.items():
         assert np.isfinite(v).all(), n
     ref = run_oracle(inp, True)
-    _report(mode, compare(gpu, ref, True))
+    _report(mode, compare(gpu, ref, True, bf16=False))
 
 
 def test_device_only_bad_offsets_flagged():
