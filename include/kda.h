@@ -134,6 +134,38 @@ KDA_API kda_status kda_prof_start(void);
 KDA_API kda_status kda_prof_stop(double* total_ms, int64_t* launches, int n);
 KDA_API const char* kda_prof_kernel_name(int i);
 
+/* Forward without any caller-provided workspace (no counterpart in the
+ * paper; this is a convenience of this library).
+ *
+ * Who needs it: callers that cannot or must not call cudaMalloc -- for
+ * example a host program that has given all device memory to its own pool
+ * and exposes no allocator to plug-ins, or a latency-critical loop where the
+ * device synchronisation that cudaMalloc/cudaFree can imply is not
+ * acceptable.  Such callers still own q, k, v, f, b, A_log, dt_bias, h0, o and
+ * h_final; only the forward's scratch moves into a fixed array inside the
+ * library.
+ *
+ * The array is KDA_NOALLOC_SCRATCH_BYTES (32 MiB) of device memory, reserved
+ * on every GPU that loads this library for as long as the process lives.  A
+ * problem whose forward scratch (kda_workspace_size(p, 0)) exceeds it is
+ * rejected with KDA_ERR_WORKSPACE before anything is launched; roughly, at
+ * dk=32/dv=64 it holds about 600 chunk-heads (e.g. 8 heads x 4800 tokens).
+ * Nothing is saved for kda_bwd.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (the device must be current); make that first call before any
+ * stream capture.  Every call on a device shares the same array and leaves
+ * its contents behind (nothing in it needs to start zeroed: each call writes
+ * everything it later reads).  Calls whose work overlaps on the GPU -- on
+ * different streams, or from different host threads -- race on the array
+ * and give wrong results: serialise them.  Arguments and statuses are those
+ * of kda_fwd with save_for_backward = 0. */
+#define KDA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+KDA_API kda_status kda_fwd_noalloc(const kda_problem* p,
+                   const void* q, const void* k, const void* v, const void* f, const void* b,
+                   const float* A_log, const float* dt_bias, const float* h0,
+                   void* o, float* h_final, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -6,6 +6,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
+
 namespace kda {
 
 // ------------------------------------------------------------ chunk table
@@ -360,3 +362,54 @@ kda_status kda_prof_stop(double* total_ms, int64_t* launches, int n) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------ allocation-free forward
+// The forward's scratch for kda_fwd_noalloc lives in this fixed array (see
+// include/kda.h).  Host code must not pass the symbol itself to a kernel:
+// on the host it names a stand-in, not device memory.  Its device address
+// is looked up once per device (with that device current) and cached.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+kda_status noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return KDA_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return KDA_OK;
+}
+}  // namespace
+
+extern "C" kda_status kda_fwd_noalloc(const kda_problem* p, const void* q, const void* k, const void* v,
+                                      const void* f, const void* b, const float* A_log, const float* dt_bias,
+                                      const float* h0, void* o, float* h_final, cudaStream_t stream) {
+  Dims d;
+  kda_status s = check_problem(p, &d);
+  if (s != KDA_OK) return s;
+  if (!q || !k || !v || !f || !b || !A_log || !dt_bias || !o) return KDA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, f, b, A_log, dt_bias, o};
+  for (const void* x : ptrs)
+    if (!aligned(x, 16)) return KDA_ERR_ALIGNMENT;
+  if ((h0 && !aligned(h0, 16)) || (h_final && !aligned(h_final, 16))) return KDA_ERR_ALIGNMENT;
+  Layout L = layout(d, 0);
+  if (L.total > KDA_NOALLOC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;  // beyond the fixed array
+  void* scratch = nullptr;
+  s = noalloc_scratch(&scratch);
+  if (s != KDA_OK) return s;
+  Ws w = bind(scratch, L, d, 0);
+  d.save = 0;
+  FwdIO io{q, k, v, f, b, A_log, dt_bias, h0, o, h_final, 0};
+  cudaError_t e = launch_chunk_table(p->cu_seqlens, d, w, stream);
+  if (e == cudaSuccess) e = launch_fwd_intra(p->dtype, d, io, w, stream);
+  if (e == cudaSuccess) e = launch_fwd_scan(p->dtype, d, io, w, stream);
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
