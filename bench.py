@@ -50,11 +50,14 @@ def algorithmic_bytes(w, kernel: str) -> float:
     th = w.B * w.T * w.H  # token-heads
     dk, dv = w.dk, w.dv
     inputs_fwd = e * (3 * dk + dv + 1)         # q, k, f, v, b
+    grads = e * (3 * dk + dv + 1)               # dq, dk, df, dv, db
     per = {
+        "fwd_chain": inputs_fwd + e * dv,       # reads q, k, f, v, b; writes o
         "fwd_intra": inputs_fwd,
         "fwd_scan": e * dv,                     # o
         "bwd_scan": e * dv,                     # dO
-        "bwd_intra": inputs_fwd + e * dv + e * (3 * dk + dv + 1),  # + dO, writes dq, dk, df, dv, db
+        "bwd_chunk": inputs_fwd + e * dv + grads,  # reads q, k, f, v, b, dO; writes the gradients
+        "bwd_intra": inputs_fwd + e * dv + grads,
     }
     return float(per.get(kernel, 0)) * th
 

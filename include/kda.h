@@ -148,9 +148,11 @@ KDA_API const char* kda_prof_kernel_name(int i);
  * The array is KDA_NOALLOC_SCRATCH_BYTES (32 MiB) of device memory, reserved
  * on every GPU that loads this library for as long as the process lives.  A
  * problem whose forward scratch (kda_workspace_size(p, 0)) exceeds it is
- * rejected with KDA_ERR_WORKSPACE before anything is launched; roughly, at
- * dk=32/dv=64 it holds about 600 chunk-heads (e.g. 8 heads x 4800 tokens).
- * Nothing is saved for kda_bwd.
+ * rejected with KDA_ERR_WORKSPACE before anything is launched.  With bf16 io
+ * at dk=32/dv=64 the forward only needs its chunk table (about 12 bytes per
+ * 64 tokens), so any realistic problem fits; the other shapes keep fp32
+ * intra-chunk factors (about 56 KB per chunk and head at dk=32/dv=64 fp32,
+ * i.e. roughly 600 chunk-heads).  Nothing is saved for kda_bwd.
  *
  * The first call on a device looks up the array's device address on that
  * device (the device must be current); make that first call before any

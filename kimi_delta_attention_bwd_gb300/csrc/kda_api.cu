@@ -125,12 +125,17 @@ static size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 struct Layout {
   size_t total;
   size_t off_err, off_nch, off_dc0, off_ct0, off_cl, off_cd;
-  size_t off_W, off_U, off_P, off_QG, off_KD, off_gam, off_Sent;
+  size_t off_W, off_U, off_P, off_QG, off_KD, off_gam, off_Sent, off_M, off_QW;
   size_t off_dE, off_dSn, off_pA, off_pdt, off_scr;
 };
 
+// Workspace layout.  Both paths start with the error word, the saved-problem
+// tag and the chunk table.  The tensor-core path (d.fast) keeps only the
+// per-chunk entry states, M and QW for the backward, and the backward's
+// state gradients and parameter-gradient partials; the general path also
+// keeps its fp32 intra-chunk factors and scratch.
 static Layout layout(const Dims& d, int for_bwd) {
-  Layout L;
+  Layout L = {};
   size_t o = 0;
   const size_t nch = (size_t)d.nc_max * d.H;
   auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes); return r; };
@@ -140,6 +145,18 @@ static Layout layout(const Dims& d, int for_bwd) {
   L.off_ct0 = take(4 * (size_t)d.nc_max);
   L.off_cl = take(4 * (size_t)d.nc_max);
   L.off_cd = take(4 * (size_t)d.nc_max);
+  if (d.fast) {
+    if (for_bwd) {
+      L.off_Sent = take(4 * nch * d.dk * d.dv);
+      L.off_M = take(4 * nch * d.dk * d.dk);
+      L.off_QW = take(4 * nch * C * d.dk);
+      L.off_dSn = take(4 * nch * d.dk * d.dv);
+      L.off_pA = take(4 * nch);
+      L.off_pdt = take(4 * nch * d.dk);
+    }
+    L.total = o;
+    return L;
+  }
   L.off_W = take(4 * nch * C * d.dk);
   L.off_U = take(4 * nch * C * d.dv);
   L.off_P = take(4 * nch * C * C);
@@ -153,8 +170,6 @@ static Layout layout(const Dims& d, int for_bwd) {
     L.off_pA = take(4 * nch);
     L.off_pdt = take(4 * nch * d.dk);
     L.off_scr = take(4 * nch * (size_t)bwd_scratch_floats(d.dk, d.dv));
-  } else {
-    L.off_Sent = L.off_dE = L.off_dSn = L.off_pA = L.off_pdt = L.off_scr = 0;
   }
   L.total = o;
   return L;
@@ -162,6 +177,7 @@ static Layout layout(const Dims& d, int for_bwd) {
 
 static Ws bind(void* ws, const Layout& L, const Dims& d, int for_bwd) {
   char* p = (char*)ws;
+  auto at = [&](size_t off) { return off ? (float*)(p + off) : nullptr; };
   Ws w;
   w.err = (int32_t*)(p + L.off_err);
   w.tag = (int32_t*)(p + L.off_err + 4);
@@ -170,20 +186,32 @@ static Ws bind(void* ws, const Layout& L, const Dims& d, int for_bwd) {
   w.chunk_tok0 = (int32_t*)(p + L.off_ct0);
   w.chunk_len = (int32_t*)(p + L.off_cl);
   w.chunk_doc = (int32_t*)(p + L.off_cd);
-  w.W = (float*)(p + L.off_W);
-  w.U = (float*)(p + L.off_U);
-  w.P = (float*)(p + L.off_P);
-  w.QG = (float*)(p + L.off_QG);
-  w.KD = (float*)(p + L.off_KD);
-  w.gam = (float*)(p + L.off_gam);
-  w.Sent = for_bwd ? (float*)(p + L.off_Sent) : nullptr;
-  w.dE = for_bwd ? (float*)(p + L.off_dE) : nullptr;
-  w.dSn = for_bwd ? (float*)(p + L.off_dSn) : nullptr;
-  w.pA = for_bwd ? (float*)(p + L.off_pA) : nullptr;
-  w.pdt = for_bwd ? (float*)(p + L.off_pdt) : nullptr;
-  w.scr = for_bwd ? (float*)(p + L.off_scr) : nullptr;
+  w.W = at(L.off_W);
+  w.U = at(L.off_U);
+  w.P = at(L.off_P);
+  w.QG = at(L.off_QG);
+  w.KD = at(L.off_KD);
+  w.gam = at(L.off_gam);
+  w.Sent = for_bwd ? at(L.off_Sent) : nullptr;
+  w.M = for_bwd ? at(L.off_M) : nullptr;
+  w.QW = for_bwd ? at(L.off_QW) : nullptr;
+  w.dE = for_bwd ? at(L.off_dE) : nullptr;
+  w.dSn = for_bwd ? at(L.off_dSn) : nullptr;
+  w.pA = for_bwd ? at(L.off_pA) : nullptr;
+  w.pdt = for_bwd ? at(L.off_pdt) : nullptr;
+  w.scr = for_bwd ? at(L.off_scr) : nullptr;
   w.scr_per_ch = bwd_scratch_floats(d.dk, d.dv);
   return w;
+}
+
+// The forward launch sequence shared by kda_fwd and kda_fwd_noalloc.
+static cudaError_t run_forward(const kda_problem* p, Dims d, const FwdIO& io, const Ws& w, cudaStream_t stream) {
+  cudaError_t e = launch_chunk_table(p->cu_seqlens, d, w, stream);
+  if (e != cudaSuccess) return e;
+  if (d.fast) return launch_fast_fwd(d, io, w, stream);
+  e = launch_fwd_intra(p->dtype, d, io, w, stream);
+  if (e == cudaSuccess) e = launch_fwd_scan(p->dtype, d, io, w, stream);
+  return e;
 }
 
 static bool supported(int dk, int dv) {
@@ -233,6 +261,7 @@ static kda_status check_problem(const kda_problem* p, Dims* d) {
   for (int i = 0; i < 8; i++) { hsh ^= (uint32_t)vals[i]; hsh *= 16777619u; }
   d->tag = (int32_t)(hsh | 1u);
   d->save = 0;
+  d->fast = fast_path(p->dtype, p->dk, p->dv) ? 1 : 0;
   return KDA_OK;
 }
 
@@ -270,10 +299,7 @@ kda_status kda_fwd(const kda_problem* p, const void* q, const void* k, const voi
   Ws w = bind(workspace, L, d, fb);
   d.save = fb;
   FwdIO io{q, k, v, f, b, A_log, dt_bias, h0, o, h_final, fb};
-  cudaError_t e = launch_chunk_table(p->cu_seqlens, d, w, stream);
-  if (e == cudaSuccess) e = launch_fwd_intra(p->dtype, d, io, w, stream);
-  if (e == cudaSuccess) e = launch_fwd_scan(p->dtype, d, io, w, stream);
-  return status_of(e);
+  return status_of(run_forward(p, d, io, w, stream));
 }
 
 kda_status kda_bwd(const kda_problem* p, const void* q, const void* k, const void* v, const void* f,
@@ -298,6 +324,7 @@ kda_status kda_bwd(const kda_problem* p, const void* q, const void* k, const voi
   if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
   Ws w = bind(workspace, L, d, 1);
   BwdIO io{q, k, v, f, b, A_log, dt_bias, dO, dh_final, dq, dk, dv, df, db, dA_log, ddt_bias, dh0};
+  if (d.fast) return status_of(launch_fast_bwd(d, io, w, stream));
   cudaError_t e = launch_bwd_scan(p->dtype, d, io, w, stream);
   if (e == cudaSuccess) e = launch_bwd_intra(p->dtype, d, io, w, stream);
   if (e == cudaSuccess) e = launch_bwd_reduce(d, io, w, stream);
@@ -326,8 +353,8 @@ const char* kda_strerror(kda_status s) {
   return "unknown status";
 }
 
-static const char* const k_names[K_COUNT] = {"chunk_table", "fwd_intra", "fwd_scan",
-                                             "bwd_scan", "bwd_intra", "bwd_reduce"};
+static const char* const k_names[K_COUNT] = {"chunk_table", "fwd_intra", "fwd_scan", "bwd_scan",
+                                             "bwd_intra", "bwd_reduce", "fwd_chain", "bwd_chunk"};
 
 const char* kda_prof_kernel_name(int i) { return (i >= 0 && i < K_COUNT) ? k_names[i] : nullptr; }
 
@@ -408,8 +435,5 @@ extern "C" kda_status kda_fwd_noalloc(const kda_problem* p, const void* q, const
   Ws w = bind(scratch, L, d, 0);
   d.save = 0;
   FwdIO io{q, k, v, f, b, A_log, dt_bias, h0, o, h_final, 0};
-  cudaError_t e = launch_chunk_table(p->cu_seqlens, d, w, stream);
-  if (e == cudaSuccess) e = launch_fwd_intra(p->dtype, d, io, w, stream);
-  if (e == cudaSuccess) e = launch_fwd_scan(p->dtype, d, io, w, stream);
-  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+  return run_forward(p, d, io, w, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

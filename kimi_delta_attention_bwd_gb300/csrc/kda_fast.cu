@@ -1,0 +1,864 @@
+// Tensor-core path for the 300M-layer head shape (dk = 32, dv = 64, bf16 io).
+//
+// Forward: one CTA per (document, head) walks the document's 64-token chunks
+// with the fp32 state S (dk x dv) in shared memory, so q, k, v, f, b are read
+// once and o written once.  Per chunk (G = in-chunk cumulative log-decay):
+//   A  = strict_lower(diag(beta) (K^ K^T with ratios exp(G_r - G_s)))
+//   P  = inclusive_lower(Q^ K^T with the same ratios)
+//   T  = (I + A)^-1,  W = T diag(beta) (K^ exp G),  U = T diag(beta) V
+//   E  = U - W S,  O = scale (Q^ exp G) S + scale P E
+//   S <- Diag(exp G_last) S + (K^ exp(G_last - G))^T E
+// The ratios never appear as exp of a positive number: rows and columns are
+// split in 16-token sub-blocks; an off-diagonal block (I > J) is
+//   (X_I exp(G - G_first(I))) diag(exp(G_first(I) - G_last(J))) (K_J exp(G_last(J) - G))^T
+// with every factor <= 1, and a diagonal block uses the same row factor with
+// the column factor exp(G_first(I) - G) <= exp(80) when the block's decay
+// span is at most 80 nats, else an exact pairwise evaluation.  The products
+// run as mma.sync m16n8k8 with fp32 accumulation and every operand split into
+// a tf32 head and a tf32 remainder (three products, ~21 significant bits):
+// with single tf32 operands the gate gradient df misses max|err|/rms <= 1e-2
+// (0.18 measured at the 300M shape), with the split it is 2.6e-4.
+//
+// Backward: a reverse scan over each document's chunks carries dS with
+//   dS_in = M^T dS_out + QW^T dO,  M = Diag(exp G_last) - KD^T W,  QW = QG - P W
+// (M and QW per chunk are saved by the forward), then one CTA per chunk
+// recomputes the chunk and forms every local gradient on chip.
+#include "kda_internal.cuh"
+#include "kda_mma.cuh"
+
+namespace kda {
+namespace fast {
+using namespace mma;
+typedef __nv_bfloat16 bf16;
+
+constexpr int DK = 32, DV = 64;
+constexpr int SQ = DK + 4;  // row stride of [C][DK] operands read along rows
+constexpr int SX = DK + 8;  // row stride of [C][DK] operands read along columns
+constexpr int SV = DV + 8;  // row stride of [C][DV] operands
+constexpr int SC = C + 4;   // row stride of [C][C] matrices
+constexpr int NTH = 256, NW = 8;
+constexpr float SPAN_MAX = 80.f;
+#ifndef KDA_SPLIT_BWD
+#define KDA_SPLIT_BWD 1
+#endif
+#ifndef KDA_SPLIT_RECOMP
+#define KDA_SPLIT_RECOMP 1
+#endif
+constexpr bool SB = KDA_SPLIT_BWD != 0;     // backward gradient products
+constexpr bool SR = KDA_SPLIT_RECOMP != 0;  // backward recomputation of the chunk
+#ifndef KDA_SPLIT_FWD
+#define KDA_SPLIT_FWD 1
+#endif
+constexpr bool SF = KDA_SPLIT_FWD != 0;     // forward chain products
+
+__device__ __forceinline__ int pidx(int I, int J) { return I * (I - 1) / 2 + J; }
+__device__ __forceinline__ float bfl(bf16 x) { return __bfloat162float(x); }
+
+// Arrays of the intra-chunk recomputation shared by the forward and backward.
+struct Intra {
+  float *qh, *kh, *gg;     // [C][SQ]  q^, k^, G
+  float *lq, *lk, *rr;     // [C][SQ]  q^ e^{G-Gb}, k^ e^{G-Gb}, k^ e^{Ge-G}
+  float *kd, *xk;          // [C][SX]  k^ e^{Gl-G}, beta k^ e^{G}
+  float* xv;               // [C][SV]  beta v
+  float* qg;               // [C][SQ]  scale q^ e^{G} (forward only)
+  float *bet, *inq, *ink, *braw;  // [C]
+  float *gl, *gam;         // [DK]
+  float *gb, *ge, *dd, *ei;  // [4][DK], [4][DK], [6][DK], [4][DK]
+  float* tot;              // [NW][DK]
+  int* spanok;             // [4]
+};
+
+// Stage layout of one chunk's raw inputs: q, k, f [C][DK], v [C][DV] (bf16).
+constexpr int STAGE_ELEMS = 3 * C * DK + C * DV;
+
+__device__ __forceinline__ void stage_chunk(bf16* st, const FwdIO& io, int H, int h, int t0, int L) {
+  const bf16* q = (const bf16*)io.q;
+  const bf16* k = (const bf16*)io.k;
+  const bf16* f = (const bf16*)io.f;
+  const bf16* v = (const bf16*)io.v;
+  for (int idx = threadIdx.x; idx < C * 4; idx += NTH) {  // 4 x 16 B per dk row
+    int r = idx >> 2, p = idx & 3;
+    if (r < L) {
+      size_t g = ((size_t)(t0 + r) * H + h) * DK + p * 8;
+      cp16(st + r * DK + p * 8, q + g);
+      cp16(st + C * DK + r * DK + p * 8, k + g);
+      cp16(st + 2 * C * DK + r * DK + p * 8, f + g);
+    }
+  }
+  for (int idx = threadIdx.x; idx < C * 8; idx += NTH) {  // 8 x 16 B per dv row
+    int r = idx >> 3, p = idx & 7;
+    if (r < L) cp16(st + 3 * C * DK + r * DV + p * 8, v + ((size_t)(t0 + r) * H + h) * DV + p * 8);
+  }
+  cp_commit();
+}
+
+// q^, k^ (L2-normalised), G (in-chunk inclusive cumulative log-decay), beta,
+// raw v (into xv).  Rows >= L are zero (G continues flat).
+__device__ void prologue(const Intra& c, const bf16* st, int L, float a, const float* dtb) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int idx = tid; idx < C * DK; idx += NTH) {
+    int r = idx / DK, i = idx % DK;
+    float qv = 0.f, kv = 0.f, gv = 0.f;
+    if (r < L) {
+      qv = bfl(st[idx]);
+      kv = bfl(st[C * DK + idx]);
+      gv = -a * softplus_f(bfl(st[2 * C * DK + idx]) + dtb[i]);
+    }
+    c.qh[r * SQ + i] = qv;
+    c.kh[r * SQ + i] = kv;
+    c.gg[r * SQ + i] = gv;
+  }
+  for (int idx = tid; idx < C * DV; idx += NTH) {
+    int r = idx / DV, j = idx % DV;
+    c.xv[r * SV + j] = r < L ? bfl(st[3 * C * DK + idx]) : 0.f;
+  }
+  if (tid < C) c.bet[tid] = tid < L ? sigmoid_f(c.braw[tid]) : 0.f;
+  __syncthreads();
+  for (int r = warp; r < C; r += NW) {  // one warp per row, lane = key channel
+    float q = c.qh[r * SQ + lane], k = c.kh[r * SQ + lane];
+    float iq = 1.0f / sqrtf(warp_sum(q * q) + L2_EPS), ik = 1.0f / sqrtf(warp_sum(k * k) + L2_EPS);
+    c.qh[r * SQ + lane] = q * iq;
+    c.kh[r * SQ + lane] = k * ik;
+    if (lane == 0) { c.inq[r] = iq; c.ink[r] = ik; }
+  }
+  {  // cumulative sum over rows: warp w scans rows 8w..8w+7 of channel `lane`
+    float run = 0.f;
+#pragma unroll
+    for (int m = 0; m < 8; m++) {
+      run += c.gg[(8 * warp + m) * SQ + lane];
+      c.gg[(8 * warp + m) * SQ + lane] = run;
+    }
+    c.tot[warp * DK + lane] = run;
+  }
+  __syncthreads();
+  {
+    float off = 0.f;
+    for (int w2 = 0; w2 < warp; w2++) off += c.tot[w2 * DK + lane];
+#pragma unroll
+    for (int m = 0; m < 8; m++) c.gg[(8 * warp + m) * SQ + lane] += off;
+  }
+  __syncthreads();
+}
+
+// Sub-block references, span guards, and the factor arrays.
+__device__ void factors(const Intra& c, int L, float scale) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp < 4) {
+    const int I = warp;
+    float b = c.gg[(16 * I) * SQ + lane], e = c.gg[(16 * I + 15) * SQ + lane];
+    float span = b - e;
+    bool ok = span <= SPAN_MAX;
+    c.gb[I * DK + lane] = b;
+    c.ge[I * DK + lane] = e;
+    c.ei[I * DK + lane] = expf(fminf(span, SPAN_MAX));
+    unsigned all = __all_sync(0xffffffffu, ok);
+    if (lane == 0) c.spanok[I] = all ? 1 : 0;
+  } else if (warp < 6) {  // 6 pairs I > J over two warps
+    for (int p = warp - 4; p < 6; p += 2) {
+      int I = p < 1 ? 1 : p < 3 ? 2 : 3, J = p - pidx(I, 0);
+      c.dd[p * DK + lane] = expf(c.gg[(16 * I) * SQ + lane] - c.gg[(16 * J + 15) * SQ + lane]);
+    }
+  } else if (warp == 6) {
+    float g = c.gg[(L - 1) * SQ + lane];
+    c.gl[lane] = g;
+    c.gam[lane] = expf(g);
+  }
+  __syncthreads();
+  for (int idx = tid; idx < C * DK; idx += NTH) {
+    int r = idx / DK, i = idx % DK, I = r >> 4;
+    float G = c.gg[r * SQ + i];
+    float eL = expf(G - c.gb[I * DK + i]), eR = expf(c.ge[I * DK + i] - G);
+    float Gm = expf(G), kdf = expf(c.gl[i] - G);
+    float q = c.qh[r * SQ + i], k = c.kh[r * SQ + i];
+    if (c.qg) c.qg[r * SQ + i] = scale * q * Gm;
+    c.kd[r * SX + i] = k * kdf;
+    c.xk[r * SX + i] = c.bet[r] * k * Gm;
+    c.rr[r * SQ + i] = k * eR;
+    c.lq[r * SQ + i] = q * eL;
+    c.lk[r * SQ + i] = k * eL;
+  }
+  for (int idx = tid; idx < C * DV; idx += NTH) {
+    int r = idx / DV, j = idx % DV;
+    c.xv[r * SV + j] *= c.bet[r];
+  }
+  __syncthreads();
+}
+
+// Exact pairwise value sum_i x_ri k_si exp(G_ri - G_si) from the raw inputs
+// (the diagonal-block fallback when the in-block decay span exceeds 80).
+__device__ __forceinline__ float pair_exact(const bf16* X, float ix, const bf16* Kr, float ik, const float* Gr,
+                                            const float* Gs) {
+  float acc = 0.f;
+  for (int i = 0; i < DK; i++) acc += (bfl(X[i]) * ix) * (bfl(Kr[i]) * ik) * expf(Gr[i] - Gs[i]);
+  return acc;
+}
+
+// A (strict lower) and P (inclusive lower).  am gets beta_r A' (BETA) or A';
+// pm gets pscale * P'.  Upper blocks are never read and are left untouched.
+template <bool BETA, bool SPL = false>
+__device__ void ap(const Intra& c, float* am, float* pm, float pscale, const bf16* qraw, const bf16* kraw, int H,
+                   int h, int t0, int L) {
+  const int warp = threadIdx.x >> 5;
+  for (int task = warp; task < 20; task += NW) {
+    const int blk = task >> 1, isP = task & 1;
+    const int I = blk < 1 ? 0 : blk < 3 ? 1 : blk < 6 ? 2 : 3;
+    const int J = blk - I * (I + 1) / 2;
+    float acc[2][4];
+    zero(acc);
+    const float* X = isP ? c.lq : c.lk;
+    if (J < I || c.spanok[I]) {
+      const float* scl = J < I ? c.dd + pidx(I, J) * DK : c.ei + I * DK;
+      rows16<2, SPL>(acc, DK / 8, [&](int m, int k) { return X[(16 * I + m) * SQ + k]; },
+                [&](int k, int j, int n) { return c.rr[(16 * J + 8 * j + n) * SQ + k] * scl[k]; });
+    } else {
+      each(acc, [&](int m, int n, float& v) {
+        int r = 16 * I + m, s = 16 * I + n;
+        if (s <= r && r < L) {  // rows past the chunk end are not read
+          const bf16* xr = (isP ? qraw : kraw) + ((size_t)(t0 + r) * H + h) * DK;
+          const bf16* ks = kraw + ((size_t)(t0 + s) * H + h) * DK;
+          v = pair_exact(xr, isP ? c.inq[r] : c.ink[r], ks, c.ink[s], c.gg + r * SQ, c.gg + s * SQ);
+        }
+      });
+    }
+    each(acc, [&](int m, int n, float& v) {
+      int r = 16 * I + m, s = 16 * J + n;
+      if (isP) pm[r * SC + s] = s <= r ? pscale * v : 0.f;
+      else am[r * SC + s] = s < r ? (BETA ? c.bet[r] * v : v) : 0.f;
+    });
+  }
+  __syncthreads();
+}
+
+// T = (I + A)^-1 for unit-lower A (A = beta_r am_rs when !BETA).  fp32 SIMT:
+// diagonal 16x16 blocks by forward substitution, then block rows.
+template <bool BETA>
+__device__ void solve(const float* am, float* tm, float* yy, const float* bet) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  auto A = [&](int r, int s) { return BETA ? am[r * SC + s] : bet[r] * am[r * SC + s]; };
+  if (warp < 4) {
+    const int I = warp, cidx = lane & 15;
+    float tc[16];
+#pragma unroll
+    for (int r = 0; r < 16; r++) {
+      float v = (r == cidx) ? 1.f : 0.f;
+#pragma unroll
+      for (int s = 0; s < r; s++) v = fmaf(-A(16 * I + r, 16 * I + s), tc[s], v);
+      tc[r] = v;
+    }
+    if (lane < 16)
+#pragma unroll
+      for (int r = 0; r < 16; r++) tm[(16 * I + r) * SC + 16 * I + cidx] = tc[r];
+  }
+  __syncthreads();
+  for (int I = 1; I < 4; I++) {
+    const int ncol = 16 * I;
+    for (int idx = tid; idx < 16 * ncol; idx += NTH) {  // Y = sum_{K=J}^{I-1} A_IK T_KJ
+      int m = idx / ncol, cc = idx % ncol, J = cc >> 4;
+      float acc = 0.f;
+      for (int s = 16 * J; s < 16 * I; s++) acc = fmaf(A(16 * I + m, s), tm[s * SC + cc], acc);
+      yy[m * C + cc] = acc;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < 16 * ncol; idx += NTH) {  // T_IJ = -T_II Y
+      int m = idx / ncol, cc = idx % ncol;
+      float acc = 0.f;
+      for (int k = 0; k <= m; k++) acc = fmaf(tm[(16 * I + m) * SC + 16 * I + k], yy[k * C + cc], acc);
+      tm[(16 * I + m) * SC + cc] = -acc;
+    }
+    __syncthreads();
+  }
+}
+
+// W = T xk (into ww, stride SQ) and U = T xv (into uu, stride SV).
+template <bool SPL = false>
+__device__ void wu(const Intra& c, const float* tm, float* ww, float* uu) {
+  const int warp = threadIdx.x >> 5;
+  const int I = warp & 3, half = warp >> 2;
+  float acc[6][4];
+  zero(acc);
+  rows16<6, SPL>(acc, 2 * (I + 1), [&](int m, int k) { return tm[(16 * I + m) * SC + k]; },
+            [&](int k, int j, int n) {
+              int jj = 6 * half + j;
+              return jj < 4 ? c.xk[k * SX + 8 * jj + n] : c.xv[k * SV + 8 * (jj - 4) + n];
+            });
+  each(acc, [&](int m, int col, float& v) {
+    int r = 16 * I + m, jj = 6 * half + (col >> 3), n = col & 7;
+    if (jj < 4) ww[r * SQ + 8 * jj + n] = v;
+    else uu[r * SV + 8 * (jj - 4) + n] = v;
+  });
+  __syncthreads();
+}
+
+// ------------------------------------------------------------------ forward
+struct FwdSm {
+  bf16 stage[STAGE_ELEMS];
+  float qh[C * SQ], kh[C * SQ], gg[C * SQ], rr[C * SQ], qg[C * SQ], ww[C * SQ];
+  float kd[C * SX], xk[C * SX];
+  float xv[C * SV], ue[C * SV];
+  float am[C * SC], tm[C * SC], pm[C * SC];
+  float ss[DK * SV];
+  float yy[16 * C];
+  float tot[NW * DK];
+  float bet[C], inq[C], ink[C], braw[C];
+  float gl[DK], gam[DK], gb[4 * DK], ge[4 * DK], dd[6 * DK], ei[4 * DK];
+  int spanok[4];
+};
+
+__global__ void __launch_bounds__(NTH, 1) fwd_chain_kernel(Dims d, FwdIO io, Ws w) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  FwdSm& sm = *reinterpret_cast<FwdSm*>(smraw);
+  const int doc = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+  if (*w.err != 0) return;
+  const int H = d.H;
+  const int cb = w.doc_chunk0[doc], ce = w.doc_chunk0[doc + 1];
+  const float a = expf(io.A_log[h]);
+  const float* dtb = io.dt_bias + h * DK;
+  const bf16* braw = (const bf16*)io.b;
+  Intra c{sm.qh, sm.kh, sm.gg, sm.qh, sm.kh, sm.rr, sm.kd, sm.xk, sm.xv, sm.qg, sm.bet, sm.inq, sm.ink,
+          sm.braw, sm.gl, sm.gam, sm.gb, sm.ge, sm.dd, sm.ei, sm.tot, sm.spanok};
+
+  for (int idx = tid; idx < DK * DV; idx += NTH) {
+    int i = idx / DV, j = idx % DV;
+    sm.ss[i * SV + j] = io.h0 ? io.h0[(((int64_t)doc * H + h) * DK + i) * DV + j] : 0.f;
+  }
+  float bnext = 0.f;
+  if (cb < ce) {
+    const int L0 = w.chunk_len[cb], t00 = w.chunk_tok0[cb];
+    stage_chunk(sm.stage, io, H, h, t00, L0);
+    if (tid < L0) bnext = bfl(braw[(size_t)(t00 + tid) * H + h]);
+  }
+  for (int ci = cb; ci < ce; ci++) {
+    const int L = w.chunk_len[ci], t0 = w.chunk_tok0[ci];
+    const int64_t ch = (int64_t)ci * H + h;
+    cp_wait_all();
+    if (tid < C) sm.braw[tid] = bnext;
+    __syncthreads();
+    prologue(c, sm.stage, L, a, dtb);
+    if (ci + 1 < ce) {  // stage the next chunk while this one computes
+      const int L1 = w.chunk_len[ci + 1], t01 = w.chunk_tok0[ci + 1];
+      stage_chunk(sm.stage, io, H, h, t01, L1);
+      bnext = tid < L1 ? bfl(braw[(size_t)(t01 + tid) * H + h]) : 0.f;
+    }
+    factors(c, L, d.scale);
+    ap<true, SF>(c, sm.am, sm.pm, d.scale, (const bf16*)io.q, (const bf16*)io.k, H, h, t0, L);
+    solve<true>(sm.am, sm.tm, sm.yy, sm.bet);
+    wu<SF>(c, sm.tm, sm.ww, sm.ue);
+    if (io.save)
+      for (int idx = tid; idx < DK * DV; idx += NTH) {
+        int i = idx / DV, j = idx % DV;
+        w.Sent[ch * DK * DV + idx] = sm.ss[i * SV + j];
+      }
+    {  // E = U - W S
+      const int I = warp & 3, half = warp >> 2;
+      float acc[4][4];
+      zero(acc);
+      rows16<4, SF>(acc, DK / 8, [&](int m, int k) { return sm.ww[(16 * I + m) * SQ + k]; },
+                [&](int k, int j, int n) { return sm.ss[k * SV + 32 * half + 8 * j + n]; });
+      each(acc, [&](int m, int col, float& v) { sm.ue[(16 * I + m) * SV + 32 * half + col] -= v; });
+    }
+    __syncthreads();
+    {  // O = QG S + P E  -> o
+      const int I = warp & 3, half = warp >> 2;
+      float acc[4][4];
+      zero(acc);
+      rows16<4, SF>(acc, DK / 8, [&](int m, int k) { return sm.qg[(16 * I + m) * SQ + k]; },
+                [&](int k, int j, int n) { return sm.ss[k * SV + 32 * half + 8 * j + n]; });
+      rows16<4, SF>(acc, 2 * (I + 1), [&](int m, int k) { return sm.pm[(16 * I + m) * SC + k]; },
+                [&](int k, int j, int n) { return sm.ue[k * SV + 32 * half + 8 * j + n]; });
+      bf16* o = (bf16*)io.o;
+      const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+      for (int j = 0; j < 4; j++)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+          int r = 16 * I + gq + 8 * hh;
+          if (r < L) {
+            int col = 32 * half + 8 * j + 2 * tq;
+            *reinterpret_cast<__nv_bfloat162*>(o + ((size_t)(t0 + r) * H + h) * DV + col) =
+                __floats2bfloat162_rn(acc[j][2 * hh], acc[j][2 * hh + 1]);
+          }
+        }
+    }
+    float snew[2][4];
+    const int mI = warp & 1, jq = warp >> 1;
+    {  // S' = gamma S + KD^T E (registers until every reader of S is done)
+      zero(snew);
+      rows16<2, SF>(snew, C / 8, [&](int m, int k) { return sm.kd[k * SX + 16 * mI + m]; },
+                [&](int k, int j, int n) { return sm.ue[k * SV + 16 * jq + 8 * j + n]; });
+      each(snew, [&](int m, int col, float& v) {
+        int i = 16 * mI + m;
+        v += sm.gam[i] * sm.ss[i * SV + 16 * jq + col];
+      });
+    }
+    if (io.save) {  // M = Diag(gamma) - KD^T W and QW = QG - P W for the backward scan
+      {
+        float acc[1][4];
+        zero(acc);
+        const int j = warp >> 1;
+        rows16<1, SF>(acc, C / 8, [&](int m, int k) { return sm.kd[k * SX + 16 * mI + m]; },
+                  [&](int k, int jj, int n) { return sm.ww[k * SQ + 8 * j + n]; });
+        each(acc, [&](int m, int col, float& v) {
+          int i = 16 * mI + m, jc = 8 * j + col;
+          w.M[ch * DK * DK + i * DK + jc] = (i == jc ? sm.gam[i] : 0.f) - v;
+        });
+      }
+      {
+        const int I = warp & 3, half = warp >> 2;
+        float acc[2][4];
+        zero(acc);
+        rows16<2, SF>(acc, 2 * (I + 1), [&](int m, int k) { return sm.pm[(16 * I + m) * SC + k]; },
+                  [&](int k, int j, int n) { return sm.ww[k * SQ + 16 * half + 8 * j + n]; });
+        each(acc, [&](int m, int col, float& v) {
+          int r = 16 * I + m, jc = 16 * half + col;
+          w.QW[ch * C * DK + r * DK + jc] = sm.qg[r * SQ + jc] - v;
+        });
+      }
+    }
+    __syncthreads();
+    each(snew, [&](int m, int col, float& v) { sm.ss[(16 * mI + m) * SV + 16 * jq + col] = v; });
+    __syncthreads();
+  }
+  if (io.h_final)
+    for (int idx = tid; idx < DK * DV; idx += NTH) {
+      int i = idx / DV, j = idx % DV;
+      io.h_final[(((int64_t)doc * H + h) * DK + i) * DV + j] = sm.ss[i * SV + j];
+    }
+}
+
+// ------------------------------------------------------------ backward scan
+constexpr int NS = 16;        // value columns per scan CTA
+constexpr int SS = NS + 8;    // row stride of [*][NS] operands
+
+__global__ void __launch_bounds__(128) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
+  __shared__ float Ms[DK * SQ];
+  __shared__ float QWs[C * SQ];
+  __shared__ float dOs[C * SS];
+  __shared__ float dS[DK * SS];
+  const int doc = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * NS, tid = threadIdx.x, warp = tid >> 5;
+  if (!saved_ok(d, w.tag, w.err)) return;
+  const int H = d.H;
+  const bf16* dO = (const bf16*)io.dO;
+  for (int idx = tid; idx < DK * NS; idx += 128) {
+    int i = idx / NS, j = idx % NS;
+    dS[i * SS + j] = io.dh_final ? io.dh_final[(((int64_t)doc * H + h) * DK + i) * DV + col0 + j] : 0.f;
+  }
+  const int cb = w.doc_chunk0[doc], ce = w.doc_chunk0[doc + 1];
+  __syncthreads();
+  const int mI = warp & 1, jn = warp >> 1;
+  for (int ci = ce - 1; ci >= cb; ci--) {
+    const int64_t ch = (int64_t)ci * H + h;
+    const int L = w.chunk_len[ci], t0 = w.chunk_tok0[ci];
+    for (int idx = tid; idx < DK * NS; idx += 128) {
+      int i = idx / NS, j = idx % NS;
+      w.dSn[ch * DK * DV + i * DV + col0 + j] = dS[i * SS + j];
+    }
+    for (int idx = tid; idx < DK * DK; idx += 128) Ms[(idx / DK) * SQ + idx % DK] = w.M[ch * DK * DK + idx];
+    for (int idx = tid; idx < C * DK; idx += 128) QWs[(idx / DK) * SQ + idx % DK] = w.QW[ch * C * DK + idx];
+    for (int idx = tid; idx < C * NS; idx += 128) {
+      int r = idx / NS, j = idx % NS;
+      dOs[r * SS + j] = r < L ? bfl(dO[((size_t)(t0 + r) * H + h) * DV + col0 + j]) : 0.f;
+    }
+    __syncthreads();
+    float acc[1][4];
+    zero(acc);
+    rows16<1, true>(acc, DK / 8, [&](int m, int k) { return Ms[k * SQ + 16 * mI + m]; },
+                    [&](int k, int j, int n) { return dS[k * SS + 8 * jn + n]; });
+    rows16<1, true>(acc, C / 8, [&](int m, int k) { return QWs[k * SQ + 16 * mI + m]; },
+                    [&](int k, int j, int n) { return dOs[k * SS + 8 * jn + n]; });
+    __syncthreads();
+    each(acc, [&](int m, int col, float& v) { dS[(16 * mI + m) * SS + 8 * jn + col] = v; });
+    __syncthreads();
+  }
+  if (io.dh0)
+    for (int idx = tid; idx < DK * NS; idx += 128) {
+      int i = idx / NS, j = idx % NS;
+      io.dh0[(((int64_t)doc * H + h) * DK + i) * DV + col0 + j] = dS[i * SS + j];
+    }
+}
+
+// ------------------------------------------------------------ backward chunk
+struct BwdSm {
+  float qh[C * SQ], kh[C * SQ], gg[C * SQ], lq[C * SQ], lk[C * SQ], rr[C * SQ], ww[C * SQ];
+  float kd[C * SX];
+  float uu[C * SV];
+  float am[C * SC], pm[C * SC], tm[C * SC];  // also the raw-input stage before ap()
+  float r1[C * SX + C * SV];                 // xk | xv, then dE (C*SV) | dW (C*SQ)
+  float ss[DK * SV], dsn[DK * SV];           // S, dS'; later YU [C][SV]
+  float e2[C * SV];                          // solve scratch, then E, then YW [C][SQ]
+  bf16 dOs[C * DV];
+  bf16 fr[C * DK];
+  float tot[NW * DK], part[NW * DK];
+  float bet[C], inq[C], ink[C], braw[C], dbet[C];
+  float gl[DK], gam[DK], dgam[DK], gb[4 * DK], ge[4 * DK], dd[6 * DK], ei[4 * DK];
+  float red[NW];
+  int spanok[4];
+};
+
+__global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws w) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  BwdSm& sm = *reinterpret_cast<BwdSm*>(smraw);
+  const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  if (!saved_ok(d, w.tag, w.err)) return;
+  if (j >= *w.n_chunks) return;
+  const int L = w.chunk_len[j];
+  if (L <= 0) return;
+  const int t0 = w.chunk_tok0[j], H = d.H;
+  const int64_t ch = (int64_t)j * H + h;
+  const float a = expf(io.A_log[h]), scale = d.scale;
+  const float* dtb = io.dt_bias + h * DK;
+  float* xk = sm.r1;
+  float* xv = sm.r1 + C * SX;
+  Intra c{sm.qh, sm.kh, sm.gg, sm.lq, sm.lk, sm.rr, sm.kd, xk, xv, nullptr, sm.bet, sm.inq, sm.ink,
+          sm.braw, sm.gl, sm.gam, sm.gb, sm.ge, sm.dd, sm.ei, sm.tot, sm.spanok};
+  bf16* st = reinterpret_cast<bf16*>(sm.am);
+
+  // ---- stage raw inputs, dO, S and dS'
+  {
+    FwdIO fio{io.q, io.k, io.v, io.f, io.b, io.A_log, io.dt_bias, nullptr, nullptr, nullptr, 0};
+    stage_chunk(st, fio, H, h, t0, L);
+    const bf16* dO = (const bf16*)io.dO;
+    for (int idx = tid; idx < C * 8; idx += NTH) {
+      int r = idx >> 3, p = idx & 7;
+      if (r < L) cp16(sm.dOs + r * DV + p * 8, dO + ((size_t)(t0 + r) * H + h) * DV + p * 8);
+    }
+    const float* Sg = w.Sent + ch * DK * DV;
+    const float* dSg = w.dSn + ch * DK * DV;
+    for (int idx = tid; idx < DK * 16; idx += NTH) {  // 16 x 16 B per fp32 row of dv = 64
+      int i = idx >> 4, p = idx & 15;
+      cp16(sm.ss + i * SV + p * 4, Sg + i * DV + p * 4);
+      cp16(sm.dsn + i * SV + p * 4, dSg + i * DV + p * 4);
+    }
+    cp_commit();
+    if (tid < C) sm.braw[tid] = tid < L ? bfl(((const bf16*)io.b)[(size_t)(t0 + tid) * H + h]) : 0.f;
+    if (tid < C) sm.dbet[tid] = 0.f;
+    for (int idx = tid; idx < C * DV; idx += NTH)
+      if (idx / DV >= L) sm.dOs[idx] = __float2bfloat16_rn(0.f);
+    cp_wait_all();
+    __syncthreads();
+    for (int idx = tid; idx < C * DK; idx += NTH) sm.fr[idx] = st[2 * C * DK + idx];
+  }
+  // ---- recompute the chunk (same arithmetic as the forward)
+  prologue(c, st, L, a, dtb);
+  factors(c, L, scale);
+  ap<false, SR>(c, sm.am, sm.pm, 1.f, (const bf16*)io.q, (const bf16*)io.k, H, h, t0, L);
+  solve<false>(sm.am, sm.tm, sm.e2, sm.bet);
+  wu<SR>(c, sm.tm, sm.ww, sm.uu);
+
+  float* dE = sm.r1;            // [C][SV]
+  float* dW = sm.r1 + C * SV;   // [C][SQ]
+  float* E = sm.e2;             // [C][SV]
+  float* YU = sm.ss;            // [C][SV] over ss | dsn
+  float* YW = sm.e2;            // [C][SQ]
+  auto dO = [&](int r, int col) { return bfl(sm.dOs[r * DV + col]); };
+  const int I = warp & 3, hk = warp >> 2;  // owner tile: rows 16I.., key columns 16hk..
+
+  // ---- dE = scale P'^T dO + KD dS'  and  E = U - W S
+  {
+    float acc[4][4], acc2[4][4];
+    zero(acc);
+    zero(acc2);
+    const int half = warp >> 2;
+    rows16<4, SB>(acc, 2 * (4 - I), [&](int m, int k) { return sm.pm[(16 * I + k) * SC + 16 * I + m]; },
+              [&](int k, int jj, int n) { return dO(16 * I + k, 32 * half + 8 * jj + n); });
+    rows16<4, SB>(acc2, DK / 8, [&](int m, int k) { return sm.kd[(16 * I + m) * SX + k]; },
+              [&](int k, int jj, int n) { return sm.dsn[k * SV + 32 * half + 8 * jj + n]; });
+    each(acc, [&](int m, int col, float& v) { v = scale * v; });
+    float accE[4][4];
+    zero(accE);
+    rows16<4, SB>(accE, DK / 8, [&](int m, int k) { return sm.ww[(16 * I + m) * SQ + k]; },
+              [&](int k, int jj, int n) { return sm.ss[k * SV + 32 * half + 8 * jj + n]; });
+#pragma unroll
+    for (int jj = 0; jj < 4; jj++)
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        int r = 16 * I + gq + 8 * (e >> 1), col = 32 * half + 8 * jj + 2 * tq + (e & 1);
+        dE[r * SV + col] = acc[jj][e] + acc2[jj][e];
+        E[r * SV + col] = sm.uu[r * SV + col] - accE[jj][e];
+      }
+  }
+  __syncthreads();
+  // ---- dP' = scale dO E^T (inclusive lower, into pm), dKD = E dS'^T, dQG = scale dO S^T (registers),
+  //      dgamma = rowsum(dS' .* S), dW = -dE S^T
+  float dKD[2][4], dQG[2][4];
+  {
+    zero(dKD);
+    zero(dQG);
+    rows16<2, SB>(dKD, DV / 8, [&](int m, int k) { return E[(16 * I + m) * SV + k]; },
+              [&](int k, int jj, int n) { return sm.dsn[(16 * hk + 8 * jj + n) * SV + k]; });
+    rows16<2, SB>(dQG, DV / 8, [&](int m, int k) { return dO(16 * I + m, k); },
+              [&](int k, int jj, int n) { return sm.ss[(16 * hk + 8 * jj + n) * SV + k]; });
+    each(dQG, [&](int m, int col, float& v) { v *= scale; });
+    float acc[2][4];
+    zero(acc);
+    rows16<2, SB>(acc, DV / 8, [&](int m, int k) { return dE[(16 * I + m) * SV + k]; },
+              [&](int k, int jj, int n) { return sm.ss[(16 * hk + 8 * jj + n) * SV + k]; });
+    each(acc, [&](int m, int col, float& v) { dW[(16 * I + m) * SQ + 16 * hk + col] = -v; });
+    for (int t = warp; t < 10; t += NW) {  // lower 16x16 blocks of dP'
+      const int bI = t < 1 ? 0 : t < 3 ? 1 : t < 6 ? 2 : 3, bJ = t - bI * (bI + 1) / 2;
+      float pp[2][4];
+      zero(pp);
+      rows16<2, SB>(pp, DV / 8, [&](int m, int k) { return dO(16 * bI + m, k); },
+                [&](int k, int jj, int n) { return E[(16 * bJ + 8 * jj + n) * SV + k]; });
+      each(pp, [&](int m, int n, float& v) {
+        int r = 16 * bI + m, s = 16 * bJ + n;
+        sm.pm[r * SC + s] = s <= r ? scale * v : 0.f;
+      });
+    }
+    if (tid < DK) {
+      float acc1 = 0.f;
+      for (int jj = 0; jj < DV; jj++) acc1 += sm.dsn[tid * SV + jj] * sm.ss[tid * SV + jj];
+      sm.dgam[tid] = acc1;
+    }
+  }
+  __syncthreads();
+  // ---- YU = T^T dE (registers), YW = T^T dW (registers)
+  float yu[4][4], yw[2][4];
+  {
+    const int half = warp >> 2;
+    zero(yu);
+    zero(yw);
+    auto Tt = [&](int m, int k) { return sm.tm[(16 * I + k) * SC + 16 * I + m]; };  // rows r >= 16 I
+    rows16<4, SB>(yu, 2 * (4 - I), Tt, [&](int k, int jj, int n) { return dE[(16 * I + k) * SV + 32 * half + 8 * jj + n]; });
+    rows16<2, SB>(yw, 2 * (4 - I), Tt, [&](int k, int jj, int n) { return dW[(16 * I + k) * SQ + 16 * hk + 8 * jj + n]; });
+  }
+  __syncthreads();
+  {  // store YU, YW; dv = beta YU
+    const int half = warp >> 2;
+    bf16* dvo = (bf16*)io.dv;
+#pragma unroll
+    for (int jj = 0; jj < 4; jj++)
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++) {
+        int r = 16 * I + gq + 8 * hh, col = 32 * half + 8 * jj + 2 * tq;
+        YU[r * SV + col] = yu[jj][2 * hh];
+        YU[r * SV + col + 1] = yu[jj][2 * hh + 1];
+        if (r < L)
+          *reinterpret_cast<__nv_bfloat162*>(dvo + ((size_t)(t0 + r) * H + h) * DV + col) =
+              __floats2bfloat162_rn(sm.bet[r] * yu[jj][2 * hh], sm.bet[r] * yu[jj][2 * hh + 1]);
+      }
+    each(yw, [&](int m, int col, float& v) { YW[(16 * I + m) * SQ + 16 * hk + col] = v; });
+  }
+  __syncthreads();
+  // ---- dbeta (U and W terms), dA = -(YU U^T + YW W^T) strict lower (into tm)
+  {
+    const bf16* vg = (const bf16*)io.v;
+    for (int r = warp; r < L; r += NW) {
+      float acc = 0.f;
+      const bf16* vr = vg + ((size_t)(t0 + r) * H + h) * DV;
+      for (int jj = lane; jj < DV; jj += 32) acc += YU[r * SV + jj] * bfl(vr[jj]);
+      acc += YW[r * SQ + lane] * sm.kh[r * SQ + lane] * expf(sm.gg[r * SQ + lane]);
+      acc = warp_sum(acc);
+      if (lane == 0) sm.dbet[r] += acc;
+    }
+    for (int t = warp; t < 10; t += NW) {
+      const int bI = t < 1 ? 0 : t < 3 ? 1 : t < 6 ? 2 : 3, bJ = t - bI * (bI + 1) / 2;
+      float aa[2][4];
+      zero(aa);
+      rows16<2, SB>(aa, DV / 8, [&](int m, int k) { return YU[(16 * bI + m) * SV + k]; },
+                [&](int k, int jj, int n) { return sm.uu[(16 * bJ + 8 * jj + n) * SV + k]; });
+      rows16<2, SB>(aa, DK / 8, [&](int m, int k) { return YW[(16 * bI + m) * SQ + k]; },
+                [&](int k, int jj, int n) { return sm.ww[(16 * bJ + 8 * jj + n) * SQ + k]; });
+      each(aa, [&](int m, int n, float& v) {
+        int r = 16 * bI + m, s = 16 * bJ + n;
+        sm.tm[r * SC + s] = s < r ? -v : 0.f;
+      });
+    }
+  }
+  __syncthreads();
+  // ---- dbeta += rowsum(dA .* A'), then MA = beta_r dA (gradient of A')
+  for (int r = warp; r < L; r += NW) {
+    float acc = 0.f;
+    for (int s = lane; s < r; s += 32) acc += sm.tm[r * SC + s] * sm.am[r * SC + s];
+    acc = warp_sum(acc);
+    if (lane == 0) sm.dbet[r] += acc;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < C * C; idx += NTH) {
+    int r = idx / C, s = idx % C;
+    if (s < r) sm.tm[r * SC + s] *= sm.bet[r];
+  }
+  __syncthreads();
+  // ---- pairwise decay-ratio terms (owner tile rows 16I.., key columns 16hk..).
+  // Row and column sums of the same pair enter dG with opposite signs and
+  // must cancel in the cumulative sum, so these products keep ~21 bits.
+  float prow[2][4], arow[2][4], col[2][4];
+  zero(prow);
+  zero(arow);
+  zero(col);
+  {
+    const bool ok = sm.spanok[I];
+    for (int J = 0; J <= I; J++) {
+      if (J == I && !ok) break;
+      const float* scl = J < I ? sm.dd + pidx(I, J) * DK : sm.ei + I * DK;
+      auto fbR = [&](int k, int jj, int n) { return sm.rr[(16 * J + k) * SQ + 16 * hk + 8 * jj + n] * scl[16 * hk + 8 * jj + n]; };
+      rows16<2, true>(prow, 2, [&](int m, int k) { return sm.pm[(16 * I + m) * SC + 16 * J + k]; }, fbR);
+      rows16<2, true>(arow, 2, [&](int m, int k) { return sm.tm[(16 * I + m) * SC + 16 * J + k]; }, fbR);
+    }
+    // col terms of columns s in block I: rows r in blocks I2 >= I
+    for (int I2 = I; I2 < 4; I2++) {
+      if (I2 == I && !ok) continue;
+      const float* scl = I2 > I ? sm.dd + pidx(I2, I) * DK : sm.ei + I * DK;
+      rows16<2, true>(col, 2, [&](int m, int k) { return sm.pm[(16 * I2 + k) * SC + 16 * I + m]; },
+                [&](int k, int jj, int n) { return sm.lq[(16 * I2 + k) * SQ + 16 * hk + 8 * jj + n] * scl[16 * hk + 8 * jj + n]; });
+      rows16<2, true>(col, 2, [&](int m, int k) { return sm.tm[(16 * I2 + k) * SC + 16 * I + m]; },
+                [&](int k, int jj, int n) { return sm.lk[(16 * I2 + k) * SQ + 16 * hk + 8 * jj + n] * scl[16 * hk + 8 * jj + n]; });
+    }
+  }
+  // ---- assemble dq^, dk^, dG per owned element
+  float dqh[2][4], dkh[2][4], dG[2][4], kdt[2][4];
+  {
+    const bool ok = sm.spanok[I];
+    const bf16* qg_ = (const bf16*)io.q;
+    const bf16* kg_ = (const bf16*)io.k;
+#pragma unroll
+    for (int jj = 0; jj < 2; jj++)
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        const int r = 16 * I + gq + 8 * (e >> 1), i = 16 * hk + 8 * jj + 2 * tq + (e & 1);
+        const float G = sm.gg[r * SQ + i];
+        const float eL = expf(G - sm.gb[I * DK + i]), eR = expf(sm.ge[I * DK + i] - G);
+        float pr = prow[jj][e] * eL, ar = arow[jj][e] * eL, cl = col[jj][e] * eR;
+        if (!ok) {  // exact diagonal-block terms
+          const float* Gr = sm.gg + r * SQ;
+          for (int s = 16 * I; s < 16 * I + 16 && s < L; s++) {  // rows past the chunk end are zero
+            float ks = bfl(kg_[((size_t)(t0 + s) * H + h) * DK + i]) * sm.ink[s];
+            float qs = bfl(qg_[((size_t)(t0 + s) * H + h) * DK + i]) * sm.inq[s];
+            if (s <= r) {
+              float ex = expf(Gr[i] - sm.gg[s * SQ + i]);
+              pr += sm.pm[r * SC + s] * ks * ex;
+              ar += sm.tm[r * SC + s] * ks * ex;
+            }
+            if (s >= r) {
+              float ex = expf(sm.gg[s * SQ + i] - Gr[i]);
+              cl += (sm.pm[s * SC + r] * qs + sm.tm[s * SC + r] * ks) * ex;
+            }
+          }
+        }
+        const float q = sm.qh[r * SQ + i], k = sm.kh[r * SQ + i];
+        const float Gm = expf(G), kdf = expf(sm.gl[i] - G);
+        const float dkg = sm.bet[r] * yw[jj][e];
+        dqh[jj][e] = pr + dQG[jj][e] * Gm;
+        dkh[jj][e] = ar + cl + dkg * Gm + dKD[jj][e] * kdf;
+        dG[jj][e] = q * pr + k * ar - k * cl + dQG[jj][e] * q * Gm + dkg * k * Gm;
+        kdt[jj][e] = dKD[jj][e] * k * kdf;
+      }
+  }
+  __syncthreads();  // everyone is done reading lq, lk, rr, pm, tm
+  float* dqs = sm.lq;
+  float* dks = sm.lk;
+  float* dGs = sm.rr;
+  float* kdts = sm.ww;
+#pragma unroll
+  for (int jj = 0; jj < 2; jj++)
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+      const int r = 16 * I + gq + 8 * (e >> 1), i = 16 * hk + 8 * jj + 2 * tq + (e & 1);
+      dqs[r * SQ + i] = dqh[jj][e];
+      dks[r * SQ + i] = dkh[jj][e];
+      dGs[r * SQ + i] = dG[jj][e];
+      kdts[r * SQ + i] = kdt[jj][e];
+    }
+  __syncthreads();
+  // ---- reverse cumulative sum of dG over the chunk (with the G_last terms):
+  //      dg_t = sum_{r >= t} (dG_r - kdt_r) + sum_r kdt_r + dgamma gamma
+  {
+    float run = 0.f, ksum = 0.f;
+    for (int m = 7; m >= 0; m--) {
+      int r = 8 * warp + m;
+      if (r < L) {
+        run += dGs[r * SQ + lane] - kdts[r * SQ + lane];
+        ksum += kdts[r * SQ + lane];
+      }
+      sm.tm[r * SC + lane] = run;  // local suffix sums (tm is free now)
+    }
+    sm.tot[warp * DK + lane] = run;
+    sm.e2[warp * DK + lane] = ksum;
+  }
+  __syncthreads();
+  {
+    float off = sm.dgam[lane] * sm.gam[lane];
+    for (int w2 = 0; w2 < NW; w2++) off += sm.e2[w2 * DK + lane];   // sum_r kdt_r
+    for (int w2 = warp + 1; w2 < NW; w2++) off += sm.tot[w2 * DK + lane];
+    bf16* dfo = (bf16*)io.df;
+    float pdt = 0.f, pA = 0.f;
+    for (int m = 0; m < 8; m++) {
+      int r = 8 * warp + m;
+      if (r < L) {
+        float dg = sm.tm[r * SC + lane] + off;
+        float x = bfl(sm.fr[r * DK + lane]) + dtb[lane];
+        float g = -a * softplus_f(x);
+        float dx = dg * (-a) * sigmoid_f(x);
+        dfo[((size_t)(t0 + r) * H + h) * DK + lane] = __float2bfloat16_rn(dx);
+        pdt += dx;
+        pA += dg * g;
+      }
+    }
+    sm.part[warp * DK + lane] = pdt;
+    pA = warp_sum(pA);
+    if (lane == 0) sm.red[warp] = pA;
+  }
+  __syncthreads();
+  if (tid < DK) {
+    float s = 0.f;
+    for (int w2 = 0; w2 < NW; w2++) s += sm.part[w2 * DK + tid];
+    w.pdt[ch * DK + tid] = s;
+  }
+  if (tid == 0) {
+    float s = 0.f;
+    for (int w2 = 0; w2 < NW; w2++) s += sm.red[w2];
+    w.pA[ch] = s;
+  }
+  // ---- L2-norm backward, db
+  {
+    bf16* dqo = (bf16*)io.dq;
+    bf16* dko = (bf16*)io.dk;
+    bf16* dbo = (bf16*)io.db;
+    for (int r = warp; r < L; r += NW) {
+      float q = sm.qh[r * SQ + lane], k = sm.kh[r * SQ + lane];
+      float dq_ = dqs[r * SQ + lane], dk_ = dks[r * SQ + lane];
+      float pq = warp_sum(q * dq_), pk = warp_sum(k * dk_);
+      size_t off = ((size_t)(t0 + r) * H + h) * DK + lane;
+      dqo[off] = __float2bfloat16_rn((dq_ - q * pq) * sm.inq[r]);
+      dko[off] = __float2bfloat16_rn((dk_ - k * pk) * sm.ink[r]);
+      if (lane == 0)
+        dbo[(size_t)(t0 + r) * H + h] = __float2bfloat16_rn(sm.dbet[r] * sm.bet[r] * sigmoid_f(-sm.braw[r]));
+    }
+  }
+}
+
+}  // namespace fast
+
+static_assert(sizeof(fast::FwdSm) <= 232448, "forward chain shared memory exceeds 227 KB");
+static_assert(sizeof(fast::BwdSm) <= 232448, "backward chunk shared memory exceeds 227 KB");
+
+bool fast_path(int dtype, int dk, int dv) { return dtype == 0 && dk == fast::DK && dv == fast::DV; }
+
+cudaError_t launch_fast_fwd(const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st) {
+  const size_t smem = sizeof(fast::FwdSm);
+  cudaError_t e = cudaFuncSetAttribute(fast::fwd_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  prof_begin(K_FWD_CHAIN, st);
+  fast::fwd_chain_kernel<<<dim3(d.n_docs, d.H), fast::NTH, smem, st>>>(d, io, w);
+  prof_end(K_FWD_CHAIN, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fast_bwd(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st) {
+  prof_begin(K_BWD_SCAN, st);
+  fast::bwd_scan_kernel<<<dim3(d.n_docs, d.H, fast::DV / fast::NS), 128, 0, st>>>(d, io, w);
+  prof_end(K_BWD_SCAN, st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t smem = sizeof(fast::BwdSm);
+  e = cudaFuncSetAttribute(fast::bwd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  prof_begin(K_BWD_CHUNK, st);
+  fast::bwd_chunk_kernel<<<dim3(d.nc_max, d.H), fast::NTH, smem, st>>>(d, io, w);
+  prof_end(K_BWD_CHUNK, st);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_bwd_reduce(d, io, w, st);
+}
+
+}  // namespace kda

@@ -19,6 +19,8 @@ enum KernelId {
   K_BWD_SCAN,
   K_BWD_INTRA,
   K_BWD_REDUCE,
+  K_FWD_CHAIN,
+  K_BWD_CHUNK,
   K_COUNT
 };
 
@@ -40,6 +42,8 @@ struct Ws {
   float* KD;   // [ch][C][dk]  K^ * exp(G_last - G)
   float* gam;  // [ch][dk]     exp(G_last)
   float* Sent; // [ch][dk][dv] state entering the chunk (saved for backward)
+  float* M;    // [ch][dk][dk] Diag(gamma) - KD^T W (tensor-core path, saved for backward)
+  float* QW;   // [ch][C][dk]  QG - P W            (tensor-core path, saved for backward)
   // backward
   float* dE;   // [ch][C][dv]  gradient of E = U - W S
   float* dSn;  // [ch][dk][dv] gradient of the state leaving the chunk
@@ -54,6 +58,7 @@ struct Dims {
   float scale;
   int32_t tag;   // nonzero hash of the problem; the forward stores it when saving
   int32_t save;  // forward saves for the backward
+  int32_t fast;  // bf16 io with dk = 32, dv = 64: tensor-core kernels
 };
 
 // Backward kernels refuse a workspace that no saving forward of the same
@@ -90,6 +95,9 @@ cudaError_t launch_fwd_scan(int dtype, const Dims& d, const FwdIO& io, const Ws&
 cudaError_t launch_bwd_scan(int dtype, const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st);
 cudaError_t launch_bwd_intra(int dtype, const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st);
 cudaError_t launch_bwd_reduce(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st);
+bool fast_path(int dtype, int dk, int dv);
+cudaError_t launch_fast_fwd(const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st);
+cudaError_t launch_fast_bwd(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st);
 
 // Timing brackets (no-ops unless kda_prof_start() armed them).
 void prof_begin(int kid, cudaStream_t st);
