@@ -385,10 +385,22 @@ __global__ void __launch_bounds__(256) bwd_reduce_kernel(Dims d, BwdIO io, Ws w)
     __syncthreads();
   }
   if (tid == 0) io.dA_log[h] = red[0];
-  for (int i = tid; i < dk; i += blockDim.x) {
+  // ddt_bias: the 256 threads split into groups that each own every
+  // G-th chunk of a block of channels; partials are combined in a fixed order.
+  const int ng = blockDim.x / 32 < 8 ? blockDim.x / 32 : 8;
+  for (int i0 = 0; i0 < dk; i0 += 32) {
+    __syncthreads();
+    const int grp = tid >> 5, i = i0 + (tid & 31);
     float s = 0.f;
-    for (int c = 0; c < nc; c++) s += w.pdt[((int64_t)c * H + h) * dk + i];
-    io.ddt_bias[h * dk + i] = s;
+    if (grp < ng && i < dk)
+      for (int c = grp; c < nc; c += ng) s += w.pdt[((int64_t)c * H + h) * dk + i];
+    red[tid] = s;
+    __syncthreads();
+    if (tid < 32 && i0 + tid < dk) {
+      float t = 0.f;
+      for (int g = 0; g < ng; g++) t += red[g * 32 + tid];
+      io.ddt_bias[h * dk + i0 + tid] = t;
+    }
   }
 }
 

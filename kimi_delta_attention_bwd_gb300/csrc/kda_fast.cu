@@ -36,20 +36,13 @@ constexpr int SQ = DK + 4;  // row stride of [C][DK] operands read along rows
 constexpr int SX = DK + 8;  // row stride of [C][DK] operands read along columns
 constexpr int SV = DV + 8;  // row stride of [C][DV] operands
 constexpr int SC = C + 4;   // row stride of [C][C] matrices
+constexpr int SO = DV + 8;  // row stride of the bf16 dO tile
 constexpr int NTH = 256, NW = 8;
 constexpr float SPAN_MAX = 80.f;
-#ifndef KDA_SPLIT_BWD
-#define KDA_SPLIT_BWD 1
-#endif
-#ifndef KDA_SPLIT_RECOMP
-#define KDA_SPLIT_RECOMP 1
-#endif
-constexpr bool SB = KDA_SPLIT_BWD != 0;     // backward gradient products
-constexpr bool SR = KDA_SPLIT_RECOMP != 0;  // backward recomputation of the chunk
-#ifndef KDA_SPLIT_FWD
-#define KDA_SPLIT_FWD 1
-#endif
-constexpr bool SF = KDA_SPLIT_FWD != 0;     // forward chain products
+// Every tensor-core product runs with split tf32 operands (see the header).
+constexpr bool SB = true;  // backward gradient products
+constexpr bool SR = true;  // backward recomputation of the chunk
+constexpr bool SF = true;  // forward chain products
 
 __device__ __forceinline__ int pidx(int I, int J) { return I * (I - 1) / 2 + J; }
 __device__ __forceinline__ float bfl(bf16 x) { return __bfloat162float(x); }
@@ -92,50 +85,85 @@ __device__ __forceinline__ void stage_chunk(bf16* st, const FwdIO& io, int H, in
   cp_commit();
 }
 
-// q^, k^ (L2-normalised), G (in-chunk inclusive cumulative log-decay), beta,
-// raw v (into xv).  Rows >= L are zero (G continues flat).
-__device__ void prologue(const Intra& c, const bf16* st, int L, float a, const float* dtb) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int idx = tid; idx < C * DK; idx += NTH) {
-    int r = idx / DK, i = idx % DK;
-    float qv = 0.f, kv = 0.f, gv = 0.f;
-    if (r < L) {
-      qv = bfl(st[idx]);
-      kv = bfl(st[C * DK + idx]);
-      gv = -a * softplus_f(bfl(st[2 * C * DK + idx]) + dtb[i]);
-    }
-    c.qh[r * SQ + i] = qv;
-    c.kh[r * SQ + i] = kv;
-    c.gg[r * SQ + i] = gv;
-  }
-  for (int idx = tid; idx < C * DV; idx += NTH) {
-    int r = idx / DV, j = idx % DV;
-    c.xv[r * SV + j] = r < L ? bfl(st[3 * C * DK + idx]) : 0.f;
-  }
-  if (tid < C) c.bet[tid] = tid < L ? sigmoid_f(c.braw[tid]) : 0.f;
-  __syncthreads();
-  for (int r = warp; r < C; r += NW) {  // one warp per row, lane = key channel
-    float q = c.qh[r * SQ + lane], k = c.kh[r * SQ + lane];
-    float iq = 1.0f / sqrtf(warp_sum(q * q) + L2_EPS), ik = 1.0f / sqrtf(warp_sum(k * k) + L2_EPS);
-    c.qh[r * SQ + lane] = q * iq;
-    c.kh[r * SQ + lane] = k * ik;
-    if (lane == 0) { c.inq[r] = iq; c.ink[r] = ik; }
-  }
-  {  // cumulative sum over rows: warp w scans rows 8w..8w+7 of channel `lane`
-    float run = 0.f;
+__device__ __forceinline__ void unpack8(const uint4& u, float* x) {
+  const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
-    for (int m = 0; m < 8; m++) {
-      run += c.gg[(8 * warp + m) * SQ + lane];
-      c.gg[(8 * warp + m) * SQ + lane] = run;
-    }
-    c.tot[warp * DK + lane] = run;
+  for (int e = 0; e < 4; e++) {
+    float2 f = __bfloat1622float2(p[e]);
+    x[2 * e] = f.x;
+    x[2 * e + 1] = f.y;
   }
+}
+
+// q^, k^ (L2-normalised), G (in-chunk inclusive cumulative log-decay), beta
+// and raw v (into xv) from the staged chunk.  Thread t owns row t / 4 and
+// key channels 8 (t % 4) .. + 7 (value columns 16 (t % 4) .. + 15).  Rows
+// >= L are zero (G continues flat).  vraw returns the thread's raw v.
+__device__ void prologue(const Intra& c, const bf16* st, int L, float a, const float* dtb, uint4 (&vraw)[2]) {
+  const int tid = threadIdx.x, r = tid >> 2, q4 = tid & 3, lane = tid & 31, warp = tid >> 5;
+  float qv[8], kv[8], gv[8];
+  const bool in = r < L;
+  if (in) {
+    unpack8(*reinterpret_cast<const uint4*>(st + r * DK + 8 * q4), qv);
+    unpack8(*reinterpret_cast<const uint4*>(st + C * DK + r * DK + 8 * q4), kv);
+    unpack8(*reinterpret_cast<const uint4*>(st + 2 * C * DK + r * DK + 8 * q4), gv);
+#pragma unroll
+    for (int e = 0; e < 8; e++) gv[e] = -a * softplus_f(gv[e] + dtb[8 * q4 + e]);
+    vraw[0] = *reinterpret_cast<const uint4*>(st + 3 * C * DK + r * DV + 16 * q4);
+    vraw[1] = *reinterpret_cast<const uint4*>(st + 3 * C * DK + r * DV + 16 * q4 + 8);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; e++) qv[e] = kv[e] = gv[e] = 0.f;
+    vraw[0] = vraw[1] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  float sq = 0.f, sk = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; e++) { sq += qv[e] * qv[e]; sk += kv[e] * kv[e]; }
+  sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+  sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+  sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+  sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+  const float iq = 1.0f / sqrtf(sq + L2_EPS), ik = 1.0f / sqrtf(sk + L2_EPS);
+  if (q4 == 0) {
+    c.inq[r] = iq;
+    c.ink[r] = ik;
+    c.bet[r] = in ? sigmoid_f(c.braw[r]) : 0.f;
+  }
+#pragma unroll
+  for (int e = 0; e < 8; e++) {
+    c.qh[r * SQ + 8 * q4 + e] = qv[e] * iq;
+    c.kh[r * SQ + 8 * q4 + e] = kv[e] * ik;
+  }
+  {  // raw v
+    float vv[8];
+    unpack8(vraw[0], vv);
+#pragma unroll
+    for (int e = 0; e < 8; e++) c.xv[r * SV + 16 * q4 + e] = vv[e];
+    unpack8(vraw[1], vv);
+#pragma unroll
+    for (int e = 0; e < 8; e++) c.xv[r * SV + 16 * q4 + 8 + e] = vv[e];
+  }
+  // cumulative sum of g over rows: within a warp (8 rows) by shuffles among
+  // lanes of equal t % 4, then across warps through smem
+#pragma unroll
+  for (int e = 0; e < 8; e++) {
+    float x = gv[e];
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      float y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    gv[e] = x;
+  }
+  if (lane >= 28)
+#pragma unroll
+    for (int e = 0; e < 8; e++) c.tot[warp * DK + 8 * q4 + e] = gv[e];
   __syncthreads();
-  {
+#pragma unroll
+  for (int e = 0; e < 8; e++) {
     float off = 0.f;
-    for (int w2 = 0; w2 < warp; w2++) off += c.tot[w2 * DK + lane];
-#pragma unroll
-    for (int m = 0; m < 8; m++) c.gg[(8 * warp + m) * SQ + lane] += off;
+    for (int w2 = 0; w2 < warp; w2++) off += c.tot[w2 * DK + 8 * q4 + e];
+    c.gg[r * SQ + 8 * q4 + e] = gv[e] + off;
   }
   __syncthreads();
 }
@@ -229,41 +257,47 @@ __device__ void ap(const Intra& c, float* am, float* pm, float pscale, const bf1
   __syncthreads();
 }
 
-// T = (I + A)^-1 for unit-lower A (A = beta_r am_rs when !BETA).  fp32 SIMT:
-// diagonal 16x16 blocks by forward substitution, then block rows.
+// T = (I + A)^-1 for unit-lower A (A = beta_r am_rs when !BETA).  The 16x16
+// diagonal blocks by forward substitution (one lane per column), then block
+// rows I = 1..3 on the tensor cores:  Y = A[I, <I] T[<I, <I],  T[I, <I] = -T_II Y.
 template <bool BETA>
 __device__ void solve(const float* am, float* tm, float* yy, const float* bet) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   auto A = [&](int r, int s) { return BETA ? am[r * SC + s] : bet[r] * am[r * SC + s]; };
-  if (warp < 4) {
-    const int I = warp, cidx = lane & 15;
+  if (warp < 2) {
+    const int I = 2 * warp + (lane >> 4), cidx = lane & 15;
     float tc[16];
 #pragma unroll
     for (int r = 0; r < 16; r++) {
-      float v = (r == cidx) ? 1.f : 0.f;
+      float v0 = (r == cidx) ? 1.f : 0.f, v1 = 0.f;
 #pragma unroll
-      for (int s = 0; s < r; s++) v = fmaf(-A(16 * I + r, 16 * I + s), tc[s], v);
-      tc[r] = v;
+      for (int s = 0; s + 1 < r; s += 2) {
+        v0 = fmaf(-A(16 * I + r, 16 * I + s), tc[s], v0);
+        v1 = fmaf(-A(16 * I + r, 16 * I + s + 1), tc[s + 1], v1);
+      }
+      if (r & 1) v0 = fmaf(-A(16 * I + r, 16 * I + r - 1), tc[r - 1], v0);
+      tc[r] = v0 + v1;
     }
-    if (lane < 16)
 #pragma unroll
-      for (int r = 0; r < 16; r++) tm[(16 * I + r) * SC + 16 * I + cidx] = tc[r];
+    for (int r = 0; r < 16; r++) tm[(16 * I + r) * SC + 16 * I + cidx] = tc[r];
   }
   __syncthreads();
   for (int I = 1; I < 4; I++) {
-    const int ncol = 16 * I;
-    for (int idx = tid; idx < 16 * ncol; idx += NTH) {  // Y = sum_{K=J}^{I-1} A_IK T_KJ
-      int m = idx / ncol, cc = idx % ncol, J = cc >> 4;
-      float acc = 0.f;
-      for (int s = 16 * J; s < 16 * I; s++) acc = fmaf(A(16 * I + m, s), tm[s * SC + cc], acc);
-      yy[m * C + cc] = acc;
+    if (warp < 2 * I) {  // Y tile w: columns 8w.. of block J = w / 2; k over blocks J..I-1
+      const int J = warp >> 1, k0 = 16 * J;
+      float acc[1][4];
+      zero(acc);
+      rows16<1, true>(acc, 2 * (I - J), [&](int m, int k) { return A(16 * I + m, k0 + k); },
+                      [&](int k, int j, int n) { return tm[(k0 + k) * SC + 8 * warp + n]; });
+      each(acc, [&](int m, int col, float& v) { yy[m * C + 8 * warp + col] = v; });
     }
     __syncthreads();
-    for (int idx = tid; idx < 16 * ncol; idx += NTH) {  // T_IJ = -T_II Y
-      int m = idx / ncol, cc = idx % ncol;
-      float acc = 0.f;
-      for (int k = 0; k <= m; k++) acc = fmaf(tm[(16 * I + m) * SC + 16 * I + k], yy[k * C + cc], acc);
-      tm[(16 * I + m) * SC + cc] = -acc;
+    if (warp < 2 * I) {
+      float acc[1][4];
+      zero(acc);
+      rows16<1, true>(acc, 2, [&](int m, int k) { return tm[(16 * I + m) * SC + 16 * I + k]; },
+                      [&](int k, int j, int n) { return yy[k * C + 8 * warp + n]; });
+      each(acc, [&](int m, int col, float& v) { tm[(16 * I + m) * SC + 8 * warp + col] = -v; });
     }
     __syncthreads();
   }
@@ -333,7 +367,8 @@ __global__ void __launch_bounds__(NTH, 1) fwd_chain_kernel(Dims d, FwdIO io, Ws 
     cp_wait_all();
     if (tid < C) sm.braw[tid] = bnext;
     __syncthreads();
-    prologue(c, sm.stage, L, a, dtb);
+    uint4 vraw[2];
+    prologue(c, sm.stage, L, a, dtb, vraw);
     if (ci + 1 < ce) {  // stage the next chunk while this one computes
       const int L1 = w.chunk_len[ci + 1], t01 = w.chunk_tok0[ci + 1];
       stage_chunk(sm.stage, io, H, h, t01, L1);
@@ -429,10 +464,14 @@ __global__ void __launch_bounds__(NTH, 1) fwd_chain_kernel(Dims d, FwdIO io, Ws 
 constexpr int NS = 16;        // value columns per scan CTA
 constexpr int SS = NS + 8;    // row stride of [*][NS] operands
 
+// One CTA per (document, head, 16 value columns), walking the chunks in
+// reverse: dS_in = M^T dS_out + QW^T dO.  The next chunk's M, QW and dO slice
+// are prefetched (cp.async, double buffer) while the current one computes;
+// QW^T dO is independent of the carried dS, so only M^T dS is on the chain.
 __global__ void __launch_bounds__(128) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
-  __shared__ float Ms[DK * SQ];
-  __shared__ float QWs[C * SQ];
-  __shared__ float dOs[C * SS];
+  __shared__ __align__(16) float Ms[2][DK * SQ];
+  __shared__ __align__(16) float QWs[2][C * SQ];
+  __shared__ __align__(16) bf16 dOs[2][C * NS];
   __shared__ float dS[DK * SS];
   const int doc = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * NS, tid = threadIdx.x, warp = tid >> 5;
   if (!saved_ok(d, w.tag, w.err)) return;
@@ -443,32 +482,45 @@ __global__ void __launch_bounds__(128) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
     dS[i * SS + j] = io.dh_final ? io.dh_final[(((int64_t)doc * H + h) * DK + i) * DV + col0 + j] : 0.f;
   }
   const int cb = w.doc_chunk0[doc], ce = w.doc_chunk0[doc + 1];
-  __syncthreads();
-  const int mI = warp & 1, jn = warp >> 1;
-  for (int ci = ce - 1; ci >= cb; ci--) {
+  auto prefetch = [&](int ci, int buf) {
     const int64_t ch = (int64_t)ci * H + h;
     const int L = w.chunk_len[ci], t0 = w.chunk_tok0[ci];
+    for (int idx = tid; idx < DK * 8; idx += 128) {  // 8 x 16 B per row of 32 floats
+      int i = idx >> 3, p = idx & 7;
+      cp16(&Ms[buf][i * SQ + p * 4], w.M + ch * DK * DK + i * DK + p * 4);
+    }
+    for (int idx = tid; idx < C * 8; idx += 128) {
+      int r = idx >> 3, p = idx & 7;
+      cp16(&QWs[buf][r * SQ + p * 4], w.QW + ch * C * DK + r * DK + p * 4);
+    }
+    for (int idx = tid; idx < C * 2; idx += 128) {  // 2 x 16 B per 16-column bf16 row slice
+      int r = idx >> 1, p = idx & 1;
+      if (r < L) cp16(&dOs[buf][r * NS + p * 8], dO + ((size_t)(t0 + r) * H + h) * DV + col0 + p * 8);
+      else *reinterpret_cast<uint4*>(&dOs[buf][r * NS + p * 8]) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    cp_commit();
+  };
+  if (cb < ce) prefetch(ce - 1, 0);
+  const int mI = warp & 1, jn = warp >> 1;
+  for (int ci = ce - 1, buf = 0; ci >= cb; ci--, buf ^= 1) {
+    const int64_t ch = (int64_t)ci * H + h;
+    cp_wait_all();
+    __syncthreads();  // buffer `buf` and the last dS update are visible
+    if (ci - 1 >= cb) prefetch(ci - 1, buf ^ 1);
     for (int idx = tid; idx < DK * NS; idx += 128) {
       int i = idx / NS, j = idx % NS;
       w.dSn[ch * DK * DV + i * DV + col0 + j] = dS[i * SS + j];
     }
-    for (int idx = tid; idx < DK * DK; idx += 128) Ms[(idx / DK) * SQ + idx % DK] = w.M[ch * DK * DK + idx];
-    for (int idx = tid; idx < C * DK; idx += 128) QWs[(idx / DK) * SQ + idx % DK] = w.QW[ch * C * DK + idx];
-    for (int idx = tid; idx < C * NS; idx += 128) {
-      int r = idx / NS, j = idx % NS;
-      dOs[r * SS + j] = r < L ? bfl(dO[((size_t)(t0 + r) * H + h) * DV + col0 + j]) : 0.f;
-    }
-    __syncthreads();
     float acc[1][4];
     zero(acc);
-    rows16<1, true>(acc, DK / 8, [&](int m, int k) { return Ms[k * SQ + 16 * mI + m]; },
+    rows16<1, true, false, true>(acc, C / 8, [&](int m, int k) { return QWs[buf][k * SQ + 16 * mI + m]; },
+                                 [&](int k, int j, int n) { return bfl(dOs[buf][k * NS + 8 * jn + n]); });
+    rows16<1, true>(acc, DK / 8, [&](int m, int k) { return Ms[buf][k * SQ + 16 * mI + m]; },
                     [&](int k, int j, int n) { return dS[k * SS + 8 * jn + n]; });
-    rows16<1, true>(acc, C / 8, [&](int m, int k) { return QWs[k * SQ + 16 * mI + m]; },
-                    [&](int k, int j, int n) { return dOs[k * SS + 8 * jn + n]; });
-    __syncthreads();
+    __syncthreads();  // every read of dS is done
     each(acc, [&](int m, int col, float& v) { dS[(16 * mI + m) * SS + 8 * jn + col] = v; });
-    __syncthreads();
   }
+  __syncthreads();
   if (io.dh0)
     for (int idx = tid; idx < DK * NS; idx += 128) {
       int i = idx / NS, j = idx % NS;
@@ -485,7 +537,7 @@ struct BwdSm {
   float r1[C * SX + C * SV];                 // xk | xv, then dE (C*SV) | dW (C*SQ)
   float ss[DK * SV], dsn[DK * SV];           // S, dS'; later YU [C][SV]
   float e2[C * SV];                          // solve scratch, then E, then YW [C][SQ]
-  bf16 dOs[C * DV];
+  bf16 dOs[C * SO];
   bf16 fr[C * DK];
   float tot[NW * DK], part[NW * DK];
   float bet[C], inq[C], ink[C], braw[C], dbet[C];
@@ -520,7 +572,7 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
     const bf16* dO = (const bf16*)io.dO;
     for (int idx = tid; idx < C * 8; idx += NTH) {
       int r = idx >> 3, p = idx & 7;
-      if (r < L) cp16(sm.dOs + r * DV + p * 8, dO + ((size_t)(t0 + r) * H + h) * DV + p * 8);
+      if (r < L) cp16(sm.dOs + r * SO + p * 8, dO + ((size_t)(t0 + r) * H + h) * DV + p * 8);
     }
     const float* Sg = w.Sent + ch * DK * DV;
     const float* dSg = w.dSn + ch * DK * DV;
@@ -533,13 +585,14 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
     if (tid < C) sm.braw[tid] = tid < L ? bfl(((const bf16*)io.b)[(size_t)(t0 + tid) * H + h]) : 0.f;
     if (tid < C) sm.dbet[tid] = 0.f;
     for (int idx = tid; idx < C * DV; idx += NTH)
-      if (idx / DV >= L) sm.dOs[idx] = __float2bfloat16_rn(0.f);
+      if (idx / DV >= L) sm.dOs[(idx / DV) * SO + idx % DV] = __float2bfloat16_rn(0.f);
     cp_wait_all();
     __syncthreads();
     for (int idx = tid; idx < C * DK; idx += NTH) sm.fr[idx] = st[2 * C * DK + idx];
   }
   // ---- recompute the chunk (same arithmetic as the forward)
-  prologue(c, st, L, a, dtb);
+  uint4 vraw[2];  // this thread's raw v (row tid / 4, columns 16 (tid % 4) ..), kept for dbeta
+  prologue(c, st, L, a, dtb, vraw);
   factors(c, L, scale);
   ap<false, SR>(c, sm.am, sm.pm, 1.f, (const bf16*)io.q, (const bf16*)io.k, H, h, t0, L);
   solve<false>(sm.am, sm.tm, sm.e2, sm.bet);
@@ -550,7 +603,7 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
   float* E = sm.e2;             // [C][SV]
   float* YU = sm.ss;            // [C][SV] over ss | dsn
   float* YW = sm.e2;            // [C][SQ]
-  auto dO = [&](int r, int col) { return bfl(sm.dOs[r * DV + col]); };
+  auto dO = [&](int r, int col) { return bfl(sm.dOs[r * SO + col]); };
   const int I = warp & 3, hk = warp >> 2;  // owner tile: rows 16I.., key columns 16hk..
 
   // ---- dE = scale P'^T dO + KD dS'  and  E = U - W S
@@ -559,7 +612,7 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
     zero(acc);
     zero(acc2);
     const int half = warp >> 2;
-    rows16<4, SB>(acc, 2 * (4 - I), [&](int m, int k) { return sm.pm[(16 * I + k) * SC + 16 * I + m]; },
+    rows16<4, SB, false, true>(acc, 2 * (4 - I), [&](int m, int k) { return sm.pm[(16 * I + k) * SC + 16 * I + m]; },
               [&](int k, int jj, int n) { return dO(16 * I + k, 32 * half + 8 * jj + n); });
     rows16<4, SB>(acc2, DK / 8, [&](int m, int k) { return sm.kd[(16 * I + m) * SX + k]; },
               [&](int k, int jj, int n) { return sm.dsn[k * SV + 32 * half + 8 * jj + n]; });
@@ -586,7 +639,7 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
     zero(dQG);
     rows16<2, SB>(dKD, DV / 8, [&](int m, int k) { return E[(16 * I + m) * SV + k]; },
               [&](int k, int jj, int n) { return sm.dsn[(16 * hk + 8 * jj + n) * SV + k]; });
-    rows16<2, SB>(dQG, DV / 8, [&](int m, int k) { return dO(16 * I + m, k); },
+    rows16<2, SB, true>(dQG, DV / 8, [&](int m, int k) { return dO(16 * I + m, k); },
               [&](int k, int jj, int n) { return sm.ss[(16 * hk + 8 * jj + n) * SV + k]; });
     each(dQG, [&](int m, int col, float& v) { v *= scale; });
     float acc[2][4];
@@ -598,7 +651,7 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
       const int bI = t < 1 ? 0 : t < 3 ? 1 : t < 6 ? 2 : 3, bJ = t - bI * (bI + 1) / 2;
       float pp[2][4];
       zero(pp);
-      rows16<2, SB>(pp, DV / 8, [&](int m, int k) { return dO(16 * bI + m, k); },
+      rows16<2, SB, true>(pp, DV / 8, [&](int m, int k) { return dO(16 * bI + m, k); },
                 [&](int k, int jj, int n) { return E[(16 * bJ + 8 * jj + n) * SV + k]; });
       each(pp, [&](int m, int n, float& v) {
         int r = 16 * bI + m, s = 16 * bJ + n;
@@ -642,14 +695,22 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
   __syncthreads();
   // ---- dbeta (U and W terms), dA = -(YU U^T + YW W^T) strict lower (into tm)
   {
-    const bf16* vg = (const bf16*)io.v;
-    for (int r = warp; r < L; r += NW) {
+    {  // thread: row tid / 4, value columns 16 (tid % 4) .., key channels 8 (tid % 4) ..
+      const int r = tid >> 2, q4 = tid & 3;
+      float vv[16];
+      unpack8(vraw[0], vv);
+      unpack8(vraw[1], vv + 8);
       float acc = 0.f;
-      const bf16* vr = vg + ((size_t)(t0 + r) * H + h) * DV;
-      for (int jj = lane; jj < DV; jj += 32) acc += YU[r * SV + jj] * bfl(vr[jj]);
-      acc += YW[r * SQ + lane] * sm.kh[r * SQ + lane] * expf(sm.gg[r * SQ + lane]);
-      acc = warp_sum(acc);
-      if (lane == 0) sm.dbet[r] += acc;
+#pragma unroll
+      for (int e = 0; e < 16; e++) acc += YU[r * SV + 16 * q4 + e] * vv[e];
+#pragma unroll
+      for (int e = 0; e < 8; e++) {
+        const int i = 8 * q4 + e;
+        acc += YW[r * SQ + i] * sm.kh[r * SQ + i] * expf(sm.gg[r * SQ + i]);
+      }
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+      if (q4 == 0 && r < L) sm.dbet[r] += acc;
     }
     for (int t = warp; t < 10; t += NW) {
       const int bI = t < 1 ? 0 : t < 3 ? 1 : t < 6 ? 2 : 3, bJ = t - bI * (bI + 1) / 2;
@@ -659,24 +720,30 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
                 [&](int k, int jj, int n) { return sm.uu[(16 * bJ + 8 * jj + n) * SV + k]; });
       rows16<2, SB>(aa, DK / 8, [&](int m, int k) { return YW[(16 * bI + m) * SQ + k]; },
                 [&](int k, int jj, int n) { return sm.ww[(16 * bJ + 8 * jj + n) * SQ + k]; });
+      // dA = -aa (strict lower); its row sums against A' feed dbeta; MA = beta_r dA
+      float rs0 = 0.f, rs1 = 0.f;
       each(aa, [&](int m, int n, float& v) {
-        int r = 16 * bI + m, s = 16 * bJ + n;
-        sm.tm[r * SC + s] = s < r ? -v : 0.f;
+        const int r = 16 * bI + m, s = 16 * bJ + n;
+        const float da = s < r ? -v : 0.f;
+        const float pa = da * sm.am[r * SC + s];
+        if (m < 8) rs0 += pa; else rs1 += pa;
+        sm.tm[r * SC + s] = sm.bet[r] * da;
       });
+      rs0 += __shfl_xor_sync(0xffffffffu, rs0, 1);
+      rs0 += __shfl_xor_sync(0xffffffffu, rs0, 2);
+      rs1 += __shfl_xor_sync(0xffffffffu, rs1, 1);
+      rs1 += __shfl_xor_sync(0xffffffffu, rs1, 2);
+      if (tq == 0) {
+        sm.part[bJ * C + 16 * bI + gq] = rs0;
+        sm.part[bJ * C + 16 * bI + gq + 8] = rs1;
+      }
     }
   }
   __syncthreads();
-  // ---- dbeta += rowsum(dA .* A'), then MA = beta_r dA (gradient of A')
-  for (int r = warp; r < L; r += NW) {
+  if (tid < L) {  // fixed-order sum over the column blocks: deterministic
     float acc = 0.f;
-    for (int s = lane; s < r; s += 32) acc += sm.tm[r * SC + s] * sm.am[r * SC + s];
-    acc = warp_sum(acc);
-    if (lane == 0) sm.dbet[r] += acc;
-  }
-  __syncthreads();
-  for (int idx = tid; idx < C * C; idx += NTH) {
-    int r = idx / C, s = idx % C;
-    if (s < r) sm.tm[r * SC + s] *= sm.bet[r];
+    for (int J = 0; J <= (tid >> 4); J++) acc += sm.part[J * C + tid];
+    sm.dbet[tid] += acc;
   }
   __syncthreads();
   // ---- pairwise decay-ratio terms (owner tile rows 16I.., key columns 16hk..).
@@ -809,20 +876,38 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
     for (int w2 = 0; w2 < NW; w2++) s += sm.red[w2];
     w.pA[ch] = s;
   }
-  // ---- L2-norm backward, db
+  // ---- L2-norm backward, db (thread: row tid / 4, key channels 8 (tid % 4) ..)
   {
-    bf16* dqo = (bf16*)io.dq;
-    bf16* dko = (bf16*)io.dk;
-    bf16* dbo = (bf16*)io.db;
-    for (int r = warp; r < L; r += NW) {
-      float q = sm.qh[r * SQ + lane], k = sm.kh[r * SQ + lane];
-      float dq_ = dqs[r * SQ + lane], dk_ = dks[r * SQ + lane];
-      float pq = warp_sum(q * dq_), pk = warp_sum(k * dk_);
-      size_t off = ((size_t)(t0 + r) * H + h) * DK + lane;
-      dqo[off] = __float2bfloat16_rn((dq_ - q * pq) * sm.inq[r]);
-      dko[off] = __float2bfloat16_rn((dk_ - k * pk) * sm.ink[r]);
-      if (lane == 0)
-        dbo[(size_t)(t0 + r) * H + h] = __float2bfloat16_rn(sm.dbet[r] * sm.bet[r] * sigmoid_f(-sm.braw[r]));
+    const int r = tid >> 2, q4 = tid & 3;
+    float qv[8], kv[8], dqv[8], dkv[8], pq = 0.f, pk = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; e++) {
+      const int i = r * SQ + 8 * q4 + e;
+      qv[e] = sm.qh[i]; kv[e] = sm.kh[i]; dqv[e] = dqs[i]; dkv[e] = dks[i];
+      pq += qv[e] * dqv[e];
+      pk += kv[e] * dkv[e];
+    }
+    pq += __shfl_xor_sync(0xffffffffu, pq, 1);
+    pq += __shfl_xor_sync(0xffffffffu, pq, 2);
+    pk += __shfl_xor_sync(0xffffffffu, pk, 1);
+    pk += __shfl_xor_sync(0xffffffffu, pk, 2);
+    if (r < L) {
+      uint4 uq, uk;
+      __nv_bfloat162* pq2 = reinterpret_cast<__nv_bfloat162*>(&uq);
+      __nv_bfloat162* pk2 = reinterpret_cast<__nv_bfloat162*>(&uk);
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        pq2[e] = __floats2bfloat162_rn((dqv[2 * e] - qv[2 * e] * pq) * sm.inq[r],
+                                       (dqv[2 * e + 1] - qv[2 * e + 1] * pq) * sm.inq[r]);
+        pk2[e] = __floats2bfloat162_rn((dkv[2 * e] - kv[2 * e] * pk) * sm.ink[r],
+                                       (dkv[2 * e + 1] - kv[2 * e + 1] * pk) * sm.ink[r]);
+      }
+      const size_t off = ((size_t)(t0 + r) * H + h) * DK + 8 * q4;
+      *reinterpret_cast<uint4*>((bf16*)io.dq + off) = uq;
+      *reinterpret_cast<uint4*>((bf16*)io.dk + off) = uk;
+      if (q4 == 0)
+        ((bf16*)io.db)[(size_t)(t0 + r) * H + h] =
+            __float2bfloat16_rn(sm.dbet[r] * sm.bet[r] * sigmoid_f(-sm.braw[r]));
     }
   }
 }

@@ -24,10 +24,12 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1
 // acc[j] (a 16 x 8 tile, j < NT) += sum_k fa(m, k) * fb(k, j, c) for k in
 // [0, 8 * ksteps), m < 16, c < 8.  One warp.  Accumulator element e of tile
 // j sits at row gq + 8 * (e >> 1), column 2 * tq + (e & 1), where
-// gq = lane / 4 and tq = lane % 4.  With SPLIT each operand is carried as a
-// tf32 high part plus a tf32 remainder and three products are accumulated
-// (hi*hi + hi*lo + lo*hi), which keeps about 21 significant bits.
-template <int NT, bool SPLIT = false, class FA, class FB>
+// gq = lane / 4 and tq = lane % 4.
+// SPLIT carries each operand as a tf32 head plus a tf32 remainder and
+// accumulates hi*hi + hi*lo + lo*hi (about 21 significant bits).  AX / BX
+// declare the A / B operand exactly representable in tf32 (a bf16 input):
+// its remainder is zero, so the product with it is skipped.
+template <int NT, bool SPLIT = false, bool AX = false, bool BX = false, class FA, class FB>
 __device__ __forceinline__ void rows16(float (&acc)[NT][4], int ksteps, FA fa, FB fb) {
   const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
   for (int ks = 0; ks < ksteps; ks++) {
@@ -35,7 +37,7 @@ __device__ __forceinline__ void rows16(float (&acc)[NT][4], int ksteps, FA fa, F
     const float fa0 = fa(gq, kk), fa1 = fa(gq + 8, kk), fa2 = fa(gq, kk + 4), fa3 = fa(gq + 8, kk + 4);
     const uint32_t a0 = tf32(fa0), a1 = tf32(fa1), a2 = tf32(fa2), a3 = tf32(fa3);
     uint32_t l0 = 0, l1 = 0, l2 = 0, l3 = 0;
-    if (SPLIT) {
+    if (SPLIT && !AX) {
       l0 = tf32(fa0 - __uint_as_float(a0));
       l1 = tf32(fa1 - __uint_as_float(a1));
       l2 = tf32(fa2 - __uint_as_float(a2));
@@ -46,11 +48,11 @@ __device__ __forceinline__ void rows16(float (&acc)[NT][4], int ksteps, FA fa, F
       const float fb0 = fb(kk, j, gq), fb1 = fb(kk + 4, j, gq);
       const uint32_t b0 = tf32(fb0), b1 = tf32(fb1);
       mma_tf32(acc[j], a0, a1, a2, a3, b0, b1);
-      if (SPLIT) {
+      if (SPLIT && !BX) {
         const uint32_t h0 = tf32(fb0 - __uint_as_float(b0)), h1 = tf32(fb1 - __uint_as_float(b1));
         mma_tf32(acc[j], a0, a1, a2, a3, h0, h1);
-        mma_tf32(acc[j], l0, l1, l2, l3, b0, b1);
       }
+      if (SPLIT && !AX) mma_tf32(acc[j], l0, l1, l2, l3, b0, b1);
     }
   }
 }
