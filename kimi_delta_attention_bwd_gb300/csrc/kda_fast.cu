@@ -134,7 +134,7 @@ __device__ void prologue(const Intra& c, const bf16* st, int L, float a, const f
     c.qh[r * SQ + 8 * q4 + e] = qv[e] * iq;
     c.kh[r * SQ + 8 * q4 + e] = kv[e] * ik;
   }
-  {  // raw v
+  if (c.xv) {  // raw v (backward recomputation); the forward builds its beta-scaled operand itself
     float vv[8];
     unpack8(vraw[0], vv);
 #pragma unroll
@@ -168,8 +168,9 @@ __device__ void prologue(const Intra& c, const bf16* st, int L, float a, const f
   __syncthreads();
 }
 
-// Sub-block references, span guards, and the factor arrays.
-__device__ void factors(const Intra& c, int L, float scale) {
+// Sub-block references (G at each 16-row block start and end), span guards,
+// the per-pair channel factors and the chunk-end gate.
+__device__ void refs(const Intra& c, int L) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (warp < 4) {
     const int I = warp;
@@ -192,6 +193,12 @@ __device__ void factors(const Intra& c, int L, float scale) {
     c.gam[lane] = expf(g);
   }
   __syncthreads();
+}
+
+// Factor arrays of the backward recomputation (fp32).
+__device__ void factors(const Intra& c, int L, float scale) {
+  const int tid = threadIdx.x;
+  refs(c, L);
   for (int idx = tid; idx < C * DK; idx += NTH) {
     int r = idx / DK, i = idx % DK, I = r >> 4;
     float G = c.gg[r * SQ + i];
@@ -212,6 +219,35 @@ __device__ void factors(const Intra& c, int L, float scale) {
   __syncthreads();
 }
 
+// Factor arrays: lq, lk (in place of q^, k^ in the forward) and rr stay fp32
+// for the decay-ratio blocks; QG = scale q^ e^G (skipped when QG.hi is
+// null), KD = k^ e^{Gl - G} and XK = beta k^ e^G go to split-bf16 tiles.
+__device__ void factors_fwd(const Intra& c, int L, float scale, const Op& QG, const Op& KD, const Op& XK) {
+  const int tid = threadIdx.x;
+  refs(c, L);
+  for (int idx = tid; idx < C * DK / 2; idx += NTH) {
+    const int r = idx / (DK / 2), i = 2 * (idx % (DK / 2)), I = r >> 4;
+    float qg2[2], kd2[2], xk2[2];
+#pragma unroll
+    for (int e = 0; e < 2; e++) {
+      const float G = c.gg[r * SQ + i + e];
+      const float eL = expf(G - c.gb[I * DK + i + e]), eR = expf(c.ge[I * DK + i + e] - G);
+      const float Gm = expf(G), kdf = expf(c.gl[i + e] - G);
+      const float q = c.qh[r * SQ + i + e], k = c.kh[r * SQ + i + e];
+      qg2[e] = scale * q * Gm;
+      kd2[e] = k * kdf;
+      xk2[e] = c.bet[r] * k * Gm;
+      c.rr[r * SQ + i + e] = k * eR;
+      c.lq[r * SQ + i + e] = q * eL;
+      c.lk[r * SQ + i + e] = k * eL;
+    }
+    if (QG.hi) op_store2(QG, r, i, qg2[0], qg2[1]);
+    op_store2(KD, r, i, kd2[0], kd2[1]);
+    op_store2(XK, r, i, xk2[0], xk2[1]);
+  }
+  __syncthreads();
+}
+
 // Exact pairwise value sum_i x_ri k_si exp(G_ri - G_si) from the raw inputs
 // (the diagonal-block fallback when the in-block decay span exceeds 80).
 __device__ __forceinline__ float pair_exact(const bf16* X, float ix, const bf16* Kr, float ik, const float* Gr,
@@ -225,7 +261,7 @@ __device__ __forceinline__ float pair_exact(const bf16* X, float ix, const bf16*
 // pm gets pscale * P'.  Upper blocks are never read and are left untouched.
 template <bool BETA, bool SPL = false>
 __device__ void ap(const Intra& c, float* am, float* pm, float pscale, const bf16* qraw, const bf16* kraw, int H,
-                   int h, int t0, int L) {
+                   int h, int t0, int L, const Op* pop = nullptr) {
   const int warp = threadIdx.x >> 5;
   for (int task = warp; task < 20; task += NW) {
     const int blk = task >> 1, isP = task & 1;
@@ -248,11 +284,23 @@ __device__ void ap(const Intra& c, float* am, float* pm, float pscale, const bf1
         }
       });
     }
-    each(acc, [&](int m, int n, float& v) {
-      int r = 16 * I + m, s = 16 * J + n;
-      if (isP) pm[r * SC + s] = s <= r ? pscale * v : 0.f;
-      else am[r * SC + s] = s < r ? (BETA ? c.bet[r] * v : v) : 0.f;
-    });
+    if (isP && pop) {  // P as a split-bf16 operand tile
+      const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+      for (int jt = 0; jt < 2; jt++)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+          const int r = 16 * I + gq + 8 * hh, s0 = 16 * J + 8 * jt + 2 * tq;
+          op_store2(*pop, r, s0, s0 <= r ? pscale * acc[jt][2 * hh] : 0.f,
+                    s0 + 1 <= r ? pscale * acc[jt][2 * hh + 1] : 0.f);
+        }
+    } else {
+      each(acc, [&](int m, int n, float& v) {
+        int r = 16 * I + m, s = 16 * J + n;
+        if (isP) pm[r * SC + s] = s <= r ? pscale * v : 0.f;
+        else am[r * SC + s] = s < r ? (BETA ? c.bet[r] * v : v) : 0.f;
+      });
+    }
   }
   __syncthreads();
 }
@@ -326,12 +374,16 @@ __device__ void wu(const Intra& c, const float* tm, float* ww, float* uu) {
 // ------------------------------------------------------------------ forward
 struct FwdSm {
   bf16 stage[STAGE_ELEMS];
-  float qh[C * SQ], kh[C * SQ], gg[C * SQ], rr[C * SQ], qg[C * SQ], ww[C * SQ];
-  float kd[C * SX], xk[C * SX];
-  float xv[C * SV], ue[C * SV];
-  float am[C * SC], tm[C * SC], pm[C * SC];
-  float ss[DK * SV];
+  float qh[C * SQ], kh[C * SQ], gg[C * SQ], rr[C * SQ];  // q^ / k^ become lq / lk
+  float am[C * SC];   // A (fp32) for the solve, then the split-bf16 T operand
+  float tm[C * SC];   // T (fp32)
+  float uf[C * SV];   // U (fp32)
+  float ss[DK * SV];  // state S (fp32)
   float yy[16 * C];
+  bf16 oqg[2 * C * DK], okd[2 * C * DK], oxk[2 * C * DK], ow[2 * C * DK];
+  bf16 oxv[2 * C * DV];  // beta v, then E
+  bf16 op[2 * C * C];    // P (scaled)
+  bf16 os[2 * DK * DV];  // S
   float tot[NW * DK];
   float bet[C], inq[C], ink[C], braw[C];
   float gl[DK], gam[DK], gb[4 * DK], ge[4 * DK], dd[6 * DK], ei[4 * DK];
@@ -342,18 +394,31 @@ __global__ void __launch_bounds__(NTH, 1) fwd_chain_kernel(Dims d, FwdIO io, Ws 
   extern __shared__ __align__(16) unsigned char smraw[];
   FwdSm& sm = *reinterpret_cast<FwdSm*>(smraw);
   const int doc = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+  const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
   if (*w.err != 0) return;
   const int H = d.H;
   const int cb = w.doc_chunk0[doc], ce = w.doc_chunk0[doc + 1];
   const float a = expf(io.A_log[h]);
   const float* dtb = io.dt_bias + h * DK;
   const bf16* braw = (const bf16*)io.b;
-  Intra c{sm.qh, sm.kh, sm.gg, sm.qh, sm.kh, sm.rr, sm.kd, sm.xk, sm.xv, sm.qg, sm.bet, sm.inq, sm.ink,
+  Intra c{sm.qh, sm.kh, sm.gg, sm.qh, sm.kh, sm.rr, nullptr, nullptr, nullptr, nullptr, sm.bet, sm.inq, sm.ink,
           sm.braw, sm.gl, sm.gam, sm.gb, sm.ge, sm.dd, sm.ei, sm.tot, sm.spanok};
+  const Op QG{sm.oqg, sm.oqg + C * DK, DK}, KD{sm.okd, sm.okd + C * DK, DK}, XK{sm.oxk, sm.oxk + C * DK, DK};
+  const Op W{sm.ow, sm.ow + C * DK, DK}, XV{sm.oxv, sm.oxv + C * DV, DV}, E = XV;
+  const Op P{sm.op, sm.op + C * C, C}, S{sm.os, sm.os + DK * DV, DV};
+  const Op T{reinterpret_cast<bf16*>(sm.am), reinterpret_cast<bf16*>(sm.am) + C * C, C};
 
-  for (int idx = tid; idx < DK * DV; idx += NTH) {
-    int i = idx / DV, j = idx % DV;
-    sm.ss[i * SV + j] = io.h0 ? io.h0[(((int64_t)doc * H + h) * DK + i) * DV + j] : 0.f;
+  for (int idx = tid; idx < DK * DV / 2; idx += NTH) {
+    const int i = idx / (DV / 2), j = 2 * (idx % (DV / 2));
+    float s0 = 0.f, s1 = 0.f;
+    if (io.h0) {
+      const float* hp = io.h0 + (((int64_t)doc * H + h) * DK + i) * DV + j;
+      s0 = hp[0];
+      s1 = hp[1];
+    }
+    sm.ss[i * SV + j] = s0;
+    sm.ss[i * SV + j + 1] = s1;
+    op_store2(S, i, j, s0, s1);
   }
   float bnext = 0.f;
   if (cb < ce) {
@@ -369,39 +434,76 @@ __global__ void __launch_bounds__(NTH, 1) fwd_chain_kernel(Dims d, FwdIO io, Ws 
     __syncthreads();
     uint4 vraw[2];
     prologue(c, sm.stage, L, a, dtb, vraw);
+    {  // beta v -> XV (thread: row tid / 4, columns 16 (tid % 4) ..)
+      const int r = tid >> 2, q4 = tid & 3;
+      const float br = r < L ? sm.bet[r] : 0.f;
+      float vv[16];
+      unpack8(vraw[0], vv);
+      unpack8(vraw[1], vv + 8);
+#pragma unroll
+      for (int e = 0; e < 16; e += 2) op_store2(XV, r, 16 * q4 + e, br * vv[e], br * vv[e + 1]);
+    }
     if (ci + 1 < ce) {  // stage the next chunk while this one computes
       const int L1 = w.chunk_len[ci + 1], t01 = w.chunk_tok0[ci + 1];
       stage_chunk(sm.stage, io, H, h, t01, L1);
       bnext = tid < L1 ? bfl(braw[(size_t)(t01 + tid) * H + h]) : 0.f;
     }
-    factors(c, L, d.scale);
-    ap<true, SF>(c, sm.am, sm.pm, d.scale, (const bf16*)io.q, (const bf16*)io.k, H, h, t0, L);
+    factors_fwd(c, L, d.scale, QG, KD, XK);
+    ap<true, SF>(c, sm.am, nullptr, d.scale, (const bf16*)io.q, (const bf16*)io.k, H, h, t0, L, &P);
     solve<true>(sm.am, sm.tm, sm.yy, sm.bet);
-    wu<SF>(c, sm.tm, sm.ww, sm.ue);
+    for (int idx = tid; idx < C * C / 2; idx += NTH) {  // T -> split-bf16 operand (over A's storage)
+      const int r = idx / (C / 2), s2 = 2 * (idx % (C / 2));
+      op_store2(T, r, s2, sm.tm[r * SC + s2], sm.tm[r * SC + s2 + 1]);
+    }
+    __syncthreads();
+    {  // W | U = T [XK | XV]  (T lower block-triangular: k < 16 (I + 1))
+      const int I = warp & 3, half = warp >> 2;
+      if (half == 0) {
+        float aw[4][4], au[2][4];
+        zero(aw);
+        zero(au);
+        gemm3<2, false, true>(aw, T, 16 * I, 0, XK, 0, 0, I + 1);
+        gemm3<1, false, true>(au, T, 16 * I, 0, XV, 0, 0, I + 1);
+#pragma unroll
+        for (int jt = 0; jt < 4; jt++)
+#pragma unroll
+          for (int hh = 0; hh < 2; hh++)
+            op_store2(W, 16 * I + gq + 8 * hh, 8 * jt + 2 * tq, aw[jt][2 * hh], aw[jt][2 * hh + 1]);
+        each(au, [&](int m, int col, float& v) { sm.uf[(16 * I + m) * SV + col] = v; });
+      } else {
+        float au[6][4];
+        zero(au);
+        gemm3<3, false, true>(au, T, 16 * I, 0, XV, 16, 0, I + 1);
+        each(au, [&](int m, int col, float& v) { sm.uf[(16 * I + m) * SV + 16 + col] = v; });
+      }
+    }
+    __syncthreads();
     if (io.save)
       for (int idx = tid; idx < DK * DV; idx += NTH) {
         int i = idx / DV, j = idx % DV;
         w.Sent[ch * DK * DV + idx] = sm.ss[i * SV + j];
       }
-    {  // E = U - W S
+    {  // E = U - W S  (into XV's storage)
       const int I = warp & 3, half = warp >> 2;
       float acc[4][4];
       zero(acc);
-      rows16<4, SF>(acc, DK / 8, [&](int m, int k) { return sm.ww[(16 * I + m) * SQ + k]; },
-                [&](int k, int j, int n) { return sm.ss[k * SV + 32 * half + 8 * j + n]; });
-      each(acc, [&](int m, int col, float& v) { sm.ue[(16 * I + m) * SV + 32 * half + col] -= v; });
+      gemm3<2, false, true>(acc, W, 16 * I, 0, S, 32 * half, 0, DK / 16);
+#pragma unroll
+      for (int jt = 0; jt < 4; jt++)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+          const int r = 16 * I + gq + 8 * hh, col = 32 * half + 8 * jt + 2 * tq;
+          op_store2(E, r, col, sm.uf[r * SV + col] - acc[jt][2 * hh], sm.uf[r * SV + col + 1] - acc[jt][2 * hh + 1]);
+        }
     }
     __syncthreads();
     {  // O = QG S + P E  -> o
       const int I = warp & 3, half = warp >> 2;
       float acc[4][4];
       zero(acc);
-      rows16<4, SF>(acc, DK / 8, [&](int m, int k) { return sm.qg[(16 * I + m) * SQ + k]; },
-                [&](int k, int j, int n) { return sm.ss[k * SV + 32 * half + 8 * j + n]; });
-      rows16<4, SF>(acc, 2 * (I + 1), [&](int m, int k) { return sm.pm[(16 * I + m) * SC + k]; },
-                [&](int k, int j, int n) { return sm.ue[k * SV + 32 * half + 8 * j + n]; });
+      gemm3<2, false, true>(acc, QG, 16 * I, 0, S, 32 * half, 0, DK / 16);
+      gemm3<2, false, true>(acc, P, 16 * I, 0, E, 32 * half, 0, I + 1);
       bf16* o = (bf16*)io.o;
-      const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
 #pragma unroll
       for (int j = 0; j < 4; j++)
 #pragma unroll
@@ -418,39 +520,44 @@ __global__ void __launch_bounds__(NTH, 1) fwd_chain_kernel(Dims d, FwdIO io, Ws 
     const int mI = warp & 1, jq = warp >> 1;
     {  // S' = gamma S + KD^T E (registers until every reader of S is done)
       zero(snew);
-      rows16<2, SF>(snew, C / 8, [&](int m, int k) { return sm.kd[k * SX + 16 * mI + m]; },
-                [&](int k, int j, int n) { return sm.ue[k * SV + 16 * jq + 8 * j + n]; });
+      gemm3<1, true, true>(snew, KD, 16 * mI, 0, E, 16 * jq, 0, C / 16);
       each(snew, [&](int m, int col, float& v) {
         int i = 16 * mI + m;
         v += sm.gam[i] * sm.ss[i * SV + 16 * jq + col];
       });
     }
     if (io.save) {  // M = Diag(gamma) - KD^T W and QW = QG - P W for the backward scan
-      {
-        float acc[1][4];
+      if (warp < 4) {
+        const int jp = warp >> 1;
+        float acc[2][4];
         zero(acc);
-        const int j = warp >> 1;
-        rows16<1, SF>(acc, C / 8, [&](int m, int k) { return sm.kd[k * SX + 16 * mI + m]; },
-                  [&](int k, int jj, int n) { return sm.ww[k * SQ + 8 * j + n]; });
+        gemm3<1, true, true>(acc, KD, 16 * mI, 0, W, 16 * jp, 0, C / 16);
         each(acc, [&](int m, int col, float& v) {
-          int i = 16 * mI + m, jc = 8 * j + col;
+          int i = 16 * mI + m, jc = 16 * jp + col;
           w.M[ch * DK * DK + i * DK + jc] = (i == jc ? sm.gam[i] : 0.f) - v;
         });
       }
       {
-        const int I = warp & 3, half = warp >> 2;
+        const int I = warp & 3, jp = warp >> 2;
         float acc[2][4];
         zero(acc);
-        rows16<2, SF>(acc, 2 * (I + 1), [&](int m, int k) { return sm.pm[(16 * I + m) * SC + k]; },
-                  [&](int k, int j, int n) { return sm.ww[k * SQ + 16 * half + 8 * j + n]; });
+        gemm3<1, false, true>(acc, P, 16 * I, 0, W, 16 * jp, 0, I + 1);
         each(acc, [&](int m, int col, float& v) {
-          int r = 16 * I + m, jc = 16 * half + col;
-          w.QW[ch * C * DK + r * DK + jc] = sm.qg[r * SQ + jc] - v;
+          int r = 16 * I + m, jc = 16 * jp + col;
+          w.QW[ch * C * DK + r * DK + jc] = op_get(QG, r, jc) - v;
         });
       }
     }
     __syncthreads();
-    each(snew, [&](int m, int col, float& v) { sm.ss[(16 * mI + m) * SV + 16 * jq + col] = v; });
+#pragma unroll
+    for (int jt = 0; jt < 2; jt++)
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++) {
+        const int i = 16 * mI + gq + 8 * hh, col = 16 * jq + 8 * jt + 2 * tq;
+        sm.ss[i * SV + col] = snew[jt][2 * hh];
+        sm.ss[i * SV + col + 1] = snew[jt][2 * hh + 1];
+        op_store2(S, i, col, snew[jt][2 * hh], snew[jt][2 * hh + 1]);
+      }
     __syncthreads();
   }
   if (io.h_final)
@@ -529,17 +636,19 @@ __global__ void __launch_bounds__(128) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
 }
 
 // ------------------------------------------------------------ backward chunk
+// Shared memory of the chunk-gradient kernel.  Regions are reused as the
+// kernel proceeds (see the comments); bf16 arrays are split operand tiles.
 struct BwdSm {
-  float qh[C * SQ], kh[C * SQ], gg[C * SQ], lq[C * SQ], lk[C * SQ], rr[C * SQ], ww[C * SQ];
-  float kd[C * SX];
-  float uu[C * SV];
-  float am[C * SC], pm[C * SC], tm[C * SC];  // also the raw-input stage before ap()
-  float r1[C * SX + C * SV];                 // xk | xv, then dE (C*SV) | dW (C*SQ)
-  float ss[DK * SV], dsn[DK * SV];           // S, dS'; later YU [C][SV]
-  float e2[C * SV];                          // solve scratch, then E, then YW [C][SQ]
-  bf16 dOs[C * SO];
-  bf16 fr[C * DK];
-  float tot[NW * DK], part[NW * DK];
+  float qh[C * SQ], kh[C * SQ], gg[C * SQ];  // q^, k^, G
+  float lq[C * SQ], lk[C * SQ], rr[C * SQ];  // decay-ratio factors; later dq^, dk^, dG
+  float am[C * SC];   // A' (fp32), then MA = beta dA in place, then scratch
+  float tm[C * SC];   // T (fp32), then dP' (fp32), then scratch
+  bf16 ra[12288];     // raw-input stage | XK (4096) + XV (8192) | E (8192) + dW (4096) | YU over E
+  bf16 rb[8192];      // P' | dE
+  bf16 oT[8192], oU[8192], oW[4096], oKD[4096];
+  bf16 oS[4096], odS[4096], odO[4096];  // S, dS' (split); dO (exact); later YW over S
+  bf16 fr[C * DK];    // raw f
+  float tot[NW * DK], part[NW * DK], ks[NW * DK];
   float bet[C], inq[C], ink[C], braw[C], dbet[C];
   float gl[DK], gam[DK], dgam[DK], gb[4 * DK], ge[4 * DK], dd[6 * DK], ei[4 * DK];
   float red[NW];
@@ -559,33 +668,40 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
   const int64_t ch = (int64_t)j * H + h;
   const float a = expf(io.A_log[h]), scale = d.scale;
   const float* dtb = io.dt_bias + h * DK;
-  float* xk = sm.r1;
-  float* xv = sm.r1 + C * SX;
-  Intra c{sm.qh, sm.kh, sm.gg, sm.lq, sm.lk, sm.rr, sm.kd, xk, xv, nullptr, sm.bet, sm.inq, sm.ink,
+  Intra c{sm.qh, sm.kh, sm.gg, sm.lq, sm.lk, sm.rr, nullptr, nullptr, nullptr, nullptr, sm.bet, sm.inq, sm.ink,
           sm.braw, sm.gl, sm.gam, sm.gb, sm.ge, sm.dd, sm.ei, sm.tot, sm.spanok};
-  bf16* st = reinterpret_cast<bf16*>(sm.am);
+  bf16* st = sm.ra;
+  const Op XK{sm.ra, sm.ra + 2048, DK}, XV{sm.ra + 4096, sm.ra + 8192, DV};
+  const Op E{sm.ra, sm.ra + 4096, DV}, dW{sm.ra + 8192, sm.ra + 10240, DK}, YU = E;
+  const Op P{sm.rb, sm.rb + 4096, C}, dE{sm.rb, sm.rb + 4096, DV};
+  const Op T{sm.oT, sm.oT + 4096, C}, U{sm.oU, sm.oU + 4096, DV}, W{sm.oW, sm.oW + 2048, DK};
+  const Op KD{sm.oKD, sm.oKD + 2048, DK}, S{sm.oS, sm.oS + 2048, DV}, dS{sm.odS, sm.odS + 2048, DV};
+  const Op dO{sm.odO, nullptr, DV}, YW{sm.oS, sm.oS + 2048, DK};
+  const Op noQG{nullptr, nullptr, DK};
 
-  // ---- stage raw inputs, dO, S and dS'
+  // ---- stage raw inputs (cp.async), dO into its operand tile, S and dS' split
   {
     FwdIO fio{io.q, io.k, io.v, io.f, io.b, io.A_log, io.dt_bias, nullptr, nullptr, nullptr, 0};
     stage_chunk(st, fio, H, h, t0, L);
-    const bf16* dO = (const bf16*)io.dO;
+    const bf16* dOg = (const bf16*)io.dO;
     for (int idx = tid; idx < C * 8; idx += NTH) {
       int r = idx >> 3, p = idx & 7;
-      if (r < L) cp16(sm.dOs + r * SO + p * 8, dO + ((size_t)(t0 + r) * H + h) * DV + p * 8);
-    }
-    const float* Sg = w.Sent + ch * DK * DV;
-    const float* dSg = w.dSn + ch * DK * DV;
-    for (int idx = tid; idx < DK * 16; idx += NTH) {  // 16 x 16 B per fp32 row of dv = 64
-      int i = idx >> 4, p = idx & 15;
-      cp16(sm.ss + i * SV + p * 4, Sg + i * DV + p * 4);
-      cp16(sm.dsn + i * SV + p * 4, dSg + i * DV + p * 4);
+      bf16* dst = sm.odO + opix(r, 8 * p, DV);
+      if (r < L) cp16(dst, dOg + ((size_t)(t0 + r) * H + h) * DV + p * 8);
+      else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
     }
     cp_commit();
+    const float* Sg = w.Sent + ch * DK * DV;
+    const float* dSg = w.dSn + ch * DK * DV;
+    for (int idx = tid; idx < DK * DV / 2; idx += NTH) {
+      const int i = idx / (DV / 2), jc = 2 * (idx % (DV / 2));
+      const float2 sv = *reinterpret_cast<const float2*>(Sg + i * DV + jc);
+      const float2 dv2 = *reinterpret_cast<const float2*>(dSg + i * DV + jc);
+      op_store2(S, i, jc, sv.x, sv.y);
+      op_store2(dS, i, jc, dv2.x, dv2.y);
+    }
     if (tid < C) sm.braw[tid] = tid < L ? bfl(((const bf16*)io.b)[(size_t)(t0 + tid) * H + h]) : 0.f;
     if (tid < C) sm.dbet[tid] = 0.f;
-    for (int idx = tid; idx < C * DV; idx += NTH)
-      if (idx / DV >= L) sm.dOs[(idx / DV) * SO + idx % DV] = __float2bfloat16_rn(0.f);
     cp_wait_all();
     __syncthreads();
     for (int idx = tid; idx < C * DK; idx += NTH) sm.fr[idx] = st[2 * C * DK + idx];
@@ -593,87 +709,130 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
   // ---- recompute the chunk (same arithmetic as the forward)
   uint4 vraw[2];  // this thread's raw v (row tid / 4, columns 16 (tid % 4) ..), kept for dbeta
   prologue(c, st, L, a, dtb, vraw);
-  factors(c, L, scale);
-  ap<false, SR>(c, sm.am, sm.pm, 1.f, (const bf16*)io.q, (const bf16*)io.k, H, h, t0, L);
-  solve<false>(sm.am, sm.tm, sm.e2, sm.bet);
-  wu<SR>(c, sm.tm, sm.ww, sm.uu);
-
-  float* dE = sm.r1;            // [C][SV]
-  float* dW = sm.r1 + C * SV;   // [C][SQ]
-  float* E = sm.e2;             // [C][SV]
-  float* YU = sm.ss;            // [C][SV] over ss | dsn
-  float* YW = sm.e2;            // [C][SQ]
-  auto dO = [&](int r, int col) { return bfl(sm.dOs[r * SO + col]); };
-  const int I = warp & 3, hk = warp >> 2;  // owner tile: rows 16I.., key columns 16hk..
-
-  // ---- dE = scale P'^T dO + KD dS'  and  E = U - W S
-  {
-    float acc[4][4], acc2[4][4];
-    zero(acc);
-    zero(acc2);
-    const int half = warp >> 2;
-    rows16<4, SB, false, true>(acc, 2 * (4 - I), [&](int m, int k) { return sm.pm[(16 * I + k) * SC + 16 * I + m]; },
-              [&](int k, int jj, int n) { return dO(16 * I + k, 32 * half + 8 * jj + n); });
-    rows16<4, SB>(acc2, DK / 8, [&](int m, int k) { return sm.kd[(16 * I + m) * SX + k]; },
-              [&](int k, int jj, int n) { return sm.dsn[k * SV + 32 * half + 8 * jj + n]; });
-    each(acc, [&](int m, int col, float& v) { v = scale * v; });
-    float accE[4][4];
-    zero(accE);
-    rows16<4, SB>(accE, DK / 8, [&](int m, int k) { return sm.ww[(16 * I + m) * SQ + k]; },
-              [&](int k, int jj, int n) { return sm.ss[k * SV + 32 * half + 8 * jj + n]; });
+  {  // beta v -> XV (over the consumed stage)
+    const int r = tid >> 2, q4 = tid & 3;
+    const float br = r < L ? sm.bet[r] : 0.f;
+    float vv[16];
+    unpack8(vraw[0], vv);
+    unpack8(vraw[1], vv + 8);
 #pragma unroll
-    for (int jj = 0; jj < 4; jj++)
-#pragma unroll
-      for (int e = 0; e < 4; e++) {
-        int r = 16 * I + gq + 8 * (e >> 1), col = 32 * half + 8 * jj + 2 * tq + (e & 1);
-        dE[r * SV + col] = acc[jj][e] + acc2[jj][e];
-        E[r * SV + col] = sm.uu[r * SV + col] - accE[jj][e];
-      }
+    for (int e = 0; e < 16; e += 2) op_store2(XV, r, 16 * q4 + e, br * vv[e], br * vv[e + 1]);
+  }
+  factors_fwd(c, L, scale, noQG, KD, XK);
+  ap<false, SR>(c, sm.am, nullptr, 1.f, (const bf16*)io.q, (const bf16*)io.k, H, h, t0, L, &P);
+  solve<false>(sm.am, sm.tm, reinterpret_cast<float*>(sm.oU), sm.bet);
+  for (int idx = tid; idx < C * C / 2; idx += NTH) {  // T -> split-bf16 operand
+    const int r = idx / (C / 2), s2 = 2 * (idx % (C / 2));
+    op_store2(T, r, s2, sm.tm[r * SC + s2], sm.tm[r * SC + s2 + 1]);
   }
   __syncthreads();
-  // ---- dP' = scale dO E^T (inclusive lower, into pm), dKD = E dS'^T, dQG = scale dO S^T (registers),
-  //      dgamma = rowsum(dS' .* S), dW = -dE S^T
+  {  // W | U = T [XK | XV]
+    const int I = warp & 3, half = warp >> 2;
+    if (half == 0) {
+      float aw[4][4], au[2][4];
+      zero(aw);
+      zero(au);
+      gemm3<2, false, true>(aw, T, 16 * I, 0, XK, 0, 0, I + 1);
+      gemm3<1, false, true>(au, T, 16 * I, 0, XV, 0, 0, I + 1);
+#pragma unroll
+      for (int jt = 0; jt < 4; jt++)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++)
+          op_store2(W, 16 * I + gq + 8 * hh, 8 * jt + 2 * tq, aw[jt][2 * hh], aw[jt][2 * hh + 1]);
+#pragma unroll
+      for (int jt = 0; jt < 2; jt++)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++)
+          op_store2(U, 16 * I + gq + 8 * hh, 8 * jt + 2 * tq, au[jt][2 * hh], au[jt][2 * hh + 1]);
+    } else {
+      float au[6][4];
+      zero(au);
+      gemm3<3, false, true>(au, T, 16 * I, 0, XV, 16, 0, I + 1);
+#pragma unroll
+      for (int jt = 0; jt < 6; jt++)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++)
+          op_store2(U, 16 * I + gq + 8 * hh, 16 + 8 * jt + 2 * tq, au[jt][2 * hh], au[jt][2 * hh + 1]);
+    }
+  }
+  __syncthreads();
+
+  const int I = warp & 3, hk = warp >> 2;  // owner tile: rows 16I.., key columns 16hk..
+  // ---- dE = scale P'^T dO + KD dS' (in registers: P' shares its storage)
+  //      and E = U - W S (over XK / XV)
+  float dEr[4][4];
+  {
+    const int half = warp >> 2;
+    float acc[4][4], acc2[4][4], accE[4][4];
+    zero(acc);
+    zero(acc2);
+    zero(accE);
+    gemm3<2, true, true>(acc, P, 16 * I, 16 * I, dO, 32 * half, 16 * I, 4 - I);
+    gemm3<2, false, true>(acc2, KD, 16 * I, 0, dS, 32 * half, 0, DK / 16);
+    gemm3<2, false, true>(accE, W, 16 * I, 0, S, 32 * half, 0, DK / 16);
+#pragma unroll
+    for (int jt = 0; jt < 4; jt++)
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++) {
+        const int r = 16 * I + gq + 8 * hh, col = 32 * half + 8 * jt + 2 * tq;
+        dEr[jt][2 * hh] = scale * acc[jt][2 * hh] + acc2[jt][2 * hh];
+        dEr[jt][2 * hh + 1] = scale * acc[jt][2 * hh + 1] + acc2[jt][2 * hh + 1];
+        op_store2(E, r, col, op_get(U, r, col) - accE[jt][2 * hh], op_get(U, r, col + 1) - accE[jt][2 * hh + 1]);
+      }
+  }
+  __syncthreads();  // P' fully read
+  {
+    const int half = warp >> 2;
+#pragma unroll
+    for (int jt = 0; jt < 4; jt++)
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++)
+        op_store2(dE, 16 * I + gq + 8 * hh, 32 * half + 8 * jt + 2 * tq, dEr[jt][2 * hh], dEr[jt][2 * hh + 1]);
+  }
+  __syncthreads();
+  // ---- dP' = scale dO E^T (inclusive lower, fp32 over T), dKD = E dS'^T,
+  //      dQG = scale dO S^T (registers), dgamma = rowsum(dS' .* S), dW = -dE S^T
   float dKD[2][4], dQG[2][4];
+  float* DP = sm.tm;
   {
     zero(dKD);
     zero(dQG);
-    rows16<2, SB>(dKD, DV / 8, [&](int m, int k) { return E[(16 * I + m) * SV + k]; },
-              [&](int k, int jj, int n) { return sm.dsn[(16 * hk + 8 * jj + n) * SV + k]; });
-    rows16<2, SB, true>(dQG, DV / 8, [&](int m, int k) { return dO(16 * I + m, k); },
-              [&](int k, int jj, int n) { return sm.ss[(16 * hk + 8 * jj + n) * SV + k]; });
+    gemm3<1, false, false>(dKD, E, 16 * I, 0, dS, 16 * hk, 0, DV / 16);
+    gemm3<1, false, false>(dQG, dO, 16 * I, 0, S, 16 * hk, 0, DV / 16);
     each(dQG, [&](int m, int col, float& v) { v *= scale; });
     float acc[2][4];
     zero(acc);
-    rows16<2, SB>(acc, DV / 8, [&](int m, int k) { return dE[(16 * I + m) * SV + k]; },
-              [&](int k, int jj, int n) { return sm.ss[(16 * hk + 8 * jj + n) * SV + k]; });
-    each(acc, [&](int m, int col, float& v) { dW[(16 * I + m) * SQ + 16 * hk + col] = -v; });
+    gemm3<1, false, false>(acc, dE, 16 * I, 0, S, 16 * hk, 0, DV / 16);
+#pragma unroll
+    for (int jt = 0; jt < 2; jt++)
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++)
+        op_store2(dW, 16 * I + gq + 8 * hh, 16 * hk + 8 * jt + 2 * tq, -acc[jt][2 * hh], -acc[jt][2 * hh + 1]);
     for (int t = warp; t < 10; t += NW) {  // lower 16x16 blocks of dP'
       const int bI = t < 1 ? 0 : t < 3 ? 1 : t < 6 ? 2 : 3, bJ = t - bI * (bI + 1) / 2;
       float pp[2][4];
       zero(pp);
-      rows16<2, SB, true>(pp, DV / 8, [&](int m, int k) { return dO(16 * bI + m, k); },
-                [&](int k, int jj, int n) { return E[(16 * bJ + 8 * jj + n) * SV + k]; });
+      gemm3<1, false, false>(pp, dO, 16 * bI, 0, E, 16 * bJ, 0, DV / 16);
       each(pp, [&](int m, int n, float& v) {
-        int r = 16 * bI + m, s = 16 * bJ + n;
-        sm.pm[r * SC + s] = s <= r ? scale * v : 0.f;
+        int r = 16 * bI + m, s2 = 16 * bJ + n;
+        DP[r * SC + s2] = s2 <= r ? scale * v : 0.f;
       });
     }
     if (tid < DK) {
       float acc1 = 0.f;
-      for (int jj = 0; jj < DV; jj++) acc1 += sm.dsn[tid * SV + jj] * sm.ss[tid * SV + jj];
+      for (int jj = 0; jj < DV; jj++) acc1 += op_get(dS, tid, jj) * op_get(S, tid, jj);
       sm.dgam[tid] = acc1;
     }
   }
   __syncthreads();
-  // ---- YU = T^T dE (registers), YW = T^T dW (registers)
+  // ---- YU = T^T dE, YW = T^T dW (registers); then YU over E, YW over S
   float yu[4][4], yw[2][4];
   {
     const int half = warp >> 2;
     zero(yu);
     zero(yw);
-    auto Tt = [&](int m, int k) { return sm.tm[(16 * I + k) * SC + 16 * I + m]; };  // rows r >= 16 I
-    rows16<4, SB>(yu, 2 * (4 - I), Tt, [&](int k, int jj, int n) { return dE[(16 * I + k) * SV + 32 * half + 8 * jj + n]; });
-    rows16<2, SB>(yw, 2 * (4 - I), Tt, [&](int k, int jj, int n) { return dW[(16 * I + k) * SQ + 16 * hk + 8 * jj + n]; });
+    gemm3<2, true, true>(yu, T, 16 * I, 16 * I, dE, 32 * half, 16 * I, 4 - I);
+    gemm3<1, true, true>(yw, T, 16 * I, 16 * I, dW, 16 * hk, 16 * I, 4 - I);
   }
   __syncthreads();
   {  // store YU, YW; dv = beta YU
@@ -684,16 +843,20 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
 #pragma unroll
       for (int hh = 0; hh < 2; hh++) {
         int r = 16 * I + gq + 8 * hh, col = 32 * half + 8 * jj + 2 * tq;
-        YU[r * SV + col] = yu[jj][2 * hh];
-        YU[r * SV + col + 1] = yu[jj][2 * hh + 1];
+        op_store2(YU, r, col, yu[jj][2 * hh], yu[jj][2 * hh + 1]);
         if (r < L)
           *reinterpret_cast<__nv_bfloat162*>(dvo + ((size_t)(t0 + r) * H + h) * DV + col) =
               __floats2bfloat162_rn(sm.bet[r] * yu[jj][2 * hh], sm.bet[r] * yu[jj][2 * hh + 1]);
       }
-    each(yw, [&](int m, int col, float& v) { YW[(16 * I + m) * SQ + 16 * hk + col] = v; });
+#pragma unroll
+    for (int jj = 0; jj < 2; jj++)
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++)
+        op_store2(YW, 16 * I + gq + 8 * hh, 16 * hk + 8 * jj + 2 * tq, yw[jj][2 * hh], yw[jj][2 * hh + 1]);
   }
   __syncthreads();
-  // ---- dbeta (U and W terms), dA = -(YU U^T + YW W^T) strict lower (into tm)
+  // ---- dbeta (U and W terms); dA = -(YU U^T + YW W^T) strict lower, fused with
+  //      dbeta += rowsum(dA .* A') and MA = beta_r dA (in place of A')
   {
     {  // thread: row tid / 4, value columns 16 (tid % 4) .., key channels 8 (tid % 4) ..
       const int r = tid >> 2, q4 = tid & 3;
@@ -702,11 +865,11 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
       unpack8(vraw[1], vv + 8);
       float acc = 0.f;
 #pragma unroll
-      for (int e = 0; e < 16; e++) acc += YU[r * SV + 16 * q4 + e] * vv[e];
+      for (int e = 0; e < 16; e++) acc += op_get(YU, r, 16 * q4 + e) * vv[e];
 #pragma unroll
       for (int e = 0; e < 8; e++) {
         const int i = 8 * q4 + e;
-        acc += YW[r * SQ + i] * sm.kh[r * SQ + i] * expf(sm.gg[r * SQ + i]);
+        acc += op_get(YW, r, i) * sm.kh[r * SQ + i] * expf(sm.gg[r * SQ + i]);
       }
       acc += __shfl_xor_sync(0xffffffffu, acc, 1);
       acc += __shfl_xor_sync(0xffffffffu, acc, 2);
@@ -716,18 +879,15 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
       const int bI = t < 1 ? 0 : t < 3 ? 1 : t < 6 ? 2 : 3, bJ = t - bI * (bI + 1) / 2;
       float aa[2][4];
       zero(aa);
-      rows16<2, SB>(aa, DV / 8, [&](int m, int k) { return YU[(16 * bI + m) * SV + k]; },
-                [&](int k, int jj, int n) { return sm.uu[(16 * bJ + 8 * jj + n) * SV + k]; });
-      rows16<2, SB>(aa, DK / 8, [&](int m, int k) { return YW[(16 * bI + m) * SQ + k]; },
-                [&](int k, int jj, int n) { return sm.ww[(16 * bJ + 8 * jj + n) * SQ + k]; });
-      // dA = -aa (strict lower); its row sums against A' feed dbeta; MA = beta_r dA
+      gemm3<1, false, false>(aa, YU, 16 * bI, 0, U, 16 * bJ, 0, DV / 16);
+      gemm3<1, false, false>(aa, YW, 16 * bI, 0, W, 16 * bJ, 0, DK / 16);
       float rs0 = 0.f, rs1 = 0.f;
       each(aa, [&](int m, int n, float& v) {
-        const int r = 16 * bI + m, s = 16 * bJ + n;
-        const float da = s < r ? -v : 0.f;
-        const float pa = da * sm.am[r * SC + s];
+        const int r = 16 * bI + m, s2 = 16 * bJ + n;
+        const float da = s2 < r ? -v : 0.f;
+        const float pa = da * sm.am[r * SC + s2];
         if (m < 8) rs0 += pa; else rs1 += pa;
-        sm.tm[r * SC + s] = sm.bet[r] * da;
+        sm.am[r * SC + s2] = sm.bet[r] * da;
       });
       rs0 += __shfl_xor_sync(0xffffffffu, rs0, 1);
       rs0 += __shfl_xor_sync(0xffffffffu, rs0, 2);
@@ -746,6 +906,7 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
     sm.dbet[tid] += acc;
   }
   __syncthreads();
+  float* MA = sm.am;
   // ---- pairwise decay-ratio terms (owner tile rows 16I.., key columns 16hk..).
   // Row and column sums of the same pair enter dG with opposite signs and
   // must cancel in the cumulative sum, so these products keep ~21 bits.
@@ -759,16 +920,16 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
       if (J == I && !ok) break;
       const float* scl = J < I ? sm.dd + pidx(I, J) * DK : sm.ei + I * DK;
       auto fbR = [&](int k, int jj, int n) { return sm.rr[(16 * J + k) * SQ + 16 * hk + 8 * jj + n] * scl[16 * hk + 8 * jj + n]; };
-      rows16<2, true>(prow, 2, [&](int m, int k) { return sm.pm[(16 * I + m) * SC + 16 * J + k]; }, fbR);
-      rows16<2, true>(arow, 2, [&](int m, int k) { return sm.tm[(16 * I + m) * SC + 16 * J + k]; }, fbR);
+      rows16<2, true>(prow, 2, [&](int m, int k) { return DP[(16 * I + m) * SC + 16 * J + k]; }, fbR);
+      rows16<2, true>(arow, 2, [&](int m, int k) { return MA[(16 * I + m) * SC + 16 * J + k]; }, fbR);
     }
     // col terms of columns s in block I: rows r in blocks I2 >= I
     for (int I2 = I; I2 < 4; I2++) {
       if (I2 == I && !ok) continue;
       const float* scl = I2 > I ? sm.dd + pidx(I2, I) * DK : sm.ei + I * DK;
-      rows16<2, true>(col, 2, [&](int m, int k) { return sm.pm[(16 * I2 + k) * SC + 16 * I + m]; },
+      rows16<2, true>(col, 2, [&](int m, int k) { return DP[(16 * I2 + k) * SC + 16 * I + m]; },
                 [&](int k, int jj, int n) { return sm.lq[(16 * I2 + k) * SQ + 16 * hk + 8 * jj + n] * scl[16 * hk + 8 * jj + n]; });
-      rows16<2, true>(col, 2, [&](int m, int k) { return sm.tm[(16 * I2 + k) * SC + 16 * I + m]; },
+      rows16<2, true>(col, 2, [&](int m, int k) { return MA[(16 * I2 + k) * SC + 16 * I + m]; },
                 [&](int k, int jj, int n) { return sm.lk[(16 * I2 + k) * SQ + 16 * hk + 8 * jj + n] * scl[16 * hk + 8 * jj + n]; });
     }
   }
@@ -793,12 +954,12 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
             float qs = bfl(qg_[((size_t)(t0 + s) * H + h) * DK + i]) * sm.inq[s];
             if (s <= r) {
               float ex = expf(Gr[i] - sm.gg[s * SQ + i]);
-              pr += sm.pm[r * SC + s] * ks * ex;
-              ar += sm.tm[r * SC + s] * ks * ex;
+              pr += DP[r * SC + s] * ks * ex;
+              ar += MA[r * SC + s] * ks * ex;
             }
             if (s >= r) {
               float ex = expf(sm.gg[s * SQ + i] - Gr[i]);
-              cl += (sm.pm[s * SC + r] * qs + sm.tm[s * SC + r] * ks) * ex;
+              cl += (DP[s * SC + r] * qs + MA[s * SC + r] * ks) * ex;
             }
           }
         }
@@ -811,11 +972,12 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
         kdt[jj][e] = dKD[jj][e] * k * kdf;
       }
   }
-  __syncthreads();  // everyone is done reading lq, lk, rr, pm, tm
+  __syncthreads();  // everyone is done reading lq, lk, rr, dP', MA
   float* dqs = sm.lq;
   float* dks = sm.lk;
   float* dGs = sm.rr;
-  float* kdts = sm.ww;
+  float* kdts = sm.tm;  // [C][SQ] over dP'
+  float* sfx = sm.am;   // local suffix sums [C][SC] over MA
 #pragma unroll
   for (int jj = 0; jj < 2; jj++)
 #pragma unroll
@@ -837,22 +999,22 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
         run += dGs[r * SQ + lane] - kdts[r * SQ + lane];
         ksum += kdts[r * SQ + lane];
       }
-      sm.tm[r * SC + lane] = run;  // local suffix sums (tm is free now)
+      sfx[r * SC + lane] = run;
     }
     sm.tot[warp * DK + lane] = run;
-    sm.e2[warp * DK + lane] = ksum;
+    sm.ks[warp * DK + lane] = ksum;
   }
   __syncthreads();
   {
     float off = sm.dgam[lane] * sm.gam[lane];
-    for (int w2 = 0; w2 < NW; w2++) off += sm.e2[w2 * DK + lane];   // sum_r kdt_r
+    for (int w2 = 0; w2 < NW; w2++) off += sm.ks[w2 * DK + lane];   // sum_r kdt_r
     for (int w2 = warp + 1; w2 < NW; w2++) off += sm.tot[w2 * DK + lane];
     bf16* dfo = (bf16*)io.df;
     float pdt = 0.f, pA = 0.f;
     for (int m = 0; m < 8; m++) {
       int r = 8 * warp + m;
       if (r < L) {
-        float dg = sm.tm[r * SC + lane] + off;
+        float dg = sfx[r * SC + lane] + off;
         float x = bfl(sm.fr[r * DK + lane]) + dtb[lane];
         float g = -a * softplus_f(x);
         float dx = dg * (-a) * sigmoid_f(x);

@@ -3,6 +3,7 @@
 #pragma once
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <cuda_bf16.h>
 
 namespace kda {
 namespace mma {
@@ -73,6 +74,108 @@ __device__ __forceinline__ void each(float (&acc)[NT][4], F fn) {
   for (int j = 0; j < NT; j++)
 #pragma unroll
     for (int e = 0; e < 4; e++) fn(gq + 8 * (e >> 1), j * 8 + 2 * tq + (e & 1), acc[j][e]);
+}
+
+// ------------------------------------------------------------ bf16 split operands
+// An operand tile of R rows x K columns (K a multiple of 8) kept as two bf16
+// arrays, hi = RN(x) and lo = RN(x - hi), in the canonical K-major core-matrix
+// layout: 8 rows x 8 elements per 128-byte core matrix, core (rb, kb) at
+// index rb * (K / 8) + kb.  The same storage serves an operand and its
+// transpose (ldmatrix with and without .trans).  lo == nullptr marks a tile
+// whose values are exact in bf16 (its remainder is zero).
+struct Op {
+  __nv_bfloat16* hi;
+  __nv_bfloat16* lo;
+  int K;
+};
+
+__device__ __forceinline__ int opix(int r, int k, int K) {
+  return ((((r >> 3) * (K >> 3)) + (k >> 3)) << 6) + ((r & 7) << 3) + (k & 7);
+}
+
+__device__ __forceinline__ void op_store2(const Op& o, int r, int k, float x0, float x1) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const int i = opix(r, k, o.K);
+  *reinterpret_cast<__nv_bfloat162*>(o.hi + i) = h;
+  if (o.lo) *reinterpret_cast<__nv_bfloat162*>(o.lo + i) = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+}
+
+__device__ __forceinline__ void op_store1(const Op& o, int r, int k, float x) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  const int i = opix(r, k, o.K);
+  o.hi[i] = h;
+  if (o.lo) o.lo[i] = __float2bfloat16_rn(x - __bfloat162float(h));
+}
+
+__device__ __forceinline__ float op_get(const Op& o, int r, int k) {
+  const int i = opix(r, k, o.K);
+  return __bfloat162float(o.hi[i]) + (o.lo ? __bfloat162float(o.lo[i]) : 0.f);
+}
+
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], const void* p) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+}
+__device__ __forceinline__ void ldsm4t(uint32_t (&r)[4], const void* p) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// A fragment (16 x 16) at logical A(m0.., k0..).  AT: A(m, k) = X[k][m].
+template <bool AT>
+__device__ __forceinline__ void frag_a(uint32_t (&r)[4], const __nv_bfloat16* X, int K, int m0, int k0) {
+  const int lane = threadIdx.x & 31, mi = lane >> 3, l7 = lane & 7;
+  if (!AT) ldsm4(r, X + opix(m0 + l7 + 8 * (mi & 1), k0 + 8 * (mi >> 1), K));
+  else ldsm4t(r, X + opix(k0 + l7 + 8 * (mi >> 1), m0 + 8 * (mi & 1), K));
+}
+
+// B fragments (16 x 16: two n8 tiles) at logical B(k0.., n0..).  BT: B(k, n) = X[k][n],
+// else B(k, n) = X[n][k].  r[0..1] feed tile n0, r[2..3] tile n0 + 8.
+template <bool BT>
+__device__ __forceinline__ void frag_b(uint32_t (&r)[4], const __nv_bfloat16* X, int K, int k0, int n0) {
+  const int lane = threadIdx.x & 31, mi = lane >> 3, l7 = lane & 7;
+  if (!BT) ldsm4(r, X + opix(n0 + l7 + 8 * (mi >> 1), k0 + 8 * (mi & 1), K));
+  else ldsm4t(r, X + opix(k0 + l7 + 8 * (mi & 1), n0 + 8 * (mi >> 1), K));
+}
+
+// acc[2p + t] (16 x 8 tiles, columns n0 + 16 p + 8 t) += A(m0.., k) B(k, n0..)
+// over ksteps blocks of 16 along k (A from ka0, B from kb0), with each
+// operand split into bf16 hi + lo and hi*hi + hi*lo + lo*hi accumulated
+// (about 16 significant bits).  An operand whose lo is null is exact.
+template <int NP, bool AT, bool BT>
+__device__ __forceinline__ void gemm3(float (&acc)[2 * NP][4], const Op& A, int m0, int ka0, const Op& B, int n0,
+                                      int kb0, int ksteps) {
+  for (int ks = 0; ks < ksteps; ks++) {
+    uint32_t ah[4], al[4];
+    frag_a<AT>(ah, A.hi, A.K, m0, ka0 + 16 * ks);
+    if (A.lo) frag_a<AT>(al, A.lo, A.K, m0, ka0 + 16 * ks);
+#pragma unroll
+    for (int p = 0; p < NP; p++) {
+      uint32_t bh[4], bl[4];
+      frag_b<BT>(bh, B.hi, B.K, kb0 + 16 * ks, n0 + 16 * p);
+      mma_bf16(acc[2 * p], ah, bh[0], bh[1]);
+      mma_bf16(acc[2 * p + 1], ah, bh[2], bh[3]);
+      if (B.lo) {
+        frag_b<BT>(bl, B.lo, B.K, kb0 + 16 * ks, n0 + 16 * p);
+        mma_bf16(acc[2 * p], ah, bl[0], bl[1]);
+        mma_bf16(acc[2 * p + 1], ah, bl[2], bl[3]);
+      }
+      if (A.lo) {
+        mma_bf16(acc[2 * p], al, bh[0], bh[1]);
+        mma_bf16(acc[2 * p + 1], al, bh[2], bh[3]);
+      }
+    }
+  }
 }
 
 // ------------------------------------------------------------ cp.async
