@@ -691,20 +691,24 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
       else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
     }
     cp_commit();
-    const float* Sg = w.Sent + ch * DK * DV;
-    const float* dSg = w.dSn + ch * DK * DV;
-    for (int idx = tid; idx < DK * DV / 2; idx += NTH) {
-      const int i = idx / (DV / 2), jc = 2 * (idx % (DV / 2));
-      const float2 sv = *reinterpret_cast<const float2*>(Sg + i * DV + jc);
-      const float2 dv2 = *reinterpret_cast<const float2*>(dSg + i * DV + jc);
-      op_store2(S, i, jc, sv.x, sv.y);
-      op_store2(dS, i, jc, dv2.x, dv2.y);
-    }
     if (tid < C) sm.braw[tid] = tid < L ? bfl(((const bf16*)io.b)[(size_t)(t0 + tid) * H + h]) : 0.f;
     if (tid < C) sm.dbet[tid] = 0.f;
-    cp_wait_all();
+    asm volatile("cp.async.wait_group 1;\n" ::);  // q, k, f, v landed; dO may still be in flight
     __syncthreads();
     for (int idx = tid; idx < C * DK; idx += NTH) sm.fr[idx] = st[2 * C * DK + idx];
+  }
+  // S and dS' are read into registers now and split into operand tiles after
+  // the recomputation, so that their latency overlaps it
+  float2 sreg[DK * DV / 2 / NTH], dsreg[DK * DV / 2 / NTH];
+  {
+    const float* Sg = w.Sent + ch * DK * DV;
+    const float* dSg = w.dSn + ch * DK * DV;
+#pragma unroll
+    for (int u = 0; u < DK * DV / 2 / NTH; u++) {
+      const int idx = tid + u * NTH, i = idx / (DV / 2), jc = 2 * (idx % (DV / 2));
+      sreg[u] = *reinterpret_cast<const float2*>(Sg + i * DV + jc);
+      dsreg[u] = *reinterpret_cast<const float2*>(dSg + i * DV + jc);
+    }
   }
   // ---- recompute the chunk (same arithmetic as the forward)
   uint4 vraw[2];  // this thread's raw v (row tid / 4, columns 16 (tid % 4) ..), kept for dbeta
@@ -755,6 +759,15 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
           op_store2(U, 16 * I + gq + 8 * hh, 16 + 8 * jt + 2 * tq, au[jt][2 * hh], au[jt][2 * hh + 1]);
     }
   }
+  __syncthreads();
+
+#pragma unroll
+  for (int u = 0; u < DK * DV / 2 / NTH; u++) {
+    const int idx = tid + u * NTH, i = idx / (DV / 2), jc = 2 * (idx % (DV / 2));
+    op_store2(S, i, jc, sreg[u].x, sreg[u].y);
+    op_store2(dS, i, jc, dsreg[u].x, dsreg[u].y);
+  }
+  cp_wait_all();  // dO
   __syncthreads();
 
   const int I = warp & 3, hk = warp >> 2;  // owner tile: rows 16I.., key columns 16hk..
