@@ -53,6 +53,8 @@ def algorithmic_bytes(w, kernel: str) -> float:
     grads = e * (3 * dk + dv + 1)               # dq, dk, df, dv, db
     per = {
         "fwd_chain": inputs_fwd + e * dv,       # reads q, k, f, v, b; writes o
+        "fwd_chunk": inputs_fwd,                # reads q, k, f, v, b
+        "fwd_state": e * dv,                    # writes o
         "fwd_intra": inputs_fwd,
         "fwd_scan": e * dv,                     # o
         "bwd_scan": e * dv,                     # dO

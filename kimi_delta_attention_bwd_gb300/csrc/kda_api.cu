@@ -125,16 +125,17 @@ static size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 struct Layout {
   size_t total;
   size_t off_err, off_nch, off_dc0, off_ct0, off_cl, off_cd;
-  size_t off_W, off_U, off_P, off_QG, off_KD, off_gam, off_Sent, off_M, off_QW;
+  size_t off_W, off_U, off_P, off_QG, off_KD, off_gam, off_Sent, off_M, off_QW, off_KU, off_PU;
   size_t off_dE, off_dSn, off_pA, off_pdt, off_scr;
 };
 
 // Workspace layout.  Both paths start with the error word, the saved-problem
-// tag and the chunk table.  The tensor-core path (d.fast) keeps only the
-// per-chunk entry states, M and QW for the backward, and the backward's
-// state gradients and parameter-gradient partials; the general path also
-// keeps its fp32 intra-chunk factors and scratch.
-static Layout layout(const Dims& d, int for_bwd) {
+// tag and the chunk table.  The tensor-core path (d.fast) keeps per chunk and
+// head M, QW (read again by the backward scan), KU and PU, and for the
+// backward the entry states, the state gradients and the parameter-gradient
+// partials; its fused forward (fused = true) needs the table alone.  The
+// general path keeps its fp32 intra-chunk factors and scratch.
+static Layout layout(const Dims& d, int for_bwd, bool fused = false) {
   Layout L = {};
   size_t o = 0;
   const size_t nch = (size_t)d.nc_max * d.H;
@@ -146,10 +147,14 @@ static Layout layout(const Dims& d, int for_bwd) {
   L.off_cl = take(4 * (size_t)d.nc_max);
   L.off_cd = take(4 * (size_t)d.nc_max);
   if (d.fast) {
-    if (for_bwd) {
-      L.off_Sent = take(4 * nch * d.dk * d.dv);
+    if (!fused) {
       L.off_M = take(4 * nch * d.dk * d.dk);
       L.off_QW = take(4 * nch * C * d.dk);
+      L.off_KU = take(4 * nch * d.dk * d.dv);
+      L.off_PU = take(4 * nch * C * d.dv);
+    }
+    if (for_bwd) {
+      L.off_Sent = take(4 * nch * d.dk * d.dv);
       L.off_dSn = take(4 * nch * d.dk * d.dv);
       L.off_pA = take(4 * nch);
       L.off_pdt = take(4 * nch * d.dk);
@@ -193,8 +198,10 @@ static Ws bind(void* ws, const Layout& L, const Dims& d, int for_bwd) {
   w.KD = at(L.off_KD);
   w.gam = at(L.off_gam);
   w.Sent = for_bwd ? at(L.off_Sent) : nullptr;
-  w.M = for_bwd ? at(L.off_M) : nullptr;
-  w.QW = for_bwd ? at(L.off_QW) : nullptr;
+  w.M = at(L.off_M);
+  w.QW = at(L.off_QW);
+  w.KU = at(L.off_KU);
+  w.PU = at(L.off_PU);
   w.dE = for_bwd ? at(L.off_dE) : nullptr;
   w.dSn = for_bwd ? at(L.off_dSn) : nullptr;
   w.pA = for_bwd ? at(L.off_pA) : nullptr;
@@ -205,10 +212,11 @@ static Ws bind(void* ws, const Layout& L, const Dims& d, int for_bwd) {
 }
 
 // The forward launch sequence shared by kda_fwd and kda_fwd_noalloc.
-static cudaError_t run_forward(const kda_problem* p, Dims d, const FwdIO& io, const Ws& w, cudaStream_t stream) {
+static cudaError_t run_forward(const kda_problem* p, Dims d, const FwdIO& io, const Ws& w, cudaStream_t stream,
+                               bool fused = false) {
   cudaError_t e = launch_chunk_table(p->cu_seqlens, d, w, stream);
   if (e != cudaSuccess) return e;
-  if (d.fast) return launch_fast_fwd(d, io, w, stream);
+  if (d.fast) return launch_fast_fwd(d, io, w, stream, fused);
   e = launch_fwd_intra(p->dtype, d, io, w, stream);
   if (e == cudaSuccess) e = launch_fwd_scan(p->dtype, d, io, w, stream);
   return e;
@@ -354,7 +362,8 @@ const char* kda_strerror(kda_status s) {
 }
 
 static const char* const k_names[K_COUNT] = {"chunk_table", "fwd_intra", "fwd_scan", "bwd_scan",
-                                             "bwd_intra", "bwd_reduce", "fwd_chain", "bwd_chunk"};
+                                             "bwd_intra", "bwd_reduce", "fwd_chain", "bwd_chunk",
+                                             "fwd_chunk", "fwd_state"};
 
 const char* kda_prof_kernel_name(int i) { return (i >= 0 && i < K_COUNT) ? k_names[i] : nullptr; }
 
@@ -427,7 +436,7 @@ extern "C" kda_status kda_fwd_noalloc(const kda_problem* p, const void* q, const
   for (const void* x : ptrs)
     if (!aligned(x, 16)) return KDA_ERR_ALIGNMENT;
   if ((h0 && !aligned(h0, 16)) || (h_final && !aligned(h_final, 16))) return KDA_ERR_ALIGNMENT;
-  Layout L = layout(d, 0);
+  Layout L = layout(d, 0, true);
   if (L.total > KDA_NOALLOC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;  // beyond the fixed array
   void* scratch = nullptr;
   s = noalloc_scratch(&scratch);
@@ -435,5 +444,5 @@ extern "C" kda_status kda_fwd_noalloc(const kda_problem* p, const void* q, const
   Ws w = bind(scratch, L, d, 0);
   d.save = 0;
   FwdIO io{q, k, v, f, b, A_log, dt_bias, h0, o, h_final, 0};
-  return run_forward(p, d, io, w, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+  return run_forward(p, d, io, w, stream, true) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

@@ -1,27 +1,32 @@
 // Tensor-core path for the 300M-layer head shape (dk = 32, dv = 64, bf16 io).
 //
-// Forward: one CTA per (document, head) walks the document's 64-token chunks
-// with the fp32 state S (dk x dv) in shared memory, so q, k, v, f, b are read
-// once and o written once.  Per chunk (G = in-chunk cumulative log-decay):
+// Per 64-token chunk (G = in-chunk cumulative log-decay):
 //   A  = strict_lower(diag(beta) (K^ K^T with ratios exp(G_r - G_s)))
 //   P  = inclusive_lower(Q^ K^T with the same ratios)
 //   T  = (I + A)^-1,  W = T diag(beta) (K^ exp G),  U = T diag(beta) V
 //   E  = U - W S,  O = scale (Q^ exp G) S + scale P E
 //   S <- Diag(exp G_last) S + (K^ exp(G_last - G))^T E
+// Forward: fwd_chunk forms, for every chunk and head in parallel, the
+// state-independent products M = Diag(gamma) - KD^T W, KU = KD^T U,
+// QW = QG - P W and PU = P U; fwd_state then carries S' = M S + KU and writes
+// O = QW S + PU, one CTA per document, head and 32 value columns.
 // The ratios never appear as exp of a positive number: rows and columns are
-// split in 16-token sub-blocks; an off-diagonal block (I > J) is
-//   (X_I exp(G - G_first(I))) diag(exp(G_first(I) - G_last(J))) (K_J exp(G_last(J) - G))^T
-// with every factor <= 1, and a diagonal block uses the same row factor with
-// the column factor exp(G_first(I) - G) <= exp(80) when the block's decay
-// span is at most 80 nats, else an exact pairwise evaluation.  The products
-// run as mma.sync m16n8k8 with fp32 accumulation and every operand split into
-// a tf32 head and a tf32 remainder (three products, ~21 significant bits):
-// with single tf32 operands the gate gradient df misses max|err|/rms <= 1e-2
-// (0.18 measured at the 300M shape), with the split it is 2.6e-4.
+// split in 16-token sub-blocks; block (I, J <= I) is
+//   (X_I exp(G - G_first(I))) (K_J exp(G_first(I) - G))^T
+// where the left factor is <= 1, the right one is <= 1 off the diagonal and
+// <= exp(80) on it when the block's decay span is at most 80 nats; a wider
+// diagonal block is evaluated pairwise and exactly.
+// Precision: with single tf32 (or bf16) operands the gate gradient df misses
+// max|err|/rms <= 1e-2 (0.18 measured at the 300M shape).  Large products
+// therefore split each operand into a bf16 head and a bf16 remainder and
+// accumulate three products in fp32 (mma.sync m16n8k16, ~16 significant
+// bits); the pairwise decay terms of the gate gradient, whose row and column
+// sums cancel in the cumulative sum, split into tf32 head + remainder
+// (m16n8k8, ~21 bits).
 //
 // Backward: a reverse scan over each document's chunks carries dS with
-//   dS_in = M^T dS_out + QW^T dO,  M = Diag(exp G_last) - KD^T W,  QW = QG - P W
-// (M and QW per chunk are saved by the forward), then one CTA per chunk
+//   dS_in = M^T dS_out + QW^T dO
+// (M and QW per chunk come from the forward), then one CTA per chunk
 // recomputes the chunk and forms every local gradient on chip.
 #include "kda_internal.cuh"
 #include "kda_mma.cuh"
@@ -36,11 +41,9 @@ constexpr int SQ = DK + 4;  // row stride of [C][DK] operands read along rows
 constexpr int SX = DK + 8;  // row stride of [C][DK] operands read along columns
 constexpr int SV = DV + 8;  // row stride of [C][DV] operands
 constexpr int SC = C + 4;   // row stride of [C][C] matrices
-constexpr int SO = DV + 8;  // row stride of the bf16 dO tile
 constexpr int NTH = 256, NW = 8;
 constexpr float SPAN_MAX = 80.f;
-// Every tensor-core product runs with split tf32 operands (see the header).
-constexpr bool SB = true;  // backward gradient products
+// Every tensor-core product runs with split operands (see the header).
 constexpr bool SR = true;  // backward recomputation of the chunk
 constexpr bool SF = true;  // forward chain products
 
@@ -372,6 +375,9 @@ __device__ void wu(const Intra& c, const float* tm, float* ww, float* uu) {
 }
 
 // ------------------------------------------------------------------ forward
+// The fused forward (kda_fwd_noalloc): one CTA per (document, head) walks the
+// document's chunks with S in shared memory and needs no scratch beyond the
+// chunk table.  It saves nothing for the backward.
 struct FwdSm {
   bf16 stage[STAGE_ELEMS];
   float qh[C * SQ], kh[C * SQ], gg[C * SQ], rr[C * SQ];  // q^ / k^ become lq / lk
@@ -428,7 +434,6 @@ __global__ void __launch_bounds__(NTH, 1) fwd_chain_kernel(Dims d, FwdIO io, Ws 
   }
   for (int ci = cb; ci < ce; ci++) {
     const int L = w.chunk_len[ci], t0 = w.chunk_tok0[ci];
-    const int64_t ch = (int64_t)ci * H + h;
     cp_wait_all();
     if (tid < C) sm.braw[tid] = bnext;
     __syncthreads();
@@ -478,11 +483,6 @@ __global__ void __launch_bounds__(NTH, 1) fwd_chain_kernel(Dims d, FwdIO io, Ws 
       }
     }
     __syncthreads();
-    if (io.save)
-      for (int idx = tid; idx < DK * DV; idx += NTH) {
-        int i = idx / DV, j = idx % DV;
-        w.Sent[ch * DK * DV + idx] = sm.ss[i * SV + j];
-      }
     {  // E = U - W S  (into XV's storage)
       const int I = warp & 3, half = warp >> 2;
       float acc[4][4];
@@ -526,28 +526,6 @@ __global__ void __launch_bounds__(NTH, 1) fwd_chain_kernel(Dims d, FwdIO io, Ws 
         v += sm.gam[i] * sm.ss[i * SV + 16 * jq + col];
       });
     }
-    if (io.save) {  // M = Diag(gamma) - KD^T W and QW = QG - P W for the backward scan
-      if (warp < 4) {
-        const int jp = warp >> 1;
-        float acc[2][4];
-        zero(acc);
-        gemm3<1, true, true>(acc, KD, 16 * mI, 0, W, 16 * jp, 0, C / 16);
-        each(acc, [&](int m, int col, float& v) {
-          int i = 16 * mI + m, jc = 16 * jp + col;
-          w.M[ch * DK * DK + i * DK + jc] = (i == jc ? sm.gam[i] : 0.f) - v;
-        });
-      }
-      {
-        const int I = warp & 3, jp = warp >> 2;
-        float acc[2][4];
-        zero(acc);
-        gemm3<1, false, true>(acc, P, 16 * I, 0, W, 16 * jp, 0, I + 1);
-        each(acc, [&](int m, int col, float& v) {
-          int r = 16 * I + m, jc = 16 * jp + col;
-          w.QW[ch * C * DK + r * DK + jc] = op_get(QG, r, jc) - v;
-        });
-      }
-    }
     __syncthreads();
 #pragma unroll
     for (int jt = 0; jt < 2; jt++)
@@ -564,6 +542,407 @@ __global__ void __launch_bounds__(NTH, 1) fwd_chain_kernel(Dims d, FwdIO io, Ws 
     for (int idx = tid; idx < DK * DV; idx += NTH) {
       int i = idx / DV, j = idx % DV;
       io.h_final[(((int64_t)doc * H + h) * DK + i) * DV + j] = sm.ss[i * SV + j];
+    }
+}
+
+// ------------------------------------------------------------------ forward
+// The forward runs in two kernels.  fwd_chunk (one CTA per chunk-head, all in
+// parallel) forms everything that does not depend on the carried state:
+//   M  = Diag(gamma) - KD^T W   [dk x dk]      KU = KD^T U   [dk x dv]
+//   QW = QG - P W               [C x dk]       PU = P U      [C x dv]
+// so that the chunk's state update and output are
+//   S' = M S + KU,   O = QW S + PU.
+// fwd_state then walks each document's chunks with S in shared memory; the
+// chain carries only these two small products, and it splits over value
+// columns (S, KU, PU and O columns are independent).
+
+// Rows of the decay-ratio right operands: R_I holds k^_s exp(G_first(I) - G_s)
+// for the 16 (I + 1) rows s of blocks J <= I, stacked from row 8 I (I + 1).
+__device__ __forceinline__ int roff(int I) { return 8 * I * (I + 1); }
+
+// Shared memory of fwd_chunk (about 104 KB: two CTAs per SM).  bf16 arrays
+// are split operand tiles; regions are reused as noted.
+struct ChunkSm {
+  float gg[C * SQ];    // G (fp32); QG (split) once the A / P blocks are done
+  bf16 x[18432];       // LQ | LK | R  ->  T (fp32) + Y scratch  ->  W | U;  KD in the last 8 KB
+  float am[C * SC];    // beta_r A (fp32), then T (split)
+  bf16 op[2 * C * C];  // P (scaled, split)
+  bf16 y[2 * C * DK + 2 * C * DV];  // XK = beta k^ e^G | XV = beta v
+  float bet[C], inq[C], ink[C];
+  float gam[DK];
+  float tot[NW * DK];
+  int spanok[4];
+};
+
+// Stores a 16 x (8 NT) accumulator tile to a row-major fp32 matrix with
+// leading dimension ld at (r0, c0), mapping each value through fn(r, c, v).
+template <int NT, class F>
+__device__ __forceinline__ void store_acc(const float (&acc)[NT][4], float* g, int ld, int r0, int c0, F fn) {
+  const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+  for (int jt = 0; jt < NT; jt++)
+#pragma unroll
+    for (int hh = 0; hh < 2; hh++) {
+      const int r = r0 + gq + 8 * hh, c = c0 + 8 * jt + 2 * tq;
+      *reinterpret_cast<float2*>(g + (size_t)r * ld + c) =
+          make_float2(fn(r, c, acc[jt][2 * hh]), fn(r, c + 1, acc[jt][2 * hh + 1]));
+    }
+}
+
+__global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws w) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  ChunkSm& sm = *reinterpret_cast<ChunkSm*>(smraw);
+  const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (*w.err != 0) return;
+  if (j >= *w.n_chunks) return;
+  const int L = w.chunk_len[j];
+  if (L <= 0) return;
+  const int t0 = w.chunk_tok0[j], H = d.H;
+  const int64_t ch = (int64_t)j * H + h;
+  const float a = expf(io.A_log[h]), scale = d.scale;
+  const float* dtb = io.dt_bias + h * DK;
+  const bf16* qraw = (const bf16*)io.q;
+  const bf16* kraw = (const bf16*)io.k;
+
+  const Op LQ{sm.x, sm.x + 2048, DK}, LK{sm.x + 4096, sm.x + 6144, DK}, R{sm.x + 8192, sm.x + 13312, DK};
+  const Op W{sm.x, sm.x + 2048, DK}, U{sm.x + 4096, sm.x + 8192, DV}, KD{sm.x + 14336, sm.x + 16384, DK};
+  const Op XK{sm.y, sm.y + 2048, DK}, XV{sm.y + 4096, sm.y + 8192, DV};
+  const Op P{sm.op, sm.op + C * C, C};
+  const Op T{reinterpret_cast<bf16*>(sm.am), reinterpret_cast<bf16*>(sm.am) + C * C, C};
+  bf16* qgb = reinterpret_cast<bf16*>(sm.gg);
+  const Op QG{qgb, qgb + C * DK, DK};
+  float* tm = reinterpret_cast<float*>(sm.x);  // [C][SC]
+  float* yy = tm + C * SC;                     // [16][C]
+
+  // ---- prologue in registers: thread = row r (tid / 4), key channels 8 (tid % 4) ..,
+  //      value columns 16 (tid % 4) ..; rows >= L are zero with G flat
+  const int r = tid >> 2, q4 = tid & 3, I = r >> 4;
+  const bool in = r < L;
+  float qv[8], kv[8], gv[8], vv[16], braw = 0.f;
+  if (in) {
+    const size_t row = (size_t)(t0 + r) * H + h;
+    unpack8(__ldg(reinterpret_cast<const uint4*>(qraw + row * DK + 8 * q4)), qv);
+    unpack8(__ldg(reinterpret_cast<const uint4*>(kraw + row * DK + 8 * q4)), kv);
+    unpack8(__ldg(reinterpret_cast<const uint4*>((const bf16*)io.f + row * DK + 8 * q4)), gv);
+    const uint4* vp = reinterpret_cast<const uint4*>((const bf16*)io.v + row * DV + 16 * q4);
+    unpack8(__ldg(vp), vv);
+    unpack8(__ldg(vp + 1), vv + 8);
+    braw = bfl(((const bf16*)io.b)[row]);
+#pragma unroll
+    for (int e = 0; e < 8; e++) gv[e] = -a * softplus_f(gv[e] + dtb[8 * q4 + e]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; e++) qv[e] = kv[e] = gv[e] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 16; e++) vv[e] = 0.f;
+  }
+  if (tid < 4) sm.spanok[tid] = 1;
+  float sq = 0.f, sk = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; e++) { sq += qv[e] * qv[e]; sk += kv[e] * kv[e]; }
+  sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+  sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+  sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+  sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+  const float iq = 1.0f / sqrtf(sq + L2_EPS), ik = 1.0f / sqrtf(sk + L2_EPS);
+  const float beta = in ? sigmoid_f(braw) : 0.f;
+  if (q4 == 0) {
+    sm.bet[r] = beta;
+    sm.inq[r] = iq;
+    sm.ink[r] = ik;
+  }
+#pragma unroll
+  for (int e = 0; e < 8; e++) { qv[e] *= iq; kv[e] *= ik; }
+  // cumulative sum of g over rows: shuffles among lanes of equal tid % 4, then warp offsets
+#pragma unroll
+  for (int e = 0; e < 8; e++) {
+    float x = gv[e];
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      const float y2 = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y2;
+    }
+    gv[e] = x;
+  }
+  if (lane >= 28)
+#pragma unroll
+    for (int e = 0; e < 8; e++) sm.tot[warp * DK + 8 * q4 + e] = gv[e];
+  __syncthreads();
+#pragma unroll
+  for (int e = 0; e < 8; e++) {
+    float off = 0.f;
+    for (int w2 = 0; w2 < warp; w2++) off += sm.tot[w2 * DK + 8 * q4 + e];
+    gv[e] += off;
+    sm.gg[r * SQ + 8 * q4 + e] = gv[e];
+  }
+  __syncthreads();
+
+  // ---- factors: LQ, LK, R (decay-ratio operands), XK, XV; QG and KD stay in
+  //      registers until their storage frees up
+  float qg[8], kd[8];
+  {
+    float gbv[8];
+    bool wide = false;
+#pragma unroll
+    for (int e = 0; e < 8; e++) {
+      gbv[e] = sm.gg[(16 * I) * SQ + 8 * q4 + e];
+      const float gl = sm.gg[(L - 1) * SQ + 8 * q4 + e];
+      const float eG = expf(gv[e]);
+      qg[e] = scale * qv[e] * eG;
+      kd[e] = kv[e] * expf(gl - gv[e]);
+      if (r == 0) sm.gam[8 * q4 + e] = expf(gl);
+      wide |= (r & 15) == 15 && gbv[e] - gv[e] > SPAN_MAX;
+    }
+    if (wide) sm.spanok[I] = 0;
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      const int i = 8 * q4 + e;
+      const float l0 = expf(gv[e] - gbv[e]), l1 = expf(gv[e + 1] - gbv[e + 1]);
+      op_store2(LQ, r, i, qv[e] * l0, qv[e + 1] * l1);
+      op_store2(LK, r, i, kv[e] * l0, kv[e + 1] * l1);
+      op_store2(XK, r, i, beta * kv[e] * expf(gv[e]), beta * kv[e + 1] * expf(gv[e + 1]));
+    }
+    for (int I2 = I; I2 < 4; I2++)
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const int i = 8 * q4 + e;
+        const float b0 = sm.gg[(16 * I2) * SQ + i], b1 = sm.gg[(16 * I2) * SQ + i + 1];
+        op_store2(R, roff(I2) + r, i, kv[e] * expf(fminf(b0 - gv[e], SPAN_MAX)),
+                  kv[e + 1] * expf(fminf(b1 - gv[e + 1], SPAN_MAX)));
+      }
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) op_store2(XV, r, 16 * q4 + e, beta * vv[e], beta * vv[e + 1]);
+  }
+  __syncthreads();
+
+  // ---- A (beta_r-scaled, strict lower, fp32) and P (scale, inclusive lower, split):
+  //      20 block tasks; a diagonal block whose decay span exceeds 80 is exact
+  for (int task = warp; task < 20; task += NW) {
+    const int blk = task >> 1, isP = task & 1;
+    const int bI = blk < 1 ? 0 : blk < 3 ? 1 : blk < 6 ? 2 : 3, bJ = blk - bI * (bI + 1) / 2;
+    float acc[2][4];
+    zero(acc);
+    if (bJ < bI || sm.spanok[bI]) {
+      gemm3<1, false, false>(acc, isP ? LQ : LK, 16 * bI, 0, R, roff(bI) + 16 * bJ, 0, DK / 16);
+    } else {
+      each(acc, [&](int m, int n, float& v) {
+        const int rr = 16 * bI + m, s = 16 * bI + n;
+        if (s <= rr && rr < L) {
+          const bf16* xr = (isP ? qraw : kraw) + ((size_t)(t0 + rr) * H + h) * DK;
+          const bf16* ks = kraw + ((size_t)(t0 + s) * H + h) * DK;
+          v = pair_exact(xr, isP ? sm.inq[rr] : sm.ink[rr], ks, sm.ink[s], sm.gg + rr * SQ, sm.gg + s * SQ);
+        }
+      });
+    }
+    if (isP) {
+      const int gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+      for (int jt = 0; jt < 2; jt++)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+          const int rr = 16 * bI + gq + 8 * hh, s0 = 16 * bJ + 8 * jt + 2 * tq;
+          op_store2(P, rr, s0, s0 <= rr ? scale * acc[jt][2 * hh] : 0.f,
+                    s0 + 1 <= rr ? scale * acc[jt][2 * hh + 1] : 0.f);
+        }
+    } else {
+      each(acc, [&](int m, int n, float& v) {
+        const int rr = 16 * bI + m, s = 16 * bJ + n;
+        sm.am[rr * SC + s] = s < rr ? sm.bet[rr] * v : 0.f;
+      });
+    }
+  }
+  __syncthreads();
+  // QG over G, KD in the tail of the x region (both free now)
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    op_store2(QG, r, 8 * q4 + e, qg[e], qg[e + 1]);
+    op_store2(KD, r, 8 * q4 + e, kd[e], kd[e + 1]);
+  }
+  solve<true>(sm.am, tm, yy, sm.bet);
+  for (int idx = tid; idx < 10 * 16 * 8; idx += NTH) {  // lower blocks of T -> split operand over A
+    const int blk = idx >> 7, rem = idx & 127;
+    const int bI = blk < 1 ? 0 : blk < 3 ? 1 : blk < 6 ? 2 : 3, bJ = blk - bI * (bI + 1) / 2;
+    const int rr = 16 * bI + (rem >> 3), s2 = 16 * bJ + 2 * (rem & 7);
+    op_store2(T, rr, s2, tm[rr * SC + s2], tm[rr * SC + s2 + 1]);
+  }
+  __syncthreads();
+  {  // W | U = T [XK | XV]  (T lower block-triangular: k < 16 (I + 1))
+    const int wI = warp & 3, half = warp >> 2;
+    if (half == 0) {
+      float aw[4][4], au[2][4];
+      zero(aw);
+      zero(au);
+      gemm3<2, false, true>(aw, T, 16 * wI, 0, XK, 0, 0, wI + 1);
+      gemm3<1, false, true>(au, T, 16 * wI, 0, XV, 0, 0, wI + 1);
+      const int gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+      for (int jt = 0; jt < 4; jt++)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++)
+          op_store2(W, 16 * wI + gq + 8 * hh, 8 * jt + 2 * tq, aw[jt][2 * hh], aw[jt][2 * hh + 1]);
+#pragma unroll
+      for (int jt = 0; jt < 2; jt++)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++)
+          op_store2(U, 16 * wI + gq + 8 * hh, 8 * jt + 2 * tq, au[jt][2 * hh], au[jt][2 * hh + 1]);
+    } else {
+      float au[6][4];
+      zero(au);
+      gemm3<3, false, true>(au, T, 16 * wI, 0, XV, 16, 0, wI + 1);
+      const int gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+      for (int jt = 0; jt < 6; jt++)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++)
+          op_store2(U, 16 * wI + gq + 8 * hh, 16 + 8 * jt + 2 * tq, au[jt][2 * hh], au[jt][2 * hh + 1]);
+    }
+  }
+  __syncthreads();
+  {  // outputs (fp32): PU and QW by row block, then the 16 x 16 tiles of M | KU
+    const int wI = warp & 3, half = warp >> 2;
+    float* PUg = w.PU + ch * C * DV;
+    float* QWg = w.QW + ch * C * DK;
+    float* Mg = w.M + ch * DK * DK;
+    float* KUg = w.KU + ch * DK * DV;
+    {
+      float acc[4][4];
+      zero(acc);
+      gemm3<2, false, true>(acc, P, 16 * wI, 0, U, 32 * half, 0, wI + 1);
+      store_acc(acc, PUg, DV, 16 * wI, 32 * half, [](int, int, float v) { return v; });
+    }
+    {
+      float acc[2][4];
+      zero(acc);
+      gemm3<1, false, true>(acc, P, 16 * wI, 0, W, 16 * half, 0, wI + 1);
+      store_acc(acc, QWg, DK, 16 * wI, 16 * half, [&](int rr, int c, float v) { return op_get(QG, rr, c) - v; });
+    }
+    // 12 tiles t = 6 mi + cc (cc < 2: M columns 16 cc, else KU columns 16 (cc - 2)),
+    // dealt so that the warps with short row blocks above take more
+    const int n = 3 - wI;
+    const int tb = (wI == 0 ? 0 : wI == 1 ? 6 : wI == 2 ? 10 : 12) + half * (n > 0 ? n : 0);
+    for (int t = tb; t < tb + n; t++) {
+      const int mi = t / 6, cc = t % 6;
+      float acc[2][4];
+      zero(acc);
+      if (cc < 2) {
+        gemm3<1, true, true>(acc, KD, 16 * mi, 0, W, 16 * cc, 0, C / 16);
+        store_acc(acc, Mg, DK, 16 * mi, 16 * cc,
+                  [&](int i, int jc, float v) { return (i == jc ? sm.gam[i] : 0.f) - v; });
+      } else {
+        gemm3<1, true, true>(acc, KD, 16 * mi, 0, U, 16 * (cc - 2), 0, C / 16);
+        store_acc(acc, KUg, DV, 16 * mi, 16 * (cc - 2), [](int, int, float v) { return v; });
+      }
+    }
+  }
+}
+
+// fwd_state: one CTA per (document, head, NS2 value columns).  The next
+// chunks' M, KU, QW and PU stream in through a three-stage cp.async ring
+// while the current chunk computes; only S' = M S + KU is on the chain.
+constexpr int NS2 = 32;        // value columns per state CTA
+constexpr int SB2 = NS2 + 8;   // row stride of [*][NS2] arrays
+constexpr int NSTG = 3;
+struct StateStage {
+  float M[DK * SQ];
+  float QW[C * SQ];
+  float KU[DK * SB2];
+  float PU[C * SB2];
+};
+struct StateSm {
+  StateStage st[NSTG];
+  float S[DK * SB2];
+};
+
+__global__ void __launch_bounds__(128) fwd_state_kernel(Dims d, FwdIO io, Ws w) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  StateSm& sm = *reinterpret_cast<StateSm*>(smraw);
+  const int doc = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * NS2, tid = threadIdx.x, warp = tid >> 5;
+  if (*w.err != 0) return;
+  const int H = d.H;
+  const int cb = w.doc_chunk0[doc], ce = w.doc_chunk0[doc + 1];
+  for (int idx = tid; idx < DK * NS2; idx += 128) {
+    const int i = idx / NS2, jc = idx % NS2;
+    sm.S[i * SB2 + jc] = io.h0 ? io.h0[(((int64_t)doc * H + h) * DK + i) * DV + col0 + jc] : 0.f;
+  }
+  auto prefetch = [&](int ci) {  // always commits a group (empty past the end)
+    if (ci < ce) {
+      StateStage& s = sm.st[(ci - cb) % NSTG];
+      const int64_t ch = (int64_t)ci * H + h;
+      for (int idx = tid; idx < DK * 8; idx += 128) {
+        const int i = idx >> 3, p = idx & 7;
+        cp16(&s.M[i * SQ + 4 * p], w.M + ch * DK * DK + i * DK + 4 * p);
+      }
+      for (int idx = tid; idx < C * 8; idx += 128) {
+        const int rr = idx >> 3, p = idx & 7;
+        cp16(&s.QW[rr * SQ + 4 * p], w.QW + ch * C * DK + rr * DK + 4 * p);
+        cp16(&s.PU[rr * SB2 + 4 * p], w.PU + ch * C * DV + rr * DV + col0 + 4 * p);
+      }
+      for (int idx = tid; idx < DK * 8; idx += 128) {
+        const int i = idx >> 3, p = idx & 7;
+        cp16(&s.KU[i * SB2 + 4 * p], w.KU + ch * DK * DV + i * DV + col0 + 4 * p);
+      }
+    }
+    cp_commit();
+  };
+  prefetch(cb);
+  prefetch(cb + 1);
+  const int mI = warp & 1, jn = warp >> 1;
+  bf16* o = (bf16*)io.o;
+  for (int ci = cb; ci < ce; ci++) {
+    const StateStage& s = sm.st[(ci - cb) % NSTG];
+    const int L = w.chunk_len[ci], t0 = w.chunk_tok0[ci];
+    asm volatile("cp.async.wait_group 1;\n" ::);
+    __syncthreads();  // this chunk's stage and the last state update are visible
+    prefetch(ci + 2);
+    if (io.save) {
+      const int64_t ch = (int64_t)ci * H + h;
+      for (int idx = tid; idx < DK * NS2 / 4; idx += 128) {
+        const int i = idx / (NS2 / 4), p = idx % (NS2 / 4);
+        *reinterpret_cast<float4*>(w.Sent + ch * DK * DV + i * DV + col0 + 4 * p) =
+            *reinterpret_cast<const float4*>(&sm.S[i * SB2 + 4 * p]);
+      }
+    }
+    float so[2][4], oo[4][4];
+    zero(so);
+    zero(oo);
+    rows16<2, true>(so, DK / 8, [&](int m, int k) { return s.M[(16 * mI + m) * SQ + k]; },
+                    [&](int k, int jj, int n) { return sm.S[k * SB2 + 16 * jn + 8 * jj + n]; });
+    rows16<4, true>(oo, DK / 8, [&](int m, int k) { return s.QW[(16 * warp + m) * SQ + k]; },
+                    [&](int k, int jj, int n) { return sm.S[k * SB2 + 8 * jj + n]; });
+    {
+      const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+      for (int jj = 0; jj < 4; jj++)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+          const int rr = 16 * warp + gq + 8 * hh, c = 8 * jj + 2 * tq;
+          if (rr < L) {
+            const float2 pu = *reinterpret_cast<const float2*>(&s.PU[rr * SB2 + c]);
+            *reinterpret_cast<__nv_bfloat162*>(o + ((size_t)(t0 + rr) * H + h) * DV + col0 + c) =
+                __floats2bfloat162_rn(oo[jj][2 * hh] + pu.x, oo[jj][2 * hh + 1] + pu.y);
+          }
+        }
+    }
+    __syncthreads();  // every read of S is done
+    {
+      const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+      for (int jj = 0; jj < 2; jj++)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+          const int i = 16 * mI + gq + 8 * hh, c = 16 * jn + 8 * jj + 2 * tq;
+          const float2 ku = *reinterpret_cast<const float2*>(&s.KU[i * SB2 + c]);
+          sm.S[i * SB2 + c] = so[jj][2 * hh] + ku.x;
+          sm.S[i * SB2 + c + 1] = so[jj][2 * hh + 1] + ku.y;
+        }
+    }
+  }
+  asm volatile("cp.async.wait_group 0;\n" ::);
+  __syncthreads();
+  if (io.h_final)
+    for (int idx = tid; idx < DK * NS2; idx += 128) {
+      const int i = idx / NS2, jc = idx % NS2;
+      io.h_final[(((int64_t)doc * H + h) * DK + i) * DV + col0 + jc] = sm.S[i * SB2 + jc];
     }
 }
 
@@ -1089,18 +1468,37 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
 
 }  // namespace fast
 
-static_assert(sizeof(fast::FwdSm) <= 232448, "forward chain shared memory exceeds 227 KB");
+static_assert(sizeof(fast::FwdSm) <= 232448, "fused forward shared memory exceeds 227 KB");
+static_assert(sizeof(fast::ChunkSm) <= 113 * 1024, "per-chunk forward must fit two CTAs per SM");
+static_assert(sizeof(fast::StateSm) <= 113 * 1024, "state chain must fit two CTAs per SM");
 static_assert(sizeof(fast::BwdSm) <= 232448, "backward chunk shared memory exceeds 227 KB");
 
 bool fast_path(int dtype, int dk, int dv) { return dtype == 0 && dk == fast::DK && dv == fast::DV; }
 
-cudaError_t launch_fast_fwd(const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st) {
-  const size_t smem = sizeof(fast::FwdSm);
-  cudaError_t e = cudaFuncSetAttribute(fast::fwd_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+cudaError_t launch_fast_fwd(const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st, bool fused) {
+  cudaError_t e;
+  if (fused) {
+    const size_t smem = sizeof(fast::FwdSm);
+    e = cudaFuncSetAttribute(fast::fwd_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    prof_begin(K_FWD_CHAIN, st);
+    fast::fwd_chain_kernel<<<dim3(d.n_docs, d.H), fast::NTH, smem, st>>>(d, io, w);
+    prof_end(K_FWD_CHAIN, st);
+    return cudaGetLastError();
+  }
+  const size_t s1 = sizeof(fast::ChunkSm), s2 = sizeof(fast::StateSm);
+  e = cudaFuncSetAttribute(fast::fwd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fast::fwd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
   if (e != cudaSuccess) return e;
-  prof_begin(K_FWD_CHAIN, st);
-  fast::fwd_chain_kernel<<<dim3(d.n_docs, d.H), fast::NTH, smem, st>>>(d, io, w);
-  prof_end(K_FWD_CHAIN, st);
+  prof_begin(K_FWD_CHUNK, st);
+  fast::fwd_chunk_kernel<<<dim3(d.nc_max, d.H), fast::NTH, s1, st>>>(d, io, w);
+  prof_end(K_FWD_CHUNK, st);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  prof_begin(K_FWD_STATE, st);
+  fast::fwd_state_kernel<<<dim3(d.n_docs, d.H, fast::DV / fast::NS2), 128, s2, st>>>(d, io, w);
+  prof_end(K_FWD_STATE, st);
   return cudaGetLastError();
 }
 

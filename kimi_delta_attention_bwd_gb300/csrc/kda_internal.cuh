@@ -21,6 +21,8 @@ enum KernelId {
   K_BWD_REDUCE,
   K_FWD_CHAIN,
   K_BWD_CHUNK,
+  K_FWD_CHUNK,
+  K_FWD_STATE,
   K_COUNT
 };
 
@@ -42,8 +44,10 @@ struct Ws {
   float* KD;   // [ch][C][dk]  K^ * exp(G_last - G)
   float* gam;  // [ch][dk]     exp(G_last)
   float* Sent; // [ch][dk][dv] state entering the chunk (saved for backward)
-  float* M;    // [ch][dk][dk] Diag(gamma) - KD^T W (tensor-core path, saved for backward)
-  float* QW;   // [ch][C][dk]  QG - P W            (tensor-core path, saved for backward)
+  float* M;    // [ch][dk][dk] Diag(gamma) - KD^T W (tensor-core path; the backward scan reads it)
+  float* QW;   // [ch][C][dk]  QG - P W            (tensor-core path; the backward scan reads it)
+  float* KU;   // [ch][dk][dv] KD^T U              (tensor-core forward scratch)
+  float* PU;   // [ch][C][dv]  P U                 (tensor-core forward scratch)
   // backward
   float* dE;   // [ch][C][dv]  gradient of E = U - W S
   float* dSn;  // [ch][dk][dv] gradient of the state leaving the chunk
@@ -96,7 +100,9 @@ cudaError_t launch_bwd_scan(int dtype, const Dims& d, const BwdIO& io, const Ws&
 cudaError_t launch_bwd_intra(int dtype, const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st);
 cudaError_t launch_bwd_reduce(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st);
 bool fast_path(int dtype, int dk, int dv);
-cudaError_t launch_fast_fwd(const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st);
+// fused: the single-kernel forward that needs only the chunk table (used by
+// kda_fwd_noalloc); else the per-chunk kernel and the state chain.
+cudaError_t launch_fast_fwd(const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st, bool fused);
 cudaError_t launch_fast_bwd(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st);
 
 // Timing brackets (no-ops unless kda_prof_start() armed them).
