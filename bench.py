@@ -58,7 +58,8 @@ def algorithmic_bytes(w, kernel: str) -> float:
         "fwd_intra": inputs_fwd,
         "fwd_scan": e * dv,                     # o
         "bwd_scan": e * dv,                     # dO
-        "bwd_chunk": inputs_fwd + e * dv + grads,  # reads q, k, f, v, b, dO; writes the gradients
+        "bwd_grad": e * (dk + dv + 1) + e * dv + e * (dv + 1),  # reads k, f, v, b, dO; writes dv, db
+        "bwd_gate": e * 3 * dk + e * 3 * dk,    # reads q, k, f; writes dq, dk, df
         "bwd_intra": inputs_fwd + e * dv + grads,
     }
     return float(per.get(kernel, 0)) * th

@@ -126,6 +126,7 @@ struct Layout {
   size_t total;
   size_t off_err, off_nch, off_dc0, off_ct0, off_cl, off_cd;
   size_t off_W, off_U, off_P, off_QG, off_KD, off_gam, off_Sent, off_M, off_QW, off_KU, off_PU;
+  size_t off_sT, off_sP, off_sW, off_sU, off_sA, off_gDP, off_gMA, off_gQG, off_gKD, off_gKG, off_gdg;
   size_t off_dE, off_dSn, off_pA, off_pdt, off_scr;
 };
 
@@ -154,10 +155,21 @@ static Layout layout(const Dims& d, int for_bwd, bool fused = false) {
       L.off_PU = take(4 * nch * C * d.dv);
     }
     if (for_bwd) {
-      L.off_Sent = take(4 * nch * d.dk * d.dv);
+      L.off_Sent = take(4 * nch * d.dk * d.dv);  // split-bf16 tiles: 4 bytes per element
       L.off_dSn = take(4 * nch * d.dk * d.dv);
       L.off_pA = take(4 * nch);
       L.off_pdt = take(4 * nch * d.dk);
+      L.off_sT = take(4 * nch * C * C);
+      L.off_sP = take(4 * nch * C * C);
+      L.off_sW = take(4 * nch * C * d.dk);
+      L.off_sU = take(4 * nch * C * d.dv);
+      L.off_sA = take(4 * nch * 10 * 256);
+      L.off_gDP = take(4 * nch * 10 * 256);
+      L.off_gMA = take(4 * nch * 10 * 256);
+      L.off_gQG = take(4 * nch * C * d.dk);
+      L.off_gKD = take(4 * nch * C * d.dk);
+      L.off_gKG = take(4 * nch * C * d.dk);
+      L.off_gdg = take(4 * nch * d.dk);
     }
     L.total = o;
     return L;
@@ -208,6 +220,20 @@ static Ws bind(void* ws, const Layout& L, const Dims& d, int for_bwd) {
   w.pdt = for_bwd ? at(L.off_pdt) : nullptr;
   w.scr = for_bwd ? at(L.off_scr) : nullptr;
   w.scr_per_ch = bwd_scratch_floats(d.dk, d.dv);
+  auto bat = [&](size_t off) { return off ? (__nv_bfloat16*)(p + off) : nullptr; };
+  w.sS = d.fast && for_bwd ? bat(L.off_Sent) : nullptr;
+  w.sdS = d.fast && for_bwd ? bat(L.off_dSn) : nullptr;
+  w.sT = bat(L.off_sT);
+  w.sP = bat(L.off_sP);
+  w.sW = bat(L.off_sW);
+  w.sU = bat(L.off_sU);
+  w.sA = at(L.off_sA);
+  w.gDP = at(L.off_gDP);
+  w.gMA = at(L.off_gMA);
+  w.gQG = at(L.off_gQG);
+  w.gKD = at(L.off_gKD);
+  w.gKG = at(L.off_gKG);
+  w.gdg = at(L.off_gdg);
   return w;
 }
 
@@ -362,8 +388,8 @@ const char* kda_strerror(kda_status s) {
 }
 
 static const char* const k_names[K_COUNT] = {"chunk_table", "fwd_intra", "fwd_scan", "bwd_scan",
-                                             "bwd_intra", "bwd_reduce", "fwd_chain", "bwd_chunk",
-                                             "fwd_chunk", "fwd_state"};
+                                             "bwd_intra", "bwd_reduce", "fwd_chain", "fwd_chunk",
+                                             "fwd_state", "bwd_grad",  "bwd_gate"};
 
 const char* kda_prof_kernel_name(int i) { return (i >= 0 && i < K_COUNT) ? k_names[i] : nullptr; }
 

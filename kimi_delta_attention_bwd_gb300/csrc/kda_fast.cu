@@ -38,13 +38,11 @@ typedef __nv_bfloat16 bf16;
 
 constexpr int DK = 32, DV = 64;
 constexpr int SQ = DK + 4;  // row stride of [C][DK] operands read along rows
-constexpr int SX = DK + 8;  // row stride of [C][DK] operands read along columns
 constexpr int SV = DV + 8;  // row stride of [C][DV] operands
 constexpr int SC = C + 4;   // row stride of [C][C] matrices
 constexpr int NTH = 256, NW = 8;
 constexpr float SPAN_MAX = 80.f;
 // Every tensor-core product runs with split operands (see the header).
-constexpr bool SR = true;  // backward recomputation of the chunk
 constexpr bool SF = true;  // forward chain products
 
 __device__ __forceinline__ int pidx(int I, int J) { return I * (I - 1) / 2 + J; }
@@ -54,9 +52,6 @@ __device__ __forceinline__ float bfl(bf16 x) { return __bfloat162float(x); }
 struct Intra {
   float *qh, *kh, *gg;     // [C][SQ]  q^, k^, G
   float *lq, *lk, *rr;     // [C][SQ]  q^ e^{G-Gb}, k^ e^{G-Gb}, k^ e^{Ge-G}
-  float *kd, *xk;          // [C][SX]  k^ e^{Gl-G}, beta k^ e^{G}
-  float* xv;               // [C][SV]  beta v
-  float* qg;               // [C][SQ]  scale q^ e^{G} (forward only)
   float *bet, *inq, *ink, *braw;  // [C]
   float *gl, *gam;         // [DK]
   float *gb, *ge, *dd, *ei;  // [4][DK], [4][DK], [6][DK], [4][DK]
@@ -99,7 +94,7 @@ __device__ __forceinline__ void unpack8(const uint4& u, float* x) {
 }
 
 // q^, k^ (L2-normalised), G (in-chunk inclusive cumulative log-decay), beta
-// and raw v (into xv) from the staged chunk.  Thread t owns row t / 4 and
+// from the staged chunk.  Thread t owns row t / 4 and
 // key channels 8 (t % 4) .. + 7 (value columns 16 (t % 4) .. + 15).  Rows
 // >= L are zero (G continues flat).  vraw returns the thread's raw v.
 __device__ void prologue(const Intra& c, const bf16* st, int L, float a, const float* dtb, uint4 (&vraw)[2]) {
@@ -136,15 +131,6 @@ __device__ void prologue(const Intra& c, const bf16* st, int L, float a, const f
   for (int e = 0; e < 8; e++) {
     c.qh[r * SQ + 8 * q4 + e] = qv[e] * iq;
     c.kh[r * SQ + 8 * q4 + e] = kv[e] * ik;
-  }
-  if (c.xv) {  // raw v (backward recomputation); the forward builds its beta-scaled operand itself
-    float vv[8];
-    unpack8(vraw[0], vv);
-#pragma unroll
-    for (int e = 0; e < 8; e++) c.xv[r * SV + 16 * q4 + e] = vv[e];
-    unpack8(vraw[1], vv);
-#pragma unroll
-    for (int e = 0; e < 8; e++) c.xv[r * SV + 16 * q4 + 8 + e] = vv[e];
   }
   // cumulative sum of g over rows: within a warp (8 rows) by shuffles among
   // lanes of equal t % 4, then across warps through smem
@@ -194,30 +180,6 @@ __device__ void refs(const Intra& c, int L) {
     float g = c.gg[(L - 1) * SQ + lane];
     c.gl[lane] = g;
     c.gam[lane] = expf(g);
-  }
-  __syncthreads();
-}
-
-// Factor arrays of the backward recomputation (fp32).
-__device__ void factors(const Intra& c, int L, float scale) {
-  const int tid = threadIdx.x;
-  refs(c, L);
-  for (int idx = tid; idx < C * DK; idx += NTH) {
-    int r = idx / DK, i = idx % DK, I = r >> 4;
-    float G = c.gg[r * SQ + i];
-    float eL = expf(G - c.gb[I * DK + i]), eR = expf(c.ge[I * DK + i] - G);
-    float Gm = expf(G), kdf = expf(c.gl[i] - G);
-    float q = c.qh[r * SQ + i], k = c.kh[r * SQ + i];
-    if (c.qg) c.qg[r * SQ + i] = scale * q * Gm;
-    c.kd[r * SX + i] = k * kdf;
-    c.xk[r * SX + i] = c.bet[r] * k * Gm;
-    c.rr[r * SQ + i] = k * eR;
-    c.lq[r * SQ + i] = q * eL;
-    c.lk[r * SQ + i] = k * eL;
-  }
-  for (int idx = tid; idx < C * DV; idx += NTH) {
-    int r = idx / DV, j = idx % DV;
-    c.xv[r * SV + j] *= c.bet[r];
   }
   __syncthreads();
 }
@@ -354,26 +316,6 @@ __device__ void solve(const float* am, float* tm, float* yy, const float* bet) {
   }
 }
 
-// W = T xk (into ww, stride SQ) and U = T xv (into uu, stride SV).
-template <bool SPL = false>
-__device__ void wu(const Intra& c, const float* tm, float* ww, float* uu) {
-  const int warp = threadIdx.x >> 5;
-  const int I = warp & 3, half = warp >> 2;
-  float acc[6][4];
-  zero(acc);
-  rows16<6, SPL>(acc, 2 * (I + 1), [&](int m, int k) { return tm[(16 * I + m) * SC + k]; },
-            [&](int k, int j, int n) {
-              int jj = 6 * half + j;
-              return jj < 4 ? c.xk[k * SX + 8 * jj + n] : c.xv[k * SV + 8 * (jj - 4) + n];
-            });
-  each(acc, [&](int m, int col, float& v) {
-    int r = 16 * I + m, jj = 6 * half + (col >> 3), n = col & 7;
-    if (jj < 4) ww[r * SQ + 8 * jj + n] = v;
-    else uu[r * SV + 8 * (jj - 4) + n] = v;
-  });
-  __syncthreads();
-}
-
 // ------------------------------------------------------------------ forward
 // The fused forward (kda_fwd_noalloc): one CTA per (document, head) walks the
 // document's chunks with S in shared memory and needs no scratch beyond the
@@ -407,7 +349,7 @@ __global__ void __launch_bounds__(NTH, 1) fwd_chain_kernel(Dims d, FwdIO io, Ws 
   const float a = expf(io.A_log[h]);
   const float* dtb = io.dt_bias + h * DK;
   const bf16* braw = (const bf16*)io.b;
-  Intra c{sm.qh, sm.kh, sm.gg, sm.qh, sm.kh, sm.rr, nullptr, nullptr, nullptr, nullptr, sm.bet, sm.inq, sm.ink,
+  Intra c{sm.qh, sm.kh, sm.gg, sm.qh, sm.kh, sm.rr, sm.bet, sm.inq, sm.ink,
           sm.braw, sm.gl, sm.gam, sm.gb, sm.ge, sm.dd, sm.ei, sm.tot, sm.spanok};
   const Op QG{sm.oqg, sm.oqg + C * DK, DK}, KD{sm.okd, sm.okd + C * DK, DK}, XK{sm.oxk, sm.oxk + C * DK, DK};
   const Op W{sm.ow, sm.ow + C * DK, DK}, XV{sm.oxv, sm.oxv + C * DV, DV}, E = XV;
@@ -573,6 +515,12 @@ struct ChunkSm {
   float tot[NW * DK];
   int spanok[4];
 };
+
+// Copies `bytes` (a multiple of 16) from shared to global memory, all threads.
+__device__ __forceinline__ void copy16(void* g, const void* smem, int bytes) {
+  for (int o = threadIdx.x * 16; o < bytes; o += NTH * 16)
+    *reinterpret_cast<uint4*>((char*)g + o) = *reinterpret_cast<const uint4*>((const char*)smem + o);
+}
 
 // Stores a 16 x (8 NT) accumulator tile to a row-major fp32 matrix with
 // leading dimension ld at (r0, c0), mapping each value through fn(r, c, v).
@@ -748,10 +696,12 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
       each(acc, [&](int m, int n, float& v) {
         const int rr = 16 * bI + m, s = 16 * bJ + n;
         sm.am[rr * SC + s] = s < rr ? sm.bet[rr] * v : 0.f;
+        if (io.save) w.sA[(ch * 10 + blk) * 256 + m * 16 + n] = s < rr ? v : 0.f;  // A' for dbeta
       });
     }
   }
   __syncthreads();
+  if (io.save) copy16(w.sP + ch * 2 * C * C, P.hi, 4 * C * C);
   // QG over G, KD in the tail of the x region (both free now)
 #pragma unroll
   for (int e = 0; e < 8; e += 2) {
@@ -766,6 +716,7 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     op_store2(T, rr, s2, tm[rr * SC + s2], tm[rr * SC + s2 + 1]);
   }
   __syncthreads();
+  if (io.save) copy16(w.sT + ch * 2 * C * C, T.hi, 4 * C * C);
   {  // W | U = T [XK | XV]  (T lower block-triangular: k < 16 (I + 1))
     const int wI = warp & 3, half = warp >> 2;
     if (half == 0) {
@@ -798,6 +749,10 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     }
   }
   __syncthreads();
+  if (io.save) {
+    copy16(w.sW + ch * 2 * C * DK, W.hi, 4 * C * DK);
+    copy16(w.sU + ch * 2 * C * DV, U.hi, 4 * C * DV);
+  }
   {  // outputs (fp32): PU and QW by row block, then the 16 x 16 tiles of M | KU
     const int wI = warp & 3, half = warp >> 2;
     float* PUg = w.PU + ch * C * DV;
@@ -894,12 +849,12 @@ __global__ void __launch_bounds__(128) fwd_state_kernel(Dims d, FwdIO io, Ws w) 
     asm volatile("cp.async.wait_group 1;\n" ::);
     __syncthreads();  // this chunk's stage and the last state update are visible
     prefetch(ci + 2);
-    if (io.save) {
+    if (io.save) {  // the entry state as a split operand tile for the backward
       const int64_t ch = (int64_t)ci * H + h;
-      for (int idx = tid; idx < DK * NS2 / 4; idx += 128) {
-        const int i = idx / (NS2 / 4), p = idx % (NS2 / 4);
-        *reinterpret_cast<float4*>(w.Sent + ch * DK * DV + i * DV + col0 + 4 * p) =
-            *reinterpret_cast<const float4*>(&sm.S[i * SB2 + 4 * p]);
+      const Op g{w.sS + ch * 2 * DK * DV, w.sS + ch * 2 * DK * DV + DK * DV, DV};
+      for (int idx = tid; idx < DK * NS2 / 2; idx += 128) {
+        const int i = idx / (NS2 / 2), jc = 2 * (idx % (NS2 / 2));
+        op_store2(g, i, col0 + jc, sm.S[i * SB2 + jc], sm.S[i * SB2 + jc + 1]);
       }
     }
     float so[2][4], oo[4][4];
@@ -993,9 +948,12 @@ __global__ void __launch_bounds__(128) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
     cp_wait_all();
     __syncthreads();  // buffer `buf` and the last dS update are visible
     if (ci - 1 >= cb) prefetch(ci - 1, buf ^ 1);
-    for (int idx = tid; idx < DK * NS; idx += 128) {
-      int i = idx / NS, j = idx % NS;
-      w.dSn[ch * DK * DV + i * DV + col0 + j] = dS[i * SS + j];
+    {  // dS' of this chunk as a split operand tile for the chunk gradients
+      const Op g{w.sdS + ch * 2 * DK * DV, w.sdS + ch * 2 * DK * DV + DK * DV, DV};
+      for (int idx = tid; idx < DK * NS / 2; idx += 128) {
+        const int i = idx / (NS / 2), jc = 2 * (idx % (NS / 2));
+        op_store2(g, i, col0 + jc, dS[i * SS + jc], dS[i * SS + jc + 1]);
+      }
     }
     float acc[1][4];
     zero(acc);
@@ -1014,29 +972,56 @@ __global__ void __launch_bounds__(128) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
     }
 }
 
-// ------------------------------------------------------------ backward chunk
-// Shared memory of the chunk-gradient kernel.  Regions are reused as the
-// kernel proceeds (see the comments); bf16 arrays are split operand tiles.
-struct BwdSm {
-  float qh[C * SQ], kh[C * SQ], gg[C * SQ];  // q^, k^, G
-  float lq[C * SQ], lk[C * SQ], rr[C * SQ];  // decay-ratio factors; later dq^, dk^, dG
-  float am[C * SC];   // A' (fp32), then MA = beta dA in place, then scratch
-  float tm[C * SC];   // T (fp32), then dP' (fp32), then scratch
-  bf16 ra[12288];     // raw-input stage | XK (4096) + XV (8192) | E (8192) + dW (4096) | YU over E
-  bf16 rb[8192];      // P' | dE
-  bf16 oT[8192], oU[8192], oW[4096], oKD[4096];
-  bf16 oS[4096], odS[4096], odO[4096];  // S, dS' (split); dO (exact); later YW over S
-  bf16 fr[C * DK];    // raw f
-  float tot[NW * DK], part[NW * DK], ks[NW * DK];
-  float bet[C], inq[C], ink[C], braw[C], dbet[C];
-  float gl[DK], gam[DK], dgam[DK], gb[4 * DK], ge[4 * DK], dd[6 * DK], ei[4 * DK];
-  float red[NW];
-  int spanok[4];
+// ------------------------------------------------------------ backward chunk kernels
+constexpr int NBLK = 10;  // lower 16 x 16 blocks of a C x C matrix, block I (I + 1) / 2 + J
+constexpr int PB = 20;    // row stride of a 16 x 16 fp32 block in shared memory
+
+__device__ __forceinline__ void blk_ij(int b, int& I, int& J) {
+  I = b < 1 ? 0 : b < 3 ? 1 : b < 6 ? 2 : 3;
+  J = b - I * (I + 1) / 2;
+}
+__device__ __forceinline__ int blk_of(int I, int J) { return I * (I + 1) / 2 + J; }
+
+// cp.async of `bytes` (a multiple of 16) from global to shared, all threads.
+__device__ __forceinline__ void cp_bytes(void* dst, const void* src, int bytes) {
+  for (int o = threadIdx.x * 16; o < bytes; o += NTH * 16) cp16((char*)dst + o, (const char*)src + o);
+}
+
+// The 8 accumulator values a thread holds of a 16 x 16 tile, in fragment
+// order (thread-major, 32 bytes per thread): bwd_grad and bwd_gate use the
+// same warp -> tile mapping, so the hand-over is two float4 per thread.
+__device__ __forceinline__ void frag_store(float* g, const float (&v)[2][4]) {
+  float4* p = reinterpret_cast<float4*>(g + threadIdx.x * 8);
+  p[0] = make_float4(v[0][0], v[0][1], v[0][2], v[0][3]);
+  p[1] = make_float4(v[1][0], v[1][1], v[1][2], v[1][3]);
+}
+__device__ __forceinline__ void frag_load(const float* g, float (&v)[2][4]) {
+  const float4* p = reinterpret_cast<const float4*>(g + threadIdx.x * 8);
+  const float4 a = p[0], b = p[1];
+  v[0][0] = a.x; v[0][1] = a.y; v[0][2] = a.z; v[0][3] = a.w;
+  v[1][0] = b.x; v[1][1] = b.y; v[1][2] = b.z; v[1][3] = b.w;
+}
+
+// bwd_grad: one CTA per chunk-head (two per SM).  From the forward's saved
+// operand tiles (T, P = scale P', W, U; A' fp32) and the chunk's entry state
+// S and exit-state gradient dS' it forms
+//   dE = P^T dO + KD dS',  E = U - W S,
+//   dP' = scale dO E^T,  dKD = E dS'^T,  dQG = scale dO S^T,  dW = -dE S^T,
+//   dgamma = rowsum(dS' .* S),  YU = T^T dE,  YW = T^T dW,  dv = beta YU,
+//   dA = -(YU U^T + YW W^T) (strict lower),  MA = beta dA,
+//   dbeta = rowsum(YU .* V) + rowsum(YW .* K^ e^G) + rowsum(dA .* A'),
+// writes dv and db, and hands dP', MA, dQG, dKD, beta YW and dgamma to bwd_gate.
+struct GradSm {
+  bf16 wk[45056];  // work area (88 KB), regions bound in the kernel
+  float gg[C * SQ];
+  bf16 rk[C * DK];
+  float bet[C], braw[C], dbet[C], part[4 * C];
+  float tot[NW * DK];
 };
 
-__global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws w) {
+__global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w) {
   extern __shared__ __align__(16) unsigned char smraw[];
-  BwdSm& sm = *reinterpret_cast<BwdSm*>(smraw);
+  GradSm& sm = *reinterpret_cast<GradSm*>(smraw);
   const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
   if (!saved_ok(d, w.tag, w.err)) return;
@@ -1047,370 +1032,522 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
   const int64_t ch = (int64_t)j * H + h;
   const float a = expf(io.A_log[h]), scale = d.scale;
   const float* dtb = io.dt_bias + h * DK;
-  Intra c{sm.qh, sm.kh, sm.gg, sm.lq, sm.lk, sm.rr, nullptr, nullptr, nullptr, nullptr, sm.bet, sm.inq, sm.ink,
-          sm.braw, sm.gl, sm.gam, sm.gb, sm.ge, sm.dd, sm.ei, sm.tot, sm.spanok};
-  bf16* st = sm.ra;
-  const Op XK{sm.ra, sm.ra + 2048, DK}, XV{sm.ra + 4096, sm.ra + 8192, DV};
-  const Op E{sm.ra, sm.ra + 4096, DV}, dW{sm.ra + 8192, sm.ra + 10240, DK}, YU = E;
-  const Op P{sm.rb, sm.rb + 4096, C}, dE{sm.rb, sm.rb + 4096, DV};
-  const Op T{sm.oT, sm.oT + 4096, C}, U{sm.oU, sm.oU + 4096, DV}, W{sm.oW, sm.oW + 2048, DK};
-  const Op KD{sm.oKD, sm.oKD + 2048, DK}, S{sm.oS, sm.oS + 2048, DV}, dS{sm.odS, sm.odS + 2048, DV};
-  const Op dO{sm.odO, nullptr, DV}, YW{sm.oS, sm.oS + 2048, DK};
-  const Op noQG{nullptr, nullptr, DK};
+  bf16* wk = sm.wk;
+  // work-area regions (bf16 offsets): dO 0 | S 4096 | dS' 8192 | P -> E 12288 |
+  // W -> dW -> YW 20480 | U -> dE -> YU 24576 | raw f -> KD 32768 | T 36864;
+  // reloaded for the dA products over the first four: U 0 | W 8192 | A' 12288
+  const Op dO{wk, nullptr, DV}, S{wk + 4096, wk + 6144, DV}, dS{wk + 8192, wk + 10240, DV};
+  const Op P{wk + 12288, wk + 16384, C}, E{wk + 12288, wk + 16384, DV};
+  const Op W{wk + 20480, wk + 22528, DK}, U{wk + 24576, wk + 28672, DV};
+  const Op KD{wk + 32768, wk + 34816, DK}, T{wk + 36864, wk + 40960, C};
+  const Op dW = W, YW = W, dE = U, YU = U;
+  const Op U2{wk, wk + 4096, DV}, W2{wk + 8192, wk + 10240, DK};
+  const float* A2 = reinterpret_cast<const float*>(wk + 12288);
+  bf16* fst = wk + 32768;
 
-  // ---- stage raw inputs (cp.async), dO into its operand tile, S and dS' split
-  {
-    FwdIO fio{io.q, io.k, io.v, io.f, io.b, io.A_log, io.dt_bias, nullptr, nullptr, nullptr, 0};
-    stage_chunk(st, fio, H, h, t0, L);
-    const bf16* dOg = (const bf16*)io.dO;
-    for (int idx = tid; idx < C * 8; idx += NTH) {
-      int r = idx >> 3, p = idx & 7;
-      bf16* dst = sm.odO + opix(r, 8 * p, DV);
-      if (r < L) cp16(dst, dOg + ((size_t)(t0 + r) * H + h) * DV + p * 8);
-      else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    cp_commit();
-    if (tid < C) sm.braw[tid] = tid < L ? bfl(((const bf16*)io.b)[(size_t)(t0 + tid) * H + h]) : 0.f;
-    if (tid < C) sm.dbet[tid] = 0.f;
-    asm volatile("cp.async.wait_group 1;\n" ::);  // q, k, f, v landed; dO may still be in flight
-    __syncthreads();
-    for (int idx = tid; idx < C * DK; idx += NTH) sm.fr[idx] = st[2 * C * DK + idx];
-  }
-  // S and dS' are read into registers now and split into operand tiles after
-  // the recomputation, so that their latency overlaps it
-  float2 sreg[DK * DV / 2 / NTH], dsreg[DK * DV / 2 / NTH];
-  {
-    const float* Sg = w.Sent + ch * DK * DV;
-    const float* dSg = w.dSn + ch * DK * DV;
-#pragma unroll
-    for (int u = 0; u < DK * DV / 2 / NTH; u++) {
-      const int idx = tid + u * NTH, i = idx / (DV / 2), jc = 2 * (idx % (DV / 2));
-      sreg[u] = *reinterpret_cast<const float2*>(Sg + i * DV + jc);
-      dsreg[u] = *reinterpret_cast<const float2*>(dSg + i * DV + jc);
+  // ---- group 1: raw k, f;  group 2: dO, S, dS', P, W, U, T
+  for (int idx = tid; idx < C * 4; idx += NTH) {
+    const int r = idx >> 2, p = idx & 3;
+    if (r < L) {
+      const size_t g = ((size_t)(t0 + r) * H + h) * DK + 8 * p;
+      cp16(sm.rk + r * DK + 8 * p, (const bf16*)io.k + g);
+      cp16(fst + r * DK + 8 * p, (const bf16*)io.f + g);
     }
   }
-  // ---- recompute the chunk (same arithmetic as the forward)
-  uint4 vraw[2];  // this thread's raw v (row tid / 4, columns 16 (tid % 4) ..), kept for dbeta
-  prologue(c, st, L, a, dtb, vraw);
-  {  // beta v -> XV (over the consumed stage)
-    const int r = tid >> 2, q4 = tid & 3;
-    const float br = r < L ? sm.bet[r] : 0.f;
-    float vv[16];
-    unpack8(vraw[0], vv);
-    unpack8(vraw[1], vv + 8);
-#pragma unroll
-    for (int e = 0; e < 16; e += 2) op_store2(XV, r, 16 * q4 + e, br * vv[e], br * vv[e + 1]);
+  cp_commit();
+  for (int idx = tid; idx < C * 8; idx += NTH) {
+    const int r = idx >> 3, p = idx & 7;
+    bf16* dst = wk + opix(r, 8 * p, DV);
+    if (r < L) cp16(dst, (const bf16*)io.dO + ((size_t)(t0 + r) * H + h) * DV + 8 * p);
+    else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
   }
-  factors_fwd(c, L, scale, noQG, KD, XK);
-  ap<false, SR>(c, sm.am, nullptr, 1.f, (const bf16*)io.q, (const bf16*)io.k, H, h, t0, L, &P);
-  solve<false>(sm.am, sm.tm, reinterpret_cast<float*>(sm.oU), sm.bet);
-  for (int idx = tid; idx < C * C / 2; idx += NTH) {  // T -> split-bf16 operand
-    const int r = idx / (C / 2), s2 = 2 * (idx % (C / 2));
-    op_store2(T, r, s2, sm.tm[r * SC + s2], sm.tm[r * SC + s2 + 1]);
-  }
-  __syncthreads();
-  {  // W | U = T [XK | XV]
-    const int I = warp & 3, half = warp >> 2;
-    if (half == 0) {
-      float aw[4][4], au[2][4];
-      zero(aw);
-      zero(au);
-      gemm3<2, false, true>(aw, T, 16 * I, 0, XK, 0, 0, I + 1);
-      gemm3<1, false, true>(au, T, 16 * I, 0, XV, 0, 0, I + 1);
-#pragma unroll
-      for (int jt = 0; jt < 4; jt++)
-#pragma unroll
-        for (int hh = 0; hh < 2; hh++)
-          op_store2(W, 16 * I + gq + 8 * hh, 8 * jt + 2 * tq, aw[jt][2 * hh], aw[jt][2 * hh + 1]);
-#pragma unroll
-      for (int jt = 0; jt < 2; jt++)
-#pragma unroll
-        for (int hh = 0; hh < 2; hh++)
-          op_store2(U, 16 * I + gq + 8 * hh, 8 * jt + 2 * tq, au[jt][2 * hh], au[jt][2 * hh + 1]);
-    } else {
-      float au[6][4];
-      zero(au);
-      gemm3<3, false, true>(au, T, 16 * I, 0, XV, 16, 0, I + 1);
-#pragma unroll
-      for (int jt = 0; jt < 6; jt++)
-#pragma unroll
-        for (int hh = 0; hh < 2; hh++)
-          op_store2(U, 16 * I + gq + 8 * hh, 16 + 8 * jt + 2 * tq, au[jt][2 * hh], au[jt][2 * hh + 1]);
-    }
-  }
-  __syncthreads();
+  cp_bytes(S.hi, w.sS + ch * 2 * DK * DV, 4 * DK * DV);
+  cp_bytes(dS.hi, w.sdS + ch * 2 * DK * DV, 4 * DK * DV);
+  cp_bytes(P.hi, w.sP + ch * 2 * C * C, 4 * C * C);
+  cp_bytes(W.hi, w.sW + ch * 2 * C * DK, 4 * C * DK);
+  cp_bytes(U.hi, w.sU + ch * 2 * C * DV, 4 * C * DV);
+  cp_bytes(T.hi, w.sT + ch * 2 * C * C, 4 * C * C);
+  cp_commit();
 
-#pragma unroll
-  for (int u = 0; u < DK * DV / 2 / NTH; u++) {
-    const int idx = tid + u * NTH, i = idx / (DV / 2), jc = 2 * (idx % (DV / 2));
-    op_store2(S, i, jc, sreg[u].x, sreg[u].y);
-    op_store2(dS, i, jc, dsreg[u].x, dsreg[u].y);
+  // ---- k^, G, beta (thread: row tid / 4, key channels 8 (tid % 4) .., value columns 16 (tid % 4) ..)
+  const int r = tid >> 2, q4 = tid & 3;
+  const bool in = r < L;
+  uint4 vraw[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+  float braw = 0.f;
+  if (in) {
+    const size_t row = (size_t)(t0 + r) * H + h;
+    const uint4* vp = reinterpret_cast<const uint4*>((const bf16*)io.v + row * DV + 16 * q4);
+    vraw[0] = __ldg(vp);
+    vraw[1] = __ldg(vp + 1);
+    braw = bfl(((const bf16*)io.b)[row]);
   }
-  cp_wait_all();  // dO
+  asm volatile("cp.async.wait_group 1;\n" ::);
   __syncthreads();
-
-  const int I = warp & 3, hk = warp >> 2;  // owner tile: rows 16I.., key columns 16hk..
-  // ---- dE = scale P'^T dO + KD dS' (in registers: P' shares its storage)
-  //      and E = U - W S (over XK / XV)
-  float dEr[4][4];
+  float kv[8], gv[8];
+  if (in) {
+    unpack8(*reinterpret_cast<const uint4*>(sm.rk + r * DK + 8 * q4), kv);
+    unpack8(*reinterpret_cast<const uint4*>(fst + r * DK + 8 * q4), gv);
+#pragma unroll
+    for (int e = 0; e < 8; e++) gv[e] = -a * softplus_f(gv[e] + dtb[8 * q4 + e]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; e++) kv[e] = gv[e] = 0.f;
+  }
   {
-    const int half = warp >> 2;
+    float sk = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; e++) sk += kv[e] * kv[e];
+    sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+    sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+    const float ik = 1.0f / sqrtf(sk + L2_EPS);
+#pragma unroll
+    for (int e = 0; e < 8; e++) kv[e] *= ik;
+  }
+  if (q4 == 0) {
+    sm.bet[r] = in ? sigmoid_f(braw) : 0.f;
+    sm.braw[r] = braw;
+  }
+#pragma unroll
+  for (int e = 0; e < 8; e++) {
+    float x = gv[e];
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      const float y2 = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y2;
+    }
+    gv[e] = x;
+  }
+  if (lane >= 28)
+#pragma unroll
+    for (int e = 0; e < 8; e++) sm.tot[warp * DK + 8 * q4 + e] = gv[e];
+  __syncthreads();
+#pragma unroll
+  for (int e = 0; e < 8; e++) {
+    float off = 0.f;
+    for (int w2 = 0; w2 < warp; w2++) off += sm.tot[w2 * DK + 8 * q4 + e];
+    gv[e] += off;
+    sm.gg[r * SQ + 8 * q4 + e] = gv[e];
+  }
+  __syncthreads();
+  float xkg[8];  // k^ e^G for the W term of dbeta
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    const int i = 8 * q4 + e;
+    const float gl0 = sm.gg[(L - 1) * SQ + i], gl1 = sm.gg[(L - 1) * SQ + i + 1];
+    op_store2(KD, r, i, kv[e] * expf(gl0 - gv[e]), kv[e + 1] * expf(gl1 - gv[e + 1]));
+    xkg[e] = kv[e] * expf(gv[e]);
+    xkg[e + 1] = kv[e + 1] * expf(gv[e + 1]);
+  }
+  cp_wait_all();
+  __syncthreads();
+
+  const int I = warp & 3, hk = warp >> 2;  // owner tile: rows 16 I .., columns 32 hk .. / 16 hk ..
+  // ---- dE = P^T dO + KD dS' and E = U - W S
+  {
     float acc[4][4], acc2[4][4], accE[4][4];
     zero(acc);
     zero(acc2);
     zero(accE);
-    gemm3<2, true, true>(acc, P, 16 * I, 16 * I, dO, 32 * half, 16 * I, 4 - I);
-    gemm3<2, false, true>(acc2, KD, 16 * I, 0, dS, 32 * half, 0, DK / 16);
-    gemm3<2, false, true>(accE, W, 16 * I, 0, S, 32 * half, 0, DK / 16);
+    gemm3<2, true, true>(acc, P, 16 * I, 16 * I, dO, 32 * hk, 16 * I, 4 - I);
+    gemm3<2, false, true>(acc2, KD, 16 * I, 0, dS, 32 * hk, 0, DK / 16);
+    gemm3<2, false, true>(accE, W, 16 * I, 0, S, 32 * hk, 0, DK / 16);
 #pragma unroll
     for (int jt = 0; jt < 4; jt++)
 #pragma unroll
       for (int hh = 0; hh < 2; hh++) {
-        const int r = 16 * I + gq + 8 * hh, col = 32 * half + 8 * jt + 2 * tq;
-        dEr[jt][2 * hh] = scale * acc[jt][2 * hh] + acc2[jt][2 * hh];
-        dEr[jt][2 * hh + 1] = scale * acc[jt][2 * hh + 1] + acc2[jt][2 * hh + 1];
-        op_store2(E, r, col, op_get(U, r, col) - accE[jt][2 * hh], op_get(U, r, col + 1) - accE[jt][2 * hh + 1]);
+        const int rr = 16 * I + gq + 8 * hh, col = 32 * hk + 8 * jt + 2 * tq;
+        acc[jt][2 * hh] += acc2[jt][2 * hh];
+        acc[jt][2 * hh + 1] += acc2[jt][2 * hh + 1];
+        accE[jt][2 * hh] = op_get(U, rr, col) - accE[jt][2 * hh];
+        accE[jt][2 * hh + 1] = op_get(U, rr, col + 1) - accE[jt][2 * hh + 1];
       }
-  }
-  __syncthreads();  // P' fully read
-  {
-    const int half = warp >> 2;
+    __syncthreads();  // P, W, U, KD fully read
 #pragma unroll
     for (int jt = 0; jt < 4; jt++)
 #pragma unroll
-      for (int hh = 0; hh < 2; hh++)
-        op_store2(dE, 16 * I + gq + 8 * hh, 32 * half + 8 * jt + 2 * tq, dEr[jt][2 * hh], dEr[jt][2 * hh + 1]);
+      for (int hh = 0; hh < 2; hh++) {
+        const int rr = 16 * I + gq + 8 * hh, col = 32 * hk + 8 * jt + 2 * tq;
+        op_store2(E, rr, col, accE[jt][2 * hh], accE[jt][2 * hh + 1]);
+        op_store2(dE, rr, col, acc[jt][2 * hh], acc[jt][2 * hh + 1]);
+      }
   }
   __syncthreads();
-  // ---- dP' = scale dO E^T (inclusive lower, fp32 over T), dKD = E dS'^T,
-  //      dQG = scale dO S^T (registers), dgamma = rowsum(dS' .* S), dW = -dE S^T
-  float dKD[2][4], dQG[2][4];
-  float* DP = sm.tm;
+  // ---- dKD, dQG (to bwd_gate), dW (over W), dP' lower blocks (to bwd_gate), dgamma
   {
+    float dKD[2][4], dQG[2][4], acc[2][4];
     zero(dKD);
     zero(dQG);
+    zero(acc);
     gemm3<1, false, false>(dKD, E, 16 * I, 0, dS, 16 * hk, 0, DV / 16);
     gemm3<1, false, false>(dQG, dO, 16 * I, 0, S, 16 * hk, 0, DV / 16);
-    each(dQG, [&](int m, int col, float& v) { v *= scale; });
-    float acc[2][4];
-    zero(acc);
     gemm3<1, false, false>(acc, dE, 16 * I, 0, S, 16 * hk, 0, DV / 16);
+    each(dQG, [&](int, int, float& v) { v *= scale; });
+    frag_store(w.gKD + ch * NTH * 8, dKD);
+    frag_store(w.gQG + ch * NTH * 8, dQG);
 #pragma unroll
     for (int jt = 0; jt < 2; jt++)
 #pragma unroll
       for (int hh = 0; hh < 2; hh++)
         op_store2(dW, 16 * I + gq + 8 * hh, 16 * hk + 8 * jt + 2 * tq, -acc[jt][2 * hh], -acc[jt][2 * hh + 1]);
-    for (int t = warp; t < 10; t += NW) {  // lower 16x16 blocks of dP'
-      const int bI = t < 1 ? 0 : t < 3 ? 1 : t < 6 ? 2 : 3, bJ = t - bI * (bI + 1) / 2;
+    for (int t = warp; t < NBLK; t += NW) {
+      int bI, bJ;
+      blk_ij(t, bI, bJ);
       float pp[2][4];
       zero(pp);
       gemm3<1, false, false>(pp, dO, 16 * bI, 0, E, 16 * bJ, 0, DV / 16);
-      each(pp, [&](int m, int n, float& v) {
-        int r = 16 * bI + m, s2 = 16 * bJ + n;
-        DP[r * SC + s2] = s2 <= r ? scale * v : 0.f;
-      });
+      float* g = w.gDP + (ch * NBLK + t) * 256;
+#pragma unroll
+      for (int jt = 0; jt < 2; jt++)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+          const int m = gq + 8 * hh, n = 8 * jt + 2 * tq;
+          const int rr = 16 * bI + m, s0 = 16 * bJ + n;
+          *reinterpret_cast<float2*>(g + m * 16 + n) =
+              make_float2(s0 <= rr ? scale * pp[jt][2 * hh] : 0.f, s0 + 1 <= rr ? scale * pp[jt][2 * hh + 1] : 0.f);
+        }
     }
     if (tid < DK) {
       float acc1 = 0.f;
       for (int jj = 0; jj < DV; jj++) acc1 += op_get(dS, tid, jj) * op_get(S, tid, jj);
-      sm.dgam[tid] = acc1;
+      w.gdg[ch * DK + tid] = acc1;
     }
   }
   __syncthreads();
-  // ---- YU = T^T dE, YW = T^T dW (registers); then YU over E, YW over S
-  float yu[4][4], yw[2][4];
+  // group 3: U, W, A' for the dA products (over dO, S, dS', E: all read by now)
+  cp_bytes(U2.hi, w.sU + ch * 2 * C * DV, 4 * C * DV);
+  cp_bytes(W2.hi, w.sW + ch * 2 * C * DK, 4 * C * DK);
+  cp_bytes(wk + 12288, w.sA + ch * NBLK * 256, NBLK * 256 * 4);
+  cp_commit();
+  // ---- YU = T^T dE, YW = T^T dW (registers, then over dE / dW); dv = beta YU; beta YW to bwd_gate
   {
-    const int half = warp >> 2;
+    float yu[4][4], yw[2][4];
     zero(yu);
     zero(yw);
-    gemm3<2, true, true>(yu, T, 16 * I, 16 * I, dE, 32 * half, 16 * I, 4 - I);
+    gemm3<2, true, true>(yu, T, 16 * I, 16 * I, dE, 32 * hk, 16 * I, 4 - I);
     gemm3<1, true, true>(yw, T, 16 * I, 16 * I, dW, 16 * hk, 16 * I, 4 - I);
-  }
-  __syncthreads();
-  {  // store YU, YW; dv = beta YU
-    const int half = warp >> 2;
+    __syncthreads();  // dE and dW fully read
     bf16* dvo = (bf16*)io.dv;
 #pragma unroll
-    for (int jj = 0; jj < 4; jj++)
+    for (int jt = 0; jt < 4; jt++)
 #pragma unroll
       for (int hh = 0; hh < 2; hh++) {
-        int r = 16 * I + gq + 8 * hh, col = 32 * half + 8 * jj + 2 * tq;
-        op_store2(YU, r, col, yu[jj][2 * hh], yu[jj][2 * hh + 1]);
-        if (r < L)
-          *reinterpret_cast<__nv_bfloat162*>(dvo + ((size_t)(t0 + r) * H + h) * DV + col) =
-              __floats2bfloat162_rn(sm.bet[r] * yu[jj][2 * hh], sm.bet[r] * yu[jj][2 * hh + 1]);
+        const int rr = 16 * I + gq + 8 * hh, col = 32 * hk + 8 * jt + 2 * tq;
+        op_store2(YU, rr, col, yu[jt][2 * hh], yu[jt][2 * hh + 1]);
+        if (rr < L)
+          *reinterpret_cast<__nv_bfloat162*>(dvo + ((size_t)(t0 + rr) * H + h) * DV + col) =
+              __floats2bfloat162_rn(sm.bet[rr] * yu[jt][2 * hh], sm.bet[rr] * yu[jt][2 * hh + 1]);
       }
 #pragma unroll
-    for (int jj = 0; jj < 2; jj++)
+    for (int jt = 0; jt < 2; jt++)
 #pragma unroll
-      for (int hh = 0; hh < 2; hh++)
-        op_store2(YW, 16 * I + gq + 8 * hh, 16 * hk + 8 * jj + 2 * tq, yw[jj][2 * hh], yw[jj][2 * hh + 1]);
+      for (int hh = 0; hh < 2; hh++) {
+        const int rr = 16 * I + gq + 8 * hh;
+        op_store2(YW, rr, 16 * hk + 8 * jt + 2 * tq, yw[jt][2 * hh], yw[jt][2 * hh + 1]);
+        yw[jt][2 * hh] *= sm.bet[rr];
+        yw[jt][2 * hh + 1] *= sm.bet[rr];
+      }
+    frag_store(w.gKG + ch * NTH * 8, yw);
   }
+  cp_wait_all();
   __syncthreads();
-  // ---- dbeta (U and W terms); dA = -(YU U^T + YW W^T) strict lower, fused with
-  //      dbeta += rowsum(dA .* A') and MA = beta_r dA (in place of A')
+  // ---- dbeta (U and W terms, row layout); dA, MA = beta dA (to bwd_gate) and the A' term
   {
-    {  // thread: row tid / 4, value columns 16 (tid % 4) .., key channels 8 (tid % 4) ..
-      const int r = tid >> 2, q4 = tid & 3;
-      float vv[16];
-      unpack8(vraw[0], vv);
-      unpack8(vraw[1], vv + 8);
-      float acc = 0.f;
+    float vv[16];
+    unpack8(vraw[0], vv);
+    unpack8(vraw[1], vv + 8);
+    float acc = 0.f;
 #pragma unroll
-      for (int e = 0; e < 16; e++) acc += op_get(YU, r, 16 * q4 + e) * vv[e];
+    for (int e = 0; e < 16; e++) acc += op_get(YU, r, 16 * q4 + e) * vv[e];
 #pragma unroll
-      for (int e = 0; e < 8; e++) {
-        const int i = 8 * q4 + e;
-        acc += op_get(YW, r, i) * sm.kh[r * SQ + i] * expf(sm.gg[r * SQ + i]);
+    for (int e = 0; e < 8; e++) acc += op_get(YW, r, 8 * q4 + e) * xkg[e];
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    if (q4 == 0) sm.dbet[r] = acc;
+  }
+  for (int t = warp; t < NBLK; t += NW) {
+    int bI, bJ;
+    blk_ij(t, bI, bJ);
+    float aa[2][4];
+    zero(aa);
+    gemm3<1, false, false>(aa, YU, 16 * bI, 0, U2, 16 * bJ, 0, DV / 16);
+    gemm3<1, false, false>(aa, YW, 16 * bI, 0, W2, 16 * bJ, 0, DK / 16);
+    float* g = w.gMA + (ch * NBLK + t) * 256;
+    const float* ab = A2 + t * 256;
+    float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+    for (int jt = 0; jt < 2; jt++)
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++) {
+        const int m = gq + 8 * hh, n = 8 * jt + 2 * tq;
+        const int rr = 16 * bI + m, s0 = 16 * bJ + n;
+        const float da0 = s0 < rr ? -aa[jt][2 * hh] : 0.f, da1 = s0 + 1 < rr ? -aa[jt][2 * hh + 1] : 0.f;
+        const float pa = da0 * ab[m * 16 + n] + da1 * ab[m * 16 + n + 1];
+        if (hh == 0) rs0 += pa; else rs1 += pa;
+        *reinterpret_cast<float2*>(g + m * 16 + n) = make_float2(sm.bet[rr] * da0, sm.bet[rr] * da1);
       }
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      if (q4 == 0 && r < L) sm.dbet[r] += acc;
-    }
-    for (int t = warp; t < 10; t += NW) {
-      const int bI = t < 1 ? 0 : t < 3 ? 1 : t < 6 ? 2 : 3, bJ = t - bI * (bI + 1) / 2;
-      float aa[2][4];
-      zero(aa);
-      gemm3<1, false, false>(aa, YU, 16 * bI, 0, U, 16 * bJ, 0, DV / 16);
-      gemm3<1, false, false>(aa, YW, 16 * bI, 0, W, 16 * bJ, 0, DK / 16);
-      float rs0 = 0.f, rs1 = 0.f;
-      each(aa, [&](int m, int n, float& v) {
-        const int r = 16 * bI + m, s2 = 16 * bJ + n;
-        const float da = s2 < r ? -v : 0.f;
-        const float pa = da * sm.am[r * SC + s2];
-        if (m < 8) rs0 += pa; else rs1 += pa;
-        sm.am[r * SC + s2] = sm.bet[r] * da;
-      });
-      rs0 += __shfl_xor_sync(0xffffffffu, rs0, 1);
-      rs0 += __shfl_xor_sync(0xffffffffu, rs0, 2);
-      rs1 += __shfl_xor_sync(0xffffffffu, rs1, 1);
-      rs1 += __shfl_xor_sync(0xffffffffu, rs1, 2);
-      if (tq == 0) {
-        sm.part[bJ * C + 16 * bI + gq] = rs0;
-        sm.part[bJ * C + 16 * bI + gq + 8] = rs1;
-      }
+    rs0 += __shfl_xor_sync(0xffffffffu, rs0, 1);
+    rs0 += __shfl_xor_sync(0xffffffffu, rs0, 2);
+    rs1 += __shfl_xor_sync(0xffffffffu, rs1, 1);
+    rs1 += __shfl_xor_sync(0xffffffffu, rs1, 2);
+    if (tq == 0) {
+      sm.part[bJ * C + 16 * bI + gq] = rs0;
+      sm.part[bJ * C + 16 * bI + gq + 8] = rs1;
     }
   }
   __syncthreads();
   if (tid < L) {  // fixed-order sum over the column blocks: deterministic
-    float acc = 0.f;
+    float acc = sm.dbet[tid];
     for (int J = 0; J <= (tid >> 4); J++) acc += sm.part[J * C + tid];
-    sm.dbet[tid] += acc;
+    ((bf16*)io.db)[(size_t)(t0 + tid) * H + h] = __float2bfloat16_rn(acc * sm.bet[tid] * sigmoid_f(-sm.braw[tid]));
   }
+}
+
+// bwd_gate: one CTA per chunk-head.  The pairwise decay-ratio terms of dq^,
+// dk^ and dG from dP' and MA (split tf32: their row and column sums enter dG
+// with opposite signs and must cancel in the cumulative sum), the remaining
+// dq^ / dk^ / dG terms, the reverse cumulative sum over the chunk into dg,
+// the gate backward (df and the per-chunk partials of dA_log and dt_bias)
+// and the L2-norm backward (dq, dk).
+struct GateSm {
+  float gg[C * SQ];           // G; then dq^
+  float dp[NBLK * 16 * PB];   // dP' lower blocks; then dk^
+  float ma[NBLK * 16 * PB];   // MA lower blocks; then dG - kdt and its suffix sums
+  bf16 rq[C * DK], rk[C * DK], rf[C * DK];
+  float inq[C], ink[C];
+  float gam[DK], dgam[DK];
+  float tot[NW * DK], ks[4 * DK], part[NW * DK], red[NW];
+  int spanok[4];
+};
+
+__global__ void __launch_bounds__(NTH, 2) bwd_gate_kernel(Dims d, BwdIO io, Ws w) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  GateSm& sm = *reinterpret_cast<GateSm*>(smraw);
+  const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  if (!saved_ok(d, w.tag, w.err)) return;
+  if (j >= *w.n_chunks) return;
+  const int L = w.chunk_len[j];
+  if (L <= 0) return;
+  const int t0 = w.chunk_tok0[j], H = d.H;
+  const int64_t ch = (int64_t)j * H + h;
+  const float a = expf(io.A_log[h]);
+  const float* dtb = io.dt_bias + h * DK;
+
+  // ---- group 1: raw q, k, f (rows past the chunk end zeroed);  group 2: dP', MA
+  for (int idx = tid; idx < C * 4; idx += NTH) {
+    const int r = idx >> 2, p = idx & 3, o = r * DK + 8 * p;
+    if (r < L) {
+      const size_t g = ((size_t)(t0 + r) * H + h) * DK + 8 * p;
+      cp16(sm.rq + o, (const bf16*)io.q + g);
+      cp16(sm.rk + o, (const bf16*)io.k + g);
+      cp16(sm.rf + o, (const bf16*)io.f + g);
+    } else {
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(sm.rq + o) = z;
+      *reinterpret_cast<uint4*>(sm.rk + o) = z;
+      *reinterpret_cast<uint4*>(sm.rf + o) = z;
+    }
+  }
+  cp_commit();
+  for (int idx = tid; idx < NBLK * 16 * 4; idx += NTH) {  // 4 x 16 B per block row
+    const int row = idx >> 2, p = idx & 3;
+    cp16(sm.dp + row * PB + 4 * p, w.gDP + ch * NBLK * 256 + row * 16 + 4 * p);
+    cp16(sm.ma + row * PB + 4 * p, w.gMA + ch * NBLK * 256 + row * 16 + 4 * p);
+  }
+  cp_commit();
+  if (tid < DK) sm.dgam[tid] = w.gdg[ch * DK + tid];
+  if (tid < 4) sm.spanok[tid] = 1;
+  asm volatile("cp.async.wait_group 1;\n" ::);
   __syncthreads();
-  float* MA = sm.am;
-  // ---- pairwise decay-ratio terms (owner tile rows 16I.., key columns 16hk..).
-  // Row and column sums of the same pair enter dG with opposite signs and
-  // must cancel in the cumulative sum, so these products keep ~21 bits.
+
+  // ---- q^, k^ norms and G (thread: row tid / 4, key channels 8 (tid % 4) ..)
+  {
+    const int r = tid >> 2, q4 = tid & 3;
+    float qv[8], kv[8], gv[8];
+    unpack8(*reinterpret_cast<const uint4*>(sm.rq + r * DK + 8 * q4), qv);
+    unpack8(*reinterpret_cast<const uint4*>(sm.rk + r * DK + 8 * q4), kv);
+    unpack8(*reinterpret_cast<const uint4*>(sm.rf + r * DK + 8 * q4), gv);
+    const bool in = r < L;
+    float sq = 0.f, sk = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; e++) {
+      gv[e] = in ? -a * softplus_f(gv[e] + dtb[8 * q4 + e]) : 0.f;
+      sq += qv[e] * qv[e];
+      sk += kv[e] * kv[e];
+    }
+    sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+    sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+    sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+    sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+    if (q4 == 0) {
+      sm.inq[r] = 1.0f / sqrtf(sq + L2_EPS);
+      sm.ink[r] = 1.0f / sqrtf(sk + L2_EPS);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; e++) {
+      float x = gv[e];
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        const float y2 = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y2;
+      }
+      gv[e] = x;
+    }
+    if (lane >= 28)
+#pragma unroll
+      for (int e = 0; e < 8; e++) sm.tot[warp * DK + 8 * q4 + e] = gv[e];
+    __syncthreads();
+    bool wide = false;
+#pragma unroll
+    for (int e = 0; e < 8; e++) {
+      float off = 0.f;
+      for (int w2 = 0; w2 < warp; w2++) off += sm.tot[w2 * DK + 8 * q4 + e];
+      gv[e] += off;
+      sm.gg[r * SQ + 8 * q4 + e] = gv[e];
+    }
+    __syncthreads();
+    const int I0 = r >> 4;
+#pragma unroll
+    for (int e = 0; e < 8; e++) {
+      const int i = 8 * q4 + e;
+      wide |= (r & 15) == 15 && sm.gg[(16 * I0) * SQ + i] - gv[e] > SPAN_MAX;
+      if (r == 0) sm.gam[i] = expf(sm.gg[(L - 1) * SQ + i]);
+    }
+    if (wide) sm.spanok[I0] = 0;
+  }
+  float dQG[2][4], dKD[2][4], dkg[2][4];
+  frag_load(w.gQG + ch * NTH * 8, dQG);
+  frag_load(w.gKD + ch * NTH * 8, dKD);
+  frag_load(w.gKG + ch * NTH * 8, dkg);
+  cp_wait_all();
+  __syncthreads();
+
+  const int I = warp & 3, hk = warp >> 2;  // owner tile: rows 16 I .., key columns 16 hk ..
+  const bool ok = sm.spanok[I];
+  const float* gbI = sm.gg + (16 * I) * SQ;       // G at the block's first row
+  const float* geI = sm.gg + (16 * I + 15) * SQ;  // and at its last
+  // ---- pairwise terms: prow / arow (columns s of blocks J <= I), col (rows r of blocks I2 >= I)
   float prow[2][4], arow[2][4], col[2][4];
   zero(prow);
   zero(arow);
   zero(col);
-  {
-    const bool ok = sm.spanok[I];
-    for (int J = 0; J <= I; J++) {
-      if (J == I && !ok) break;
-      const float* scl = J < I ? sm.dd + pidx(I, J) * DK : sm.ei + I * DK;
-      auto fbR = [&](int k, int jj, int n) { return sm.rr[(16 * J + k) * SQ + 16 * hk + 8 * jj + n] * scl[16 * hk + 8 * jj + n]; };
-      rows16<2, true>(prow, 2, [&](int m, int k) { return DP[(16 * I + m) * SC + 16 * J + k]; }, fbR);
-      rows16<2, true>(arow, 2, [&](int m, int k) { return MA[(16 * I + m) * SC + 16 * J + k]; }, fbR);
-    }
-    // col terms of columns s in block I: rows r in blocks I2 >= I
-    for (int I2 = I; I2 < 4; I2++) {
-      if (I2 == I && !ok) continue;
-      const float* scl = I2 > I ? sm.dd + pidx(I2, I) * DK : sm.ei + I * DK;
-      rows16<2, true>(col, 2, [&](int m, int k) { return DP[(16 * I2 + k) * SC + 16 * I + m]; },
-                [&](int k, int jj, int n) { return sm.lq[(16 * I2 + k) * SQ + 16 * hk + 8 * jj + n] * scl[16 * hk + 8 * jj + n]; });
-      rows16<2, true>(col, 2, [&](int m, int k) { return MA[(16 * I2 + k) * SC + 16 * I + m]; },
-                [&](int k, int jj, int n) { return sm.lk[(16 * I2 + k) * SQ + 16 * hk + 8 * jj + n] * scl[16 * hk + 8 * jj + n]; });
-    }
+  for (int J = 0; J <= I; J++) {
+    if (J == I && !ok) break;
+    const float* DPb = sm.dp + blk_of(I, J) * 16 * PB;
+    const float* MAb = sm.ma + blk_of(I, J) * 16 * PB;
+    rows16_2a<2>(prow, arow, 2, [&](int m, int k) { return DPb[m * PB + k]; },
+                 [&](int m, int k) { return MAb[m * PB + k]; },
+                 [&](int k, int jj, int n) {
+                   const int s = 16 * J + k, i = 16 * hk + 8 * jj + n;
+                   return bfl(sm.rk[s * DK + i]) * sm.ink[s] * expf(fminf(gbI[i] - sm.gg[s * SQ + i], SPAN_MAX));
+                 });
   }
-  // ---- assemble dq^, dk^, dG per owned element
-  float dqh[2][4], dkh[2][4], dG[2][4], kdt[2][4];
+  for (int I2 = I; I2 < 4; I2++) {
+    if (I2 == I && !ok) continue;
+    const float* DPb = sm.dp + blk_of(I2, I) * 16 * PB;
+    const float* MAb = sm.ma + blk_of(I2, I) * 16 * PB;
+    rows16_ab<2>(col, 2, [&](int m, int k) { return DPb[k * PB + m]; },
+                 [&](int m, int k) { return MAb[k * PB + m]; },
+                 [&](int k, int jj, int n) {
+                   const int rr = 16 * I2 + k, i = 16 * hk + 8 * jj + n;
+                   const float x = expf(fminf(sm.gg[rr * SQ + i] - geI[i], SPAN_MAX));
+                   return make_float2(bfl(sm.rq[rr * DK + i]) * sm.inq[rr] * x, bfl(sm.rk[rr * DK + i]) * sm.ink[rr] * x);
+                 });
+  }
+  // ---- assemble dq^, dk^, dG - kdt per owned element; column totals of kdt
+  float dqh[2][4], dkh[2][4], dGk[2][4], kcol[2][2];
   {
-    const bool ok = sm.spanok[I];
-    const bf16* qg_ = (const bf16*)io.q;
-    const bf16* kg_ = (const bf16*)io.k;
+    const float* DPd = sm.dp + blk_of(I, I) * 16 * PB;
+    const float* MAd = sm.ma + blk_of(I, I) * 16 * PB;
 #pragma unroll
-    for (int jj = 0; jj < 2; jj++)
+    for (int jj = 0; jj < 2; jj++) {
+      kcol[jj][0] = kcol[jj][1] = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; e++) {
-        const int r = 16 * I + gq + 8 * (e >> 1), i = 16 * hk + 8 * jj + 2 * tq + (e & 1);
-        const float G = sm.gg[r * SQ + i];
-        const float eL = expf(G - sm.gb[I * DK + i]), eR = expf(sm.ge[I * DK + i] - G);
+        const int m = gq + 8 * (e >> 1), rr = 16 * I + m, i = 16 * hk + 8 * jj + 2 * tq + (e & 1);
+        const float G = sm.gg[rr * SQ + i];
+        const float eL = expf(G - gbI[i]), eR = expf(geI[i] - G);
         float pr = prow[jj][e] * eL, ar = arow[jj][e] * eL, cl = col[jj][e] * eR;
-        if (!ok) {  // exact diagonal-block terms
-          const float* Gr = sm.gg + r * SQ;
-          for (int s = 16 * I; s < 16 * I + 16 && s < L; s++) {  // rows past the chunk end are zero
-            float ks = bfl(kg_[((size_t)(t0 + s) * H + h) * DK + i]) * sm.ink[s];
-            float qs = bfl(qg_[((size_t)(t0 + s) * H + h) * DK + i]) * sm.inq[s];
-            if (s <= r) {
-              float ex = expf(Gr[i] - sm.gg[s * SQ + i]);
-              pr += DP[r * SC + s] * ks * ex;
-              ar += MA[r * SC + s] * ks * ex;
+        if (!ok) {  // exact diagonal-block terms (rows past the chunk end are zero)
+          for (int s = 16 * I; s < 16 * I + 16 && s < L; s++) {
+            const int n = s - 16 * I;
+            const float ks = bfl(sm.rk[s * DK + i]) * sm.ink[s], qs = bfl(sm.rq[s * DK + i]) * sm.inq[s];
+            if (s <= rr) {
+              const float ex = expf(G - sm.gg[s * SQ + i]);
+              pr += DPd[m * PB + n] * ks * ex;
+              ar += MAd[m * PB + n] * ks * ex;
             }
-            if (s >= r) {
-              float ex = expf(sm.gg[s * SQ + i] - Gr[i]);
-              cl += (DP[s * SC + r] * qs + MA[s * SC + r] * ks) * ex;
+            if (s >= rr) {
+              const float ex = expf(sm.gg[s * SQ + i] - G);
+              cl += (DPd[n * PB + m] * qs + MAd[n * PB + m] * ks) * ex;
             }
           }
         }
-        const float q = sm.qh[r * SQ + i], k = sm.kh[r * SQ + i];
-        const float Gm = expf(G), kdf = expf(sm.gl[i] - G);
-        const float dkg = sm.bet[r] * yw[jj][e];
+        const float q = bfl(sm.rq[rr * DK + i]) * sm.inq[rr], k = bfl(sm.rk[rr * DK + i]) * sm.ink[rr];
+        const float Gm = expf(G), kdf = expf(sm.gg[(L - 1) * SQ + i] - G);
+        const float kdt = dKD[jj][e] * k * kdf;
         dqh[jj][e] = pr + dQG[jj][e] * Gm;
-        dkh[jj][e] = ar + cl + dkg * Gm + dKD[jj][e] * kdf;
-        dG[jj][e] = q * pr + k * ar - k * cl + dQG[jj][e] * q * Gm + dkg * k * Gm;
-        kdt[jj][e] = dKD[jj][e] * k * kdf;
+        dkh[jj][e] = ar + cl + dkg[jj][e] * Gm + dKD[jj][e] * kdf;
+        dGk[jj][e] = q * pr + k * ar - k * cl + dQG[jj][e] * q * Gm + dkg[jj][e] * k * Gm - kdt;
+        kcol[jj][e & 1] += kdt;
       }
+    }
   }
-  __syncthreads();  // everyone is done reading lq, lk, rr, dP', MA
-  float* dqs = sm.lq;
-  float* dks = sm.lk;
-  float* dGs = sm.rr;
-  float* kdts = sm.tm;  // [C][SQ] over dP'
-  float* sfx = sm.am;   // local suffix sums [C][SC] over MA
 #pragma unroll
   for (int jj = 0; jj < 2; jj++)
 #pragma unroll
-    for (int e = 0; e < 4; e++) {
-      const int r = 16 * I + gq + 8 * (e >> 1), i = 16 * hk + 8 * jj + 2 * tq + (e & 1);
-      dqs[r * SQ + i] = dqh[jj][e];
-      dks[r * SQ + i] = dkh[jj][e];
-      dGs[r * SQ + i] = dG[jj][e];
-      kdts[r * SQ + i] = kdt[jj][e];
+    for (int c2 = 0; c2 < 2; c2++) {
+      float x = kcol[jj][c2];
+      x += __shfl_xor_sync(0xffffffffu, x, 4);
+      x += __shfl_xor_sync(0xffffffffu, x, 8);
+      x += __shfl_xor_sync(0xffffffffu, x, 16);
+      kcol[jj][c2] = x;
     }
+  __syncthreads();  // every read of G, dP' and MA is done
+  float* dqs = sm.gg;
+  float* dks = sm.dp;
+  float* dgs = sm.ma;
+#pragma unroll
+  for (int jj = 0; jj < 2; jj++) {
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+      const int rr = 16 * I + gq + 8 * (e >> 1), i = 16 * hk + 8 * jj + 2 * tq + (e & 1);
+      dqs[rr * SQ + i] = dqh[jj][e];
+      dks[rr * SQ + i] = dkh[jj][e];
+      dgs[rr * SQ + i] = dGk[jj][e];
+    }
+    if (gq == 0) {
+      sm.ks[I * DK + 16 * hk + 8 * jj + 2 * tq] = kcol[jj][0];
+      sm.ks[I * DK + 16 * hk + 8 * jj + 2 * tq + 1] = kcol[jj][1];
+    }
+  }
   __syncthreads();
-  // ---- reverse cumulative sum of dG over the chunk (with the G_last terms):
+  // ---- reverse cumulative sum over the chunk:
   //      dg_t = sum_{r >= t} (dG_r - kdt_r) + sum_r kdt_r + dgamma gamma
   {
-    float run = 0.f, ksum = 0.f;
+    float run = 0.f;
     for (int m = 7; m >= 0; m--) {
-      int r = 8 * warp + m;
-      if (r < L) {
-        run += dGs[r * SQ + lane] - kdts[r * SQ + lane];
-        ksum += kdts[r * SQ + lane];
-      }
-      sfx[r * SC + lane] = run;
+      const int rr = 8 * warp + m;
+      run += dgs[rr * SQ + lane];
+      dgs[rr * SQ + lane] = run;
     }
     sm.tot[warp * DK + lane] = run;
-    sm.ks[warp * DK + lane] = ksum;
   }
   __syncthreads();
   {
     float off = sm.dgam[lane] * sm.gam[lane];
-    for (int w2 = 0; w2 < NW; w2++) off += sm.ks[w2 * DK + lane];   // sum_r kdt_r
+    for (int i4 = 0; i4 < 4; i4++) off += sm.ks[i4 * DK + lane];
     for (int w2 = warp + 1; w2 < NW; w2++) off += sm.tot[w2 * DK + lane];
     bf16* dfo = (bf16*)io.df;
     float pdt = 0.f, pA = 0.f;
     for (int m = 0; m < 8; m++) {
-      int r = 8 * warp + m;
-      if (r < L) {
-        float dg = sfx[r * SC + lane] + off;
-        float x = bfl(sm.fr[r * DK + lane]) + dtb[lane];
-        float g = -a * softplus_f(x);
-        float dx = dg * (-a) * sigmoid_f(x);
-        dfo[((size_t)(t0 + r) * H + h) * DK + lane] = __float2bfloat16_rn(dx);
+      const int rr = 8 * warp + m;
+      if (rr < L) {
+        const float dg = dgs[rr * SQ + lane] + off;
+        const float x = bfl(sm.rf[rr * DK + lane]) + dtb[lane];
+        const float g = -a * softplus_f(x);
+        const float dx = dg * (-a) * sigmoid_f(x);
+        dfo[((size_t)(t0 + rr) * H + h) * DK + lane] = __float2bfloat16_rn(dx);
         pdt += dx;
         pA += dg * g;
       }
@@ -1430,14 +1567,19 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
     for (int w2 = 0; w2 < NW; w2++) s += sm.red[w2];
     w.pA[ch] = s;
   }
-  // ---- L2-norm backward, db (thread: row tid / 4, key channels 8 (tid % 4) ..)
+  // ---- L2-norm backward (thread: row tid / 4, key channels 8 (tid % 4) ..)
   {
     const int r = tid >> 2, q4 = tid & 3;
     float qv[8], kv[8], dqv[8], dkv[8], pq = 0.f, pk = 0.f;
+    unpack8(*reinterpret_cast<const uint4*>(sm.rq + r * DK + 8 * q4), qv);
+    unpack8(*reinterpret_cast<const uint4*>(sm.rk + r * DK + 8 * q4), kv);
+    const float iq = sm.inq[r], ik = sm.ink[r];
 #pragma unroll
     for (int e = 0; e < 8; e++) {
-      const int i = r * SQ + 8 * q4 + e;
-      qv[e] = sm.qh[i]; kv[e] = sm.kh[i]; dqv[e] = dqs[i]; dkv[e] = dks[i];
+      qv[e] *= iq;
+      kv[e] *= ik;
+      dqv[e] = dqs[r * SQ + 8 * q4 + e];
+      dkv[e] = dks[r * SQ + 8 * q4 + e];
       pq += qv[e] * dqv[e];
       pk += kv[e] * dkv[e];
     }
@@ -1451,17 +1593,12 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
       __nv_bfloat162* pk2 = reinterpret_cast<__nv_bfloat162*>(&uk);
 #pragma unroll
       for (int e = 0; e < 4; e++) {
-        pq2[e] = __floats2bfloat162_rn((dqv[2 * e] - qv[2 * e] * pq) * sm.inq[r],
-                                       (dqv[2 * e + 1] - qv[2 * e + 1] * pq) * sm.inq[r]);
-        pk2[e] = __floats2bfloat162_rn((dkv[2 * e] - kv[2 * e] * pk) * sm.ink[r],
-                                       (dkv[2 * e + 1] - kv[2 * e + 1] * pk) * sm.ink[r]);
+        pq2[e] = __floats2bfloat162_rn((dqv[2 * e] - qv[2 * e] * pq) * iq, (dqv[2 * e + 1] - qv[2 * e + 1] * pq) * iq);
+        pk2[e] = __floats2bfloat162_rn((dkv[2 * e] - kv[2 * e] * pk) * ik, (dkv[2 * e + 1] - kv[2 * e + 1] * pk) * ik);
       }
       const size_t off = ((size_t)(t0 + r) * H + h) * DK + 8 * q4;
       *reinterpret_cast<uint4*>((bf16*)io.dq + off) = uq;
       *reinterpret_cast<uint4*>((bf16*)io.dk + off) = uk;
-      if (q4 == 0)
-        ((bf16*)io.db)[(size_t)(t0 + r) * H + h] =
-            __float2bfloat16_rn(sm.dbet[r] * sm.bet[r] * sigmoid_f(-sm.braw[r]));
     }
   }
 }
@@ -1471,7 +1608,8 @@ __global__ void __launch_bounds__(NTH, 1) bwd_chunk_kernel(Dims d, BwdIO io, Ws 
 static_assert(sizeof(fast::FwdSm) <= 232448, "fused forward shared memory exceeds 227 KB");
 static_assert(sizeof(fast::ChunkSm) <= 113 * 1024, "per-chunk forward must fit two CTAs per SM");
 static_assert(sizeof(fast::StateSm) <= 113 * 1024, "state chain must fit two CTAs per SM");
-static_assert(sizeof(fast::BwdSm) <= 232448, "backward chunk shared memory exceeds 227 KB");
+static_assert(sizeof(fast::GradSm) <= 112 * 1024, "chunk-gradient kernel must fit two CTAs per SM");
+static_assert(sizeof(fast::GateSm) <= 112 * 1024, "gate kernel must fit two CTAs per SM");
 
 bool fast_path(int dtype, int dk, int dv) { return dtype == 0 && dk == fast::DK && dv == fast::DV; }
 
@@ -1508,12 +1646,19 @@ cudaError_t launch_fast_bwd(const Dims& d, const BwdIO& io, const Ws& w, cudaStr
   prof_end(K_BWD_SCAN, st);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t smem = sizeof(fast::BwdSm);
-  e = cudaFuncSetAttribute(fast::bwd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t s1 = sizeof(fast::GradSm), s2 = sizeof(fast::GateSm);
+  e = cudaFuncSetAttribute(fast::bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fast::bwd_gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
   if (e != cudaSuccess) return e;
-  prof_begin(K_BWD_CHUNK, st);
-  fast::bwd_chunk_kernel<<<dim3(d.nc_max, d.H), fast::NTH, smem, st>>>(d, io, w);
-  prof_end(K_BWD_CHUNK, st);
+  prof_begin(K_BWD_GRAD, st);
+  fast::bwd_grad_kernel<<<dim3(d.nc_max, d.H), fast::NTH, s1, st>>>(d, io, w);
+  prof_end(K_BWD_GRAD, st);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  prof_begin(K_BWD_GATE, st);
+  fast::bwd_gate_kernel<<<dim3(d.nc_max, d.H), fast::NTH, s2, st>>>(d, io, w);
+  prof_end(K_BWD_GATE, st);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_bwd_reduce(d, io, w, st);

@@ -20,9 +20,10 @@ enum KernelId {
   K_BWD_INTRA,
   K_BWD_REDUCE,
   K_FWD_CHAIN,
-  K_BWD_CHUNK,
   K_FWD_CHUNK,
   K_FWD_STATE,
+  K_BWD_GRAD,
+  K_BWD_GATE,
   K_COUNT
 };
 
@@ -48,6 +49,15 @@ struct Ws {
   float* QW;   // [ch][C][dk]  QG - P W            (tensor-core path; the backward scan reads it)
   float* KU;   // [ch][dk][dv] KD^T U              (tensor-core forward scratch)
   float* PU;   // [ch][C][dv]  P U                 (tensor-core forward scratch)
+  // tensor-core path, split-bf16 operand tiles (hi tile, then lo tile) saved
+  // by the forward: S entering the chunk, T, P = scale P', W, U; and the
+  // state gradient leaving the chunk from the backward scan
+  __nv_bfloat16 *sS, *sT, *sP, *sW, *sU, *sdS;
+  float* sA;   // [ch][10][16][16] A' (unscaled) lower 16 x 16 blocks
+  // tensor-core backward, bwd_grad -> bwd_gate
+  float *gDP, *gMA;        // [ch][10][16][16] dP', beta dA lower blocks
+  float *gQG, *gKD, *gKG;  // [ch][256 threads][8] dQG, dKD, beta YW in fragment order
+  float* gdg;              // [ch][dk] dgamma
   // backward
   float* dE;   // [ch][C][dv]  gradient of E = U - W S
   float* dSn;  // [ch][dk][dv] gradient of the state leaving the chunk

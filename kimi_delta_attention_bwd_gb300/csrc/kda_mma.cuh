@@ -1,5 +1,6 @@
-// Warp-level tensor-core helpers (mma.sync m16n8k8, tf32 operands, fp32
-// accumulate) and cp.async staging used by the dk=32 / dv=64 kernels.
+// Warp-level tensor-core helpers (mma.sync: tf32 m16n8k8 and bf16 m16n8k16,
+// fp32 accumulate), split-operand tiles and cp.async staging used by the
+// dk=32 / dv=64 kernels.
 #pragma once
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -54,6 +55,78 @@ __device__ __forceinline__ void rows16(float (&acc)[NT][4], int ksteps, FA fa, F
         mma_tf32(acc[j], a0, a1, a2, a3, h0, h1);
       }
       if (SPLIT && !AX) mma_tf32(acc[j], l0, l1, l2, l3, b0, b1);
+    }
+  }
+}
+
+// Split-tf32 helpers of the pairwise decay terms (3 products each, ~21 bits).
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = tf32(x);
+  lo = tf32(x - __uint_as_float(hi));
+}
+
+// acc1 += A1 B and acc2 += A2 B (16 x 8 NT tiles over K = 8 ksteps): two A
+// operands share each B fragment.  fb(k, j, n) gives B(k, 8 j + n).
+template <int NT, class FA1, class FA2, class FB>
+__device__ __forceinline__ void rows16_2a(float (&acc1)[NT][4], float (&acc2)[NT][4], int ksteps, FA1 fa1, FA2 fa2,
+                                          FB fb) {
+  const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
+  for (int ks = 0; ks < ksteps; ks++) {
+    const int kk = ks * 8 + tq;
+    uint32_t a[4], al[4], c[4], cl[4];
+    split_tf32(fa1(gq, kk), a[0], al[0]);
+    split_tf32(fa1(gq + 8, kk), a[1], al[1]);
+    split_tf32(fa1(gq, kk + 4), a[2], al[2]);
+    split_tf32(fa1(gq + 8, kk + 4), a[3], al[3]);
+    split_tf32(fa2(gq, kk), c[0], cl[0]);
+    split_tf32(fa2(gq + 8, kk), c[1], cl[1]);
+    split_tf32(fa2(gq, kk + 4), c[2], cl[2]);
+    split_tf32(fa2(gq + 8, kk + 4), c[3], cl[3]);
+#pragma unroll
+    for (int j = 0; j < NT; j++) {
+      uint32_t b0, b0l, b1, b1l;
+      split_tf32(fb(kk, j, gq), b0, b0l);
+      split_tf32(fb(kk + 4, j, gq), b1, b1l);
+      mma_tf32(acc1[j], a[0], a[1], a[2], a[3], b0, b1);
+      mma_tf32(acc1[j], a[0], a[1], a[2], a[3], b0l, b1l);
+      mma_tf32(acc1[j], al[0], al[1], al[2], al[3], b0, b1);
+      mma_tf32(acc2[j], c[0], c[1], c[2], c[3], b0, b1);
+      mma_tf32(acc2[j], c[0], c[1], c[2], c[3], b0l, b1l);
+      mma_tf32(acc2[j], cl[0], cl[1], cl[2], cl[3], b0, b1);
+    }
+  }
+}
+
+// acc += A1 B1 + A2 B2 (16 x 8 NT tiles over K = 8 ksteps); fb(k, j, n)
+// returns the pair (B1(k, 8 j + n), B2(k, 8 j + n)).
+template <int NT, class FA1, class FA2, class FB>
+__device__ __forceinline__ void rows16_ab(float (&acc)[NT][4], int ksteps, FA1 fa1, FA2 fa2, FB fb) {
+  const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
+  for (int ks = 0; ks < ksteps; ks++) {
+    const int kk = ks * 8 + tq;
+    uint32_t a[4], al[4], c[4], cl[4];
+    split_tf32(fa1(gq, kk), a[0], al[0]);
+    split_tf32(fa1(gq + 8, kk), a[1], al[1]);
+    split_tf32(fa1(gq, kk + 4), a[2], al[2]);
+    split_tf32(fa1(gq + 8, kk + 4), a[3], al[3]);
+    split_tf32(fa2(gq, kk), c[0], cl[0]);
+    split_tf32(fa2(gq + 8, kk), c[1], cl[1]);
+    split_tf32(fa2(gq, kk + 4), c[2], cl[2]);
+    split_tf32(fa2(gq + 8, kk + 4), c[3], cl[3]);
+#pragma unroll
+    for (int j = 0; j < NT; j++) {
+      const float2 v0 = fb(kk, j, gq), v1 = fb(kk + 4, j, gq);
+      uint32_t b0, b0l, b1, b1l, d0, d0l, d1, d1l;
+      split_tf32(v0.x, b0, b0l);
+      split_tf32(v1.x, b1, b1l);
+      split_tf32(v0.y, d0, d0l);
+      split_tf32(v1.y, d1, d1l);
+      mma_tf32(acc[j], a[0], a[1], a[2], a[3], b0, b1);
+      mma_tf32(acc[j], a[0], a[1], a[2], a[3], b0l, b1l);
+      mma_tf32(acc[j], al[0], al[1], al[2], al[3], b0, b1);
+      mma_tf32(acc[j], c[0], c[1], c[2], c[3], d0, d1);
+      mma_tf32(acc[j], c[0], c[1], c[2], c[3], d0l, d1l);
+      mma_tf32(acc[j], cl[0], cl[1], cl[2], cl[3], d0, d1);
     }
   }
 }
