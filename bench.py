@@ -54,10 +54,11 @@ def algorithmic_bytes(w, kernel: str) -> float:
     per = {
         "fwd_chain": inputs_fwd + e * dv,       # reads q, k, f, v, b; writes o
         "fwd_chunk": inputs_fwd,                # reads q, k, f, v, b
-        "fwd_state": e * dv,                    # writes o
+        "fwd_out": e * dv,                      # writes o
         "fwd_intra": inputs_fwd,
         "fwd_scan": e * dv,                     # o
-        "bwd_scan": e * dv,                     # dO
+        "bwd_scan": e * dv,                     # dO (general path)
+        "bwd_x": e * dv,                        # reads dO
         "bwd_grad": e * (dk + dv + 1) + e * dv + e * (dv + 1),  # reads k, f, v, b, dO; writes dv, db
         "bwd_gate": e * 3 * dk + e * 3 * dk,    # reads q, k, f; writes dq, dk, df
         "bwd_intra": inputs_fwd + e * dv + grads,

@@ -153,9 +153,9 @@ static Layout layout(const Dims& d, int for_bwd, bool fused = false) {
       L.off_QW = take(4 * nch * C * d.dk);
       L.off_KU = take(4 * nch * d.dk * d.dv);
       L.off_PU = take(4 * nch * C * d.dv);
+      L.off_Sent = take(4 * nch * d.dk * d.dv);  // split-bf16 tiles: 4 bytes per element
     }
     if (for_bwd) {
-      L.off_Sent = take(4 * nch * d.dk * d.dv);  // split-bf16 tiles: 4 bytes per element
       L.off_dSn = take(4 * nch * d.dk * d.dv);
       L.off_pA = take(4 * nch);
       L.off_pdt = take(4 * nch * d.dk);
@@ -195,6 +195,7 @@ static Layout layout(const Dims& d, int for_bwd, bool fused = false) {
 static Ws bind(void* ws, const Layout& L, const Dims& d, int for_bwd) {
   char* p = (char*)ws;
   auto at = [&](size_t off) { return off ? (float*)(p + off) : nullptr; };
+  auto bat = [&](size_t off) { return off ? (__nv_bfloat16*)(p + off) : nullptr; };
   Ws w;
   w.err = (int32_t*)(p + L.off_err);
   w.tag = (int32_t*)(p + L.off_err + 4);
@@ -210,8 +211,8 @@ static Ws bind(void* ws, const Layout& L, const Dims& d, int for_bwd) {
   w.KD = at(L.off_KD);
   w.gam = at(L.off_gam);
   w.Sent = for_bwd ? at(L.off_Sent) : nullptr;
-  w.M = at(L.off_M);
-  w.QW = at(L.off_QW);
+  w.sM = bat(L.off_M);
+  w.sQW = bat(L.off_QW);
   w.KU = at(L.off_KU);
   w.PU = at(L.off_PU);
   w.dE = for_bwd ? at(L.off_dE) : nullptr;
@@ -220,8 +221,7 @@ static Ws bind(void* ws, const Layout& L, const Dims& d, int for_bwd) {
   w.pdt = for_bwd ? at(L.off_pdt) : nullptr;
   w.scr = for_bwd ? at(L.off_scr) : nullptr;
   w.scr_per_ch = bwd_scratch_floats(d.dk, d.dv);
-  auto bat = [&](size_t off) { return off ? (__nv_bfloat16*)(p + off) : nullptr; };
-  w.sS = d.fast && for_bwd ? bat(L.off_Sent) : nullptr;
+  w.sS = d.fast ? bat(L.off_Sent) : nullptr;
   w.sdS = d.fast && for_bwd ? bat(L.off_dSn) : nullptr;
   w.sT = bat(L.off_sT);
   w.sP = bat(L.off_sP);

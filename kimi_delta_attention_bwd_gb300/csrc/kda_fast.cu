@@ -494,9 +494,7 @@ __global__ void __launch_bounds__(NTH, 1) fwd_chain_kernel(Dims d, FwdIO io, Ws 
 //   QW = QG - P W               [C x dk]       PU = P U      [C x dv]
 // so that the chunk's state update and output are
 //   S' = M S + KU,   O = QW S + PU.
-// fwd_state then walks each document's chunks with S in shared memory; the
-// chain carries only these two small products, and it splits over value
-// columns (S, KU, PU and O columns are independent).
+// fwd_state then carries S through each document's chunks and writes O.
 
 // Rows of the decay-ratio right operands: R_I holds k^_s exp(G_first(I) - G_s)
 // for the 16 (I + 1) rows s of blocks J <= I, stacked from row 8 I (I + 1).
@@ -516,10 +514,29 @@ struct ChunkSm {
   int spanok[4];
 };
 
+// cp.async of `bytes` (a multiple of 16) from global to shared, all threads.
+__device__ __forceinline__ void cp_bytes(void* dst, const void* src, int bytes) {
+  for (int o = threadIdx.x * 16; o < bytes; o += NTH * 16) cp16((char*)dst + o, (const char*)src + o);
+}
+
 // Copies `bytes` (a multiple of 16) from shared to global memory, all threads.
 __device__ __forceinline__ void copy16(void* g, const void* smem, int bytes) {
   for (int o = threadIdx.x * 16; o < bytes; o += NTH * 16)
     *reinterpret_cast<uint4*>((char*)g + o) = *reinterpret_cast<const uint4*>((const char*)smem + o);
+}
+
+// Stores a 16 x (8 NT) accumulator tile at (r0, c0) of a split operand tile
+// (global or shared), mapping each value through fn(r, c, v).
+template <int NT, class F>
+__device__ __forceinline__ void store_acc_op(const float (&acc)[NT][4], const Op& g, int r0, int c0, F fn) {
+  const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+  for (int jt = 0; jt < NT; jt++)
+#pragma unroll
+    for (int hh = 0; hh < 2; hh++) {
+      const int r = r0 + gq + 8 * hh, c = c0 + 8 * jt + 2 * tq;
+      op_store2(g, r, c, fn(r, c, acc[jt][2 * hh]), fn(r, c + 1, acc[jt][2 * hh + 1]));
+    }
 }
 
 // Stores a 16 x (8 NT) accumulator tile to a row-major fp32 matrix with
@@ -753,12 +770,12 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     copy16(w.sW + ch * 2 * C * DK, W.hi, 4 * C * DK);
     copy16(w.sU + ch * 2 * C * DV, U.hi, 4 * C * DV);
   }
-  {  // outputs (fp32): PU and QW by row block, then the 16 x 16 tiles of M | KU
+  {  // outputs: PU and QW by row block, then the 16 x 16 tiles of M | KU (M, QW split)
     const int wI = warp & 3, half = warp >> 2;
     float* PUg = w.PU + ch * C * DV;
-    float* QWg = w.QW + ch * C * DK;
-    float* Mg = w.M + ch * DK * DK;
     float* KUg = w.KU + ch * DK * DV;
+    const Op QWg{w.sQW + ch * 2 * C * DK, w.sQW + ch * 2 * C * DK + C * DK, DK};
+    const Op Mg{w.sM + ch * 2 * DK * DK, w.sM + ch * 2 * DK * DK + DK * DK, DK};
     {
       float acc[4][4];
       zero(acc);
@@ -769,7 +786,7 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
       float acc[2][4];
       zero(acc);
       gemm3<1, false, true>(acc, P, 16 * wI, 0, W, 16 * half, 0, wI + 1);
-      store_acc(acc, QWg, DK, 16 * wI, 16 * half, [&](int rr, int c, float v) { return op_get(QG, rr, c) - v; });
+      store_acc_op(acc, QWg, 16 * wI, 16 * half, [&](int rr, int c, float v) { return op_get(QG, rr, c) - v; });
     }
     // 12 tiles t = 6 mi + cc (cc < 2: M columns 16 cc, else KU columns 16 (cc - 2)),
     // dealt so that the warps with short row blocks above take more
@@ -781,8 +798,7 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
       zero(acc);
       if (cc < 2) {
         gemm3<1, true, true>(acc, KD, 16 * mi, 0, W, 16 * cc, 0, C / 16);
-        store_acc(acc, Mg, DK, 16 * mi, 16 * cc,
-                  [&](int i, int jc, float v) { return (i == jc ? sm.gam[i] : 0.f) - v; });
+        store_acc_op(acc, Mg, 16 * mi, 16 * cc, [&](int i, int jc, float v) { return (i == jc ? sm.gam[i] : 0.f) - v; });
       } else {
         gemm3<1, true, true>(acc, KD, 16 * mi, 0, U, 16 * (cc - 2), 0, C / 16);
         store_acc(acc, KUg, DV, 16 * mi, 16 * (cc - 2), [](int, int, float v) { return v; });
@@ -791,185 +807,230 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
   }
 }
 
-// fwd_state: one CTA per (document, head, NS2 value columns).  The next
-// chunks' M, KU, QW and PU stream in through a three-stage cp.async ring
-// while the current chunk computes; only S' = M S + KU is on the chain.
-constexpr int NS2 = 32;        // value columns per state CTA
-constexpr int SB2 = NS2 + 8;   // row stride of [*][NS2] arrays
+// ------------------------------------------------------------ state chains
+// Both chains are affine recurrences over a document's chunks,
+//   forward:   S_{c+1} = M_c S_c + KU_c,        O_c = QW_c S_c + PU_c
+//   backward:  dS_c    = M_c^T dS_{c+1} + QW_c^T dO_c
+// (from h0 / dh_final; the last state is h_final / dh0).  Value columns are
+// independent: one CTA of four warps per (document, head, 32 value columns)
+// carries a 32 x 32 slice as a split-bf16 operand tile in shared memory and
+// streams the chunk's operands through a three-stage cp.async ring.  Only the
+// state product is on the chain; the output (forward) and QW^T dO (backward)
+// take the same step's other warps' slack.  Each step also stores the carried
+// state (S entering the chunk, dS leaving it) as a split operand tile for the
+// per-chunk kernels.  The fp32 state rounds to ~16 bits only as an operand;
+// h_final and dh0 are the fp32 accumulators.
+constexpr int NSC = 32;   // value columns per chain CTA
 constexpr int NSTG = 3;
-struct StateStage {
-  float M[DK * SQ];
-  float QW[C * SQ];
-  float KU[DK * SB2];
-  float PU[C * SB2];
+constexpr int CTH = 128;  // chain threads
+
+// Copies the 32 x NSC slice tile (K = NSC) into columns col0.. of the chunk's
+// full 32 x dv state tile (K = dv) in global memory: whole 8 x 8 core matrices.
+__device__ __forceinline__ void slice_to_global(bf16* g, const bf16* s, int col0) {
+  for (int idx = threadIdx.x; idx < 2 * 16 * 8; idx += CTH) {  // (hi|lo) x 16 cores x 8 uint4
+    const int part = idx >> 7, core = (idx >> 3) & 15, q = idx & 7;
+    const int rb = core >> 2, kb = core & 3;
+    const uint4 v = *reinterpret_cast<const uint4*>(s + part * DK * NSC + (rb * (NSC / 8) + kb) * 64 + q * 8);
+    *reinterpret_cast<uint4*>(g + part * DK * DV + (rb * (DV / 8) + (col0 >> 3) + kb) * 64 + q * 8) = v;
+  }
+}
+
+struct FChainStage {
+  bf16 M[2 * DK * DK];   // M (split)
+  bf16 QW[2 * C * DK];   // QW (split)
+  float KU[DK * NSC];    // columns col0.. of KU
+  float PU[C * NSC];     // columns col0.. of PU
 };
-struct StateSm {
-  StateStage st[NSTG];
-  float S[DK * SB2];
+struct FChainSm {
+  FChainStage st[NSTG];
+  bf16 S[2 * DK * NSC];  // the carried state (split)
 };
 
-__global__ void __launch_bounds__(128) fwd_state_kernel(Dims d, FwdIO io, Ws w) {
+__global__ void __launch_bounds__(CTH) fwd_state_kernel(Dims d, FwdIO io, Ws w) {
   extern __shared__ __align__(16) unsigned char smraw[];
-  StateSm& sm = *reinterpret_cast<StateSm*>(smraw);
-  const int doc = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * NS2, tid = threadIdx.x, warp = tid >> 5;
+  FChainSm& sm = *reinterpret_cast<FChainSm*>(smraw);
+  const int doc = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * NSC, tid = threadIdx.x, warp = tid >> 5;
+  const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
   if (*w.err != 0) return;
   const int H = d.H;
-  const int cb = w.doc_chunk0[doc], ce = w.doc_chunk0[doc + 1];
-  for (int idx = tid; idx < DK * NS2; idx += 128) {
-    const int i = idx / NS2, jc = idx % NS2;
-    sm.S[i * SB2 + jc] = io.h0 ? io.h0[(((int64_t)doc * H + h) * DK + i) * DV + col0 + jc] : 0.f;
+  const int cb = w.doc_chunk0[doc], n = w.doc_chunk0[doc + 1] - cb;
+  const int64_t dh = ((int64_t)doc * H + h) * DK * DV;
+  const Op S{sm.S, sm.S + DK * NSC, NSC};
+  for (int idx = tid; idx < DK * NSC / 2; idx += CTH) {
+    const int i = idx / (NSC / 2), jc = 2 * (idx % (NSC / 2));
+    float2 v = make_float2(0.f, 0.f);
+    if (io.h0) v = *reinterpret_cast<const float2*>(io.h0 + dh + i * DV + col0 + jc);
+    op_store2(S, i, jc, v.x, v.y);
   }
-  auto prefetch = [&](int ci) {  // always commits a group (empty past the end)
-    if (ci < ce) {
-      StateStage& s = sm.st[(ci - cb) % NSTG];
-      const int64_t ch = (int64_t)ci * H + h;
-      for (int idx = tid; idx < DK * 8; idx += 128) {
-        const int i = idx >> 3, p = idx & 7;
-        cp16(&s.M[i * SQ + 4 * p], w.M + ch * DK * DK + i * DK + 4 * p);
+  auto prefetch = [&](int step) {  // always commits a group (empty past the end)
+    if (step < n) {
+      FChainStage& s = sm.st[step % NSTG];
+      const int64_t ch = (int64_t)(cb + step) * H + h;
+      for (int o = tid * 16; o < 4 * DK * DK; o += CTH * 16) cp16((char*)s.M + o, (const char*)(w.sM + ch * 2 * DK * DK) + o);
+      for (int o = tid * 16; o < 4 * C * DK; o += CTH * 16) cp16((char*)s.QW + o, (const char*)(w.sQW + ch * 2 * C * DK) + o);
+      for (int idx = tid; idx < DK * NSC / 4; idx += CTH) {
+        const int i = idx / (NSC / 4), p = idx % (NSC / 4);
+        cp16(&s.KU[i * NSC + 4 * p], w.KU + ch * DK * DV + i * DV + col0 + 4 * p);
       }
-      for (int idx = tid; idx < C * 8; idx += 128) {
-        const int rr = idx >> 3, p = idx & 7;
-        cp16(&s.QW[rr * SQ + 4 * p], w.QW + ch * C * DK + rr * DK + 4 * p);
-        cp16(&s.PU[rr * SB2 + 4 * p], w.PU + ch * C * DV + rr * DV + col0 + 4 * p);
-      }
-      for (int idx = tid; idx < DK * 8; idx += 128) {
-        const int i = idx >> 3, p = idx & 7;
-        cp16(&s.KU[i * SB2 + 4 * p], w.KU + ch * DK * DV + i * DV + col0 + 4 * p);
+      for (int idx = tid; idx < C * NSC / 4; idx += CTH) {
+        const int r = idx / (NSC / 4), p = idx % (NSC / 4);
+        cp16(&s.PU[r * NSC + 4 * p], w.PU + ch * C * DV + r * DV + col0 + 4 * p);
       }
     }
     cp_commit();
   };
-  prefetch(cb);
-  prefetch(cb + 1);
+  for (int s = 0; s < NSTG - 1; s++) prefetch(s);
+  float snew[2][4];  // this warp's tile of the updated state: rows 16 (warp & 1) .., columns 16 (warp >> 1) ..
+  zero(snew);
   const int mI = warp & 1, jn = warp >> 1;
   bf16* o = (bf16*)io.o;
-  for (int ci = cb; ci < ce; ci++) {
-    const StateStage& s = sm.st[(ci - cb) % NSTG];
-    const int L = w.chunk_len[ci], t0 = w.chunk_tok0[ci];
-    asm volatile("cp.async.wait_group 1;\n" ::);
-    __syncthreads();  // this chunk's stage and the last state update are visible
-    prefetch(ci + 2);
-    if (io.save) {  // the entry state as a split operand tile for the backward
-      const int64_t ch = (int64_t)ci * H + h;
-      const Op g{w.sS + ch * 2 * DK * DV, w.sS + ch * 2 * DK * DV + DK * DV, DV};
-      for (int idx = tid; idx < DK * NS2 / 2; idx += 128) {
-        const int i = idx / (NS2 / 2), jc = 2 * (idx % (NS2 / 2));
-        op_store2(g, i, col0 + jc, sm.S[i * SB2 + jc], sm.S[i * SB2 + jc + 1]);
-      }
-    }
-    float so[2][4], oo[4][4];
-    zero(so);
+  for (int step = 0; step < n; step++) {
+    const FChainStage& s = sm.st[step % NSTG];
+    const int ci = cb + step, L = w.chunk_len[ci], t0 = w.chunk_tok0[ci];
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(NSTG - 2));
+    __syncthreads();  // this step's stage and the last state update are visible
+    prefetch(step + NSTG - 1);
+    const Op Mo{const_cast<bf16*>(s.M), const_cast<bf16*>(s.M) + DK * DK, DK};
+    const Op QWo{const_cast<bf16*>(s.QW), const_cast<bf16*>(s.QW) + C * DK, DK};
+    zero(snew);
+    gemm3<1, false, true>(snew, Mo, 16 * mI, 0, S, 16 * jn, 0, DK / 16);
+    float oo[4][4];
     zero(oo);
-    rows16<2, true>(so, DK / 8, [&](int m, int k) { return s.M[(16 * mI + m) * SQ + k]; },
-                    [&](int k, int jj, int n) { return sm.S[k * SB2 + 16 * jn + 8 * jj + n]; });
-    rows16<4, true>(oo, DK / 8, [&](int m, int k) { return s.QW[(16 * warp + m) * SQ + k]; },
-                    [&](int k, int jj, int n) { return sm.S[k * SB2 + 8 * jj + n]; });
-    {
-      const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+    gemm3<2, false, true>(oo, QWo, 16 * warp, 0, S, 0, 0, DK / 16);
+    slice_to_global(w.sS + ((int64_t)ci * H + h) * 2 * DK * DV, sm.S, col0);
 #pragma unroll
-      for (int jj = 0; jj < 4; jj++)
+    for (int jj = 0; jj < 2; jj++)
 #pragma unroll
-        for (int hh = 0; hh < 2; hh++) {
-          const int rr = 16 * warp + gq + 8 * hh, c = 8 * jj + 2 * tq;
-          if (rr < L) {
-            const float2 pu = *reinterpret_cast<const float2*>(&s.PU[rr * SB2 + c]);
-            *reinterpret_cast<__nv_bfloat162*>(o + ((size_t)(t0 + rr) * H + h) * DV + col0 + c) =
-                __floats2bfloat162_rn(oo[jj][2 * hh] + pu.x, oo[jj][2 * hh + 1] + pu.y);
-          }
-        }
-    }
-    __syncthreads();  // every read of S is done
-    {
-      const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+      for (int hh = 0; hh < 2; hh++) {
+        const int i = 16 * mI + gq + 8 * hh, c = 16 * jn + 8 * jj + 2 * tq;
+        snew[jj][2 * hh] += s.KU[i * NSC + c];
+        snew[jj][2 * hh + 1] += s.KU[i * NSC + c + 1];
+      }
+#pragma unroll
+    for (int jj = 0; jj < 4; jj++)
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++) {
+        const int r = 16 * warp + gq + 8 * hh, c = 8 * jj + 2 * tq;
+        if (r < L)
+          *reinterpret_cast<__nv_bfloat162*>(o + ((size_t)(t0 + r) * H + h) * DV + col0 + c) =
+              __floats2bfloat162_rn(oo[jj][2 * hh] + s.PU[r * NSC + c], oo[jj][2 * hh + 1] + s.PU[r * NSC + c + 1]);
+      }
+    __syncthreads();  // every read of the state tile is done
+#pragma unroll
+    for (int jj = 0; jj < 2; jj++)
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++)
+        op_store2(S, 16 * mI + gq + 8 * hh, 16 * jn + 8 * jj + 2 * tq, snew[jj][2 * hh], snew[jj][2 * hh + 1]);
+  }
+  cp_wait_all();
+  if (io.h_final) {
+    if (n > 0) {
 #pragma unroll
       for (int jj = 0; jj < 2; jj++)
 #pragma unroll
         for (int hh = 0; hh < 2; hh++) {
           const int i = 16 * mI + gq + 8 * hh, c = 16 * jn + 8 * jj + 2 * tq;
-          const float2 ku = *reinterpret_cast<const float2*>(&s.KU[i * SB2 + c]);
-          sm.S[i * SB2 + c] = so[jj][2 * hh] + ku.x;
-          sm.S[i * SB2 + c + 1] = so[jj][2 * hh + 1] + ku.y;
+          *reinterpret_cast<float2*>(io.h_final + dh + i * DV + col0 + c) = make_float2(snew[jj][2 * hh], snew[jj][2 * hh + 1]);
         }
+    } else {
+      for (int idx = tid; idx < DK * NSC; idx += CTH) {
+        const int i = idx / NSC, jc = idx % NSC;
+        io.h_final[dh + i * DV + col0 + jc] = io.h0 ? io.h0[dh + i * DV + col0 + jc] : 0.f;
+      }
     }
   }
-  asm volatile("cp.async.wait_group 0;\n" ::);
-  __syncthreads();
-  if (io.h_final)
-    for (int idx = tid; idx < DK * NS2; idx += 128) {
-      const int i = idx / NS2, jc = idx % NS2;
-      io.h_final[(((int64_t)doc * H + h) * DK + i) * DV + col0 + jc] = sm.S[i * SB2 + jc];
-    }
 }
 
-// ------------------------------------------------------------ backward scan
-constexpr int NS = 16;        // value columns per scan CTA
-constexpr int SS = NS + 8;    // row stride of [*][NS] operands
+struct BChainStage {
+  bf16 M[2 * DK * DK];  // M (split)
+  bf16 QW[2 * C * DK];  // QW (split)
+  bf16 dO[C * NSC];     // columns col0.. of dO (exact bf16, operand layout)
+};
+struct BChainSm {
+  BChainStage st[NSTG];
+  bf16 dS[2 * DK * NSC];  // the carried state gradient (split)
+};
 
-// One CTA per (document, head, 16 value columns), walking the chunks in
-// reverse: dS_in = M^T dS_out + QW^T dO.  The next chunk's M, QW and dO slice
-// are prefetched (cp.async, double buffer) while the current one computes;
-// QW^T dO is independent of the carried dS, so only M^T dS is on the chain.
-__global__ void __launch_bounds__(128) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
-  __shared__ __align__(16) float Ms[2][DK * SQ];
-  __shared__ __align__(16) float QWs[2][C * SQ];
-  __shared__ __align__(16) bf16 dOs[2][C * NS];
-  __shared__ float dS[DK * SS];
-  const int doc = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * NS, tid = threadIdx.x, warp = tid >> 5;
+__global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  BChainSm& sm = *reinterpret_cast<BChainSm*>(smraw);
+  const int doc = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * NSC, tid = threadIdx.x, warp = tid >> 5;
+  const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
   if (!saved_ok(d, w.tag, w.err)) return;
   const int H = d.H;
-  const bf16* dO = (const bf16*)io.dO;
-  for (int idx = tid; idx < DK * NS; idx += 128) {
-    int i = idx / NS, j = idx % NS;
-    dS[i * SS + j] = io.dh_final ? io.dh_final[(((int64_t)doc * H + h) * DK + i) * DV + col0 + j] : 0.f;
+  const int cb = w.doc_chunk0[doc], ce = w.doc_chunk0[doc + 1], n = ce - cb;
+  const int64_t dh = ((int64_t)doc * H + h) * DK * DV;
+  const Op dS{sm.dS, sm.dS + DK * NSC, NSC};
+  for (int idx = tid; idx < DK * NSC / 2; idx += CTH) {
+    const int i = idx / (NSC / 2), jc = 2 * (idx % (NSC / 2));
+    float2 v = make_float2(0.f, 0.f);
+    if (io.dh_final) v = *reinterpret_cast<const float2*>(io.dh_final + dh + i * DV + col0 + jc);
+    op_store2(dS, i, jc, v.x, v.y);
   }
-  const int cb = w.doc_chunk0[doc], ce = w.doc_chunk0[doc + 1];
-  auto prefetch = [&](int ci, int buf) {
-    const int64_t ch = (int64_t)ci * H + h;
-    const int L = w.chunk_len[ci], t0 = w.chunk_tok0[ci];
-    for (int idx = tid; idx < DK * 8; idx += 128) {  // 8 x 16 B per row of 32 floats
-      int i = idx >> 3, p = idx & 7;
-      cp16(&Ms[buf][i * SQ + p * 4], w.M + ch * DK * DK + i * DK + p * 4);
-    }
-    for (int idx = tid; idx < C * 8; idx += 128) {
-      int r = idx >> 3, p = idx & 7;
-      cp16(&QWs[buf][r * SQ + p * 4], w.QW + ch * C * DK + r * DK + p * 4);
-    }
-    for (int idx = tid; idx < C * 2; idx += 128) {  // 2 x 16 B per 16-column bf16 row slice
-      int r = idx >> 1, p = idx & 1;
-      if (r < L) cp16(&dOs[buf][r * NS + p * 8], dO + ((size_t)(t0 + r) * H + h) * DV + col0 + p * 8);
-      else *reinterpret_cast<uint4*>(&dOs[buf][r * NS + p * 8]) = make_uint4(0u, 0u, 0u, 0u);
+  const bf16* dOg = (const bf16*)io.dO;
+  auto prefetch = [&](int step) {  // always commits a group (empty past the end)
+    if (step < n) {
+      BChainStage& s = sm.st[step % NSTG];
+      const int ci = ce - 1 - step, L = w.chunk_len[ci], t0 = w.chunk_tok0[ci];
+      const int64_t ch = (int64_t)ci * H + h;
+      for (int o = tid * 16; o < 4 * DK * DK; o += CTH * 16) cp16((char*)s.M + o, (const char*)(w.sM + ch * 2 * DK * DK) + o);
+      for (int o = tid * 16; o < 4 * C * DK; o += CTH * 16) cp16((char*)s.QW + o, (const char*)(w.sQW + ch * 2 * C * DK) + o);
+      for (int idx = tid; idx < C * NSC / 8; idx += CTH) {
+        const int r = idx / (NSC / 8), p = idx % (NSC / 8);
+        bf16* dst = s.dO + opix(r, 8 * p, NSC);
+        if (r < L) cp16(dst, dOg + ((size_t)(t0 + r) * H + h) * DV + col0 + 8 * p);
+        else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+      }
     }
     cp_commit();
   };
-  if (cb < ce) prefetch(ce - 1, 0);
+  for (int s = 0; s < NSTG - 1; s++) prefetch(s);
+  float acc[2][4];  // this warp's tile of the carried gradient: rows 16 (warp & 1) .., columns 16 (warp >> 1) ..
+  zero(acc);
   const int mI = warp & 1, jn = warp >> 1;
-  for (int ci = ce - 1, buf = 0; ci >= cb; ci--, buf ^= 1) {
-    const int64_t ch = (int64_t)ci * H + h;
-    cp_wait_all();
-    __syncthreads();  // buffer `buf` and the last dS update are visible
-    if (ci - 1 >= cb) prefetch(ci - 1, buf ^ 1);
-    {  // dS' of this chunk as a split operand tile for the chunk gradients
-      const Op g{w.sdS + ch * 2 * DK * DV, w.sdS + ch * 2 * DK * DV + DK * DV, DV};
-      for (int idx = tid; idx < DK * NS / 2; idx += 128) {
-        const int i = idx / (NS / 2), jc = 2 * (idx % (NS / 2));
-        op_store2(g, i, col0 + jc, dS[i * SS + jc], dS[i * SS + jc + 1]);
+  for (int step = 0; step < n; step++) {
+    const BChainStage& s = sm.st[step % NSTG];
+    const int ci = ce - 1 - step;
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(NSTG - 2));
+    __syncthreads();  // this step's stage and the last state update are visible
+    prefetch(step + NSTG - 1);
+    const Op Mo{const_cast<bf16*>(s.M), const_cast<bf16*>(s.M) + DK * DK, DK};
+    const Op QWo{const_cast<bf16*>(s.QW), const_cast<bf16*>(s.QW) + C * DK, DK};
+    const Op dOo{const_cast<bf16*>(s.dO), nullptr, NSC};
+    float ax[2][4];
+    zero(acc);
+    zero(ax);
+    gemm3<1, true, true>(ax, QWo, 16 * mI, 0, dOo, 16 * jn, 0, C / 16);
+    gemm3<1, true, true>(acc, Mo, 16 * mI, 0, dS, 16 * jn, 0, DK / 16);
+    slice_to_global(w.sdS + ((int64_t)ci * H + h) * 2 * DK * DV, sm.dS, col0);
+#pragma unroll
+    for (int jj = 0; jj < 2; jj++)
+#pragma unroll
+      for (int e = 0; e < 4; e++) acc[jj][e] += ax[jj][e];
+    __syncthreads();  // every read of the state tile is done
+#pragma unroll
+    for (int jj = 0; jj < 2; jj++)
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++)
+        op_store2(dS, 16 * mI + gq + 8 * hh, 16 * jn + 8 * jj + 2 * tq, acc[jj][2 * hh], acc[jj][2 * hh + 1]);
+  }
+  cp_wait_all();
+  if (io.dh0) {
+    if (n > 0) {
+#pragma unroll
+      for (int jj = 0; jj < 2; jj++)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+          const int i = 16 * mI + gq + 8 * hh, c = 16 * jn + 8 * jj + 2 * tq;
+          *reinterpret_cast<float2*>(io.dh0 + dh + i * DV + col0 + c) = make_float2(acc[jj][2 * hh], acc[jj][2 * hh + 1]);
+        }
+    } else {
+      for (int idx = tid; idx < DK * NSC; idx += CTH) {
+        const int i = idx / NSC, jc = idx % NSC;
+        io.dh0[dh + i * DV + col0 + jc] = io.dh_final ? io.dh_final[dh + i * DV + col0 + jc] : 0.f;
       }
     }
-    float acc[1][4];
-    zero(acc);
-    rows16<1, true, false, true>(acc, C / 8, [&](int m, int k) { return QWs[buf][k * SQ + 16 * mI + m]; },
-                                 [&](int k, int j, int n) { return bfl(dOs[buf][k * NS + 8 * jn + n]); });
-    rows16<1, true>(acc, DK / 8, [&](int m, int k) { return Ms[buf][k * SQ + 16 * mI + m]; },
-                    [&](int k, int j, int n) { return dS[k * SS + 8 * jn + n]; });
-    __syncthreads();  // every read of dS is done
-    each(acc, [&](int m, int col, float& v) { dS[(16 * mI + m) * SS + 8 * jn + col] = v; });
   }
-  __syncthreads();
-  if (io.dh0)
-    for (int idx = tid; idx < DK * NS; idx += 128) {
-      int i = idx / NS, j = idx % NS;
-      io.dh0[(((int64_t)doc * H + h) * DK + i) * DV + col0 + j] = dS[i * SS + j];
-    }
 }
 
 // ------------------------------------------------------------ backward chunk kernels
@@ -981,11 +1042,6 @@ __device__ __forceinline__ void blk_ij(int b, int& I, int& J) {
   J = b - I * (I + 1) / 2;
 }
 __device__ __forceinline__ int blk_of(int I, int J) { return I * (I + 1) / 2 + J; }
-
-// cp.async of `bytes` (a multiple of 16) from global to shared, all threads.
-__device__ __forceinline__ void cp_bytes(void* dst, const void* src, int bytes) {
-  for (int o = threadIdx.x * 16; o < bytes; o += NTH * 16) cp16((char*)dst + o, (const char*)src + o);
-}
 
 // The 8 accumulator values a thread holds of a 16 x 16 tile, in fragment
 // order (thread-major, 32 bytes per thread): bwd_grad and bwd_gate use the
@@ -1607,7 +1663,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_gate_kernel(Dims d, BwdIO io, Ws w
 
 static_assert(sizeof(fast::FwdSm) <= 232448, "fused forward shared memory exceeds 227 KB");
 static_assert(sizeof(fast::ChunkSm) <= 113 * 1024, "per-chunk forward must fit two CTAs per SM");
-static_assert(sizeof(fast::StateSm) <= 113 * 1024, "state chain must fit two CTAs per SM");
+
 static_assert(sizeof(fast::GradSm) <= 112 * 1024, "chunk-gradient kernel must fit two CTAs per SM");
 static_assert(sizeof(fast::GateSm) <= 112 * 1024, "gate kernel must fit two CTAs per SM");
 
@@ -1624,7 +1680,7 @@ cudaError_t launch_fast_fwd(const Dims& d, const FwdIO& io, const Ws& w, cudaStr
     prof_end(K_FWD_CHAIN, st);
     return cudaGetLastError();
   }
-  const size_t s1 = sizeof(fast::ChunkSm), s2 = sizeof(fast::StateSm);
+  const size_t s1 = sizeof(fast::ChunkSm), s2 = sizeof(fast::FChainSm);
   e = cudaFuncSetAttribute(fast::fwd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(fast::fwd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
@@ -1635,21 +1691,23 @@ cudaError_t launch_fast_fwd(const Dims& d, const FwdIO& io, const Ws& w, cudaStr
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_begin(K_FWD_STATE, st);
-  fast::fwd_state_kernel<<<dim3(d.n_docs, d.H, fast::DV / fast::NS2), 128, s2, st>>>(d, io, w);
+  fast::fwd_state_kernel<<<dim3(d.n_docs, d.H, fast::DV / fast::NSC), fast::CTH, s2, st>>>(d, io, w);
   prof_end(K_FWD_STATE, st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fast_bwd(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st) {
-  prof_begin(K_BWD_SCAN, st);
-  fast::bwd_scan_kernel<<<dim3(d.n_docs, d.H, fast::DV / fast::NS), 128, 0, st>>>(d, io, w);
-  prof_end(K_BWD_SCAN, st);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const size_t s1 = sizeof(fast::GradSm), s2 = sizeof(fast::GateSm);
-  e = cudaFuncSetAttribute(fast::bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
+  const size_t sc = sizeof(fast::BChainSm), s1 = sizeof(fast::GradSm), s2 = sizeof(fast::GateSm);
+  cudaError_t e = cudaFuncSetAttribute(fast::bwd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fast::bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(fast::bwd_gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
+  if (e != cudaSuccess) return e;
+  prof_begin(K_BWD_SCAN, st);
+  fast::bwd_scan_kernel<<<dim3(d.n_docs, d.H, fast::DV / fast::NSC), fast::CTH, sc, st>>>(d, io, w);
+  prof_end(K_BWD_SCAN, st);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_begin(K_BWD_GRAD, st);
   fast::bwd_grad_kernel<<<dim3(d.nc_max, d.H), fast::NTH, s1, st>>>(d, io, w);

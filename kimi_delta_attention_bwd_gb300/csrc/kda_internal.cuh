@@ -45,14 +45,15 @@ struct Ws {
   float* KD;   // [ch][C][dk]  K^ * exp(G_last - G)
   float* gam;  // [ch][dk]     exp(G_last)
   float* Sent; // [ch][dk][dv] state entering the chunk (saved for backward)
-  float* M;    // [ch][dk][dk] Diag(gamma) - KD^T W (tensor-core path; the backward scan reads it)
-  float* QW;   // [ch][C][dk]  QG - P W            (tensor-core path; the backward scan reads it)
   float* KU;   // [ch][dk][dv] KD^T U              (tensor-core forward scratch)
   float* PU;   // [ch][C][dv]  P U                 (tensor-core forward scratch)
-  // tensor-core path, split-bf16 operand tiles (hi tile, then lo tile) saved
-  // by the forward: S entering the chunk, T, P = scale P', W, U; and the
-  // state gradient leaving the chunk from the backward scan
+  // tensor-core path, split-bf16 operand tiles (hi tile, then lo tile): S
+  // entering the chunk (forward chain); T, P = scale P', W, U saved by the
+  // forward; the state gradient leaving the chunk (backward chain)
   __nv_bfloat16 *sS, *sT, *sP, *sW, *sU, *sdS;
+  // M = Diag(gamma) - KD^T W [ch][dk][dk] and QW = QG - P W [ch][C][dk] (split
+  // tiles from the per-chunk forward; both chains read them)
+  __nv_bfloat16 *sM, *sQW;
   float* sA;   // [ch][10][16][16] A' (unscaled) lower 16 x 16 blocks
   // tensor-core backward, bwd_grad -> bwd_gate
   float *gDP, *gMA;        // [ch][10][16][16] dP', beta dA lower blocks
