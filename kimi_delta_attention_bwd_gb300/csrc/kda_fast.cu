@@ -42,6 +42,10 @@ constexpr int SV = DV + 8;  // row stride of [C][DV] operands
 constexpr int SC = C + 4;   // row stride of [C][C] matrices
 constexpr int NTH = 256, NW = 8;
 constexpr float SPAN_MAX = 80.f;
+// The per-chunk kernels keep G in log2 units (G2 = G log2(e)) so that every
+// decay factor exp(G_a - G_b) is one exp2f of a difference.
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float SPAN2 = SPAN_MAX * LOG2E;
 // Every tensor-core product runs with split operands (see the header).
 constexpr bool SF = true;  // forward chain products
 
@@ -219,6 +223,14 @@ __device__ __forceinline__ float pair_exact(const bf16* X, float ix, const bf16*
                                             const float* Gs) {
   float acc = 0.f;
   for (int i = 0; i < DK; i++) acc += (bfl(X[i]) * ix) * (bfl(Kr[i]) * ik) * expf(Gr[i] - Gs[i]);
+  return acc;
+}
+
+// pair_exact with G in log2 units.
+__device__ __forceinline__ float pair_exact2(const bf16* X, float ix, const bf16* Kr, float ik, const float* Gr,
+                                             const float* Gs) {
+  float acc = 0.f;
+  for (int i = 0; i < DK; i++) acc += (bfl(X[i]) * ix) * (bfl(Kr[i]) * ik) * exp2f(Gr[i] - Gs[i]);
   return acc;
 }
 
@@ -503,7 +515,7 @@ __device__ __forceinline__ int roff(int I) { return 8 * I * (I + 1); }
 // Shared memory of fwd_chunk (about 104 KB: two CTAs per SM).  bf16 arrays
 // are split operand tiles; regions are reused as noted.
 struct ChunkSm {
-  float gg[C * SQ];    // G (fp32); QG (split) once the A / P blocks are done
+  float gg[C * SQ];    // G2 = G log2(e) (fp32); QG (split) once the A / P blocks are done
   bf16 x[18432];       // LQ | LK | R  ->  T (fp32) + Y scratch  ->  W | U;  KD in the last 8 KB
   float am[C * SC];    // beta_r A (fp32), then T (split)
   bf16 op[2 * C * C];  // P (scaled, split)
@@ -594,7 +606,7 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     unpack8(__ldg(vp + 1), vv + 8);
     braw = bfl(((const bf16*)io.b)[row]);
 #pragma unroll
-    for (int e = 0; e < 8; e++) gv[e] = -a * softplus_f(gv[e] + dtb[8 * q4 + e]);
+    for (int e = 0; e < 8; e++) gv[e] = -a * LOG2E * softplus_f(gv[e] + dtb[8 * q4 + e]);
   } else {
 #pragma unroll
     for (int e = 0; e < 8; e++) qv[e] = kv[e] = gv[e] = 0.f;
@@ -646,34 +658,35 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
   //      registers until their storage frees up
   float qg[8], kd[8];
   {
-    float gbv[8];
+    float gbv[8], xk[8];
     bool wide = false;
 #pragma unroll
     for (int e = 0; e < 8; e++) {
       gbv[e] = sm.gg[(16 * I) * SQ + 8 * q4 + e];
       const float gl = sm.gg[(L - 1) * SQ + 8 * q4 + e];
-      const float eG = expf(gv[e]);
+      const float eG = exp2f(gv[e]);
       qg[e] = scale * qv[e] * eG;
-      kd[e] = kv[e] * expf(gl - gv[e]);
-      if (r == 0) sm.gam[8 * q4 + e] = expf(gl);
-      wide |= (r & 15) == 15 && gbv[e] - gv[e] > SPAN_MAX;
+      kd[e] = kv[e] * exp2f(gl - gv[e]);
+      xk[e] = beta * kv[e] * eG;
+      if (r == 0) sm.gam[8 * q4 + e] = exp2f(gl);
+      wide |= (r & 15) == 15 && gbv[e] - gv[e] > SPAN2;
     }
     if (wide) sm.spanok[I] = 0;
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
       const int i = 8 * q4 + e;
-      const float l0 = expf(gv[e] - gbv[e]), l1 = expf(gv[e + 1] - gbv[e + 1]);
+      const float l0 = exp2f(gv[e] - gbv[e]), l1 = exp2f(gv[e + 1] - gbv[e + 1]);
       op_store2(LQ, r, i, qv[e] * l0, qv[e + 1] * l1);
       op_store2(LK, r, i, kv[e] * l0, kv[e + 1] * l1);
-      op_store2(XK, r, i, beta * kv[e] * expf(gv[e]), beta * kv[e + 1] * expf(gv[e + 1]));
+      op_store2(XK, r, i, xk[e], xk[e + 1]);
     }
     for (int I2 = I; I2 < 4; I2++)
 #pragma unroll
       for (int e = 0; e < 8; e += 2) {
         const int i = 8 * q4 + e;
         const float b0 = sm.gg[(16 * I2) * SQ + i], b1 = sm.gg[(16 * I2) * SQ + i + 1];
-        op_store2(R, roff(I2) + r, i, kv[e] * expf(fminf(b0 - gv[e], SPAN_MAX)),
-                  kv[e + 1] * expf(fminf(b1 - gv[e + 1], SPAN_MAX)));
+        op_store2(R, roff(I2) + r, i, kv[e] * exp2f(fminf(b0 - gv[e], SPAN2)),
+                  kv[e + 1] * exp2f(fminf(b1 - gv[e + 1], SPAN2)));
       }
 #pragma unroll
     for (int e = 0; e < 16; e += 2) op_store2(XV, r, 16 * q4 + e, beta * vv[e], beta * vv[e + 1]);
@@ -695,7 +708,7 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
         if (s <= rr && rr < L) {
           const bf16* xr = (isP ? qraw : kraw) + ((size_t)(t0 + rr) * H + h) * DK;
           const bf16* ks = kraw + ((size_t)(t0 + s) * H + h) * DK;
-          v = pair_exact(xr, isP ? sm.inq[rr] : sm.ink[rr], ks, sm.ink[s], sm.gg + rr * SQ, sm.gg + s * SQ);
+          v = pair_exact2(xr, isP ? sm.inq[rr] : sm.ink[rr], ks, sm.ink[s], sm.gg + rr * SQ, sm.gg + s * SQ);
         }
       });
     }
@@ -1069,7 +1082,7 @@ __device__ __forceinline__ void frag_load(const float* g, float (&v)[2][4]) {
 // writes dv and db, and hands dP', MA, dQG, dKD, beta YW and dgamma to bwd_gate.
 struct GradSm {
   bf16 wk[45056];  // work area (88 KB), regions bound in the kernel
-  float gg[C * SQ];
+  float gg[C * SQ];  // G2 = G log2(e)
   bf16 rk[C * DK];
   float bet[C], braw[C], dbet[C], part[4 * C];
   float tot[NW * DK];
@@ -1144,7 +1157,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
     unpack8(*reinterpret_cast<const uint4*>(sm.rk + r * DK + 8 * q4), kv);
     unpack8(*reinterpret_cast<const uint4*>(fst + r * DK + 8 * q4), gv);
 #pragma unroll
-    for (int e = 0; e < 8; e++) gv[e] = -a * softplus_f(gv[e] + dtb[8 * q4 + e]);
+    for (int e = 0; e < 8; e++) gv[e] = -a * LOG2E * softplus_f(gv[e] + dtb[8 * q4 + e]);
   } else {
 #pragma unroll
     for (int e = 0; e < 8; e++) kv[e] = gv[e] = 0.f;
@@ -1190,9 +1203,9 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   for (int e = 0; e < 8; e += 2) {
     const int i = 8 * q4 + e;
     const float gl0 = sm.gg[(L - 1) * SQ + i], gl1 = sm.gg[(L - 1) * SQ + i + 1];
-    op_store2(KD, r, i, kv[e] * expf(gl0 - gv[e]), kv[e + 1] * expf(gl1 - gv[e + 1]));
-    xkg[e] = kv[e] * expf(gv[e]);
-    xkg[e + 1] = kv[e + 1] * expf(gv[e + 1]);
+    op_store2(KD, r, i, kv[e] * exp2f(gl0 - gv[e]), kv[e + 1] * exp2f(gl1 - gv[e + 1]));
+    xkg[e] = kv[e] * exp2f(gv[e]);
+    xkg[e + 1] = kv[e + 1] * exp2f(gv[e + 1]);
   }
   cp_wait_all();
   __syncthreads();
@@ -1365,7 +1378,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
 // the gate backward (df and the per-chunk partials of dA_log and dt_bias)
 // and the L2-norm backward (dq, dk).
 struct GateSm {
-  float gg[C * SQ];           // G; then dq^
+  float gg[C * SQ];           // G2 = G log2(e); then dq^
   float dp[NBLK * 16 * PB];   // dP' lower blocks; then dk^
   float ma[NBLK * 16 * PB];   // MA lower blocks; then dG - kdt and its suffix sums
   bf16 rq[C * DK], rk[C * DK], rf[C * DK];
@@ -1427,7 +1440,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_gate_kernel(Dims d, BwdIO io, Ws w
     float sq = 0.f, sk = 0.f;
 #pragma unroll
     for (int e = 0; e < 8; e++) {
-      gv[e] = in ? -a * softplus_f(gv[e] + dtb[8 * q4 + e]) : 0.f;
+      gv[e] = in ? -a * LOG2E * softplus_f(gv[e] + dtb[8 * q4 + e]) : 0.f;
       sq += qv[e] * qv[e];
       sk += kv[e] * kv[e];
     }
@@ -1466,8 +1479,8 @@ __global__ void __launch_bounds__(NTH, 2) bwd_gate_kernel(Dims d, BwdIO io, Ws w
 #pragma unroll
     for (int e = 0; e < 8; e++) {
       const int i = 8 * q4 + e;
-      wide |= (r & 15) == 15 && sm.gg[(16 * I0) * SQ + i] - gv[e] > SPAN_MAX;
-      if (r == 0) sm.gam[i] = expf(sm.gg[(L - 1) * SQ + i]);
+      wide |= (r & 15) == 15 && sm.gg[(16 * I0) * SQ + i] - gv[e] > SPAN2;
+      if (r == 0) sm.gam[i] = exp2f(sm.gg[(L - 1) * SQ + i]);
     }
     if (wide) sm.spanok[I0] = 0;
   }
@@ -1495,7 +1508,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_gate_kernel(Dims d, BwdIO io, Ws w
                  [&](int m, int k) { return MAb[m * PB + k]; },
                  [&](int k, int jj, int n) {
                    const int s = 16 * J + k, i = 16 * hk + 8 * jj + n;
-                   return bfl(sm.rk[s * DK + i]) * sm.ink[s] * expf(fminf(gbI[i] - sm.gg[s * SQ + i], SPAN_MAX));
+                   return bfl(sm.rk[s * DK + i]) * sm.ink[s] * exp2f(fminf(gbI[i] - sm.gg[s * SQ + i], SPAN2));
                  });
   }
   for (int I2 = I; I2 < 4; I2++) {
@@ -1506,7 +1519,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_gate_kernel(Dims d, BwdIO io, Ws w
                  [&](int m, int k) { return MAb[k * PB + m]; },
                  [&](int k, int jj, int n) {
                    const int rr = 16 * I2 + k, i = 16 * hk + 8 * jj + n;
-                   const float x = expf(fminf(sm.gg[rr * SQ + i] - geI[i], SPAN_MAX));
+                   const float x = exp2f(fminf(sm.gg[rr * SQ + i] - geI[i], SPAN2));
                    return make_float2(bfl(sm.rq[rr * DK + i]) * sm.inq[rr] * x, bfl(sm.rk[rr * DK + i]) * sm.ink[rr] * x);
                  });
   }
@@ -1522,25 +1535,25 @@ __global__ void __launch_bounds__(NTH, 2) bwd_gate_kernel(Dims d, BwdIO io, Ws w
       for (int e = 0; e < 4; e++) {
         const int m = gq + 8 * (e >> 1), rr = 16 * I + m, i = 16 * hk + 8 * jj + 2 * tq + (e & 1);
         const float G = sm.gg[rr * SQ + i];
-        const float eL = expf(G - gbI[i]), eR = expf(geI[i] - G);
+        const float eL = exp2f(G - gbI[i]), eR = exp2f(geI[i] - G);
         float pr = prow[jj][e] * eL, ar = arow[jj][e] * eL, cl = col[jj][e] * eR;
         if (!ok) {  // exact diagonal-block terms (rows past the chunk end are zero)
           for (int s = 16 * I; s < 16 * I + 16 && s < L; s++) {
             const int n = s - 16 * I;
             const float ks = bfl(sm.rk[s * DK + i]) * sm.ink[s], qs = bfl(sm.rq[s * DK + i]) * sm.inq[s];
             if (s <= rr) {
-              const float ex = expf(G - sm.gg[s * SQ + i]);
+              const float ex = exp2f(G - sm.gg[s * SQ + i]);
               pr += DPd[m * PB + n] * ks * ex;
               ar += MAd[m * PB + n] * ks * ex;
             }
             if (s >= rr) {
-              const float ex = expf(sm.gg[s * SQ + i] - G);
+              const float ex = exp2f(sm.gg[s * SQ + i] - G);
               cl += (DPd[n * PB + m] * qs + MAd[n * PB + m] * ks) * ex;
             }
           }
         }
         const float q = bfl(sm.rq[rr * DK + i]) * sm.inq[rr], k = bfl(sm.rk[rr * DK + i]) * sm.ink[rr];
-        const float Gm = expf(G), kdf = expf(sm.gg[(L - 1) * SQ + i] - G);
+        const float Gm = exp2f(G), kdf = exp2f(sm.gg[(L - 1) * SQ + i] - G);
         const float kdt = dKD[jj][e] * k * kdf;
         dqh[jj][e] = pr + dQG[jj][e] * Gm;
         dkh[jj][e] = ar + cl + dkg[jj][e] * Gm + dKD[jj][e] * kdf;
