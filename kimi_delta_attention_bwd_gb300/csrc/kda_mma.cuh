@@ -229,23 +229,32 @@ template <int NP, bool AT, bool BT>
 __device__ __forceinline__ void gemm3(float (&acc)[2 * NP][4], const Op& A, int m0, int ka0, const Op& B, int n0,
                                       int kb0, int ksteps) {
   for (int ks = 0; ks < ksteps; ks++) {
-    uint32_t ah[4], al[4];
+    uint32_t ah[4], al[4], bh[NP][4], bl[NP][4];
     frag_a<AT>(ah, A.hi, A.K, m0, ka0 + 16 * ks);
     if (A.lo) frag_a<AT>(al, A.lo, A.K, m0, ka0 + 16 * ks);
 #pragma unroll
     for (int p = 0; p < NP; p++) {
-      uint32_t bh[4], bl[4];
-      frag_b<BT>(bh, B.hi, B.K, kb0 + 16 * ks, n0 + 16 * p);
-      mma_bf16(acc[2 * p], ah, bh[0], bh[1]);
-      mma_bf16(acc[2 * p + 1], ah, bh[2], bh[3]);
-      if (B.lo) {
-        frag_b<BT>(bl, B.lo, B.K, kb0 + 16 * ks, n0 + 16 * p);
-        mma_bf16(acc[2 * p], ah, bl[0], bl[1]);
-        mma_bf16(acc[2 * p + 1], ah, bl[2], bl[3]);
+      frag_b<BT>(bh[p], B.hi, B.K, kb0 + 16 * ks, n0 + 16 * p);
+      if (B.lo) frag_b<BT>(bl[p], B.lo, B.K, kb0 + 16 * ks, n0 + 16 * p);
+    }
+    // consecutive products go to different accumulators
+#pragma unroll
+    for (int p = 0; p < NP; p++) {
+      mma_bf16(acc[2 * p], ah, bh[p][0], bh[p][1]);
+      mma_bf16(acc[2 * p + 1], ah, bh[p][2], bh[p][3]);
+    }
+    if (B.lo) {
+#pragma unroll
+      for (int p = 0; p < NP; p++) {
+        mma_bf16(acc[2 * p], ah, bl[p][0], bl[p][1]);
+        mma_bf16(acc[2 * p + 1], ah, bl[p][2], bl[p][3]);
       }
-      if (A.lo) {
-        mma_bf16(acc[2 * p], al, bh[0], bh[1]);
-        mma_bf16(acc[2 * p + 1], al, bh[2], bh[3]);
+    }
+    if (A.lo) {
+#pragma unroll
+      for (int p = 0; p < NP; p++) {
+        mma_bf16(acc[2 * p], al, bh[p][0], bh[p][1]);
+        mma_bf16(acc[2 * p + 1], al, bh[p][2], bh[p][3]);
       }
     }
   }
