@@ -526,17 +526,6 @@ struct ChunkSm {
   int spanok[4];
 };
 
-// cp.async of `bytes` (a multiple of 16) from global to shared, all threads.
-__device__ __forceinline__ void cp_bytes(void* dst, const void* src, int bytes) {
-  for (int o = threadIdx.x * 16; o < bytes; o += NTH * 16) cp16((char*)dst + o, (const char*)src + o);
-}
-
-// Copies `bytes` (a multiple of 16) from shared to global memory, all threads.
-__device__ __forceinline__ void copy16(void* g, const void* smem, int bytes) {
-  for (int o = threadIdx.x * 16; o < bytes; o += NTH * 16)
-    *reinterpret_cast<uint4*>((char*)g + o) = *reinterpret_cast<const uint4*>((const char*)smem + o);
-}
-
 // Stores a 16 x (8 NT) accumulator tile at (r0, c0) of a split operand tile
 // (global or shared), mapping each value through fn(r, c, v).
 template <int NT, class F>
@@ -730,8 +719,12 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
       });
     }
   }
+  if (io.save) fence_async_smem();
   __syncthreads();
-  if (io.save) copy16(w.sP + ch * 2 * C * C, P.hi, 4 * C * C);
+  if (io.save && tid == 0) {  // P for the backward (its tile is not written again)
+    bulk_s2g(w.sP + ch * 2 * C * C, P.hi, 4 * C * C);
+    bulk_commit();
+  }
   // QG over G, KD in the tail of the x region (both free now)
 #pragma unroll
   for (int e = 0; e < 8; e += 2) {
@@ -745,8 +738,12 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     const int rr = 16 * bI + (rem >> 3), s2 = 16 * bJ + 2 * (rem & 7);
     op_store2(T, rr, s2, tm[rr * SC + s2], tm[rr * SC + s2 + 1]);
   }
+  if (io.save) fence_async_smem();
   __syncthreads();
-  if (io.save) copy16(w.sT + ch * 2 * C * C, T.hi, 4 * C * C);
+  if (io.save && tid == 0) {  // T for the backward (its tile is not written again)
+    bulk_s2g(w.sT + ch * 2 * C * C, T.hi, 4 * C * C);
+    bulk_commit();
+  }
   {  // W | U = T [XK | XV]  (T lower block-triangular: k < 16 (I + 1))
     const int wI = warp & 3, half = warp >> 2;
     if (half == 0) {
@@ -778,15 +775,21 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
           op_store2(U, 16 * wI + gq + 8 * hh, 16 + 8 * jt + 2 * tq, au[jt][2 * hh], au[jt][2 * hh + 1]);
     }
   }
+  if (io.save) fence_async_smem();
   __syncthreads();
-  if (io.save) {
-    copy16(w.sW + ch * 2 * C * DK, W.hi, 4 * C * DK);
-    copy16(w.sU + ch * 2 * C * DV, U.hi, 4 * C * DV);
+  if (io.save && tid == 0) {  // W and U for the backward
+    bulk_s2g(w.sW + ch * 2 * C * DK, W.hi, 4 * C * DK);
+    bulk_s2g(w.sU + ch * 2 * C * DV, U.hi, 4 * C * DV);
+    bulk_commit();
   }
-  {  // outputs: PU and QW by row block, then the 16 x 16 tiles of M | KU (M, QW split)
+  // outputs: PU and QW by row block, then the 16 x 16 tiles of M | KU (M, QW
+  // split, straight to global; PU and KU staged over XK | XV, then bulk stores)
+  float* PUs = reinterpret_cast<float*>(sm.y);  // [C][DV]
+  float* KUs = PUs + C * DV;                    // [DK][DV]
+  {
     const int wI = warp & 3, half = warp >> 2;
-    float* PUg = w.PU + ch * C * DV;
-    float* KUg = w.KU + ch * DK * DV;
+    float* PUg = PUs;
+    float* KUg = KUs;
     const Op QWg{w.sQW + ch * 2 * C * DK, w.sQW + ch * 2 * C * DK + C * DK, DK};
     const Op Mg{w.sM + ch * 2 * DK * DK, w.sM + ch * 2 * DK * DK + DK * DK, DK};
     {
@@ -817,6 +820,14 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
         store_acc(acc, KUg, DV, 16 * mi, 16 * (cc - 2), [](int, int, float v) { return v; });
       }
     }
+  }
+  fence_async_smem();
+  __syncthreads();
+  if (tid == 0) {
+    bulk_s2g(w.PU + ch * C * DV, PUs, 4 * C * DV);
+    bulk_s2g(w.KU + ch * DK * DV, KUs, 4 * DK * DV);
+    bulk_commit();
+    bulk_wait_all();  // every bulk store of this CTA has completed
   }
 }
 
@@ -1082,6 +1093,7 @@ __device__ __forceinline__ void frag_load(const float* g, float (&v)[2][4]) {
 // writes dv and db, and hands dP', MA, dQG, dKD, beta YW and dgamma to bwd_gate.
 struct GradSm {
   bf16 wk[45056];  // work area (88 KB), regions bound in the kernel
+  uint64_t bar[2];  // bulk-load completion: saved tiles, then the dA operands
   float gg[C * SQ];  // G2 = G log2(e)
   bf16 rk[C * DK];
   float bet[C], braw[C], dbet[C], part[4 * C];
@@ -1130,13 +1142,19 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
     if (r < L) cp16(dst, (const bf16*)io.dO + ((size_t)(t0 + r) * H + h) * DV + 8 * p);
     else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
   }
-  cp_bytes(S.hi, w.sS + ch * 2 * DK * DV, 4 * DK * DV);
-  cp_bytes(dS.hi, w.sdS + ch * 2 * DK * DV, 4 * DK * DV);
-  cp_bytes(P.hi, w.sP + ch * 2 * C * C, 4 * C * C);
-  cp_bytes(W.hi, w.sW + ch * 2 * C * DK, 4 * C * DK);
-  cp_bytes(U.hi, w.sU + ch * 2 * C * DV, 4 * C * DV);
-  cp_bytes(T.hi, w.sT + ch * 2 * C * C, 4 * C * C);
   cp_commit();
+  if (tid == 0) {  // the saved tiles in one bulk transaction group
+    mbar_init(&sm.bar[0], 1);
+    mbar_init(&sm.bar[1], 1);
+    mbar_init_fence();
+    mbar_expect_tx(&sm.bar[0], 2 * 4 * DK * DV + 2 * 4 * C * C + 4 * C * DK + 4 * C * DV);
+    bulk_g2s(S.hi, w.sS + ch * 2 * DK * DV, 4 * DK * DV, &sm.bar[0]);
+    bulk_g2s(dS.hi, w.sdS + ch * 2 * DK * DV, 4 * DK * DV, &sm.bar[0]);
+    bulk_g2s(P.hi, w.sP + ch * 2 * C * C, 4 * C * C, &sm.bar[0]);
+    bulk_g2s(W.hi, w.sW + ch * 2 * C * DK, 4 * C * DK, &sm.bar[0]);
+    bulk_g2s(U.hi, w.sU + ch * 2 * C * DV, 4 * C * DV, &sm.bar[0]);
+    bulk_g2s(T.hi, w.sT + ch * 2 * C * C, 4 * C * C, &sm.bar[0]);
+  }
 
   // ---- k^, G, beta (thread: row tid / 4, key channels 8 (tid % 4) .., value columns 16 (tid % 4) ..)
   const int r = tid >> 2, q4 = tid & 3;
@@ -1208,7 +1226,11 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
     xkg[e + 1] = kv[e + 1] * exp2f(gv[e + 1]);
   }
   cp_wait_all();
-  __syncthreads();
+  if (__syncthreads_or(!mbar_wait(&sm.bar[0], 0))) {  // a bulk load did not complete in bound
+    mbar_wait(&sm.bar[0], 0);
+    if (tid == 0) atomicExch(w.err, -7);
+    return;
+  }
 
   const int I = warp & 3, hk = warp >> 2;  // owner tile: rows 16 I .., columns 32 hk .. / 16 hk ..
   // ---- dE = P^T dO + KD dS' and E = U - W S
@@ -1264,14 +1286,14 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
       float pp[2][4];
       zero(pp);
       gemm3<1, false, false>(pp, dO, 16 * bI, 0, E, 16 * bJ, 0, DV / 16);
-      float* g = w.gDP + (ch * NBLK + t) * 256;
+      float* g = w.gDP + (ch * NBLK + t) * 16 * PB;
 #pragma unroll
       for (int jt = 0; jt < 2; jt++)
 #pragma unroll
         for (int hh = 0; hh < 2; hh++) {
           const int m = gq + 8 * hh, n = 8 * jt + 2 * tq;
           const int rr = 16 * bI + m, s0 = 16 * bJ + n;
-          *reinterpret_cast<float2*>(g + m * 16 + n) =
+          *reinterpret_cast<float2*>(g + m * PB + n) =
               make_float2(s0 <= rr ? scale * pp[jt][2 * hh] : 0.f, s0 + 1 <= rr ? scale * pp[jt][2 * hh + 1] : 0.f);
         }
     }
@@ -1281,12 +1303,14 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
       w.gdg[ch * DK + tid] = acc1;
     }
   }
+  fence_async_smem();
   __syncthreads();
-  // group 3: U, W, A' for the dA products (over dO, S, dS', E: all read by now)
-  cp_bytes(U2.hi, w.sU + ch * 2 * C * DV, 4 * C * DV);
-  cp_bytes(W2.hi, w.sW + ch * 2 * C * DK, 4 * C * DK);
-  cp_bytes(wk + 12288, w.sA + ch * NBLK * 256, NBLK * 256 * 4);
-  cp_commit();
+  if (tid == 0) {  // U, W, A' for the dA products (over dO, S, dS', E: all read by now)
+    mbar_expect_tx(&sm.bar[1], 4 * C * DV + 4 * C * DK + NBLK * 256 * 4);
+    bulk_g2s(U2.hi, w.sU + ch * 2 * C * DV, 4 * C * DV, &sm.bar[1]);
+    bulk_g2s(W2.hi, w.sW + ch * 2 * C * DK, 4 * C * DK, &sm.bar[1]);
+    bulk_g2s(wk + 12288, w.sA + ch * NBLK * 256, NBLK * 256 * 4, &sm.bar[1]);
+  }
   // ---- YU = T^T dE, YW = T^T dW (registers, then over dE / dW); dv = beta YU; beta YW to bwd_gate
   {
     float yu[4][4], yw[2][4];
@@ -1317,8 +1341,11 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
       }
     frag_store(w.gKG + ch * NTH * 8, yw);
   }
-  cp_wait_all();
-  __syncthreads();
+  if (__syncthreads_or(!mbar_wait(&sm.bar[1], 0))) {
+    mbar_wait(&sm.bar[1], 0);
+    if (tid == 0) atomicExch(w.err, -7);
+    return;
+  }
   // ---- dbeta (U and W terms, row layout); dA, MA = beta dA (to bwd_gate) and the A' term
   {
     float vv[16];
@@ -1340,7 +1367,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
     zero(aa);
     gemm3<1, false, false>(aa, YU, 16 * bI, 0, U2, 16 * bJ, 0, DV / 16);
     gemm3<1, false, false>(aa, YW, 16 * bI, 0, W2, 16 * bJ, 0, DK / 16);
-    float* g = w.gMA + (ch * NBLK + t) * 256;
+    float* g = w.gMA + (ch * NBLK + t) * 16 * PB;
     const float* ab = A2 + t * 256;
     float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
@@ -1352,7 +1379,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
         const float da0 = s0 < rr ? -aa[jt][2 * hh] : 0.f, da1 = s0 + 1 < rr ? -aa[jt][2 * hh + 1] : 0.f;
         const float pa = da0 * ab[m * 16 + n] + da1 * ab[m * 16 + n + 1];
         if (hh == 0) rs0 += pa; else rs1 += pa;
-        *reinterpret_cast<float2*>(g + m * 16 + n) = make_float2(sm.bet[rr] * da0, sm.bet[rr] * da1);
+        *reinterpret_cast<float2*>(g + m * PB + n) = make_float2(sm.bet[rr] * da0, sm.bet[rr] * da1);
       }
     rs0 += __shfl_xor_sync(0xffffffffu, rs0, 1);
     rs0 += __shfl_xor_sync(0xffffffffu, rs0, 2);
@@ -1386,6 +1413,7 @@ struct GateSm {
   float gam[DK], dgam[DK];
   float tot[NW * DK], ks[4 * DK], part[NW * DK], red[NW];
   int spanok[4];
+  uint64_t bar;  // bulk-load completion of dP' and MA
 };
 
 __global__ void __launch_bounds__(NTH, 2) bwd_gate_kernel(Dims d, BwdIO io, Ws w) {
@@ -1418,15 +1446,16 @@ __global__ void __launch_bounds__(NTH, 2) bwd_gate_kernel(Dims d, BwdIO io, Ws w
     }
   }
   cp_commit();
-  for (int idx = tid; idx < NBLK * 16 * 4; idx += NTH) {  // 4 x 16 B per block row
-    const int row = idx >> 2, p = idx & 3;
-    cp16(sm.dp + row * PB + 4 * p, w.gDP + ch * NBLK * 256 + row * 16 + 4 * p);
-    cp16(sm.ma + row * PB + 4 * p, w.gMA + ch * NBLK * 256 + row * 16 + 4 * p);
+  if (tid == 0) {
+    mbar_init(&sm.bar, 1);
+    mbar_init_fence();
+    mbar_expect_tx(&sm.bar, 2 * NBLK * 16 * PB * 4);
+    bulk_g2s(sm.dp, w.gDP + ch * NBLK * 16 * PB, NBLK * 16 * PB * 4, &sm.bar);
+    bulk_g2s(sm.ma, w.gMA + ch * NBLK * 16 * PB, NBLK * 16 * PB * 4, &sm.bar);
   }
-  cp_commit();
   if (tid < DK) sm.dgam[tid] = w.gdg[ch * DK + tid];
   if (tid < 4) sm.spanok[tid] = 1;
-  asm volatile("cp.async.wait_group 1;\n" ::);
+  cp_wait_all();
   __syncthreads();
 
   // ---- q^, k^ norms and G (thread: row tid / 4, key channels 8 (tid % 4) ..)
@@ -1488,8 +1517,11 @@ __global__ void __launch_bounds__(NTH, 2) bwd_gate_kernel(Dims d, BwdIO io, Ws w
   frag_load(w.gQG + ch * NTH * 8, dQG);
   frag_load(w.gKD + ch * NTH * 8, dKD);
   frag_load(w.gKG + ch * NTH * 8, dkg);
-  cp_wait_all();
-  __syncthreads();
+  if (__syncthreads_or(!mbar_wait(&sm.bar, 0))) {  // a bulk load did not complete in bound
+    mbar_wait(&sm.bar, 0);
+    if (tid == 0) atomicExch(w.err, -7);
+    return;
+  }
 
   const int I = warp & 3, hk = warp >> 2;  // owner tile: rows 16 I .., key columns 16 hk ..
   const bool ok = sm.spanok[I];
