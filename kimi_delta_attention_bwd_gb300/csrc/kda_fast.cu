@@ -30,6 +30,7 @@
 // recomputes the chunk and forms every local gradient on chip.
 #include "kda_internal.cuh"
 #include "kda_mma.cuh"
+#include "kda_tc.cuh"
 
 namespace kda {
 namespace fast {
@@ -41,6 +42,7 @@ constexpr int SQ = DK + 4;  // row stride of [C][DK] operands read along rows
 constexpr int SV = DV + 8;  // row stride of [C][DV] operands
 constexpr int SC = C + 4;   // row stride of [C][C] matrices
 constexpr int NTH = 256, NW = 8;
+constexpr uint32_t TCOLS = 256;  // TMEM columns of a tensor-core CTA (two per SM share the 512)
 constexpr float SPAN_MAX = 80.f;
 // The per-chunk kernels keep G in log2 units (G2 = G log2(e)) so that every
 // decay factor exp(G_a - G_b) is one exp2f of a difference.
@@ -526,6 +528,16 @@ struct ChunkSm {
   int spanok[4];
 };
 
+// The six upper 16 x 16 blocks of a C x C split tile set to zero (the backward
+// reads whole tiles with the tensor core).
+__device__ __forceinline__ void zero_upper(const Op& t) {
+  for (int idx = threadIdx.x; idx < 6 * 16 * 8; idx += NTH) {
+    const int u = idx >> 7, rem = idx & 127;
+    const int bI = u < 3 ? 0 : u < 5 ? 1 : 2, bJ = u < 3 ? u + 1 : u < 5 ? u - 1 : 3;
+    op_store2(t, 16 * bI + (rem >> 3), 16 * bJ + 2 * (rem & 7), 0.f, 0.f);
+  }
+}
+
 // Stores a 16 x (8 NT) accumulator tile at (r0, c0) of a split operand tile
 // (global or shared), mapping each value through fn(r, c, v).
 template <int NT, class F>
@@ -554,6 +566,10 @@ __device__ __forceinline__ void store_acc(const float (&acc)[NT][4], float* g, i
           make_float2(fn(r, c, acc[jt][2 * hh]), fn(r, c + 1, acc[jt][2 * hh + 1]));
     }
 }
+
+static_assert(offsetof(ChunkSm, x) % 16 == 0 && offsetof(ChunkSm, am) % 16 == 0 && offsetof(ChunkSm, op) % 16 == 0 &&
+                  offsetof(ChunkSm, y) % 16 == 0,
+              "operand tiles need 16-byte rows");
 
 __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws w) {
   extern __shared__ __align__(16) unsigned char smraw[];
@@ -719,7 +735,10 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
       });
     }
   }
-  if (io.save) fence_async_smem();
+  if (io.save) {
+    zero_upper(P);
+    fence_async_smem();
+  }
   __syncthreads();
   if (io.save && tid == 0) {  // P for the backward (its tile is not written again)
     bulk_s2g(w.sP + ch * 2 * C * C, P.hi, 4 * C * C);
@@ -738,7 +757,10 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     const int rr = 16 * bI + (rem >> 3), s2 = 16 * bJ + 2 * (rem & 7);
     op_store2(T, rr, s2, tm[rr * SC + s2], tm[rr * SC + s2 + 1]);
   }
-  if (io.save) fence_async_smem();
+  if (io.save) {
+    zero_upper(T);
+    fence_async_smem();
+  }
   __syncthreads();
   if (io.save && tid == 0) {  // T for the backward (its tile is not written again)
     bulk_s2g(w.sT + ch * 2 * C * C, T.hi, 4 * C * C);
@@ -1092,13 +1114,15 @@ __device__ __forceinline__ void frag_load(const float* g, float (&v)[2][4]) {
 //   dbeta = rowsum(YU .* V) + rowsum(YW .* K^ e^G) + rowsum(dA .* A'),
 // writes dv and db, and hands dP', MA, dQG, dKD, beta YW and dgamma to bwd_gate.
 struct GradSm {
-  bf16 wk[45056];  // work area (88 KB), regions bound in the kernel
-  uint64_t bar[2];  // bulk-load completion: saved tiles, then the dA operands
-  float gg[C * SQ];  // G2 = G log2(e)
-  bf16 rk[C * DK];
+  __align__(16) bf16 wk[45056];  // work area (88 KB), regions bound in the kernel
+  __align__(16) float gg[C * SQ];
+  __align__(16) bf16 rk[C * DK];  // 16-byte cp.async / vector access
   float bet[C], braw[C], dbet[C], part[4 * C];
   float tot[NW * DK];
+  uint64_t bar[3];  // bulk-load completion (saved tiles, the dA operands); MMA rounds
+  uint32_t tslot;   // TMEM base address
 };
+static_assert(offsetof(GradSm, rk) % 16 == 0 && offsetof(GradSm, gg) % 16 == 0, "vector-accessed arrays");
 
 __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w) {
   extern __shared__ __align__(16) unsigned char smraw[];
@@ -1146,6 +1170,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   if (tid == 0) {  // the saved tiles in one bulk transaction group
     mbar_init(&sm.bar[0], 1);
     mbar_init(&sm.bar[1], 1);
+    mbar_init(&sm.bar[2], 1);
     mbar_init_fence();
     mbar_expect_tx(&sm.bar[0], 2 * 4 * DK * DV + 2 * 4 * C * C + 4 * C * DK + 4 * C * DV);
     bulk_g2s(S.hi, w.sS + ch * 2 * DK * DV, 4 * DK * DV, &sm.bar[0]);
@@ -1155,6 +1180,8 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
     bulk_g2s(U.hi, w.sU + ch * 2 * C * DV, 4 * C * DV, &sm.bar[0]);
     bulk_g2s(T.hi, w.sT + ch * 2 * C * C, 4 * C * C, &sm.bar[0]);
   }
+
+  if (warp == 0) tc::tmem_alloc(&sm.tslot, TCOLS);  // published by the barrier below
 
   // ---- k^, G, beta (thread: row tid / 4, key channels 8 (tid % 4) .., value columns 16 (tid % 4) ..)
   const int r = tid >> 2, q4 = tid & 3;
@@ -1169,7 +1196,10 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
     braw = bfl(((const bf16*)io.b)[row]);
   }
   asm volatile("cp.async.wait_group 1;\n" ::);
+  tc::fence_before();
   __syncthreads();
+  tc::fence_after();
+  const uint32_t tb = sm.tslot;
   float kv[8], gv[8];
   if (in) {
     unpack8(*reinterpret_cast<const uint4*>(sm.rk + r * DK + 8 * q4), kv);
@@ -1226,52 +1256,82 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
     xkg[e + 1] = kv[e + 1] * exp2f(gv[e + 1]);
   }
   cp_wait_all();
+  fence_async_smem();  // KD and dO are read by the tensor core next
+  tc::fence_before();
   if (__syncthreads_or(!mbar_wait(&sm.bar[0], 0))) {  // a bulk load did not complete in bound
     mbar_wait(&sm.bar[0], 0);
+    if (warp == 0) tc::tmem_dealloc(tb, TCOLS);
     if (tid == 0) atomicExch(w.err, -7);
     return;
   }
+  // MMA rounds: one thread issues, completion on bar[2] (phase mph), all warps
+  // then read their fragments.  TMEM columns: dE 0 | E 64 | dKD 128 | dQG 160 |
+  // dW' 192 | YW 224;  dP' reuses 0, YU 64, dA 128.
+  uint32_t mph = 0;
+  auto round_done = [&]() -> bool {  // uniform over the CTA
+    const bool ok = mbar_wait(&sm.bar[2], mph);
+    mph ^= 1;
+    tc::fence_after();
+    return !__syncthreads_or(!ok);
+  };
+  auto bail = [&]() {
+    mbar_wait(&sm.bar[2], mph ^ 1);
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tb, TCOLS);
+    if (tid == 0) atomicExch(w.err, -7);
+  };
 
   const int I = warp & 3, hk = warp >> 2;  // owner tile: rows 16 I .., columns 32 hk .. / 16 hk ..
   // ---- dE = P^T dO + KD dS' and E = U - W S
+  if (tid == 0) {
+    tc::fence_after();
+    tc::gemm_split(tb + 0, tc::mnmaj(P), tc::mnmaj(dO), 64, C / 16, false);
+    tc::gemm_split(tb + 0, tc::kmaj(KD), tc::mnmaj(dS), 64, DK / 16, true);
+    tc::gemm_split(tb + 64, tc::kmaj(W), tc::mnmaj(S), 64, DK / 16, false);
+    tc::commit(&sm.bar[2]);
+  }
+  if (!round_done()) { bail(); return; }
   {
-    float acc[4][4], acc2[4][4], accE[4][4];
-    zero(acc);
-    zero(acc2);
-    zero(accE);
-    gemm3<2, true, true>(acc, P, 16 * I, 16 * I, dO, 32 * hk, 16 * I, 4 - I);
-    gemm3<2, false, true>(acc2, KD, 16 * I, 0, dS, 32 * hk, 0, DK / 16);
-    gemm3<2, false, true>(accE, W, 16 * I, 0, S, 32 * hk, 0, DK / 16);
+    float dEr[4][4], ws[4][4];
+    tc::ld_frag<4>(tb + 0, 32 * hk, dEr);
+    tc::ld_frag<4>(tb + 64, 32 * hk, ws);
+    // each thread reads U at the positions it then overwrites with dE; E goes over P
 #pragma unroll
     for (int jt = 0; jt < 4; jt++)
 #pragma unroll
       for (int hh = 0; hh < 2; hh++) {
         const int rr = 16 * I + gq + 8 * hh, col = 32 * hk + 8 * jt + 2 * tq;
-        acc[jt][2 * hh] += acc2[jt][2 * hh];
-        acc[jt][2 * hh + 1] += acc2[jt][2 * hh + 1];
-        accE[jt][2 * hh] = op_get(U, rr, col) - accE[jt][2 * hh];
-        accE[jt][2 * hh + 1] = op_get(U, rr, col + 1) - accE[jt][2 * hh + 1];
-      }
-    __syncthreads();  // P, W, U, KD fully read
-#pragma unroll
-    for (int jt = 0; jt < 4; jt++)
-#pragma unroll
-      for (int hh = 0; hh < 2; hh++) {
-        const int rr = 16 * I + gq + 8 * hh, col = 32 * hk + 8 * jt + 2 * tq;
-        op_store2(E, rr, col, accE[jt][2 * hh], accE[jt][2 * hh + 1]);
-        op_store2(dE, rr, col, acc[jt][2 * hh], acc[jt][2 * hh + 1]);
+        const float e0 = op_get(U, rr, col) - ws[jt][2 * hh], e1 = op_get(U, rr, col + 1) - ws[jt][2 * hh + 1];
+        op_store2(E, rr, col, e0, e1);
+        op_store2(dE, rr, col, dEr[jt][2 * hh], dEr[jt][2 * hh + 1]);
       }
   }
+  fence_async_smem();
+  tc::fence_before();
   __syncthreads();
-  // ---- dKD, dQG (to bwd_gate), dW (over W), dP' lower blocks (to bwd_gate), dgamma
+  // ---- dKD = E dS'^T, dQG = scale dO S^T (to bwd_gate), dW = -dE S^T (over W),
+  //      dP' = scale dO E^T lower blocks (to bwd_gate), dgamma
+  if (tid == 0) {
+    tc::fence_after();
+    tc::gemm_split(tb + 128, tc::kmaj(E), tc::kmaj(dS), 32, DV / 16, false);
+    tc::gemm_split(tb + 160, tc::kmaj(dO), tc::kmaj(S), 32, DV / 16, false);
+    tc::gemm_split(tb + 192, tc::kmaj(dE), tc::kmaj(S), 32, DV / 16, false);
+    tc::gemm_split(tb + 0, tc::kmaj(dO), tc::kmaj(E), 64, DV / 16, false);
+    tc::commit(&sm.bar[2]);
+  }
+  if (tid < DK) {
+    float acc1 = 0.f;
+    for (int jj = 0; jj < DV; jj++) acc1 += op_get(dS, tid, jj) * op_get(S, tid, jj);
+    w.gdg[ch * DK + tid] = acc1;
+  }
+  if (!round_done()) { bail(); return; }
   {
-    float dKD[2][4], dQG[2][4], acc[2][4];
-    zero(dKD);
-    zero(dQG);
-    zero(acc);
-    gemm3<1, false, false>(dKD, E, 16 * I, 0, dS, 16 * hk, 0, DV / 16);
-    gemm3<1, false, false>(dQG, dO, 16 * I, 0, S, 16 * hk, 0, DV / 16);
-    gemm3<1, false, false>(acc, dE, 16 * I, 0, S, 16 * hk, 0, DV / 16);
+    float dKD[2][4], dQG[2][4], acc[2][4], pp[4][4];
+    tc::ld_frag<2>(tb + 128, 16 * hk, dKD);
+    tc::ld_frag<2>(tb + 160, 16 * hk, dQG);
+    tc::ld_frag<2>(tb + 192, 16 * hk, acc);
+    tc::ld_frag<4>(tb + 0, 32 * hk, pp);
     each(dQG, [&](int, int, float& v) { v *= scale; });
     frag_store(w.gKD + ch * NTH * 8, dKD);
     frag_store(w.gQG + ch * NTH * 8, dQG);
@@ -1280,45 +1340,44 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
 #pragma unroll
       for (int hh = 0; hh < 2; hh++)
         op_store2(dW, 16 * I + gq + 8 * hh, 16 * hk + 8 * jt + 2 * tq, -acc[jt][2 * hh], -acc[jt][2 * hh + 1]);
-    for (int t = warp; t < NBLK; t += NW) {
-      int bI, bJ;
-      blk_ij(t, bI, bJ);
-      float pp[2][4];
-      zero(pp);
-      gemm3<1, false, false>(pp, dO, 16 * bI, 0, E, 16 * bJ, 0, DV / 16);
-      float* g = w.gDP + (ch * NBLK + t) * 16 * PB;
+#pragma unroll
+    for (int jb = 0; jb < 2; jb++) {  // blocks (I, J) of this warp's 32 columns, J <= I
+      const int J = 2 * hk + jb;
+      if (J > I) continue;
+      float* g = w.gDP + (ch * NBLK + blk_of(I, J)) * 16 * PB;
 #pragma unroll
       for (int jt = 0; jt < 2; jt++)
 #pragma unroll
         for (int hh = 0; hh < 2; hh++) {
           const int m = gq + 8 * hh, n = 8 * jt + 2 * tq;
-          const int rr = 16 * bI + m, s0 = 16 * bJ + n;
+          const int rr = 16 * I + m, s0 = 16 * J + n;
+          const float* v = pp[2 * jb + jt];
           *reinterpret_cast<float2*>(g + m * PB + n) =
-              make_float2(s0 <= rr ? scale * pp[jt][2 * hh] : 0.f, s0 + 1 <= rr ? scale * pp[jt][2 * hh + 1] : 0.f);
+              make_float2(s0 <= rr ? scale * v[2 * hh] : 0.f, s0 + 1 <= rr ? scale * v[2 * hh + 1] : 0.f);
         }
-    }
-    if (tid < DK) {
-      float acc1 = 0.f;
-      for (int jj = 0; jj < DV; jj++) acc1 += op_get(dS, tid, jj) * op_get(S, tid, jj);
-      w.gdg[ch * DK + tid] = acc1;
     }
   }
   fence_async_smem();
+  tc::fence_before();
   __syncthreads();
-  if (tid == 0) {  // U, W, A' for the dA products (over dO, S, dS', E: all read by now)
+  // ---- U, W, A' for the dA products (bulk, over dO, S, dS', E: all read by now);
+  //      YU = T^T dE, YW = T^T dW
+  if (tid == 0) {
     mbar_expect_tx(&sm.bar[1], 4 * C * DV + 4 * C * DK + NBLK * 256 * 4);
     bulk_g2s(U2.hi, w.sU + ch * 2 * C * DV, 4 * C * DV, &sm.bar[1]);
     bulk_g2s(W2.hi, w.sW + ch * 2 * C * DK, 4 * C * DK, &sm.bar[1]);
     bulk_g2s(wk + 12288, w.sA + ch * NBLK * 256, NBLK * 256 * 4, &sm.bar[1]);
+    tc::fence_after();
+    tc::gemm_split(tb + 64, tc::mnmaj(T), tc::mnmaj(dE), 64, C / 16, false);
+    tc::gemm_split(tb + 224, tc::mnmaj(T), tc::mnmaj(dW), 32, C / 16, false);
+    tc::commit(&sm.bar[2]);
   }
-  // ---- YU = T^T dE, YW = T^T dW (registers, then over dE / dW); dv = beta YU; beta YW to bwd_gate
-  {
+  if (!round_done()) { bail(); return; }
+  {  // YU over dE, YW over dW (each thread overwrites only what it read... the MMA read them: done);
+     // dv = beta YU; beta YW to bwd_gate
     float yu[4][4], yw[2][4];
-    zero(yu);
-    zero(yw);
-    gemm3<2, true, true>(yu, T, 16 * I, 16 * I, dE, 32 * hk, 16 * I, 4 - I);
-    gemm3<1, true, true>(yw, T, 16 * I, 16 * I, dW, 16 * hk, 16 * I, 4 - I);
-    __syncthreads();  // dE and dW fully read
+    tc::ld_frag<4>(tb + 64, 32 * hk, yu);
+    tc::ld_frag<2>(tb + 224, 16 * hk, yw);
     bf16* dvo = (bf16*)io.dv;
 #pragma unroll
     for (int jt = 0; jt < 4; jt++)
@@ -1341,12 +1400,22 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
       }
     frag_store(w.gKG + ch * NTH * 8, yw);
   }
+  fence_async_smem();
+  tc::fence_before();
   if (__syncthreads_or(!mbar_wait(&sm.bar[1], 0))) {
     mbar_wait(&sm.bar[1], 0);
+    if (warp == 0) tc::tmem_dealloc(tb, TCOLS);
     if (tid == 0) atomicExch(w.err, -7);
     return;
   }
-  // ---- dbeta (U and W terms, row layout); dA, MA = beta dA (to bwd_gate) and the A' term
+  // ---- dA = -(YU U^T + YW W^T) strict lower; dbeta (U and W terms, row layout); MA = beta dA
+  //      (to bwd_gate) and the A' term of dbeta
+  if (tid == 0) {
+    tc::fence_after();
+    tc::gemm_split(tb + 128, tc::kmaj(YU), tc::kmaj(U2), 64, DV / 16, false);
+    tc::gemm_split(tb + 128, tc::kmaj(YW), tc::kmaj(W2), 64, DK / 16, true);
+    tc::commit(&sm.bar[2]);
+  }
   {
     float vv[16];
     unpack8(vraw[0], vv);
@@ -1360,37 +1429,45 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
     acc += __shfl_xor_sync(0xffffffffu, acc, 2);
     if (q4 == 0) sm.dbet[r] = acc;
   }
-  for (int t = warp; t < NBLK; t += NW) {
-    int bI, bJ;
-    blk_ij(t, bI, bJ);
-    float aa[2][4];
-    zero(aa);
-    gemm3<1, false, false>(aa, YU, 16 * bI, 0, U2, 16 * bJ, 0, DV / 16);
-    gemm3<1, false, false>(aa, YW, 16 * bI, 0, W2, 16 * bJ, 0, DK / 16);
-    float* g = w.gMA + (ch * NBLK + t) * 16 * PB;
-    const float* ab = A2 + t * 256;
-    float rs0 = 0.f, rs1 = 0.f;
+  if (!round_done()) { bail(); return; }
+  {
+    float aa[4][4];
+    tc::ld_frag<4>(tb + 128, 32 * hk, aa);
+    const float* A2 = reinterpret_cast<const float*>(wk + 12288);
 #pragma unroll
-    for (int jt = 0; jt < 2; jt++)
+    for (int jb = 0; jb < 2; jb++) {
+      const int J = 2 * hk + jb;
+      float rs0 = 0.f, rs1 = 0.f;
+      if (J <= I) {
+        const int t = blk_of(I, J);
+        float* g = w.gMA + (ch * NBLK + t) * 16 * PB;
+        const float* ab = A2 + t * 256;
 #pragma unroll
-      for (int hh = 0; hh < 2; hh++) {
-        const int m = gq + 8 * hh, n = 8 * jt + 2 * tq;
-        const int rr = 16 * bI + m, s0 = 16 * bJ + n;
-        const float da0 = s0 < rr ? -aa[jt][2 * hh] : 0.f, da1 = s0 + 1 < rr ? -aa[jt][2 * hh + 1] : 0.f;
-        const float pa = da0 * ab[m * 16 + n] + da1 * ab[m * 16 + n + 1];
-        if (hh == 0) rs0 += pa; else rs1 += pa;
-        *reinterpret_cast<float2*>(g + m * PB + n) = make_float2(sm.bet[rr] * da0, sm.bet[rr] * da1);
+        for (int jt = 0; jt < 2; jt++)
+#pragma unroll
+          for (int hh = 0; hh < 2; hh++) {
+            const int m = gq + 8 * hh, n = 8 * jt + 2 * tq;
+            const int rr = 16 * I + m, s0 = 16 * J + n;
+            const float* v = aa[2 * jb + jt];
+            const float da0 = s0 < rr ? -v[2 * hh] : 0.f, da1 = s0 + 1 < rr ? -v[2 * hh + 1] : 0.f;
+            const float pa = da0 * ab[m * 16 + n] + da1 * ab[m * 16 + n + 1];
+            if (hh == 0) rs0 += pa; else rs1 += pa;
+            *reinterpret_cast<float2*>(g + m * PB + n) = make_float2(sm.bet[rr] * da0, sm.bet[rr] * da1);
+          }
       }
-    rs0 += __shfl_xor_sync(0xffffffffu, rs0, 1);
-    rs0 += __shfl_xor_sync(0xffffffffu, rs0, 2);
-    rs1 += __shfl_xor_sync(0xffffffffu, rs1, 1);
-    rs1 += __shfl_xor_sync(0xffffffffu, rs1, 2);
-    if (tq == 0) {
-      sm.part[bJ * C + 16 * bI + gq] = rs0;
-      sm.part[bJ * C + 16 * bI + gq + 8] = rs1;
+      rs0 += __shfl_xor_sync(0xffffffffu, rs0, 1);
+      rs0 += __shfl_xor_sync(0xffffffffu, rs0, 2);
+      rs1 += __shfl_xor_sync(0xffffffffu, rs1, 1);
+      rs1 += __shfl_xor_sync(0xffffffffu, rs1, 2);
+      if (J <= I && tq == 0) {
+        sm.part[J * C + 16 * I + gq] = rs0;
+        sm.part[J * C + 16 * I + gq + 8] = rs1;
+      }
     }
   }
+  tc::fence_before();
   __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tb, TCOLS);
   if (tid < L) {  // fixed-order sum over the column blocks: deterministic
     float acc = sm.dbet[tid];
     for (int J = 0; J <= (tid >> 4); J++) acc += sm.part[J * C + tid];
@@ -1415,6 +1492,10 @@ struct GateSm {
   int spanok[4];
   uint64_t bar;  // bulk-load completion of dP' and MA
 };
+
+static_assert(offsetof(GateSm, rq) % 16 == 0 && offsetof(GateSm, rk) % 16 == 0 && offsetof(GateSm, rf) % 16 == 0 &&
+                  offsetof(GateSm, dp) % 16 == 0 && offsetof(GateSm, ma) % 16 == 0,
+              "vector-accessed arrays");
 
 __global__ void __launch_bounds__(NTH, 2) bwd_gate_kernel(Dims d, BwdIO io, Ws w) {
   extern __shared__ __align__(16) unsigned char smraw[];
