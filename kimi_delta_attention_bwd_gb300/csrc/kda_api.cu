@@ -296,6 +296,7 @@ static kda_status check_problem(const kda_problem* p, Dims* d) {
   d->tag = (int32_t)(hsh | 1u);
   d->save = 0;
   d->fast = fast_path(p->dtype, p->dk, p->dv) ? 1 : 0;
+  d->ahead = 0;
   return KDA_OK;
 }
 

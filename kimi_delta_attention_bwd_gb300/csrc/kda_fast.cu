@@ -538,6 +538,20 @@ __device__ __forceinline__ void zero_upper(const Op& t) {
   }
 }
 
+// The chunk-head that the per-chunk kernels run one wave (d.ahead CTAs) after
+// CTA (j, h); false past the end.  Prefetching its inputs into L2 turns the
+// next wave's cold DRAM reads into L2 hits.
+__device__ __forceinline__ bool ahead_of(const Dims& d, const Ws& w, int j, int h, int& j2, int& h2) {
+  const int64_t nxt = (int64_t)h * d.nc_max + j + d.ahead;
+  j2 = (int)(nxt % d.nc_max);
+  h2 = (int)(nxt / d.nc_max);
+  return d.ahead > 0 && h2 < d.H && j2 < *w.n_chunks;
+}
+// Thread tid < L prefetches row tid of a [tokens][H][n] bf16 tensor (n * 2 <= 128 bytes).
+__device__ __forceinline__ void prefetch_rows(const void* base, int n, int t0, int L, int H, int h) {
+  if ((int)threadIdx.x < L) prefetch_l2((const bf16*)base + ((size_t)(t0 + threadIdx.x) * H + h) * n);
+}
+
 // Stores a 16 x (8 NT) accumulator tile at (r0, c0) of a split operand tile
 // (global or shared), mapping each value through fn(r, c, v).
 template <int NT, class F>
@@ -585,6 +599,17 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
   const float* dtb = io.dt_bias + h * DK;
   const bf16* qraw = (const bf16*)io.q;
   const bf16* kraw = (const bf16*)io.k;
+  {
+    int j2, h2;
+    if (ahead_of(d, w, j, h, j2, h2)) {
+      const int L2 = w.chunk_len[j2], t2 = w.chunk_tok0[j2];
+      prefetch_rows(io.q, DK, t2, L2, H, h2);
+      prefetch_rows(io.k, DK, t2, L2, H, h2);
+      prefetch_rows(io.f, DK, t2, L2, H, h2);
+      prefetch_rows(io.v, DV, t2, L2, H, h2);
+      prefetch_rows(io.b, 1, t2, L2, H, h2);
+    }
+  }
 
   const Op LQ{sm.x, sm.x + 2048, DK}, LK{sm.x + 4096, sm.x + 6144, DK}, R{sm.x + 8192, sm.x + 13312, DK};
   const Op W{sm.x, sm.x + 2048, DK}, U{sm.x + 4096, sm.x + 8192, DV}, KD{sm.x + 14336, sm.x + 16384, DK};
@@ -1181,6 +1206,27 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
     bulk_g2s(T.hi, w.sT + ch * 2 * C * C, 4 * C * C, &sm.bar[0]);
   }
 
+  {
+    int j2, h2;
+    if (ahead_of(d, w, j, h, j2, h2)) {
+      const int L2 = w.chunk_len[j2], t2 = w.chunk_tok0[j2];
+      const int64_t c2 = (int64_t)j2 * H + h2;
+      prefetch_rows(io.k, DK, t2, L2, H, h2);
+      prefetch_rows(io.f, DK, t2, L2, H, h2);
+      prefetch_rows(io.v, DV, t2, L2, H, h2);
+      prefetch_rows(io.dO, DV, t2, L2, H, h2);
+      prefetch_rows(io.b, 1, t2, L2, H, h2);
+      if (tid == 0) {
+        bulk_prefetch_l2(w.sS + c2 * 2 * DK * DV, 4 * DK * DV);
+        bulk_prefetch_l2(w.sdS + c2 * 2 * DK * DV, 4 * DK * DV);
+        bulk_prefetch_l2(w.sP + c2 * 2 * C * C, 4 * C * C);
+        bulk_prefetch_l2(w.sW + c2 * 2 * C * DK, 4 * C * DK);
+        bulk_prefetch_l2(w.sU + c2 * 2 * C * DV, 4 * C * DV);
+        bulk_prefetch_l2(w.sT + c2 * 2 * C * C, 4 * C * C);
+        bulk_prefetch_l2(w.sA + c2 * NBLK * 256, NBLK * 256 * 4);
+      }
+    }
+  }
   if (warp == 0) tc::tmem_alloc(&sm.tslot, TCOLS);  // published by the barrier below
 
   // ---- k^, G, beta (thread: row tid / 4, key channels 8 (tid % 4) .., value columns 16 (tid % 4) ..)
@@ -1320,10 +1366,20 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
     tc::gemm_split(tb + 0, tc::kmaj(dO), tc::kmaj(E), 64, DV / 16, false);
     tc::commit(&sm.bar[2]);
   }
-  if (tid < DK) {
+  {  // dgamma_i = sum_j dS'_ij S_ij: thread = row tid / 8, columns 8 (tid % 8) ..
+    const int i = tid >> 3, c8 = 8 * (tid & 7), o = opix(i, c8, DV);
+    float x[8], y[8], xl[8], yl[8];
+    unpack8(*reinterpret_cast<const uint4*>(dS.hi + o), x);
+    unpack8(*reinterpret_cast<const uint4*>(dS.lo + o), xl);
+    unpack8(*reinterpret_cast<const uint4*>(S.hi + o), y);
+    unpack8(*reinterpret_cast<const uint4*>(S.lo + o), yl);
     float acc1 = 0.f;
-    for (int jj = 0; jj < DV; jj++) acc1 += op_get(dS, tid, jj) * op_get(S, tid, jj);
-    w.gdg[ch * DK + tid] = acc1;
+#pragma unroll
+    for (int e = 0; e < 8; e++) acc1 += (x[e] + xl[e]) * (y[e] + yl[e]);
+    acc1 += __shfl_xor_sync(0xffffffffu, acc1, 1);
+    acc1 += __shfl_xor_sync(0xffffffffu, acc1, 2);
+    acc1 += __shfl_xor_sync(0xffffffffu, acc1, 4);
+    if ((tid & 7) == 0) w.gdg[ch * DK + i] = acc1;
   }
   if (!round_done()) { bail(); return; }
   {
@@ -1511,6 +1567,23 @@ __global__ void __launch_bounds__(NTH, 2) bwd_gate_kernel(Dims d, BwdIO io, Ws w
   const float a = expf(io.A_log[h]);
   const float* dtb = io.dt_bias + h * DK;
 
+  {
+    int j2, h2;
+    if (ahead_of(d, w, j, h, j2, h2)) {
+      const int L2 = w.chunk_len[j2], t2 = w.chunk_tok0[j2];
+      const int64_t c2 = (int64_t)j2 * H + h2;
+      prefetch_rows(io.q, DK, t2, L2, H, h2);
+      prefetch_rows(io.k, DK, t2, L2, H, h2);
+      prefetch_rows(io.f, DK, t2, L2, H, h2);
+      if (tid == 0) {
+        bulk_prefetch_l2(w.gDP + c2 * NBLK * 16 * PB, NBLK * 16 * PB * 4);
+        bulk_prefetch_l2(w.gMA + c2 * NBLK * 16 * PB, NBLK * 16 * PB * 4);
+        bulk_prefetch_l2(w.gQG + c2 * NTH * 8, NTH * 8 * 4);
+        bulk_prefetch_l2(w.gKD + c2 * NTH * 8, NTH * 8 * 4);
+        bulk_prefetch_l2(w.gKG + c2 * NTH * 8, NTH * 8 * 4);
+      }
+    }
+  }
   // ---- group 1: raw q, k, f (rows past the chunk end zeroed);  group 2: dP', MA
   for (int idx = tid; idx < C * 4; idx += NTH) {
     const int r = idx >> 2, p = idx & 3, o = r * DK + 8 * p;
@@ -1795,7 +1868,22 @@ static_assert(sizeof(fast::GateSm) <= 112 * 1024, "gate kernel must fit two CTAs
 
 bool fast_path(int dtype, int dk, int dv) { return dtype == 0 && dk == fast::DK && dv == fast::DV; }
 
-cudaError_t launch_fast_fwd(const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st, bool fused) {
+// CTAs of the per-chunk kernels in flight on the current device (two per SM).
+static int wave_ctas() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = 2 * n;
+  }
+  return cached[dev];
+}
+
+cudaError_t launch_fast_fwd(const Dims& d0, const FwdIO& io, const Ws& w, cudaStream_t st, bool fused) {
+  Dims d = d0;
+  d.ahead = wave_ctas();
   cudaError_t e;
   if (fused) {
     const size_t smem = sizeof(fast::FwdSm);
@@ -1822,7 +1910,9 @@ cudaError_t launch_fast_fwd(const Dims& d, const FwdIO& io, const Ws& w, cudaStr
   return cudaGetLastError();
 }
 
-cudaError_t launch_fast_bwd(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st) {
+cudaError_t launch_fast_bwd(const Dims& d0, const BwdIO& io, const Ws& w, cudaStream_t st) {
+  Dims d = d0;
+  d.ahead = wave_ctas();
   const size_t sc = sizeof(fast::BChainSm), s1 = sizeof(fast::GradSm), s2 = sizeof(fast::GateSm);
   cudaError_t e = cudaFuncSetAttribute(fast::bwd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
   if (e == cudaSuccess)

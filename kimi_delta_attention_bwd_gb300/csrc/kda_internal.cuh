@@ -74,6 +74,7 @@ struct Dims {
   int32_t tag;   // nonzero hash of the problem; the forward stores it when saving
   int32_t save;  // forward saves for the backward
   int32_t fast;  // bf16 io with dk = 32, dv = 64: tensor-core kernels
+  int32_t ahead; // CTAs in flight (one wave) of the per-chunk tensor-core kernels: their L2 prefetch distance
 };
 
 // Backward kernels refuse a workspace that no saving forward of the same
