@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from kimi_delta_attention_bwd_gb300.inputs import BASE_SEED, WORKLOADS, make_inputs, numpy_f64  # noqa: E402
+from kimi_delta_attention_bwd_gb300.inputs import BASE_SEED, WORKLOADS, custom, make_inputs, numpy_f64  # noqa: E402
 
 METRIC = "KDA fwd and fwd+bwd tokens/s on 1 GB300 at 300M shape; % of roofline"
 STEP_WORKLOAD = 3   # fwd+bwd training step at the 300M layer shape
@@ -266,6 +266,33 @@ def make_step(w, inp, dev):
     return step, d, grads
 
 
+DECODE_SEQS = 2048  # concurrent sequences of the decode step (fp32 state 134 MB, larger than L2)
+
+
+def decode_bench(args, dev, flush, world, stream, hbm, rank):
+    """Single-token step of DECODE_SEQS sequences at the 300M head shape."""
+    from kimi_delta_attention_bwd_gb300 import kda_decode_step
+    w = WORKLOADS[STEP_WORKLOAD]
+    n, H, dk, dv = DECODE_SEQS, w.H, w.dk, w.dv
+    inp = make_inputs(custom(n, 1, H, dk, dv, dtype="bf16", h0=True), seed=BASE_SEED + 77 + 1000 * rank,
+                      with_grad_inputs=False)
+    d = {k: (t.to(dev) if isinstance(t, torch.Tensor) else t) for k, t in inp.items()}
+    q, k, v, f, b = (d[x][:, 0].contiguous() for x in ("q", "k", "v", "f", "b"))
+    state = d["h0"].clone()
+    o = torch.empty(n, H, dv, dtype=torch.bfloat16, device=dev)
+
+    def step():
+        kda_decode_step(q, k, v, f, b, d["A_log"], d["dt_bias"], state, scale=d["scale"], out=o)
+
+    ms = max_over_ranks(time_steps(step, args.steps, args.warmup, flush, world, stream), world, dev)
+    nbytes = n * H * (2 * dk * dv * 4 + 2 * (3 * dk + 2 * dv + 1))  # state in + out, q k f v o b
+    achieved = nbytes / (ms / 1e3) / 1e9
+    return {"value": world * n / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "workload": f"decode step, {n} sequences x {H} heads, {dk}/{dv}, bf16 io, fp32 state",
+            "roofline": {"bound": "hbm", "kernel": "decode", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "algorithmic_bytes_per_launch": nbytes, "launch_ms": ms}}
+
+
 def time_steps(step, steps, warmup, flush, world, stream):
     for _ in range(warmup):
         step()
@@ -302,6 +329,8 @@ def run_ours(args, rank, world, local):
     fstep, _, _ = make_step(wf, make_inputs(wf, seed=BASE_SEED + FWD_WORKLOAD + 1000 * rank), dev)
     fwd_ms = max_over_ranks(time_steps(fstep, args.steps, args.warmup, flush, world, stream), world, dev)
     del fstep
+    torch.cuda.empty_cache()
+    dec = decode_bench(args, dev, flush, world, stream, hbm, rank)
     torch.cuda.empty_cache()
 
     # the training step (timed region with per-kernel event brackets and clock sampling)
@@ -359,6 +388,7 @@ def run_ours(args, rank, world, local):
                        "l2": "flushed between timed steps (512 MiB write)"},
             "fwd": {"value": world * wf.tokens / (fwd_ms / 1e3), "unit": "tokens/s", "ms_per_step": fwd_ms,
                     "workload": wf.name},
+            "decode": dec,
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": traffic, "peak_kind": peak_kind,
                          "algorithmic_bytes_per_launch": ab, "launch_ms": dom_ms},

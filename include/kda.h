@@ -168,6 +168,26 @@ KDA_API kda_status kda_fwd_noalloc(const kda_problem* p,
                    const float* A_log, const float* dt_bias, const float* h0,
                    void* o, float* h_final, cudaStream_t stream);
 
+/* Single-token recurrent step (decode): one token for each of n_seq
+ * independent sequences, applied to their states in place.  Per sequence and
+ * head, the same recurrence as above for one token ("Pure KDA 300M" guide,
+ * Overview; the inference-only forward backend discussed in the openkimi
+ * README, "Testing and verification"):
+ *   S <- (I - beta k^ k^T) Diag(exp g) S + beta k^ v^T,   o = scale S^T q^
+ * Layouts (device pointers, 16-byte aligned, contiguous):
+ *   q, k, f : [n_seq, H, dk]     v, o : [n_seq, H, dv]     b : [n_seq, H]
+ *   A_log : [H] fp32    dt_bias : [H, dk] fp32
+ *   state : [n_seq, H, dk, dv] fp32, read and overwritten with the new state
+ * dtype is KDA_BF16 or KDA_F32 for q, k, v, f, b and o; (dk, dv) as kda_fwd;
+ * scale <= 0 selects 1/sqrt(dk).  Needs no workspace.  Returns
+ * KDA_ERR_INVALID_ARG / _UNSUPPORTED / _ALIGNMENT before any launch, or
+ * KDA_ERR_CUDA if the launch fails.  Steps on the same stream chain: each reads
+ * the state the previous one wrote. */
+KDA_API kda_status kda_decode(int n_seq, int H, int dk, int dv, int dtype, float scale,
+                   const void* q, const void* k, const void* v, const void* f, const void* b,
+                   const float* A_log, const float* dt_bias, float* state, void* o,
+                   cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

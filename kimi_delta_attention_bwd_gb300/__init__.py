@@ -5,6 +5,7 @@ libkda_gb300.so through its C ABI, include/kda.h):
 
   o, h_final, ctx = kda_forward(q, k, v, f, b, A_log, dt_bias, ...)
   grads = kda_backward(ctx, dO, dh_final=None)
+  o = kda_decode_step(q, k, v, f, b, A_log, dt_bias, state)   # one token, state in place
 
 Layouts: q, k, f [B, T, H, dk]; v [B, T, H, dv]; b [B, T, H] (bf16 or fp32);
 A_log [H], dt_bias [H, dk] fp32; optional cu_seqlens int32 [n_docs + 1] over
@@ -20,7 +21,7 @@ import torch
 from . import _lib
 from ._lib import KdaError, kda_device_status, kda_strerror_text  # noqa: F401
 
-__all__ = ["kda_forward", "kda_backward", "KdaContext", "KdaError", "kda_device_status"]
+__all__ = ["kda_forward", "kda_backward", "kda_decode_step", "KdaContext", "KdaError", "kda_device_status"]
 
 
 @dataclass
@@ -97,3 +98,22 @@ def kda_backward(ctx: KdaContext, dO, dh_final=None, want_dh0: bool = True, grad
                  grads["dq"], grads["dk"], grads["dv"], grads["df"], grads["db"], grads["dA_log"],
                  grads["ddt_bias"], grads.get("dh0"), ctx.workspace)
     return grads
+
+
+def kda_decode_step(q, k, v, f, b, A_log, dt_bias, state, scale: Optional[float] = None,
+                    out: Optional[torch.Tensor] = None):
+    """One token for each of n sequences: q, k, f [n, H, dk], v [n, H, dv],
+    b [n, H] (bf16 or fp32), state [n, H, dk, dv] fp32 updated in place.
+    Returns o [n, H, dv] in the io dtype."""
+    n, H, dk = q.shape
+    dv = v.shape[-1]
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (f, "f"), (b, "b")):
+        _check(t, nm, q.dtype)
+    _check(A_log, "A_log", torch.float32)
+    _check(dt_bias, "dt_bias", torch.float32)
+    _check(state, "state", torch.float32)
+    if tuple(state.shape) != (n, H, dk, dv):
+        raise ValueError(f"state must be {(n, H, dk, dv)}, got {tuple(state.shape)}")
+    o = out if out is not None else torch.empty(n, H, dv, dtype=q.dtype, device=q.device)
+    _lib.kda_decode(n, H, dk, dv, q.dtype, scale, q, k, v, f, b, A_log, dt_bias, state, o)
+    return o

@@ -72,6 +72,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.kda_prof_stop.restype = I
         lib.kda_prof_kernel_name.argtypes = [I]
         lib.kda_prof_kernel_name.restype = ctypes.c_char_p
+        lib.kda_decode.argtypes = [I, I, I, I, I, ctypes.c_float] + [P] * 9 + [P]
+        lib.kda_decode.restype = I
         _lib = lib
         return lib
 
@@ -138,6 +140,15 @@ def kda_bwd(problem, q, k, v, f, b, A_log, dt_bias, h0, dO, dh_final, dq, dk, dv
                         _stream())
     if st != 0:
         raise KdaError(st, "kda_bwd")
+
+
+def kda_decode(n_seq, H, dk, dv, dtype, scale, q, k, v, f, b, A_log, dt_bias, state, o):
+    """Raw single-token step; state [n_seq, H, dk, dv] fp32 is updated in place."""
+    dt = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32 if dtype == torch.float32 else 99
+    st = load().kda_decode(int(n_seq), int(H), int(dk), int(dv), dt, float(scale or 0.0), _p(q), _p(k), _p(v),
+                           _p(f), _p(b), _p(A_log), _p(dt_bias), _p(state), _p(o), _stream())
+    if st != 0:
+        raise KdaError(st, "kda_decode")
 
 
 def kda_device_status(workspace) -> int:

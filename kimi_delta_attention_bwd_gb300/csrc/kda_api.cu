@@ -390,7 +390,7 @@ const char* kda_strerror(kda_status s) {
 
 static const char* const k_names[K_COUNT] = {"chunk_table", "fwd_intra", "fwd_scan", "bwd_scan",
                                              "bwd_intra", "bwd_reduce", "fwd_chain", "fwd_chunk",
-                                             "fwd_state", "bwd_grad",  "bwd_gate"};
+                                             "fwd_state", "bwd_grad",  "bwd_gate",   "decode"};
 
 const char* kda_prof_kernel_name(int i) { return (i >= 0 && i < K_COUNT) ? k_names[i] : nullptr; }
 

@@ -24,6 +24,7 @@ enum KernelId {
   K_FWD_STATE,
   K_BWD_GRAD,
   K_BWD_GATE,
+  K_DECODE,
   K_COUNT
 };
 
