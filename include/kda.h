@@ -30,6 +30,10 @@
  *      v, o, dO, dv        : [B, T, H, dv]
  *      b, db               : [B, T, H]
  *      A_log, dA_log       : [H] fp32       dt_bias, ddt_bias : [H, dk] fp32
+ *    With gate = KDA_GATE_SCALAR (the scalar-gated Gated DeltaNet variant, one
+ *    log-decay per token and head broadcast over the dk channels; the openkimi
+ *    README, "Testing and verification", contrasts it with KDA's channel-wise
+ *    decay): f, df : [B, T, H] and dt_bias, ddt_bias : [H].
  *      h0, h_final, dh_final, dh0 : [n_docs, H, dk, dv] fp32
  *  - Alignment: every tensor pointer 16-byte aligned; workspace 256-byte.
  *  - Gradient outputs are overwritten, never accumulated.
@@ -78,6 +82,11 @@ typedef enum kda_dtype { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
  *  cu_seqlens_host : optional HOST copy of cu_seqlens; when given it is
  *              validated on the host (KDA_ERR_BAD_SEQLENS before any launch).
  */
+typedef enum kda_gate {
+    KDA_GATE_CHANNEL = 0,  /* KDA: one log-decay per key channel, f [.., H, dk], dt_bias [H, dk] */
+    KDA_GATE_SCALAR = 1    /* scalar-gated (GDN): one per head, f [.., H], dt_bias [H]; df [.., H], ddt_bias [H] */
+} kda_gate;
+
 typedef struct kda_problem {
     int32_t B, T, H, dk, dv;
     int32_t dtype;
@@ -85,6 +94,7 @@ typedef struct kda_problem {
     int32_t n_docs;
     const int32_t* cu_seqlens;
     const int32_t* cu_seqlens_host;
+    int32_t gate;          /* kda_gate */
 } kda_problem;
 
 /* Bytes of device workspace kda_fwd / kda_bwd need for this problem
@@ -179,11 +189,12 @@ KDA_API kda_status kda_fwd_noalloc(const kda_problem* p,
  *   A_log : [H] fp32    dt_bias : [H, dk] fp32
  *   state : [n_seq, H, dk, dv] fp32, read and overwritten with the new state
  * dtype is KDA_BF16 or KDA_F32 for q, k, v, f, b and o; (dk, dv) as kda_fwd;
+ * gate as kda_problem.gate (KDA_GATE_SCALAR: f [n_seq, H], dt_bias [H]);
  * scale <= 0 selects 1/sqrt(dk).  Needs no workspace.  Returns
  * KDA_ERR_INVALID_ARG / _UNSUPPORTED / _ALIGNMENT before any launch, or
  * KDA_ERR_CUDA if the launch fails.  Steps on the same stream chain: each reads
  * the state the previous one wrote. */
-KDA_API kda_status kda_decode(int n_seq, int H, int dk, int dv, int dtype, float scale,
+KDA_API kda_status kda_decode(int n_seq, int H, int dk, int dv, int dtype, int gate, float scale,
                    const void* q, const void* k, const void* v, const void* f, const void* b,
                    const float* A_log, const float* dt_bias, float* state, void* o,
                    cudaStream_t stream);

@@ -8,7 +8,7 @@ libkda_gb300.so through its C ABI, include/kda.h):
   o = kda_decode_step(q, k, v, f, b, A_log, dt_bias, state)   # one token, state in place
 
 Layouts: q, k, f [B, T, H, dk]; v [B, T, H, dv]; b [B, T, H] (bf16 or fp32);
-A_log [H], dt_bias [H, dk] fp32; optional cu_seqlens int32 [n_docs + 1] over
+A_log [H], dt_bias [H, dk] fp32 (scalar-gated variant: f [B, T, H], dt_bias [H]); optional cu_seqlens int32 [n_docs + 1] over
 the flattened B*T tokens; states [n_docs, H, dk, dv] fp32.
 """
 from __future__ import annotations
@@ -50,6 +50,21 @@ def _check(t, name, dtype=None):
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _gate_of(f, dt_bias, qshape):
+    """Gate mode from the shapes: f with q's shape (dt_bias [H, dk]) is KDA's
+    per-channel gate; f without the dk axis (dt_bias [H]) is the scalar gate."""
+    *lead, H, dk = qshape
+    if tuple(f.shape) == tuple(qshape):
+        if tuple(dt_bias.shape) != (H, dk):
+            raise ValueError(f"dt_bias must be {(H, dk)} for a per-channel gate")
+        return _lib.KDA_GATE_CHANNEL
+    if tuple(f.shape) == tuple(lead) + (H,):
+        if tuple(dt_bias.shape) != (H,):
+            raise ValueError(f"dt_bias must be {(H,)} for a scalar gate")
+        return _lib.KDA_GATE_SCALAR
+    raise ValueError(f"f must be {tuple(qshape)} (per-channel gate) or {tuple(lead) + (H,)} (scalar gate)")
+
+
 def kda_forward(q, k, v, f, b, A_log, dt_bias, scale: Optional[float] = None, h0=None,
                 cu_seqlens=None, cu_seqlens_host=None, save_for_backward: bool = True,
                 workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
@@ -67,7 +82,8 @@ def kda_forward(q, k, v, f, b, A_log, dt_bias, scale: Optional[float] = None, h0
     n_docs = B if cu_seqlens is None else cu_seqlens.numel() - 1
     if h0 is not None:
         _check(h0, "h0", torch.float32)
-    prob = _lib.make_problem(B, T, H, dk, dv, q.dtype, scale, cu_seqlens, cu_seqlens_host)
+    gate = _gate_of(f, dt_bias, (B, T, H, dk))
+    prob = _lib.make_problem(B, T, H, dk, dv, q.dtype, scale, cu_seqlens, cu_seqlens_host, gate)
     if workspace is None:
         workspace = _lib.alloc_workspace(prob, save_for_backward, q.device)
     o = out if out is not None else torch.empty(B, T, H, dv, dtype=q.dtype, device=q.device)
@@ -91,7 +107,7 @@ def kda_backward(ctx: KdaContext, dO, dh_final=None, want_dh0: bool = True, grad
             "dq": torch.empty_like(q), "dk": torch.empty_like(ctx.k), "dv": torch.empty_like(ctx.v),
             "df": torch.empty_like(ctx.f), "db": torch.empty_like(ctx.b),
             "dA_log": torch.empty(H, dtype=torch.float32, device=q.device),
-            "ddt_bias": torch.empty(H, dk, dtype=torch.float32, device=q.device),
+            "ddt_bias": torch.empty_like(ctx.dt_bias),
             "dh0": torch.empty(ctx.n_docs, H, dk, dv, dtype=torch.float32, device=q.device) if want_dh0 else None,
         }
     _lib.kda_bwd(ctx.problem, ctx.q, ctx.k, ctx.v, ctx.f, ctx.b, ctx.A_log, ctx.dt_bias, ctx.h0, dO, dh_final,
@@ -102,8 +118,9 @@ def kda_backward(ctx: KdaContext, dO, dh_final=None, want_dh0: bool = True, grad
 
 def kda_decode_step(q, k, v, f, b, A_log, dt_bias, state, scale: Optional[float] = None,
                     out: Optional[torch.Tensor] = None):
-    """One token for each of n sequences: q, k, f [n, H, dk], v [n, H, dv],
-    b [n, H] (bf16 or fp32), state [n, H, dk, dv] fp32 updated in place.
+    """One token for each of n sequences: q, k, f [n, H, dk] (or f [n, H] for
+    the scalar gate), v [n, H, dv], b [n, H] (bf16 or fp32), state
+    [n, H, dk, dv] fp32 updated in place.
     Returns o [n, H, dv] in the io dtype."""
     n, H, dk = q.shape
     dv = v.shape[-1]
@@ -114,6 +131,7 @@ def kda_decode_step(q, k, v, f, b, A_log, dt_bias, state, scale: Optional[float]
     _check(state, "state", torch.float32)
     if tuple(state.shape) != (n, H, dk, dv):
         raise ValueError(f"state must be {(n, H, dk, dv)}, got {tuple(state.shape)}")
+    gate = _gate_of(f, dt_bias, (n, H, dk))
     o = out if out is not None else torch.empty(n, H, dv, dtype=q.dtype, device=q.device)
-    _lib.kda_decode(n, H, dk, dv, q.dtype, scale, q, k, v, f, b, A_log, dt_bias, state, o)
+    _lib.kda_decode(n, H, dk, dv, q.dtype, scale, q, k, v, f, b, A_log, dt_bias, state, o, gate)
     return o

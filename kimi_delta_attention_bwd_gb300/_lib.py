@@ -31,7 +31,9 @@ class kda_problem(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("H", ctypes.c_int32),
                 ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("scale", ctypes.c_float), ("n_docs", ctypes.c_int32),
-                ("cu_seqlens", ctypes.c_void_p), ("cu_seqlens_host", ctypes.c_void_p)]
+                ("cu_seqlens", ctypes.c_void_p), ("cu_seqlens_host", ctypes.c_void_p), ("gate", ctypes.c_int32)]
+
+KDA_GATE_CHANNEL, KDA_GATE_SCALAR = 0, 1
 
 
 _lib = None
@@ -72,7 +74,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.kda_prof_stop.restype = I
         lib.kda_prof_kernel_name.argtypes = [I]
         lib.kda_prof_kernel_name.restype = ctypes.c_char_p
-        lib.kda_decode.argtypes = [I, I, I, I, I, ctypes.c_float] + [P] * 9 + [P]
+        lib.kda_decode.argtypes = [I, I, I, I, I, I, ctypes.c_float] + [P] * 9 + [P]
         lib.kda_decode.restype = I
         _lib = lib
         return lib
@@ -97,10 +99,12 @@ def _stream():
     return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
-def make_problem(B, T, H, dk, dv, dtype, scale=None, cu_seqlens=None, cu_seqlens_host=None):
+def make_problem(B, T, H, dk, dv, dtype, scale=None, cu_seqlens=None, cu_seqlens_host=None, gate=KDA_GATE_CHANNEL):
     """Builds the kda_problem struct.  cu_seqlens: device int32 tensor or None;
-    cu_seqlens_host: host int32 tensor/array kept alive by the caller, or None."""
+    cu_seqlens_host: host int32 tensor/array kept alive by the caller, or None;
+    gate: KDA_GATE_CHANNEL (KDA) or KDA_GATE_SCALAR (scalar-gated GDN)."""
     p = kda_problem()
+    p.gate = int(gate)
     p.B, p.T, p.H, p.dk, p.dv = int(B), int(T), int(H), int(dk), int(dv)
     p.dtype = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32 if dtype == torch.float32 else 99
     p.scale = float(scale) if scale is not None else 0.0
@@ -142,10 +146,10 @@ def kda_bwd(problem, q, k, v, f, b, A_log, dt_bias, h0, dO, dh_final, dq, dk, dv
         raise KdaError(st, "kda_bwd")
 
 
-def kda_decode(n_seq, H, dk, dv, dtype, scale, q, k, v, f, b, A_log, dt_bias, state, o):
+def kda_decode(n_seq, H, dk, dv, dtype, scale, q, k, v, f, b, A_log, dt_bias, state, o, gate=KDA_GATE_CHANNEL):
     """Raw single-token step; state [n_seq, H, dk, dv] fp32 is updated in place."""
     dt = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32 if dtype == torch.float32 else 99
-    st = load().kda_decode(int(n_seq), int(H), int(dk), int(dv), dt, float(scale or 0.0), _p(q), _p(k), _p(v),
+    st = load().kda_decode(int(n_seq), int(H), int(dk), int(dv), dt, int(gate), float(scale or 0.0), _p(q), _p(k), _p(v),
                            _p(f), _p(b), _p(A_log), _p(dt_bias), _p(state), _p(o), _stream())
     if st != 0:
         raise KdaError(st, "kda_decode")

@@ -259,6 +259,7 @@ static kda_status check_problem(const kda_problem* p, Dims* d) {
   if (!p) return KDA_ERR_INVALID_ARG;
   if (p->B <= 0 || p->T <= 0 || p->H <= 0 || p->dk <= 0 || p->dv <= 0) return KDA_ERR_INVALID_ARG;
   if (p->dtype != KDA_BF16 && p->dtype != KDA_F32) return KDA_ERR_INVALID_ARG;
+  if (p->gate != KDA_GATE_CHANNEL && p->gate != KDA_GATE_SCALAR) return KDA_ERR_INVALID_ARG;
   if (!supported(p->dk, p->dv)) return KDA_ERR_UNSUPPORTED;
   const int64_t ntok = (int64_t)p->B * p->T;
   if (ntok > (int64_t)1 << 30 || p->H > 4096) return KDA_ERR_INVALID_ARG;
@@ -291,12 +292,13 @@ static kda_status check_problem(const kda_problem* p, Dims* d) {
   if (ncm > (int64_t)1 << 30) return KDA_ERR_INVALID_ARG;
   d->nc_max = (int)ncm;
   uint32_t hsh = 2166136261u;  // FNV-1a over the sizes that fix the layout
-  const int32_t vals[8] = {p->B, p->T, p->H, p->dk, p->dv, p->dtype, n_docs, 0x4b4441};
-  for (int i = 0; i < 8; i++) { hsh ^= (uint32_t)vals[i]; hsh *= 16777619u; }
+  const int32_t vals[9] = {p->B, p->T, p->H, p->dk, p->dv, p->dtype, n_docs, p->gate, 0x4b4441};
+  for (int i = 0; i < 9; i++) { hsh ^= (uint32_t)vals[i]; hsh *= 16777619u; }
   d->tag = (int32_t)(hsh | 1u);
   d->save = 0;
   d->fast = fast_path(p->dtype, p->dk, p->dv) ? 1 : 0;
   d->ahead = 0;
+  d->gate = p->gate;
   return KDA_OK;
 }
 

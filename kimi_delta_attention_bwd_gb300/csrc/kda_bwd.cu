@@ -170,7 +170,8 @@ __global__ void __launch_bounds__(256) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
       int64_t off = ((int64_t)(t0 + r) * H + h) * DK + i;
       qv = ldf(q + off);
       kv = ldf(k + off);
-      gv = -a * softplus_f(ldf(f + off) + io.dt_bias[h * DK + i]);
+      gv = d.gate ? -a * softplus_f(ldf(f + ((int64_t)(t0 + r) * H + h)) + io.dt_bias[h])
+                  : -a * softplus_f(ldf(f + off) + io.dt_bias[h * DK + i]);
     }
     qh[idx] = qv; kh[idx] = kv; G[idx] = gv;
   }
@@ -341,10 +342,11 @@ __global__ void __launch_bounds__(256) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
     for (int r = L - 1; r >= 0; r--) {
       acc += dG[r * DK + i];
       int64_t off = ((int64_t)(t0 + r) * H + h) * DK + i;
-      float x = ldf(f + off) + io.dt_bias[h * DK + i];
+      float x = d.gate ? ldf(f + ((int64_t)(t0 + r) * H + h)) + io.dt_bias[h] : ldf(f + off) + io.dt_bias[h * DK + i];
       float g = -a * softplus_f(x);
       float dx = acc * (-a) * sigmoid_f(x);
-      stf(dfo + off, dx);
+      if (d.gate) dG[r * DK + i] = dx;  // summed over the channels below
+      else stf(dfo + off, dx);
       pdt += dx;
       pA_local += acc * g;
     }
@@ -352,6 +354,15 @@ __global__ void __launch_bounds__(256) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   }
   float tot = block_sum(pA_local, red);
   if (tid == 0) w.pA[ch] = tot;
+  if (d.gate) {  // scalar gate: df of a token is the sum over its channels (fixed order)
+    __syncthreads();
+    for (int r = warp; r < L; r += nw) {
+      float sdx = 0.f;
+      for (int i = lane; i < DK; i += 32) sdx += dG[r * DK + i];
+      sdx = warp_sum(sdx);
+      if (lane == 0) stf(dfo + (int64_t)(t0 + r) * H + h, sdx);
+    }
+  }
 
   // ---- L2-norm backward and db
   TI* dqo = (TI*)io.dq;
@@ -370,38 +381,56 @@ __global__ void __launch_bounds__(256) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   }
 }
 
-// dA_log[h] and ddt_bias[h, :] summed over chunks in a fixed order.
-__global__ void __launch_bounds__(256) bwd_reduce_kernel(Dims d, BwdIO io, Ws w) {
-  const int h = blockIdx.x, tid = threadIdx.x, H = d.H, dk = d.dk;
-  const int nc = *w.n_chunks;
-  __shared__ float red[256];
+// dA_log[h] and ddt_bias[h, :] summed over chunks in a fixed order: 32
+// groups of 32 threads, group g owning chunks g, g + 32, ... of a block of 32
+// channels with four independent partial sums, then the groups in order.
+// The scalar gate sums ddt_bias over the channels too.
+constexpr int RTH = 1024, RG = RTH / 32;
+__global__ void __launch_bounds__(RTH) bwd_reduce_kernel(Dims d, BwdIO io, Ws w) {
+  const int h = blockIdx.x, tid = threadIdx.x, grp = tid >> 5, lane = tid & 31, H = d.H, dk = d.dk;
+  __shared__ float red[RTH];
   if (!saved_ok(d, w.tag, w.err)) return;
-  float acc = 0.f;
-  for (int c = tid; c < nc; c += blockDim.x) acc += w.pA[(int64_t)c * H + h];
-  red[tid] = acc;
-  __syncthreads();
-  for (int s = 128; s > 0; s >>= 1) {
-    if (tid < s) red[tid] += red[tid + s];
+  const int nc = *w.n_chunks;
+  {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int c = tid;
+    for (; c + 3 * RTH < nc; c += 4 * RTH)
+#pragma unroll
+      for (int u = 0; u < 4; u++) acc[u] += w.pA[(int64_t)(c + u * RTH) * H + h];
+    for (; c < nc; c += RTH) acc[0] += w.pA[(int64_t)c * H + h];
+    red[tid] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     __syncthreads();
+    for (int s2 = RTH / 2; s2 > 0; s2 >>= 1) {
+      if (tid < s2) red[tid] += red[tid + s2];
+      __syncthreads();
+    }
+    if (tid == 0) io.dA_log[h] = red[0];
   }
-  if (tid == 0) io.dA_log[h] = red[0];
-  // ddt_bias: the 256 threads split into groups that each own every
-  // G-th chunk of a block of channels; partials are combined in a fixed order.
-  const int ng = blockDim.x / 32 < 8 ? blockDim.x / 32 : 8;
+  float gsum = 0.f;
   for (int i0 = 0; i0 < dk; i0 += 32) {
     __syncthreads();
-    const int grp = tid >> 5, i = i0 + (tid & 31);
-    float s = 0.f;
-    if (grp < ng && i < dk)
-      for (int c = grp; c < nc; c += ng) s += w.pdt[((int64_t)c * H + h) * dk + i];
-    red[tid] = s;
+    const int i = i0 + lane;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (i < dk) {
+      int c = grp;
+      for (; c + 3 * RG < nc; c += 4 * RG)
+#pragma unroll
+        for (int u = 0; u < 4; u++) acc[u] += w.pdt[((int64_t)(c + u * RG) * H + h) * dk + i];
+      for (; c < nc; c += RG) acc[0] += w.pdt[((int64_t)c * H + h) * dk + i];
+    }
+    red[tid] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     __syncthreads();
-    if (tid < 32 && i0 + tid < dk) {
+    if (grp == 0) {
       float t = 0.f;
-      for (int g = 0; g < ng; g++) t += red[g * 32 + tid];
-      io.ddt_bias[h * dk + i0 + tid] = t;
+      for (int g = 0; g < RG; g++) t += red[g * 32 + lane];
+      if (!d.gate && i < dk) io.ddt_bias[h * dk + i] = t;
+      if (d.gate) {
+        t = warp_sum(i < dk ? t : 0.f);
+        gsum += t;
+      }
     }
   }
+  if (d.gate && tid == 0) io.ddt_bias[h] = gsum;
 }
 
 template <typename TI, int DK, int DV>
@@ -452,7 +481,7 @@ cudaError_t launch_bwd_intra(int dtype, const Dims& d, const BwdIO& io, const Ws
 }
 cudaError_t launch_bwd_reduce(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st) {
   prof_begin(K_BWD_REDUCE, st);
-  bwd_reduce_kernel<<<d.H, 256, 0, st>>>(d, io, w);
+  bwd_reduce_kernel<<<d.H, RTH, 0, st>>>(d, io, w);
   prof_end(K_BWD_REDUCE, st);
   return cudaGetLastError();
 }

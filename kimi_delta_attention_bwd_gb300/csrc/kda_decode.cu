@@ -18,7 +18,7 @@ constexpr int DTH = 256;
 // One CTA per (sequence, head).  Thread t: value column t % DV, key rows of
 // group t / DV (DK / (DTH / DV) consecutive rows).
 template <int DK, int DV, typename T>
-__global__ void __launch_bounds__(DTH) decode_kernel(int H, float scale, const T* __restrict__ q,
+__global__ void __launch_bounds__(DTH) decode_kernel(int H, int gate, float scale, const T* __restrict__ q,
                                                      const T* __restrict__ k, const T* __restrict__ v,
                                                      const T* __restrict__ f, const T* __restrict__ b,
                                                      const float* __restrict__ A_log,
@@ -48,7 +48,8 @@ __global__ void __launch_bounds__(DTH) decode_kernel(int H, float scale, const T
       const int i = lane + 32 * e;
       qh[i] = qv[e] * iq;
       kh[i] = kv[e] * ik;
-      dec[i] = expf(-a * softplus_f(ldf(f + (size_t)sh * DK + i) + dt_bias[h * DK + i]));
+      dec[i] = gate ? expf(-a * softplus_f(ldf(f + sh) + dt_bias[h]))
+                    : expf(-a * softplus_f(ldf(f + (size_t)sh * DK + i) + dt_bias[h * DK + i]));
     }
   } else if (warp == 1) {
     for (int j = lane; j < DV; j += 32) vv[j] = ldf(v + (size_t)sh * DV + j);
@@ -89,16 +90,16 @@ __global__ void __launch_bounds__(DTH) decode_kernel(int H, float scale, const T
 }
 
 template <int DK, int DV>
-cudaError_t launch_decode(int dtype, int n, int H, float scale, const void* q, const void* k, const void* v,
+cudaError_t launch_decode(int dtype, int gate, int n, int H, float scale, const void* q, const void* k, const void* v,
                           const void* f, const void* b, const float* A_log, const float* dt_bias, float* state,
                           void* o, cudaStream_t st) {
   prof_begin(K_DECODE, st);
   if (dtype == KDA_BF16) {
     typedef __nv_bfloat16 T;
-    decode_kernel<DK, DV, T><<<n * H, DTH, 0, st>>>(H, scale, (const T*)q, (const T*)k, (const T*)v, (const T*)f,
+    decode_kernel<DK, DV, T><<<n * H, DTH, 0, st>>>(H, gate, scale, (const T*)q, (const T*)k, (const T*)v, (const T*)f,
                                                     (const T*)b, A_log, dt_bias, state, (T*)o);
   } else {
-    decode_kernel<DK, DV, float><<<n * H, DTH, 0, st>>>(H, scale, (const float*)q, (const float*)k, (const float*)v,
+    decode_kernel<DK, DV, float><<<n * H, DTH, 0, st>>>(H, gate, scale, (const float*)q, (const float*)k, (const float*)v,
                                                         (const float*)f, (const float*)b, A_log, dt_bias, state,
                                                         (float*)o);
   }
@@ -109,23 +110,25 @@ cudaError_t launch_decode(int dtype, int n, int H, float scale, const void* q, c
 }  // namespace
 }  // namespace kda
 
-extern "C" KDA_API kda_status kda_decode(int n_seq, int H, int dk, int dv, int dtype, float scale, const void* q,
+extern "C" KDA_API kda_status kda_decode(int n_seq, int H, int dk, int dv, int dtype, int gate, float scale,
+                                         const void* q,
                                          const void* k, const void* v, const void* f, const void* b,
                                          const float* A_log, const float* dt_bias, float* state, void* o,
                                          cudaStream_t stream) {
   using namespace kda;
   if (n_seq <= 0 || H <= 0 || H > 4096 || (int64_t)n_seq * H > ((int64_t)1 << 30)) return KDA_ERR_INVALID_ARG;
   if (dtype != KDA_BF16 && dtype != KDA_F32) return KDA_ERR_INVALID_ARG;
+  if (gate != KDA_GATE_CHANNEL && gate != KDA_GATE_SCALAR) return KDA_ERR_INVALID_ARG;
   if (!q || !k || !v || !f || !b || !A_log || !dt_bias || !state || !o) return KDA_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, f, b, A_log, dt_bias, state, o};
   for (const void* x : ptrs)
     if ((uintptr_t)x % 16 != 0) return KDA_ERR_ALIGNMENT;
   const float sc = scale > 0.f ? scale : 1.0f / sqrtf((float)dk);
   cudaError_t e;
-  if (dk == 32 && dv == 64) e = launch_decode<32, 64>(dtype, n_seq, H, sc, q, k, v, f, b, A_log, dt_bias, state, o, stream);
-  else if (dk == 64 && dv == 64) e = launch_decode<64, 64>(dtype, n_seq, H, sc, q, k, v, f, b, A_log, dt_bias, state, o, stream);
-  else if (dk == 64 && dv == 128) e = launch_decode<64, 128>(dtype, n_seq, H, sc, q, k, v, f, b, A_log, dt_bias, state, o, stream);
-  else if (dk == 128 && dv == 128) e = launch_decode<128, 128>(dtype, n_seq, H, sc, q, k, v, f, b, A_log, dt_bias, state, o, stream);
+  if (dk == 32 && dv == 64) e = launch_decode<32, 64>(dtype, gate, n_seq, H, sc, q, k, v, f, b, A_log, dt_bias, state, o, stream);
+  else if (dk == 64 && dv == 64) e = launch_decode<64, 64>(dtype, gate, n_seq, H, sc, q, k, v, f, b, A_log, dt_bias, state, o, stream);
+  else if (dk == 64 && dv == 128) e = launch_decode<64, 128>(dtype, gate, n_seq, H, sc, q, k, v, f, b, A_log, dt_bias, state, o, stream);
+  else if (dk == 128 && dv == 128) e = launch_decode<128, 128>(dtype, gate, n_seq, H, sc, q, k, v, f, b, A_log, dt_bias, state, o, stream);
   else return KDA_ERR_UNSUPPORTED;
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

@@ -68,7 +68,7 @@ struct Intra {
 // Stage layout of one chunk's raw inputs: q, k, f [C][DK], v [C][DV] (bf16).
 constexpr int STAGE_ELEMS = 3 * C * DK + C * DV;
 
-__device__ __forceinline__ void stage_chunk(bf16* st, const FwdIO& io, int H, int h, int t0, int L) {
+__device__ __forceinline__ void stage_chunk(bf16* st, const FwdIO& io, int H, int h, int t0, int L, bool gdn) {
   const bf16* q = (const bf16*)io.q;
   const bf16* k = (const bf16*)io.k;
   const bf16* f = (const bf16*)io.f;
@@ -79,7 +79,7 @@ __device__ __forceinline__ void stage_chunk(bf16* st, const FwdIO& io, int H, in
       size_t g = ((size_t)(t0 + r) * H + h) * DK + p * 8;
       cp16(st + r * DK + p * 8, q + g);
       cp16(st + C * DK + r * DK + p * 8, k + g);
-      cp16(st + 2 * C * DK + r * DK + p * 8, f + g);
+      if (!gdn) cp16(st + 2 * C * DK + r * DK + p * 8, f + g);
     }
   }
   for (int idx = threadIdx.x; idx < C * 8; idx += NTH) {  // 8 x 16 B per dv row
@@ -103,16 +103,25 @@ __device__ __forceinline__ void unpack8(const uint4& u, float* x) {
 // from the staged chunk.  Thread t owns row t / 4 and
 // key channels 8 (t % 4) .. + 7 (value columns 16 (t % 4) .. + 15).  Rows
 // >= L are zero (G continues flat).  vraw returns the thread's raw v.
-__device__ void prologue(const Intra& c, const bf16* st, int L, float a, const float* dtb, uint4 (&vraw)[2]) {
+// fg (scalar gate): f of this head, one value per token at stride H from token
+// t0; dtb then points at the head's single dt_bias.
+__device__ void prologue(const Intra& c, const bf16* st, int L, float a, const float* dtb, uint4 (&vraw)[2],
+                         const bf16* fg, int t0, int H) {
   const int tid = threadIdx.x, r = tid >> 2, q4 = tid & 3, lane = tid & 31, warp = tid >> 5;
   float qv[8], kv[8], gv[8];
   const bool in = r < L;
   if (in) {
     unpack8(*reinterpret_cast<const uint4*>(st + r * DK + 8 * q4), qv);
     unpack8(*reinterpret_cast<const uint4*>(st + C * DK + r * DK + 8 * q4), kv);
-    unpack8(*reinterpret_cast<const uint4*>(st + 2 * C * DK + r * DK + 8 * q4), gv);
+    if (fg) {
+      const float g = -a * softplus_f(bfl(fg[(size_t)(t0 + r) * H]) + dtb[0]);
 #pragma unroll
-    for (int e = 0; e < 8; e++) gv[e] = -a * softplus_f(gv[e] + dtb[8 * q4 + e]);
+      for (int e = 0; e < 8; e++) gv[e] = g;
+    } else {
+      unpack8(*reinterpret_cast<const uint4*>(st + 2 * C * DK + r * DK + 8 * q4), gv);
+#pragma unroll
+      for (int e = 0; e < 8; e++) gv[e] = -a * softplus_f(gv[e] + dtb[8 * q4 + e]);
+    }
     vraw[0] = *reinterpret_cast<const uint4*>(st + 3 * C * DK + r * DV + 16 * q4);
     vraw[1] = *reinterpret_cast<const uint4*>(st + 3 * C * DK + r * DV + 16 * q4 + 8);
   } else {
@@ -361,7 +370,9 @@ __global__ void __launch_bounds__(NTH, 1) fwd_chain_kernel(Dims d, FwdIO io, Ws 
   const int H = d.H;
   const int cb = w.doc_chunk0[doc], ce = w.doc_chunk0[doc + 1];
   const float a = expf(io.A_log[h]);
-  const float* dtb = io.dt_bias + h * DK;
+  const bool gdn = d.gate != 0;
+  const float* dtb = io.dt_bias + h * (gdn ? 1 : DK);
+  const bf16* fg = gdn ? (const bf16*)io.f + h : nullptr;
   const bf16* braw = (const bf16*)io.b;
   Intra c{sm.qh, sm.kh, sm.gg, sm.qh, sm.kh, sm.rr, sm.bet, sm.inq, sm.ink,
           sm.braw, sm.gl, sm.gam, sm.gb, sm.ge, sm.dd, sm.ei, sm.tot, sm.spanok};
@@ -385,7 +396,7 @@ __global__ void __launch_bounds__(NTH, 1) fwd_chain_kernel(Dims d, FwdIO io, Ws 
   float bnext = 0.f;
   if (cb < ce) {
     const int L0 = w.chunk_len[cb], t00 = w.chunk_tok0[cb];
-    stage_chunk(sm.stage, io, H, h, t00, L0);
+    stage_chunk(sm.stage, io, H, h, t00, L0, gdn);
     if (tid < L0) bnext = bfl(braw[(size_t)(t00 + tid) * H + h]);
   }
   for (int ci = cb; ci < ce; ci++) {
@@ -394,7 +405,7 @@ __global__ void __launch_bounds__(NTH, 1) fwd_chain_kernel(Dims d, FwdIO io, Ws 
     if (tid < C) sm.braw[tid] = bnext;
     __syncthreads();
     uint4 vraw[2];
-    prologue(c, sm.stage, L, a, dtb, vraw);
+    prologue(c, sm.stage, L, a, dtb, vraw, fg, t0, H);
     {  // beta v -> XV (thread: row tid / 4, columns 16 (tid % 4) ..)
       const int r = tid >> 2, q4 = tid & 3;
       const float br = r < L ? sm.bet[r] : 0.f;
@@ -406,7 +417,7 @@ __global__ void __launch_bounds__(NTH, 1) fwd_chain_kernel(Dims d, FwdIO io, Ws 
     }
     if (ci + 1 < ce) {  // stage the next chunk while this one computes
       const int L1 = w.chunk_len[ci + 1], t01 = w.chunk_tok0[ci + 1];
-      stage_chunk(sm.stage, io, H, h, t01, L1);
+      stage_chunk(sm.stage, io, H, h, t01, L1, gdn);
       bnext = tid < L1 ? bfl(braw[(size_t)(t01 + tid) * H + h]) : 0.f;
     }
     factors_fwd(c, L, d.scale, QG, KD, XK);
@@ -596,7 +607,8 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
   const int t0 = w.chunk_tok0[j], H = d.H;
   const int64_t ch = (int64_t)j * H + h;
   const float a = expf(io.A_log[h]), scale = d.scale;
-  const float* dtb = io.dt_bias + h * DK;
+  const bool gdn = d.gate != 0;
+  const float* dtb = io.dt_bias + h * (gdn ? 1 : DK);
   const bf16* qraw = (const bf16*)io.q;
   const bf16* kraw = (const bf16*)io.k;
   {
@@ -605,7 +617,7 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
       const int L2 = w.chunk_len[j2], t2 = w.chunk_tok0[j2];
       prefetch_rows(io.q, DK, t2, L2, H, h2);
       prefetch_rows(io.k, DK, t2, L2, H, h2);
-      prefetch_rows(io.f, DK, t2, L2, H, h2);
+      prefetch_rows(io.f, gdn ? 1 : DK, t2, L2, H, h2);
       prefetch_rows(io.v, DV, t2, L2, H, h2);
       prefetch_rows(io.b, 1, t2, L2, H, h2);
     }
@@ -630,13 +642,19 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     const size_t row = (size_t)(t0 + r) * H + h;
     unpack8(__ldg(reinterpret_cast<const uint4*>(qraw + row * DK + 8 * q4)), qv);
     unpack8(__ldg(reinterpret_cast<const uint4*>(kraw + row * DK + 8 * q4)), kv);
-    unpack8(__ldg(reinterpret_cast<const uint4*>((const bf16*)io.f + row * DK + 8 * q4)), gv);
+    if (!gdn) unpack8(__ldg(reinterpret_cast<const uint4*>((const bf16*)io.f + row * DK + 8 * q4)), gv);
     const uint4* vp = reinterpret_cast<const uint4*>((const bf16*)io.v + row * DV + 16 * q4);
     unpack8(__ldg(vp), vv);
     unpack8(__ldg(vp + 1), vv + 8);
     braw = bfl(((const bf16*)io.b)[row]);
+    if (gdn) {
+      const float g = -a * LOG2E * softplus_f(bfl(((const bf16*)io.f)[row]) + dtb[0]);
 #pragma unroll
-    for (int e = 0; e < 8; e++) gv[e] = -a * LOG2E * softplus_f(gv[e] + dtb[8 * q4 + e]);
+      for (int e = 0; e < 8; e++) gv[e] = g;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; e++) gv[e] = -a * LOG2E * softplus_f(gv[e] + dtb[8 * q4 + e]);
+    }
   } else {
 #pragma unroll
     for (int e = 0; e < 8; e++) qv[e] = kv[e] = gv[e] = 0.f;
@@ -1161,7 +1179,8 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   const int t0 = w.chunk_tok0[j], H = d.H;
   const int64_t ch = (int64_t)j * H + h;
   const float a = expf(io.A_log[h]), scale = d.scale;
-  const float* dtb = io.dt_bias + h * DK;
+  const bool gdn = d.gate != 0;
+  const float* dtb = io.dt_bias + h * (gdn ? 1 : DK);
   bf16* wk = sm.wk;
   // work-area regions (bf16 offsets): dO 0 | S 4096 | dS' 8192 | P -> E 12288 |
   // W -> dW -> YW 20480 | U -> dE -> YU 24576 | raw f -> KD 32768 | T 36864;
@@ -1181,7 +1200,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
     if (r < L) {
       const size_t g = ((size_t)(t0 + r) * H + h) * DK + 8 * p;
       cp16(sm.rk + r * DK + 8 * p, (const bf16*)io.k + g);
-      cp16(fst + r * DK + 8 * p, (const bf16*)io.f + g);
+      if (!gdn) cp16(fst + r * DK + 8 * p, (const bf16*)io.f + g);
     }
   }
   cp_commit();
@@ -1212,7 +1231,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
       const int L2 = w.chunk_len[j2], t2 = w.chunk_tok0[j2];
       const int64_t c2 = (int64_t)j2 * H + h2;
       prefetch_rows(io.k, DK, t2, L2, H, h2);
-      prefetch_rows(io.f, DK, t2, L2, H, h2);
+      prefetch_rows(io.f, gdn ? 1 : DK, t2, L2, H, h2);
       prefetch_rows(io.v, DV, t2, L2, H, h2);
       prefetch_rows(io.dO, DV, t2, L2, H, h2);
       prefetch_rows(io.b, 1, t2, L2, H, h2);
@@ -1249,9 +1268,15 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   float kv[8], gv[8];
   if (in) {
     unpack8(*reinterpret_cast<const uint4*>(sm.rk + r * DK + 8 * q4), kv);
-    unpack8(*reinterpret_cast<const uint4*>(fst + r * DK + 8 * q4), gv);
+    if (gdn) {
+      const float g = -a * LOG2E * softplus_f(bfl(((const bf16*)io.f)[(size_t)(t0 + r) * H + h]) + dtb[0]);
 #pragma unroll
-    for (int e = 0; e < 8; e++) gv[e] = -a * LOG2E * softplus_f(gv[e] + dtb[8 * q4 + e]);
+      for (int e = 0; e < 8; e++) gv[e] = g;
+    } else {
+      unpack8(*reinterpret_cast<const uint4*>(fst + r * DK + 8 * q4), gv);
+#pragma unroll
+      for (int e = 0; e < 8; e++) gv[e] = -a * LOG2E * softplus_f(gv[e] + dtb[8 * q4 + e]);
+    }
   } else {
 #pragma unroll
     for (int e = 0; e < 8; e++) kv[e] = gv[e] = 0.f;
@@ -1565,7 +1590,9 @@ __global__ void __launch_bounds__(NTH, 2) bwd_gate_kernel(Dims d, BwdIO io, Ws w
   const int t0 = w.chunk_tok0[j], H = d.H;
   const int64_t ch = (int64_t)j * H + h;
   const float a = expf(io.A_log[h]);
-  const float* dtb = io.dt_bias + h * DK;
+  const bool gdn = d.gate != 0;
+  const float* dtb = io.dt_bias + h * (gdn ? 1 : DK);
+  const bf16* fsc = (const bf16*)io.f + h;  // scalar gate: f of this head, stride H
 
   {
     int j2, h2;
@@ -1574,7 +1601,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_gate_kernel(Dims d, BwdIO io, Ws w
       const int64_t c2 = (int64_t)j2 * H + h2;
       prefetch_rows(io.q, DK, t2, L2, H, h2);
       prefetch_rows(io.k, DK, t2, L2, H, h2);
-      prefetch_rows(io.f, DK, t2, L2, H, h2);
+      prefetch_rows(io.f, gdn ? 1 : DK, t2, L2, H, h2);
       if (tid == 0) {
         bulk_prefetch_l2(w.gDP + c2 * NBLK * 16 * PB, NBLK * 16 * PB * 4);
         bulk_prefetch_l2(w.gMA + c2 * NBLK * 16 * PB, NBLK * 16 * PB * 4);
@@ -1591,7 +1618,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_gate_kernel(Dims d, BwdIO io, Ws w
       const size_t g = ((size_t)(t0 + r) * H + h) * DK + 8 * p;
       cp16(sm.rq + o, (const bf16*)io.q + g);
       cp16(sm.rk + o, (const bf16*)io.k + g);
-      cp16(sm.rf + o, (const bf16*)io.f + g);
+      if (!gdn) cp16(sm.rf + o, (const bf16*)io.f + g);
     } else {
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
       *reinterpret_cast<uint4*>(sm.rq + o) = z;
@@ -1621,9 +1648,10 @@ __global__ void __launch_bounds__(NTH, 2) bwd_gate_kernel(Dims d, BwdIO io, Ws w
     unpack8(*reinterpret_cast<const uint4*>(sm.rf + r * DK + 8 * q4), gv);
     const bool in = r < L;
     float sq = 0.f, sk = 0.f;
+    const float gs = in && gdn ? -a * LOG2E * softplus_f(bfl(fsc[(size_t)(t0 + r) * H]) + dtb[0]) : 0.f;
 #pragma unroll
     for (int e = 0; e < 8; e++) {
-      gv[e] = in ? -a * LOG2E * softplus_f(gv[e] + dtb[8 * q4 + e]) : 0.f;
+      gv[e] = !in ? 0.f : gdn ? gs : -a * LOG2E * softplus_f(gv[e] + dtb[8 * q4 + e]);
       sq += qv[e] * qv[e];
       sk += kv[e] * kv[e];
     }
@@ -1797,12 +1825,17 @@ __global__ void __launch_bounds__(NTH, 2) bwd_gate_kernel(Dims d, BwdIO io, Ws w
     float pdt = 0.f, pA = 0.f;
     for (int m = 0; m < 8; m++) {
       const int rr = 8 * warp + m;
-      if (rr < L) {
+      if (rr < L) {  // uniform over the warp
         const float dg = dgs[rr * SQ + lane] + off;
-        const float x = bfl(sm.rf[rr * DK + lane]) + dtb[lane];
+        const float x = gdn ? bfl(fsc[(size_t)(t0 + rr) * H]) + dtb[0] : bfl(sm.rf[rr * DK + lane]) + dtb[lane];
         const float g = -a * softplus_f(x);
         const float dx = dg * (-a) * sigmoid_f(x);
-        dfo[((size_t)(t0 + rr) * H + h) * DK + lane] = __float2bfloat16_rn(dx);
+        if (gdn) {  // the scalar gate feeds every channel: its gradient is the channel sum
+          const float ds = warp_sum(dx);
+          if (lane == 0) dfo[(size_t)(t0 + rr) * H + h] = __float2bfloat16_rn(ds);
+        } else {
+          dfo[((size_t)(t0 + rr) * H + h) * DK + lane] = __float2bfloat16_rn(dx);
+        }
         pdt += dx;
         pA += dg * g;
       }

@@ -49,7 +49,8 @@ __global__ void __launch_bounds__(256) fwd_intra_kernel(Dims d, FwdIO io, Ws w) 
       int64_t off = ((int64_t)(t0 + r) * H + h) * DK + i;
       qv = ldf(q + off);
       kv = ldf(k + off);
-      gv = -a * softplus_f(ldf(f + off) + io.dt_bias[h * DK + i]);
+      gv = d.gate ? -a * softplus_f(ldf(f + ((int64_t)(t0 + r) * H + h)) + io.dt_bias[h])
+                  : -a * softplus_f(ldf(f + off) + io.dt_bias[h * DK + i]);
     }
     qh[idx] = qv; kh[idx] = kv; G[idx] = gv;
   }

@@ -76,6 +76,7 @@ struct Dims {
   int32_t save;  // forward saves for the backward
   int32_t fast;  // bf16 io with dk = 32, dv = 64: tensor-core kernels
   int32_t ahead; // CTAs in flight (one wave) of the per-chunk tensor-core kernels: their L2 prefetch distance
+  int32_t gate;  // 0: per key channel (KDA); 1: scalar per head (GDN), f [Ntok, H], dt_bias [H]
 };
 
 // Backward kernels refuse a workspace that no saving forward of the same

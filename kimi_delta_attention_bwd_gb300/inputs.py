@@ -44,6 +44,7 @@ class KdaWorkload:
     varlen: Optional[str]  # None, "docs600" or "rows8192_docs2048"
     h0: bool
     dh_final: bool
+    gate: str = "channel"  # "channel": f [B,T,H,dk], dt_bias [H,dk] (KDA); "scalar": f [B,T,H], dt_bias [H] (GDN)
 
     @property
     def tokens(self) -> int:
@@ -64,9 +65,9 @@ WORKLOADS = [
 ]
 
 
-def custom(B, T, H, dk, dv, dtype="bf16", h0=False, dh_final=False, name="custom") -> KdaWorkload:
+def custom(B, T, H, dk, dv, dtype="bf16", h0=False, dh_final=False, name="custom", gate="channel") -> KdaWorkload:
     """An ad-hoc workload (edge cases and small parity cases)."""
-    return KdaWorkload(99, name, B, T, H, dk, dv, dtype, True, None, h0, dh_final)
+    return KdaWorkload(99, name, B, T, H, dk, dv, dtype, True, None, h0, dh_final, gate)
 
 
 def doc_lengths_docs600(total: int, rng: np.random.RandomState) -> list[int]:
@@ -115,7 +116,7 @@ def make_inputs(w: KdaWorkload | int, seed: Optional[int] = None, with_grad_inpu
                 lengths=None):
     """Draw the inputs of one workload.  Returns a dict of CPU tensors:
     q, k, f [B,T,H,dk]; v [B,T,H,dv]; b [B,T,H] in the io dtype;
-    A_log [H], dt_bias [H,dk] float32; cu_seqlens int32 [n+1] or None
+    A_log [H], dt_bias [H,dk] float32 (scalar gate: f [B,T,H], dt_bias [H]); cu_seqlens int32 [n+1] or None
     (None means equal-length rows; explicit `lengths` override the workload's
     own document draw); h0 [n,H,dk,dv] float32 or None;
     dO [B,T,H,dv] (io dtype) and dh_final float32 or None when the workload
@@ -138,11 +139,13 @@ def make_inputs(w: KdaWorkload | int, seed: Optional[int] = None, with_grad_inpu
     out["q"] = randn(B, T, H, dk)
     out["k"] = randn(B, T, H, dk)
     out["v"] = randn(B, T, H, dv)
-    out["f"] = randn(B, T, H, dk)
+    scalar = w.gate == "scalar"
+    out["f"] = randn(B, T, H) if scalar else randn(B, T, H, dk)
     out["b"] = randn(B, T, H)
     u = torch.rand(H, generator=gen, dtype=torch.float64)
     out["A_log"] = torch.log(1.0 + 15.0 * u).to(torch.float32)
-    ud = torch.rand(H, dk, generator=gen, dtype=torch.float64)
+    ud = torch.rand(H, generator=gen, dtype=torch.float64) if scalar else torch.rand(H, dk, generator=gen,
+                                                                                     dtype=torch.float64)
     dtv = torch.exp(math.log(1e-3) + ud * (math.log(1e-1) - math.log(1e-3)))
     out["dt_bias"] = (dtv + torch.log(-torch.expm1(-dtv))).to(torch.float32)
     if lengths is not None:
@@ -189,7 +192,7 @@ def numpy_f64(inp) -> dict:
     for name in ("q", "k", "v", "f", "dO"):
         if name in inp and inp[name] is not None:
             t = inp[name]
-            r[name] = f64(t.reshape(B * T, H, t.shape[-1]))
+            r[name] = f64(t.reshape(B * T, H, t.shape[-1]) if t.dim() == 4 else t.reshape(B * T, H))
     r["b"] = f64(inp["b"].reshape(B * T, H))
     r["A_log"] = f64(inp["A_log"])
     r["dt_bias"] = f64(inp["dt_bias"])

@@ -89,12 +89,24 @@ def run_gpu(inp, backward: bool, device="cuda"):
 
 
 def run_oracle(inp, backward: bool, units=None, threads=None):
+    """The oracle on the same inputs.  A scalar gate (f [.., H], dt_bias [H])
+    is the per-channel gate with every channel equal: the oracle runs on f
+    and dt_bias repeated over dk, and the gate gradients are summed over the
+    channels (the chain rule of the broadcast)."""
     from oracle import oracle
     x = numpy_f64(inp)
+    scalar = x["f"].ndim == x["q"].ndim - 1
+    if scalar:
+        dk = x["q"].shape[-1]
+        x["f"] = np.repeat(x["f"][..., None], dk, axis=-1)
+        x["dt_bias"] = np.repeat(x["dt_bias"][:, None], dk, axis=1)
     o, hf = oracle.forward(x, units=units, threads=threads)
     res = {"o": o, "h_final": hf}
     if backward:
         g = oracle.backward(x, x["dO"], x.get("dh_final"), units=units, threads=threads)
+        if scalar:
+            g["df"] = g["df"].sum(axis=-1)
+            g["ddt_bias"] = g["ddt_bias"].sum(axis=-1)
         res.update(g)
     return res
 

@@ -69,7 +69,9 @@ def test_decode_rejects_bad_arguments():
     lib = _lib.load()
     z = torch.zeros(64, device="cuda")
     p = _lib._p
-    st = lib.kda_decode(2, 2, 48, 64, 0, 0.0, *([p(z)] * 9), _lib._stream())
+    st = lib.kda_decode(2, 2, 48, 64, 0, 0, 0.0, *([p(z)] * 9), _lib._stream())
     assert st == -2  # unsupported (dk, dv)
-    st = lib.kda_decode(0, 2, 32, 64, 0, 0.0, *([p(z)] * 9), _lib._stream())
+    st = lib.kda_decode(0, 2, 32, 64, 0, 0, 0.0, *([p(z)] * 9), _lib._stream())
     assert st == -1
+    st = lib.kda_decode(2, 2, 32, 64, 0, 7, 0.0, *([p(z)] * 9), _lib._stream())
+    assert st == -1  # unknown gate mode
