@@ -293,6 +293,30 @@ def decode_bench(args, dev, flush, world, stream, hbm, rank):
                          "frac": achieved / hbm, "algorithmic_bytes_per_launch": nbytes, "launch_ms": ms}}
 
 
+def norm_gate_bench(args, dev, flush, world, stream, hbm, rank):
+    """Gated RMSNorm epilogue forward and backward over the 300M layer's KDA
+    output (16 x 2048 tokens x 8 heads rows of dv = 64, bf16)."""
+    from kimi_delta_attention_bwd_gb300 import kda_norm_gate, kda_norm_gate_backward
+    from kimi_delta_attention_bwd_gb300.inputs import norm_gate_inputs
+    w = WORKLOADS[STEP_WORKLOAD]
+    n, dv = w.B * w.T * w.H, w.dv
+    d = {k: t.to(dev) for k, t in norm_gate_inputs(n, dv, "bf16", seed=BASE_SEED + 78 + 1000 * rank).items()}
+    y = torch.empty_like(d["x"])
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+    fwd_ms = max_over_ranks(time_steps(lambda: kda_norm_gate(d["x"], d["g"], d["w"], out=y), args.steps, args.warmup,
+                                       flush, world, stream), world, dev)
+    bwd_ms = max_over_ranks(time_steps(lambda: kda_norm_gate_backward(d["x"], d["g"], d["w"], d["dy"], workspace=ws),
+                                       args.steps, args.warmup, flush, world, stream), world, dev)
+    fb, bb = n * 3 * dv * 2, n * 5 * dv * 2  # x, g in, y out; x, g, dy in, dx, dg out
+    return {"workload": f"gated RMSNorm epilogue, {n} rows x {dv}, bf16", "unit": "tokens/s",
+            "fwd": {"value": world * w.tokens / (fwd_ms / 1e3), "ms_per_step": fwd_ms,
+                    "roofline": {"bound": "hbm", "achieved": fb / (fwd_ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                                 "frac": fb / (fwd_ms / 1e3) / 1e9 / hbm, "algorithmic_bytes_per_launch": fb}},
+            "bwd": {"value": world * w.tokens / (bwd_ms / 1e3), "ms_per_step": bwd_ms,
+                    "roofline": {"bound": "hbm", "achieved": bb / (bwd_ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                                 "frac": bb / (bwd_ms / 1e3) / 1e9 / hbm, "algorithmic_bytes_per_launch": bb}}}
+
+
 def time_steps(step, steps, warmup, flush, world, stream):
     for _ in range(warmup):
         step()
@@ -331,6 +355,8 @@ def run_ours(args, rank, world, local):
     del fstep
     torch.cuda.empty_cache()
     dec = decode_bench(args, dev, flush, world, stream, hbm, rank)
+    torch.cuda.empty_cache()
+    ngate = norm_gate_bench(args, dev, flush, world, stream, hbm, rank)
     torch.cuda.empty_cache()
 
     # the training step (timed region with per-kernel event brackets and clock sampling)
@@ -389,6 +415,7 @@ def run_ours(args, rank, world, local):
             "fwd": {"value": world * wf.tokens / (fwd_ms / 1e3), "unit": "tokens/s", "ms_per_step": fwd_ms,
                     "workload": wf.name},
             "decode": dec,
+            "norm_gate": ngate,
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": traffic, "peak_kind": peak_kind,
                          "algorithmic_bytes_per_launch": ab, "launch_ms": dom_ms},

@@ -199,6 +199,25 @@ KDA_API kda_status kda_decode(int n_seq, int H, int dk, int dv, int dtype, int g
                    const float* A_log, const float* dt_bias, float* state, void* o,
                    cudaStream_t stream);
 
+/* Gated RMSNorm output epilogue, per row (token and head) over the value dim
+ * dv ("Pure KDA 300M" guide, Overview: per-head output gate and RMSNorm with
+ * eps 1e-6; openkimi README, "What is implemented": fused RMSNorm plus sigmoid
+ * gate on the KDA output):
+ *   r = 1 / sqrt(mean_j x_j^2 + eps),   y_j = x_j * r * w_j * sigmoid(g_j)
+ * x (the KDA output o), g (the output gate), y, dy, dx, dg : [n_rows, dv] in
+ * dtype (KDA_BF16 or KDA_F32); w, dw : [dv] fp32, one weight vector shared by
+ * the heads; dv is 64 or 128; eps <= 0 selects 1e-6.  Device pointers,
+ * 16-byte aligned.  The backward overwrites dx (the dO of kda_bwd), dg and dw;
+ * its scratch (per-CTA partials of dw, summed in a fixed order) is
+ * kda_norm_gate_workspace_size(n_rows, dv) bytes (0 for invalid sizes). */
+KDA_API size_t kda_norm_gate_workspace_size(int64_t n_rows, int dv);
+KDA_API kda_status kda_norm_gate_fwd(int64_t n_rows, int dv, int dtype, float eps,
+                   const void* x, const void* g, const float* w, void* y, cudaStream_t stream);
+KDA_API kda_status kda_norm_gate_bwd(int64_t n_rows, int dv, int dtype, float eps,
+                   const void* x, const void* g, const float* w, const void* dy,
+                   void* dx, void* dg, float* dw, void* workspace, size_t workspace_bytes,
+                   cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

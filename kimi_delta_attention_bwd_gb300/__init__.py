@@ -6,6 +6,8 @@ libkda_gb300.so through its C ABI, include/kda.h):
   o, h_final, ctx = kda_forward(q, k, v, f, b, A_log, dt_bias, ...)
   grads = kda_backward(ctx, dO, dh_final=None)
   o = kda_decode_step(q, k, v, f, b, A_log, dt_bias, state)   # one token, state in place
+  y = kda_norm_gate(o, gate, weight)                           # gated RMSNorm epilogue
+  do, dgate, dweight = kda_norm_gate_backward(o, gate, weight, dy)
 
 Layouts: q, k, f [B, T, H, dk]; v [B, T, H, dv]; b [B, T, H] (bf16 or fp32);
 A_log [H], dt_bias [H, dk] fp32 (scalar-gated variant: f [B, T, H], dt_bias [H]); optional cu_seqlens int32 [n_docs + 1] over
@@ -21,7 +23,8 @@ import torch
 from . import _lib
 from ._lib import KdaError, kda_device_status, kda_strerror_text  # noqa: F401
 
-__all__ = ["kda_forward", "kda_backward", "kda_decode_step", "KdaContext", "KdaError", "kda_device_status"]
+__all__ = ["kda_forward", "kda_backward", "kda_decode_step", "kda_norm_gate", "kda_norm_gate_backward", "KdaContext",
+           "KdaError", "kda_device_status"]
 
 
 @dataclass
@@ -135,3 +138,33 @@ def kda_decode_step(q, k, v, f, b, A_log, dt_bias, state, scale: Optional[float]
     o = out if out is not None else torch.empty(n, H, dv, dtype=q.dtype, device=q.device)
     _lib.kda_decode(n, H, dk, dv, q.dtype, scale, q, k, v, f, b, A_log, dt_bias, state, o, gate)
     return o
+
+
+def kda_norm_gate(x, g, w, eps: Optional[float] = None, out: Optional[torch.Tensor] = None):
+    """Gated RMSNorm epilogue over the last axis (dv = 64 or 128):
+    y = x / sqrt(mean(x^2) + eps) * w * sigmoid(g); x, g [..., dv] (bf16 or
+    fp32, e.g. the KDA output [B, T, H, dv]), w [dv] fp32."""
+    _check(x, "x")
+    _check(g, "g", x.dtype)
+    _check(w, "w", torch.float32)
+    if g.shape != x.shape or tuple(w.shape) != (x.shape[-1],):
+        raise ValueError("g must match x and w must be [dv]")
+    dv = x.shape[-1]
+    y = out if out is not None else torch.empty_like(x)
+    _lib.kda_norm_gate_fwd(x.numel() // dv, dv, x.dtype, eps, x, g, w, y)
+    return y
+
+
+def kda_norm_gate_backward(x, g, w, dy, eps: Optional[float] = None, workspace: Optional[torch.Tensor] = None):
+    """Backward of kda_norm_gate: returns (dx, dg, dw)."""
+    _check(dy, "dy", x.dtype)
+    if dy.shape != x.shape:
+        raise ValueError("dy must match x")
+    dv = x.shape[-1]
+    n = x.numel() // dv
+    if workspace is None:
+        workspace = torch.empty(_lib.kda_norm_gate_workspace_size(n, dv), dtype=torch.uint8, device=x.device)
+    dx, dg = torch.empty_like(x), torch.empty_like(g)
+    dw = torch.empty_like(w)
+    _lib.kda_norm_gate_bwd(n, dv, x.dtype, eps, x, g, w, dy, dx, dg, dw, workspace)
+    return dx, dg, dw

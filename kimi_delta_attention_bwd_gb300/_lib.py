@@ -76,6 +76,13 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.kda_prof_kernel_name.restype = ctypes.c_char_p
         lib.kda_decode.argtypes = [I, I, I, I, I, I, ctypes.c_float] + [P] * 9 + [P]
         lib.kda_decode.restype = I
+        I64 = ctypes.c_int64
+        lib.kda_norm_gate_workspace_size.argtypes = [I64, I]
+        lib.kda_norm_gate_workspace_size.restype = SZ
+        lib.kda_norm_gate_fwd.argtypes = [I64, I, I, ctypes.c_float, P, P, P, P, P]
+        lib.kda_norm_gate_fwd.restype = I
+        lib.kda_norm_gate_bwd.argtypes = [I64, I, I, ctypes.c_float, P, P, P, P, P, P, P, P, SZ, P]
+        lib.kda_norm_gate_bwd.restype = I
         _lib = lib
         return lib
 
@@ -153,6 +160,28 @@ def kda_decode(n_seq, H, dk, dv, dtype, scale, q, k, v, f, b, A_log, dt_bias, st
                            _p(f), _p(b), _p(A_log), _p(dt_bias), _p(state), _p(o), _stream())
     if st != 0:
         raise KdaError(st, "kda_decode")
+
+
+def _dt(dtype):
+    return KDA_BF16 if dtype == torch.bfloat16 else KDA_F32 if dtype == torch.float32 else 99
+
+
+def kda_norm_gate_fwd(n_rows, dv, dtype, eps, x, g, w, y):
+    st = load().kda_norm_gate_fwd(int(n_rows), int(dv), _dt(dtype), float(eps or 0.0), _p(x), _p(g), _p(w), _p(y),
+                                  _stream())
+    if st != 0:
+        raise KdaError(st, "kda_norm_gate_fwd")
+
+
+def kda_norm_gate_bwd(n_rows, dv, dtype, eps, x, g, w, dy, dx, dg, dw, workspace):
+    st = load().kda_norm_gate_bwd(int(n_rows), int(dv), _dt(dtype), float(eps or 0.0), _p(x), _p(g), _p(w), _p(dy),
+                                  _p(dx), _p(dg), _p(dw), _p(workspace), workspace.numel(), _stream())
+    if st != 0:
+        raise KdaError(st, "kda_norm_gate_bwd")
+
+
+def kda_norm_gate_workspace_size(n_rows, dv) -> int:
+    return int(load().kda_norm_gate_workspace_size(int(n_rows), int(dv)))
 
 
 def kda_device_status(workspace) -> int:

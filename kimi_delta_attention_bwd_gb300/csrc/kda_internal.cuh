@@ -25,6 +25,9 @@ enum KernelId {
   K_BWD_GRAD,
   K_BWD_GATE,
   K_DECODE,
+  K_NORM_FWD,
+  K_NORM_BWD,
+  K_NORM_RED,
   K_COUNT
 };
 

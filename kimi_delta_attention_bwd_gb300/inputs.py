@@ -201,3 +201,15 @@ def numpy_f64(inp) -> dict:
     r["cu_seqlens"] = seq_offsets(inp)
     r["scale"] = float(inp["scale"])
     return r
+
+
+def norm_gate_inputs(n_rows: int, dv: int, dtype: str = "bf16", seed: int = BASE_SEED + 50):
+    """Inputs of the gated RMSNorm epilogue: x, g, dy ~ N(0, 1) [n_rows, dv] in
+    the io dtype, w ~ 1 + 0.1 N(0, 1) [dv] float32."""
+    gen = torch.Generator().manual_seed(seed)
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    x = torch.randn(n_rows, dv, generator=gen).to(dt)
+    g = torch.randn(n_rows, dv, generator=gen).to(dt)
+    dy = torch.randn(n_rows, dv, generator=gen).to(dt)
+    w = (1.0 + 0.1 * torch.randn(dv, generator=gen)).to(torch.float32)
+    return {"x": x, "g": g, "w": w, "dy": dy}
