@@ -317,6 +317,30 @@ def norm_gate_bench(args, dev, flush, world, stream, hbm, rank):
                                  "frac": bb / (bwd_ms / 1e3) / 1e9 / hbm, "algorithmic_bytes_per_launch": bb}}}
 
 
+def short_conv_bench(args, dev, flush, world, stream, hbm, rank):
+    """Short causal conv (width 4, silu) on the 300M layer's concatenated
+    q | k | v (16 x 2048 tokens x C = H (2 dk + dv) = 1024 channels, bf16)."""
+    from kimi_delta_attention_bwd_gb300 import _lib, kda_short_conv, kda_short_conv_backward
+    from kimi_delta_attention_bwd_gb300.inputs import short_conv_inputs
+    w = WORKLOADS[STEP_WORKLOAD]
+    n, C = w.B * w.T, w.H * (2 * w.dk + w.dv)
+    d = {k: t.to(dev) for k, t in short_conv_inputs(n, C, "bf16", seed=BASE_SEED + 79 + 1000 * rank).items()}
+    y = torch.empty_like(d["x"])
+    ws = torch.empty(_lib.kda_short_conv_workspace_size(n, C), dtype=torch.uint8, device=dev)
+    fwd_ms = max_over_ranks(time_steps(lambda: kda_short_conv(d["x"], d["w"], out=y), args.steps, args.warmup,
+                                       flush, world, stream), world, dev)
+    bwd_ms = max_over_ranks(time_steps(lambda: kda_short_conv_backward(d["x"], d["w"], d["dy"], workspace=ws),
+                                       args.steps, args.warmup, flush, world, stream), world, dev)
+    fb, bb = n * C * 2 * 2, n * C * 3 * 2  # x in, y out; x, dy in, dx out
+    return {"workload": f"short causal conv width 4 + silu, {n} tokens x {C} channels, bf16", "unit": "tokens/s",
+            "fwd": {"value": world * n / (fwd_ms / 1e3), "ms_per_step": fwd_ms,
+                    "roofline": {"bound": "hbm", "achieved": fb / (fwd_ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                                 "frac": fb / (fwd_ms / 1e3) / 1e9 / hbm, "algorithmic_bytes_per_launch": fb}},
+            "bwd": {"value": world * n / (bwd_ms / 1e3), "ms_per_step": bwd_ms,
+                    "roofline": {"bound": "hbm", "achieved": bb / (bwd_ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                                 "frac": bb / (bwd_ms / 1e3) / 1e9 / hbm, "algorithmic_bytes_per_launch": bb}}}
+
+
 def time_steps(step, steps, warmup, flush, world, stream):
     for _ in range(warmup):
         step()
@@ -357,6 +381,8 @@ def run_ours(args, rank, world, local):
     dec = decode_bench(args, dev, flush, world, stream, hbm, rank)
     torch.cuda.empty_cache()
     ngate = norm_gate_bench(args, dev, flush, world, stream, hbm, rank)
+    torch.cuda.empty_cache()
+    sconv = short_conv_bench(args, dev, flush, world, stream, hbm, rank)
     torch.cuda.empty_cache()
 
     # the training step (timed region with per-kernel event brackets and clock sampling)
@@ -416,6 +442,7 @@ def run_ours(args, rank, world, local):
                     "workload": wf.name},
             "decode": dec,
             "norm_gate": ngate,
+            "short_conv": sconv,
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": traffic, "peak_kind": peak_kind,
                          "algorithmic_bytes_per_launch": ab, "launch_ms": dom_ms},

@@ -218,6 +218,27 @@ KDA_API kda_status kda_norm_gate_bwd(int64_t n_rows, int dv, int dtype, float ep
                    void* dx, void* dg, float* dw, void* workspace, size_t workspace_bytes,
                    cudaStream_t stream);
 
+/* Varlen short causal depthwise convolution, kernel width 4, the step before
+ * the KDA path on the concatenated q | k | v channels ("Pure KDA 300M" guide,
+ * Overview: short-conv kernel size 4, depthwise on the concatenated QKV; its
+ * troubleshooting section uses FLA's causal_conv1d on [B, T, D]; torchtitan PR
+ * "[kimi k3] Support sample packing in KDA": per-document reset):
+ *   z_t,c = sum_{j<4} w[c, j] x_{t-3+j, c}   (x before the document start is 0)
+ *   y_t,c = silu(z_t,c) = z sigmoid(z) (activation 1), or z (activation 0)
+ * x, y, dy, dx : [n_tok, C] token-major in dtype (C a multiple of 8 for bf16,
+ * 4 for fp32; 16-byte aligned); w, dw : [C, 4] fp32 (w 16-byte aligned).  cu_seqlens (device
+ * int32 [n_docs + 1], 0 = c0 <= ... = n_tok) delimits documents; NULL is one
+ * document.  The backward overwrites dx and dw (per-tile partials of dw in the
+ * workspace, summed in a fixed order): kda_short_conv_workspace_size(n_tok, C)
+ * bytes. */
+KDA_API size_t kda_short_conv_workspace_size(int64_t n_tok, int C);
+KDA_API kda_status kda_short_conv_fwd(int64_t n_tok, int C, int dtype, int activation,
+                   const int32_t* cu_seqlens, int n_docs, const void* x, const float* w, void* y,
+                   cudaStream_t stream);
+KDA_API kda_status kda_short_conv_bwd(int64_t n_tok, int C, int dtype, int activation,
+                   const int32_t* cu_seqlens, int n_docs, const void* x, const float* w, const void* dy,
+                   void* dx, float* dw, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -6,6 +6,7 @@ libkda_gb300.so through its C ABI, include/kda.h):
   o, h_final, ctx = kda_forward(q, k, v, f, b, A_log, dt_bias, ...)
   grads = kda_backward(ctx, dO, dh_final=None)
   o = kda_decode_step(q, k, v, f, b, A_log, dt_bias, state)   # one token, state in place
+  qkv = kda_short_conv(qkv_raw, conv_w, cu_seqlens)            # short causal conv (k=4) + silu
   y = kda_norm_gate(o, gate, weight)                           # gated RMSNorm epilogue
   do, dgate, dweight = kda_norm_gate_backward(o, gate, weight, dy)
 
@@ -23,8 +24,8 @@ import torch
 from . import _lib
 from ._lib import KdaError, kda_device_status, kda_strerror_text  # noqa: F401
 
-__all__ = ["kda_forward", "kda_backward", "kda_decode_step", "kda_norm_gate", "kda_norm_gate_backward", "KdaContext",
-           "KdaError", "kda_device_status"]
+__all__ = ["kda_forward", "kda_backward", "kda_decode_step", "kda_norm_gate", "kda_norm_gate_backward",
+           "kda_short_conv", "kda_short_conv_backward", "KdaContext", "KdaError", "kda_device_status"]
 
 
 @dataclass
@@ -168,3 +169,33 @@ def kda_norm_gate_backward(x, g, w, dy, eps: Optional[float] = None, workspace: 
     dw = torch.empty_like(w)
     _lib.kda_norm_gate_bwd(n, dv, x.dtype, eps, x, g, w, dy, dx, dg, dw, workspace)
     return dx, dg, dw
+
+
+def kda_short_conv(x, w, cu_seqlens=None, activation: str = "silu", out: Optional[torch.Tensor] = None):
+    """Short causal depthwise convolution (width 4) over tokens, reset at the
+    cu_seqlens document starts: x [..., C] token-major (e.g. the concatenated
+    q | k | v projections [B, T, C]), w [C, 4] fp32; activation "silu" or
+    "none"."""
+    _check(x, "x")
+    _check(w, "w", torch.float32)
+    C = x.shape[-1]
+    if tuple(w.shape) != (C, 4):
+        raise ValueError(f"w must be {(C, 4)}")
+    if cu_seqlens is not None:
+        _check(cu_seqlens, "cu_seqlens", torch.int32)
+    y = out if out is not None else torch.empty_like(x)
+    _lib.kda_short_conv_fwd(x.numel() // C, C, x.dtype, 1 if activation == "silu" else 0, cu_seqlens, x, w, y)
+    return y
+
+
+def kda_short_conv_backward(x, w, dy, cu_seqlens=None, activation: str = "silu",
+                            workspace: Optional[torch.Tensor] = None):
+    """Backward of kda_short_conv: returns (dx, dw)."""
+    _check(dy, "dy", x.dtype)
+    C = x.shape[-1]
+    n = x.numel() // C
+    if workspace is None:
+        workspace = torch.empty(_lib.kda_short_conv_workspace_size(n, C), dtype=torch.uint8, device=x.device)
+    dx, dw = torch.empty_like(x), torch.empty_like(w)
+    _lib.kda_short_conv_bwd(n, C, x.dtype, 1 if activation == "silu" else 0, cu_seqlens, x, w, dy, dx, dw, workspace)
+    return dx, dw

@@ -83,6 +83,12 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.kda_norm_gate_fwd.restype = I
         lib.kda_norm_gate_bwd.argtypes = [I64, I, I, ctypes.c_float, P, P, P, P, P, P, P, P, SZ, P]
         lib.kda_norm_gate_bwd.restype = I
+        lib.kda_short_conv_workspace_size.argtypes = [I64, I]
+        lib.kda_short_conv_workspace_size.restype = SZ
+        lib.kda_short_conv_fwd.argtypes = [I64, I, I, I, P, I, P, P, P, P]
+        lib.kda_short_conv_fwd.restype = I
+        lib.kda_short_conv_bwd.argtypes = [I64, I, I, I, P, I, P, P, P, P, P, P, SZ, P]
+        lib.kda_short_conv_bwd.restype = I
         _lib = lib
         return lib
 
@@ -182,6 +188,26 @@ def kda_norm_gate_bwd(n_rows, dv, dtype, eps, x, g, w, dy, dx, dg, dw, workspace
 
 def kda_norm_gate_workspace_size(n_rows, dv) -> int:
     return int(load().kda_norm_gate_workspace_size(int(n_rows), int(dv)))
+
+
+def kda_short_conv_fwd(n_tok, C, dtype, activation, cu_seqlens, x, w, y):
+    nd = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    st = load().kda_short_conv_fwd(int(n_tok), int(C), _dt(dtype), int(activation), _p(cu_seqlens), nd, _p(x), _p(w),
+                                   _p(y), _stream())
+    if st != 0:
+        raise KdaError(st, "kda_short_conv_fwd")
+
+
+def kda_short_conv_bwd(n_tok, C, dtype, activation, cu_seqlens, x, w, dy, dx, dw, workspace):
+    nd = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    st = load().kda_short_conv_bwd(int(n_tok), int(C), _dt(dtype), int(activation), _p(cu_seqlens), nd, _p(x), _p(w),
+                                   _p(dy), _p(dx), _p(dw), _p(workspace), workspace.numel(), _stream())
+    if st != 0:
+        raise KdaError(st, "kda_short_conv_bwd")
+
+
+def kda_short_conv_workspace_size(n_tok, C) -> int:
+    return int(load().kda_short_conv_workspace_size(int(n_tok), int(C)))
 
 
 def kda_device_status(workspace) -> int:

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libkda_gb300.so")
-SOURCES = ["kda_api.cu", "kda_fwd.cu", "kda_bwd.cu", "kda_fast.cu", "kda_decode.cu", "kda_norm.cu"]
+SOURCES = ["kda_api.cu", "kda_fwd.cu", "kda_bwd.cu", "kda_fast.cu", "kda_decode.cu", "kda_norm.cu", "kda_conv.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

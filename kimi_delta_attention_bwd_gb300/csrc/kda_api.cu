@@ -393,7 +393,8 @@ const char* kda_strerror(kda_status s) {
 static const char* const k_names[K_COUNT] = {"chunk_table", "fwd_intra", "fwd_scan", "bwd_scan",
                                              "bwd_intra", "bwd_reduce", "fwd_chain", "fwd_chunk",
                                              "fwd_state", "bwd_grad",  "bwd_gate",   "decode",
-                                             "norm_gate_fwd", "norm_gate_bwd", "norm_gate_reduce"};
+                                             "norm_gate_fwd", "norm_gate_bwd", "norm_gate_reduce",
+                                             "conv_fwd",  "conv_bwd",  "conv_reduce"};
 
 const char* kda_prof_kernel_name(int i) { return (i >= 0 && i < K_COUNT) ? k_names[i] : nullptr; }
 

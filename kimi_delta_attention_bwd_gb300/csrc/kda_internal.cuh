@@ -28,6 +28,9 @@ enum KernelId {
   K_NORM_FWD,
   K_NORM_BWD,
   K_NORM_RED,
+  K_CONV_FWD,
+  K_CONV_BWD,
+  K_CONV_RED,
   K_COUNT
 };
 
@@ -122,6 +125,9 @@ bool fast_path(int dtype, int dk, int dv);
 cudaError_t launch_fast_fwd(const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st, bool fused);
 cudaError_t launch_fast_bwd(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st);
 
+// out[c] = sum over the rows of a [nrows][ncols] fp32 array, in a fixed order.
+cudaError_t launch_sum_rows(const float* part, int nrows, int ncols, float* out, cudaStream_t st);
+
 // Timing brackets (no-ops unless kda_prof_start() armed them).
 void prof_begin(int kid, cudaStream_t st);
 void prof_end(int kid, cudaStream_t st);
@@ -141,6 +147,10 @@ __device__ __forceinline__ float softplus_f(float x) {
   return fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x)));
 }
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+// Sigmoid from the fast exponential and reciprocal intrinsics (relative error
+// ~1e-6): for the streaming epilogue / prologue kernels whose outputs are
+// stored in bf16 or fp32 and need no more.
+__device__ __forceinline__ float sigmoid_fast(float x) { return __frcp_rn(1.0f + __expf(-x)); }
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll

@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(NTHR) norm_gate_fwd_kernel(int64_t n, float ep
   ss = row_sum<LPR>(ss);
   const float r = 1.0f / sqrtf(ss / DV + eps);
 #pragma unroll
-  for (int e = 0; e < EPL; e++) yv[e] = xv[e] * r * w[c0 + e] * sigmoid_f(gv[e]);
+  for (int e = 0; e < EPL; e++) yv[e] = xv[e] * r * w[c0 + e] * sigmoid_fast(gv[e]);
   if (ok) st16(y + row * DV + c0, yv);
 }
 
@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(NTHR) norm_gate_bwd_kernel(int64_t n, int64_t 
     float m = 0.f;
 #pragma unroll
     for (int e = 0; e < EPL; e++) {
-      const float s = sigmoid_f(gv[e]);
+      const float s = sigmoid_fast(gv[e]);
       xh[e] = xv[e] * r;
       a[e] = dyv[e] * wv[e] * s;
       o2[e] = dyv[e] * xh[e] * wv[e] * s * (1.0f - s);  // dg
@@ -146,13 +146,41 @@ __global__ void __launch_bounds__(NTHR) norm_gate_bwd_kernel(int64_t n, int64_t 
   }
 }
 
-__global__ void norm_gate_reduce_kernel(int nblk, int dv, const float* __restrict__ part, float* __restrict__ dw) {
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= dv) return;
-  float s = 0.f;
-  for (int b = 0; b < nblk; b++) s += part[(int64_t)b * dv + j];
-  dw[j] = s;
+}  // namespace
+
+// out[c] = sum_r part[r][c] over r = 0 .. nrows - 1, in a fixed order: a CTA
+// owns 32 columns; its 8 row groups each sum every 8th row with four
+// independent partial sums, then the groups are added in order.
+__global__ void __launch_bounds__(256) sum_rows_kernel(const float* __restrict__ part, int nrows, int ncols,
+                                                       float* __restrict__ out) {
+  __shared__ float red[8][32];
+  const int cx = threadIdx.x & 31, gy = threadIdx.x >> 5, c = blockIdx.x * 32 + cx;
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  if (c < ncols) {
+    int r = gy;
+    for (; r + 24 < nrows; r += 32) {
+      a0 += part[(int64_t)r * ncols + c];
+      a1 += part[(int64_t)(r + 8) * ncols + c];
+      a2 += part[(int64_t)(r + 16) * ncols + c];
+      a3 += part[(int64_t)(r + 24) * ncols + c];
+    }
+    for (; r < nrows; r += 8) a0 += part[(int64_t)r * ncols + c];
+  }
+  red[gy][cx] = (a0 + a1) + (a2 + a3);
+  __syncthreads();
+  if (gy == 0 && c < ncols) {
+    float s = 0.f;
+    for (int g = 0; g < 8; g++) s += red[g][cx];
+    out[c] = s;
+  }
 }
+
+cudaError_t launch_sum_rows(const float* part, int nrows, int ncols, float* out, cudaStream_t st) {
+  sum_rows_kernel<<<(ncols + 31) / 32, 256, 0, st>>>(part, nrows, ncols, out);
+  return cudaGetLastError();
+}
+
+namespace {
 
 int bwd_blocks(int64_t n) {
   const int64_t want = (n + 31) / 32;  // at least 32 rows per CTA
@@ -241,7 +269,7 @@ extern "C" KDA_API kda_status kda_norm_gate_bwd(int64_t n_rows, int dv, int dtyp
   prof_end(K_NORM_BWD, st);
   if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
   prof_begin(K_NORM_RED, st);
-  norm_gate_reduce_kernel<<<(dv + 127) / 128, 128, 0, st>>>(nblk, dv, part, dw);
+  const cudaError_t e2 = launch_sum_rows(part, nblk, dv, dw, st);
   prof_end(K_NORM_RED, st);
-  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+  return e2 == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

@@ -213,3 +213,14 @@ def norm_gate_inputs(n_rows: int, dv: int, dtype: str = "bf16", seed: int = BASE
     dy = torch.randn(n_rows, dv, generator=gen).to(dt)
     w = (1.0 + 0.1 * torch.randn(dv, generator=gen)).to(torch.float32)
     return {"x": x, "g": g, "w": w, "dy": dy}
+
+
+def short_conv_inputs(n_tok: int, C: int, dtype: str = "bf16", seed: int = BASE_SEED + 60):
+    """Inputs of the short convolution: x, dy ~ N(0, 1) [n_tok, C] in the io
+    dtype, w ~ N(0, 0.5^2) [C, 4] float32."""
+    gen = torch.Generator().manual_seed(seed)
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    x = torch.randn(n_tok, C, generator=gen).to(dt)
+    dy = torch.randn(n_tok, C, generator=gen).to(dt)
+    w = (0.5 * torch.randn(C, 4, generator=gen)).to(torch.float32)
+    return {"x": x, "w": w, "dy": dy}
