@@ -224,9 +224,10 @@ def run_reference(args, rank, world):
     return 0
 
 
-def cpu_baseline(min_seconds=10.0, max_reps=20):
+def cpu_baseline(min_seconds=10.0, max_reps=200):
     """The oracle as it stands on the host cores: full workload steps
-    repeated until at least `min_seconds` have elapsed."""
+    repeated until at least `min_seconds` have elapsed (a bounded sample of
+    about 10 s of CPU work)."""
     w = WORKLOADS[STEP_WORKLOAD]
     x = numpy_f64(make_inputs(w))
     cpu_oracle_step(x, w)  # first touch of the output pages
