@@ -1578,7 +1578,7 @@ static_assert(offsetof(GateSm, rq) % 16 == 0 && offsetof(GateSm, rk) % 16 == 0 &
                   offsetof(GateSm, dp) % 16 == 0 && offsetof(GateSm, ma) % 16 == 0,
               "vector-accessed arrays");
 
-__global__ void __launch_bounds__(NTH, 2) bwd_gate_kernel(Dims d, BwdIO io, Ws w) {
+__global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w) {
   extern __shared__ __align__(16) unsigned char smraw[];
   GateSm& sm = *reinterpret_cast<GateSm*>(smraw);
   const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1897,7 +1897,7 @@ static_assert(sizeof(fast::FwdSm) <= 232448, "fused forward shared memory exceed
 static_assert(sizeof(fast::ChunkSm) <= 113 * 1024, "per-chunk forward must fit two CTAs per SM");
 
 static_assert(sizeof(fast::GradSm) <= 112 * 1024, "chunk-gradient kernel must fit two CTAs per SM");
-static_assert(sizeof(fast::GateSm) <= 112 * 1024, "gate kernel must fit two CTAs per SM");
+static_assert(sizeof(fast::GateSm) <= 75 * 1024, "gate kernel must fit three CTAs per SM");
 
 bool fast_path(int dtype, int dk, int dv) { return dtype == 0 && dk == fast::DK && dv == fast::DV; }
 
