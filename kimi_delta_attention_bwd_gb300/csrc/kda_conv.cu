@@ -47,6 +47,20 @@ __device__ __forceinline__ void vst(__nv_bfloat16* p, const float (&v)[8]) {
 __device__ __forceinline__ void vst(float* p, const float (&v)[4]) {
   *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
 }
+// 8-byte variants (four bf16 channels) for the backward, whose per-thread state
+// (taps, weight-gradient sums, two windows) grows with the channel count.
+__device__ __forceinline__ void vld(const __nv_bfloat16* p, float (&v)[4]) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
+__device__ __forceinline__ void vst(__nv_bfloat16* p, const float (&v)[4]) {
+  uint2 u;
+  *reinterpret_cast<__nv_bfloat162*>(&u.x) = __floats2bfloat162_rn(v[0], v[1]);
+  *reinterpret_cast<__nv_bfloat162*>(&u.y) = __floats2bfloat162_rn(v[2], v[3]);
+  *reinterpret_cast<uint2*>(p) = u;
+}
 
 // Document of token t: the largest d < n_docs with cu[d] <= t (cu non-decreasing
 // from 0; without cu one document).  Returns its start, and its end in *end.
@@ -135,12 +149,14 @@ __global__ void __launch_bounds__(CTHR) conv_fwd_kernel(int64_t n_tok, int C, in
 // Backward.  At step u the thread forms dz_u (from x_{u-3..u}) and emits
 // dx_{u-3} from dz_{u-3..u}; a token's document start is kept for the last
 // four positions so that no window reaches across a document boundary.
+constexpr int NB = 4;  // channels per thread in the backward
+
 template <typename T>
 __global__ void __launch_bounds__(CTHR) conv_bwd_kernel(int64_t n_tok, int C, int act, const int32_t* __restrict__ cu,
                                                        int n_docs, const T* __restrict__ x,
                                                        const float* __restrict__ w, const T* __restrict__ dy,
                                                        T* __restrict__ dx, float* __restrict__ part) {
-  constexpr int N = V16<T>::N;
+  constexpr int N = NB;
   const int cv = blockIdx.x * CTHR + threadIdx.x;
   if (cv >= C / N) return;
   const int c0 = cv * N;
@@ -171,7 +187,6 @@ __global__ void __launch_bounds__(CTHR) conv_bwd_kernel(int64_t n_tok, int C, in
     for (int e = 0; e < N; e++) dzw[k][e] = 0.f;
     dsw[k] = start;  // positions before t0 only pair with dz of tokens >= t0 through dx_{< t0}: never emitted
   }
-#pragma unroll 4
   for (int64_t u = t0; u < t1 + (KW - 1); u++) {  // dx of the last token needs dz up to t1 + 2
     float dzu[N];
     const bool live = u < n_tok;
@@ -288,7 +303,7 @@ extern "C" KDA_API kda_status kda_short_conv_bwd(int64_t n_tok, int C, int dtype
   if (!a16(x) || !a16(dy) || !a16(dx) || !a16(w) || (uintptr_t)dw % 4 != 0) return KDA_ERR_ALIGNMENT;
   if (!workspace || workspace_bytes < kda_short_conv_workspace_size(n_tok, C)) return KDA_ERR_WORKSPACE;
   if ((uintptr_t)workspace % 16 != 0) return KDA_ERR_ALIGNMENT;
-  const int nvec = C / (dtype == KDA_BF16 ? 8 : 4);
+  const int nvec = C / NB;
   const int n_tiles = (int)((n_tok + TBB - 1) / TBB);
   const dim3 grid((nvec + CTHR - 1) / CTHR, (unsigned)n_tiles);
   float* part = (float*)workspace;
