@@ -537,6 +537,8 @@ struct ChunkSm {
   float gam[DK];
   float tot[NW * DK];
   int spanok[4];
+  uint64_t bar;    // tensor-core rounds
+  uint32_t tslot;  // TMEM base address
 };
 
 // The six upper 16 x 16 blocks of a C x C split tile set to zero (the backward
@@ -611,6 +613,11 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
   const float* dtb = io.dt_bias + h * (gdn ? 1 : DK);
   const bf16* qraw = (const bf16*)io.q;
   const bf16* kraw = (const bf16*)io.k;
+  if (warp == 0) tc::tmem_alloc(&sm.tslot, TCOLS);  // published by the first barrier below
+  if (tid == 0) {
+    mbar_init(&sm.bar, 1);
+    mbar_init_fence();
+  }
   {
     int j2, h2;
     if (ahead_of(d, w, j, h, j2, h2)) {
@@ -692,7 +699,10 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
   if (lane >= 28)
 #pragma unroll
     for (int e = 0; e < 8; e++) sm.tot[warp * DK + 8 * q4 + e] = gv[e];
+  tc::fence_before();
   __syncthreads();
+  tc::fence_after();
+  const uint32_t tb = sm.tslot;
 #pragma unroll
   for (int e = 0; e < 8; e++) {
     float off = 0.f;
@@ -778,10 +788,8 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
       });
     }
   }
-  if (io.save) {
-    zero_upper(P);
-    fence_async_smem();
-  }
+  zero_upper(P);  // the tensor core reads whole tiles
+  fence_async_smem();
   __syncthreads();
   if (io.save && tid == 0) {  // P for the backward (its tile is not written again)
     bulk_s2g(w.sP + ch * 2 * C * C, P.hi, 4 * C * C);
@@ -794,53 +802,60 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     op_store2(KD, r, 8 * q4 + e, kd[e], kd[e + 1]);
   }
   solve<true>(sm.am, tm, yy, sm.bet);
-  for (int idx = tid; idx < 10 * 16 * 8; idx += NTH) {  // lower blocks of T -> split operand over A
-    const int blk = idx >> 7, rem = idx & 127;
-    const int bI = blk < 1 ? 0 : blk < 3 ? 1 : blk < 6 ? 2 : 3, bJ = blk - bI * (bI + 1) / 2;
-    const int rr = 16 * bI + (rem >> 3), s2 = 16 * bJ + 2 * (rem & 7);
-    op_store2(T, rr, s2, tm[rr * SC + s2], tm[rr * SC + s2 + 1]);
+  for (int idx = tid; idx < C * C / 2; idx += NTH) {  // T -> split operand over A (upper blocks zero)
+    const int rr = idx / (C / 2), s2 = 2 * (idx % (C / 2));
+    const bool low = (s2 >> 4) <= (rr >> 4);
+    op_store2(T, rr, s2, low ? tm[rr * SC + s2] : 0.f, low ? tm[rr * SC + s2 + 1] : 0.f);
   }
-  if (io.save) {
-    zero_upper(T);
-    fence_async_smem();
-  }
+  fence_async_smem();
+  tc::fence_before();
   __syncthreads();
   if (io.save && tid == 0) {  // T for the backward (its tile is not written again)
     bulk_s2g(w.sT + ch * 2 * C * C, T.hi, 4 * C * C);
     bulk_commit();
   }
-  {  // W | U = T [XK | XV]  (T lower block-triangular: k < 16 (I + 1))
-    const int wI = warp & 3, half = warp >> 2;
-    if (half == 0) {
-      float aw[4][4], au[2][4];
-      zero(aw);
-      zero(au);
-      gemm3<2, false, true>(aw, T, 16 * wI, 0, XK, 0, 0, wI + 1);
-      gemm3<1, false, true>(au, T, 16 * wI, 0, XV, 0, 0, wI + 1);
-      const int gq = lane >> 2, tq = lane & 3;
-#pragma unroll
-      for (int jt = 0; jt < 4; jt++)
-#pragma unroll
-        for (int hh = 0; hh < 2; hh++)
-          op_store2(W, 16 * wI + gq + 8 * hh, 8 * jt + 2 * tq, aw[jt][2 * hh], aw[jt][2 * hh + 1]);
-#pragma unroll
-      for (int jt = 0; jt < 2; jt++)
-#pragma unroll
-        for (int hh = 0; hh < 2; hh++)
-          op_store2(U, 16 * wI + gq + 8 * hh, 8 * jt + 2 * tq, au[jt][2 * hh], au[jt][2 * hh + 1]);
-    } else {
-      float au[6][4];
-      zero(au);
-      gemm3<3, false, true>(au, T, 16 * wI, 0, XV, 16, 0, wI + 1);
-      const int gq = lane >> 2, tq = lane & 3;
-#pragma unroll
-      for (int jt = 0; jt < 6; jt++)
-#pragma unroll
-        for (int hh = 0; hh < 2; hh++)
-          op_store2(U, 16 * wI + gq + 8 * hh, 16 + 8 * jt + 2 * tq, au[jt][2 * hh], au[jt][2 * hh + 1]);
-    }
+  // tensor-core rounds: one thread issues, completion on sm.bar, then every warp
+  // reads the m16n8 fragments of its 16 rows.  TMEM columns: W 0 | U 32;
+  // then PU 96 | QW' 160 | KU' 192 | M' 0 (rows 32.. of KU' and M' are unused)
+  uint32_t mph = 0;
+  auto round_done = [&]() -> bool {  // uniform over the CTA
+    const bool ok = mbar_wait(&sm.bar, mph);
+    mph ^= 1;
+    tc::fence_after();
+    return !__syncthreads_or(!ok);
+  };
+  auto bail = [&]() {
+    mbar_wait(&sm.bar, mph ^ 1);
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tb, TCOLS);
+    if (tid == 0) atomicExch(w.err, -7);
+  };
+  if (tid == 0) {  // W | U = T [XK | XV]
+    tc::fence_after();
+    tc::gemm_split(tb + 0, tc::kmaj(T), tc::mnmaj(XK), 32, C / 16, false);
+    tc::gemm_split(tb + 32, tc::kmaj(T), tc::mnmaj(XV), 64, C / 16, false);
+    tc::commit(&sm.bar);
   }
-  if (io.save) fence_async_smem();
+  if (!round_done()) { bail(); return; }
+  {
+    const int wI = warp & 3, hk = warp >> 2, gq = lane >> 2, tq = lane & 3;
+    float aw[2][4], au[4][4];
+    tc::ld_frag<2>(tb + 0, 16 * hk, aw);
+    tc::ld_frag<4>(tb + 32, 32 * hk, au);
+#pragma unroll
+    for (int jt = 0; jt < 2; jt++)
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++)
+        op_store2(W, 16 * wI + gq + 8 * hh, 16 * hk + 8 * jt + 2 * tq, aw[jt][2 * hh], aw[jt][2 * hh + 1]);
+#pragma unroll
+    for (int jt = 0; jt < 4; jt++)
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++)
+        op_store2(U, 16 * wI + gq + 8 * hh, 32 * hk + 8 * jt + 2 * tq, au[jt][2 * hh], au[jt][2 * hh + 1]);
+  }
+  fence_async_smem();
+  tc::fence_before();
   __syncthreads();
   if (io.save && tid == 0) {  // W and U for the backward
     bulk_s2g(w.sW + ch * 2 * C * DK, W.hi, 4 * C * DK);
@@ -851,43 +866,36 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
   // split, straight to global; PU and KU staged over XK | XV, then bulk stores)
   float* PUs = reinterpret_cast<float*>(sm.y);  // [C][DV]
   float* KUs = PUs + C * DV;                    // [DK][DV]
+  if (tid == 0) {  // PU = P U, QW' = P W, KU' = KD^T U, M' = KD^T W (KD^T: rows 32.. unused)
+    tc::fence_after();
+    tc::gemm_split(tb + 96, tc::kmaj(P), tc::mnmaj(U), 64, C / 16, false);
+    tc::gemm_split(tb + 160, tc::kmaj(P), tc::mnmaj(W), 32, C / 16, false);
+    tc::gemm_split(tb + 192, tc::mnmaj(KD), tc::mnmaj(U), 64, C / 16, false);
+    tc::gemm_split(tb + 0, tc::mnmaj(KD), tc::mnmaj(W), 32, C / 16, false);
+    tc::commit(&sm.bar);
+  }
+  if (!round_done()) { bail(); return; }
   {
-    const int wI = warp & 3, half = warp >> 2;
-    float* PUg = PUs;
-    float* KUg = KUs;
+    const int wI = warp & 3, hk = warp >> 2;
     const Op QWg{w.sQW + ch * 2 * C * DK, w.sQW + ch * 2 * C * DK + C * DK, DK};
     const Op Mg{w.sM + ch * 2 * DK * DK, w.sM + ch * 2 * DK * DK + DK * DK, DK};
-    {
-      float acc[4][4];
-      zero(acc);
-      gemm3<2, false, true>(acc, P, 16 * wI, 0, U, 32 * half, 0, wI + 1);
-      store_acc(acc, PUg, DV, 16 * wI, 32 * half, [](int, int, float v) { return v; });
-    }
-    {
-      float acc[2][4];
-      zero(acc);
-      gemm3<1, false, true>(acc, P, 16 * wI, 0, W, 16 * half, 0, wI + 1);
-      store_acc_op(acc, QWg, 16 * wI, 16 * half, [&](int rr, int c, float v) { return op_get(QG, rr, c) - v; });
-    }
-    // 12 tiles t = 6 mi + cc (cc < 2: M columns 16 cc, else KU columns 16 (cc - 2)),
-    // dealt so that the warps with short row blocks above take more
-    const int n = 3 - wI;
-    const int tb = (wI == 0 ? 0 : wI == 1 ? 6 : wI == 2 ? 10 : 12) + half * (n > 0 ? n : 0);
-    for (int t = tb; t < tb + n; t++) {
-      const int mi = t / 6, cc = t % 6;
-      float acc[2][4];
-      zero(acc);
-      if (cc < 2) {
-        gemm3<1, true, true>(acc, KD, 16 * mi, 0, W, 16 * cc, 0, C / 16);
-        store_acc_op(acc, Mg, 16 * mi, 16 * cc, [&](int i, int jc, float v) { return (i == jc ? sm.gam[i] : 0.f) - v; });
-      } else {
-        gemm3<1, true, true>(acc, KD, 16 * mi, 0, U, 16 * (cc - 2), 0, C / 16);
-        store_acc(acc, KUg, DV, 16 * mi, 16 * (cc - 2), [](int, int, float v) { return v; });
-      }
+    float pu[4][4], qw[2][4];
+    tc::ld_frag<4>(tb + 96, 32 * hk, pu);
+    tc::ld_frag<2>(tb + 160, 16 * hk, qw);
+    store_acc(pu, PUs, DV, 16 * wI, 32 * hk, [](int, int, float v) { return v; });
+    store_acc_op(qw, QWg, 16 * wI, 16 * hk, [&](int rr, int c, float v) { return op_get(QG, rr, c) - v; });
+    if (wI < 2) {  // rows i < dk of the KD^T products
+      float ku[4][4], mm[2][4];
+      tc::ld_frag<4>(tb + 192, 32 * hk, ku);
+      tc::ld_frag<2>(tb + 0, 16 * hk, mm);
+      store_acc(ku, KUs, DV, 16 * wI, 32 * hk, [](int, int, float v) { return v; });
+      store_acc_op(mm, Mg, 16 * wI, 16 * hk, [&](int i, int jc, float v) { return (i == jc ? sm.gam[i] : 0.f) - v; });
     }
   }
+  tc::fence_before();
   fence_async_smem();
   __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tb, TCOLS);
   if (tid == 0) {
     bulk_s2g(w.PU + ch * C * DV, PUs, 4 * C * DV);
     bulk_s2g(w.KU + ch * DK * DV, KUs, 4 * DK * DV);
