@@ -900,7 +900,7 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     bulk_s2g(w.PU + ch * C * DV, PUs, 4 * C * DV);
     bulk_s2g(w.KU + ch * DK * DV, KUs, 4 * DK * DV);
     bulk_commit();
-    bulk_wait_all();  // every bulk store of this CTA has completed
+    bulk_wait_read();  // the stores' shared-memory reads are done (the writes complete with the grid)
   }
 }
 

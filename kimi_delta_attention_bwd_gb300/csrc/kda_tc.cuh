@@ -81,16 +81,31 @@ __device__ __forceinline__ void mma_issue(uint32_t d, uint64_t a, uint64_t b, ui
       : "memory");
 }
 
+// Descriptor increment of one K-step (16 columns = two core matrices along
+// K) of a view, in the descriptor's 16-byte address units.
+__device__ __forceinline__ uint64_t vstep(const View& v) {
+  return v.mn ? (uint64_t)(2 * (v.Kc / 8) * 128 / 16) : (uint64_t)(2 * 128 / 16);
+}
+
 // D (M = 64 rows, N columns at TMEM address d) = (or +=, when acc) A B over
 // ksteps x 16, every operand split into bf16 hi + lo: hi*hi + hi*lo + lo*hi
-// (a null lo is exact and skips its product).  One thread issues.
+// (a null lo is exact and skips its product).  One thread issues.  The
+// descriptors are built once and stepped along K by adding to their start
+// address field (a shared-memory address stays below 2^18 bytes, so the
+// 14-bit field never carries).
 __device__ __forceinline__ void gemm_split(uint32_t d, const View& A, const View& B, int N, int ksteps, bool acc) {
   const uint32_t id = idesc_bf16(64, N, A.mn, B.mn);
+  const uint64_t sa = vstep(A), sb = vstep(B);
+  uint64_t ah = vdesc(A, A.hi, 0), bh = vdesc(B, B.hi, 0);
+  uint64_t al = A.lo ? vdesc(A, A.lo, 0) : 0, bl = B.lo ? vdesc(B, B.lo, 0) : 0;
   for (int ks = 0; ks < ksteps; ks++) {
-    const uint64_t ah = vdesc(A, A.hi, ks), bh = vdesc(B, B.hi, ks);
     mma_issue(d, ah, bh, id, (acc || ks > 0) ? 1u : 0u);
-    if (B.lo) mma_issue(d, ah, vdesc(B, B.lo, ks), id, 1u);
-    if (A.lo) mma_issue(d, vdesc(A, A.lo, ks), bh, id, 1u);
+    if (B.lo) mma_issue(d, ah, bl, id, 1u);
+    if (A.lo) mma_issue(d, al, bh, id, 1u);
+    ah += sa;
+    bh += sb;
+    al += sa;
+    bl += sb;
   }
 }
 
