@@ -552,13 +552,30 @@ __device__ __forceinline__ void zero_upper(const Op& t) {
 }
 
 // The chunk-head that the per-chunk kernels run one wave (d.ahead CTAs) after
-// CTA (j, h); false past the end.  Prefetching its inputs into L2 turns the
-// next wave's cold DRAM reads into L2 hits.
-__device__ __forceinline__ bool ahead_of(const Dims& d, const Ws& w, int j, int h, int& j2, int& h2) {
+// CTA (j, h), from registers only; false past the last head.  Its table row is
+// loaded with the CTA's own (rows past the last chunk have length 0), and
+// prefetching its inputs into L2 turns the next wave's cold DRAM reads into
+// L2 hits.
+__device__ __forceinline__ bool ahead_of(const Dims& d, int j, int h, int& j2, int& h2) {
   const int64_t nxt = (int64_t)h * d.nc_max + j + d.ahead;
   j2 = (int)(nxt % d.nc_max);
   h2 = (int)(nxt / d.nc_max);
-  return d.ahead > 0 && h2 < d.H && j2 < *w.n_chunks;
+  return d.ahead > 0 && h2 < d.H;
+}
+// A thread's 8 consecutive channel values rotated by q4 pairs in place:
+// v'[2 p + b] = v[2 ((p + q4) & 3) + b].  Stored by store8_rot, the 32 lanes of
+// a warp (8 rows x 4 channel groups, one core matrix each) then write 32
+// different banks instead of 8.
+__device__ __forceinline__ void rot_pairs(float (&v)[8], int q4) {
+  float t[8];
+#pragma unroll
+  for (int i = 0; i < 8; i++) t[i] = (q4 & 1) ? v[(i + 2) & 7] : v[i];
+#pragma unroll
+  for (int i = 0; i < 8; i++) v[i] = (q4 & 2) ? t[(i + 4) & 7] : t[i];
+}
+__device__ __forceinline__ void store8_rot(const Op& t, int r, int c0, const float (&v)[8], int q4) {
+#pragma unroll
+  for (int p = 0; p < 4; p++) op_store2(t, r, c0 + 2 * ((p + q4) & 3), v[2 * p], v[2 * p + 1]);
 }
 // Thread tid < L prefetches row tid of a [tokens][H][n] bf16 tensor (n * 2 <= 128 bytes).
 __device__ __forceinline__ void prefetch_rows(const void* base, int n, int t0, int L, int H, int h) {
@@ -602,11 +619,12 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
   extern __shared__ __align__(16) unsigned char smraw[];
   ChunkSm& sm = *reinterpret_cast<ChunkSm*>(smraw);
   const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (*w.err != 0) return;
-  if (j >= *w.n_chunks) return;
-  const int L = w.chunk_len[j];
-  if (L <= 0) return;
-  const int t0 = w.chunk_tok0[j], H = d.H;
+  int j2, h2;
+  const bool pf = ahead_of(d, j, h, j2, h2);
+  const int err = *w.err, L = w.chunk_len[j], t0 = w.chunk_tok0[j];  // one round trip
+  const int L2 = pf ? w.chunk_len[j2] : 0, t2 = pf ? w.chunk_tok0[j2] : 0;
+  if (err != 0 || L <= 0) return;
+  const int H = d.H;
   const int64_t ch = (int64_t)j * H + h;
   const float a = expf(io.A_log[h]), scale = d.scale;
   const bool gdn = d.gate != 0;
@@ -618,16 +636,12 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     mbar_init(&sm.bar, 1);
     mbar_init_fence();
   }
-  {
-    int j2, h2;
-    if (ahead_of(d, w, j, h, j2, h2)) {
-      const int L2 = w.chunk_len[j2], t2 = w.chunk_tok0[j2];
-      prefetch_rows(io.q, DK, t2, L2, H, h2);
-      prefetch_rows(io.k, DK, t2, L2, H, h2);
-      prefetch_rows(io.f, gdn ? 1 : DK, t2, L2, H, h2);
-      prefetch_rows(io.v, DV, t2, L2, H, h2);
-      prefetch_rows(io.b, 1, t2, L2, H, h2);
-    }
+  if (L2 > 0) {
+    prefetch_rows(io.q, DK, t2, L2, H, h2);
+    prefetch_rows(io.k, DK, t2, L2, H, h2);
+    prefetch_rows(io.f, gdn ? 1 : DK, t2, L2, H, h2);
+    prefetch_rows(io.v, DV, t2, L2, H, h2);
+    prefetch_rows(io.b, 1, t2, L2, H, h2);
   }
 
   const Op LQ{sm.x, sm.x + 2048, DK}, LK{sm.x + 4096, sm.x + 6144, DK}, R{sm.x + 8192, sm.x + 13312, DK};
@@ -684,6 +698,14 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     sm.ink[r] = ik;
   }
 #pragma unroll
+  for (int hv = 0; hv < 2; hv++) {  // XV = beta v (its region is free from the start)
+    float xv[8];
+#pragma unroll
+    for (int e = 0; e < 8; e++) xv[e] = beta * vv[8 * hv + e];
+    rot_pairs(xv, q4);
+    store8_rot(XV, r, 16 * q4 + 8 * hv, xv, q4);
+  }
+#pragma unroll
   for (int e = 0; e < 8; e++) { qv[e] *= iq; kv[e] *= ik; }
   // cumulative sum of g over rows: shuffles among lanes of equal tid % 4, then warp offsets
 #pragma unroll
@@ -730,24 +752,30 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
       wide |= (r & 15) == 15 && gbv[e] - gv[e] > SPAN2;
     }
     if (wide) sm.spanok[I] = 0;
+    {
+      float lq[8], lk[8];
 #pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-      const int i = 8 * q4 + e;
-      const float l0 = exp2f(gv[e] - gbv[e]), l1 = exp2f(gv[e + 1] - gbv[e + 1]);
-      op_store2(LQ, r, i, qv[e] * l0, qv[e + 1] * l1);
-      op_store2(LK, r, i, kv[e] * l0, kv[e + 1] * l1);
-      op_store2(XK, r, i, xk[e], xk[e + 1]);
-    }
-    for (int I2 = I; I2 < 4; I2++)
-#pragma unroll
-      for (int e = 0; e < 8; e += 2) {
-        const int i = 8 * q4 + e;
-        const float b0 = sm.gg[(16 * I2) * SQ + i], b1 = sm.gg[(16 * I2) * SQ + i + 1];
-        op_store2(R, roff(I2) + r, i, kv[e] * exp2f(fminf(b0 - gv[e], SPAN2)),
-                  kv[e + 1] * exp2f(fminf(b1 - gv[e + 1], SPAN2)));
+      for (int e = 0; e < 8; e++) {
+        const float l = exp2f(gv[e] - gbv[e]);
+        lq[e] = qv[e] * l;
+        lk[e] = kv[e] * l;
       }
+      rot_pairs(lq, q4);
+      rot_pairs(lk, q4);
+      rot_pairs(xk, q4);
+      store8_rot(LQ, r, 8 * q4, lq, q4);
+      store8_rot(LK, r, 8 * q4, lk, q4);
+      store8_rot(XK, r, 8 * q4, xk, q4);
+      rot_pairs(qg, q4);  // stored after the A / P blocks
+      rot_pairs(kd, q4);
+    }
+    for (int I2 = I; I2 < 4; I2++) {
+      float rv[8];
 #pragma unroll
-    for (int e = 0; e < 16; e += 2) op_store2(XV, r, 16 * q4 + e, beta * vv[e], beta * vv[e + 1]);
+      for (int e = 0; e < 8; e++) rv[e] = kv[e] * exp2f(fminf(sm.gg[(16 * I2) * SQ + 8 * q4 + e] - gv[e], SPAN2));
+      rot_pairs(rv, q4);
+      store8_rot(R, roff(I2) + r, 8 * q4, rv, q4);
+    }
   }
   __syncthreads();
 
@@ -796,14 +824,12 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     bulk_commit();
   }
   // QG over G, KD in the tail of the x region (both free now)
-#pragma unroll
-  for (int e = 0; e < 8; e += 2) {
-    op_store2(QG, r, 8 * q4 + e, qg[e], qg[e + 1]);
-    op_store2(KD, r, 8 * q4 + e, kd[e], kd[e + 1]);
-  }
+  store8_rot(QG, r, 8 * q4, qg, q4);  // rotated in the factors step
+  store8_rot(KD, r, 8 * q4, kd, q4);
   solve<true>(sm.am, tm, yy, sm.bet);
   for (int idx = tid; idx < C * C / 2; idx += NTH) {  // T -> split operand over A (upper blocks zero)
-    const int rr = idx / (C / 2), s2 = 2 * (idx % (C / 2));
+    const int core = idx >> 5, ln = idx & 31;  // a warp writes one whole core matrix
+    const int rr = 8 * (core >> 3) + (ln >> 2), s2 = 8 * (core & 7) + 2 * (ln & 3);
     const bool low = (s2 >> 4) <= (rr >> 4);
     op_store2(T, rr, s2, low ? tm[rr * SC + s2] : 0.f, low ? tm[rr * SC + s2 + 1] : 0.f);
   }
@@ -862,10 +888,8 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     bulk_s2g(w.sU + ch * 2 * C * DV, U.hi, 4 * C * DV);
     bulk_commit();
   }
-  // outputs: PU and QW by row block, then the 16 x 16 tiles of M | KU (M, QW
-  // split, straight to global; PU and KU staged over XK | XV, then bulk stores)
-  float* PUs = reinterpret_cast<float*>(sm.y);  // [C][DV]
-  float* KUs = PUs + C * DV;                    // [DK][DV]
+  // outputs, straight from the fragments to global: PU and KU (fp32), QW and M
+  // (split)
   if (tid == 0) {  // PU = P U, QW' = P W, KU' = KD^T U, M' = KD^T W (KD^T: rows 32.. unused)
     tc::fence_after();
     tc::gemm_split(tb + 96, tc::kmaj(P), tc::mnmaj(U), 64, C / 16, false);
@@ -882,26 +906,20 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     float pu[4][4], qw[2][4];
     tc::ld_frag<4>(tb + 96, 32 * hk, pu);
     tc::ld_frag<2>(tb + 160, 16 * hk, qw);
-    store_acc(pu, PUs, DV, 16 * wI, 32 * hk, [](int, int, float v) { return v; });
+    store_acc(pu, w.PU + ch * C * DV, DV, 16 * wI, 32 * hk, [](int, int, float v) { return v; });
     store_acc_op(qw, QWg, 16 * wI, 16 * hk, [&](int rr, int c, float v) { return op_get(QG, rr, c) - v; });
     if (wI < 2) {  // rows i < dk of the KD^T products
       float ku[4][4], mm[2][4];
       tc::ld_frag<4>(tb + 192, 32 * hk, ku);
       tc::ld_frag<2>(tb + 0, 16 * hk, mm);
-      store_acc(ku, KUs, DV, 16 * wI, 32 * hk, [](int, int, float v) { return v; });
+      store_acc(ku, w.KU + ch * DK * DV, DV, 16 * wI, 32 * hk, [](int, int, float v) { return v; });
       store_acc_op(mm, Mg, 16 * wI, 16 * hk, [&](int i, int jc, float v) { return (i == jc ? sm.gam[i] : 0.f) - v; });
     }
   }
   tc::fence_before();
-  fence_async_smem();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tb, TCOLS);
-  if (tid == 0) {
-    bulk_s2g(w.PU + ch * C * DV, PUs, 4 * C * DV);
-    bulk_s2g(w.KU + ch * DK * DV, KUs, 4 * DK * DV);
-    bulk_commit();
-    bulk_wait_read();  // the stores' shared-memory reads are done (the writes complete with the grid)
-  }
+  if (tid == 0) bulk_wait_read();  // the saves' shared-memory reads are done (the writes complete with the grid)
 }
 
 // ------------------------------------------------------------ state chains
@@ -1180,11 +1198,16 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   GradSm& sm = *reinterpret_cast<GradSm*>(smraw);
   const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
-  if (!saved_ok(d, w.tag, w.err)) return;
-  if (j >= *w.n_chunks) return;
-  const int L = w.chunk_len[j];
-  if (L <= 0) return;
-  const int t0 = w.chunk_tok0[j], H = d.H;
+  int j2, h2;
+  const bool pf = ahead_of(d, j, h, j2, h2);
+  const int tag = *w.tag, err = *w.err, L = w.chunk_len[j], t0 = w.chunk_tok0[j];  // one round trip
+  const int L2 = pf ? w.chunk_len[j2] : 0, t2 = pf ? w.chunk_tok0[j2] : 0;
+  if (tag != d.tag) {
+    *w.err = -5;
+    return;
+  }
+  if (err != 0 || L <= 0) return;
+  const int H = d.H;
   const int64_t ch = (int64_t)j * H + h;
   const float a = expf(io.A_log[h]), scale = d.scale;
   const bool gdn = d.gate != 0;
@@ -1234,9 +1257,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   }
 
   {
-    int j2, h2;
-    if (ahead_of(d, w, j, h, j2, h2)) {
-      const int L2 = w.chunk_len[j2], t2 = w.chunk_tok0[j2];
+    if (L2 > 0) {
       const int64_t c2 = (int64_t)j2 * H + h2;
       prefetch_rows(io.k, DK, t2, L2, H, h2);
       prefetch_rows(io.f, gdn ? 1 : DK, t2, L2, H, h2);
@@ -1591,11 +1612,16 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
   GateSm& sm = *reinterpret_cast<GateSm*>(smraw);
   const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
-  if (!saved_ok(d, w.tag, w.err)) return;
-  if (j >= *w.n_chunks) return;
-  const int L = w.chunk_len[j];
-  if (L <= 0) return;
-  const int t0 = w.chunk_tok0[j], H = d.H;
+  int j2, h2;
+  const bool pf = ahead_of(d, j, h, j2, h2);
+  const int tag = *w.tag, err = *w.err, L = w.chunk_len[j], t0 = w.chunk_tok0[j];  // one round trip
+  const int L2 = pf ? w.chunk_len[j2] : 0, t2 = pf ? w.chunk_tok0[j2] : 0;
+  if (tag != d.tag) {
+    *w.err = -5;
+    return;
+  }
+  if (err != 0 || L <= 0) return;
+  const int H = d.H;
   const int64_t ch = (int64_t)j * H + h;
   const float a = expf(io.A_log[h]);
   const bool gdn = d.gate != 0;
@@ -1603,9 +1629,7 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
   const bf16* fsc = (const bf16*)io.f + h;  // scalar gate: f of this head, stride H
 
   {
-    int j2, h2;
-    if (ahead_of(d, w, j, h, j2, h2)) {
-      const int L2 = w.chunk_len[j2], t2 = w.chunk_tok0[j2];
+    if (L2 > 0) {
       const int64_t c2 = (int64_t)j2 * H + h2;
       prefetch_rows(io.q, DK, t2, L2, H, h2);
       prefetch_rows(io.k, DK, t2, L2, H, h2);
