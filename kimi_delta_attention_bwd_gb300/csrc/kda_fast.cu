@@ -577,6 +577,24 @@ __device__ __forceinline__ void store8_rot(const Op& t, int r, int c0, const flo
 #pragma unroll
   for (int p = 0; p < 4; p++) op_store2(t, r, c0 + 2 * ((p + q4) & 3), v[2 * p], v[2 * p + 1]);
 }
+// Adds to g[e] (channel 8 q4 + e of this thread's row) the totals of the rows
+// of the earlier warps (tot: each warp's last-row inclusive sums, [NW][DK]),
+// in warp order: lane c forms channel c's prefix and shuffles hand each
+// thread its eight.
+__device__ __forceinline__ void add_warp_prefix(float (&g)[8], const float* tot, int warp, int lane, int q4) {
+  float pre = 0.f;
+#pragma unroll
+  for (int w2 = 0; w2 < NW - 1; w2++)
+    if (w2 < warp) pre += tot[w2 * DK + lane];
+#pragma unroll
+  for (int e = 0; e < 8; e++) g[e] += __shfl_sync(0xffffffffu, pre, 8 * q4 + e);
+}
+// Row r, channels 8 q4 .. 8 q4 + 7 of a [C][SQ] fp32 array (two 16-byte stores).
+__device__ __forceinline__ void store_row8(float* gg, int r, int q4, const float (&g)[8]) {
+  float4* p = reinterpret_cast<float4*>(gg + r * SQ + 8 * q4);
+  p[0] = make_float4(g[0], g[1], g[2], g[3]);
+  p[1] = make_float4(g[4], g[5], g[6], g[7]);
+}
 // Thread tid < L prefetches row tid of a [tokens][H][n] bf16 tensor (n * 2 <= 128 bytes).
 __device__ __forceinline__ void prefetch_rows(const void* base, int n, int t0, int L, int H, int h) {
   if ((int)threadIdx.x < L) prefetch_l2((const bf16*)base + ((size_t)(t0 + threadIdx.x) * H + h) * n);
@@ -725,13 +743,8 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
   __syncthreads();
   tc::fence_after();
   const uint32_t tb = sm.tslot;
-#pragma unroll
-  for (int e = 0; e < 8; e++) {
-    float off = 0.f;
-    for (int w2 = 0; w2 < warp; w2++) off += sm.tot[w2 * DK + 8 * q4 + e];
-    gv[e] += off;
-    sm.gg[r * SQ + 8 * q4 + e] = gv[e];
-  }
+  add_warp_prefix(gv, sm.tot, warp, lane, q4);
+  store_row8(sm.gg, r, q4, gv);
   __syncthreads();
 
   // ---- factors: LQ, LK, R (decay-ratio operands), XK, XV; QG and KD stay in
@@ -1200,6 +1213,12 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   const int gq = lane >> 2, tq = lane & 3;
   int j2, h2;
   const bool pf = ahead_of(d, j, h, j2, h2);
+  const bool gdn = d.gate != 0;
+  const float* dtb = io.dt_bias + h * (gdn ? 1 : DK);
+  float dtv[8];  // dt_bias of this thread's key channels 8 (tid % 4) ..
+#pragma unroll
+  for (int e = 0; e < 8; e++) dtv[e] = dtb[gdn ? 0 : 8 * (tid & 3) + e];
+  const float alog = io.A_log[h];
   const int tag = *w.tag, err = *w.err, L = w.chunk_len[j], t0 = w.chunk_tok0[j];  // one round trip
   const int L2 = pf ? w.chunk_len[j2] : 0, t2 = pf ? w.chunk_tok0[j2] : 0;
   if (tag != d.tag) {
@@ -1209,9 +1228,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   if (err != 0 || L <= 0) return;
   const int H = d.H;
   const int64_t ch = (int64_t)j * H + h;
-  const float a = expf(io.A_log[h]), scale = d.scale;
-  const bool gdn = d.gate != 0;
-  const float* dtb = io.dt_bias + h * (gdn ? 1 : DK);
+  const float a = expf(alog), scale = d.scale;
   bf16* wk = sm.wk;
   // work-area regions (bf16 offsets): dO 0 | S 4096 | dS' 8192 | P -> E 12288 |
   // W -> dW -> YW 20480 | U -> dE -> YU 24576 | raw f -> KD 32768 | T 36864;
@@ -1281,13 +1298,14 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   const int r = tid >> 2, q4 = tid & 3;
   const bool in = r < L;
   uint4 vraw[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
-  float braw = 0.f;
+  float braw = 0.f, fs = 0.f;  // fs: the scalar gate input of this row
   if (in) {
     const size_t row = (size_t)(t0 + r) * H + h;
     const uint4* vp = reinterpret_cast<const uint4*>((const bf16*)io.v + row * DV + 16 * q4);
     vraw[0] = __ldg(vp);
     vraw[1] = __ldg(vp + 1);
     braw = bfl(((const bf16*)io.b)[row]);
+    if (gdn) fs = bfl(((const bf16*)io.f)[row]);
   }
   asm volatile("cp.async.wait_group 1;\n" ::);
   tc::fence_before();
@@ -1298,13 +1316,13 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   if (in) {
     unpack8(*reinterpret_cast<const uint4*>(sm.rk + r * DK + 8 * q4), kv);
     if (gdn) {
-      const float g = -a * LOG2E * softplus_f(bfl(((const bf16*)io.f)[(size_t)(t0 + r) * H + h]) + dtb[0]);
+      const float g = -a * LOG2E * softplus_f(fs + dtv[0]);
 #pragma unroll
       for (int e = 0; e < 8; e++) gv[e] = g;
     } else {
       unpack8(*reinterpret_cast<const uint4*>(fst + r * DK + 8 * q4), gv);
 #pragma unroll
-      for (int e = 0; e < 8; e++) gv[e] = -a * LOG2E * softplus_f(gv[e] + dtb[8 * q4 + e]);
+      for (int e = 0; e < 8; e++) gv[e] = -a * LOG2E * softplus_f(gv[e] + dtv[e]);
     }
   } else {
 #pragma unroll
@@ -1338,13 +1356,8 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
 #pragma unroll
     for (int e = 0; e < 8; e++) sm.tot[warp * DK + 8 * q4 + e] = gv[e];
   __syncthreads();
-#pragma unroll
-  for (int e = 0; e < 8; e++) {
-    float off = 0.f;
-    for (int w2 = 0; w2 < warp; w2++) off += sm.tot[w2 * DK + 8 * q4 + e];
-    gv[e] += off;
-    sm.gg[r * SQ + 8 * q4 + e] = gv[e];
-  }
+  add_warp_prefix(gv, sm.tot, warp, lane, q4);
+  store_row8(sm.gg, r, q4, gv);
   __syncthreads();
   float xkg[8];  // k^ e^G for the W term of dbeta
 #pragma unroll
@@ -1614,6 +1627,13 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
   const int gq = lane >> 2, tq = lane & 3;
   int j2, h2;
   const bool pf = ahead_of(d, j, h, j2, h2);
+  const bool gdn = d.gate != 0;
+  const float* dtb = io.dt_bias + h * (gdn ? 1 : DK);
+  float dtv[8];  // dt_bias of key channels 8 (tid % 4) .. (the prologue's rows)
+#pragma unroll
+  for (int e = 0; e < 8; e++) dtv[e] = dtb[gdn ? 0 : 8 * (tid & 3) + e];
+  const float dtl = dtb[gdn ? 0 : lane];  // and of channel `lane` (the gate step)
+  const float alog = io.A_log[h];
   const int tag = *w.tag, err = *w.err, L = w.chunk_len[j], t0 = w.chunk_tok0[j];  // one round trip
   const int L2 = pf ? w.chunk_len[j2] : 0, t2 = pf ? w.chunk_tok0[j2] : 0;
   if (tag != d.tag) {
@@ -1623,9 +1643,7 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
   if (err != 0 || L <= 0) return;
   const int H = d.H;
   const int64_t ch = (int64_t)j * H + h;
-  const float a = expf(io.A_log[h]);
-  const bool gdn = d.gate != 0;
-  const float* dtb = io.dt_bias + h * (gdn ? 1 : DK);
+  const float a = expf(alog);
   const bf16* fsc = (const bf16*)io.f + h;  // scalar gate: f of this head, stride H
 
   {
@@ -1680,10 +1698,10 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
     unpack8(*reinterpret_cast<const uint4*>(sm.rf + r * DK + 8 * q4), gv);
     const bool in = r < L;
     float sq = 0.f, sk = 0.f;
-    const float gs = in && gdn ? -a * LOG2E * softplus_f(bfl(fsc[(size_t)(t0 + r) * H]) + dtb[0]) : 0.f;
+    const float gs = in && gdn ? -a * LOG2E * softplus_f(bfl(fsc[(size_t)(t0 + r) * H]) + dtv[0]) : 0.f;
 #pragma unroll
     for (int e = 0; e < 8; e++) {
-      gv[e] = !in ? 0.f : gdn ? gs : -a * LOG2E * softplus_f(gv[e] + dtb[8 * q4 + e]);
+      gv[e] = !in ? 0.f : gdn ? gs : -a * LOG2E * softplus_f(gv[e] + dtv[e]);
       sq += qv[e] * qv[e];
       sk += kv[e] * kv[e];
     }
@@ -1710,13 +1728,8 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
       for (int e = 0; e < 8; e++) sm.tot[warp * DK + 8 * q4 + e] = gv[e];
     __syncthreads();
     bool wide = false;
-#pragma unroll
-    for (int e = 0; e < 8; e++) {
-      float off = 0.f;
-      for (int w2 = 0; w2 < warp; w2++) off += sm.tot[w2 * DK + 8 * q4 + e];
-      gv[e] += off;
-      sm.gg[r * SQ + 8 * q4 + e] = gv[e];
-    }
+    add_warp_prefix(gv, sm.tot, warp, lane, q4);
+    store_row8(sm.gg, r, q4, gv);
     __syncthreads();
     const int I0 = r >> 4;
 #pragma unroll
@@ -1841,6 +1854,7 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
   //      dg_t = sum_{r >= t} (dG_r - kdt_r) + sum_r kdt_r + dgamma gamma
   {
     float run = 0.f;
+#pragma unroll
     for (int m = 7; m >= 0; m--) {
       const int rr = 8 * warp + m;
       run += dgs[rr * SQ + lane];
@@ -1852,14 +1866,17 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
   {
     float off = sm.dgam[lane] * sm.gam[lane];
     for (int i4 = 0; i4 < 4; i4++) off += sm.ks[i4 * DK + lane];
-    for (int w2 = warp + 1; w2 < NW; w2++) off += sm.tot[w2 * DK + lane];
+#pragma unroll
+    for (int w2 = 1; w2 < NW; w2++)
+      if (w2 > warp) off += sm.tot[w2 * DK + lane];
     bf16* dfo = (bf16*)io.df;
     float pdt = 0.f, pA = 0.f;
+#pragma unroll
     for (int m = 0; m < 8; m++) {
       const int rr = 8 * warp + m;
       if (rr < L) {  // uniform over the warp
         const float dg = dgs[rr * SQ + lane] + off;
-        const float x = gdn ? bfl(fsc[(size_t)(t0 + rr) * H]) + dtb[0] : bfl(sm.rf[rr * DK + lane]) + dtb[lane];
+        const float x = (gdn ? bfl(fsc[(size_t)(t0 + rr) * H]) : bfl(sm.rf[rr * DK + lane])) + dtl;
         const float g = -a * softplus_f(x);
         const float dx = dg * (-a) * sigmoid_f(x);
         if (gdn) {  // the scalar gate feeds every channel: its gradient is the channel sum
