@@ -114,13 +114,13 @@ __device__ void prologue(const Intra& c, const bf16* st, int L, float a, const f
     unpack8(*reinterpret_cast<const uint4*>(st + r * DK + 8 * q4), qv);
     unpack8(*reinterpret_cast<const uint4*>(st + C * DK + r * DK + 8 * q4), kv);
     if (fg) {
-      const float g = -a * softplus_f(bfl(fg[(size_t)(t0 + r) * H]) + dtb[0]);
+      const float g = -a * softplus_fast(bfl(fg[(size_t)(t0 + r) * H]) + dtb[0]);
 #pragma unroll
       for (int e = 0; e < 8; e++) gv[e] = g;
     } else {
       unpack8(*reinterpret_cast<const uint4*>(st + 2 * C * DK + r * DK + 8 * q4), gv);
 #pragma unroll
-      for (int e = 0; e < 8; e++) gv[e] = -a * softplus_f(gv[e] + dtb[8 * q4 + e]);
+      for (int e = 0; e < 8; e++) gv[e] = -a * softplus_fast(gv[e] + dtb[8 * q4 + e]);
     }
     vraw[0] = *reinterpret_cast<const uint4*>(st + 3 * C * DK + r * DV + 16 * q4);
     vraw[1] = *reinterpret_cast<const uint4*>(st + 3 * C * DK + r * DV + 16 * q4 + 8);
@@ -140,7 +140,7 @@ __device__ void prologue(const Intra& c, const bf16* st, int L, float a, const f
   if (q4 == 0) {
     c.inq[r] = iq;
     c.ink[r] = ik;
-    c.bet[r] = in ? sigmoid_f(c.braw[r]) : 0.f;
+    c.bet[r] = in ? sigmoid_fast(c.braw[r]) : 0.f;
   }
 #pragma unroll
   for (int e = 0; e < 8; e++) {
@@ -241,7 +241,7 @@ __device__ __forceinline__ float pair_exact(const bf16* X, float ix, const bf16*
 __device__ __forceinline__ float pair_exact2(const bf16* X, float ix, const bf16* Kr, float ik, const float* Gr,
                                              const float* Gs) {
   float acc = 0.f;
-  for (int i = 0; i < DK; i++) acc += (bfl(X[i]) * ix) * (bfl(Kr[i]) * ik) * exp2f(Gr[i] - Gs[i]);
+  for (int i = 0; i < DK; i++) acc += (bfl(X[i]) * ix) * (bfl(Kr[i]) * ik) * ex2(Gr[i] - Gs[i]);
   return acc;
 }
 
@@ -525,6 +525,128 @@ __global__ void __launch_bounds__(NTH, 1) fwd_chain_kernel(Dims d, FwdIO io, Ws 
 // for the 16 (I + 1) rows s of blocks J <= I, stacked from row 8 I (I + 1).
 __device__ __forceinline__ int roff(int I) { return 8 * I * (I + 1); }
 
+// ---- fwd_chunk's solve, T = (I + A)^-1, by merging block inverses: a
+// unit-lower [[I + A_a, 0], [A_ba, I + A_b]] has the inverse
+// [[T_a, 0], [-T_b A_ba T_a, T_b]].  The four 16 x 16 diagonal inverses come
+// from forward substitution (one warp each, inside the A / P step), merge into
+// the two 32 x 32 ones and those into T: four rounds of small products instead
+// of a row-by-row sweep.
+
+// Diagonal inverse I is kept in an upper block of the A array (never written
+// by the A / P step): (0, 1), (0, 2), (0, 3), (1, 3).
+__device__ __forceinline__ int tdoff(int I) { return I < 3 ? 16 * (I + 1) : 16 * SC + 48; }
+
+// Forward substitution of diagonal block I of A (beta-scaled, fp32, stride
+// SC) by one warp, lane c % 16 owning column c; T_II to td (stride SC).
+__device__ __forceinline__ void diag_inverse(const float* am, float* td, int I) {
+  const int lane = threadIdx.x & 31, cidx = lane & 15;
+  const float* Ab = am + (16 * I) * SC + 16 * I;
+  float tc[16];
+#pragma unroll
+  for (int r = 0; r < 16; r++) {
+    float v0 = (r == cidx) ? 1.f : 0.f, v1 = 0.f;
+#pragma unroll
+    for (int s = 0; s + 1 < r; s += 2) {
+      v0 = fmaf(-Ab[r * SC + s], tc[s], v0);
+      v1 = fmaf(-Ab[r * SC + s + 1], tc[s + 1], v1);
+    }
+    if (r & 1) v0 = fmaf(-Ab[r * SC + r - 1], tc[r - 1], v0);
+    tc[r] = v0 + v1;
+  }
+  if (lane < 16)
+#pragma unroll
+    for (int r = 0; r < 16; r++) td[r * SC + cidx] = tc[r];
+}
+
+// acc (a 16 x 8 m16n8 fragment) = sum over k < 8 KS of fl(m, k) fr(k, n) in
+// split tf32 (hi*hi + hi*lo + lo*hi, about 21 bits); all operand loads are
+// issued before the products.
+template <int KS, class FL, class FR>
+__device__ __forceinline__ void tile_tf32(float (&acc)[4], FL fl, FR fr) {
+  const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
+  uint32_t ah[KS][4], al[KS][4], bh[KS][2], bl[KS][2];
+#pragma unroll
+  for (int ks = 0; ks < KS; ks++) {
+    const int kk = 8 * ks + tq;
+    split_tf32(fl(gq, kk), ah[ks][0], al[ks][0]);
+    split_tf32(fl(gq + 8, kk), ah[ks][1], al[ks][1]);
+    split_tf32(fl(gq, kk + 4), ah[ks][2], al[ks][2]);
+    split_tf32(fl(gq + 8, kk + 4), ah[ks][3], al[ks][3]);
+    split_tf32(fr(kk, gq), bh[ks][0], bl[ks][0]);
+    split_tf32(fr(kk + 4, gq), bh[ks][1], bl[ks][1]);
+  }
+  acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < KS; ks++) {
+    mma_tf32(acc, ah[ks][0], ah[ks][1], ah[ks][2], ah[ks][3], bh[ks][0], bh[ks][1]);
+    mma_tf32(acc, ah[ks][0], ah[ks][1], ah[ks][2], ah[ks][3], bl[ks][0], bl[ks][1]);
+    mma_tf32(acc, al[ks][0], al[ks][1], al[ks][2], al[ks][3], bh[ks][0], bh[ks][1]);
+  }
+}
+template <class F>
+__device__ __forceinline__ void tile_store(const float (&acc)[4], F fn) {
+  const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
+  fn(gq, 2 * tq, acc[0]);
+  fn(gq, 2 * tq + 1, acc[1]);
+  fn(gq + 8, 2 * tq, acc[2]);
+  fn(gq + 8, 2 * tq + 1, acc[3]);
+}
+
+constexpr int YS = 40;  // row stride of the merge scratch [32][YS]
+
+// The merges after the diagonal inverses (in the td blocks of am): T's lower
+// blocks assembled in tm (fp32, stride SC); yy is scratch.  Ends with a barrier.
+__device__ void solve_merge(const float* am, float* tm, float* yy) {
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (warp < 4) {  // X_10 = A_10 T_00 and X_32 = A_32 T_22
+    const int p = warp >> 1, n0 = 8 * (warp & 1);
+    const float* Al = am + (16 + 32 * p) * SC + 32 * p;
+    const float* Tr = am + tdoff(2 * p) + n0;
+    float acc[4];
+    tile_tf32<2>(acc, [&](int m, int k) { return Al[m * SC + k]; }, [&](int k, int n) { return Tr[k * SC + n]; });
+    tile_store(acc, [&](int m, int n, float v) { yy[(16 * p + m) * YS + n0 + n] = v; });
+  } else {  // the diagonal inverses into T
+    for (int idx = tid - 128; idx < 4 * 256; idx += 128) {
+      const int I = idx >> 8, r = (idx >> 4) & 15, c = idx & 15;
+      tm[(16 * I + r) * SC + 16 * I + c] = am[tdoff(I) + r * SC + c];
+    }
+  }
+  __syncthreads();
+  if (warp < 4) {  // T_10 = -T_11 X_10 and T_32 = -T_33 X_32
+    const int p = warp >> 1, n0 = 8 * (warp & 1);
+    const float* Tl = am + tdoff(2 * p + 1);
+    float acc[4];
+    tile_tf32<2>(acc, [&](int m, int k) { return Tl[m * SC + k]; },
+                 [&](int k, int n) { return yy[(16 * p + k) * YS + n0 + n]; });
+    float* out = tm + (16 + 32 * p) * SC + 32 * p + n0;
+    tile_store(acc, [&](int m, int n, float v) { out[m * SC + n] = -v; });
+  }
+  __syncthreads();
+  const int rb = warp >> 2, n0 = 8 * (warp & 3);  // one 16 x 8 tile of a 32 x 32 block per warp
+  {  // Y = A[32.., ..32) T[..32, ..32): columns 16.. of the lower T need k >= 16 only
+    const float* Al = am + (32 + 16 * rb) * SC;
+    float acc[4];
+    if (n0 < 16)
+      tile_tf32<4>(acc, [&](int m, int k) { return Al[m * SC + k]; }, [&](int k, int n) { return tm[k * SC + n0 + n]; });
+    else
+      tile_tf32<2>(acc, [&](int m, int k) { return Al[m * SC + 16 + k]; },
+                   [&](int k, int n) { return tm[(16 + k) * SC + n0 + n]; });
+    tile_store(acc, [&](int m, int n, float v) { yy[(16 * rb + m) * YS + n0 + n] = v; });
+  }
+  __syncthreads();
+  {  // T[32.., ..32) = -T[32.., 32..) Y: rows 32..47 of the lower T need k < 16 only
+    const float* Tl = tm + (32 + 16 * rb) * SC + 32;
+    float acc[4];
+    if (rb == 0)
+      tile_tf32<2>(acc, [&](int m, int k) { return Tl[m * SC + k]; }, [&](int k, int n) { return yy[k * YS + n0 + n]; });
+    else
+      tile_tf32<4>(acc, [&](int m, int k) { return Tl[m * SC + k]; }, [&](int k, int n) { return yy[k * YS + n0 + n]; });
+    float* out = tm + (32 + 16 * rb) * SC + n0;
+    tile_store(acc, [&](int m, int n, float v) { out[m * SC + n] = -v; });
+  }
+  __syncthreads();
+}
+
 // Shared memory of fwd_chunk (about 104 KB: two CTAs per SM).  bf16 arrays
 // are split operand tiles; regions are reused as noted.
 struct ChunkSm {
@@ -670,7 +792,8 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
   bf16* qgb = reinterpret_cast<bf16*>(sm.gg);
   const Op QG{qgb, qgb + C * DK, DK};
   float* tm = reinterpret_cast<float*>(sm.x);  // [C][SC]
-  float* yy = tm + C * SC;                     // [16][C]
+  float* yy = tm + C * SC;                     // [32][YS], below KD
+  static_assert((C * SC + 32 * YS) * 4 <= 14336 * 2, "solve scratch overlaps KD");
 
   // ---- prologue in registers: thread = row r (tid / 4), key channels 8 (tid % 4) ..,
   //      value columns 16 (tid % 4) ..; rows >= L are zero with G flat
@@ -687,12 +810,12 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     unpack8(__ldg(vp + 1), vv + 8);
     braw = bfl(((const bf16*)io.b)[row]);
     if (gdn) {
-      const float g = -a * LOG2E * softplus_f(bfl(((const bf16*)io.f)[row]) + dtb[0]);
+      const float g = -a * LOG2E * softplus_fast(bfl(((const bf16*)io.f)[row]) + dtb[0]);
 #pragma unroll
       for (int e = 0; e < 8; e++) gv[e] = g;
     } else {
 #pragma unroll
-      for (int e = 0; e < 8; e++) gv[e] = -a * LOG2E * softplus_f(gv[e] + dtb[8 * q4 + e]);
+      for (int e = 0; e < 8; e++) gv[e] = -a * LOG2E * softplus_fast(gv[e] + dtb[8 * q4 + e]);
     }
   } else {
 #pragma unroll
@@ -709,7 +832,7 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
   sk += __shfl_xor_sync(0xffffffffu, sk, 1);
   sk += __shfl_xor_sync(0xffffffffu, sk, 2);
   const float iq = 1.0f / sqrtf(sq + L2_EPS), ik = 1.0f / sqrtf(sk + L2_EPS);
-  const float beta = in ? sigmoid_f(braw) : 0.f;
+  const float beta = in ? sigmoid_fast(braw) : 0.f;
   if (q4 == 0) {
     sm.bet[r] = beta;
     sm.inq[r] = iq;
@@ -757,11 +880,11 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     for (int e = 0; e < 8; e++) {
       gbv[e] = sm.gg[(16 * I) * SQ + 8 * q4 + e];
       const float gl = sm.gg[(L - 1) * SQ + 8 * q4 + e];
-      const float eG = exp2f(gv[e]);
+      const float eG = ex2(gv[e]);
       qg[e] = scale * qv[e] * eG;
-      kd[e] = kv[e] * exp2f(gl - gv[e]);
+      kd[e] = kv[e] * ex2(gl - gv[e]);
       xk[e] = beta * kv[e] * eG;
-      if (r == 0) sm.gam[8 * q4 + e] = exp2f(gl);
+      if (r == 0) sm.gam[8 * q4 + e] = ex2(gl);
       wide |= (r & 15) == 15 && gbv[e] - gv[e] > SPAN2;
     }
     if (wide) sm.spanok[I] = 0;
@@ -769,7 +892,7 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
       float lq[8], lk[8];
 #pragma unroll
       for (int e = 0; e < 8; e++) {
-        const float l = exp2f(gv[e] - gbv[e]);
+        const float l = ex2(gv[e] - gbv[e]);
         lq[e] = qv[e] * l;
         lk[e] = kv[e] * l;
       }
@@ -785,7 +908,7 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     for (int I2 = I; I2 < 4; I2++) {
       float rv[8];
 #pragma unroll
-      for (int e = 0; e < 8; e++) rv[e] = kv[e] * exp2f(fminf(sm.gg[(16 * I2) * SQ + 8 * q4 + e] - gv[e], SPAN2));
+      for (int e = 0; e < 8; e++) rv[e] = kv[e] * ex2(fminf(sm.gg[(16 * I2) * SQ + 8 * q4 + e] - gv[e], SPAN2));
       rot_pairs(rv, q4);
       store8_rot(R, roff(I2) + r, 8 * q4, rv, q4);
     }
@@ -794,8 +917,18 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
 
   // ---- A (beta_r-scaled, strict lower, fp32) and P (scale, inclusive lower, split):
   //      20 block tasks; a diagonal block whose decay span exceeds 80 is exact
+  //      tasks 4..7 (warps 4..7) are the diagonal A blocks, which their warp then inverts
   for (int task = warp; task < 20; task += NW) {
-    const int blk = task >> 1, isP = task & 1;
+    int blk, isP;
+    if (task >= 4 && task < 8) {
+      blk = (task - 4) * (task - 1) / 2;  // block (I, I), I = task - 4
+      isP = 0;
+    } else {
+      const int u = task < 4 ? task : task - 4;  // P blocks 0..9, then A blocks 1, 3, 4, 6, 7, 8
+      const int i = u - 10;
+      isP = u < 10;
+      blk = isP ? u : i < 2 ? 2 * i + 1 : i < 3 ? 4 : i + 3;
+    }
     const int bI = blk < 1 ? 0 : blk < 3 ? 1 : blk < 6 ? 2 : 3, bJ = blk - bI * (bI + 1) / 2;
     float acc[2][4];
     zero(acc);
@@ -829,6 +962,10 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
       });
     }
   }
+  if (warp >= 4) {  // the diagonal A block this warp computed first
+    __syncwarp();
+    diag_inverse(sm.am, sm.am + tdoff(warp - 4), warp - 4);
+  }
   zero_upper(P);  // the tensor core reads whole tiles
   fence_async_smem();
   __syncthreads();
@@ -839,7 +976,7 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
   // QG over G, KD in the tail of the x region (both free now)
   store8_rot(QG, r, 8 * q4, qg, q4);  // rotated in the factors step
   store8_rot(KD, r, 8 * q4, kd, q4);
-  solve<true>(sm.am, tm, yy, sm.bet);
+  solve_merge(sm.am, tm, yy);
   for (int idx = tid; idx < C * C / 2; idx += NTH) {  // T -> split operand over A (upper blocks zero)
     const int core = idx >> 5, ln = idx & 31;  // a warp writes one whole core matrix
     const int rr = 8 * (core >> 3) + (ln >> 2), s2 = 8 * (core & 7) + 2 * (ln & 3);
@@ -1316,13 +1453,13 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   if (in) {
     unpack8(*reinterpret_cast<const uint4*>(sm.rk + r * DK + 8 * q4), kv);
     if (gdn) {
-      const float g = -a * LOG2E * softplus_f(fs + dtv[0]);
+      const float g = -a * LOG2E * softplus_fast(fs + dtv[0]);
 #pragma unroll
       for (int e = 0; e < 8; e++) gv[e] = g;
     } else {
       unpack8(*reinterpret_cast<const uint4*>(fst + r * DK + 8 * q4), gv);
 #pragma unroll
-      for (int e = 0; e < 8; e++) gv[e] = -a * LOG2E * softplus_f(gv[e] + dtv[e]);
+      for (int e = 0; e < 8; e++) gv[e] = -a * LOG2E * softplus_fast(gv[e] + dtv[e]);
     }
   } else {
 #pragma unroll
@@ -1339,7 +1476,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
     for (int e = 0; e < 8; e++) kv[e] *= ik;
   }
   if (q4 == 0) {
-    sm.bet[r] = in ? sigmoid_f(braw) : 0.f;
+    sm.bet[r] = in ? sigmoid_fast(braw) : 0.f;
     sm.braw[r] = braw;
   }
 #pragma unroll
@@ -1364,9 +1501,9 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   for (int e = 0; e < 8; e += 2) {
     const int i = 8 * q4 + e;
     const float gl0 = sm.gg[(L - 1) * SQ + i], gl1 = sm.gg[(L - 1) * SQ + i + 1];
-    op_store2(KD, r, i, kv[e] * exp2f(gl0 - gv[e]), kv[e + 1] * exp2f(gl1 - gv[e + 1]));
-    xkg[e] = kv[e] * exp2f(gv[e]);
-    xkg[e + 1] = kv[e + 1] * exp2f(gv[e + 1]);
+    op_store2(KD, r, i, kv[e] * ex2(gl0 - gv[e]), kv[e + 1] * ex2(gl1 - gv[e + 1]));
+    xkg[e] = kv[e] * ex2(gv[e]);
+    xkg[e + 1] = kv[e + 1] * ex2(gv[e + 1]);
   }
   cp_wait_all();
   fence_async_smem();  // KD and dO are read by the tensor core next
@@ -1594,7 +1731,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   if (tid < L) {  // fixed-order sum over the column blocks: deterministic
     float acc = sm.dbet[tid];
     for (int J = 0; J <= (tid >> 4); J++) acc += sm.part[J * C + tid];
-    ((bf16*)io.db)[(size_t)(t0 + tid) * H + h] = __float2bfloat16_rn(acc * sm.bet[tid] * sigmoid_f(-sm.braw[tid]));
+    ((bf16*)io.db)[(size_t)(t0 + tid) * H + h] = __float2bfloat16_rn(acc * sm.bet[tid] * sigmoid_fast(-sm.braw[tid]));
   }
 }
 
@@ -1698,10 +1835,10 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
     unpack8(*reinterpret_cast<const uint4*>(sm.rf + r * DK + 8 * q4), gv);
     const bool in = r < L;
     float sq = 0.f, sk = 0.f;
-    const float gs = in && gdn ? -a * LOG2E * softplus_f(bfl(fsc[(size_t)(t0 + r) * H]) + dtv[0]) : 0.f;
+    const float gs = in && gdn ? -a * LOG2E * softplus_fast(bfl(fsc[(size_t)(t0 + r) * H]) + dtv[0]) : 0.f;
 #pragma unroll
     for (int e = 0; e < 8; e++) {
-      gv[e] = !in ? 0.f : gdn ? gs : -a * LOG2E * softplus_f(gv[e] + dtv[e]);
+      gv[e] = !in ? 0.f : gdn ? gs : -a * LOG2E * softplus_fast(gv[e] + dtv[e]);
       sq += qv[e] * qv[e];
       sk += kv[e] * kv[e];
     }
@@ -1736,7 +1873,7 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
     for (int e = 0; e < 8; e++) {
       const int i = 8 * q4 + e;
       wide |= (r & 15) == 15 && sm.gg[(16 * I0) * SQ + i] - gv[e] > SPAN2;
-      if (r == 0) sm.gam[i] = exp2f(sm.gg[(L - 1) * SQ + i]);
+      if (r == 0) sm.gam[i] = ex2(sm.gg[(L - 1) * SQ + i]);
     }
     if (wide) sm.spanok[I0] = 0;
   }
@@ -1767,7 +1904,7 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
                  [&](int m, int k) { return MAb[m * PB + k]; },
                  [&](int k, int jj, int n) {
                    const int s = 16 * J + k, i = 16 * hk + 8 * jj + n;
-                   return bfl(sm.rk[s * DK + i]) * sm.ink[s] * exp2f(fminf(gbI[i] - sm.gg[s * SQ + i], SPAN2));
+                   return bfl(sm.rk[s * DK + i]) * sm.ink[s] * ex2(fminf(gbI[i] - sm.gg[s * SQ + i], SPAN2));
                  });
   }
   for (int I2 = I; I2 < 4; I2++) {
@@ -1778,7 +1915,7 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
                  [&](int m, int k) { return MAb[k * PB + m]; },
                  [&](int k, int jj, int n) {
                    const int rr = 16 * I2 + k, i = 16 * hk + 8 * jj + n;
-                   const float x = exp2f(fminf(sm.gg[rr * SQ + i] - geI[i], SPAN2));
+                   const float x = ex2(fminf(sm.gg[rr * SQ + i] - geI[i], SPAN2));
                    return make_float2(bfl(sm.rq[rr * DK + i]) * sm.inq[rr] * x, bfl(sm.rk[rr * DK + i]) * sm.ink[rr] * x);
                  });
   }
@@ -1794,25 +1931,25 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
       for (int e = 0; e < 4; e++) {
         const int m = gq + 8 * (e >> 1), rr = 16 * I + m, i = 16 * hk + 8 * jj + 2 * tq + (e & 1);
         const float G = sm.gg[rr * SQ + i];
-        const float eL = exp2f(G - gbI[i]), eR = exp2f(geI[i] - G);
+        const float eL = ex2(G - gbI[i]), eR = ex2(geI[i] - G);
         float pr = prow[jj][e] * eL, ar = arow[jj][e] * eL, cl = col[jj][e] * eR;
         if (!ok) {  // exact diagonal-block terms (rows past the chunk end are zero)
           for (int s = 16 * I; s < 16 * I + 16 && s < L; s++) {
             const int n = s - 16 * I;
             const float ks = bfl(sm.rk[s * DK + i]) * sm.ink[s], qs = bfl(sm.rq[s * DK + i]) * sm.inq[s];
             if (s <= rr) {
-              const float ex = exp2f(G - sm.gg[s * SQ + i]);
+              const float ex = ex2(G - sm.gg[s * SQ + i]);
               pr += DPd[m * PB + n] * ks * ex;
               ar += MAd[m * PB + n] * ks * ex;
             }
             if (s >= rr) {
-              const float ex = exp2f(sm.gg[s * SQ + i] - G);
+              const float ex = ex2(sm.gg[s * SQ + i] - G);
               cl += (DPd[n * PB + m] * qs + MAd[n * PB + m] * ks) * ex;
             }
           }
         }
         const float q = bfl(sm.rq[rr * DK + i]) * sm.inq[rr], k = bfl(sm.rk[rr * DK + i]) * sm.ink[rr];
-        const float Gm = exp2f(G), kdf = exp2f(sm.gg[(L - 1) * SQ + i] - G);
+        const float Gm = ex2(G), kdf = ex2(sm.gg[(L - 1) * SQ + i] - G);
         const float kdt = dKD[jj][e] * k * kdf;
         dqh[jj][e] = pr + dQG[jj][e] * Gm;
         dkh[jj][e] = ar + cl + dkg[jj][e] * Gm + dKD[jj][e] * kdf;
@@ -1877,8 +2014,8 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
       if (rr < L) {  // uniform over the warp
         const float dg = dgs[rr * SQ + lane] + off;
         const float x = (gdn ? bfl(fsc[(size_t)(t0 + rr) * H]) : bfl(sm.rf[rr * DK + lane])) + dtl;
-        const float g = -a * softplus_f(x);
-        const float dx = dg * (-a) * sigmoid_f(x);
+        const float g = -a * softplus_fast(x);
+        const float dx = dg * (-a) * sigmoid_fast(x);
         if (gdn) {  // the scalar gate feeds every channel: its gradient is the channel sum
           const float ds = warp_sum(dx);
           if (lane == 0) dfo[(size_t)(t0 + rr) * H + h] = __float2bfloat16_rn(ds);

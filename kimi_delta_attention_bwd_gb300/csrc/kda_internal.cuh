@@ -151,6 +151,18 @@ __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf
 // ~1e-6): for the streaming epilogue / prologue kernels whose outputs are
 // stored in bf16 or fp32 and need no more.
 __device__ __forceinline__ float sigmoid_fast(float x) { return __frcp_rn(1.0f + __expf(-x)); }
+// Softplus from the same intrinsics (absolute error below 1e-6): for the
+// tensor-core path, where it sets the log-decay g = -exp(A_log) softplus(.)
+// that then enters bf16-split products.
+// 2^x by the hardware approximation (PTX ex2.approx.ftz: relative error about
+// 2^-22; results below 2^-126 flush to zero, far below anything a decay factor
+// contributes next to O(1) values).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float softplus_fast(float x) { return fmaxf(x, 0.0f) + __logf(1.0f + __expf(-fabsf(x))); }
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
