@@ -163,7 +163,7 @@ static Layout layout(const Dims& d, int for_bwd, bool fused = false) {
       L.off_sP = take(4 * nch * C * C);
       L.off_sW = take(4 * nch * C * d.dk);
       L.off_sU = take(4 * nch * C * d.dv);
-      L.off_sA = take(4 * nch * 10 * 256);
+      L.off_sA = take(4 * nch * 10 * 16 * 20);  // A' blocks, rows padded to 20
       L.off_gDP = take(4 * nch * 10 * 16 * 20);
       L.off_gMA = take(4 * nch * 10 * 16 * 20);
       L.off_gQG = take(4 * nch * C * d.dk);

@@ -41,6 +41,8 @@ constexpr int DK = 32, DV = 64;
 constexpr int SQ = DK + 4;  // row stride of [C][DK] operands read along rows
 constexpr int SV = DV + 8;  // row stride of [C][DV] operands
 constexpr int SC = C + 4;   // row stride of [C][C] matrices
+constexpr int NBLK = 10;    // lower 16 x 16 blocks of a C x C matrix, block I (I + 1) / 2 + J
+constexpr int PB = 20;      // row stride of a 16 x 16 fp32 block (shared memory and the hand-over arrays)
 constexpr int NTH = 256, NW = 8;
 constexpr uint32_t TCOLS = 256;  // TMEM columns of a tensor-core CTA (two per SM share the 512)
 constexpr float SPAN_MAX = 80.f;
@@ -958,7 +960,7 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
       each(acc, [&](int m, int n, float& v) {
         const int rr = 16 * bI + m, s = 16 * bJ + n;
         sm.am[rr * SC + s] = s < rr ? sm.bet[rr] * v : 0.f;
-        if (io.save) w.sA[(ch * 10 + blk) * 256 + m * 16 + n] = s < rr ? v : 0.f;  // A' for dbeta
+        if (io.save) w.sA[(ch * NBLK + blk) * 16 * PB + m * PB + n] = s < rr ? v : 0.f;  // A' for dbeta
       });
     }
   }
@@ -1299,8 +1301,6 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
 }
 
 // ------------------------------------------------------------ backward chunk kernels
-constexpr int NBLK = 10;  // lower 16 x 16 blocks of a C x C matrix, block I (I + 1) / 2 + J
-constexpr int PB = 20;    // row stride of a 16 x 16 fp32 block in shared memory
 
 __device__ __forceinline__ void blk_ij(int b, int& I, int& J) {
   I = b < 1 ? 0 : b < 3 ? 1 : b < 6 ? 2 : 3;
@@ -1376,7 +1376,6 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   const Op KD{wk + 32768, wk + 34816, DK}, T{wk + 36864, wk + 40960, C};
   const Op dW = W, YW = W, dE = U, YU = U;
   const Op U2{wk, wk + 4096, DV}, W2{wk + 8192, wk + 10240, DK};
-  const float* A2 = reinterpret_cast<const float*>(wk + 12288);
   bf16* fst = wk + 32768;
 
   // ---- group 1: raw k, f;  group 2: dO, S, dS', P, W, U, T
@@ -1425,7 +1424,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
         bulk_prefetch_l2(w.sW + c2 * 2 * C * DK, 4 * C * DK);
         bulk_prefetch_l2(w.sU + c2 * 2 * C * DV, 4 * C * DV);
         bulk_prefetch_l2(w.sT + c2 * 2 * C * C, 4 * C * C);
-        bulk_prefetch_l2(w.sA + c2 * NBLK * 256, NBLK * 256 * 4);
+        bulk_prefetch_l2(w.sA + c2 * NBLK * 16 * PB, NBLK * 16 * PB * 4);
       }
     }
   }
@@ -1570,20 +1569,24 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
     tc::gemm_split(tb + 0, tc::kmaj(dO), tc::kmaj(E), 64, DV / 16, false);
     tc::commit(&sm.bar[2]);
   }
-  {  // dgamma_i = sum_j dS'_ij S_ij: thread = row tid / 8, columns 8 (tid % 8) ..
-    const int i = tid >> 3, c8 = 8 * (tid & 7), o = opix(i, c8, DV);
-    float x[8], y[8], xl[8], yl[8];
-    unpack8(*reinterpret_cast<const uint4*>(dS.hi + o), x);
-    unpack8(*reinterpret_cast<const uint4*>(dS.lo + o), xl);
-    unpack8(*reinterpret_cast<const uint4*>(S.hi + o), y);
-    unpack8(*reinterpret_cast<const uint4*>(S.lo + o), yl);
+  if (warp < 4) {  // dgamma_i = sum_j dS'_ij S_ij: lane = row i % 8 x column chunks (lane / 8, + 4); a
+                    // quarter-warp reads whole core matrices
+    const int i = 8 * warp + (lane & 7);
     float acc1 = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; e++) acc1 += (x[e] + xl[e]) * (y[e] + yl[e]);
-    acc1 += __shfl_xor_sync(0xffffffffu, acc1, 1);
-    acc1 += __shfl_xor_sync(0xffffffffu, acc1, 2);
-    acc1 += __shfl_xor_sync(0xffffffffu, acc1, 4);
-    if ((tid & 7) == 0) w.gdg[ch * DK + i] = acc1;
+    for (int hc = 0; hc < 2; hc++) {
+      const int o = opix(i, 8 * ((lane >> 3) + 4 * hc), DV);
+      float x[8], y[8], xl[8], yl[8];
+      unpack8(*reinterpret_cast<const uint4*>(dS.hi + o), x);
+      unpack8(*reinterpret_cast<const uint4*>(dS.lo + o), xl);
+      unpack8(*reinterpret_cast<const uint4*>(S.hi + o), y);
+      unpack8(*reinterpret_cast<const uint4*>(S.lo + o), yl);
+#pragma unroll
+      for (int e = 0; e < 8; e++) acc1 += (x[e] + xl[e]) * (y[e] + yl[e]);
+    }
+    acc1 += __shfl_xor_sync(0xffffffffu, acc1, 8);
+    acc1 += __shfl_xor_sync(0xffffffffu, acc1, 16);
+    if (lane < 8) w.gdg[ch * DK + i] = acc1;
   }
   if (!round_done()) { bail(); return; }
   {
@@ -1623,10 +1626,10 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   // ---- U, W, A' for the dA products (bulk, over dO, S, dS', E: all read by now);
   //      YU = T^T dE, YW = T^T dW
   if (tid == 0) {
-    mbar_expect_tx(&sm.bar[1], 4 * C * DV + 4 * C * DK + NBLK * 256 * 4);
+    mbar_expect_tx(&sm.bar[1], 4 * C * DV + 4 * C * DK + NBLK * 16 * PB * 4);
     bulk_g2s(U2.hi, w.sU + ch * 2 * C * DV, 4 * C * DV, &sm.bar[1]);
     bulk_g2s(W2.hi, w.sW + ch * 2 * C * DK, 4 * C * DK, &sm.bar[1]);
-    bulk_g2s(wk + 12288, w.sA + ch * NBLK * 256, NBLK * 256 * 4, &sm.bar[1]);
+    bulk_g2s(wk + 12288, w.sA + ch * NBLK * 16 * PB, NBLK * 16 * PB * 4, &sm.bar[1]);
     tc::fence_after();
     tc::gemm_split(tb + 64, tc::mnmaj(T), tc::mnmaj(dE), 64, C / 16, false);
     tc::gemm_split(tb + 224, tc::mnmaj(T), tc::mnmaj(dW), 32, C / 16, false);
@@ -1676,15 +1679,27 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
     tc::gemm_split(tb + 128, tc::kmaj(YW), tc::kmaj(W2), 64, DK / 16, true);
     tc::commit(&sm.bar[2]);
   }
-  {
-    float vv[16];
-    unpack8(vraw[0], vv);
-    unpack8(vraw[1], vv + 8);
+  {  // bf16 pairs read in the rotated order of store8_rot: the 32 lanes hit 32 banks
+    float va[8], vb[8];
+    unpack8(vraw[0], va);
+    unpack8(vraw[1], vb);
+    rot_pairs(va, q4);
+    rot_pairs(vb, q4);
+    rot_pairs(xkg, q4);
+    auto pair = [&](const Op& t, int c) {
+      const int i = opix(r, c, t.K);
+      const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(t.hi + i));
+      const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(t.lo + i));
+      return make_float2(hi.x + lo.x, hi.y + lo.y);
+    };
     float acc = 0.f;
 #pragma unroll
-    for (int e = 0; e < 16; e++) acc += op_get(YU, r, 16 * q4 + e) * vv[e];
-#pragma unroll
-    for (int e = 0; e < 8; e++) acc += op_get(YW, r, 8 * q4 + e) * xkg[e];
+    for (int p = 0; p < 4; p++) {
+      const int c2 = 2 * ((p + q4) & 3);
+      const float2 u0 = pair(YU, 16 * q4 + c2), u1 = pair(YU, 16 * q4 + 8 + c2), y = pair(YW, 8 * q4 + c2);
+      acc += u0.x * va[2 * p] + u0.y * va[2 * p + 1] + u1.x * vb[2 * p] + u1.y * vb[2 * p + 1];
+      acc += y.x * xkg[2 * p] + y.y * xkg[2 * p + 1];
+    }
     acc += __shfl_xor_sync(0xffffffffu, acc, 1);
     acc += __shfl_xor_sync(0xffffffffu, acc, 2);
     if (q4 == 0) sm.dbet[r] = acc;
@@ -1701,7 +1716,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
       if (J <= I) {
         const int t = blk_of(I, J);
         float* g = w.gMA + (ch * NBLK + t) * 16 * PB;
-        const float* ab = A2 + t * 256;
+        const float* ab = A2 + t * 16 * PB;
 #pragma unroll
         for (int jt = 0; jt < 2; jt++)
 #pragma unroll
@@ -1710,7 +1725,8 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
             const int rr = 16 * I + m, s0 = 16 * J + n;
             const float* v = aa[2 * jb + jt];
             const float da0 = s0 < rr ? -v[2 * hh] : 0.f, da1 = s0 + 1 < rr ? -v[2 * hh + 1] : 0.f;
-            const float pa = da0 * ab[m * 16 + n] + da1 * ab[m * 16 + n + 1];
+            const float2 a2 = *reinterpret_cast<const float2*>(ab + m * PB + n);
+            const float pa = da0 * a2.x + da1 * a2.y;
             if (hh == 0) rs0 += pa; else rs1 += pa;
             *reinterpret_cast<float2*>(g + m * PB + n) = make_float2(sm.bet[rr] * da0, sm.bet[rr] * da1);
           }
