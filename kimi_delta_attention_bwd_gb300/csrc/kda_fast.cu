@@ -1765,12 +1765,20 @@ struct GateSm {
   float inq[C], ink[C];
   float gam[DK], dgam[DK];
   float tot[NW * DK], ks[4 * DK], part[NW * DK], red[NW];
+  // operand tiles of the pairwise terms, [C][DK] with columns swizzled by tix:
+  // kl = k^ 2^(G_last(I) - G), qf / kf = q^ / k^ 2^(G - G_first(I)) over the
+  // row's 16-row block I (each at most |q^|, |k^|)
+  float kl[C * DK], qf[C * DK], kf[C * DK];
   int spanok[4];
   uint64_t bar;  // bulk-load completion of dP' and MA
 };
+// Element (r, c) of a swizzled [C][DK] tile: the four rows r = 0..3 (mod 4) of
+// a fragment load put their eight columns in different bank groups.
+__device__ __forceinline__ int tix(int r, int c) { return r * DK + (c ^ ((r & 3) << 3)); }
 
 static_assert(offsetof(GateSm, rq) % 16 == 0 && offsetof(GateSm, rk) % 16 == 0 && offsetof(GateSm, rf) % 16 == 0 &&
-                  offsetof(GateSm, dp) % 16 == 0 && offsetof(GateSm, ma) % 16 == 0,
+                  offsetof(GateSm, dp) % 16 == 0 && offsetof(GateSm, ma) % 16 == 0 && offsetof(GateSm, kl) % 16 == 0 &&
+                  offsetof(GateSm, qf) % 16 == 0 && offsetof(GateSm, kf) % 16 == 0,
               "vector-accessed arrays");
 
 __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w) {
@@ -1892,11 +1900,27 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
       if (r == 0) sm.gam[i] = ex2(sm.gg[(L - 1) * SQ + i]);
     }
     if (wide) sm.spanok[I0] = 0;
+    {  // the pairwise operand tiles of this row
+      const float iq = sm.inq[r], ik = sm.ink[r];
+      const float* gbr = sm.gg + (16 * I0) * SQ + 8 * q4;
+      const float* ger = sm.gg + (16 * I0 + 15) * SQ + 8 * q4;
+      float kl[8], qf[8], kf[8];
+#pragma unroll
+      for (int e = 0; e < 8; e++) {
+        const float eF = ex2(gv[e] - gbr[e]), eL = ex2(ger[e] - gv[e]);
+        kl[e] = kv[e] * ik * eL;
+        qf[e] = qv[e] * iq * eF;
+        kf[e] = kv[e] * ik * eF;
+      }
+      const int c0 = tix(r, 8 * q4);  // eight consecutive columns
+      *reinterpret_cast<float4*>(sm.kl + c0) = make_float4(kl[0], kl[1], kl[2], kl[3]);
+      *reinterpret_cast<float4*>(sm.kl + c0 + 4) = make_float4(kl[4], kl[5], kl[6], kl[7]);
+      *reinterpret_cast<float4*>(sm.qf + c0) = make_float4(qf[0], qf[1], qf[2], qf[3]);
+      *reinterpret_cast<float4*>(sm.qf + c0 + 4) = make_float4(qf[4], qf[5], qf[6], qf[7]);
+      *reinterpret_cast<float4*>(sm.kf + c0) = make_float4(kf[0], kf[1], kf[2], kf[3]);
+      *reinterpret_cast<float4*>(sm.kf + c0 + 4) = make_float4(kf[4], kf[5], kf[6], kf[7]);
+    }
   }
-  float dQG[2][4], dKD[2][4], dkg[2][4];
-  frag_load(w.gQG + ch * NTH * 8, dQG);
-  frag_load(w.gKD + ch * NTH * 8, dKD);
-  frag_load(w.gKG + ch * NTH * 8, dkg);
   if (__syncthreads_or(!mbar_wait(&sm.bar, 0))) {  // a bulk load did not complete in bound
     mbar_wait(&sm.bar, 0);
     if (tid == 0) atomicExch(w.err, -7);
@@ -1912,30 +1936,56 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
   zero(prow);
   zero(arow);
   zero(col);
-  for (int J = 0; J <= I; J++) {
-    if (J == I && !ok) break;
+  //      over the block pairs, with per-channel factors in Horner form (every ratio <= 1):
+  //      prow = sum_J 2^(G_first(I) - G_last(J)) dP'_IJ kl_J (J ascending), col = sum_I2
+  //      2^(G_first(I2) - G_last(I)) (dP'^T qf + MA^T kf)_I2 (I2 descending); the diagonal
+  //      factor 2^span(I) only when the block is in range
+  auto scale = [&](float (&x)[2][4], const float* ga, const float* gb) {  // x *= 2^(ga - gb) per column
+#pragma unroll
+    for (int jj = 0; jj < 2; jj++)
+#pragma unroll
+      for (int c1 = 0; c1 < 2; c1++) {
+        const int i = 16 * hk + 8 * jj + 2 * tq + c1;
+        const float f = ex2(ga[i] - gb[i]);
+        x[jj][c1] *= f;
+        x[jj][2 + c1] *= f;
+      }
+  };
+  const int Jl = ok ? I : I - 1;  // the last block J of prow / arow
+  for (int J = 0; J <= Jl; J++) {
     const float* DPb = sm.dp + blk_of(I, J) * 16 * PB;
     const float* MAb = sm.ma + blk_of(I, J) * 16 * PB;
+    if (J > 0) {
+      const float* geJ = sm.gg + (16 * J + 15) * SQ;
+      scale(prow, geJ, geJ - 16 * SQ);
+      scale(arow, geJ, geJ - 16 * SQ);
+    }
     rows16_2a<2>(prow, arow, 2, [&](int m, int k) { return DPb[m * PB + k]; },
                  [&](int m, int k) { return MAb[m * PB + k]; },
-                 [&](int k, int jj, int n) {
-                   const int s = 16 * J + k, i = 16 * hk + 8 * jj + n;
-                   return bfl(sm.rk[s * DK + i]) * sm.ink[s] * ex2(fminf(gbI[i] - sm.gg[s * SQ + i], SPAN2));
-                 });
+                 [&](int k, int jj, int n) { return sm.kl[tix(16 * J + k, 16 * hk + 8 * jj + n)]; });
   }
-  for (int I2 = I; I2 < 4; I2++) {
-    if (I2 == I && !ok) continue;
+  if (Jl >= 0) {
+    scale(prow, gbI, sm.gg + (16 * Jl + 15) * SQ);
+    scale(arow, gbI, sm.gg + (16 * Jl + 15) * SQ);
+  }
+  const int Il = ok ? I : I + 1;  // the last block I2 of col
+  for (int I2 = 3; I2 >= Il; I2--) {
     const float* DPb = sm.dp + blk_of(I2, I) * 16 * PB;
     const float* MAb = sm.ma + blk_of(I2, I) * 16 * PB;
+    if (I2 < 3) scale(col, sm.gg + (16 * I2 + 16) * SQ, sm.gg + (16 * I2) * SQ);
     rows16_ab<2>(col, 2, [&](int m, int k) { return DPb[k * PB + m]; },
                  [&](int m, int k) { return MAb[k * PB + m]; },
                  [&](int k, int jj, int n) {
-                   const int rr = 16 * I2 + k, i = 16 * hk + 8 * jj + n;
-                   const float x = ex2(fminf(sm.gg[rr * SQ + i] - geI[i], SPAN2));
-                   return make_float2(bfl(sm.rq[rr * DK + i]) * sm.inq[rr] * x, bfl(sm.rk[rr * DK + i]) * sm.ink[rr] * x);
+                   const int t = tix(16 * I2 + k, 16 * hk + 8 * jj + n);
+                   return make_float2(sm.qf[t], sm.kf[t]);
                  });
   }
+  if (Il <= 3) scale(col, sm.gg + (16 * Il) * SQ, geI);
   // ---- assemble dq^, dk^, dG - kdt per owned element; column totals of kdt
+  float dQG[2][4], dKD[2][4], dkg[2][4];  // bwd_grad's hand-over (L2-resident: prefetched a wave ahead)
+  frag_load(w.gQG + ch * NTH * 8, dQG);
+  frag_load(w.gKD + ch * NTH * 8, dKD);
+  frag_load(w.gKG + ch * NTH * 8, dkg);
   float dqh[2][4], dkh[2][4], dGk[2][4], kcol[2][2];
   {
     const float* DPd = sm.dp + blk_of(I, I) * 16 * PB;
