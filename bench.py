@@ -461,6 +461,37 @@ def run_ours(args, rank, world, local):
     return 0
 
 
+def ncu_pass():
+    """One untimed pass for profiler captures (select launches with ncu's -k /
+    -s / -c): a warm-up forward+backward of the bench step's workload, the same
+    forward+backward again, then one decode step, the gated norm forward and
+    backward and the short convolution forward and backward, in that order."""
+    from kimi_delta_attention_bwd_gb300 import (kda_backward, kda_decode_step, kda_forward, kda_norm_gate,
+                                                kda_norm_gate_backward, kda_short_conv, kda_short_conv_backward)
+    from kimi_delta_attention_bwd_gb300.inputs import norm_gate_inputs, short_conv_inputs
+    dev = torch.device("cuda", 0)
+    w = WORKLOADS[STEP_WORKLOAD]
+    d = {k: (t.to(dev) if isinstance(t, torch.Tensor) else t) for k, t in make_inputs(w).items()}
+    for _ in range(2):
+        o, hf, ctx = kda_forward(d["q"], d["k"], d["v"], d["f"], d["b"], d["A_log"], d["dt_bias"], scale=d["scale"])
+        kda_backward(ctx, d["dO"])
+    di = {k: (t.to(dev) if isinstance(t, torch.Tensor) else t)
+          for k, t in make_inputs(custom(DECODE_SEQS, 1, w.H, w.dk, w.dv, dtype="bf16", h0=True),
+                                  with_grad_inputs=False).items()}
+    state = di["h0"].clone()
+    kda_decode_step(*(di[x][:, 0].contiguous() for x in ("q", "k", "v", "f", "b")), di["A_log"], di["dt_bias"], state,
+                    scale=di["scale"])
+    ng = {k: t.to(dev) for k, t in norm_gate_inputs(w.B * w.T * w.H, w.dv).items()}
+    kda_norm_gate(ng["x"], ng["g"], ng["w"])
+    kda_norm_gate_backward(ng["x"], ng["g"], ng["w"], ng["dy"])
+    sc = {k: t.to(dev) for k, t in short_conv_inputs(w.B * w.T, 1024).items()}
+    kda_short_conv(sc["x"], sc["w"])
+    kda_short_conv_backward(sc["x"], sc["w"], sc["dy"])
+    torch.cuda.synchronize()
+    print("ncu pass done")
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -468,7 +499,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-pass", action="store_true", help="one untimed pass of every kernel, for ncu captures")
     args = ap.parse_args()
+    if args.ncu_pass:
+        return ncu_pass()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     if args.impl == "reference":
         # rank 0 alone times the oracle; the other ranks exit without work
