@@ -653,10 +653,10 @@ __device__ void solve_merge(const float* am, float* tm, float* yy) {
 // are split operand tiles; regions are reused as noted.
 struct ChunkSm {
   float gg[C * SQ];    // G2 = G log2(e) (fp32); QG (split) once the A / P blocks are done
-  bf16 x[18432];       // LQ | LK | R  ->  T (fp32) + Y scratch  ->  W | U;  KD in the last 8 KB
+  bf16 x[18432];       // LQ | LK | R  ->  T (fp32) + Y scratch  ->  [W | U];  KD in the last 8 KB
   float am[C * SC];    // beta_r A (fp32), then T (split)
   bf16 op[2 * C * C];  // P (scaled, split)
-  bf16 y[2 * C * DK + 2 * C * DV];  // XK = beta k^ e^G | XV = beta v
+  bf16 y[2 * C * DK + 2 * C * DV];  // [XK | XV] (XK = beta k^ e^G, XV = beta v)  ->  W | U for the save
   float bet[C], inq[C], ink[C];
   float gam[DK];
   float tot[NW * DK];
@@ -787,8 +787,10 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
   }
 
   const Op LQ{sm.x, sm.x + 2048, DK}, LK{sm.x + 4096, sm.x + 6144, DK}, R{sm.x + 8192, sm.x + 13312, DK};
-  const Op W{sm.x, sm.x + 2048, DK}, U{sm.x + 4096, sm.x + 8192, DV}, KD{sm.x + 14336, sm.x + 16384, DK};
-  const Op XK{sm.y, sm.y + 2048, DK}, XV{sm.y + 4096, sm.y + 8192, DV};
+  // [XK | XV] and [W | U] are single 96-column tiles (one tensor-core operand
+  // each); W and U for the backward are copied apart over XKV once it is read
+  const Op WU{sm.x, sm.x + 6144, DK + DV}, KD{sm.x + 14336, sm.x + 16384, DK};
+  const Op XKV{sm.y, sm.y + 6144, DK + DV}, Ws{sm.y, sm.y + 2048, DK}, Us{sm.y + 4096, sm.y + 8192, DV};
   const Op P{sm.op, sm.op + C * C, C};
   const Op T{reinterpret_cast<bf16*>(sm.am), reinterpret_cast<bf16*>(sm.am) + C * C, C};
   bf16* qgb = reinterpret_cast<bf16*>(sm.gg);
@@ -846,7 +848,7 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
 #pragma unroll
     for (int e = 0; e < 8; e++) xv[e] = beta * vv[8 * hv + e];
     rot_pairs(xv, q4);
-    store8_rot(XV, r, 16 * q4 + 8 * hv, xv, q4);
+    store8_rot(XKV, r, DK + 16 * q4 + 8 * hv, xv, q4);
   }
 #pragma unroll
   for (int e = 0; e < 8; e++) { qv[e] *= iq; kv[e] *= ik; }
@@ -903,7 +905,7 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
       rot_pairs(xk, q4);
       store8_rot(LQ, r, 8 * q4, lq, q4);
       store8_rot(LK, r, 8 * q4, lk, q4);
-      store8_rot(XK, r, 8 * q4, xk, q4);
+      store8_rot(XKV, r, 8 * q4, xk, q4);
       rot_pairs(qg, q4);  // stored after the A / P blocks
       rot_pairs(kd, q4);
     }
@@ -993,8 +995,8 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     bulk_commit();
   }
   // tensor-core rounds: one thread issues, completion on sm.bar, then every warp
-  // reads the m16n8 fragments of its 16 rows.  TMEM columns: W 0 | U 32;
-  // then PU 96 | QW' 160 | KU' 192 | M' 0 (rows 32.. of KU' and M' are unused)
+  // reads the m16n8 fragments of its 16 rows.  TMEM columns: W 0 | U 32; then
+  // M' 0 | KU' 32 (rows 32.. unused) and QW' 96 | PU 128
   uint32_t mph = 0;
   auto round_done = [&]() -> bool {  // uniform over the CTA
     const bool ok = mbar_wait(&sm.bar, mph);
@@ -1011,8 +1013,7 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
   };
   if (tid == 0) {  // W | U = T [XK | XV]
     tc::fence_after();
-    tc::gemm_split(tb + 0, tc::kmaj(T), tc::mnmaj(XK), 32, C / 16, false);
-    tc::gemm_split(tb + 32, tc::kmaj(T), tc::mnmaj(XV), 64, C / 16, false);
+    tc::gemm_split(tb + 0, tc::kmaj(T), tc::mnmaj(XKV), DK + DV, C / 16, false);
     tc::commit(&sm.bar);
   }
   if (!round_done()) { bail(); return; }
@@ -1024,30 +1025,34 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
 #pragma unroll
     for (int jt = 0; jt < 2; jt++)
 #pragma unroll
-      for (int hh = 0; hh < 2; hh++)
-        op_store2(W, 16 * wI + gq + 8 * hh, 16 * hk + 8 * jt + 2 * tq, aw[jt][2 * hh], aw[jt][2 * hh + 1]);
+      for (int hh = 0; hh < 2; hh++) {
+        const int rr = 16 * wI + gq + 8 * hh, c = 16 * hk + 8 * jt + 2 * tq;
+        op_store2(WU, rr, c, aw[jt][2 * hh], aw[jt][2 * hh + 1]);
+        if (io.save) op_store2(Ws, rr, c, aw[jt][2 * hh], aw[jt][2 * hh + 1]);
+      }
 #pragma unroll
     for (int jt = 0; jt < 4; jt++)
 #pragma unroll
-      for (int hh = 0; hh < 2; hh++)
-        op_store2(U, 16 * wI + gq + 8 * hh, 32 * hk + 8 * jt + 2 * tq, au[jt][2 * hh], au[jt][2 * hh + 1]);
+      for (int hh = 0; hh < 2; hh++) {
+        const int rr = 16 * wI + gq + 8 * hh, c = 32 * hk + 8 * jt + 2 * tq;
+        op_store2(WU, rr, DK + c, au[jt][2 * hh], au[jt][2 * hh + 1]);
+        if (io.save) op_store2(Us, rr, c, au[jt][2 * hh], au[jt][2 * hh + 1]);
+      }
   }
   fence_async_smem();
   tc::fence_before();
   __syncthreads();
   if (io.save && tid == 0) {  // W and U for the backward
-    bulk_s2g(w.sW + ch * 2 * C * DK, W.hi, 4 * C * DK);
-    bulk_s2g(w.sU + ch * 2 * C * DV, U.hi, 4 * C * DV);
+    bulk_s2g(w.sW + ch * 2 * C * DK, Ws.hi, 4 * C * DK);
+    bulk_s2g(w.sU + ch * 2 * C * DV, Us.hi, 4 * C * DV);
     bulk_commit();
   }
   // outputs, straight from the fragments to global: PU and KU (fp32), QW and M
   // (split)
-  if (tid == 0) {  // PU = P U, QW' = P W, KU' = KD^T U, M' = KD^T W (KD^T: rows 32.. unused)
+  if (tid == 0) {  // [QW' | PU] = P [W | U], [M' | KU'] = KD^T [W | U] (KD^T: rows 32.. unused)
     tc::fence_after();
-    tc::gemm_split(tb + 96, tc::kmaj(P), tc::mnmaj(U), 64, C / 16, false);
-    tc::gemm_split(tb + 160, tc::kmaj(P), tc::mnmaj(W), 32, C / 16, false);
-    tc::gemm_split(tb + 192, tc::mnmaj(KD), tc::mnmaj(U), 64, C / 16, false);
-    tc::gemm_split(tb + 0, tc::mnmaj(KD), tc::mnmaj(W), 32, C / 16, false);
+    tc::gemm_split(tb + 96, tc::kmaj(P), tc::mnmaj(WU), DK + DV, C / 16, false);
+    tc::gemm_split(tb + 0, tc::mnmaj(KD), tc::mnmaj(WU), DK + DV, C / 16, false);
     tc::commit(&sm.bar);
   }
   if (!round_done()) { bail(); return; }
@@ -1056,13 +1061,13 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     const Op QWg{w.sQW + ch * 2 * C * DK, w.sQW + ch * 2 * C * DK + C * DK, DK};
     const Op Mg{w.sM + ch * 2 * DK * DK, w.sM + ch * 2 * DK * DK + DK * DK, DK};
     float pu[4][4], qw[2][4];
-    tc::ld_frag<4>(tb + 96, 32 * hk, pu);
-    tc::ld_frag<2>(tb + 160, 16 * hk, qw);
+    tc::ld_frag<4>(tb + 128, 32 * hk, pu);
+    tc::ld_frag<2>(tb + 96, 16 * hk, qw);
     store_acc(pu, w.PU + ch * C * DV, DV, 16 * wI, 32 * hk, [](int, int, float v) { return v; });
     store_acc_op(qw, QWg, 16 * wI, 16 * hk, [&](int rr, int c, float v) { return op_get(QG, rr, c) - v; });
     if (wI < 2) {  // rows i < dk of the KD^T products
       float ku[4][4], mm[2][4];
-      tc::ld_frag<4>(tb + 192, 32 * hk, ku);
+      tc::ld_frag<4>(tb + 32, 32 * hk, ku);
       tc::ld_frag<2>(tb + 0, 16 * hk, mm);
       store_acc(ku, w.KU + ch * DK * DV, DV, 16 * wI, 32 * hk, [](int, int, float v) { return v; });
       store_acc_op(mm, Mg, 16 * wI, 16 * hk, [&](int i, int jc, float v) { return (i == jc ? sm.gam[i] : 0.f) - v; });
