@@ -1063,13 +1063,15 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     float pu[4][4], qw[2][4];
     tc::ld_frag<4>(tb + 128, 32 * hk, pu);
     tc::ld_frag<2>(tb + 96, 16 * hk, qw);
-    store_acc(pu, w.PU + ch * C * DV, DV, 16 * wI, 32 * hk, [](int, int, float v) { return v; });
+    // PU and KU per 32-column half (warp column hk), [ch][half][rows][32]: the chain CTA of a half
+    // loads its slice in one copy
+    store_acc(pu, w.PU + (ch * 2 + hk) * C * 32, 32, 16 * wI, 0, [](int, int, float v) { return v; });
     store_acc_op(qw, QWg, 16 * wI, 16 * hk, [&](int rr, int c, float v) { return op_get(QG, rr, c) - v; });
     if (wI < 2) {  // rows i < dk of the KD^T products
       float ku[4][4], mm[2][4];
       tc::ld_frag<4>(tb + 32, 32 * hk, ku);
       tc::ld_frag<2>(tb + 0, 16 * hk, mm);
-      store_acc(ku, w.KU + ch * DK * DV, DV, 16 * wI, 32 * hk, [](int, int, float v) { return v; });
+      store_acc(ku, w.KU + (ch * 2 + hk) * DK * 32, 32, 16 * wI, 0, [](int, int, float v) { return v; });
       store_acc_op(mm, Mg, 16 * wI, 16 * hk, [&](int i, int jc, float v) { return (i == jc ? sm.gam[i] : 0.f) - v; });
     }
   }
@@ -1086,7 +1088,9 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
 // (from h0 / dh_final; the last state is h_final / dh0).  Value columns are
 // independent: one CTA of four warps per (document, head, 32 value columns)
 // carries a 32 x 32 slice as a split-bf16 operand tile in shared memory and
-// streams the chunk's operands through a three-stage cp.async ring.  Only the
+// streams the chunk's operands through a three-stage ring of 1-D bulk copies
+// (one thread issues, completion on the stage's mbarrier; the backward's dO
+// rows, strided in the input, by cp.async).  Only the
 // state product is on the chain; the output (forward) and QW^T dO (backward)
 // take the same step's other warps' slack.  Each step also stores the carried
 // state (S entering the chunk, dS leaving it) as a split operand tile for the
@@ -1116,7 +1120,11 @@ struct FChainStage {
 struct FChainSm {
   FChainStage st[NSTG];
   bf16 S[2 * DK * NSC];  // the carried state (split)
+  uint64_t bar[NSTG];    // stage completion
 };
+static_assert(sizeof(FChainStage) % 16 == 0 && offsetof(FChainStage, QW) % 16 == 0 && offsetof(FChainStage, KU) % 16 == 0 &&
+                  offsetof(FChainStage, PU) % 16 == 0,
+              "bulk-copy targets need 16-byte alignment");
 
 __global__ void __launch_bounds__(CTH) fwd_state_kernel(Dims d, FwdIO io, Ws w) {
   extern __shared__ __align__(16) unsigned char smraw[];
@@ -1134,23 +1142,24 @@ __global__ void __launch_bounds__(CTH) fwd_state_kernel(Dims d, FwdIO io, Ws w) 
     if (io.h0) v = *reinterpret_cast<const float2*>(io.h0 + dh + i * DV + col0 + jc);
     op_store2(S, i, jc, v.x, v.y);
   }
-  auto prefetch = [&](int step) {  // always commits a group (empty past the end)
-    if (step < n) {
-      FChainStage& s = sm.st[step % NSTG];
-      const int64_t ch = (int64_t)(cb + step) * H + h;
-      for (int o = tid * 16; o < 4 * DK * DK; o += CTH * 16) cp16((char*)s.M + o, (const char*)(w.sM + ch * 2 * DK * DK) + o);
-      for (int o = tid * 16; o < 4 * C * DK; o += CTH * 16) cp16((char*)s.QW + o, (const char*)(w.sQW + ch * 2 * C * DK) + o);
-      for (int idx = tid; idx < DK * NSC / 4; idx += CTH) {
-        const int i = idx / (NSC / 4), p = idx % (NSC / 4);
-        cp16(&s.KU[i * NSC + 4 * p], w.KU + ch * DK * DV + i * DV + col0 + 4 * p);
-      }
-      for (int idx = tid; idx < C * NSC / 4; idx += CTH) {
-        const int r = idx / (NSC / 4), p = idx % (NSC / 4);
-        cp16(&s.PU[r * NSC + 4 * p], w.PU + ch * C * DV + r * DV + col0 + 4 * p);
-      }
+  if (tid == 0) {
+    for (int s2 = 0; s2 < NSTG; s2++) mbar_init(&sm.bar[s2], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();  // the barriers are initialised before any thread waits on them
+  auto prefetch = [&](int step) {  // thread 0: the stage of `step` (M, QW, this half of KU and PU)
+    if (step < n && tid == 0) {
+      const int slot = step % NSTG;
+      FChainStage& s = sm.st[slot];
+      const int64_t ch = (int64_t)(cb + step) * H + h, hc = ch * 2 + blockIdx.z;
+      mbar_expect_tx(&sm.bar[slot], (uint32_t)sizeof(FChainStage));
+      bulk_g2s(s.M, w.sM + ch * 2 * DK * DK, 4 * DK * DK, &sm.bar[slot]);
+      bulk_g2s(s.QW, w.sQW + ch * 2 * C * DK, 4 * C * DK, &sm.bar[slot]);
+      bulk_g2s(s.KU, w.KU + hc * DK * NSC, 4 * DK * NSC, &sm.bar[slot]);
+      bulk_g2s(s.PU, w.PU + hc * C * NSC, 4 * C * NSC, &sm.bar[slot]);
     }
-    cp_commit();
   };
+  static_assert(sizeof(FChainStage) == 4 * DK * DK + 4 * C * DK + 4 * DK * NSC + 4 * C * NSC, "stage bytes");
   for (int s = 0; s < NSTG - 1; s++) prefetch(s);
   float snew[2][4];  // this warp's tile of the updated state: rows 16 (warp & 1) .., columns 16 (warp >> 1) ..
   zero(snew);
@@ -1159,8 +1168,11 @@ __global__ void __launch_bounds__(CTH) fwd_state_kernel(Dims d, FwdIO io, Ws w) 
   for (int step = 0; step < n; step++) {
     const FChainStage& s = sm.st[step % NSTG];
     const int ci = cb + step, L = w.chunk_len[ci], t0 = w.chunk_tok0[ci];
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(NSTG - 2));
-    __syncthreads();  // this step's stage and the last state update are visible
+    if (__syncthreads_or(!mbar_wait(&sm.bar[step % NSTG], (step / NSTG) & 1))) {  // a stage did not arrive in bound
+      for (int k2 = step; k2 < n && k2 < step + NSTG - 1; k2++) mbar_wait(&sm.bar[k2 % NSTG], (k2 / NSTG) & 1);
+      if (tid == 0) atomicExch(w.err, -7);
+      return;
+    }  // this step's stage and the last state update are visible
     prefetch(step + NSTG - 1);
     const Op Mo{const_cast<bf16*>(s.M), const_cast<bf16*>(s.M) + DK * DK, DK};
     const Op QWo{const_cast<bf16*>(s.QW), const_cast<bf16*>(s.QW) + C * DK, DK};
@@ -1194,7 +1206,6 @@ __global__ void __launch_bounds__(CTH) fwd_state_kernel(Dims d, FwdIO io, Ws w) 
       for (int hh = 0; hh < 2; hh++)
         op_store2(S, 16 * mI + gq + 8 * hh, 16 * jn + 8 * jj + 2 * tq, snew[jj][2 * hh], snew[jj][2 * hh + 1]);
   }
-  cp_wait_all();
   if (io.h_final) {
     if (n > 0) {
 #pragma unroll
@@ -1221,7 +1232,9 @@ struct BChainStage {
 struct BChainSm {
   BChainStage st[NSTG];
   bf16 dS[2 * DK * NSC];  // the carried state gradient (split)
+  uint64_t bar[NSTG];     // completion of the stage's M and QW
 };
+static_assert(sizeof(BChainStage) % 16 == 0 && offsetof(BChainStage, QW) % 16 == 0, "bulk-copy targets need 16-byte alignment");
 
 __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
   extern __shared__ __align__(16) unsigned char smraw[];
@@ -1240,13 +1253,22 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
     op_store2(dS, i, jc, v.x, v.y);
   }
   const bf16* dOg = (const bf16*)io.dO;
-  auto prefetch = [&](int step) {  // always commits a group (empty past the end)
+  if (tid == 0) {
+    for (int s2 = 0; s2 < NSTG; s2++) mbar_init(&sm.bar[s2], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();  // the barriers are initialised before any thread waits on them
+  auto prefetch = [&](int step) {  // always commits a cp.async group (empty past the end)
     if (step < n) {
-      BChainStage& s = sm.st[step % NSTG];
+      const int slot = step % NSTG;
+      BChainStage& s = sm.st[slot];
       const int ci = ce - 1 - step, L = w.chunk_len[ci], t0 = w.chunk_tok0[ci];
       const int64_t ch = (int64_t)ci * H + h;
-      for (int o = tid * 16; o < 4 * DK * DK; o += CTH * 16) cp16((char*)s.M + o, (const char*)(w.sM + ch * 2 * DK * DK) + o);
-      for (int o = tid * 16; o < 4 * C * DK; o += CTH * 16) cp16((char*)s.QW + o, (const char*)(w.sQW + ch * 2 * C * DK) + o);
+      if (tid == 0) {
+        mbar_expect_tx(&sm.bar[slot], 4 * DK * DK + 4 * C * DK);
+        bulk_g2s(s.M, w.sM + ch * 2 * DK * DK, 4 * DK * DK, &sm.bar[slot]);
+        bulk_g2s(s.QW, w.sQW + ch * 2 * C * DK, 4 * C * DK, &sm.bar[slot]);
+      }
       for (int idx = tid; idx < C * NSC / 8; idx += CTH) {
         const int r = idx / (NSC / 8), p = idx % (NSC / 8);
         bf16* dst = s.dO + opix(r, 8 * p, NSC);
@@ -1264,7 +1286,12 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
     const BChainStage& s = sm.st[step % NSTG];
     const int ci = ce - 1 - step;
     asm volatile("cp.async.wait_group %0;\n" ::"n"(NSTG - 2));
-    __syncthreads();  // this step's stage and the last state update are visible
+    if (__syncthreads_or(!mbar_wait(&sm.bar[step % NSTG], (step / NSTG) & 1))) {  // a stage did not arrive in bound
+      for (int k2 = step; k2 < n && k2 < step + NSTG - 1; k2++) mbar_wait(&sm.bar[k2 % NSTG], (k2 / NSTG) & 1);
+      cp_wait_all();
+      if (tid == 0) atomicExch(w.err, -7);
+      return;
+    }  // this step's stage and the last state update are visible
     prefetch(step + NSTG - 1);
     const Op Mo{const_cast<bf16*>(s.M), const_cast<bf16*>(s.M) + DK * DK, DK};
     const Op QWo{const_cast<bf16*>(s.QW), const_cast<bf16*>(s.QW) + C * DK, DK};
