@@ -1102,8 +1102,9 @@ constexpr int CTH = 128;  // chain threads
 
 // Copies the 32 x NSC slice tile (K = NSC) into columns col0.. of the chunk's
 // full 32 x dv state tile (K = dv) in global memory: whole 8 x 8 core matrices.
-__device__ __forceinline__ void slice_to_global(bf16* g, const bf16* s, int col0) {
-  for (int idx = threadIdx.x; idx < 2 * 16 * 8; idx += CTH) {  // (hi|lo) x 16 cores x 8 uint4
+// t: the copying thread's index among CTH threads.
+__device__ __forceinline__ void slice_to_global(bf16* g, const bf16* s, int col0, int t) {
+  for (int idx = t; idx < 2 * 16 * 8; idx += CTH) {  // (hi|lo) x 16 cores x 8 uint4
     const int part = idx >> 7, core = (idx >> 3) & 15, q = idx & 7;
     const int rb = core >> 2, kb = core & 3;
     const uint4 v = *reinterpret_cast<const uint4*>(s + part * DK * NSC + (rb * (NSC / 8) + kb) * 64 + q * 8);
@@ -1119,14 +1120,17 @@ struct FChainStage {
 };
 struct FChainSm {
   FChainStage st[NSTG];
-  bf16 S[2 * DK * NSC];  // the carried state (split)
-  uint64_t bar[NSTG];    // stage completion
+  bf16 S[2][2 * DK * NSC];  // the carried state (split), double-buffered
+  uint64_t bar[NSTG];       // stage completion
 };
 static_assert(sizeof(FChainStage) % 16 == 0 && offsetof(FChainStage, QW) % 16 == 0 && offsetof(FChainStage, KU) % 16 == 0 &&
                   offsetof(FChainStage, PU) % 16 == 0,
               "bulk-copy targets need 16-byte alignment");
 
-__global__ void __launch_bounds__(CTH) fwd_state_kernel(Dims d, FwdIO io, Ws w) {
+// fwd_state: warps 0..3 carry the state (S' = M S + KU into the other buffer
+// of the double-buffered tile), warps 4..7 write the output O = QW S + PU and
+// store the entering state, both on the step's state; one barrier per step.
+__global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws w) {
   extern __shared__ __align__(16) unsigned char smraw[];
   FChainSm& sm = *reinterpret_cast<FChainSm*>(smraw);
   const int doc = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * NSC, tid = threadIdx.x, warp = tid >> 5;
@@ -1135,12 +1139,12 @@ __global__ void __launch_bounds__(CTH) fwd_state_kernel(Dims d, FwdIO io, Ws w) 
   const int H = d.H;
   const int cb = w.doc_chunk0[doc], n = w.doc_chunk0[doc + 1] - cb;
   const int64_t dh = ((int64_t)doc * H + h) * DK * DV;
-  const Op S{sm.S, sm.S + DK * NSC, NSC};
-  for (int idx = tid; idx < DK * NSC / 2; idx += CTH) {
+  const Op S0{sm.S[0], sm.S[0] + DK * NSC, NSC}, S1{sm.S[1], sm.S[1] + DK * NSC, NSC};
+  for (int idx = tid; idx < DK * NSC / 2; idx += 2 * CTH) {
     const int i = idx / (NSC / 2), jc = 2 * (idx % (NSC / 2));
     float2 v = make_float2(0.f, 0.f);
     if (io.h0) v = *reinterpret_cast<const float2*>(io.h0 + dh + i * DV + col0 + jc);
-    op_store2(S, i, jc, v.x, v.y);
+    op_store2(S0, i, jc, v.x, v.y);
   }
   if (tid == 0) {
     for (int s2 = 0; s2 < NSTG; s2++) mbar_init(&sm.bar[s2], 1);
@@ -1161,62 +1165,66 @@ __global__ void __launch_bounds__(CTH) fwd_state_kernel(Dims d, FwdIO io, Ws w) 
   };
   static_assert(sizeof(FChainStage) == 4 * DK * DK + 4 * C * DK + 4 * DK * NSC + 4 * C * NSC, "stage bytes");
   for (int s = 0; s < NSTG - 1; s++) prefetch(s);
-  float snew[2][4];  // this warp's tile of the updated state: rows 16 (warp & 1) .., columns 16 (warp >> 1) ..
+  const bool carry = warp < 4;
+  const int wq = warp & 3, mI = wq & 1, jn = wq >> 1;
+  float snew[2][4];  // (carry warps) tile of the updated state: rows 16 mI .., columns 16 jn ..
   zero(snew);
-  const int mI = warp & 1, jn = warp >> 1;
   bf16* o = (bf16*)io.o;
   for (int step = 0; step < n; step++) {
     const FChainStage& s = sm.st[step % NSTG];
-    const int ci = cb + step, L = w.chunk_len[ci], t0 = w.chunk_tok0[ci];
+    const int ci = cb + step;
     if (__syncthreads_or(!mbar_wait(&sm.bar[step % NSTG], (step / NSTG) & 1))) {  // a stage did not arrive in bound
       for (int k2 = step; k2 < n && k2 < step + NSTG - 1; k2++) mbar_wait(&sm.bar[k2 % NSTG], (k2 / NSTG) & 1);
       if (tid == 0) atomicExch(w.err, -7);
       return;
-    }  // this step's stage and the last state update are visible
+    }  // this step's stage and state are visible; the other state buffer is free
     prefetch(step + NSTG - 1);
     const Op Mo{const_cast<bf16*>(s.M), const_cast<bf16*>(s.M) + DK * DK, DK};
     const Op QWo{const_cast<bf16*>(s.QW), const_cast<bf16*>(s.QW) + C * DK, DK};
-    zero(snew);
-    gemm3<1, false, true>(snew, Mo, 16 * mI, 0, S, 16 * jn, 0, DK / 16);
-    float oo[4][4];
-    zero(oo);
-    gemm3<2, false, true>(oo, QWo, 16 * warp, 0, S, 0, 0, DK / 16);
-    slice_to_global(w.sS + ((int64_t)ci * H + h) * 2 * DK * DV, sm.S, col0);
-#pragma unroll
-    for (int jj = 0; jj < 2; jj++)
-#pragma unroll
-      for (int hh = 0; hh < 2; hh++) {
-        const int i = 16 * mI + gq + 8 * hh, c = 16 * jn + 8 * jj + 2 * tq;
-        snew[jj][2 * hh] += s.KU[i * NSC + c];
-        snew[jj][2 * hh + 1] += s.KU[i * NSC + c + 1];
-      }
-#pragma unroll
-    for (int jj = 0; jj < 4; jj++)
-#pragma unroll
-      for (int hh = 0; hh < 2; hh++) {
-        const int r = 16 * warp + gq + 8 * hh, c = 8 * jj + 2 * tq;
-        if (r < L)
-          *reinterpret_cast<__nv_bfloat162*>(o + ((size_t)(t0 + r) * H + h) * DV + col0 + c) =
-              __floats2bfloat162_rn(oo[jj][2 * hh] + s.PU[r * NSC + c], oo[jj][2 * hh + 1] + s.PU[r * NSC + c + 1]);
-      }
-    __syncthreads();  // every read of the state tile is done
-#pragma unroll
-    for (int jj = 0; jj < 2; jj++)
-#pragma unroll
-      for (int hh = 0; hh < 2; hh++)
-        op_store2(S, 16 * mI + gq + 8 * hh, 16 * jn + 8 * jj + 2 * tq, snew[jj][2 * hh], snew[jj][2 * hh + 1]);
-  }
-  if (io.h_final) {
-    if (n > 0) {
+    const Op& Sc = (step & 1) ? S1 : S0;
+    if (carry) {
+      const Op& Sn = (step & 1) ? S0 : S1;
+      zero(snew);
+      gemm3<1, false, true>(snew, Mo, 16 * mI, 0, Sc, 16 * jn, 0, DK / 16);
 #pragma unroll
       for (int jj = 0; jj < 2; jj++)
 #pragma unroll
         for (int hh = 0; hh < 2; hh++) {
           const int i = 16 * mI + gq + 8 * hh, c = 16 * jn + 8 * jj + 2 * tq;
-          *reinterpret_cast<float2*>(io.h_final + dh + i * DV + col0 + c) = make_float2(snew[jj][2 * hh], snew[jj][2 * hh + 1]);
+          snew[jj][2 * hh] += s.KU[i * NSC + c];
+          snew[jj][2 * hh + 1] += s.KU[i * NSC + c + 1];
+          op_store2(Sn, i, c, snew[jj][2 * hh], snew[jj][2 * hh + 1]);
         }
     } else {
-      for (int idx = tid; idx < DK * NSC; idx += CTH) {
+      const int L = w.chunk_len[ci], t0 = w.chunk_tok0[ci];
+      float oo[4][4];
+      zero(oo);
+      gemm3<2, false, true>(oo, QWo, 16 * wq, 0, Sc, 0, 0, DK / 16);
+      slice_to_global(w.sS + ((int64_t)ci * H + h) * 2 * DK * DV, Sc.hi, col0, tid - CTH);
+#pragma unroll
+      for (int jj = 0; jj < 4; jj++)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+          const int r = 16 * wq + gq + 8 * hh, c = 8 * jj + 2 * tq;
+          if (r < L)
+            *reinterpret_cast<__nv_bfloat162*>(o + ((size_t)(t0 + r) * H + h) * DV + col0 + c) =
+                __floats2bfloat162_rn(oo[jj][2 * hh] + s.PU[r * NSC + c], oo[jj][2 * hh + 1] + s.PU[r * NSC + c + 1]);
+        }
+    }
+  }
+  if (io.h_final) {
+    if (n > 0) {
+      if (carry)
+#pragma unroll
+        for (int jj = 0; jj < 2; jj++)
+#pragma unroll
+          for (int hh = 0; hh < 2; hh++) {
+            const int i = 16 * mI + gq + 8 * hh, c = 16 * jn + 8 * jj + 2 * tq;
+            *reinterpret_cast<float2*>(io.h_final + dh + i * DV + col0 + c) =
+                make_float2(snew[jj][2 * hh], snew[jj][2 * hh + 1]);
+          }
+    } else {
+      for (int idx = tid; idx < DK * NSC; idx += 2 * CTH) {
         const int i = idx / NSC, jc = idx % NSC;
         io.h_final[dh + i * DV + col0 + jc] = io.h0 ? io.h0[dh + i * DV + col0 + jc] : 0.f;
       }
@@ -1301,7 +1309,7 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
     zero(ax);
     gemm3<1, true, true>(ax, QWo, 16 * mI, 0, dOo, 16 * jn, 0, C / 16);
     gemm3<1, true, true>(acc, Mo, 16 * mI, 0, dS, 16 * jn, 0, DK / 16);
-    slice_to_global(w.sdS + ((int64_t)ci * H + h) * 2 * DK * DV, sm.dS, col0);
+    slice_to_global(w.sdS + ((int64_t)ci * H + h) * 2 * DK * DV, sm.dS, col0, threadIdx.x);
 #pragma unroll
     for (int jj = 0; jj < 2; jj++)
 #pragma unroll
@@ -2222,7 +2230,7 @@ cudaError_t launch_fast_fwd(const Dims& d0, const FwdIO& io, const Ws& w, cudaSt
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_begin(K_FWD_STATE, st);
-  fast::fwd_state_kernel<<<dim3(d.n_docs, d.H, fast::DV / fast::NSC), fast::CTH, s2, st>>>(d, io, w);
+  fast::fwd_state_kernel<<<dim3(d.n_docs, d.H, fast::DV / fast::NSC), 2 * fast::CTH, s2, st>>>(d, io, w);
   prof_end(K_FWD_STATE, st);
   return cudaGetLastError();
 }
