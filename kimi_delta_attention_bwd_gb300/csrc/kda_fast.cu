@@ -2126,10 +2126,25 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
           const float ds = warp_sum(dx);
           if (lane == 0) dfo[(size_t)(t0 + rr) * H + h] = __float2bfloat16_rn(ds);
         } else {
-          dfo[((size_t)(t0 + rr) * H + h) * DK + lane] = __float2bfloat16_rn(dx);
+          dgs[rr * SQ + lane] = dx;  // over the value just read: this warp's rows, stored below
         }
         pdt += dx;
         pA += dg * g;
+      }
+    }
+    if (!gdn) {  // df of the warp's 8 rows: lane = row lane / 4, channels 8 (lane % 4) .., one 16-byte store
+      __syncwarp();
+      const int m = lane >> 2, rr = 8 * warp + m, c0 = 8 * (lane & 3);
+      if (rr < L) {
+        const float4 x0 = *reinterpret_cast<const float4*>(dgs + rr * SQ + c0);
+        const float4 x1 = *reinterpret_cast<const float4*>(dgs + rr * SQ + c0 + 4);
+        uint4 u;
+        __nv_bfloat162* u2 = reinterpret_cast<__nv_bfloat162*>(&u);
+        u2[0] = __floats2bfloat162_rn(x0.x, x0.y);
+        u2[1] = __floats2bfloat162_rn(x0.z, x0.w);
+        u2[2] = __floats2bfloat162_rn(x1.x, x1.y);
+        u2[3] = __floats2bfloat162_rn(x1.z, x1.w);
+        *reinterpret_cast<uint4*>(dfo + ((size_t)(t0 + rr) * H + h) * DK + c0) = u;
       }
     }
     sm.part[warp * DK + lane] = pdt;

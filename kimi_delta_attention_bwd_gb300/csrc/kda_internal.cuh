@@ -147,10 +147,11 @@ __device__ __forceinline__ float softplus_f(float x) {
   return fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x)));
 }
 __device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
-// Sigmoid from the fast exponential and reciprocal intrinsics (relative error
-// ~1e-6): for the streaming epilogue / prologue kernels whose outputs are
-// stored in bf16 or fp32 and need no more.
-__device__ __forceinline__ float sigmoid_fast(float x) { return __frcp_rn(1.0f + __expf(-x)); }
+// Sigmoid from the fast exponential and the fast division intrinsic (relative
+// error ~1e-6; 0 once exp(-x) overflows, the function's limit): for the
+// streaming epilogue / prologue kernels whose outputs are stored in bf16 or
+// fp32 and need no more.
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 // Softplus from the same intrinsics (absolute error below 1e-6): for the
 // tensor-core path, where it sets the log-decay g = -exp(A_log) softplus(.)
 // that then enters bf16-split products.
