@@ -1342,6 +1342,23 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
 
 // ------------------------------------------------------------ backward chunk kernels
 
+// Tensor-core rounds with several issuing threads.  A small product is bound by
+// the issue of its MMAs (about 60 cycles each), not by the tensor core, so the
+// independent products of a round (each with its own accumulator) are issued in
+// parallel: lane 0 of warp q < NISS runs share(q) and commits to the round's
+// barrier, or arrives on it plainly when share(q) issued nothing; the barrier
+// (NISS arrivals) completes once every share's MMAs have.
+constexpr int NISS = 4;
+template <class F>
+__device__ __forceinline__ void issue_round(uint64_t* bar, F share) {
+  const int q = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0 && q < NISS) {
+    tc::fence_after();
+    if (share(q)) tc::commit(bar);
+    else mbar_arrive(bar);
+  }
+}
+
 __device__ __forceinline__ void blk_ij(int b, int& I, int& J) {
   I = b < 1 ? 0 : b < 3 ? 1 : b < 6 ? 2 : 3;
   J = b - I * (I + 1) / 2;
@@ -1438,7 +1455,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   if (tid == 0) {  // the saved tiles in one bulk transaction group
     mbar_init(&sm.bar[0], 1);
     mbar_init(&sm.bar[1], 1);
-    mbar_init(&sm.bar[2], 1);
+    mbar_init(&sm.bar[2], NISS);
     mbar_init_fence();
     mbar_expect_tx(&sm.bar[0], 2 * 4 * DK * DV + 2 * 4 * C * C + 4 * C * DK + 4 * C * DV);
     bulk_g2s(S.hi, w.sS + ch * 2 * DK * DV, 4 * DK * DV, &sm.bar[0]);
@@ -1573,13 +1590,15 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
 
   const int I = warp & 3, hk = warp >> 2;  // owner tile: rows 16 I .., columns 32 hk .. / 16 hk ..
   // ---- dE = P^T dO + KD dS' and E = U - W S
-  if (tid == 0) {
-    tc::fence_after();
-    tc::gemm_split(tb + 0, tc::mnmaj(P), tc::mnmaj(dO), 64, C / 16, false);
-    tc::gemm_split(tb + 0, tc::kmaj(KD), tc::mnmaj(dS), 64, DK / 16, true);
-    tc::gemm_split(tb + 64, tc::kmaj(W), tc::mnmaj(S), 64, DK / 16, false);
-    tc::commit(&sm.bar[2]);
-  }
+  issue_round(&sm.bar[2], [&](int q) {
+    if (q == 0) {
+      tc::gemm_split(tb + 0, tc::mnmaj(P), tc::mnmaj(dO), 64, C / 16, false);
+      tc::gemm_split(tb + 0, tc::kmaj(KD), tc::mnmaj(dS), 64, DK / 16, true);
+    } else if (q == 1) {
+      tc::gemm_split(tb + 64, tc::kmaj(W), tc::mnmaj(S), 64, DK / 16, false);
+    }
+    return q < 2;
+  });
   if (!round_done()) { bail(); return; }
   {
     float dEr[4][4], ws[4][4];
@@ -1601,14 +1620,13 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   __syncthreads();
   // ---- dKD = E dS'^T, dQG = scale dO S^T (to bwd_gate), dW = -dE S^T (over W),
   //      dP' = scale dO E^T lower blocks (to bwd_gate), dgamma
-  if (tid == 0) {
-    tc::fence_after();
-    tc::gemm_split(tb + 128, tc::kmaj(E), tc::kmaj(dS), 32, DV / 16, false);
-    tc::gemm_split(tb + 160, tc::kmaj(dO), tc::kmaj(S), 32, DV / 16, false);
-    tc::gemm_split(tb + 192, tc::kmaj(dE), tc::kmaj(S), 32, DV / 16, false);
-    tc::gemm_split(tb + 0, tc::kmaj(dO), tc::kmaj(E), 64, DV / 16, false);
-    tc::commit(&sm.bar[2]);
-  }
+  issue_round(&sm.bar[2], [&](int q) {
+    if (q == 0) tc::gemm_split(tb + 128, tc::kmaj(E), tc::kmaj(dS), 32, DV / 16, false);
+    else if (q == 1) tc::gemm_split(tb + 160, tc::kmaj(dO), tc::kmaj(S), 32, DV / 16, false);
+    else if (q == 2) tc::gemm_split(tb + 192, tc::kmaj(dE), tc::kmaj(S), 32, DV / 16, false);
+    else tc::gemm_split(tb + 0, tc::kmaj(dO), tc::kmaj(E), 64, DV / 16, false);
+    return true;
+  });
   if (warp < 4) {  // dgamma_i = sum_j dS'_ij S_ij: lane = row i % 8 x column chunks (lane / 8, + 4); a
                     // quarter-warp reads whole core matrices
     const int i = 8 * warp + (lane & 7);
@@ -1670,11 +1688,12 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
     bulk_g2s(U2.hi, w.sU + ch * 2 * C * DV, 4 * C * DV, &sm.bar[1]);
     bulk_g2s(W2.hi, w.sW + ch * 2 * C * DK, 4 * C * DK, &sm.bar[1]);
     bulk_g2s(wk + 12288, w.sA + ch * NBLK * 16 * PB, NBLK * 16 * PB * 4, &sm.bar[1]);
-    tc::fence_after();
-    tc::gemm_split(tb + 64, tc::mnmaj(T), tc::mnmaj(dE), 64, C / 16, false);
-    tc::gemm_split(tb + 224, tc::mnmaj(T), tc::mnmaj(dW), 32, C / 16, false);
-    tc::commit(&sm.bar[2]);
   }
+  issue_round(&sm.bar[2], [&](int q) {
+    if (q == 0) tc::gemm_split(tb + 64, tc::mnmaj(T), tc::mnmaj(dE), 64, C / 16, false);
+    else if (q == 1) tc::gemm_split(tb + 224, tc::mnmaj(T), tc::mnmaj(dW), 32, C / 16, false);
+    return q < 2;
+  });
   if (!round_done()) { bail(); return; }
   {  // YU over dE, YW over dW (each thread overwrites only what it read... the MMA read them: done);
      // dv = beta YU; beta YW to bwd_gate
@@ -1713,12 +1732,13 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   }
   // ---- dA = -(YU U^T + YW W^T) strict lower; dbeta (U and W terms, row layout); MA = beta dA
   //      (to bwd_gate) and the A' term of dbeta
-  if (tid == 0) {
-    tc::fence_after();
-    tc::gemm_split(tb + 128, tc::kmaj(YU), tc::kmaj(U2), 64, DV / 16, false);
-    tc::gemm_split(tb + 128, tc::kmaj(YW), tc::kmaj(W2), 64, DK / 16, true);
-    tc::commit(&sm.bar[2]);
-  }
+  issue_round(&sm.bar[2], [&](int q) {
+    if (q == 0) {
+      tc::gemm_split(tb + 128, tc::kmaj(YU), tc::kmaj(U2), 64, DV / 16, false);
+      tc::gemm_split(tb + 128, tc::kmaj(YW), tc::kmaj(W2), 64, DK / 16, true);
+    }
+    return q == 0;
+  });
   {  // bf16 pairs read in the rotated order of store8_rot: the 32 lanes hit 32 banks
     float va[8], vb[8];
     unpack8(vraw[0], va);
