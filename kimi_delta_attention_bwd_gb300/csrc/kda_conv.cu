@@ -62,6 +62,38 @@ __device__ __forceinline__ void vst(__nv_bfloat16* p, const float (&v)[4]) {
   *reinterpret_cast<uint2*>(p) = u;
 }
 
+// Raw loads (16 or 8 bytes) and their unpacking: a thread loads a batch of
+// rows before it uses any, so its loads are in flight together.
+__device__ __forceinline__ uint4 raw16(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+__device__ __forceinline__ uint2 raw8(const void* p) { return __ldg(reinterpret_cast<const uint2*>(p)); }
+__device__ __forceinline__ void unpack(const uint4& u, float (&v)[8]) {  // 8 bf16
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int e = 0; e < 4; e++) {
+    const float2 f = __bfloat1622float2(h[e]);
+    v[2 * e] = f.x;
+    v[2 * e + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void unpack(const uint4& u, float (&v)[4]) {  // 4 fp32
+  v[0] = __uint_as_float(u.x); v[1] = __uint_as_float(u.y); v[2] = __uint_as_float(u.z); v[3] = __uint_as_float(u.w);
+}
+__device__ __forceinline__ void unpack(const uint2& u, float (&v)[4]) {  // 4 bf16
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
+template <typename T> struct Raw4;  // the raw type of 4 channels
+template <> struct Raw4<__nv_bfloat16> {
+  using type = uint2;
+  static __device__ __forceinline__ uint2 ld(const __nv_bfloat16* p) { return raw8(p); }
+};
+template <> struct Raw4<float> {
+  using type = uint4;
+  static __device__ __forceinline__ uint4 ld(const float* p) { return raw16(p); }
+};
+constexpr int LB = 4;  // rows per load batch
+
 // Document of token t: the largest d < n_docs with cu[d] <= t (cu non-decreasing
 // from 0; without cu one document).  Returns its start, and its end in *end.
 __device__ __forceinline__ int64_t doc_of(const int32_t* cu, int n_docs, int64_t n_tok, int64_t t, int& d,
@@ -123,26 +155,34 @@ __global__ void __launch_bounds__(CTHR) conv_fwd_kernel(int64_t n_tok, int C, in
       for (int e = 0; e < N; e++) win[k][e] = 0.f;
     }
   }
-#pragma unroll 4
-  for (int64_t t = t0; t < t1; t++) {
-    if (t >= end) {  // a new document: the window restarts from zero
-      next_doc(cu, n_docs, n_tok, t, d, start, end);
+  for (int64_t tb = t0; tb < t1; tb += LB) {
+    uint4 raw[LB];  // the batch's rows, loaded before any is used
 #pragma unroll
-      for (int k = 0; k < KW - 1; k++)
+    for (int k = 0; k < LB; k++)
+      if (tb + k < t1) raw[k] = raw16(x + (tb + k) * C + c0);
 #pragma unroll
-        for (int e = 0; e < N; e++) win[k][e] = 0.f;
+    for (int k = 0; k < LB; k++) {
+      const int64_t t = tb + k;
+      if (t >= t1) break;
+      if (t >= end) {  // a new document: the window restarts from zero
+        next_doc(cu, n_docs, n_tok, t, d, start, end);
+#pragma unroll
+        for (int k2 = 0; k2 < KW - 1; k2++)
+#pragma unroll
+          for (int e = 0; e < N; e++) win[k2][e] = 0.f;
+      }
+      float xt[N], out[N];
+      unpack(raw[k], xt);
+#pragma unroll
+      for (int e = 0; e < N; e++) {
+        const float z = wv[e][0] * win[0][e] + wv[e][1] * win[1][e] + wv[e][2] * win[2][e] + wv[e][3] * xt[e];
+        out[e] = act ? silu(z) : z;
+        win[0][e] = win[1][e];
+        win[1][e] = win[2][e];
+        win[2][e] = xt[e];
+      }
+      vst(y + t * C + c0, out);
     }
-    float xt[N], out[N];
-    vld(x + t * C + c0, xt);
-#pragma unroll
-    for (int e = 0; e < N; e++) {
-      const float z = wv[e][0] * win[0][e] + wv[e][1] * win[1][e] + wv[e][2] * win[2][e] + wv[e][3] * xt[e];
-      out[e] = act ? silu(z) : z;
-      win[0][e] = win[1][e];
-      win[1][e] = win[2][e];
-      win[2][e] = xt[e];
-    }
-    vst(y + t * C + c0, out);
   }
 }
 
@@ -187,7 +227,22 @@ __global__ void __launch_bounds__(CTHR) conv_bwd_kernel(int64_t n_tok, int C, in
     for (int e = 0; e < N; e++) dzw[k][e] = 0.f;
     dsw[k] = start;  // positions before t0 only pair with dz of tokens >= t0 through dx_{< t0}: never emitted
   }
-  for (int64_t u = t0; u < t1 + (KW - 1); u++) {  // dx of the last token needs dz up to t1 + 2
+  using R = typename Raw4<T>::type;
+  const int64_t u1 = t1 + (KW - 1);  // dx of the last token needs dz up to t1 + 2
+  for (int64_t ub = t0; ub < u1; ub += LB) {
+  R rx[LB], rdy[LB];  // the batch's rows of x and dy, loaded before any is used
+#pragma unroll
+  for (int k = 0; k < LB; k++) {
+    rx[k] = rdy[k] = R{};
+    if (ub + k < u1 && ub + k < n_tok) {
+      rx[k] = Raw4<T>::ld(x + (ub + k) * C + c0);
+      rdy[k] = Raw4<T>::ld(dy + (ub + k) * C + c0);
+    }
+  }
+#pragma unroll
+  for (int kb = 0; kb < LB; kb++) {
+    const int64_t u = ub + kb;
+    if (u >= u1) break;
     float dzu[N];
     const bool live = u < n_tok;
     if (live) {
@@ -199,8 +254,8 @@ __global__ void __launch_bounds__(CTHR) conv_bwd_kernel(int64_t n_tok, int C, in
           for (int e = 0; e < N; e++) xw[k][e] = 0.f;
       }
       float xu[N], dyu[N];
-      vld(x + u * C + c0, xu);
-      vld(dy + u * C + c0, dyu);
+      unpack(rx[kb], xu);
+      unpack(rdy[kb], dyu);
 #pragma unroll
       for (int e = 0; e < N; e++) {
         const float z = wv[e][0] * xw[0][e] + wv[e][1] * xw[1][e] + wv[e][2] * xw[2][e] + wv[e][3] * xu[e];
@@ -243,6 +298,7 @@ __global__ void __launch_bounds__(CTHR) conv_bwd_kernel(int64_t n_tok, int C, in
     dsw[0] = dsw[1];
     dsw[1] = dsw[2];
     dsw[2] = dsw[3];
+  }
   }
   float* pp = part + ((int64_t)blockIdx.y * C + c0) * KW;
 #pragma unroll
