@@ -9,10 +9,16 @@
 // a thread owns 16 bytes of channels over a run of tokens and slides its
 // window in registers.
 #include "kda_internal.cuh"
+#include "kda_mma.cuh"
 #include "../../include/kda.h"
 
 namespace kda {
 namespace {
+using mma::bulk_g2s;
+using mma::mbar_expect_tx;
+using mma::mbar_init;
+using mma::mbar_init_fence;
+using mma::mbar_wait;
 
 constexpr int KW = 4;     // kernel width
 constexpr int TBF = 16;   // tokens per thread, forward (more warps in flight; halo reads hit L2)
@@ -23,16 +29,6 @@ template <typename T>
 struct V16 {
   static constexpr int N = 16 / sizeof(T);
 };
-__device__ __forceinline__ void vld(const __nv_bfloat16* p, float (&v)[8]) {
-  const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-  for (int e = 0; e < 4; e++) {
-    const float2 f = __bfloat1622float2(h[e]);
-    v[2 * e] = f.x;
-    v[2 * e + 1] = f.y;
-  }
-}
 __device__ __forceinline__ void vld(const float* p, float (&v)[4]) {
   const float4 f = __ldg(reinterpret_cast<const float4*>(p));
   v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
@@ -127,43 +123,59 @@ __device__ __forceinline__ float dsilu(float z) {
   return s * (1.0f + z * (1.0f - s));
 }
 
+// Forward.  A CTA covers TBF tokens x (CTHR x 16 bytes) of channels: its input
+// rows t0 - 3 .. t1 - 1 are copied into shared memory first, one 1-D bulk copy
+// per row (all in flight together, completion on an mbarrier), then each
+// thread slides its window down its 16-byte column.  Should the bounded wait
+// run out, the thread reads its rows from global memory instead.
 template <typename T>
 __global__ void __launch_bounds__(CTHR) conv_fwd_kernel(int64_t n_tok, int C, int act, const int32_t* __restrict__ cu,
                                                        int n_docs, const T* __restrict__ x,
                                                        const float* __restrict__ w, T* __restrict__ y) {
   constexpr int N = V16<T>::N;
-  const int cv = blockIdx.x * CTHR + threadIdx.x;
-  if (cv >= C / N) return;
-  const int c0 = cv * N;
+  extern __shared__ __align__(16) unsigned char csm[];  // (TBF + KW - 1) rows x CTHR x 16 bytes, then the barrier
+  uint64_t* bar = reinterpret_cast<uint64_t*>(csm + (TBF + KW - 1) * CTHR * 16);
+  const int cblk = blockIdx.x * CTHR * N, cw = min(CTHR * N, C - cblk);  // the CTA's channels
   const int64_t t0 = (int64_t)blockIdx.y * TBF, t1 = t0 + TBF < n_tok ? t0 + TBF : n_tok;
+  const int64_t rb = t0 - (KW - 1), r0 = rb > 0 ? rb : 0;  // row slot of token p: p - rb
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_expect_tx(bar, (uint32_t)((t1 - r0) * cw * sizeof(T)));
+    for (int64_t p = r0; p < t1; p++)
+      bulk_g2s(csm + (p - rb) * CTHR * 16, x + p * C + cblk, (uint32_t)(cw * sizeof(T)), bar);
+  }
+  const int cv = threadIdx.x, c0 = cblk + cv * N;
+  const bool active = cv * N < cw;
   float wv[N][KW];
 #pragma unroll
   for (int e = 0; e < N; e++) {  // the thread's N x 4 taps are contiguous
-    const float4 t4 = __ldg(reinterpret_cast<const float4*>(w + (c0 + e) * KW));
+    float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (active) t4 = __ldg(reinterpret_cast<const float4*>(w + (c0 + e) * KW));
     wv[e][0] = t4.x; wv[e][1] = t4.y; wv[e][2] = t4.z; wv[e][3] = t4.w;
   }
   int d;
   int64_t end;
   int64_t start = doc_of(cu, n_docs, n_tok, t0, d, end);
-  float win[KW - 1][N];  // x_{t-3}, x_{t-2}, x_{t-1}
+  const bool staged = mbar_wait(bar, 0);
+  auto row = [&](int64_t p) -> uint4 {  // this thread's 16 bytes of token p
+    return staged ? *reinterpret_cast<const uint4*>(csm + (p - rb) * CTHR * 16 + cv * 16) : raw16(x + p * C + c0);
+  };
+  if (active) {
+    float win[KW - 1][N];  // x_{t-3}, x_{t-2}, x_{t-1}
 #pragma unroll
-  for (int k = 0; k < KW - 1; k++) {
-    const int64_t p = t0 - (KW - 1) + k;
-    if (p >= start && p >= 0) vld(x + p * C + c0, win[k]);
-    else {
+    for (int k = 0; k < KW - 1; k++) {
+      const int64_t p = rb + k;
+      if (p >= start && p >= 0) unpack(row(p), win[k]);
+      else {
 #pragma unroll
-      for (int e = 0; e < N; e++) win[k][e] = 0.f;
+        for (int e = 0; e < N; e++) win[k][e] = 0.f;
+      }
     }
-  }
-  for (int64_t tb = t0; tb < t1; tb += LB) {
-    uint4 raw[LB];  // the batch's rows, loaded before any is used
-#pragma unroll
-    for (int k = 0; k < LB; k++)
-      if (tb + k < t1) raw[k] = raw16(x + (tb + k) * C + c0);
-#pragma unroll
-    for (int k = 0; k < LB; k++) {
-      const int64_t t = tb + k;
-      if (t >= t1) break;
+    for (int64_t t = t0; t < t1; t++) {
       if (t >= end) {  // a new document: the window restarts from zero
         next_doc(cu, n_docs, n_tok, t, d, start, end);
 #pragma unroll
@@ -172,7 +184,7 @@ __global__ void __launch_bounds__(CTHR) conv_fwd_kernel(int64_t n_tok, int C, in
           for (int e = 0; e < N; e++) win[k2][e] = 0.f;
       }
       float xt[N], out[N];
-      unpack(raw[k], xt);
+      unpack(row(t), xt);
 #pragma unroll
       for (int e = 0; e < N; e++) {
         const float z = wv[e][0] * win[0][e] + wv[e][1] * win[1][e] + wv[e][2] * win[2][e] + wv[e][3] * xt[e];
@@ -184,6 +196,7 @@ __global__ void __launch_bounds__(CTHR) conv_fwd_kernel(int64_t n_tok, int C, in
       vst(y + t * C + c0, out);
     }
   }
+  if (!staged) mbar_wait(bar, 0);  // the copies land before the CTA's shared memory is released
 }
 
 // Backward.  At step u the thread forms dz_u (from x_{u-3..u}) and emits
@@ -338,12 +351,13 @@ extern "C" KDA_API kda_status kda_short_conv_fwd(int64_t n_tok, int C, int dtype
   const int nvec = C / (dtype == KDA_BF16 ? 8 : 4);
   const dim3 grid((nvec + CTHR - 1) / CTHR, (unsigned)((n_tok + TBF - 1) / TBF));
   if (grid.y > 2147483647u) return KDA_ERR_INVALID_ARG;
+  const size_t smem = (TBF + KW - 1) * CTHR * 16 + sizeof(uint64_t);
   prof_begin(K_CONV_FWD, st);
   if (dtype == KDA_BF16)
-    conv_fwd_kernel<__nv_bfloat16><<<grid, CTHR, 0, st>>>(n_tok, C, activation, cu_seqlens, n_docs,
+    conv_fwd_kernel<__nv_bfloat16><<<grid, CTHR, smem, st>>>(n_tok, C, activation, cu_seqlens, n_docs,
                                                            (const __nv_bfloat16*)x, w, (__nv_bfloat16*)y);
   else
-    conv_fwd_kernel<float><<<grid, CTHR, 0, st>>>(n_tok, C, activation, cu_seqlens, n_docs, (const float*)x, w,
+    conv_fwd_kernel<float><<<grid, CTHR, smem, st>>>(n_tok, C, activation, cu_seqlens, n_docs, (const float*)x, w,
                                                    (float*)y);
   prof_end(K_CONV_FWD, st);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
