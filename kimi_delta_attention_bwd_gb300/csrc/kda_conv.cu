@@ -22,7 +22,7 @@ using mma::mbar_wait;
 
 constexpr int KW = 4;     // kernel width
 constexpr int TBF = 16;   // tokens per thread, forward (more warps in flight; halo reads hit L2)
-constexpr int TBB = 32;   // tokens per thread, backward
+constexpr int TBB = 64;   // tokens per thread, backward (fewer weight-gradient partials)
 constexpr int CTHR = 128;
 
 template <typename T>
