@@ -1063,15 +1063,21 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     float pu[4][4], qw[2][4];
     tc::ld_frag<4>(tb + 128, 32 * hk, pu);
     tc::ld_frag<2>(tb + 96, 16 * hk, qw);
-    // PU and KU per 32-column half (warp column hk), [ch][half][rows][32]: the chain CTA of a half
-    // loads its slice in one copy
-    store_acc(pu, w.PU + (ch * 2 + hk) * C * 32, 32, 16 * wI, 0, [](int, int, float v) { return v; });
+    // PU and KU per 32-column half (warp column hk), each half contiguous so that the chain CTA
+    // of a half loads it in one copy, and in fragment order: fragment jt of lane l of warp row wI
+    // (4 values) at float4 (4 wI + jt) x 32 + l, so a warp's store and the chain warp's read of
+    // one fragment cover 512 contiguous bytes
+    float4* pud = reinterpret_cast<float4*>(w.PU + (ch * 2 + hk) * C * 32) + wI * 128 + lane;
+#pragma unroll
+    for (int jt = 0; jt < 4; jt++) pud[32 * jt] = make_float4(pu[jt][0], pu[jt][1], pu[jt][2], pu[jt][3]);
     store_acc_op(qw, QWg, 16 * wI, 16 * hk, [&](int rr, int c, float v) { return op_get(QG, rr, c) - v; });
     if (wI < 2) {  // rows i < dk of the KD^T products
       float ku[4][4], mm[2][4];
       tc::ld_frag<4>(tb + 32, 32 * hk, ku);
       tc::ld_frag<2>(tb + 0, 16 * hk, mm);
-      store_acc(ku, w.KU + (ch * 2 + hk) * DK * 32, 32, 16 * wI, 0, [](int, int, float v) { return v; });
+      float4* kud = reinterpret_cast<float4*>(w.KU + (ch * 2 + hk) * DK * 32) + wI * 128 + lane;
+#pragma unroll
+      for (int jt = 0; jt < 4; jt++) kud[32 * jt] = make_float4(ku[jt][0], ku[jt][1], ku[jt][2], ku[jt][3]);
       store_acc_op(mm, Mg, 16 * wI, 16 * hk, [&](int i, int jc, float v) { return (i == jc ? sm.gam[i] : 0.f) - v; });
     }
   }
@@ -1115,8 +1121,8 @@ __device__ __forceinline__ void slice_to_global(bf16* g, const bf16* s, int col0
 struct FChainStage {
   bf16 M[2 * DK * DK];   // M (split)
   bf16 QW[2 * C * DK];   // QW (split)
-  float KU[DK * NSC];    // columns col0.. of KU
-  float PU[C * NSC];     // columns col0.. of PU
+  float KU[DK * NSC];    // columns col0.. of KU (fragment order)
+  float PU[C * NSC];     // columns col0.. of PU (fragment order)
 };
 struct FChainSm {
   FChainStage st[NSTG];
@@ -1186,30 +1192,37 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
       const Op& Sn = (step & 1) ? S0 : S1;
       zero(snew);
       gemm3<1, false, true>(snew, Mo, 16 * mI, 0, Sc, 16 * jn, 0, DK / 16);
+      // KU in fragment order: this lane's values of columns 16 jn .. are fragments 2 jn, 2 jn + 1
+      const float4* kup = reinterpret_cast<const float4*>(s.KU) + (4 * mI + 2 * jn) * 32 + lane;
 #pragma unroll
-      for (int jj = 0; jj < 2; jj++)
+      for (int jj = 0; jj < 2; jj++) {
+        const float4 k4 = kup[32 * jj];
+        snew[jj][0] += k4.x;
+        snew[jj][1] += k4.y;
+        snew[jj][2] += k4.z;
+        snew[jj][3] += k4.w;
 #pragma unroll
-        for (int hh = 0; hh < 2; hh++) {
-          const int i = 16 * mI + gq + 8 * hh, c = 16 * jn + 8 * jj + 2 * tq;
-          snew[jj][2 * hh] += s.KU[i * NSC + c];
-          snew[jj][2 * hh + 1] += s.KU[i * NSC + c + 1];
-          op_store2(Sn, i, c, snew[jj][2 * hh], snew[jj][2 * hh + 1]);
-        }
+        for (int hh = 0; hh < 2; hh++)
+          op_store2(Sn, 16 * mI + gq + 8 * hh, 16 * jn + 8 * jj + 2 * tq, snew[jj][2 * hh], snew[jj][2 * hh + 1]);
+      }
     } else {
       const int L = w.chunk_len[ci], t0 = w.chunk_tok0[ci];
       float oo[4][4];
       zero(oo);
       gemm3<2, false, true>(oo, QWo, 16 * wq, 0, Sc, 0, 0, DK / 16);
       slice_to_global(w.sS + ((int64_t)ci * H + h) * 2 * DK * DV, Sc.hi, col0, tid - CTH);
+      const float4* pup = reinterpret_cast<const float4*>(s.PU) + 4 * wq * 32 + lane;  // fragment order
 #pragma unroll
-      for (int jj = 0; jj < 4; jj++)
-#pragma unroll
-        for (int hh = 0; hh < 2; hh++) {
-          const int r = 16 * wq + gq + 8 * hh, c = 8 * jj + 2 * tq;
-          if (r < L)
-            *reinterpret_cast<__nv_bfloat162*>(o + ((size_t)(t0 + r) * H + h) * DV + col0 + c) =
-                __floats2bfloat162_rn(oo[jj][2 * hh] + s.PU[r * NSC + c], oo[jj][2 * hh + 1] + s.PU[r * NSC + c + 1]);
-        }
+      for (int jj = 0; jj < 4; jj++) {
+        const float4 p4 = pup[32 * jj];
+        const int r = 16 * wq + gq, c = 8 * jj + 2 * tq;
+        if (r < L)
+          *reinterpret_cast<__nv_bfloat162*>(o + ((size_t)(t0 + r) * H + h) * DV + col0 + c) =
+              __floats2bfloat162_rn(oo[jj][0] + p4.x, oo[jj][1] + p4.y);
+        if (r + 8 < L)
+          *reinterpret_cast<__nv_bfloat162*>(o + ((size_t)(t0 + r + 8) * H + h) * DV + col0 + c) =
+              __floats2bfloat162_rn(oo[jj][2] + p4.z, oo[jj][3] + p4.w);
+      }
     }
   }
   if (io.h_final) {

@@ -52,8 +52,8 @@ struct Ws {
   float* KD;   // [ch][C][dk]  K^ * exp(G_last - G)
   float* gam;  // [ch][dk]     exp(G_last)
   float* Sent; // [ch][dk][dv] state entering the chunk (saved for backward)
-  float* KU;   // [ch][dk][dv] KD^T U              (tensor-core forward scratch)
-  float* PU;   // [ch][C][dv]  P U                 (tensor-core forward scratch)
+  float* KU;   // [ch][2][dk x 32] KD^T U, per 32-column half in fragment order (tensor-core forward scratch)
+  float* PU;   // [ch][2][C x 32]  P U, per 32-column half in fragment order    (tensor-core forward scratch)
   // tensor-core path, split-bf16 operand tiles (hi tile, then lo tile): S
   // entering the chunk (forward chain); T, P = scale P', W, U saved by the
   // forward; the state gradient leaving the chunk (backward chain)
