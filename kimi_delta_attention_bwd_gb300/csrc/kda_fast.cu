@@ -1379,16 +1379,17 @@ __device__ __forceinline__ void blk_ij(int b, int& I, int& J) {
 __device__ __forceinline__ int blk_of(int I, int J) { return I * (I + 1) / 2 + J; }
 
 // The 8 accumulator values a thread holds of a 16 x 16 tile, in fragment
-// order (thread-major, 32 bytes per thread): bwd_grad and bwd_gate use the
-// same warp -> tile mapping, so the hand-over is two float4 per thread.
+// order: bwd_grad and bwd_gate use the same warp -> tile mapping, so the
+// hand-over is two float4 per thread, the second NTH float4 after the first
+// (each store / load instruction of a warp covers 512 contiguous bytes).
 __device__ __forceinline__ void frag_store(float* g, const float (&v)[2][4]) {
-  float4* p = reinterpret_cast<float4*>(g + threadIdx.x * 8);
+  float4* p = reinterpret_cast<float4*>(g) + threadIdx.x;
   p[0] = make_float4(v[0][0], v[0][1], v[0][2], v[0][3]);
-  p[1] = make_float4(v[1][0], v[1][1], v[1][2], v[1][3]);
+  p[NTH] = make_float4(v[1][0], v[1][1], v[1][2], v[1][3]);
 }
 __device__ __forceinline__ void frag_load(const float* g, float (&v)[2][4]) {
-  const float4* p = reinterpret_cast<const float4*>(g + threadIdx.x * 8);
-  const float4 a = p[0], b = p[1];
+  const float4* p = reinterpret_cast<const float4*>(g) + threadIdx.x;
+  const float4 a = p[0], b = p[NTH];
   v[0][0] = a.x; v[0][1] = a.y; v[0][2] = a.z; v[0][3] = a.w;
   v[1][0] = b.x; v[1][1] = b.y; v[1][2] = b.z; v[1][3] = b.w;
 }
