@@ -675,7 +675,7 @@ __device__ __forceinline__ void zero_upper(const Op& t) {
   }
 }
 
-// The chunk-head that the per-chunk kernels run one wave (d.ahead CTAs) after
+// The chunk-head that fwd_chunk runs one wave (d.ahead CTAs) after
 // CTA (j, h), from registers only; false past the last head.  Its table row is
 // loaded with the CTA's own (rows past the last chunk have length 0), and
 // prefetching its inputs into L2 turns the next wave's cold DRAM reads into
@@ -1419,8 +1419,6 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   GradSm& sm = *reinterpret_cast<GradSm*>(smraw);
   const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
-  int j2, h2;
-  const bool pf = ahead_of(d, j, h, j2, h2);
   const bool gdn = d.gate != 0;
   const float* dtb = io.dt_bias + h * (gdn ? 1 : DK);
   float dtv[8];  // dt_bias of this thread's key channels 8 (tid % 4) ..
@@ -1428,7 +1426,6 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   for (int e = 0; e < 8; e++) dtv[e] = dtb[gdn ? 0 : 8 * (tid & 3) + e];
   const float alog = io.A_log[h];
   const int tag = *w.tag, err = *w.err, L = w.chunk_len[j], t0 = w.chunk_tok0[j];  // one round trip
-  const int L2 = pf ? w.chunk_len[j2] : 0, t2 = pf ? w.chunk_tok0[j2] : 0;
   if (tag != d.tag) {
     *w.err = -5;
     return;
@@ -1480,25 +1477,6 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
     bulk_g2s(T.hi, w.sT + ch * 2 * C * C, 4 * C * C, &sm.bar[0]);
   }
 
-  {
-    if (L2 > 0) {
-      const int64_t c2 = (int64_t)j2 * H + h2;
-      prefetch_rows(io.k, DK, t2, L2, H, h2);
-      prefetch_rows(io.f, gdn ? 1 : DK, t2, L2, H, h2);
-      prefetch_rows(io.v, DV, t2, L2, H, h2);
-      prefetch_rows(io.dO, DV, t2, L2, H, h2);
-      prefetch_rows(io.b, 1, t2, L2, H, h2);
-      if (tid == 0) {
-        bulk_prefetch_l2(w.sS + c2 * 2 * DK * DV, 4 * DK * DV);
-        bulk_prefetch_l2(w.sdS + c2 * 2 * DK * DV, 4 * DK * DV);
-        bulk_prefetch_l2(w.sP + c2 * 2 * C * C, 4 * C * C);
-        bulk_prefetch_l2(w.sW + c2 * 2 * C * DK, 4 * C * DK);
-        bulk_prefetch_l2(w.sU + c2 * 2 * C * DV, 4 * C * DV);
-        bulk_prefetch_l2(w.sT + c2 * 2 * C * C, 4 * C * C);
-        bulk_prefetch_l2(w.sA + c2 * NBLK * 16 * PB, NBLK * 16 * PB * 4);
-      }
-    }
-  }
   if (warp == 0) tc::tmem_alloc(&sm.tslot, TCOLS);  // published by the barrier below
 
   // ---- k^, G, beta (thread: row tid / 4, key channels 8 (tid % 4) .., value columns 16 (tid % 4) ..)
@@ -1860,8 +1838,6 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
   GateSm& sm = *reinterpret_cast<GateSm*>(smraw);
   const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
-  int j2, h2;
-  const bool pf = ahead_of(d, j, h, j2, h2);
   const bool gdn = d.gate != 0;
   const float* dtb = io.dt_bias + h * (gdn ? 1 : DK);
   float dtv[8];  // dt_bias of key channels 8 (tid % 4) .. (the prologue's rows)
@@ -1870,7 +1846,6 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
   const float dtl = dtb[gdn ? 0 : lane];  // and of channel `lane` (the gate step)
   const float alog = io.A_log[h];
   const int tag = *w.tag, err = *w.err, L = w.chunk_len[j], t0 = w.chunk_tok0[j];  // one round trip
-  const int L2 = pf ? w.chunk_len[j2] : 0, t2 = pf ? w.chunk_tok0[j2] : 0;
   if (tag != d.tag) {
     *w.err = -5;
     return;
@@ -1881,21 +1856,6 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
   const float a = expf(alog);
   const bf16* fsc = (const bf16*)io.f + h;  // scalar gate: f of this head, stride H
 
-  {
-    if (L2 > 0) {
-      const int64_t c2 = (int64_t)j2 * H + h2;
-      prefetch_rows(io.q, DK, t2, L2, H, h2);
-      prefetch_rows(io.k, DK, t2, L2, H, h2);
-      prefetch_rows(io.f, gdn ? 1 : DK, t2, L2, H, h2);
-      if (tid == 0) {
-        bulk_prefetch_l2(w.gDP + c2 * NBLK * 16 * PB, NBLK * 16 * PB * 4);
-        bulk_prefetch_l2(w.gMA + c2 * NBLK * 16 * PB, NBLK * 16 * PB * 4);
-        bulk_prefetch_l2(w.gQG + c2 * NTH * 8, NTH * 8 * 4);
-        bulk_prefetch_l2(w.gKD + c2 * NTH * 8, NTH * 8 * 4);
-        bulk_prefetch_l2(w.gKG + c2 * NTH * 8, NTH * 8 * 4);
-      }
-    }
-  }
   // ---- group 1: raw q, k, f (rows past the chunk end zeroed);  group 2: dP', MA
   for (int idx = tid; idx < C * 4; idx += NTH) {
     const int r = idx >> 2, p = idx & 3, o = r * DK + 8 * p;
@@ -2286,7 +2246,7 @@ cudaError_t launch_fast_fwd(const Dims& d0, const FwdIO& io, const Ws& w, cudaSt
 
 cudaError_t launch_fast_bwd(const Dims& d0, const BwdIO& io, const Ws& w, cudaStream_t st) {
   Dims d = d0;
-  d.ahead = wave_ctas();
+  d.ahead = 0;  // the backward's chunk kernels prefetch nothing (measured: the L2 prefetch of the next wave slowed them)
   const size_t sc = sizeof(fast::BChainSm), s1 = sizeof(fast::GradSm), s2 = sizeof(fast::GateSm);
   cudaError_t e = cudaFuncSetAttribute(fast::bwd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
   if (e == cudaSuccess)
