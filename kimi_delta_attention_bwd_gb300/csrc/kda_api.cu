@@ -290,6 +290,7 @@ static kda_status check_problem(const kda_problem* p, Dims* d) {
                               : (int64_t)p->B * ((p->T + C - 1) / C);
   if (ncm < 1) ncm = 1;
   if (ncm > (int64_t)1 << 30) return KDA_ERR_INVALID_ARG;
+  if (ncm * p->H > (int64_t)2147483647) return KDA_ERR_INVALID_ARG;  // one CTA per chunk-head on a 1-D grid
   d->nc_max = (int)ncm;
   uint32_t hsh = 2166136261u;  // FNV-1a over the sizes that fix the layout
   const int32_t vals[9] = {p->B, p->T, p->H, p->dk, p->dv, p->dtype, n_docs, p->gate, 0x4b4441};

@@ -675,16 +675,18 @@ __device__ __forceinline__ void zero_upper(const Op& t) {
   }
 }
 
-// The chunk-head that fwd_chunk runs one wave (d.ahead CTAs) after
-// CTA (j, h), from registers only; false past the last head.  Its table row is
+// The per-chunk kernels run on a 1-D grid, heads fastest: CTA n is chunk n / H
+// of head n % H, so the H heads of a chunk, whose rows share the token-major
+// 128-byte lines, run together.  The chunk-head that fwd_chunk runs one wave
+// (d.ahead CTAs) after CTA (j, h), from registers only; false past the last chunk.  Its table row is
 // loaded with the CTA's own (rows past the last chunk have length 0), and
 // prefetching its inputs into L2 turns the next wave's cold DRAM reads into
 // L2 hits.
 __device__ __forceinline__ bool ahead_of(const Dims& d, int j, int h, int& j2, int& h2) {
-  const int64_t nxt = (int64_t)h * d.nc_max + j + d.ahead;
-  j2 = (int)(nxt % d.nc_max);
-  h2 = (int)(nxt / d.nc_max);
-  return d.ahead > 0 && h2 < d.H;
+  const int64_t nxt = (int64_t)j * d.H + h + d.ahead;
+  j2 = (int)(nxt / d.H);
+  h2 = (int)(nxt % d.H);
+  return d.ahead > 0 && j2 < d.nc_max;
 }
 // A thread's 8 consecutive channel values rotated by q4 pairs in place:
 // v'[2 p + b] = v[2 ((p + q4) & 3) + b].  Stored by store8_rot, the 32 lanes of
@@ -760,7 +762,7 @@ static_assert(offsetof(ChunkSm, x) % 16 == 0 && offsetof(ChunkSm, am) % 16 == 0 
 __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws w) {
   extern __shared__ __align__(16) unsigned char smraw[];
   ChunkSm& sm = *reinterpret_cast<ChunkSm*>(smraw);
-  const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int j = (int)(blockIdx.x / (unsigned)d.H), h = (int)(blockIdx.x % (unsigned)d.H), tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int j2, h2;
   const bool pf = ahead_of(d, j, h, j2, h2);
   const int err = *w.err, L = w.chunk_len[j], t0 = w.chunk_tok0[j];  // one round trip
@@ -1417,7 +1419,7 @@ static_assert(offsetof(GradSm, rk) % 16 == 0 && offsetof(GradSm, gg) % 16 == 0, 
 __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w) {
   extern __shared__ __align__(16) unsigned char smraw[];
   GradSm& sm = *reinterpret_cast<GradSm*>(smraw);
-  const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int j = (int)(blockIdx.x / (unsigned)d.H), h = (int)(blockIdx.x % (unsigned)d.H), tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
   const bool gdn = d.gate != 0;
   const float* dtb = io.dt_bias + h * (gdn ? 1 : DK);
@@ -1836,7 +1838,7 @@ static_assert(offsetof(GateSm, rq) % 16 == 0 && offsetof(GateSm, rk) % 16 == 0 &
 __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w) {
   extern __shared__ __align__(16) unsigned char smraw[];
   GateSm& sm = *reinterpret_cast<GateSm*>(smraw);
-  const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int j = (int)(blockIdx.x / (unsigned)d.H), h = (int)(blockIdx.x % (unsigned)d.H), tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
   const bool gdn = d.gate != 0;
   const float* dtb = io.dt_bias + h * (gdn ? 1 : DK);
@@ -2234,7 +2236,7 @@ cudaError_t launch_fast_fwd(const Dims& d0, const FwdIO& io, const Ws& w, cudaSt
     e = cudaFuncSetAttribute(fast::fwd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
   if (e != cudaSuccess) return e;
   prof_begin(K_FWD_CHUNK, st);
-  fast::fwd_chunk_kernel<<<dim3(d.nc_max, d.H), fast::NTH, s1, st>>>(d, io, w);
+  fast::fwd_chunk_kernel<<<dim3(d.nc_max * d.H), fast::NTH, s1, st>>>(d, io, w);
   prof_end(K_FWD_CHUNK, st);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -2260,12 +2262,12 @@ cudaError_t launch_fast_bwd(const Dims& d0, const BwdIO& io, const Ws& w, cudaSt
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_begin(K_BWD_GRAD, st);
-  fast::bwd_grad_kernel<<<dim3(d.nc_max, d.H), fast::NTH, s1, st>>>(d, io, w);
+  fast::bwd_grad_kernel<<<dim3(d.nc_max * d.H), fast::NTH, s1, st>>>(d, io, w);
   prof_end(K_BWD_GRAD, st);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_begin(K_BWD_GATE, st);
-  fast::bwd_gate_kernel<<<dim3(d.nc_max, d.H), fast::NTH, s2, st>>>(d, io, w);
+  fast::bwd_gate_kernel<<<dim3(d.nc_max * d.H), fast::NTH, s2, st>>>(d, io, w);
   prof_end(K_BWD_GATE, st);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
