@@ -677,8 +677,8 @@ __device__ __forceinline__ void zero_upper(const Op& t) {
 
 // The per-chunk kernels run on a 1-D grid, heads fastest: CTA n is chunk n / H
 // of head n % H, so the H heads of a chunk, whose rows share the token-major
-// 128-byte lines, run together.  The chunk-head that fwd_chunk runs one wave
-// (d.ahead CTAs) after CTA (j, h), from registers only; false past the last chunk.  Its table row is
+// 128-byte lines, run together.  The chunk-head that fwd_chunk runs d.ahead
+// CTAs (half a wave) after CTA (j, h), from registers only; false past the last chunk.  Its table row is
 // loaded with the CTA's own (rows past the last chunk have length 0), and
 // prefetching its inputs into L2 turns the next wave's cold DRAM reads into
 // L2 hits.
@@ -2219,7 +2219,7 @@ static int wave_ctas() {
 
 cudaError_t launch_fast_fwd(const Dims& d0, const FwdIO& io, const Ws& w, cudaStream_t st, bool fused) {
   Dims d = d0;
-  d.ahead = wave_ctas();
+  d.ahead = wave_ctas() / 2;  // fwd_chunk's L2 prefetch: the CTA half a wave later
   cudaError_t e;
   if (fused) {
     const size_t smem = sizeof(fast::FwdSm);
