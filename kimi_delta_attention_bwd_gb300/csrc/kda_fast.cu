@@ -677,11 +677,11 @@ __device__ __forceinline__ void zero_upper(const Op& t) {
 
 // The per-chunk kernels run on a 1-D grid, heads fastest: CTA n is chunk n / H
 // of head n % H, so the H heads of a chunk, whose rows share the token-major
-// 128-byte lines, run together.  The chunk-head that fwd_chunk runs d.ahead
-// CTAs (half a wave) after CTA (j, h), from registers only; false past the last chunk.  Its table row is
-// loaded with the CTA's own (rows past the last chunk have length 0), and
-// prefetching its inputs into L2 turns the next wave's cold DRAM reads into
-// L2 hits.
+// 128-byte lines, run together.  ahead_of gives the chunk-head that fwd_chunk
+// runs d.ahead CTAs (half a wave) after CTA (j, h), from registers only; false
+// past the last chunk.  Its table row is loaded with the CTA's own (rows past
+// the last chunk have length 0), and prefetching its inputs into L2 turns the
+// later CTA's cold DRAM reads into L2 hits.
 __device__ __forceinline__ bool ahead_of(const Dims& d, int j, int h, int& j2, int& h2) {
   const int64_t nxt = (int64_t)j * d.H + h + d.ahead;
   j2 = (int)(nxt / d.H);
