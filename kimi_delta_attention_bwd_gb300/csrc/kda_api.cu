@@ -125,14 +125,14 @@ static size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 struct Layout {
   size_t total;
   size_t off_err, off_nch, off_dc0, off_ct0, off_cl, off_cd;
-  size_t off_W, off_U, off_P, off_QG, off_KD, off_gam, off_Sent, off_M, off_QW, off_KU, off_PU;
+  size_t off_W, off_U, off_P, off_QG, off_KD, off_gam, off_Sent, off_CH;
   size_t off_sT, off_sP, off_sW, off_sU, off_sA, off_gDP, off_gMA, off_gQG, off_gKD, off_gKG, off_gdg;
   size_t off_dE, off_dSn, off_pA, off_pdt, off_scr;
 };
 
 // Workspace layout.  Both paths start with the error word, the saved-problem
 // tag and the chunk table.  The tensor-core path (d.fast) keeps per chunk and
-// head M, QW (read again by the backward scan), KU and PU, and for the
+// head one block of M, QW (read again by the backward scan), KU and PU, and for the
 // backward the entry states, the state gradients and the parameter-gradient
 // partials; its fused forward (fused = true) needs the table alone.  The
 // general path keeps its fp32 intra-chunk factors and scratch.
@@ -149,10 +149,7 @@ static Layout layout(const Dims& d, int for_bwd, bool fused = false) {
   L.off_cd = take(4 * (size_t)d.nc_max);
   if (d.fast) {
     if (!fused) {
-      L.off_M = take(4 * nch * d.dk * d.dk);
-      L.off_QW = take(4 * nch * C * d.dk);
-      L.off_KU = take(4 * nch * d.dk * d.dv);
-      L.off_PU = take(4 * nch * C * d.dv);
+      L.off_CH = take(4 * nch * (d.dk * d.dk + C * d.dk + d.dk * d.dv + C * d.dv));  // M, QW, KU, PU
       L.off_Sent = take(4 * nch * d.dk * d.dv);  // split-bf16 tiles: 4 bytes per element
     }
     if (for_bwd) {
@@ -211,10 +208,7 @@ static Ws bind(void* ws, const Layout& L, const Dims& d, int for_bwd) {
   w.KD = at(L.off_KD);
   w.gam = at(L.off_gam);
   w.Sent = for_bwd ? at(L.off_Sent) : nullptr;
-  w.sM = bat(L.off_M);
-  w.sQW = bat(L.off_QW);
-  w.KU = at(L.off_KU);
-  w.PU = at(L.off_PU);
+  w.chb = L.off_CH ? (unsigned char*)(p + L.off_CH) : nullptr;
   w.dE = for_bwd ? at(L.off_dE) : nullptr;
   w.dSn = for_bwd ? at(L.off_dSn) : nullptr;
   w.pA = for_bwd ? at(L.off_pA) : nullptr;

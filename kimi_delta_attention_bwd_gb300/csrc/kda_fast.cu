@@ -54,6 +54,17 @@ constexpr float SPAN2 = SPAN_MAX * LOG2E;
 constexpr bool SF = true;  // forward chain products
 
 __device__ __forceinline__ int pidx(int I, int J) { return I * (I - 1) / 2 + J; }
+
+// The chain operands of a chunk-head in one block, [KU0 | PU0 | M | QW | KU1 |
+// PU1] (byte offsets below; KU, PU per 32-column half in fragment order, M, QW
+// split bf16): either half's fwd_state stage (its KU and PU with the shared M
+// and QW) and bwd_scan's M | QW are each one contiguous copy.
+constexpr int CB_KU0 = 0, CB_PU0 = 4 * DK * 32, CB_M = CB_PU0 + 4 * C * 32, CB_QW = CB_M + 4 * DK * DK,
+              CB_KU1 = CB_QW + 4 * C * DK, CB_PU1 = CB_KU1 + 4 * DK * 32, CB_BYTES = CB_PU1 + 4 * C * 32;
+constexpr int CB_STAGE = CB_KU1 - CB_KU0;  // one half's stage: 24 KB from CB_KU0 (half 0) or CB_M (half 1)
+static_assert(CB_BYTES == 4 * (DK * DK + C * DK + DK * DV + C * DV) && CB_BYTES - CB_M == CB_STAGE,
+              "chain block layout");
+__device__ __forceinline__ unsigned char* chblk(const Ws& w, int64_t ch) { return w.chb + ch * CB_BYTES; }
 __device__ __forceinline__ float bfl(bf16 x) { return __bfloat162float(x); }
 
 // Arrays of the intra-chunk recomputation shared by the forward and backward.
@@ -1060,8 +1071,9 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
   if (!round_done()) { bail(); return; }
   {
     const int wI = warp & 3, hk = warp >> 2;
-    const Op QWg{w.sQW + ch * 2 * C * DK, w.sQW + ch * 2 * C * DK + C * DK, DK};
-    const Op Mg{w.sM + ch * 2 * DK * DK, w.sM + ch * 2 * DK * DK + DK * DK, DK};
+    bf16* qwg = reinterpret_cast<bf16*>(chblk(w, ch) + CB_QW);
+    bf16* mg = reinterpret_cast<bf16*>(chblk(w, ch) + CB_M);
+    const Op QWg{qwg, qwg + C * DK, DK}, Mg{mg, mg + DK * DK, DK};
     float pu[4][4], qw[2][4];
     tc::ld_frag<4>(tb + 128, 32 * hk, pu);
     tc::ld_frag<2>(tb + 96, 16 * hk, qw);
@@ -1069,7 +1081,7 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     // of a half loads it in one copy, and in fragment order: fragment jt of lane l of warp row wI
     // (4 values) at float4 (4 wI + jt) x 32 + l, so a warp's store and the chain warp's read of
     // one fragment cover 512 contiguous bytes
-    float4* pud = reinterpret_cast<float4*>(w.PU + (ch * 2 + hk) * C * 32) + wI * 128 + lane;
+    float4* pud = reinterpret_cast<float4*>(chblk(w, ch) + (hk ? CB_PU1 : CB_PU0)) + wI * 128 + lane;
 #pragma unroll
     for (int jt = 0; jt < 4; jt++) pud[32 * jt] = make_float4(pu[jt][0], pu[jt][1], pu[jt][2], pu[jt][3]);
     store_acc_op(qw, QWg, 16 * wI, 16 * hk, [&](int rr, int c, float v) { return op_get(QG, rr, c) - v; });
@@ -1077,7 +1089,7 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
       float ku[4][4], mm[2][4];
       tc::ld_frag<4>(tb + 32, 32 * hk, ku);
       tc::ld_frag<2>(tb + 0, 16 * hk, mm);
-      float4* kud = reinterpret_cast<float4*>(w.KU + (ch * 2 + hk) * DK * 32) + wI * 128 + lane;
+      float4* kud = reinterpret_cast<float4*>(chblk(w, ch) + (hk ? CB_KU1 : CB_KU0)) + wI * 128 + lane;
 #pragma unroll
       for (int jt = 0; jt < 4; jt++) kud[32 * jt] = make_float4(ku[jt][0], ku[jt][1], ku[jt][2], ku[jt][3]);
       store_acc_op(mm, Mg, 16 * wI, 16 * hk, [&](int i, int jc, float v) { return (i == jc ? sm.gam[i] : 0.f) - v; });
@@ -1120,20 +1132,15 @@ __device__ __forceinline__ void slice_to_global(bf16* g, const bf16* s, int col0
   }
 }
 
-struct FChainStage {
-  bf16 M[2 * DK * DK];   // M (split)
-  bf16 QW[2 * C * DK];   // QW (split)
-  float KU[DK * NSC];    // columns col0.. of KU (fragment order)
-  float PU[C * NSC];     // columns col0.. of PU (fragment order)
+struct FChainStage {  // one copy of this half's part of the chain block: KU, PU, M, QW (half 0)
+  __align__(16) unsigned char raw[CB_STAGE];  // or M, QW, KU, PU (half 1)
 };
 struct FChainSm {
   FChainStage st[NSTG];
   bf16 S[2][2 * DK * NSC];  // the carried state (split), double-buffered
   uint64_t bar[NSTG];       // stage completion
 };
-static_assert(sizeof(FChainStage) % 16 == 0 && offsetof(FChainStage, QW) % 16 == 0 && offsetof(FChainStage, KU) % 16 == 0 &&
-                  offsetof(FChainStage, PU) % 16 == 0,
-              "bulk-copy targets need 16-byte alignment");
+static_assert(sizeof(FChainStage) % 16 == 0, "bulk-copy targets need 16-byte alignment");
 
 // fwd_state: warps 0..3 carry the state (S' = M S + KU into the other buffer
 // of the double-buffered tile), warps 4..7 write the output O = QW S + PU and
@@ -1159,19 +1166,17 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
     mbar_init_fence();
   }
   __syncthreads();  // the barriers are initialised before any thread waits on them
-  auto prefetch = [&](int step) {  // thread 0: the stage of `step` (M, QW, this half of KU and PU)
-    if (step < n && tid == 0) {
+  // the stage of `step`: one copy, issued by a side-group thread (not on the carry warps' path)
+  const int oKU = blockIdx.z ? CB_KU1 - CB_M : 0, oPU = oKU + (CB_PU0 - CB_KU0);
+  const int oM = blockIdx.z ? 0 : CB_M - CB_KU0, oQW = oM + (CB_QW - CB_M);
+  auto prefetch = [&](int step) {
+    if (step < n && tid == CTH) {
       const int slot = step % NSTG;
-      FChainStage& s = sm.st[slot];
-      const int64_t ch = (int64_t)(cb + step) * H + h, hc = ch * 2 + blockIdx.z;
-      mbar_expect_tx(&sm.bar[slot], (uint32_t)sizeof(FChainStage));
-      bulk_g2s(s.M, w.sM + ch * 2 * DK * DK, 4 * DK * DK, &sm.bar[slot]);
-      bulk_g2s(s.QW, w.sQW + ch * 2 * C * DK, 4 * C * DK, &sm.bar[slot]);
-      bulk_g2s(s.KU, w.KU + hc * DK * NSC, 4 * DK * NSC, &sm.bar[slot]);
-      bulk_g2s(s.PU, w.PU + hc * C * NSC, 4 * C * NSC, &sm.bar[slot]);
+      const int64_t ch = (int64_t)(cb + step) * H + h;
+      mbar_expect_tx(&sm.bar[slot], (uint32_t)CB_STAGE);
+      bulk_g2s(sm.st[slot].raw, chblk(w, ch) + (blockIdx.z ? CB_M : CB_KU0), CB_STAGE, &sm.bar[slot]);
     }
   };
-  static_assert(sizeof(FChainStage) == 4 * DK * DK + 4 * C * DK + 4 * DK * NSC + 4 * C * NSC, "stage bytes");
   for (int s = 0; s < NSTG - 1; s++) prefetch(s);
   const bool carry = warp < 4;
   const int wq = warp & 3, mI = wq & 1, jn = wq >> 1;
@@ -1187,15 +1192,19 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
       return;
     }  // this step's stage and state are visible; the other state buffer is free
     prefetch(step + NSTG - 1);
-    const Op Mo{const_cast<bf16*>(s.M), const_cast<bf16*>(s.M) + DK * DK, DK};
-    const Op QWo{const_cast<bf16*>(s.QW), const_cast<bf16*>(s.QW) + C * DK, DK};
+    bf16* smp = reinterpret_cast<bf16*>(const_cast<unsigned char*>(s.raw) + oM);
+    bf16* sqp = reinterpret_cast<bf16*>(const_cast<unsigned char*>(s.raw) + oQW);
+    const float* sku = reinterpret_cast<const float*>(s.raw + oKU);
+    const float* spu = reinterpret_cast<const float*>(s.raw + oPU);
+    const Op Mo{smp, smp + DK * DK, DK};
+    const Op QWo{sqp, sqp + C * DK, DK};
     const Op& Sc = (step & 1) ? S1 : S0;
     if (carry) {
       const Op& Sn = (step & 1) ? S0 : S1;
       zero(snew);
       gemm3<1, false, true>(snew, Mo, 16 * mI, 0, Sc, 16 * jn, 0, DK / 16);
       // KU in fragment order: this lane's values of columns 16 jn .. are fragments 2 jn, 2 jn + 1
-      const float4* kup = reinterpret_cast<const float4*>(s.KU) + (4 * mI + 2 * jn) * 32 + lane;
+      const float4* kup = reinterpret_cast<const float4*>(sku) + (4 * mI + 2 * jn) * 32 + lane;
 #pragma unroll
       for (int jj = 0; jj < 2; jj++) {
         const float4 k4 = kup[32 * jj];
@@ -1213,7 +1222,7 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
       zero(oo);
       gemm3<2, false, true>(oo, QWo, 16 * wq, 0, Sc, 0, 0, DK / 16);
       slice_to_global(w.sS + ((int64_t)ci * H + h) * 2 * DK * DV, Sc.hi, col0, tid - CTH);
-      const float4* pup = reinterpret_cast<const float4*>(s.PU) + 4 * wq * 32 + lane;  // fragment order
+      const float4* pup = reinterpret_cast<const float4*>(spu) + 4 * wq * 32 + lane;  // fragment order
 #pragma unroll
       for (int jj = 0; jj < 4; jj++) {
         const float4 p4 = pup[32 * jj];
@@ -1257,7 +1266,8 @@ struct BChainSm {
   bf16 dS[2 * DK * NSC];  // the carried state gradient (split)
   uint64_t bar[NSTG];     // completion of the stage's M and QW
 };
-static_assert(sizeof(BChainStage) % 16 == 0 && offsetof(BChainStage, QW) % 16 == 0, "bulk-copy targets need 16-byte alignment");
+static_assert(sizeof(BChainStage) % 16 == 0 && offsetof(BChainStage, QW) == 4 * DK * DK && offsetof(BChainStage, dO) == CB_KU1 - CB_M,
+              "M | QW arrive in one copy");
 
 __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
   extern __shared__ __align__(16) unsigned char smraw[];
@@ -1287,10 +1297,9 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
       BChainStage& s = sm.st[slot];
       const int ci = ce - 1 - step, L = w.chunk_len[ci], t0 = w.chunk_tok0[ci];
       const int64_t ch = (int64_t)ci * H + h;
-      if (tid == 0) {
-        mbar_expect_tx(&sm.bar[slot], 4 * DK * DK + 4 * C * DK);
-        bulk_g2s(s.M, w.sM + ch * 2 * DK * DK, 4 * DK * DK, &sm.bar[slot]);
-        bulk_g2s(s.QW, w.sQW + ch * 2 * C * DK, 4 * C * DK, &sm.bar[slot]);
+      if (tid == 0) {  // M | QW, adjacent in the chain block and in the stage
+        mbar_expect_tx(&sm.bar[slot], CB_KU1 - CB_M);
+        bulk_g2s(s.M, chblk(w, ch) + CB_M, CB_KU1 - CB_M, &sm.bar[slot]);
       }
       for (int idx = tid; idx < C * NSC / 8; idx += CTH) {
         const int r = idx / (NSC / 8), p = idx % (NSC / 8);

@@ -52,15 +52,15 @@ struct Ws {
   float* KD;   // [ch][C][dk]  K^ * exp(G_last - G)
   float* gam;  // [ch][dk]     exp(G_last)
   float* Sent; // [ch][dk][dv] state entering the chunk (saved for backward)
-  float* KU;   // [ch][2][dk x 32] KD^T U, per 32-column half in fragment order (tensor-core forward scratch)
-  float* PU;   // [ch][2][C x 32]  P U, per 32-column half in fragment order    (tensor-core forward scratch)
   // tensor-core path, split-bf16 operand tiles (hi tile, then lo tile): S
   // entering the chunk (forward chain); T, P = scale P', W, U saved by the
   // forward; the state gradient leaving the chunk (backward chain)
   __nv_bfloat16 *sS, *sT, *sP, *sW, *sU, *sdS;
   // M = Diag(gamma) - KD^T W [ch][dk][dk] and QW = QG - P W [ch][C][dk] (split
   // tiles from the per-chunk forward; both chains read them)
-  __nv_bfloat16 *sM, *sQW;
+  // tensor-core forward: per chunk-head the chain operands M, QW (split bf16) and KU, PU (fp32,
+  // per 32-column half in fragment order) in one block, [KU0 | PU0 | M | QW | KU1 | PU1]
+  unsigned char* chb;
   float* sA;   // [ch][10][16][16] A' (unscaled) lower 16 x 16 blocks
   // tensor-core backward, bwd_grad -> bwd_gate
   float *gDP, *gMA;        // [ch][10][16][16] dP', beta dA lower blocks
