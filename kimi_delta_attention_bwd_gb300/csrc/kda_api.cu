@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* cu, Di
   __shared__ int s_bad;
   __shared__ int s_carry;
   __shared__ int s_wsum[32];
+  pdl_release();  // fwd_chunk may launch; it waits for this table before reading it
   const int tid = threadIdx.x, n = d.n_docs;
   auto off = [&](int i) -> int { return cu ? cu[i] : i * d.T; };
   if (tid == 0) {

@@ -389,6 +389,7 @@ constexpr int RTH = 1024, RG = RTH / 32;
 __global__ void __launch_bounds__(RTH) bwd_reduce_kernel(Dims d, BwdIO io, Ws w) {
   const int h = blockIdx.x, tid = threadIdx.x, grp = tid >> 5, lane = tid & 31, H = d.H, dk = d.dk;
   __shared__ float red[RTH];
+  pdl_wait();  // the per-chunk partials of the kernel before
   if (!saved_ok(d, w.tag, w.err)) return;
   const int nc = *w.n_chunks;
   {
@@ -481,9 +482,9 @@ cudaError_t launch_bwd_intra(int dtype, const Dims& d, const BwdIO& io, const Ws
 }
 cudaError_t launch_bwd_reduce(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st) {
   prof_begin(K_BWD_REDUCE, st);
-  bwd_reduce_kernel<<<d.H, RTH, 0, st>>>(d, io, w);
+  const cudaError_t e = launch_pdl(bwd_reduce_kernel, dim3(d.H), dim3(RTH), 0, st, d, io, w);
   prof_end(K_BWD_REDUCE, st);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace kda

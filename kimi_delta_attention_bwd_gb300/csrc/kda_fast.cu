@@ -774,6 +774,8 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
   extern __shared__ __align__(16) unsigned char smraw[];
   ChunkSm& sm = *reinterpret_cast<ChunkSm*>(smraw);
   const int j = (int)(blockIdx.x / (unsigned)d.H), h = (int)(blockIdx.x % (unsigned)d.H), tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait();     // the chunk table of the kernel before
+  pdl_release();  // fwd_state may launch (it waits for this grid)
   int j2, h2;
   const bool pf = ahead_of(d, j, h, j2, h2);
   const int err = *w.err, L = w.chunk_len[j], t0 = w.chunk_tok0[j];  // one round trip
@@ -1150,6 +1152,7 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
   FChainSm& sm = *reinterpret_cast<FChainSm*>(smraw);
   const int doc = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * NSC, tid = threadIdx.x, warp = tid >> 5;
   const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+  pdl_wait();  // fwd_chunk's products
   if (*w.err != 0) return;
   const int H = d.H;
   const int cb = w.doc_chunk0[doc], n = w.doc_chunk0[doc + 1] - cb;
@@ -1274,6 +1277,7 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
   BChainSm& sm = *reinterpret_cast<BChainSm*>(smraw);
   const int doc = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * NSC, tid = threadIdx.x, warp = tid >> 5;
   const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+  pdl_release();  // bwd_grad may launch: it waits for this grid before reading dS
   if (!saved_ok(d, w.tag, w.err)) return;
   const int H = d.H;
   const int cb = w.doc_chunk0[doc], ce = w.doc_chunk0[doc + 1], n = ce - cb;
@@ -1436,6 +1440,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
 #pragma unroll
   for (int e = 0; e < 8; e++) dtv[e] = dtb[gdn ? 0 : 8 * (tid & 3) + e];
   const float alog = io.A_log[h];
+  pdl_release();  // bwd_gate may launch: it waits for this grid before its hand-over reads
   const int tag = *w.tag, err = *w.err, L = w.chunk_len[j], t0 = w.chunk_tok0[j];  // one round trip
   if (tag != d.tag) {
     *w.err = -5;
@@ -1481,11 +1486,12 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
     mbar_init_fence();
     mbar_expect_tx(&sm.bar[0], 2 * 4 * DK * DV + 2 * 4 * C * C + 4 * C * DK + 4 * C * DV);
     bulk_g2s(S.hi, w.sS + ch * 2 * DK * DV, 4 * DK * DV, &sm.bar[0]);
-    bulk_g2s(dS.hi, w.sdS + ch * 2 * DK * DV, 4 * DK * DV, &sm.bar[0]);
     bulk_g2s(P.hi, w.sP + ch * 2 * C * C, 4 * C * C, &sm.bar[0]);
     bulk_g2s(W.hi, w.sW + ch * 2 * C * DK, 4 * C * DK, &sm.bar[0]);
     bulk_g2s(U.hi, w.sU + ch * 2 * C * DV, 4 * C * DV, &sm.bar[0]);
     bulk_g2s(T.hi, w.sT + ch * 2 * C * C, 4 * C * C, &sm.bar[0]);
+    pdl_wait();  // dS' is bwd_scan's (the kernel before): the forward's tiles above are not
+    bulk_g2s(dS.hi, w.sdS + ch * 2 * DK * DV, 4 * DK * DV, &sm.bar[0]);
   }
 
   if (warp == 0) tc::tmem_alloc(&sm.tslot, TCOLS);  // published by the barrier below
@@ -1856,6 +1862,7 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
   for (int e = 0; e < 8; e++) dtv[e] = dtb[gdn ? 0 : 8 * (tid & 3) + e];
   const float dtl = dtb[gdn ? 0 : lane];  // and of channel `lane` (the gate step)
   const float alog = io.A_log[h];
+  pdl_release();  // bwd_reduce may launch (it waits for this grid)
   const int tag = *w.tag, err = *w.err, L = w.chunk_len[j], t0 = w.chunk_tok0[j];  // one round trip
   if (tag != d.tag) {
     *w.err = -5;
@@ -1883,6 +1890,7 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
     }
   }
   cp_commit();
+  pdl_wait();  // every read below of bwd_grad's hand-over (the kernel before) follows this
   if (tid == 0) {
     mbar_init(&sm.bar, 1);
     mbar_init_fence();
@@ -2245,14 +2253,15 @@ cudaError_t launch_fast_fwd(const Dims& d0, const FwdIO& io, const Ws& w, cudaSt
     e = cudaFuncSetAttribute(fast::fwd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
   if (e != cudaSuccess) return e;
   prof_begin(K_FWD_CHUNK, st);
-  fast::fwd_chunk_kernel<<<dim3(d.nc_max * d.H), fast::NTH, s1, st>>>(d, io, w);
+  e = launch_pdl(fast::fwd_chunk_kernel, dim3(d.nc_max * d.H), dim3(fast::NTH), s1, st, d, io, w);
   prof_end(K_FWD_CHUNK, st);
-  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_begin(K_FWD_STATE, st);
-  fast::fwd_state_kernel<<<dim3(d.n_docs, d.H, fast::DV / fast::NSC), 2 * fast::CTH, s2, st>>>(d, io, w);
+  e = launch_pdl(fast::fwd_state_kernel, dim3(d.n_docs, d.H, fast::DV / fast::NSC), dim3(2 * fast::CTH), s2, st, d,
+                 io, w);
   prof_end(K_FWD_STATE, st);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_fast_bwd(const Dims& d0, const BwdIO& io, const Ws& w, cudaStream_t st) {
@@ -2271,14 +2280,14 @@ cudaError_t launch_fast_bwd(const Dims& d0, const BwdIO& io, const Ws& w, cudaSt
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_begin(K_BWD_GRAD, st);
-  fast::bwd_grad_kernel<<<dim3(d.nc_max * d.H), fast::NTH, s1, st>>>(d, io, w);
+  e = launch_pdl(fast::bwd_grad_kernel, dim3(d.nc_max * d.H), dim3(fast::NTH), s1, st, d, io, w);
   prof_end(K_BWD_GRAD, st);
-  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_begin(K_BWD_GATE, st);
-  fast::bwd_gate_kernel<<<dim3(d.nc_max * d.H), fast::NTH, s2, st>>>(d, io, w);
+  e = launch_pdl(fast::bwd_gate_kernel, dim3(d.nc_max * d.H), dim3(fast::NTH), s2, st, d, io, w);
   prof_end(K_BWD_GATE, st);
-  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_bwd_reduce(d, io, w, st);
 }

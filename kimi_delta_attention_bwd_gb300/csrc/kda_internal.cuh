@@ -113,6 +113,21 @@ struct BwdIO {
 };
 
 // Launch wrappers (return cudaGetLastError of their launches).
+// Launches kernel k with the programmatic-stream-serialization attribute (see pdl_wait).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, args...);
+}
 cudaError_t launch_chunk_table(const int32_t* cu, const Dims& d, const Ws& w, cudaStream_t st);
 cudaError_t launch_fwd_intra(int dtype, const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st);
 cudaError_t launch_fwd_scan(int dtype, const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st);
@@ -164,6 +179,15 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 __device__ __forceinline__ float softplus_fast(float x) { return fmaxf(x, 0.0f) + __logf(1.0f + __expf(-fabsf(x))); }
+
+// Programmatic dependent launch.  A kernel launched by launch_pdl may start
+// while the kernel before it in the stream is finishing: pdl_wait() returns
+// once that grid has completed and its writes are visible (at once when the
+// kernel was launched normally, or the previous grid never released), and
+// must precede every read of what that grid wrote; pdl_release() lets the
+// next grid launch once every CTA of this grid has called it or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
