@@ -11,7 +11,8 @@ Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
 on the launch stream; between steps a 512 MiB buffer is written so that the
 L2 (129 MB on GB300) is flushed before every timed step.  Under torchrun each
 rank runs its own batch (weak scaling, no collective on the data path); the
-reported time is the max over ranks.
+reported time is the max over ranks.  The line also carries the same step
+with L2 left warm and the step captured once as a CUDA graph and replayed.
 
 --impl reference times the plain CPU oracle (the only other implementation
 of the method here) on the host cores, one full workload per step.
@@ -350,13 +351,30 @@ def time_steps(step, steps, warmup, flush, world, stream):
     barrier(world)
     torch.cuda.synchronize()
     for i in range(steps):
-        flush.zero_()
+        if flush is not None:
+            flush.zero_()
         evs[i][0].record(stream)
         step()
         evs[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     return sum(a.elapsed_time(b) for a, b in evs) / steps
+
+
+def graph_replay(step, stream):
+    """Captures one step in a CUDA graph (after two eager warm-up steps on a
+    side stream) and returns the callable that replays it on `stream`."""
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+        step()
+    stream.wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    torch.cuda.synchronize()
+    return g.replay
 
 
 def e2e_pipelined(host, outs_host, d, ws, steps, warmup, world):
@@ -464,6 +482,11 @@ def run_ours(args, rank, world, local):
     time_steps(step, args.steps, 0, flush, world, stream)
     prof = _lib.prof_stop()
     ms = max_over_ranks(ms, world, dev)
+    # secondary figures: the same step with L2 left warm, and replayed as one CUDA graph (flushed)
+    warm_ms = max_over_ranks(time_steps(step, args.steps, 0, None, world, stream), world, dev)
+    replay = graph_replay(step, stream)
+    graph_ms = max_over_ranks(time_steps(replay, args.steps, args.warmup, flush, world, stream), world, dev)
+    del replay
     value = world * w.tokens / (ms / 1e3)
     launches = int(sum(c for _, c in prof.values()))
     dom = max(prof, key=lambda k: prof[k][0])
@@ -515,6 +538,9 @@ def run_ours(args, rank, world, local):
             "step_roofline": {"bound": "hbm", "algorithmic_bytes": step_bytes(w),
                               "achieved": step_bytes(w) / (ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
                               "frac": step_bytes(w) / (ms / 1e3) / 1e9 / hbm},
+            "secondary": {"warm_l2_ms_per_step": warm_ms, "cuda_graph_ms_per_step": graph_ms,
+                          "note": "warm: no L2 flush between steps; cuda_graph: the step captured once and "
+                                  "replayed, L2 flushed"},
             "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items() if v[1]},
             "gpu_launches": launches,
             "clocks": clk,
