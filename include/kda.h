@@ -21,6 +21,12 @@
  *    workspace.  Host pointers are named *_host.
  *  - Calls are asynchronous on the given stream; nothing synchronises the
  *    device except kda_device_status() and kda_prof_stop().
+ *  - CUDA graphs: kda_fwd, kda_bwd, kda_decode and the norm and convolution
+ *    calls issue only kernel launches on the given stream, so they can be
+ *    captured (cudaStreamBeginCapture) and replayed; a replay reads the
+ *    captured pointers' current contents and gives the bits of an eager call.
+ *    kda_device_status() and kda_prof_stop() synchronise and cannot be
+ *    captured; the first kda_fwd_noalloc() on a device must precede capture.
  *  - Arguments are validated on the host before any launch; a failed check
  *    returns its status and launches nothing.  An invalid cu_seqlens array
  *    that only exists on the device is caught by the device (no work is done,

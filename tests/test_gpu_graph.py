@@ -56,3 +56,46 @@ def test_graph_replay_matches_eager(case):
         torch.cuda.synchronize()
         for k, v in eager.items():
             assert torch.equal(captured[k], v), k
+
+
+def test_graph_replay_of_decode_norm_and_conv():
+    """Two chained decode steps, the gated norm and the short convolution
+    (forward and backward each) captured together and replayed: the same bits
+    as the eager calls, the decode state included."""
+    from kimi_delta_attention_bwd_gb300 import (kda_decode_step, kda_norm_gate, kda_norm_gate_backward,
+                                                kda_short_conv, kda_short_conv_backward)
+    from kimi_delta_attention_bwd_gb300.inputs import norm_gate_inputs, short_conv_inputs
+
+    inp = to_dev(make_inputs(custom(6, 2, 4, 32, 64, dtype="bf16", h0=True), seed=33, with_grad_inputs=False))
+    ng = to_dev(norm_gate_inputs(300, 64))
+    sc = to_dev(short_conv_inputs(500, 192))
+    cu = torch.tensor([0, 7, 8, 300, 500], dtype=torch.int32, device="cuda")
+
+    def calls(state):
+        outs = {}
+        for t in range(2):
+            sl = lambda x: x[:, t].contiguous()  # noqa: E731
+            outs[f"o{t}"] = kda_decode_step(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["f"]), sl(inp["b"]),
+                                            inp["A_log"], inp["dt_bias"], state, scale=inp["scale"])
+        outs["state"] = state
+        outs["y"] = kda_norm_gate(ng["x"], ng["g"], ng["w"])
+        outs["dx"], outs["dg"], outs["dw"] = kda_norm_gate_backward(ng["x"], ng["g"], ng["w"], ng["dy"])
+        outs["cy"] = kda_short_conv(sc["x"], sc["w"], cu)
+        outs["cdx"], outs["cdw"] = kda_short_conv_backward(sc["x"], sc["w"], sc["dy"], cu)
+        return outs
+
+    state_g = inp["h0"].clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        calls(inp["h0"].clone())
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        captured = calls(state_g)
+    state_g.copy_(inp["h0"])  # capture launched nothing: start the replay from h0
+    graph.replay()
+    eager = calls(inp["h0"].clone())
+    torch.cuda.synchronize()
+    for k, v in eager.items():
+        assert torch.equal(captured[k], v), k
