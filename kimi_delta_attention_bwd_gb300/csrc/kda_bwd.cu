@@ -11,14 +11,16 @@
 // gradients (bwd_reduce).  Derivation: reverse-mode differentiation of the
 // recurrence of the "Pure KDA 300M" guide (Overview), chunked as in the
 // forward kernels.
-#include "kda_internal.cuh"
+#include "kda_simt.cuh"
 
 namespace kda {
 
-constexpr int NT = 16;  // dv columns per scan CTA
+constexpr int NT = 16;      // dv columns per scan CTA
+constexpr int GTH = 1024;   // threads of the per-chunk kernels
+constexpr int STH = 512;    // threads of the scan kernels
 
 template <typename TI, int DK, int DV>
-__global__ void __launch_bounds__(256) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
+__global__ void __launch_bounds__(STH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
   const int doc = blockIdx.x, h = blockIdx.y, c0col = blockIdx.z * NT, tid = threadIdx.x;
   if (!saved_ok(d, w.tag, w.err)) return;
   const int H = d.H;
@@ -67,10 +69,10 @@ __global__ void __launch_bounds__(256) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
       w.dE[(ch * C + s) * DV + c0col + jj] = acc;
     }
     __syncthreads();
-    float nv[(DK * NT + 255) / 256];
+    float nv[(DK * NT + STH - 1) / STH];
 #pragma unroll
-    for (int u = 0; u < (DK * NT + 255) / 256; u++) {
-      int idx = tid + u * 256;
+    for (int u = 0; u < (DK * NT + STH - 1) / STH; u++) {
+      int idx = tid + u * STH;
       if (idx < DK * NT) {
         int i = idx / NT, jj = idx % NT;
         float acc = gm[i] * dS[idx];
@@ -80,8 +82,8 @@ __global__ void __launch_bounds__(256) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
     }
     __syncthreads();
 #pragma unroll
-    for (int u = 0; u < (DK * NT + 255) / 256; u++) {
-      int idx = tid + u * 256;
+    for (int u = 0; u < (DK * NT + STH - 1) / STH; u++) {
+      int idx = tid + u * STH;
       if (idx < DK * NT) dS[idx] = nv[u];
     }
     __syncthreads();
@@ -110,7 +112,7 @@ __device__ __forceinline__ float block_sum(float x, float* red) {
 
 // One CTA per (chunk, head): all local gradients of the chunk.
 template <typename TI, int DK, int DV>
-__global__ void __launch_bounds__(256) bwd_intra_kernel(Dims d, BwdIO io, Ws w) {
+__global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) {
   const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   if (!saved_ok(d, w.tag, w.err)) return;
   if (j >= *w.n_chunks) return;
@@ -126,8 +128,7 @@ __global__ void __launch_bounds__(256) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   float* kh = qh + C * DK;      // [C][DK]
   float* G = kh + C * DK;       // [C][DK]
   float* Ap = G + C * DK;       // [C][C] unscaled strict-lower K^K^T with ratios
-  float* Pp = Ap + C * C;       // [C][C] unscaled inclusive-lower Q^K^T with ratios
-  float* Tm = Pp + C * C;       // [C][C]
+  float* Tm = Ap + C * C;       // [C][C]
   float* dAm = Tm + C * C;      // [C][C]
   float* dPm = dAm + C * C;     // [C][C]
   float* bet = dPm + C * C;     // [C]
@@ -137,6 +138,7 @@ __global__ void __launch_bounds__(256) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   float* omb = dbet + C;        // [C]  1 - beta, as sigmoid(-b) (exact near beta = 1)
   float* dgam = omb + C;        // [DK]
   float* red = dgam + DK;       // [32]
+  float* slab = red + 32;       // staged-product slabs
 
   float* scr = w.scr + ch * w.scr_per_ch;
   float* E = scr;               // [C][DV]
@@ -198,22 +200,20 @@ __global__ void __launch_bounds__(256) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   }
   __syncthreads();
 
-  // ---- intra-chunk factors (same arithmetic as the forward)
-  for (int idx = tid; idx < C * C; idx += blockDim.x) {
-    int r = idx / C, s = idx % C;
-    float accA = 0.f, accP = 0.f;
-    if (s <= r) {
-      for (int i = 0; i < DK; i++) {
-        float e = expf(G[r * DK + i] - G[s * DK + i]);
-        float ks = kh[s * DK + i] * e;
-        accP += qh[r * DK + i] * ks;
-        accA += kh[r * DK + i] * ks;
-      }
+  // ---- intra-chunk factors (same arithmetic as the forward): one warp per
+  //      (r, s), lanes over the key channels (A' only: dP comes from dO)
+  for (int idx = warp; idx < C * C; idx += nw) {
+    const int r = idx / C, s = idx % C;
+    float accA = 0.f;
+    if (s < r) {
+      for (int i = lane; i < DK; i += 32) accA += kh[r * DK + i] * kh[s * DK + i] * expf(G[r * DK + i] - G[s * DK + i]);
+      accA = warp_sum(accA);
     }
-    Ap[idx] = s < r ? accA : 0.f;
-    dAm[idx] = s < r ? bet[r] * accA : 0.f;   // A = diag(beta) Ap, used for the solve
-    Pp[idx] = accP;
-    Tm[idx] = (r == s) ? 1.f : 0.f;
+    if (lane == 0) {
+      Ap[idx] = accA;
+      dAm[idx] = bet[r] * accA;  // A = diag(beta) Ap, used for the solve
+      Tm[idx] = (r == s) ? 1.f : 0.f;
+    }
   }
   __syncthreads();
   for (int r = 1; r < C; r++) {
@@ -225,51 +225,59 @@ __global__ void __launch_bounds__(256) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
     __syncthreads();
   }
 
-  // ---- E = U - W S,  dQG = scale dO S^T,  dW = -dE S^T,  dgamma
-  for (int idx = tid; idx < C * DV; idx += blockDim.x) {
-    int r = idx / DV, jj = idx % DV;
-    float acc = Ug[idx];
-    for (int i = 0; i < DK; i++) acc -= Wg[r * DK + i] * Sg[i * DV + jj];
-    E[idx] = acc;
+  // ---- E = U - W S (scratch), dgamma; then with the value columns as k:
+  //      dQG = scale dO S^T, dW = -dE S^T, dKd = E dS'^T (products staged
+  //      through shared memory, every global read coalesced)
+  {
+    float acc[MmShape<DV, GTH>::RPT][4];
+    mm_zero<DV, GTH>(acc);
+    cta_mm<DV, DK, GTH, true, true>(acc, slab, [&](int m, int k) { return Wg[m * DK + k]; },
+                                    [&](int k, int n) { return Sg[k * DV + n]; });
+    mm_out<DV, GTH>(acc, [&](int m, int n, float v) { E[m * DV + n] = Ug[m * DV + n] - v; });
   }
-  for (int idx = tid; idx < C * DK; idx += blockDim.x) {
-    int r = idx / DK, i = idx % DK;
-    float a1 = 0.f, a2 = 0.f;
-    if (r < L)
-      for (int jj = 0; jj < DV; jj++) a1 += ldf(dO + ((int64_t)(t0 + r) * H + h) * DV + jj) * Sg[i * DV + jj];
-    for (int jj = 0; jj < DV; jj++) a2 += dEg[r * DV + jj] * Sg[i * DV + jj];
-    dQG[idx] = scale * a1;
-    dW[idx] = -a2;
-  }
-  for (int i = tid; i < DK; i += blockDim.x) {
+  for (int i = warp; i < DK; i += nw) {
     float acc = 0.f;
-    for (int jj = 0; jj < DV; jj++) acc += dSg[i * DV + jj] * Sg[i * DV + jj];
-    dgam[i] = acc;
+    for (int jj = lane; jj < DV; jj += 32) acc += dSg[i * DV + jj] * Sg[i * DV + jj];
+    acc = warp_sum(acc);
+    if (lane == 0) dgam[i] = acc;
   }
-  __syncthreads();
+  const TI* dOc = dO + ((int64_t)t0 * H + h) * DV;  // row r of the chunk at dOc + r H dv
+  auto fdO = [&](int m, int k) { return m < L ? ldf(dOc + (int64_t)m * H * DV + k) : 0.f; };
+  {
+    float acc[MmShape<DK, GTH>::RPT][4];
+    mm_zero<DK, GTH>(acc);
+    cta_mm<DK, DV, GTH, true, false>(acc, slab, fdO, [&](int k, int n) { return Sg[n * DV + k]; });
+    mm_out<DK, GTH>(acc, [&](int m, int n, float v) { dQG[m * DK + n] = scale * v; });
+    mm_zero<DK, GTH>(acc);
+    cta_mm<DK, DV, GTH, true, false>(acc, slab, [&](int m, int k) { return dEg[m * DV + k]; },
+                                     [&](int k, int n) { return Sg[n * DV + k]; });
+    mm_out<DK, GTH>(acc, [&](int m, int n, float v) { dW[m * DK + n] = -v; });
+    mm_zero<DK, GTH>(acc);
+    cta_mm<DK, DV, GTH, true, false>(acc, slab, [&](int m, int k) { return E[m * DV + k]; },
+                                     [&](int k, int n) { return dSg[n * DV + k]; });
+    mm_out<DK, GTH>(acc, [&](int m, int n, float v) { dKd[m * DK + n] = v; });
+  }
 
-  // ---- dP = scale dO E^T (inclusive lower), dKd = E dS'^T,  YU = T^T dE,  YW = T^T dW
-  for (int idx = tid; idx < C * C; idx += blockDim.x) {
-    int r = idx / C, s = idx % C;
-    float acc = 0.f;
-    if (s <= r && r < L)
-      for (int jj = 0; jj < DV; jj++) acc += ldf(dO + ((int64_t)(t0 + r) * H + h) * DV + jj) * E[s * DV + jj];
-    dPm[idx] = scale * acc;
+  // ---- dP = scale dO E^T (inclusive lower, rows < L), YW = T^T dW, YU = T^T dE
+  {
+    float acc[MmShape<C, GTH>::RPT][4];
+    mm_zero<C, GTH>(acc);
+    cta_mm<C, DV, GTH, true, false>(acc, slab, fdO, [&](int k, int n) { return E[n * DV + k]; });
+    mm_out<C, GTH>(acc, [&](int m, int n, float v) { dPm[m * C + n] = n <= m && m < L ? scale * v : 0.f; });
   }
-  for (int idx = tid; idx < C * DK; idx += blockDim.x) {
-    int r = idx / DK, i = idx % DK;
-    float acc = 0.f;
-    for (int jj = 0; jj < DV; jj++) acc += E[r * DV + jj] * dSg[i * DV + jj];
-    dKd[idx] = acc;
-    float acc2 = 0.f;
-    for (int rr = r; rr < C; rr++) acc2 += Tm[rr * C + r] * dW[rr * DK + i];
-    YW[idx] = acc2;
+  {
+    float acc[MmShape<DK, GTH>::RPT][4];
+    mm_zero<DK, GTH>(acc);
+    cta_mm<DK, C, GTH, false, true>(acc, slab, [&](int m, int k) { return Tm[k * C + m]; },
+                                    [&](int k, int n) { return dW[k * DK + n]; });
+    mm_out<DK, GTH>(acc, [&](int m, int n, float v) { YW[m * DK + n] = v; });
   }
-  for (int idx = tid; idx < C * DV; idx += blockDim.x) {
-    int s = idx / DV, jj = idx % DV;
-    float acc = 0.f;
-    for (int r = s; r < C; r++) acc += Tm[r * C + s] * dEg[r * DV + jj];
-    YU[idx] = acc;
+  {
+    float acc[MmShape<DV, GTH>::RPT][4];
+    mm_zero<DV, GTH>(acc);
+    cta_mm<DV, C, GTH, false, true>(acc, slab, [&](int m, int k) { return Tm[k * C + m]; },
+                                    [&](int k, int n) { return dEg[k * DV + n]; });
+    mm_out<DV, GTH>(acc, [&](int m, int n, float v) { YU[m * DV + n] = v; });
   }
   __syncthreads();
 
@@ -286,14 +294,14 @@ __global__ void __launch_bounds__(256) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
     acc = warp_sum(acc);
     if (lane == 0) dbet[r] += acc;
   }
-  for (int idx = tid; idx < C * C; idx += blockDim.x) {
-    int r = idx / C, s = idx % C;
-    float acc = 0.f;
-    if (s < r) {
-      for (int jj = 0; jj < DV; jj++) acc += YU[r * DV + jj] * Ug[s * DV + jj];
-      for (int i = 0; i < DK; i++) acc += YW[r * DK + i] * Wg[s * DK + i];
-    }
-    dAm[idx] = -acc;
+  {
+    float acc[MmShape<C, GTH>::RPT][4];
+    mm_zero<C, GTH>(acc);
+    cta_mm<C, DV, GTH, true, false>(acc, slab, [&](int m, int k) { return YU[m * DV + k]; },
+                                    [&](int k, int n) { return Ug[n * DV + k]; });
+    cta_mm<C, DK, GTH, true, false>(acc, slab, [&](int m, int k) { return YW[m * DK + k]; },
+                                    [&](int k, int n) { return Wg[n * DK + k]; });
+    mm_out<C, GTH>(acc, [&](int m, int n, float v) { dAm[m * C + n] = n < m ? -v : 0.f; });
   }
   __syncthreads();
   for (int r = warp; r < L; r += nw) {
@@ -441,19 +449,20 @@ static cudaError_t bwd_scan_launch(const Dims& d, const BwdIO& io, const Ws& w, 
   if (e != cudaSuccess) return e;
   dim3 grid(d.n_docs, d.H, DV / NT);
   prof_begin(K_BWD_SCAN, st);
-  bwd_scan_kernel<TI, DK, DV><<<grid, 256, smem, st>>>(d, io, w);
+  bwd_scan_kernel<TI, DK, DV><<<grid, STH, smem, st>>>(d, io, w);
   prof_end(K_BWD_SCAN, st);
   return cudaGetLastError();
 }
 
 template <typename TI, int DK, int DV>
 static cudaError_t bwd_intra_launch(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st) {
-  size_t smem = sizeof(float) * (3 * C * DK + 5 * C * C + 5 * C + DK + 32);
+  constexpr int NMAX = DK > DV ? DK : DV;
+  size_t smem = sizeof(float) * (3 * C * DK + 4 * C * C + 5 * C + DK + 32 + mm_slab_floats(NMAX > C ? NMAX : C));
   cudaError_t e = cudaFuncSetAttribute(bwd_intra_kernel<TI, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(d.nc_max, d.H);
   prof_begin(K_BWD_INTRA, st);
-  bwd_intra_kernel<TI, DK, DV><<<grid, 256, smem, st>>>(d, io, w);
+  bwd_intra_kernel<TI, DK, DV><<<grid, GTH, smem, st>>>(d, io, w);
   prof_end(K_BWD_INTRA, st);
   return cudaGetLastError();
 }

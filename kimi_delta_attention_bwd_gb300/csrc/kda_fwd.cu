@@ -10,14 +10,18 @@
 // This is the recurrence of the "Pure KDA 300M" guide (Overview) and of the
 // openkimi KDA oracle unrolled over one chunk; every decay ratio used is
 // exp of a non-positive number, so nothing can overflow.
-#include "kda_internal.cuh"
+#include "kda_simt.cuh"
 
 namespace kda {
+
+constexpr int NT = 16;      // dv columns per scan CTA
+constexpr int GTH = 1024;   // threads of the per-chunk kernels
+constexpr int STH = 512;    // threads of the scan kernels
 
 // One CTA per (chunk, head): the gate/norm prologue and the intra-chunk
 // factors W, U, P, QG, KD, gamma, written to the workspace.
 template <typename TI, int DK, int DV>
-__global__ void __launch_bounds__(256) fwd_intra_kernel(Dims d, FwdIO io, Ws w) {
+__global__ void __launch_bounds__(GTH) fwd_intra_kernel(Dims d, FwdIO io, Ws w) {
   const int j = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   if (j >= *w.n_chunks) return;
   const int L = w.chunk_len[j];
@@ -34,6 +38,7 @@ __global__ void __launch_bounds__(256) fwd_intra_kernel(Dims d, FwdIO io, Ws w) 
   float* Am = vv + C * DV;      // [C][C]
   float* Tm = Am + C * C;       // [C][C]
   float* bet = Tm + C * C;      // [C]
+  float* slab = bet + C;        // staged-product slabs
 
   const TI* q = (const TI*)io.q;
   const TI* k = (const TI*)io.k;
@@ -77,22 +82,27 @@ __global__ void __launch_bounds__(256) fwd_intra_kernel(Dims d, FwdIO io, Ws w) 
   }
   __syncthreads();
 
-  // A (strict lower, beta-scaled) and P (inclusive lower, scale-scaled).
+  // A (strict lower, beta-scaled) and P (inclusive lower, scale-scaled): one
+  // warp per (r, s), lanes over the key channels.
   float* Pg = w.P + ch * C * C;
-  for (int idx = tid; idx < C * C; idx += blockDim.x) {
-    int r = idx / C, s = idx % C;
+  for (int idx = warp; idx < C * C; idx += nw) {
+    const int r = idx / C, s = idx % C;
     float accA = 0.f, accP = 0.f;
     if (s <= r) {
-      for (int i = 0; i < DK; i++) {
-        float e = expf(G[r * DK + i] - G[s * DK + i]);
-        float ks = kh[s * DK + i] * e;
+      for (int i = lane; i < DK; i += 32) {
+        const float e = expf(G[r * DK + i] - G[s * DK + i]);
+        const float ks = kh[s * DK + i] * e;
         accP += qh[r * DK + i] * ks;
         accA += kh[r * DK + i] * ks;
       }
+      accP = warp_sum(accP);
+      accA = warp_sum(accA);
     }
-    Am[idx] = s < r ? bet[r] * accA : 0.f;
-    Pg[idx] = d.scale * accP;
-    Tm[idx] = (r == s) ? 1.f : 0.f;
+    if (lane == 0) {
+      Am[idx] = s < r ? bet[r] * accA : 0.f;
+      Pg[idx] = d.scale * accP;
+      Tm[idx] = (r == s) ? 1.f : 0.f;
+    }
   }
   __syncthreads();
 
@@ -110,31 +120,38 @@ __global__ void __launch_bounds__(256) fwd_intra_kernel(Dims d, FwdIO io, Ws w) 
   float* QGg = w.QG + ch * C * DK;
   float* KDg = w.KD + ch * C * DK;
   const float* Glast = G + (L - 1) * DK;
+  float* xk = qh;  // XK = diag(beta) (K^ * Gamma) over Q^ once QG is out
   for (int idx = tid; idx < C * DK; idx += blockDim.x) {
-    int r = idx / DK, i = idx % DK;
-    float acc = 0.f;
-    for (int s = 0; s <= r; s++) acc += Tm[r * C + s] * bet[s] * kh[s * DK + i] * expf(G[s * DK + i]);
-    Wg[idx] = acc;
-    float Gr = G[idx];
-    QGg[idx] = d.scale * qh[idx] * expf(Gr);
+    const int r = idx / DK, i = idx % DK;
+    const float Gr = G[idx], eG = expf(Gr);
+    QGg[idx] = d.scale * qh[idx] * eG;
     KDg[idx] = kh[idx] * expf(Glast[i] - Gr);
-  }
-  float* Ug = w.U + ch * C * DV;
-  for (int idx = tid; idx < C * DV; idx += blockDim.x) {
-    int r = idx / DV, jj = idx % DV;
-    float acc = 0.f;
-    for (int s = 0; s <= r; s++) acc += Tm[r * C + s] * bet[s] * vv[s * DV + jj];
-    Ug[idx] = acc;
+    xk[idx] = bet[r] * kh[idx] * eG;
   }
   for (int i = tid; i < DK; i += blockDim.x) w.gam[ch * DK + i] = expf(Glast[i]);
+  // W = T XK and U = T diag(beta) V (T unit lower, its upper part zero)
+  {
+    float acc[MmShape<DK, GTH>::RPT][4];
+    mm_zero<DK, GTH>(acc);
+    cta_mm<DK, C, GTH, true, true>(acc, slab, [&](int m, int k) { return Tm[m * C + k]; },
+                                   [&](int k, int n) { return xk[k * DK + n]; });
+    mm_out<DK, GTH>(acc, [&](int m, int n, float v) { Wg[m * DK + n] = v; });
+  }
+  float* Ug = w.U + ch * C * DV;
+  {
+    float acc[MmShape<DV, GTH>::RPT][4];
+    mm_zero<DV, GTH>(acc);
+    cta_mm<DV, C, GTH, true, true>(acc, slab, [&](int m, int k) { return Tm[m * C + k]; },
+                                   [&](int k, int n) { return bet[k] * vv[k * DV + n]; });
+    mm_out<DV, GTH>(acc, [&](int m, int n, float v) { Ug[m * DV + n] = v; });
+  }
 }
 
-constexpr int NT = 16;  // dv columns per scan CTA
 
 // One CTA per (document, head, 16 value columns): walks the document's
 // chunks in order carrying the fp32 state slice S[:, cols].
 template <typename TI, int DK, int DV>
-__global__ void __launch_bounds__(256) fwd_scan_kernel(Dims d, FwdIO io, Ws w) {
+__global__ void __launch_bounds__(STH) fwd_scan_kernel(Dims d, FwdIO io, Ws w) {
   const int doc = blockIdx.x, h = blockIdx.y, c0col = blockIdx.z * NT, tid = threadIdx.x;
   if (*w.err != 0) return;
   const int H = d.H;
@@ -186,10 +203,10 @@ __global__ void __launch_bounds__(256) fwd_scan_kernel(Dims d, FwdIO io, Ws w) {
         stf(o + ((int64_t)(t0 + r) * H + h) * DV + c0col + jj, acc);
       }
     }
-    float nv[(DK * NT + 255) / 256];
+    float nv[(DK * NT + STH - 1) / STH];
 #pragma unroll
-    for (int u = 0; u < (DK * NT + 255) / 256; u++) {
-      int idx = tid + u * 256;
+    for (int u = 0; u < (DK * NT + STH - 1) / STH; u++) {
+      int idx = tid + u * STH;
       if (idx < DK * NT) {
         int i = idx / NT, jj = idx % NT;
         float acc = gm[i] * S[idx];
@@ -199,8 +216,8 @@ __global__ void __launch_bounds__(256) fwd_scan_kernel(Dims d, FwdIO io, Ws w) {
     }
     __syncthreads();
 #pragma unroll
-    for (int u = 0; u < (DK * NT + 255) / 256; u++) {
-      int idx = tid + u * 256;
+    for (int u = 0; u < (DK * NT + STH - 1) / STH; u++) {
+      int idx = tid + u * STH;
       if (idx < DK * NT) S[idx] = nv[u];
     }
     __syncthreads();
@@ -214,12 +231,13 @@ __global__ void __launch_bounds__(256) fwd_scan_kernel(Dims d, FwdIO io, Ws w) {
 
 template <typename TI, int DK, int DV>
 static cudaError_t fwd_intra_launch(const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st) {
-  size_t smem = sizeof(float) * (3 * C * DK + C * DV + 2 * C * C + C);
+  constexpr int NMAX = DK > DV ? DK : DV;
+  size_t smem = sizeof(float) * (3 * C * DK + C * DV + 2 * C * C + C + mm_slab_floats(NMAX > C ? NMAX : C));
   cudaError_t e = cudaFuncSetAttribute(fwd_intra_kernel<TI, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(d.nc_max, d.H);
   prof_begin(K_FWD_INTRA, st);
-  fwd_intra_kernel<TI, DK, DV><<<grid, 256, smem, st>>>(d, io, w);
+  fwd_intra_kernel<TI, DK, DV><<<grid, GTH, smem, st>>>(d, io, w);
   prof_end(K_FWD_INTRA, st);
   return cudaGetLastError();
 }
@@ -231,7 +249,7 @@ static cudaError_t fwd_scan_launch(const Dims& d, const FwdIO& io, const Ws& w, 
   if (e != cudaSuccess) return e;
   dim3 grid(d.n_docs, d.H, DV / NT);
   prof_begin(K_FWD_SCAN, st);
-  fwd_scan_kernel<TI, DK, DV><<<grid, 256, smem, st>>>(d, io, w);
+  fwd_scan_kernel<TI, DK, DV><<<grid, STH, smem, st>>>(d, io, w);
   prof_end(K_FWD_SCAN, st);
   return cudaGetLastError();
 }
