@@ -15,83 +15,82 @@
 
 namespace kda {
 
-constexpr int NT = 16;      // dv columns per scan CTA
-constexpr int GTH = 1024;   // threads of the per-chunk kernels
-constexpr int STH = 512;    // threads of the scan kernels
+constexpr int NT = 32;        // dv columns per scan CTA
+constexpr int LDS = NT + 4;   // row stride of the scans' [rows][NT] tiles (16-byte rows)
+constexpr int GTH = 1024;     // threads of the per-chunk kernels
+constexpr int STH = 256;      // threads of the scan kernels
 
+// One CTA per (document, head, NT value columns): walks the document's
+// chunks backwards carrying the state-gradient slice dS[:, cols] in shared
+// memory; each step's products read the chunk's factors through the staged
+// slab.
 template <typename TI, int DK, int DV>
 __global__ void __launch_bounds__(STH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
   const int doc = blockIdx.x, h = blockIdx.y, c0col = blockIdx.z * NT, tid = threadIdx.x;
   if (!saved_ok(d, w.tag, w.err)) return;
   const int H = d.H;
-  extern __shared__ float sm[];
-  float* dS = sm;              // [DK][NT]
-  float* dEt = dS + DK * NT;   // [C][NT]
-  float* dOt = dEt + C * NT;   // [C][NT]
-  float* Wt = dOt + C * NT;    // [C][DK]
-  float* QGt = Wt + C * DK;    // [C][DK]
-  float* KDt = QGt + C * DK;   // [C][DK]
-  float* Pt = KDt + C * DK;    // [C][C]
-  float* gm = Pt + C * C;      // [DK]
+  extern __shared__ __align__(16) float sm[];
+  float* dS = sm;                // [DK][LDS] the carried state gradient
+  float* dOt = dS + DK * LDS;    // [C][LDS]  dO rows of the chunk (zero past L)
+  float* dEt = dOt + C * LDS;    // [C][LDS]
+  float* slab = dEt + C * LDS;   // A slab of the staged products
   const TI* dO = (const TI*)io.dO;
+  const int64_t dh = ((int64_t)doc * H + h) * DK * DV;
 
-  for (int idx = tid; idx < DK * NT; idx += blockDim.x) {
-    int i = idx / NT, jj = idx % NT;
-    dS[idx] = io.dh_final ? io.dh_final[(((int64_t)doc * H + h) * DK + i) * DV + c0col + jj] : 0.f;
+  for (int idx = tid; idx < DK * NT; idx += STH) {
+    const int i = idx / NT, jj = idx % NT;
+    dS[i * LDS + jj] = io.dh_final ? io.dh_final[dh + i * DV + c0col + jj] : 0.f;
   }
   const int cb = w.doc_chunk0[doc], ce = w.doc_chunk0[doc + 1];
-  __syncthreads();
   for (int c = ce - 1; c >= cb; c--) {
     const int64_t ch = (int64_t)c * H + h;
     const int L = w.chunk_len[c], t0 = w.chunk_tok0[c];
-    for (int idx = tid; idx < DK * NT; idx += blockDim.x) {
-      int i = idx / NT, jj = idx % NT;
-      w.dSn[(ch * DK + i) * DV + c0col + jj] = dS[idx];
+    __syncthreads();  // the previous step's dS and its readers are done
+    if (c > cb) {  // the previous chunk's factors and dO rows into L2 while this one runs
+      const int64_t nx = ch - H;
+      prefetch_span<STH>(w.P + nx * C * C, C * C);
+      prefetch_span<STH>(w.KD + nx * C * DK, C * DK);
+      prefetch_span<STH>(w.QG + nx * C * DK, C * DK);
+      prefetch_span<STH>(w.W + nx * C * DK, C * DK);
+      const int Ln = w.chunk_len[c - 1], tn = w.chunk_tok0[c - 1];
+      if (tid < Ln) asm volatile("prefetch.global.L2 [%0];" ::"l"(dO + ((int64_t)(tn + tid) * H + h) * DV + c0col));
     }
-    for (int idx = tid; idx < C * DK; idx += blockDim.x) {
-      Wt[idx] = w.W[ch * C * DK + idx];
-      QGt[idx] = w.QG[ch * C * DK + idx];
-      KDt[idx] = w.KD[ch * C * DK + idx];
+    for (int idx = tid; idx < DK * NT; idx += STH) {
+      const int i = idx / NT, jj = idx % NT;
+      w.dSn[(ch * DK + i) * DV + c0col + jj] = dS[i * LDS + jj];
     }
-    for (int idx = tid; idx < C * C; idx += blockDim.x) Pt[idx] = w.P[ch * C * C + idx];
-    for (int i = tid; i < DK; i += blockDim.x) gm[i] = w.gam[ch * DK + i];
-    for (int idx = tid; idx < C * NT; idx += blockDim.x) {
-      int r = idx / NT, jj = idx % NT;
-      dOt[idx] = r < L ? ldf(dO + ((int64_t)(t0 + r) * H + h) * DV + c0col + jj) : 0.f;
+    for (int idx = tid; idx < C * NT; idx += STH) {
+      const int r = idx / NT, jj = idx % NT;
+      dOt[r * LDS + jj] = r < L ? ldf(dO + ((int64_t)(t0 + r) * H + h) * DV + c0col + jj) : 0.f;
     }
-    __syncthreads();
-    for (int idx = tid; idx < C * NT; idx += blockDim.x) {
-      int s = idx / NT, jj = idx % NT;
-      float acc = 0.f;
-      for (int r = s; r < C; r++) acc += Pt[r * C + s] * dOt[r * NT + jj];
-      for (int i = 0; i < DK; i++) acc += KDt[s * DK + i] * dS[i * NT + jj];
-      dEt[idx] = acc;
-      w.dE[(ch * C + s) * DV + c0col + jj] = acc;
+    {  // dE = P^T dO + KD dS' (to the workspace for the per-chunk kernel, and to dEt)
+      const float* P = w.P + ch * C * C;
+      const float* KD = w.KD + ch * C * DK;
+      MmAcc<C, NT, STH> acc;
+      mm_zero<C, NT, STH>(acc);
+      cta_mm_sb<C, NT, C, STH, false>(acc, slab, [&](int m, int k) { return P[k * C + m]; }, dOt, LDS);
+      cta_mm_sb<C, NT, DK, STH, true>(acc, slab, [&](int m, int k) { return KD[m * DK + k]; }, dS, LDS);
+      mm_out<C, NT, STH>(acc, [&](int m, int n, float v) {
+        dEt[m * LDS + n] = v;
+        w.dE[(ch * C + m) * DV + c0col + n] = v;
+      });
     }
-    __syncthreads();
-    float nv[(DK * NT + STH - 1) / STH];
-#pragma unroll
-    for (int u = 0; u < (DK * NT + STH - 1) / STH; u++) {
-      int idx = tid + u * STH;
-      if (idx < DK * NT) {
-        int i = idx / NT, jj = idx % NT;
-        float acc = gm[i] * dS[idx];
-        for (int r = 0; r < C; r++) acc += QGt[r * DK + i] * dOt[r * NT + jj] - Wt[r * DK + i] * dEt[r * NT + jj];
-        nv[u] = acc;
-      }
+    {  // dS = Diag(gamma) dS' + QG^T dO - W^T dE (each thread rewrites only the entries it owns)
+      const float* QG = w.QG + ch * C * DK;
+      const float* W = w.W + ch * C * DK;
+      const float* gm = w.gam + ch * DK;
+      MmAcc<DK, NT, STH> acc;
+      mm_zero<DK, NT, STH>(acc);
+      cta_mm_sb<DK, NT, C, STH, false>(acc, slab, [&](int m, int k) { return QG[k * DK + m]; }, dOt, LDS);
+      cta_mm_sb<DK, NT, C, STH, false>(acc, slab, [&](int m, int k) { return -W[k * DK + m]; }, dEt, LDS);
+      mm_out<DK, NT, STH>(acc, [&](int m, int n, float v) { dS[m * LDS + n] = gm[m] * dS[m * LDS + n] + v; });
     }
-    __syncthreads();
-#pragma unroll
-    for (int u = 0; u < (DK * NT + STH - 1) / STH; u++) {
-      int idx = tid + u * STH;
-      if (idx < DK * NT) dS[idx] = nv[u];
-    }
-    __syncthreads();
   }
+  __syncthreads();
   if (io.dh0)
-    for (int idx = tid; idx < DK * NT; idx += blockDim.x) {
-      int i = idx / NT, jj = idx % NT;
-      io.dh0[(((int64_t)doc * H + h) * DK + i) * DV + c0col + jj] = dS[idx];
+    for (int idx = tid; idx < DK * NT; idx += STH) {
+      const int i = idx / NT, jj = idx % NT;
+      io.dh0[dh + i * DV + c0col + jj] = dS[i * LDS + jj];
     }
 }
 
@@ -126,10 +125,10 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   extern __shared__ float sm[];
   float* qh = sm;               // [C][DK]
   float* kh = qh + C * DK;      // [C][DK]
-  float* G = kh + C * DK;       // [C][DK]
+  float* G = kh + C * DK;       // [C][DK] in-chunk cumulative log-decay, log2 units
   float* Ap = G + C * DK;       // [C][C] unscaled strict-lower K^K^T with ratios
-  float* Tm = Ap + C * C;       // [C][C]
-  float* dAm = Tm + C * C;      // [C][C]
+  float* Tt = Ap + C * C;       // [C][C] T transposed
+  float* dAm = Tt + C * C;      // [C][C]
   float* dPm = dAm + C * C;     // [C][C]
   float* bet = dPm + C * C;     // [C]
   float* nq = bet + C;          // [C]
@@ -196,7 +195,7 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   }
   for (int i = tid; i < DK; i += blockDim.x) {
     float acc = 0.f;
-    for (int r = 0; r < C; r++) { acc += G[r * DK + i]; G[r * DK + i] = acc; }
+    for (int r = 0; r < C; r++) { acc += G[r * DK + i]; G[r * DK + i] = acc * LOG2E_S; }  // G log2(e)
   }
   __syncthreads();
 
@@ -206,34 +205,40 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
     const int r = idx / C, s = idx % C;
     float accA = 0.f;
     if (s < r) {
-      for (int i = lane; i < DK; i += 32) accA += kh[r * DK + i] * kh[s * DK + i] * expf(G[r * DK + i] - G[s * DK + i]);
+      for (int i = lane; i < DK; i += 32) accA += kh[r * DK + i] * kh[s * DK + i] * exp2f(G[r * DK + i] - G[s * DK + i]);
       accA = warp_sum(accA);
     }
     if (lane == 0) {
       Ap[idx] = accA;
       dAm[idx] = bet[r] * accA;  // A = diag(beta) Ap, used for the solve
-      Tm[idx] = (r == s) ? 1.f : 0.f;
+      Tt[idx] = (r == s) ? 1.f : 0.f;
     }
   }
   __syncthreads();
-  for (int r = 1; r < C; r++) {
-    for (int c = tid; c < r; c += blockDim.x) {
+  // T = (I + A)^-1 by forward substitution
+  // (held transposed, Tt[c][r] = T[r][c]): each column is its own forward
+  // substitution down the rows; one warp per column, lanes over the sum
+  for (int c = warp; c < C; c += nw) {
+    float* tc = Tt + c * C;
+    for (int r = c + 1; r < C; r++) {
       float acc = 0.f;
-      for (int s = c; s < r; s++) acc += dAm[r * C + s] * Tm[s * C + c];
-      Tm[r * C + c] = -acc;
+      for (int s = c + lane; s < r; s += 32) acc += dAm[r * C + s] * tc[s];
+      acc = warp_sum(acc);
+      if (lane == 0) tc[r] = -acc;
+      __syncwarp();
     }
-    __syncthreads();
   }
+  __syncthreads();
 
   // ---- E = U - W S (scratch), dgamma; then with the value columns as k:
   //      dQG = scale dO S^T, dW = -dE S^T, dKd = E dS'^T (products staged
   //      through shared memory, every global read coalesced)
   {
-    float acc[MmShape<DV, GTH>::RPT][4];
-    mm_zero<DV, GTH>(acc);
-    cta_mm<DV, DK, GTH, true, true>(acc, slab, [&](int m, int k) { return Wg[m * DK + k]; },
+    MmAcc<C, DV, GTH> acc;
+    mm_zero<C, DV, GTH>(acc);
+    cta_mm<C, DV, DK, GTH, true, true>(acc, slab, [&](int m, int k) { return Wg[m * DK + k]; },
                                     [&](int k, int n) { return Sg[k * DV + n]; });
-    mm_out<DV, GTH>(acc, [&](int m, int n, float v) { E[m * DV + n] = Ug[m * DV + n] - v; });
+    mm_out<C, DV, GTH>(acc, [&](int m, int n, float v) { E[m * DV + n] = Ug[m * DV + n] - v; });
   }
   for (int i = warp; i < DK; i += nw) {
     float acc = 0.f;
@@ -244,40 +249,40 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   const TI* dOc = dO + ((int64_t)t0 * H + h) * DV;  // row r of the chunk at dOc + r H dv
   auto fdO = [&](int m, int k) { return m < L ? ldf(dOc + (int64_t)m * H * DV + k) : 0.f; };
   {
-    float acc[MmShape<DK, GTH>::RPT][4];
-    mm_zero<DK, GTH>(acc);
-    cta_mm<DK, DV, GTH, true, false>(acc, slab, fdO, [&](int k, int n) { return Sg[n * DV + k]; });
-    mm_out<DK, GTH>(acc, [&](int m, int n, float v) { dQG[m * DK + n] = scale * v; });
-    mm_zero<DK, GTH>(acc);
-    cta_mm<DK, DV, GTH, true, false>(acc, slab, [&](int m, int k) { return dEg[m * DV + k]; },
+    MmAcc<C, DK, GTH> acc;
+    mm_zero<C, DK, GTH>(acc);
+    cta_mm<C, DK, DV, GTH, true, false>(acc, slab, fdO, [&](int k, int n) { return Sg[n * DV + k]; });
+    mm_out<C, DK, GTH>(acc, [&](int m, int n, float v) { dQG[m * DK + n] = scale * v; });
+    mm_zero<C, DK, GTH>(acc);
+    cta_mm<C, DK, DV, GTH, true, false>(acc, slab, [&](int m, int k) { return dEg[m * DV + k]; },
                                      [&](int k, int n) { return Sg[n * DV + k]; });
-    mm_out<DK, GTH>(acc, [&](int m, int n, float v) { dW[m * DK + n] = -v; });
-    mm_zero<DK, GTH>(acc);
-    cta_mm<DK, DV, GTH, true, false>(acc, slab, [&](int m, int k) { return E[m * DV + k]; },
+    mm_out<C, DK, GTH>(acc, [&](int m, int n, float v) { dW[m * DK + n] = -v; });
+    mm_zero<C, DK, GTH>(acc);
+    cta_mm<C, DK, DV, GTH, true, false>(acc, slab, [&](int m, int k) { return E[m * DV + k]; },
                                      [&](int k, int n) { return dSg[n * DV + k]; });
-    mm_out<DK, GTH>(acc, [&](int m, int n, float v) { dKd[m * DK + n] = v; });
+    mm_out<C, DK, GTH>(acc, [&](int m, int n, float v) { dKd[m * DK + n] = v; });
   }
 
   // ---- dP = scale dO E^T (inclusive lower, rows < L), YW = T^T dW, YU = T^T dE
   {
-    float acc[MmShape<C, GTH>::RPT][4];
-    mm_zero<C, GTH>(acc);
-    cta_mm<C, DV, GTH, true, false>(acc, slab, fdO, [&](int k, int n) { return E[n * DV + k]; });
-    mm_out<C, GTH>(acc, [&](int m, int n, float v) { dPm[m * C + n] = n <= m && m < L ? scale * v : 0.f; });
+    MmAcc<C, C, GTH> acc;
+    mm_zero<C, C, GTH>(acc);
+    cta_mm<C, C, DV, GTH, true, false>(acc, slab, fdO, [&](int k, int n) { return E[n * DV + k]; });
+    mm_out<C, C, GTH>(acc, [&](int m, int n, float v) { dPm[m * C + n] = n <= m && m < L ? scale * v : 0.f; });
   }
   {
-    float acc[MmShape<DK, GTH>::RPT][4];
-    mm_zero<DK, GTH>(acc);
-    cta_mm<DK, C, GTH, false, true>(acc, slab, [&](int m, int k) { return Tm[k * C + m]; },
+    MmAcc<C, DK, GTH> acc;
+    mm_zero<C, DK, GTH>(acc);
+    cta_mm<C, DK, C, GTH, true, true>(acc, slab, [&](int m, int k) { return Tt[m * C + k]; },
                                     [&](int k, int n) { return dW[k * DK + n]; });
-    mm_out<DK, GTH>(acc, [&](int m, int n, float v) { YW[m * DK + n] = v; });
+    mm_out<C, DK, GTH>(acc, [&](int m, int n, float v) { YW[m * DK + n] = v; });
   }
   {
-    float acc[MmShape<DV, GTH>::RPT][4];
-    mm_zero<DV, GTH>(acc);
-    cta_mm<DV, C, GTH, false, true>(acc, slab, [&](int m, int k) { return Tm[k * C + m]; },
+    MmAcc<C, DV, GTH> acc;
+    mm_zero<C, DV, GTH>(acc);
+    cta_mm<C, DV, C, GTH, true, true>(acc, slab, [&](int m, int k) { return Tt[m * C + k]; },
                                     [&](int k, int n) { return dEg[k * DV + n]; });
-    mm_out<DV, GTH>(acc, [&](int m, int n, float v) { YU[m * DV + n] = v; });
+    mm_out<C, DV, GTH>(acc, [&](int m, int n, float v) { YU[m * DV + n] = v; });
   }
   __syncthreads();
 
@@ -290,18 +295,18 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   for (int r = warp; r < L; r += nw) {
     float acc = 0.f;
     for (int jj = lane; jj < DV; jj += 32) acc += YU[r * DV + jj] * ldf(v + ((int64_t)(t0 + r) * H + h) * DV + jj);
-    for (int i = lane; i < DK; i += 32) acc += YW[r * DK + i] * kh[r * DK + i] * expf(G[r * DK + i]);
+    for (int i = lane; i < DK; i += 32) acc += YW[r * DK + i] * kh[r * DK + i] * exp2f(G[r * DK + i]);
     acc = warp_sum(acc);
     if (lane == 0) dbet[r] += acc;
   }
   {
-    float acc[MmShape<C, GTH>::RPT][4];
-    mm_zero<C, GTH>(acc);
-    cta_mm<C, DV, GTH, true, false>(acc, slab, [&](int m, int k) { return YU[m * DV + k]; },
+    MmAcc<C, C, GTH> acc;
+    mm_zero<C, C, GTH>(acc);
+    cta_mm<C, C, DV, GTH, true, false>(acc, slab, [&](int m, int k) { return YU[m * DV + k]; },
                                     [&](int k, int n) { return Ug[n * DV + k]; });
-    cta_mm<C, DK, GTH, true, false>(acc, slab, [&](int m, int k) { return YW[m * DK + k]; },
+    cta_mm<C, C, DK, GTH, true, false>(acc, slab, [&](int m, int k) { return YW[m * DK + k]; },
                                     [&](int k, int n) { return Wg[n * DK + k]; });
-    mm_out<C, GTH>(acc, [&](int m, int n, float v) { dAm[m * C + n] = n < m ? -v : 0.f; });
+    mm_out<C, C, GTH>(acc, [&](int m, int n, float v) { dAm[m * C + n] = n < m ? -v : 0.f; });
   }
   __syncthreads();
   for (int r = warp; r < L; r += nw) {
@@ -320,19 +325,19 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
     float Gr = G[idx];
     float prow = 0.f, arow = 0.f, col = 0.f;
     for (int s = 0; s <= r; s++) {
-      float e = expf(Gr - G[s * DK + i]);
+      float e = exp2f(Gr - G[s * DK + i]);
       prow += dPm[r * C + s] * kh[s * DK + i] * e;
       arow += dAm[r * C + s] * kh[s * DK + i] * e;   // dAm is 0 on the diagonal
     }
     for (int rr = r; rr < C; rr++) {
-      float e = expf(G[rr * DK + i] - Gr);
+      float e = exp2f(G[rr * DK + i] - Gr);
       col += dPm[rr * C + r] * qh[rr * DK + i] * e + dAm[rr * C + r] * kh[rr * DK + i] * e;
     }
-    float Gam = expf(Gr);
-    float KDr = kh[idx] * expf(G[(L - 1) * DK + i] - Gr);
+    float Gam = exp2f(Gr);
+    float KDr = kh[idx] * exp2f(G[(L - 1) * DK + i] - Gr);
     float dkg = bet[r] * YW[idx];  // gradient of K^ * Gamma
     dqh[idx] = prow + dQG[idx] * Gam;
-    dkh[idx] = arow + col + dkg * Gam + dKd[idx] * expf(G[(L - 1) * DK + i] - Gr);
+    dkh[idx] = arow + col + dkg * Gam + dKd[idx] * exp2f(G[(L - 1) * DK + i] - Gr);
     dG[idx] = qh[idx] * prow + kh[idx] * arow - kh[idx] * col + dQG[idx] * qh[idx] * Gam
               + dkg * kh[idx] * Gam - dKd[idx] * KDr;
   }
@@ -343,8 +348,8 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   float pA_local = 0.f;
   for (int i = tid; i < DK; i += blockDim.x) {
     float Glast = G[(L - 1) * DK + i];
-    float extra = dgam[i] * expf(Glast);
-    for (int r = 0; r < L; r++) extra += dKd[r * DK + i] * kh[r * DK + i] * expf(Glast - G[r * DK + i]);
+    float extra = dgam[i] * exp2f(Glast);
+    for (int r = 0; r < L; r++) extra += dKd[r * DK + i] * kh[r * DK + i] * exp2f(Glast - G[r * DK + i]);
     float acc = extra;  // dG at row L-1 gets the G_last terms
     float pdt = 0.f;
     for (int r = L - 1; r >= 0; r--) {
@@ -444,7 +449,7 @@ __global__ void __launch_bounds__(RTH) bwd_reduce_kernel(Dims d, BwdIO io, Ws w)
 
 template <typename TI, int DK, int DV>
 static cudaError_t bwd_scan_launch(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st) {
-  size_t smem = sizeof(float) * (DK * NT + 2 * C * NT + 3 * C * DK + C * C + DK);
+  size_t smem = sizeof(float) * ((DK + 2 * C) * LDS + KS * ((DK > C ? DK : C) + 1));
   cudaError_t e = cudaFuncSetAttribute(bwd_scan_kernel<TI, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(d.n_docs, d.H, DV / NT);
@@ -457,7 +462,7 @@ static cudaError_t bwd_scan_launch(const Dims& d, const BwdIO& io, const Ws& w, 
 template <typename TI, int DK, int DV>
 static cudaError_t bwd_intra_launch(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st) {
   constexpr int NMAX = DK > DV ? DK : DV;
-  size_t smem = sizeof(float) * (3 * C * DK + 4 * C * C + 5 * C + DK + 32 + mm_slab_floats(NMAX > C ? NMAX : C));
+  size_t smem = sizeof(float) * (3 * C * DK + 4 * C * C + 5 * C + DK + 32 + mm_slab_floats(C, NMAX > C ? NMAX : C));
   cudaError_t e = cudaFuncSetAttribute(bwd_intra_kernel<TI, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(d.nc_max, d.H);

@@ -14,9 +14,10 @@
 
 namespace kda {
 
-constexpr int NT = 16;      // dv columns per scan CTA
-constexpr int GTH = 1024;   // threads of the per-chunk kernels
-constexpr int STH = 512;    // threads of the scan kernels
+constexpr int NT = 32;        // dv columns per scan CTA
+constexpr int LDS = NT + 4;   // row stride of the scans' [rows][NT] tiles (16-byte rows)
+constexpr int GTH = 1024;     // threads of the per-chunk kernels
+constexpr int STH = 256;      // threads of the scan kernels
 
 // One CTA per (chunk, head): the gate/norm prologue and the intra-chunk
 // factors W, U, P, QG, KD, gamma, written to the workspace.
@@ -33,11 +34,11 @@ __global__ void __launch_bounds__(GTH) fwd_intra_kernel(Dims d, FwdIO io, Ws w) 
   extern __shared__ float sm[];
   float* qh = sm;               // [C][DK]
   float* kh = qh + C * DK;      // [C][DK]
-  float* G = kh + C * DK;       // [C][DK]
+  float* G = kh + C * DK;       // [C][DK] in-chunk cumulative log-decay, log2 units
   float* vv = G + C * DK;       // [C][DV]
   float* Am = vv + C * DV;      // [C][C]
-  float* Tm = Am + C * C;       // [C][C]
-  float* bet = Tm + C * C;      // [C]
+  float* Tt = Am + C * C;       // [C][C] T transposed
+  float* bet = Tt + C * C;      // [C]
   float* slab = bet + C;        // staged-product slabs
 
   const TI* q = (const TI*)io.q;
@@ -78,7 +79,7 @@ __global__ void __launch_bounds__(GTH) fwd_intra_kernel(Dims d, FwdIO io, Ws w) 
   }
   for (int i = tid; i < DK; i += blockDim.x) {
     float acc = 0.f;
-    for (int r = 0; r < C; r++) { acc += G[r * DK + i]; G[r * DK + i] = acc; }
+    for (int r = 0; r < C; r++) { acc += G[r * DK + i]; G[r * DK + i] = acc * LOG2E_S; }  // G log2(e)
   }
   __syncthreads();
 
@@ -90,7 +91,7 @@ __global__ void __launch_bounds__(GTH) fwd_intra_kernel(Dims d, FwdIO io, Ws w) 
     float accA = 0.f, accP = 0.f;
     if (s <= r) {
       for (int i = lane; i < DK; i += 32) {
-        const float e = expf(G[r * DK + i] - G[s * DK + i]);
+        const float e = exp2f(G[r * DK + i] - G[s * DK + i]);
         const float ks = kh[s * DK + i] * e;
         accP += qh[r * DK + i] * ks;
         accA += kh[r * DK + i] * ks;
@@ -101,20 +102,25 @@ __global__ void __launch_bounds__(GTH) fwd_intra_kernel(Dims d, FwdIO io, Ws w) 
     if (lane == 0) {
       Am[idx] = s < r ? bet[r] * accA : 0.f;
       Pg[idx] = d.scale * accP;
-      Tm[idx] = (r == s) ? 1.f : 0.f;
+      Tt[idx] = (r == s) ? 1.f : 0.f;
     }
   }
   __syncthreads();
 
-  // T = (I + A)^-1 by forward substitution, one row per step.
-  for (int r = 1; r < C; r++) {
-    for (int c = tid; c < r; c += blockDim.x) {
+  // T = (I + A)^-1 by forward substitution
+  // (held transposed, Tt[c][r] = T[r][c]): each column is its own forward
+  // substitution down the rows; one warp per column, lanes over the sum
+  for (int c = warp; c < C; c += nw) {
+    float* tc = Tt + c * C;
+    for (int r = c + 1; r < C; r++) {
       float acc = 0.f;
-      for (int s = c; s < r; s++) acc += Am[r * C + s] * Tm[s * C + c];
-      Tm[r * C + c] = -acc;
+      for (int s = c + lane; s < r; s += 32) acc += Am[r * C + s] * tc[s];
+      acc = warp_sum(acc);
+      if (lane == 0) tc[r] = -acc;
+      __syncwarp();
     }
-    __syncthreads();
   }
+  __syncthreads();
 
   float* Wg = w.W + ch * C * DK;
   float* QGg = w.QG + ch * C * DK;
@@ -123,116 +129,107 @@ __global__ void __launch_bounds__(GTH) fwd_intra_kernel(Dims d, FwdIO io, Ws w) 
   float* xk = qh;  // XK = diag(beta) (K^ * Gamma) over Q^ once QG is out
   for (int idx = tid; idx < C * DK; idx += blockDim.x) {
     const int r = idx / DK, i = idx % DK;
-    const float Gr = G[idx], eG = expf(Gr);
+    const float Gr = G[idx], eG = exp2f(Gr);
     QGg[idx] = d.scale * qh[idx] * eG;
-    KDg[idx] = kh[idx] * expf(Glast[i] - Gr);
+    KDg[idx] = kh[idx] * exp2f(Glast[i] - Gr);
     xk[idx] = bet[r] * kh[idx] * eG;
   }
-  for (int i = tid; i < DK; i += blockDim.x) w.gam[ch * DK + i] = expf(Glast[i]);
+  for (int i = tid; i < DK; i += blockDim.x) w.gam[ch * DK + i] = exp2f(Glast[i]);
   // W = T XK and U = T diag(beta) V (T unit lower, its upper part zero)
   {
-    float acc[MmShape<DK, GTH>::RPT][4];
-    mm_zero<DK, GTH>(acc);
-    cta_mm<DK, C, GTH, true, true>(acc, slab, [&](int m, int k) { return Tm[m * C + k]; },
+    MmAcc<C, DK, GTH> acc;
+    mm_zero<C, DK, GTH>(acc);
+    cta_mm<C, DK, C, GTH, false, true>(acc, slab, [&](int m, int k) { return Tt[k * C + m]; },
                                    [&](int k, int n) { return xk[k * DK + n]; });
-    mm_out<DK, GTH>(acc, [&](int m, int n, float v) { Wg[m * DK + n] = v; });
+    mm_out<C, DK, GTH>(acc, [&](int m, int n, float v) { Wg[m * DK + n] = v; });
   }
   float* Ug = w.U + ch * C * DV;
   {
-    float acc[MmShape<DV, GTH>::RPT][4];
-    mm_zero<DV, GTH>(acc);
-    cta_mm<DV, C, GTH, true, true>(acc, slab, [&](int m, int k) { return Tm[m * C + k]; },
+    MmAcc<C, DV, GTH> acc;
+    mm_zero<C, DV, GTH>(acc);
+    cta_mm<C, DV, C, GTH, false, true>(acc, slab, [&](int m, int k) { return Tt[k * C + m]; },
                                    [&](int k, int n) { return bet[k] * vv[k * DV + n]; });
-    mm_out<DV, GTH>(acc, [&](int m, int n, float v) { Ug[m * DV + n] = v; });
+    mm_out<C, DV, GTH>(acc, [&](int m, int n, float v) { Ug[m * DV + n] = v; });
   }
 }
 
 
-// One CTA per (document, head, 16 value columns): walks the document's
-// chunks in order carrying the fp32 state slice S[:, cols].
+// One CTA per (document, head, NT value columns): walks the document's
+// chunks in order carrying the fp32 state slice S[:, cols] in shared memory;
+// each step's products read the chunk's factors through the staged slab.
 template <typename TI, int DK, int DV>
 __global__ void __launch_bounds__(STH) fwd_scan_kernel(Dims d, FwdIO io, Ws w) {
   const int doc = blockIdx.x, h = blockIdx.y, c0col = blockIdx.z * NT, tid = threadIdx.x;
   if (*w.err != 0) return;
   const int H = d.H;
-  extern __shared__ float sm[];
-  float* S = sm;               // [DK][NT]
-  float* E = S + DK * NT;      // [C][NT]
-  float* Wt = E + C * NT;      // [C][DK]
-  float* QGt = Wt + C * DK;    // [C][DK]
-  float* KDt = QGt + C * DK;   // [C][DK]
-  float* Pt = KDt + C * DK;    // [C][C]
-  float* gm = Pt + C * C;      // [DK]
+  extern __shared__ __align__(16) float sm[];
+  float* S = sm;               // [DK][LDS] the carried state slice
+  float* E = S + DK * LDS;     // [C][LDS]
+  float* slab = E + C * LDS;   // A slab of the staged products
   TI* o = (TI*)io.o;
+  const int64_t dh = ((int64_t)doc * H + h) * DK * DV;
 
-  for (int idx = tid; idx < DK * NT; idx += blockDim.x) {
-    int i = idx / NT, jj = idx % NT;
-    S[idx] = io.h0 ? io.h0[(((int64_t)doc * H + h) * DK + i) * DV + c0col + jj] : 0.f;
+  for (int idx = tid; idx < DK * NT; idx += STH) {
+    const int i = idx / NT, jj = idx % NT;
+    S[i * LDS + jj] = io.h0 ? io.h0[dh + i * DV + c0col + jj] : 0.f;
   }
   const int cb = w.doc_chunk0[doc], ce = w.doc_chunk0[doc + 1];
-  __syncthreads();
   for (int c = cb; c < ce; c++) {
     const int64_t ch = (int64_t)c * H + h;
     const int L = w.chunk_len[c], t0 = w.chunk_tok0[c];
+    const float* W = w.W + ch * C * DK;
+    __syncthreads();  // the previous step's state is complete
+    if (c + 1 < ce) {  // the next chunk's factors into L2 while this one runs
+      const int64_t nx = ch + H;
+      prefetch_span<STH>(w.W + nx * C * DK, C * DK);
+      prefetch_span<STH>(w.QG + nx * C * DK, C * DK);
+      prefetch_span<STH>(w.KD + nx * C * DK, C * DK);
+      prefetch_span<STH>(w.P + nx * C * C, C * C);
+      if (tid < C) asm volatile("prefetch.global.L2 [%0];" ::"l"(w.U + (nx * C + tid) * DV + c0col));
+    }
     if (io.save)
-      for (int idx = tid; idx < DK * NT; idx += blockDim.x) {
-        int i = idx / NT, jj = idx % NT;
-        w.Sent[(ch * DK + i) * DV + c0col + jj] = S[idx];
+      for (int idx = tid; idx < DK * NT; idx += STH) {
+        const int i = idx / NT, jj = idx % NT;
+        w.Sent[(ch * DK + i) * DV + c0col + jj] = S[i * LDS + jj];
       }
-    for (int idx = tid; idx < C * DK; idx += blockDim.x) {
-      Wt[idx] = w.W[ch * C * DK + idx];
-      QGt[idx] = w.QG[ch * C * DK + idx];
-      KDt[idx] = w.KD[ch * C * DK + idx];
+    {  // E = U[:, cols] - W S
+      MmAcc<C, NT, STH> acc;
+      mm_zero<C, NT, STH>(acc);
+      cta_mm_sb<C, NT, DK, STH, true>(acc, slab, [&](int m, int k) { return W[m * DK + k]; }, S, LDS);
+      mm_out<C, NT, STH>(acc, [&](int m, int n, float v) { E[m * LDS + n] = w.U[(ch * C + m) * DV + c0col + n] - v; });
     }
-    for (int idx = tid; idx < C * C; idx += blockDim.x) Pt[idx] = w.P[ch * C * C + idx];
-    for (int i = tid; i < DK; i += blockDim.x) gm[i] = w.gam[ch * DK + i];
-    __syncthreads();
-    for (int idx = tid; idx < C * NT; idx += blockDim.x) {
-      int r = idx / NT, jj = idx % NT;
-      float acc = w.U[(ch * C + r) * DV + c0col + jj];
-      for (int i = 0; i < DK; i++) acc -= Wt[r * DK + i] * S[i * NT + jj];
-      E[idx] = acc;
+    {  // O = QG S + P E (rows < L)
+      const float* QG = w.QG + ch * C * DK;
+      const float* P = w.P + ch * C * C;
+      MmAcc<C, NT, STH> acc;
+      mm_zero<C, NT, STH>(acc);
+      cta_mm_sb<C, NT, DK, STH, true>(acc, slab, [&](int m, int k) { return QG[m * DK + k]; }, S, LDS);
+      cta_mm_sb<C, NT, C, STH, true>(acc, slab, [&](int m, int k) { return P[m * C + k]; }, E, LDS);
+      mm_out<C, NT, STH>(acc, [&](int m, int n, float v) {
+        if (m < L) stf(o + ((int64_t)(t0 + m) * H + h) * DV + c0col + n, v);
+      });
     }
-    __syncthreads();
-    for (int idx = tid; idx < C * NT; idx += blockDim.x) {
-      int r = idx / NT, jj = idx % NT;
-      if (r < L) {
-        float acc = 0.f;
-        for (int i = 0; i < DK; i++) acc += QGt[r * DK + i] * S[i * NT + jj];
-        for (int s = 0; s <= r; s++) acc += Pt[r * C + s] * E[s * NT + jj];
-        stf(o + ((int64_t)(t0 + r) * H + h) * DV + c0col + jj, acc);
-      }
+    {  // S' = Diag(gamma) S + KD^T E (each thread rewrites only the entries it owns)
+      const float* KD = w.KD + ch * C * DK;
+      const float* gm = w.gam + ch * DK;
+      MmAcc<DK, NT, STH> acc;
+      mm_zero<DK, NT, STH>(acc);
+      cta_mm_sb<DK, NT, C, STH, false>(acc, slab, [&](int m, int k) { return KD[k * DK + m]; }, E, LDS);
+      mm_out<DK, NT, STH>(acc, [&](int m, int n, float v) { S[m * LDS + n] = gm[m] * S[m * LDS + n] + v; });
     }
-    float nv[(DK * NT + STH - 1) / STH];
-#pragma unroll
-    for (int u = 0; u < (DK * NT + STH - 1) / STH; u++) {
-      int idx = tid + u * STH;
-      if (idx < DK * NT) {
-        int i = idx / NT, jj = idx % NT;
-        float acc = gm[i] * S[idx];
-        for (int r = 0; r < C; r++) acc += KDt[r * DK + i] * E[r * NT + jj];
-        nv[u] = acc;
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int u = 0; u < (DK * NT + STH - 1) / STH; u++) {
-      int idx = tid + u * STH;
-      if (idx < DK * NT) S[idx] = nv[u];
-    }
-    __syncthreads();
   }
+  __syncthreads();
   if (io.h_final)
-    for (int idx = tid; idx < DK * NT; idx += blockDim.x) {
-      int i = idx / NT, jj = idx % NT;
-      io.h_final[(((int64_t)doc * H + h) * DK + i) * DV + c0col + jj] = S[idx];
+    for (int idx = tid; idx < DK * NT; idx += STH) {
+      const int i = idx / NT, jj = idx % NT;
+      io.h_final[dh + i * DV + c0col + jj] = S[i * LDS + jj];
     }
 }
 
 template <typename TI, int DK, int DV>
 static cudaError_t fwd_intra_launch(const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st) {
   constexpr int NMAX = DK > DV ? DK : DV;
-  size_t smem = sizeof(float) * (3 * C * DK + C * DV + 2 * C * C + C + mm_slab_floats(NMAX > C ? NMAX : C));
+  size_t smem = sizeof(float) * (3 * C * DK + C * DV + 2 * C * C + C + mm_slab_floats(C, NMAX > C ? NMAX : C));
   cudaError_t e = cudaFuncSetAttribute(fwd_intra_kernel<TI, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(d.nc_max, d.H);
@@ -244,7 +241,7 @@ static cudaError_t fwd_intra_launch(const Dims& d, const FwdIO& io, const Ws& w,
 
 template <typename TI, int DK, int DV>
 static cudaError_t fwd_scan_launch(const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st) {
-  size_t smem = sizeof(float) * (DK * NT + C * NT + 3 * C * DK + C * C + DK);
+  size_t smem = sizeof(float) * ((DK + C) * LDS + KS * ((DK > C ? DK : C) + 1));
   cudaError_t e = cudaFuncSetAttribute(fwd_scan_kernel<TI, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(d.n_docs, d.H, DV / NT);

@@ -1,4 +1,4 @@
-// CTA-wide fp32 products of the general (SIMT) kernels: C x N outputs of
+// CTA-wide fp32 products of the general (SIMT) kernels: M x N outputs of
 // sum_k A(m, k) B(k, n), with the operands staged through shared memory in
 // KS-wide slabs so that every global read is coalesced and every shared
 // read is a broadcast or a conflict-free 16-byte load.
@@ -8,68 +8,123 @@
 namespace kda {
 
 constexpr int KS = 32;         // k slab of a staged product
-constexpr int APAD = C + 4;    // row stride of the A slab [KS][C]
+constexpr float LOG2E_S = 1.4426950408889634f;  // the general kernels keep G in log2 units
 
-// Floats of shared memory the two slabs of an N-column product take.
-constexpr int mm_slab_floats(int nmax) { return KS * APAD + KS * (nmax + 4); }
+// Floats of shared memory the slabs of products with up to mmax rows and
+// nmax columns take (the A slab [KS][mmax + 1], then the B slab [KS][nmax + 4]).
+constexpr int mm_slab_floats(int mmax, int nmax) { return KS * (mmax + 1) + KS * (nmax + 4); }
 
-// Thread layout of an N-column product on NTH threads: NG = N / 4 column
-// groups of four, RPT rows per thread; threads at or past ACT are idle.
-template <int N, int NTH>
+// Thread layout of an M x N product on NTH threads: NG = N / 4 column groups
+// of four, RPT rows per thread; threads at or past ACT are idle.
+template <int M, int N, int NTH>
 struct MmShape {
   static constexpr int NG = N / 4;
-  static constexpr int ACT = NG * C < NTH ? NG * C : NTH;
-  static constexpr int RPT = C * NG / ACT;
-  static_assert(N % 4 == 0 && ACT % NG == 0 && (C * NG) % ACT == 0, "product shape");
+  static constexpr int ACT = NG * M < NTH ? NG * M : NTH;
+  static constexpr int RPT = M * NG / ACT;
+  static_assert(N % 4 == 0 && ACT % NG == 0 && (M * NG) % ACT == 0, "product shape");
 };
+template <int M, int N, int NTH>
+using MmAcc = float[MmShape<M, N, NTH>::RPT][4];
 
-// acc (this thread's RPT x 4 outputs: rows RPT (tid / NG) + q, columns
-// 4 (tid % NG) + e) += sum over k < K of fa(m, k) fb(k, n).  AK: A's k index
-// is contiguous in memory (else m); BN: B's n index is contiguous (else k);
-// these pick the staging order.  as / bs: mm_slab_floats(N) floats of shared
-// memory (as first).  Every thread of the CTA must call it; it starts with a
-// barrier (the slabs' previous readers, and the operands' writers, are done)
-// and ends without one.
-template <int N, int K, int NTH, bool AK, bool BN, class FA, class FB>
-__device__ __forceinline__ void cta_mm(float (&acc)[MmShape<N, NTH>::RPT][4], float* sm_slab, FA fa, FB fb) {
-  using S = MmShape<N, NTH>;
-  constexpr int BS = N + 4;
-  static_assert(K % KS == 0, "k must be a multiple of the slab");
-  float* as = sm_slab;
-  float* bs = sm_slab + KS * APAD;
-  const int tid = threadIdx.x, ng = tid % S::NG, m0 = (tid / S::NG) * S::RPT;
-  for (int k0 = 0; k0 < K; k0 += KS) {
-    __syncthreads();
-    for (int e = tid; e < C * KS; e += NTH) {
-      const int m = AK ? e / KS : e % C, k = AK ? e % KS : e / C;
-      as[k * APAD + m] = fa(m, k0 + k);
-    }
-    for (int e = tid; e < KS * N; e += NTH) {
-      const int k = BN ? e / N : e % KS, n = BN ? e % N : e / KS;
-      bs[k * BS + n] = fb(k0 + k, n);
-    }
-    __syncthreads();
-    if (tid < S::ACT) {
+// Stages the A slab: as[k][m] = fa(m, k0 + k) for k < KS, m < M.  AK: A's k
+// index is contiguous in memory (else m), which picks the thread order.
+template <int M, int NTH, bool AK, class FA>
+__device__ __forceinline__ void stage_a(float* as, int k0, FA fa) {
+  for (int e = threadIdx.x; e < M * KS; e += NTH) {
+    const int m = AK ? e / KS : e % M, k = AK ? e % KS : e / M;
+    as[k * (M + 1) + m] = fa(m, k0 + k);
+  }
+}
+
+// acc[q][e] += sum over k < KS of as[k][m0 + q] b(k)[4 ng + e], with b's row
+// k at bs + k * ldb (16-byte aligned, ldb a multiple of 4).
+template <int M, int N, int NTH>
+__device__ __forceinline__ void slab_fma(MmAcc<M, N, NTH>& acc, const float* as, const float* bs, int ldb) {
+  using S = MmShape<M, N, NTH>;
+  const int tid = threadIdx.x;
+  if (tid >= S::ACT) return;
+  const int ng = tid % S::NG, m0 = (tid / S::NG) * S::RPT;
 #pragma unroll 8
-      for (int k = 0; k < KS; k++) {
-        const float4 b = *reinterpret_cast<const float4*>(bs + k * BS + 4 * ng);
+  for (int k = 0; k < KS; k++) {
+    const float4 b = *reinterpret_cast<const float4*>(bs + k * ldb + 4 * ng);
 #pragma unroll
-        for (int q = 0; q < S::RPT; q++) {
-          const float a = as[k * APAD + m0 + q];
-          acc[q][0] = fmaf(a, b.x, acc[q][0]);
-          acc[q][1] = fmaf(a, b.y, acc[q][1]);
-          acc[q][2] = fmaf(a, b.z, acc[q][2]);
-          acc[q][3] = fmaf(a, b.w, acc[q][3]);
-        }
-      }
+    for (int q = 0; q < S::RPT; q++) {
+      const float a = as[k * (M + 1) + m0 + q];
+      acc[q][0] = fmaf(a, b.x, acc[q][0]);
+      acc[q][1] = fmaf(a, b.y, acc[q][1]);
+      acc[q][2] = fmaf(a, b.z, acc[q][2]);
+      acc[q][3] = fmaf(a, b.w, acc[q][3]);
     }
   }
 }
 
+// acc (this thread's RPT x 4 outputs: rows RPT (tid / NG) + q, columns
+// 4 (tid % NG) + e) += sum over k < K of fa(m, k) fb(k, n), both operands
+// staged.  BN: B's n index is contiguous (else k).  slab: mm_slab_floats(M, N)
+// floats of shared memory.  Every thread of the CTA must call it; it starts
+// with a barrier (the slab's previous readers, and the operands' writers,
+// are done) and ends without one.
+template <int M, int N, int K, int NTH, bool AK, bool BN, class FA, class FB>
+__device__ __forceinline__ void cta_mm(MmAcc<M, N, NTH>& acc, float* slab, FA fa, FB fb) {
+  static_assert(K % KS == 0, "k must be a multiple of the slab");
+  constexpr int BS = N + 4;
+  float* as = slab;
+  float* bs = slab + KS * (M + 1);
+  for (int k0 = 0; k0 < K; k0 += KS) {
+    __syncthreads();
+    stage_a<M, NTH, AK>(as, k0, fa);
+    for (int e = threadIdx.x; e < KS * N; e += NTH) {
+      const int k = BN ? e / N : e % KS, n = BN ? e % N : e / KS;
+      bs[k * BS + n] = fb(k0 + k, n);
+    }
+    __syncthreads();
+    slab_fma<M, N, NTH>(acc, as, bs, BS);
+  }
+}
+
+// As cta_mm, with B already in shared memory: row k of B at b + k * ldb
+// (16-byte aligned, ldb a multiple of 4); only A is staged (slab: at least
+// KS (M + 1) floats).  Every A element this thread stages, over all K / KS
+// slabs, is loaded into registers first, so that the product waits for one
+// memory latency rather than one per slab.
+template <int M, int N, int K, int NTH, bool AK, class FA>
+__device__ __forceinline__ void cta_mm_sb(MmAcc<M, N, NTH>& acc, float* slab, FA fa, const float* b, int ldb) {
+  static_assert(K % KS == 0 && (M * KS) % NTH == 0, "k must be a multiple of the slab, the slab of the threads");
+  constexpr int NS = K / KS, PER = M * KS / NTH;
+  float pre[NS][PER];
+#pragma unroll
+  for (int sl = 0; sl < NS; sl++)
+#pragma unroll
+    for (int u = 0; u < PER; u++) {
+      const int e = threadIdx.x + u * NTH;
+      const int m = AK ? e / KS : e % M, k = AK ? e % KS : e / M;
+      pre[sl][u] = fa(m, sl * KS + k);
+    }
+#pragma unroll
+  for (int sl = 0; sl < NS; sl++) {
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < PER; u++) {
+      const int e = threadIdx.x + u * NTH;
+      const int m = AK ? e / KS : e % M, k = AK ? e % KS : e / M;
+      slab[k * (M + 1) + m] = pre[sl][u];
+    }
+    __syncthreads();
+    slab_fma<M, N, NTH>(acc, slab, b + sl * KS * ldb, ldb);
+  }
+}
+
+// Threads of the CTA prefetch n floats from p into L2 (one request per
+// 128-byte line).
+template <int NTH>
+__device__ __forceinline__ void prefetch_span(const float* p, int n) {
+  for (int o = threadIdx.x * 32; o < n; o += NTH * 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + o));
+}
+
 // Calls out(m, n, acc[q][e]) for every output this thread holds.
-template <int N, int NTH, class F>
-__device__ __forceinline__ void mm_out(const float (&acc)[MmShape<N, NTH>::RPT][4], F out) {
-  using S = MmShape<N, NTH>;
+template <int M, int N, int NTH, class F>
+__device__ __forceinline__ void mm_out(const MmAcc<M, N, NTH>& acc, F out) {
+  using S = MmShape<M, N, NTH>;
   const int tid = threadIdx.x;
   if (tid >= S::ACT) return;
   const int ng = tid % S::NG, m0 = (tid / S::NG) * S::RPT;
@@ -79,10 +134,10 @@ __device__ __forceinline__ void mm_out(const float (&acc)[MmShape<N, NTH>::RPT][
     for (int e = 0; e < 4; e++) out(m0 + q, 4 * ng + e, acc[q][e]);
 }
 
-template <int N, int NTH>
-__device__ __forceinline__ void mm_zero(float (&acc)[MmShape<N, NTH>::RPT][4]) {
+template <int M, int N, int NTH>
+__device__ __forceinline__ void mm_zero(MmAcc<M, N, NTH>& acc) {
 #pragma unroll
-  for (int q = 0; q < MmShape<N, NTH>::RPT; q++) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+  for (int q = 0; q < MmShape<M, N, NTH>::RPT; q++) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
 }
 
 }  // namespace kda
