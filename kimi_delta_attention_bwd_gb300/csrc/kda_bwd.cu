@@ -139,6 +139,13 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   float* red = dgam + DK;       // [32]
   float* slab = red + 32;       // staged-product slabs
 
+  // this chunk's saved state, state gradient and factors into L2 while the prologue runs
+  prefetch_span<GTH>(w.Sent + ch * DK * DV, DK * DV);
+  prefetch_span<GTH>(w.dSn + ch * DK * DV, DK * DV);
+  prefetch_span<GTH>(w.W + ch * C * DK, C * DK);
+  prefetch_span<GTH>(w.U + ch * C * DV, C * DV);
+  prefetch_span<GTH>(w.dE + ch * C * DV, C * DV);
+
   float* scr = w.scr + ch * w.scr_per_ch;
   float* E = scr;               // [C][DV]
   float* YU = E + C * DV;       // [C][DV]
@@ -199,26 +206,34 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   }
   __syncthreads();
 
-  // ---- intra-chunk factors (same arithmetic as the forward): one warp per
-  //      (r, s), lanes over the key channels (A' only: dP comes from dO)
-  for (int idx = warp; idx < C * C; idx += nw) {
+  // ---- intra-chunk factors (same arithmetic as the forward; A' only, dP comes
+  //      from dO): the C (C - 1) / 2 strictly lower pairs (r, s), one per
+  //      thread, each lane walking the key channels in a rotated order
+  //      (conflict-free reads); then the rest of Ap and dAm, and T's identity
+  for (int idx = tid; idx < C * C; idx += blockDim.x) {
     const int r = idx / C, s = idx % C;
+    if (s >= r) Ap[idx] = dAm[idx] = 0.f;
+    Tt[idx] = (r == s) ? 1.f : 0.f;
+  }
+  for (int p = tid; p < C * (C - 1) / 2; p += blockDim.x) {
+    int r = (int)((1.f + sqrtf(1.f + 8.f * (float)p)) * 0.5f);  // p = r (r - 1) / 2 + s, s < r
+    while (r * (r - 1) / 2 > p) r--;
+    while ((r + 1) * r / 2 <= p) r++;
+    const int s = p - r * (r - 1) / 2;
     float accA = 0.f;
-    if (s < r) {
-      for (int i = lane; i < DK; i += 32) accA += kh[r * DK + i] * kh[s * DK + i] * exp2f(G[r * DK + i] - G[s * DK + i]);
-      accA = warp_sum(accA);
+    for (int i0 = 0; i0 < DK; i0++) {
+      const int i = (i0 + lane) & (DK - 1);
+      accA += kh[r * DK + i] * kh[s * DK + i] * exp2f(G[r * DK + i] - G[s * DK + i]);
     }
-    if (lane == 0) {
-      Ap[idx] = accA;
-      dAm[idx] = bet[r] * accA;  // A = diag(beta) Ap, used for the solve
-      Tt[idx] = (r == s) ? 1.f : 0.f;
-    }
+    Ap[r * C + s] = accA;
+    dAm[r * C + s] = bet[r] * accA;  // A = diag(beta) Ap, used for the solve
   }
   __syncthreads();
   // T = (I + A)^-1 by forward substitution
   // (held transposed, Tt[c][r] = T[r][c]): each column is its own forward
   // substitution down the rows; one warp per column, lanes over the sum
-  for (int c = warp; c < C; c += nw) {
+  for (int cc = warp; cc < C; cc += nw) {  // columns w and C - 1 - w: equal work per warp
+    const int c = cc < C / 2 ? cc : C / 2 + C - 1 - cc;
     float* tc = Tt + c * C;
     for (int r = c + 1; r < C; r++) {
       float acc = 0.f;
@@ -343,27 +358,60 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   }
   __syncthreads();
 
-  // ---- per channel: G_last terms, reverse cumsum -> dg, gate backward, partials
+  // ---- per channel: G_last terms, reverse cumsum -> dg, gate backward, partials.
+  //      Channel i's rows split into NSEG segments of RPS rows, one thread each:
+  //      segment totals first, then each segment adds the totals after it (a
+  //      fixed order, so the sums are deterministic) and walks its own rows
+  constexpr int NSEG = GTH / DK, RPS = C / NSEG;
+  static_assert(NSEG * DK == GTH && NSEG * RPS == C, "gate segments");
+  float* segd = slab;              // [NSEG][DK] segment totals of dG
+  float* sege = segd + NSEG * DK;  // [NSEG][DK] segment totals of the G_last terms
+  float* segp = sege + NSEG * DK;  // [NSEG][DK] segment partials of ddt_bias
   TI* dfo = (TI*)io.df;
-  float pA_local = 0.f;
-  for (int i = tid; i < DK; i += blockDim.x) {
-    float Glast = G[(L - 1) * DK + i];
-    float extra = dgam[i] * exp2f(Glast);
-    for (int r = 0; r < L; r++) extra += dKd[r * DK + i] * kh[r * DK + i] * exp2f(Glast - G[r * DK + i]);
-    float acc = extra;  // dG at row L-1 gets the G_last terms
-    float pdt = 0.f;
-    for (int r = L - 1; r >= 0; r--) {
-      acc += dG[r * DK + i];
-      int64_t off = ((int64_t)(t0 + r) * H + h) * DK + i;
-      float x = d.gate ? ldf(f + ((int64_t)(t0 + r) * H + h)) + io.dt_bias[h] : ldf(f + off) + io.dt_bias[h * DK + i];
-      float g = -a * softplus_f(x);
-      float dx = acc * (-a) * sigmoid_f(x);
-      if (d.gate) dG[r * DK + i] = dx;  // summed over the channels below
-      else stf(dfo + off, dx);
-      pdt += dx;
-      pA_local += acc * g;
+  const int gi = tid % DK, gseg = tid / DK, r0 = gseg * RPS;
+  const float Glast = G[(L - 1) * DK + gi];
+  {
+    float sd = 0.f, se = 0.f;
+#pragma unroll
+    for (int u = 0; u < RPS; u++) {
+      const int r = r0 + u;
+      if (r < L) {
+        sd += dG[r * DK + gi];
+        se += dKd[r * DK + gi] * kh[r * DK + gi] * exp2f(Glast - G[r * DK + gi]);
+      }
     }
-    w.pdt[ch * DK + i] = pdt;
+    segd[gseg * DK + gi] = sd;
+    sege[gseg * DK + gi] = se;
+  }
+  __syncthreads();
+  float pA_local = 0.f;
+  {
+    float acc = dgam[gi] * exp2f(Glast);  // dG at row L-1 gets the G_last terms
+    for (int sg = 0; sg < NSEG; sg++) acc += sege[sg * DK + gi];
+    for (int sg = NSEG - 1; sg > gseg; sg--) acc += segd[sg * DK + gi];
+    float pdt = 0.f;
+#pragma unroll
+    for (int u = RPS - 1; u >= 0; u--) {
+      const int r = r0 + u;
+      if (r < L) {
+        acc += dG[r * DK + gi];
+        const int64_t off = ((int64_t)(t0 + r) * H + h) * DK + gi;
+        const float x = d.gate ? ldf(f + ((int64_t)(t0 + r) * H + h)) + io.dt_bias[h] : ldf(f + off) + io.dt_bias[h * DK + gi];
+        const float g = -a * softplus_f(x);
+        const float dx = acc * (-a) * sigmoid_f(x);
+        if (d.gate) dG[r * DK + gi] = dx;  // summed over the channels below
+        else stf(dfo + off, dx);
+        pdt += dx;
+        pA_local += acc * g;
+      }
+    }
+    segp[gseg * DK + gi] = pdt;
+  }
+  __syncthreads();
+  for (int i = tid; i < DK; i += blockDim.x) {
+    float p = 0.f;
+    for (int sg = 0; sg < NSEG; sg++) p += segp[sg * DK + i];
+    w.pdt[ch * DK + i] = p;
   }
   float tot = block_sum(pA_local, red);
   if (tid == 0) w.pA[ch] = tot;

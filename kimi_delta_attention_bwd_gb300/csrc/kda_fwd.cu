@@ -83,34 +83,41 @@ __global__ void __launch_bounds__(GTH) fwd_intra_kernel(Dims d, FwdIO io, Ws w) 
   }
   __syncthreads();
 
-  // A (strict lower, beta-scaled) and P (inclusive lower, scale-scaled): one
-  // warp per (r, s), lanes over the key channels.
+  // A (strict lower, beta-scaled) and P (inclusive lower, scale-scaled): the
+  // C (C + 1) / 2 pairs s <= r, one per thread, each lane walking the key
+  // channels in a rotated order (conflict-free reads); then the upper parts
+  // and T's identity.
   float* Pg = w.P + ch * C * C;
-  for (int idx = warp; idx < C * C; idx += nw) {
+  for (int idx = tid; idx < C * C; idx += blockDim.x) {
     const int r = idx / C, s = idx % C;
+    if (s > r) {
+      Am[idx] = 0.f;
+      Pg[idx] = 0.f;
+    }
+    Tt[idx] = (r == s) ? 1.f : 0.f;
+  }
+  for (int p = tid; p < C * (C + 1) / 2; p += blockDim.x) {
+    int r = (int)((sqrtf(8.f * (float)p + 1.f) - 1.f) * 0.5f);  // p = r (r + 1) / 2 + s, s <= r
+    while (r * (r + 1) / 2 > p) r--;
+    while ((r + 1) * (r + 2) / 2 <= p) r++;
+    const int s = p - r * (r + 1) / 2;
     float accA = 0.f, accP = 0.f;
-    if (s <= r) {
-      for (int i = lane; i < DK; i += 32) {
-        const float e = exp2f(G[r * DK + i] - G[s * DK + i]);
-        const float ks = kh[s * DK + i] * e;
-        accP += qh[r * DK + i] * ks;
-        accA += kh[r * DK + i] * ks;
-      }
-      accP = warp_sum(accP);
-      accA = warp_sum(accA);
+    for (int i0 = 0; i0 < DK; i0++) {
+      const int i = (i0 + lane) & (DK - 1);
+      const float ks = kh[s * DK + i] * exp2f(G[r * DK + i] - G[s * DK + i]);
+      accP += qh[r * DK + i] * ks;
+      accA += kh[r * DK + i] * ks;
     }
-    if (lane == 0) {
-      Am[idx] = s < r ? bet[r] * accA : 0.f;
-      Pg[idx] = d.scale * accP;
-      Tt[idx] = (r == s) ? 1.f : 0.f;
-    }
+    Am[r * C + s] = s < r ? bet[r] * accA : 0.f;
+    Pg[r * C + s] = d.scale * accP;
   }
   __syncthreads();
 
   // T = (I + A)^-1 by forward substitution
   // (held transposed, Tt[c][r] = T[r][c]): each column is its own forward
   // substitution down the rows; one warp per column, lanes over the sum
-  for (int c = warp; c < C; c += nw) {
+  for (int cc = warp; cc < C; cc += nw) {  // columns w and C - 1 - w: equal work per warp
+    const int c = cc < C / 2 ? cc : C / 2 + C - 1 - cc;
     float* tc = Tt + c * C;
     for (int r = c + 1; r < C; r++) {
       float acc = 0.f;

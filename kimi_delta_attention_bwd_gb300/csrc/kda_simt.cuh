@@ -66,18 +66,39 @@ __device__ __forceinline__ void slab_fma(MmAcc<M, N, NTH>& acc, const float* as,
 // are done) and ends without one.
 template <int M, int N, int K, int NTH, bool AK, bool BN, class FA, class FB>
 __device__ __forceinline__ void cta_mm(MmAcc<M, N, NTH>& acc, float* slab, FA fa, FB fb) {
-  static_assert(K % KS == 0, "k must be a multiple of the slab");
-  constexpr int BS = N + 4;
+  static_assert(K % KS == 0 && (M * KS) % NTH == 0 && (N * KS) % NTH == 0, "k a multiple of the slab, slabs of the threads");
+  constexpr int BS = N + 4, PA = M * KS / NTH, PB = N * KS / NTH;
   float* as = slab;
   float* bs = slab + KS * (M + 1);
+  // software pipeline: slab k0 + KS is loaded into registers while slab k0 is multiplied
+  float ra[PA], rb[PB];
+  auto load = [&](int k0) {
+#pragma unroll
+    for (int u = 0; u < PA; u++) {
+      const int e = threadIdx.x + u * NTH;
+      ra[u] = fa(AK ? e / KS : e % M, k0 + (AK ? e % KS : e / M));
+    }
+#pragma unroll
+    for (int u = 0; u < PB; u++) {
+      const int e = threadIdx.x + u * NTH;
+      rb[u] = fb(k0 + (BN ? e / N : e % KS), BN ? e % N : e / KS);
+    }
+  };
+  load(0);
   for (int k0 = 0; k0 < K; k0 += KS) {
     __syncthreads();
-    stage_a<M, NTH, AK>(as, k0, fa);
-    for (int e = threadIdx.x; e < KS * N; e += NTH) {
-      const int k = BN ? e / N : e % KS, n = BN ? e % N : e / KS;
-      bs[k * BS + n] = fb(k0 + k, n);
+#pragma unroll
+    for (int u = 0; u < PA; u++) {
+      const int e = threadIdx.x + u * NTH;
+      as[(AK ? e % KS : e / M) * (M + 1) + (AK ? e / KS : e % M)] = ra[u];
+    }
+#pragma unroll
+    for (int u = 0; u < PB; u++) {
+      const int e = threadIdx.x + u * NTH;
+      bs[(BN ? e / N : e % KS) * BS + (BN ? e % N : e / KS)] = rb[u];
     }
     __syncthreads();
+    if (k0 + KS < K) load(k0 + KS);
     slab_fma<M, N, NTH>(acc, as, bs, BS);
   }
 }
