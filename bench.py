@@ -75,10 +75,17 @@ def step_bytes(w, backward=True) -> float:
     return float(th * (fwd + (bwd if backward else 0)))
 
 
-def source_sha() -> str:
+# Sources of the tensor-core kernels: their translation unit with its headers,
+# and the host code that lays out their workspace and launches them.  A
+# profile taken on these files stays valid while they are unchanged.
+TC_SOURCES = ("kda_api.cu", "kda_fast.cu", "kda_internal.cuh", "kda_mma.cuh", "kda_tc.cuh")
+
+
+def source_sha(files=None) -> str:
+    """sha256 (16 hex digits) over the named kernel source files (default: all of csrc)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kimi_delta_attention_bwd_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files or os.listdir(csrc)):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -86,7 +93,8 @@ def source_sha() -> str:
 
 def ncu_traffic(kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or
-    None when absent or taken on different kernel sources."""
+    None when absent or taken on different kernel sources (the entry names
+    the source files its hash covers)."""
     p = os.path.join(PROFILES, "ncu_traffic.json")
     try:
         with open(p) as fh:
@@ -94,7 +102,7 @@ def ncu_traffic(kernel: str):
     except (OSError, ValueError):
         return None
     e = d.get(kernel)
-    if not e or e.get("source_sha") != source_sha():
+    if not e or e.get("source_sha") != source_sha(e.get("source_files")):
         return None
     return e.get("bytes_per_launch")
 
