@@ -209,11 +209,10 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   // ---- intra-chunk factors (same arithmetic as the forward; A' only, dP comes
   //      from dO): the C (C - 1) / 2 strictly lower pairs (r, s), one per
   //      thread, each lane walking the key channels in a rotated order
-  //      (conflict-free reads); then the rest of Ap and dAm, and T's identity
+  //      (conflict-free reads); then the rest of Ap and dAm
   for (int idx = tid; idx < C * C; idx += blockDim.x) {
     const int r = idx / C, s = idx % C;
     if (s >= r) Ap[idx] = dAm[idx] = 0.f;
-    Tt[idx] = (r == s) ? 1.f : 0.f;
   }
   for (int p = tid; p < C * (C - 1) / 2; p += blockDim.x) {
     int r = (int)((1.f + sqrtf(1.f + 8.f * (float)p)) * 0.5f);  // p = r (r - 1) / 2 + s, s < r
@@ -229,21 +228,8 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
     dAm[r * C + s] = bet[r] * accA;  // A = diag(beta) Ap, used for the solve
   }
   __syncthreads();
-  // T = (I + A)^-1 by forward substitution
-  // (held transposed, Tt[c][r] = T[r][c]): each column is its own forward
-  // substitution down the rows; one warp per column, lanes over the sum
-  for (int cc = warp; cc < C; cc += nw) {  // columns w and C - 1 - w: equal work per warp
-    const int c = cc < C / 2 ? cc : C / 2 + C - 1 - cc;
-    float* tc = Tt + c * C;
-    for (int r = c + 1; r < C; r++) {
-      float acc = 0.f;
-      for (int s = c + lane; s < r; s += 32) acc += dAm[r * C + s] * tc[s];
-      acc = warp_sum(acc);
-      if (lane == 0) tc[r] = -acc;
-      __syncwarp();
-    }
-  }
-  __syncthreads();
+  // T = (I + A)^-1, held transposed (Tt[c][r] = T[r][c])
+  unit_lower_inverse_t<GTH>(dAm, Tt, slab);
 
   // ---- E = U - W S (scratch), dgamma; then with the value columns as k:
   //      dQG = scale dO S^T, dW = -dE S^T, dKd = E dS'^T (products staged

@@ -85,8 +85,7 @@ __global__ void __launch_bounds__(GTH) fwd_intra_kernel(Dims d, FwdIO io, Ws w) 
 
   // A (strict lower, beta-scaled) and P (inclusive lower, scale-scaled): the
   // C (C + 1) / 2 pairs s <= r, one per thread, each lane walking the key
-  // channels in a rotated order (conflict-free reads); then the upper parts
-  // and T's identity.
+  // channels in a rotated order (conflict-free reads); then the upper parts.
   float* Pg = w.P + ch * C * C;
   for (int idx = tid; idx < C * C; idx += blockDim.x) {
     const int r = idx / C, s = idx % C;
@@ -94,7 +93,6 @@ __global__ void __launch_bounds__(GTH) fwd_intra_kernel(Dims d, FwdIO io, Ws w) 
       Am[idx] = 0.f;
       Pg[idx] = 0.f;
     }
-    Tt[idx] = (r == s) ? 1.f : 0.f;
   }
   for (int p = tid; p < C * (C + 1) / 2; p += blockDim.x) {
     int r = (int)((sqrtf(8.f * (float)p + 1.f) - 1.f) * 0.5f);  // p = r (r + 1) / 2 + s, s <= r
@@ -113,21 +111,8 @@ __global__ void __launch_bounds__(GTH) fwd_intra_kernel(Dims d, FwdIO io, Ws w) 
   }
   __syncthreads();
 
-  // T = (I + A)^-1 by forward substitution
-  // (held transposed, Tt[c][r] = T[r][c]): each column is its own forward
-  // substitution down the rows; one warp per column, lanes over the sum
-  for (int cc = warp; cc < C; cc += nw) {  // columns w and C - 1 - w: equal work per warp
-    const int c = cc < C / 2 ? cc : C / 2 + C - 1 - cc;
-    float* tc = Tt + c * C;
-    for (int r = c + 1; r < C; r++) {
-      float acc = 0.f;
-      for (int s = c + lane; s < r; s += 32) acc += Am[r * C + s] * tc[s];
-      acc = warp_sum(acc);
-      if (lane == 0) tc[r] = -acc;
-      __syncwarp();
-    }
-  }
-  __syncthreads();
+  // T = (I + A)^-1, held transposed (Tt[c][r] = T[r][c])
+  unit_lower_inverse_t<GTH>(Am, Tt, slab);
 
   float* Wg = w.W + ch * C * DK;
   float* QGg = w.QG + ch * C * DK;

@@ -135,6 +135,60 @@ __device__ __forceinline__ void cta_mm_sb(MmAcc<M, N, NTH>& acc, float* slab, FA
   }
 }
 
+// T = (I + A)^-1 for the strictly lower C x C matrix A (row-major), written
+// transposed: tt[c * C + r] = T[r][c], zero above the diagonal.  In 16 x 16
+// blocks: the four diagonal blocks by forward substitution (one warp each,
+// lane = column, the column in registers), then the blocks below them by
+// block distance, T_IJ = -T_II sum over K in [J, I) of A_IK T_KJ; each
+// thread's sum over k starts at a lane-dependent offset so that the
+// transposed reads fall in distinct banks.  x: 768 floats of scratch.  Every
+// thread of the CTA calls it (NTH >= 768); A must be visible on entry (a
+// barrier after it was written), and the result is on exit.
+template <int NTH>
+__device__ __forceinline__ void unit_lower_inverse_t(const float* A, float* tt, float* x) {
+  static_assert(C == 64 && NTH >= 768, "blocked inverse layout");
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int idx = tid; idx < C * C; idx += NTH) {  // the blocks above the diagonal
+    const int c = idx / C, r = idx % C;
+    if ((r >> 4) < (c >> 4)) tt[idx] = 0.f;
+  }
+  if (warp < 4 && lane < 16) {
+    const int I = warp, c = lane;
+    const float* Ab = A + 16 * I * C + 16 * I;
+    float t[16];
+#pragma unroll
+    for (int r = 0; r < 16; r++) {
+      float v = (r == c) ? 1.f : 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < r; s2++) v = fmaf(-Ab[r * C + s2], t[s2], v);
+      t[r] = v;
+    }
+#pragma unroll
+    for (int r = 0; r < 16; r++) tt[(16 * I + c) * C + 16 * I + r] = t[r];
+  }
+  __syncthreads();
+  for (int dl = 1; dl < 4; dl++) {
+    const int nb = 4 - dl, span = 16 * dl;
+    const int J = tid >> 8, I = J + dl, r = (tid >> 4) & 15, c = tid & 15;
+    if (tid < nb * 256) {  // X_IJ = sum_K A_IK T_KJ
+      float v = 0.f;
+      for (int kk = 0; kk < span; kk++) {
+        const int k = 16 * J + (kk + c) % span;
+        v = fmaf(A[(16 * I + r) * C + k], tt[(16 * J + c) * C + k], v);
+      }
+      x[tid] = v;
+    }
+    __syncthreads();
+    if (tid < nb * 256) {  // T_IJ = -T_II X_IJ
+      float v = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; k++) v = fmaf(tt[(16 * I + k) * C + 16 * I + r], x[J * 256 + k * 16 + c], v);
+      tt[(16 * J + c) * C + 16 * I + r] = -v;
+    }
+    __syncthreads();
+  }
+}
+
 // Threads of the CTA prefetch n floats from p into L2 (one request per
 // 128-byte line).
 template <int NTH>
