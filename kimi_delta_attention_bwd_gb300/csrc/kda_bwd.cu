@@ -235,11 +235,11 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   //      dQG = scale dO S^T, dW = -dE S^T, dKd = E dS'^T (products staged
   //      through shared memory, every global read coalesced)
   {
-    MmAcc<C, DV, GTH> acc;
-    mm_zero<C, DV, GTH>(acc);
-    cta_mm<C, DV, DK, GTH, true, true>(acc, slab, [&](int m, int k) { return Wg[m * DK + k]; },
+    TcAcc<C, DV, GTH> acc;
+    tc_zero<C, DV, GTH>(acc);
+    cta_mma<C, DV, DK, GTH, true, true>(acc, slab, [&](int m, int k) { return Wg[m * DK + k]; },
                                     [&](int k, int n) { return Sg[k * DV + n]; });
-    mm_out<C, DV, GTH>(acc, [&](int m, int n, float v) { E[m * DV + n] = Ug[m * DV + n] - v; });
+    tc_out<C, DV, GTH>(acc, [&](int m, int n, float v) { E[m * DV + n] = Ug[m * DV + n] - v; });
   }
   for (int i = warp; i < DK; i += nw) {
     float acc = 0.f;
@@ -250,40 +250,40 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   const TI* dOc = dO + ((int64_t)t0 * H + h) * DV;  // row r of the chunk at dOc + r H dv
   auto fdO = [&](int m, int k) { return m < L ? ldf(dOc + (int64_t)m * H * DV + k) : 0.f; };
   {
-    MmAcc<C, DK, GTH> acc;
-    mm_zero<C, DK, GTH>(acc);
-    cta_mm<C, DK, DV, GTH, true, false>(acc, slab, fdO, [&](int k, int n) { return Sg[n * DV + k]; });
-    mm_out<C, DK, GTH>(acc, [&](int m, int n, float v) { dQG[m * DK + n] = scale * v; });
-    mm_zero<C, DK, GTH>(acc);
-    cta_mm<C, DK, DV, GTH, true, false>(acc, slab, [&](int m, int k) { return dEg[m * DV + k]; },
+    TcAcc<C, DK, GTH> acc;
+    tc_zero<C, DK, GTH>(acc);
+    cta_mma<C, DK, DV, GTH, true, false>(acc, slab, fdO, [&](int k, int n) { return Sg[n * DV + k]; });
+    tc_out<C, DK, GTH>(acc, [&](int m, int n, float v) { dQG[m * DK + n] = scale * v; });
+    tc_zero<C, DK, GTH>(acc);
+    cta_mma<C, DK, DV, GTH, true, false>(acc, slab, [&](int m, int k) { return dEg[m * DV + k]; },
                                      [&](int k, int n) { return Sg[n * DV + k]; });
-    mm_out<C, DK, GTH>(acc, [&](int m, int n, float v) { dW[m * DK + n] = -v; });
-    mm_zero<C, DK, GTH>(acc);
-    cta_mm<C, DK, DV, GTH, true, false>(acc, slab, [&](int m, int k) { return E[m * DV + k]; },
+    tc_out<C, DK, GTH>(acc, [&](int m, int n, float v) { dW[m * DK + n] = -v; });
+    tc_zero<C, DK, GTH>(acc);
+    cta_mma<C, DK, DV, GTH, true, false>(acc, slab, [&](int m, int k) { return E[m * DV + k]; },
                                      [&](int k, int n) { return dSg[n * DV + k]; });
-    mm_out<C, DK, GTH>(acc, [&](int m, int n, float v) { dKd[m * DK + n] = v; });
+    tc_out<C, DK, GTH>(acc, [&](int m, int n, float v) { dKd[m * DK + n] = v; });
   }
 
   // ---- dP = scale dO E^T (inclusive lower, rows < L), YW = T^T dW, YU = T^T dE
   {
-    MmAcc<C, C, GTH> acc;
-    mm_zero<C, C, GTH>(acc);
-    cta_mm<C, C, DV, GTH, true, false>(acc, slab, fdO, [&](int k, int n) { return E[n * DV + k]; });
-    mm_out<C, C, GTH>(acc, [&](int m, int n, float v) { dPm[m * C + n] = n <= m && m < L ? scale * v : 0.f; });
+    TcAcc<C, C, GTH> acc;
+    tc_zero<C, C, GTH>(acc);
+    cta_mma<C, C, DV, GTH, true, false>(acc, slab, fdO, [&](int k, int n) { return E[n * DV + k]; });
+    tc_out<C, C, GTH>(acc, [&](int m, int n, float v) { dPm[m * C + n] = n <= m && m < L ? scale * v : 0.f; });
   }
   {
-    MmAcc<C, DK, GTH> acc;
-    mm_zero<C, DK, GTH>(acc);
-    cta_mm<C, DK, C, GTH, true, true>(acc, slab, [&](int m, int k) { return Tt[m * C + k]; },
+    TcAcc<C, DK, GTH> acc;
+    tc_zero<C, DK, GTH>(acc);
+    cta_mma<C, DK, C, GTH, true, true>(acc, slab, [&](int m, int k) { return Tt[m * C + k]; },
                                     [&](int k, int n) { return dW[k * DK + n]; });
-    mm_out<C, DK, GTH>(acc, [&](int m, int n, float v) { YW[m * DK + n] = v; });
+    tc_out<C, DK, GTH>(acc, [&](int m, int n, float v) { YW[m * DK + n] = v; });
   }
   {
-    MmAcc<C, DV, GTH> acc;
-    mm_zero<C, DV, GTH>(acc);
-    cta_mm<C, DV, C, GTH, true, true>(acc, slab, [&](int m, int k) { return Tt[m * C + k]; },
+    TcAcc<C, DV, GTH> acc;
+    tc_zero<C, DV, GTH>(acc);
+    cta_mma<C, DV, C, GTH, true, true>(acc, slab, [&](int m, int k) { return Tt[m * C + k]; },
                                     [&](int k, int n) { return dEg[k * DV + n]; });
-    mm_out<C, DV, GTH>(acc, [&](int m, int n, float v) { YU[m * DV + n] = v; });
+    tc_out<C, DV, GTH>(acc, [&](int m, int n, float v) { YU[m * DV + n] = v; });
   }
   __syncthreads();
 
@@ -301,13 +301,13 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
     if (lane == 0) dbet[r] += acc;
   }
   {
-    MmAcc<C, C, GTH> acc;
-    mm_zero<C, C, GTH>(acc);
-    cta_mm<C, C, DV, GTH, true, false>(acc, slab, [&](int m, int k) { return YU[m * DV + k]; },
+    TcAcc<C, C, GTH> acc;
+    tc_zero<C, C, GTH>(acc);
+    cta_mma<C, C, DV, GTH, true, false>(acc, slab, [&](int m, int k) { return YU[m * DV + k]; },
                                     [&](int k, int n) { return Ug[n * DV + k]; });
-    cta_mm<C, C, DK, GTH, true, false>(acc, slab, [&](int m, int k) { return YW[m * DK + k]; },
+    cta_mma<C, C, DK, GTH, true, false>(acc, slab, [&](int m, int k) { return YW[m * DK + k]; },
                                     [&](int k, int n) { return Wg[n * DK + k]; });
-    mm_out<C, C, GTH>(acc, [&](int m, int n, float v) { dAm[m * C + n] = n < m ? -v : 0.f; });
+    tc_out<C, C, GTH>(acc, [&](int m, int n, float v) { dAm[m * C + n] = n < m ? -v : 0.f; });
   }
   __syncthreads();
   for (int r = warp; r < L; r += nw) {
@@ -496,7 +496,7 @@ static cudaError_t bwd_scan_launch(const Dims& d, const BwdIO& io, const Ws& w, 
 template <typename TI, int DK, int DV>
 static cudaError_t bwd_intra_launch(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st) {
   constexpr int NMAX = DK > DV ? DK : DV;
-  size_t smem = sizeof(float) * (3 * C * DK + 4 * C * C + 5 * C + DK + 32 + mm_slab_floats(C, NMAX > C ? NMAX : C));
+  size_t smem = sizeof(float) * (3 * C * DK + 4 * C * C + 5 * C + DK + 32 + tc_slab_floats(C, NMAX > C ? NMAX : C));
   cudaError_t e = cudaFuncSetAttribute(bwd_intra_kernel<TI, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(d.nc_max, d.H);

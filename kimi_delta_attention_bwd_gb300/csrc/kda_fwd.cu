@@ -129,19 +129,19 @@ __global__ void __launch_bounds__(GTH) fwd_intra_kernel(Dims d, FwdIO io, Ws w) 
   for (int i = tid; i < DK; i += blockDim.x) w.gam[ch * DK + i] = exp2f(Glast[i]);
   // W = T XK and U = T diag(beta) V (T unit lower, its upper part zero)
   {
-    MmAcc<C, DK, GTH> acc;
-    mm_zero<C, DK, GTH>(acc);
-    cta_mm<C, DK, C, GTH, false, true>(acc, slab, [&](int m, int k) { return Tt[k * C + m]; },
+    TcAcc<C, DK, GTH> acc;
+    tc_zero<C, DK, GTH>(acc);
+    cta_mma<C, DK, C, GTH, false, true>(acc, slab, [&](int m, int k) { return Tt[k * C + m]; },
                                    [&](int k, int n) { return xk[k * DK + n]; });
-    mm_out<C, DK, GTH>(acc, [&](int m, int n, float v) { Wg[m * DK + n] = v; });
+    tc_out<C, DK, GTH>(acc, [&](int m, int n, float v) { Wg[m * DK + n] = v; });
   }
   float* Ug = w.U + ch * C * DV;
   {
-    MmAcc<C, DV, GTH> acc;
-    mm_zero<C, DV, GTH>(acc);
-    cta_mm<C, DV, C, GTH, false, true>(acc, slab, [&](int m, int k) { return Tt[k * C + m]; },
+    TcAcc<C, DV, GTH> acc;
+    tc_zero<C, DV, GTH>(acc);
+    cta_mma<C, DV, C, GTH, false, true>(acc, slab, [&](int m, int k) { return Tt[k * C + m]; },
                                    [&](int k, int n) { return bet[k] * vv[k * DV + n]; });
-    mm_out<C, DV, GTH>(acc, [&](int m, int n, float v) { Ug[m * DV + n] = v; });
+    tc_out<C, DV, GTH>(acc, [&](int m, int n, float v) { Ug[m * DV + n] = v; });
   }
 }
 
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(STH) fwd_scan_kernel(Dims d, FwdIO io, Ws w) {
 template <typename TI, int DK, int DV>
 static cudaError_t fwd_intra_launch(const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st) {
   constexpr int NMAX = DK > DV ? DK : DV;
-  size_t smem = sizeof(float) * (3 * C * DK + C * DV + 2 * C * C + C + mm_slab_floats(C, NMAX > C ? NMAX : C));
+  size_t smem = sizeof(float) * (3 * C * DK + C * DV + 2 * C * C + C + tc_slab_floats(C, NMAX > C ? NMAX : C));
   cudaError_t e = cudaFuncSetAttribute(fwd_intra_kernel<TI, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(d.nc_max, d.H);
