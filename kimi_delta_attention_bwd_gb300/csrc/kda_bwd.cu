@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
     float accA = 0.f;
     for (int i0 = 0; i0 < DK; i0++) {
       const int i = (i0 + lane) & (DK - 1);
-      accA += kh[r * DK + i] * kh[s * DK + i] * exp2f(G[r * DK + i] - G[s * DK + i]);
+      accA += kh[r * DK + i] * kh[s * DK + i] * ex2(G[r * DK + i] - G[s * DK + i]);
     }
     Ap[r * C + s] = accA;
     dAm[r * C + s] = bet[r] * accA;  // A = diag(beta) Ap, used for the solve
@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   for (int r = warp; r < L; r += nw) {
     float acc = 0.f;
     for (int jj = lane; jj < DV; jj += 32) acc += YU[r * DV + jj] * ldf(v + ((int64_t)(t0 + r) * H + h) * DV + jj);
-    for (int i = lane; i < DK; i += 32) acc += YW[r * DK + i] * kh[r * DK + i] * exp2f(G[r * DK + i]);
+    for (int i = lane; i < DK; i += 32) acc += YW[r * DK + i] * kh[r * DK + i] * ex2(G[r * DK + i]);
     acc = warp_sum(acc);
     if (lane == 0) dbet[r] += acc;
   }
@@ -326,19 +326,19 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
     float Gr = G[idx];
     float prow = 0.f, arow = 0.f, col = 0.f;
     for (int s = 0; s <= r; s++) {
-      float e = exp2f(Gr - G[s * DK + i]);
+      float e = ex2(Gr - G[s * DK + i]);
       prow += dPm[r * C + s] * kh[s * DK + i] * e;
       arow += dAm[r * C + s] * kh[s * DK + i] * e;   // dAm is 0 on the diagonal
     }
     for (int rr = r; rr < C; rr++) {
-      float e = exp2f(G[rr * DK + i] - Gr);
+      float e = ex2(G[rr * DK + i] - Gr);
       col += dPm[rr * C + r] * qh[rr * DK + i] * e + dAm[rr * C + r] * kh[rr * DK + i] * e;
     }
-    float Gam = exp2f(Gr);
-    float KDr = kh[idx] * exp2f(G[(L - 1) * DK + i] - Gr);
+    float Gam = ex2(Gr);
+    float KDr = kh[idx] * ex2(G[(L - 1) * DK + i] - Gr);
     float dkg = bet[r] * YW[idx];  // gradient of K^ * Gamma
     dqh[idx] = prow + dQG[idx] * Gam;
-    dkh[idx] = arow + col + dkg * Gam + dKd[idx] * exp2f(G[(L - 1) * DK + i] - Gr);
+    dkh[idx] = arow + col + dkg * Gam + dKd[idx] * ex2(G[(L - 1) * DK + i] - Gr);
     dG[idx] = qh[idx] * prow + kh[idx] * arow - kh[idx] * col + dQG[idx] * qh[idx] * Gam
               + dkg * kh[idx] * Gam - dKd[idx] * KDr;
   }
@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
       const int r = r0 + u;
       if (r < L) {
         sd += dG[r * DK + gi];
-        se += dKd[r * DK + gi] * kh[r * DK + gi] * exp2f(Glast - G[r * DK + gi]);
+        se += dKd[r * DK + gi] * kh[r * DK + gi] * ex2(Glast - G[r * DK + gi]);
       }
     }
     segd[gseg * DK + gi] = sd;
@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   __syncthreads();
   float pA_local = 0.f;
   {
-    float acc = dgam[gi] * exp2f(Glast);  // dG at row L-1 gets the G_last terms
+    float acc = dgam[gi] * ex2(Glast);  // dG at row L-1 gets the G_last terms
     for (int sg = 0; sg < NSEG; sg++) acc += sege[sg * DK + gi];
     for (int sg = NSEG - 1; sg > gseg; sg--) acc += segd[sg * DK + gi];
     float pdt = 0.f;

@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(GTH) fwd_intra_kernel(Dims d, FwdIO io, Ws w) 
     float accA = 0.f, accP = 0.f;
     for (int i0 = 0; i0 < DK; i0++) {
       const int i = (i0 + lane) & (DK - 1);
-      const float ks = kh[s * DK + i] * exp2f(G[r * DK + i] - G[s * DK + i]);
+      const float ks = kh[s * DK + i] * ex2(G[r * DK + i] - G[s * DK + i]);
       accP += qh[r * DK + i] * ks;
       accA += kh[r * DK + i] * ks;
     }
@@ -121,12 +121,12 @@ __global__ void __launch_bounds__(GTH) fwd_intra_kernel(Dims d, FwdIO io, Ws w) 
   float* xk = qh;  // XK = diag(beta) (K^ * Gamma) over Q^ once QG is out
   for (int idx = tid; idx < C * DK; idx += blockDim.x) {
     const int r = idx / DK, i = idx % DK;
-    const float Gr = G[idx], eG = exp2f(Gr);
+    const float Gr = G[idx], eG = ex2(Gr);
     QGg[idx] = d.scale * qh[idx] * eG;
-    KDg[idx] = kh[idx] * exp2f(Glast[i] - Gr);
+    KDg[idx] = kh[idx] * ex2(Glast[i] - Gr);
     xk[idx] = bet[r] * kh[idx] * eG;
   }
-  for (int i = tid; i < DK; i += blockDim.x) w.gam[ch * DK + i] = exp2f(Glast[i]);
+  for (int i = tid; i < DK; i += blockDim.x) w.gam[ch * DK + i] = ex2(Glast[i]);
   // W = T XK and U = T diag(beta) V (T unit lower, its upper part zero)
   {
     TcAcc<C, DK, GTH> acc;
