@@ -117,6 +117,27 @@ def test_head_shapes(dk, dv):
     _report(f"{dk}/{dv}", compare(gpu, ref, True))
 
 
+@pytest.mark.parametrize("dk,dv", [(64, 128), (128, 128)])
+@pytest.mark.parametrize("mode", ["edge_docs", "fast_decay", "beta1"])
+def test_head_shapes_hard_cases(dk, dv, mode):
+    """The large-head kernels on packed documents with one-token, empty and
+    partial chunks, on per-token log-decays down to about -60 (in-chunk spans
+    far past fp32's exp range) and on beta = 1."""
+    lens = [1, 0, 64, 1, 65, 0, 69] if mode == "edge_docs" else None
+    w = custom(1 if lens else 2, 200, 2, dk, dv, dtype="bf16", h0=True, dh_final=True)
+    inp = make_inputs(w, seed=15, lengths=lens)
+    if mode == "fast_decay":
+        inp["A_log"].fill_(3.0)
+        inp["f"].mul_(3.0).add_(1.0)
+    elif mode == "beta1":
+        inp["b"].fill_(30.0)
+    gpu = run_gpu(inp, True)
+    for n, v in gpu.items():
+        assert np.isfinite(v).all(), n
+    ref = run_oracle(inp, True)
+    _report(f"{dk}/{dv} {mode}", compare(gpu, ref, True))
+
+
 @pytest.mark.parametrize("mode", ["beta0", "beta1", "fast_decay", "no_decay"])
 def test_degenerate_gates(mode):
     w = custom(2, 192, 2, 32, 64, dtype="f32", h0=True, dh_final=True)
