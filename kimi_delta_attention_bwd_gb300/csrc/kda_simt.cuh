@@ -25,16 +25,6 @@ struct MmShape {
 template <int M, int N, int NTH>
 using MmAcc = float[MmShape<M, N, NTH>::RPT][4];
 
-// Stages the A slab: as[k][m] = fa(m, k0 + k) for k < KS, m < M.  AK: A's k
-// index is contiguous in memory (else m), which picks the thread order.
-template <int M, int NTH, bool AK, class FA>
-__device__ __forceinline__ void stage_a(float* as, int k0, FA fa) {
-  for (int e = threadIdx.x; e < M * KS; e += NTH) {
-    const int m = AK ? e / KS : e % M, k = AK ? e % KS : e / M;
-    as[k * (M + 1) + m] = fa(m, k0 + k);
-  }
-}
-
 // acc[q][e] += sum over k < KS of as[k][m0 + q] b(k)[4 ng + e], with b's row
 // k at bs + k * ldb (16-byte aligned, ldb a multiple of 4).
 template <int M, int N, int NTH>
