@@ -55,7 +55,7 @@ def algorithmic_bytes(w, kernel: str) -> float:
     per = {
         "fwd_chain": inputs_fwd + e * dv,       # reads q, k, f, v, b; writes o
         "fwd_chunk": inputs_fwd,                # reads q, k, f, v, b
-        "fwd_out": e * dv,                      # writes o
+        "fwd_state": e * dv,                    # writes o
         "fwd_intra": inputs_fwd,
         "fwd_scan": e * dv,                     # o
         "bwd_scan": e * dv,                     # dO (general path)
