@@ -18,6 +18,8 @@ CASES = [
      [1, 0, 130, 64, 105]),
     ("general path fp32 32/64", custom(1, 200, 2, 32, 64, dtype="f32", h0=True, dh_final=True, gate="scalar"), None),
     ("general path bf16 64/128", custom(1, 150, 2, 64, 128, dtype="bf16", dh_final=True, gate="scalar"), None),
+    ("general path bf16 128/128 varlen", custom(1, 200, 2, 128, 128, dtype="bf16", h0=True, dh_final=True,
+                                                 gate="scalar"), [70, 1, 129]),
 ]
 
 

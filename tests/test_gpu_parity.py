@@ -138,6 +138,17 @@ def test_head_shapes_hard_cases(dk, dv, mode):
     _report(f"{dk}/{dv} {mode}", compare(gpu, ref, True))
 
 
+@pytest.mark.parametrize("dk,dv", [(64, 128), (128, 128)])
+def test_head_shapes_fp32_io(dk, dv):
+    """fp32 inputs and outputs on the large-head kernels (split-tf32 products),
+    packed documents with partial chunks."""
+    w = custom(1, 230, 2, dk, dv, dtype="f32", h0=True, dh_final=True)
+    inp = make_inputs(w, seed=16, lengths=[100, 1, 129])
+    gpu = run_gpu(inp, True)
+    ref = run_oracle(inp, True)
+    _report(f"{dk}/{dv} f32", compare(gpu, ref, True, bf16=False))
+
+
 @pytest.mark.parametrize("mode", ["beta0", "beta1", "fast_decay", "no_decay"])
 def test_degenerate_gates(mode):
     w = custom(2, 192, 2, 32, 64, dtype="f32", h0=True, dh_final=True)
