@@ -594,6 +594,29 @@ def ncu_pass():
     return 0
 
 
+def ncu_large_heads():
+    """One untimed pass of the general (large-head) kernels for profiler
+    captures: a warm-up forward+backward, then the same again, of one 8192-token
+    row of the 128/128 packed workload (H 16, log-normal documents of median
+    2048, h0 and dS_final, bf16) -- a quarter of that workload, so that a
+    multi-pass capture stays small."""
+    from kimi_delta_attention_bwd_gb300 import kda_backward, kda_forward
+    from kimi_delta_attention_bwd_gb300.inputs import doc_lengths_rows
+    dev = torch.device("cuda", 0)
+    w = custom(1, 8192, 16, 128, 128, dtype="bf16", h0=True, dh_final=True)
+    lens = doc_lengths_rows(1, 8192, 2048.0, np.random.RandomState(BASE_SEED + 4))
+    inp = make_inputs(w, seed=BASE_SEED + 4, lengths=lens)
+    d = {k: (t.to(dev) if isinstance(t, torch.Tensor) else t) for k, t in inp.items()}
+    cu_host = inp["cu_seqlens"].numpy()
+    for _ in range(2):
+        o, hf, ctx = kda_forward(d["q"], d["k"], d["v"], d["f"], d["b"], d["A_log"], d["dt_bias"], scale=d["scale"],
+                                 h0=d["h0"], cu_seqlens=d["cu_seqlens"], cu_seqlens_host=cu_host)
+        kda_backward(ctx, d["dO"], d["dh_final"])
+    torch.cuda.synchronize()
+    print("ncu large-head pass done:", len(lens), "documents")
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -602,9 +625,13 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ncu-pass", action="store_true", help="one untimed pass of every kernel, for ncu captures")
+    ap.add_argument("--ncu-large-heads", action="store_true",
+                    help="one untimed pass of the large-head (128/128) kernels, for ncu captures")
     args = ap.parse_args()
     if args.ncu_pass:
         return ncu_pass()
+    if args.ncu_large_heads:
+        return ncu_large_heads()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     if args.impl == "reference":
         # rank 0 alone times the oracle; the other ranks exit without work
