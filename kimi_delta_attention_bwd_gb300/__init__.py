@@ -9,6 +9,8 @@ libkda_gb300.so through its C ABI, include/kda.h):
   qkv = kda_short_conv(qkv_raw, conv_w, cu_seqlens)            # short causal conv (k=4) + silu
   y = kda_norm_gate(o, gate, weight)                           # gated RMSNorm epilogue
   do, dgate, dweight = kda_norm_gate_backward(o, gate, weight, dy)
+  o = kda_attention(q, k, v, f, b, A_log, dt_bias)             # the same as a torch.autograd op
+  x = short_conv(x_raw, conv_w); y = gated_norm(o, gate, weight)  # likewise
 
 Layouts: q, k, f [B, T, H, dk]; v [B, T, H, dv]; b [B, T, H] (bf16 or fp32);
 A_log [H], dt_bias [H, dk] fp32 (scalar-gated variant: f [B, T, H], dt_bias [H]); optional cu_seqlens int32 [n_docs + 1] over
@@ -25,7 +27,8 @@ from . import _lib
 from ._lib import KdaError, kda_device_status, kda_strerror_text  # noqa: F401
 
 __all__ = ["kda_forward", "kda_backward", "kda_decode_step", "kda_norm_gate", "kda_norm_gate_backward",
-           "kda_short_conv", "kda_short_conv_backward", "KdaContext", "KdaError", "kda_device_status"]
+           "kda_short_conv", "kda_short_conv_backward", "KdaContext", "KdaError", "kda_device_status",
+           "kda_attention", "short_conv", "gated_norm"]
 
 
 @dataclass
@@ -199,3 +202,6 @@ def kda_short_conv_backward(x, w, dy, cu_seqlens=None, activation: str = "silu",
     dx, dw = torch.empty_like(x), torch.empty_like(w)
     _lib.kda_short_conv_bwd(n, C, x.dtype, 1 if activation == "silu" else 0, cu_seqlens, x, w, dy, dx, dw, workspace)
     return dx, dw
+
+
+from .autograd import gated_norm, kda_attention, short_conv  # noqa: E402  (differentiable forms)
