@@ -57,6 +57,19 @@ def _check(t, name, dtype=None):
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _shape(t, name, shape):
+    """Shapes are checked before anything is launched: the C ABI sees only
+    pointers, so a tensor smaller than its declared layout would be read out
+    of bounds."""
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _dims(t, name, n):
+    if t.dim() != n:
+        raise ValueError(f"{name} must have {n} dimensions, got shape {tuple(t.shape)}")
+
+
 def _gate_of(f, dt_bias, qshape):
     """Gate mode from the shapes: f with q's shape (dt_bias [H, dk]) is KDA's
     per-channel gate; f without the dk axis (dt_bias [H]) is the scalar gate."""
@@ -78,18 +91,34 @@ def kda_forward(q, k, v, f, b, A_log, dt_bias, scale: Optional[float] = None, h0
                 want_final_state: bool = True):
     """Forward pass.  Returns (o, h_final or None, ctx); ctx feeds kda_backward
     when save_for_backward is set."""
+    _dims(q, "q", 4)
+    _dims(v, "v", 4)
     B, T, H, dk = q.shape
     dv = v.shape[-1]
+    _shape(k, "k", q.shape)
+    _shape(v, "v", (B, T, H, dv))
+    _shape(b, "b", (B, T, H))
+    _shape(A_log, "A_log", (H,))
+    gate = _gate_of(f, dt_bias, (B, T, H, dk))
+    if cu_seqlens is not None:
+        _dims(cu_seqlens, "cu_seqlens", 1)
+        if cu_seqlens.numel() < 2:
+            raise ValueError("cu_seqlens must hold at least two offsets")
+    n_docs = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if h0 is not None:
+        _shape(h0, "h0", (n_docs, H, dk, dv))
+    if out is not None:
+        _shape(out, "out", (B, T, H, dv))
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (f, "f"), (b, "b")):
         _check(t, n, q.dtype)
     _check(A_log, "A_log", torch.float32)
     _check(dt_bias, "dt_bias", torch.float32)
     if cu_seqlens is not None:
         _check(cu_seqlens, "cu_seqlens", torch.int32)
-    n_docs = B if cu_seqlens is None else cu_seqlens.numel() - 1
     if h0 is not None:
         _check(h0, "h0", torch.float32)
-    gate = _gate_of(f, dt_bias, (B, T, H, dk))
+    if out is not None:
+        _check(out, "out", q.dtype)
     prob = _lib.make_problem(B, T, H, dk, dv, q.dtype, scale, cu_seqlens, cu_seqlens_host, gate)
     if workspace is None:
         workspace = _lib.alloc_workspace(prob, save_for_backward, q.device)
@@ -103,12 +132,26 @@ def kda_forward(q, k, v, f, b, A_log, dt_bias, scale: Optional[float] = None, h0
 def kda_backward(ctx: KdaContext, dO, dh_final=None, want_dh0: bool = True, grads: Optional[dict] = None):
     """Backward of sum(o * dO) + sum(h_final * dh_final).  Returns a dict with
     dq, dk, dv, df, db (io dtype), dA_log, ddt_bias, dh0 (fp32)."""
-    _check(dO, "dO", ctx.q.dtype)
-    if dh_final is not None:
-        _check(dh_final, "dh_final", torch.float32)
     q = ctx.q
     B, T, H, dk = q.shape
     dv = ctx.v.shape[-1]
+    _shape(dO, "dO", (B, T, H, dv))
+    if dh_final is not None:
+        _shape(dh_final, "dh_final", (ctx.n_docs, H, dk, dv))
+    outs = ()
+    if grads is not None:  # caller-supplied outputs: the shapes and dtypes of what they receive
+        outs = [(n, like.shape, like.dtype) for n, like in (("dq", q), ("dk", ctx.k), ("dv", ctx.v), ("df", ctx.f),
+                                                            ("db", ctx.b), ("dA_log", ctx.A_log),
+                                                            ("ddt_bias", ctx.dt_bias))]
+        if grads.get("dh0") is not None:
+            outs.append(("dh0", (ctx.n_docs, H, dk, dv), torch.float32))
+        for n, shape, _ in outs:
+            _shape(grads[n], n, shape)
+    _check(dO, "dO", q.dtype)
+    if dh_final is not None:
+        _check(dh_final, "dh_final", torch.float32)
+    for n, _, dtype in outs:
+        _check(grads[n], n, dtype)
     if grads is None:
         grads = {
             "dq": torch.empty_like(q), "dk": torch.empty_like(ctx.k), "dv": torch.empty_like(ctx.v),
@@ -129,30 +172,55 @@ def kda_decode_step(q, k, v, f, b, A_log, dt_bias, state, scale: Optional[float]
     the scalar gate), v [n, H, dv], b [n, H] (bf16 or fp32), state
     [n, H, dk, dv] fp32 updated in place.
     Returns o [n, H, dv] in the io dtype."""
+    _dims(q, "q", 3)
+    _dims(v, "v", 3)
     n, H, dk = q.shape
     dv = v.shape[-1]
+    _shape(k, "k", q.shape)
+    _shape(b, "b", (n, H))
+    _shape(A_log, "A_log", (H,))
+    _shape(state, "state", (n, H, dk, dv))
+    gate = _gate_of(f, dt_bias, (n, H, dk))
+    if out is not None:
+        _shape(out, "out", (n, H, dv))
     for t, nm in ((q, "q"), (k, "k"), (v, "v"), (f, "f"), (b, "b")):
         _check(t, nm, q.dtype)
     _check(A_log, "A_log", torch.float32)
     _check(dt_bias, "dt_bias", torch.float32)
     _check(state, "state", torch.float32)
-    if tuple(state.shape) != (n, H, dk, dv):
-        raise ValueError(f"state must be {(n, H, dk, dv)}, got {tuple(state.shape)}")
-    gate = _gate_of(f, dt_bias, (n, H, dk))
+    if out is not None:
+        _check(out, "out", q.dtype)
     o = out if out is not None else torch.empty(n, H, dv, dtype=q.dtype, device=q.device)
     _lib.kda_decode(n, H, dk, dv, q.dtype, scale, q, k, v, f, b, A_log, dt_bias, state, o, gate)
     return o
+
+
+def _norm_args(x, g, w):
+    _shape(g, "g", x.shape)
+    _shape(w, "w", (x.shape[-1],))
+    _check(x, "x")
+    _check(g, "g", x.dtype)
+    _check(w, "w", torch.float32)
+
+
+def _conv_args(x, w, cu_seqlens):
+    _shape(w, "w", (x.shape[-1], 4))
+    if cu_seqlens is not None:
+        _dims(cu_seqlens, "cu_seqlens", 1)
+    _check(x, "x")
+    _check(w, "w", torch.float32)
+    if cu_seqlens is not None:
+        _check(cu_seqlens, "cu_seqlens", torch.int32)
 
 
 def kda_norm_gate(x, g, w, eps: Optional[float] = None, out: Optional[torch.Tensor] = None):
     """Gated RMSNorm epilogue over the last axis (dv = 64 or 128):
     y = x / sqrt(mean(x^2) + eps) * w * sigmoid(g); x, g [..., dv] (bf16 or
     fp32, e.g. the KDA output [B, T, H, dv]), w [dv] fp32."""
-    _check(x, "x")
-    _check(g, "g", x.dtype)
-    _check(w, "w", torch.float32)
-    if g.shape != x.shape or tuple(w.shape) != (x.shape[-1],):
-        raise ValueError("g must match x and w must be [dv]")
+    _norm_args(x, g, w)
+    if out is not None:
+        _shape(out, "out", x.shape)
+        _check(out, "out", x.dtype)
     dv = x.shape[-1]
     y = out if out is not None else torch.empty_like(x)
     _lib.kda_norm_gate_fwd(x.numel() // dv, dv, x.dtype, eps, x, g, w, y)
@@ -161,9 +229,9 @@ def kda_norm_gate(x, g, w, eps: Optional[float] = None, out: Optional[torch.Tens
 
 def kda_norm_gate_backward(x, g, w, dy, eps: Optional[float] = None, workspace: Optional[torch.Tensor] = None):
     """Backward of kda_norm_gate: returns (dx, dg, dw)."""
+    _shape(dy, "dy", x.shape)
+    _norm_args(x, g, w)
     _check(dy, "dy", x.dtype)
-    if dy.shape != x.shape:
-        raise ValueError("dy must match x")
     dv = x.shape[-1]
     n = x.numel() // dv
     if workspace is None:
@@ -179,13 +247,11 @@ def kda_short_conv(x, w, cu_seqlens=None, activation: str = "silu", out: Optiona
     cu_seqlens document starts: x [..., C] token-major (e.g. the concatenated
     q | k | v projections [B, T, C]), w [C, 4] fp32; activation "silu" or
     "none"."""
-    _check(x, "x")
-    _check(w, "w", torch.float32)
+    _conv_args(x, w, cu_seqlens)
+    if out is not None:
+        _shape(out, "out", x.shape)
+        _check(out, "out", x.dtype)
     C = x.shape[-1]
-    if tuple(w.shape) != (C, 4):
-        raise ValueError(f"w must be {(C, 4)}")
-    if cu_seqlens is not None:
-        _check(cu_seqlens, "cu_seqlens", torch.int32)
     y = out if out is not None else torch.empty_like(x)
     _lib.kda_short_conv_fwd(x.numel() // C, C, x.dtype, 1 if activation == "silu" else 0, cu_seqlens, x, w, y)
     return y
@@ -194,6 +260,8 @@ def kda_short_conv(x, w, cu_seqlens=None, activation: str = "silu", out: Optiona
 def kda_short_conv_backward(x, w, dy, cu_seqlens=None, activation: str = "silu",
                             workspace: Optional[torch.Tensor] = None):
     """Backward of kda_short_conv: returns (dx, dw)."""
+    _shape(dy, "dy", x.shape)
+    _conv_args(x, w, cu_seqlens)
     _check(dy, "dy", x.dtype)
     C = x.shape[-1]
     n = x.numel() // C

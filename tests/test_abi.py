@@ -111,3 +111,51 @@ def test_binding_refuses_non_cuda_tensors():
     with pytest.raises(ValueError):
         kda_forward(x, x, torch.zeros(1, 4, 1, 64), x, torch.zeros(1, 4, 1), torch.zeros(1), torch.zeros(1, 32),
                     scale=None)
+
+
+def _fwd_args(B=1, T=4, H=2, dk=32, dv=64):
+    return dict(q=torch.zeros(B, T, H, dk), k=torch.zeros(B, T, H, dk), v=torch.zeros(B, T, H, dv),
+                f=torch.zeros(B, T, H, dk), b=torch.zeros(B, T, H), A_log=torch.zeros(H), dt_bias=torch.zeros(H, dk))
+
+
+@pytest.mark.parametrize("name,bad", [("k", (1, 4, 2, 16)), ("v", (1, 3, 2, 64)), ("b", (1, 4, 1)),
+                                      ("A_log", (3,)), ("dt_bias", (2, 16)), ("f", (1, 4, 2, 8)),
+                                      ("h0", (2, 2, 32, 64)), ("out", (1, 4, 2, 32))])
+def test_binding_rejects_mismatched_shapes_before_any_launch(name, bad):
+    # the C ABI sees pointers only: a tensor smaller than its layout would be read out of bounds, so the
+    # binding checks every shape first (these CPU tensors never reach the library)
+    from kimi_delta_attention_bwd_gb300 import kda_forward
+    a = _fwd_args()
+    a[name] = torch.zeros(bad)
+    with pytest.raises(ValueError, match=name):
+        kda_forward(**a)
+
+
+def test_backward_and_epilogue_bindings_reject_mismatched_shapes():
+    from kimi_delta_attention_bwd_gb300 import (KdaContext, kda_backward, kda_decode_step, kda_norm_gate,
+                                                kda_norm_gate_backward, kda_short_conv, kda_short_conv_backward)
+    a = _fwd_args()
+    ctx = KdaContext(None, a["q"], a["k"], a["v"], a["f"], a["b"], a["A_log"], a["dt_bias"], None, None, None, None, 1)
+    with pytest.raises(ValueError, match="dO"):
+        kda_backward(ctx, torch.zeros(1, 4, 2, 32))
+    with pytest.raises(ValueError, match="dh_final"):
+        kda_backward(ctx, torch.zeros(1, 4, 2, 64), torch.zeros(2, 2, 32, 64))
+    with pytest.raises(ValueError, match="dq"):
+        kda_backward(ctx, torch.zeros(1, 4, 2, 64), grads={"dq": torch.zeros(1, 4, 2, 16)})
+    d = {n: t[0] for n, t in a.items() if n not in ("A_log", "dt_bias")}  # one token of 4 sequences
+    with pytest.raises(ValueError, match="b"):
+        kda_decode_step(d["q"], d["k"], d["v"], d["f"], torch.zeros(4, 3), a["A_log"], a["dt_bias"],
+                        torch.zeros(4, 2, 32, 64))
+    with pytest.raises(ValueError, match="state"):
+        kda_decode_step(d["q"], d["k"], d["v"], d["f"], d["b"], a["A_log"], a["dt_bias"], torch.zeros(4, 2, 32, 32))
+    x = torch.zeros(10, 64)
+    with pytest.raises(ValueError, match="g"):
+        kda_norm_gate(x, torch.zeros(10, 32), torch.zeros(64))
+    with pytest.raises(ValueError, match="w"):
+        kda_norm_gate_backward(x, x, torch.zeros(32), x)
+    with pytest.raises(ValueError, match="dy"):
+        kda_norm_gate_backward(x, x, torch.zeros(64), torch.zeros(9, 64))
+    with pytest.raises(ValueError, match="w"):
+        kda_short_conv(x, torch.zeros(64, 3))
+    with pytest.raises(ValueError, match="dy"):
+        kda_short_conv_backward(x, torch.zeros(64, 4), torch.zeros(10, 32))
