@@ -50,23 +50,28 @@ def build(precision: str = "f64", force: bool = False) -> str:
     return out
 
 
+def declare(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Sets the argument and return types of the oracle's C entry points."""
+    P = ctypes.c_void_p
+    i, d = ctypes.c_int, ctypes.c_double
+    lib.kda_oracle_forward.argtypes = [i, i, i, i, P, P, P, P, P, P, P, d, d, i, P, P, i, P, P, P, P]
+    lib.kda_oracle_forward.restype = i
+    lib.kda_oracle_backward.argtypes = [i, i, i, i, P, P, P, P, P, P, P, d, d, i, P, P, P, P,
+                                        i, P, P, P, P, P, P, P, P, P]
+    lib.kda_oracle_backward.restype = i
+    lib.kda_oracle_gate.argtypes = [d, d]
+    lib.kda_oracle_gate.restype = d
+    lib.kda_oracle_sigmoid.argtypes = [d]
+    lib.kda_oracle_sigmoid.restype = d
+    lib.kda_oracle_real_bytes.restype = i
+    return lib
+
+
 def load(precision: str = "f64") -> ctypes.CDLL:
     with _lock:
         if precision in _libs:
             return _libs[precision]
-        lib = ctypes.CDLL(build(precision))
-        P = ctypes.c_void_p
-        i, d = ctypes.c_int, ctypes.c_double
-        lib.kda_oracle_forward.argtypes = [i, i, i, i, P, P, P, P, P, P, P, d, d, i, P, P, i, P, P, P, P]
-        lib.kda_oracle_forward.restype = i
-        lib.kda_oracle_backward.argtypes = [i, i, i, i, P, P, P, P, P, P, P, d, d, i, P, P, P, P,
-                                            i, P, P, P, P, P, P, P, P, P]
-        lib.kda_oracle_backward.restype = i
-        lib.kda_oracle_gate.argtypes = [d, d]
-        lib.kda_oracle_gate.restype = d
-        lib.kda_oracle_sigmoid.argtypes = [d]
-        lib.kda_oracle_sigmoid.restype = d
-        lib.kda_oracle_real_bytes.restype = i
+        lib = declare(ctypes.CDLL(build(precision)))
         _libs[precision] = lib
         return lib
 

@@ -285,6 +285,50 @@ def test_finite_differences_every_gradient():
         assert err < 1e-6, (grad, err)
 
 
+def test_finite_differences_across_checkpoint_segments():
+    """The backward rebuilds S_{t-1} from states checkpointed every 64 tokens.
+    On documents of 70 and 140 tokens (two and three checkpoint segments),
+    with an initial state and a final-state gradient, central differences at
+    entries sampled in every segment (both sides of each segment boundary)
+    match every analytic gradient.  A checkpoint restored one segment off, or
+    taken after its segment instead of before, gives the tokens of that
+    segment the wrong previous states and fails here."""
+    x = tiny([70, 140], H=2, dk=3, dv=2, seed=18, h0=True)
+    rng = np.random.RandomState(19)
+    dO = rng.randn(*x["v"].shape)
+    dhf = rng.randn(*x["h0"].shape)
+    g = oracle.backward(x, dO, dhf, threads=1)
+    hstep = 1e-6
+    # document 0: tokens 0..69 (segments [0, 64), [64, 70)); document 1: 70..209
+    # (segments [70, 134), [134, 198), [198, 210))
+    toks = [0, 31, 63, 64, 69, 70, 100, 133, 134, 170, 197, 198, 209]
+
+    def fd(inp, idx):
+        base = x[inp]
+        xp, xm = base.copy(), base.copy()
+        xp[idx] += hstep
+        xm[idx] -= hstep
+        return (loss(dict(x, **{inp: xp}), dO, dhf) - loss(dict(x, **{inp: xm}), dO, dhf)) / (2 * hstep)
+
+    cases = []
+    for inp, grad in [("q", "dq"), ("k", "dk"), ("v", "dv"), ("f", "df"), ("b", "db")]:
+        shape = x[inp].shape
+        for t in toks:
+            rest = tuple(rng.randint(0, n) for n in shape[1:])
+            cases.append((inp, grad, (t,) + rest))
+    for inp, grad in [("A_log", "dA_log"), ("dt_bias", "ddt_bias"), ("h0", "dh0")]:
+        for idx in np.ndindex(x[inp].shape):
+            cases.append((inp, grad, idx))
+    by_grad = {}
+    for inp, grad, idx in cases:
+        by_grad.setdefault(grad, []).append((fd(inp, idx), g[grad][idx]))
+    for grad, pairs in by_grad.items():
+        num = np.array([p[0] for p in pairs])
+        ana = np.array([p[1] for p in pairs])
+        err = np.abs(num - ana).max() / max(1e-12, np.abs(num).max())
+        assert err < 1e-6, (grad, err)
+
+
 def test_gradients_with_large_gates_and_no_h0():
     x = tiny([7, 3], H=1, dk=3, dv=2, seed=11, gate_scale=4.0)
     rng = np.random.RandomState(12)
