@@ -40,6 +40,8 @@ from kimi_delta_attention_bwd_gb300.inputs import BASE_SEED, WORKLOADS, custom, 
 METRIC = "KDA fwd and fwd+bwd tokens/s on 1 GB300 at 300M shape; % of roofline"
 STEP_WORKLOAD = 3   # fwd+bwd training step at the 300M layer shape
 FWD_WORKLOAD = 1    # forward only at the same shape
+VARLEN_WORKLOAD = 2  # forward of one packed row of 32768 tokens (log-normal documents)
+LARGE_WORKLOAD = 4   # fwd+bwd at dk = dv = 128, 16 heads, packed documents with states
 PROFILES = os.path.join(ROOT, "profiles")
 
 
@@ -67,12 +69,40 @@ def algorithmic_bytes(w, kernel: str) -> float:
     return float(per.get(kernel, 0)) * th
 
 
-def step_bytes(w, backward=True) -> float:
+def step_bytes(w, backward=True, n_docs=None) -> float:
+    """Algorithmic bytes of one step: every per-token input read once and
+    every output written once (forward: q, k, f, v, b in, o out; backward:
+    the same inputs and dO in, dq, dk, df, dv, db out), plus the fp32 states
+    the workload carries (h0 in and h_final out; dh_final in and dh0 out)."""
     e = 2 if w.dtype == "bf16" else 4
     th = w.B * w.T * w.H
     fwd = e * (3 * w.dk + 2 * w.dv + 1)
     bwd = e * (3 * w.dk + 2 * w.dv + 1) + e * (3 * w.dk + w.dv + 1)
-    return float(th * (fwd + (bwd if backward else 0)))
+    states = 0
+    if w.h0:
+        states += 2 * (n_docs or w.B) * w.H * w.dk * w.dv * 4
+    if backward and w.dh_final:
+        states += 2 * (n_docs or w.B) * w.H * w.dk * w.dv * 4
+    return float(th * (fwd + (bwd if backward else 0)) + states)
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the CPU baseline."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for ln in fh:
+                if ln.lower().startswith(("model name", "cpu model")):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
 
 
 # Sources of the tensor-core kernels: their translation unit with its headers,
@@ -226,6 +256,7 @@ def run_reference(args, rank, world):
             "config": {"workload": w.name, "global_batch": w.B, "seq_len": w.T, "heads": w.H, "dk": w.dk,
                        "dv": w.dv, "parallelism": "single process, host cores"},
             "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "cpu_model": cpu_model(),
                              "sample": f"each step = the full workload ({w.B}x{w.T} tokens x {w.H} heads, "
                                        "forward + backward) on the CPU oracle, threaded over (row, head)"},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -249,6 +280,7 @@ def cpu_baseline(min_seconds=10.0, max_reps=200):
             break
     el = time.perf_counter() - t0
     return {"value": reps * w.tokens / el, "unit": "tokens/s", "cores": os.cpu_count() or 1, "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": f"{reps} full workload steps ({w.B}x{w.T} tokens x {w.H} heads, fwd+bwd) in {el:.1f} s, "
                       "threaded over (row, head) units"}
 
@@ -267,13 +299,47 @@ def make_step(w, inp, dev):
                  "dA_log": torch.empty(w.H, device=dev), "ddt_bias": torch.empty(w.H, w.dk, device=dev),
                  "dh0": None}
 
+    n_docs = w.B if d.get("cu_seqlens") is None else int(d["cu_seqlens"].numel()) - 1
+    if grads is not None and w.dh_final:
+        grads["dh0"] = torch.empty(n_docs, w.H, w.dk, w.dv, device=dev)
+    hf = torch.empty(n_docs, w.H, w.dk, w.dv, device=dev) if w.h0 else None
+
     def step():
         _, _, ctx = kda_forward(d["q"], d["k"], d["v"], d["f"], d["b"], d["A_log"], d["dt_bias"],
                                 scale=d["scale"], h0=d.get("h0"), cu_seqlens=d.get("cu_seqlens"),
-                                save_for_backward=w.backward, workspace=ws, out=o, want_final_state=False)
+                                save_for_backward=w.backward, workspace=ws, out=o, want_final_state=w.h0,
+                                final_state=hf)
         if w.backward:
             kda_backward(ctx, d["dO"], d.get("dh_final"), grads=grads)
     return step, d, grads
+
+
+def workload_bench(wi, args, dev, flush, world, stream, hbm, rank):
+    """One workload's step (forward, or forward + backward) timed as launched,
+    then a second pass with per-kernel event brackets for the split and the
+    dominant kernel's roofline."""
+    from kimi_delta_attention_bwd_gb300 import _lib
+    w = WORKLOADS[wi]
+    inp = make_inputs(w, seed=BASE_SEED + wi + 1000 * rank)
+    n_docs = w.B if inp.get("cu_seqlens") is None else int(inp["cu_seqlens"].numel()) - 1
+    step, _, _ = make_step(w, inp, dev)
+    ms = max_over_ranks(time_steps(step, args.steps, args.warmup, flush, world, stream), world, dev)
+    _lib.prof_start()
+    time_steps(step, args.steps, 0, flush, world, stream)
+    prof = _lib.prof_stop()
+    del step
+    torch.cuda.empty_cache()
+    sb = step_bytes(w, w.backward, n_docs)
+    dom = max(prof, key=lambda k: prof[k][0])
+    dom_ms = prof[dom][0] / max(1, prof[dom][1])
+    ab = algorithmic_bytes(w, dom)
+    return {"value": world * w.tokens / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "workload": w.name,
+            "roofline": {"bound": "hbm", "algorithmic_bytes": sb, "achieved": sb / (ms / 1e3) / 1e9, "peak": hbm,
+                         "unit": "GB/s", "frac": sb / (ms / 1e3) / 1e9 / hbm},
+            "dominant_kernel": {"kernel": dom, "launch_ms": dom_ms, "algorithmic_bytes_per_launch": ab,
+                                "achieved": ab / (dom_ms / 1e3) / 1e9, "frac": ab / (dom_ms / 1e3) / 1e9 / hbm,
+                                "traffic": ncu_traffic(dom)},
+            "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items() if v[1]}}
 
 
 DECODE_SEQS = 2048  # concurrent sequences of the decode step (fp32 state 134 MB, larger than L2)
@@ -460,12 +526,10 @@ def run_ours(args, rank, world, local):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     hbm, tflops, peak_kind = peaks()
 
-    # forward-only number at the same shape
-    wf = WORKLOADS[FWD_WORKLOAD]
-    fstep, _, _ = make_step(wf, make_inputs(wf, seed=BASE_SEED + FWD_WORKLOAD + 1000 * rank), dev)
-    fwd_ms = max_over_ranks(time_steps(fstep, args.steps, args.warmup, flush, world, stream), world, dev)
-    del fstep
-    torch.cuda.empty_cache()
+    # forward-only at the same shape, the packed varlen forward and the large-head training step
+    fwd = workload_bench(FWD_WORKLOAD, args, dev, flush, world, stream, hbm, rank)
+    varlen = workload_bench(VARLEN_WORKLOAD, args, dev, flush, world, stream, hbm, rank)
+    large = workload_bench(LARGE_WORKLOAD, args, dev, flush, world, stream, hbm, rank)
     dec = decode_bench(args, dev, flush, world, stream, hbm, rank)
     torch.cuda.empty_cache()
     ngate = norm_gate_bench(args, dev, flush, world, stream, hbm, rank)
@@ -535,8 +599,10 @@ def run_ours(args, rank, world, local):
             "config": {"workload": w.name, "global_batch": w.B * world, "seq_len": w.T, "heads": w.H,
                        "dk": w.dk, "dv": w.dv, "parallelism": f"dp{world} (independent batches per GPU)",
                        "l2": "flushed between timed steps (512 MiB write)"},
-            "fwd": {"value": world * wf.tokens / (fwd_ms / 1e3), "unit": "tokens/s", "ms_per_step": fwd_ms,
-                    "workload": wf.name},
+            "fwd_value": fwd["value"], "fwd_roofline_frac": fwd["roofline"]["frac"],
+            "fwd": fwd,
+            "varlen_fwd": varlen,
+            "large_head_step": large,
             "decode": dec,
             "norm_gate": ngate,
             "short_conv": sconv,

@@ -17,8 +17,11 @@
  *
  * Conventions for every entry point:
  *  - All tensor pointers are DEVICE pointers owned by the caller.  The
- *    library never allocates device memory; scratch lives in the caller's
- *    workspace.  Host pointers are named *_host.
+ *    library never allocates device memory at run time; scratch lives in the
+ *    caller's workspace.  The one exception is kda_fwd_noalloc(), whose
+ *    scratch is a fixed static array (KDA_NOALLOC_SCRATCH_BYTES, 32 MiB)
+ *    reserved on every GPU that loads the library.  Host pointers are named
+ *    *_host.
  *  - Calls are asynchronous on the given stream; nothing synchronises the
  *    device except kda_device_status() and kda_prof_stop().
  *  - CUDA graphs: kda_fwd, kda_bwd, kda_decode and the norm and convolution
@@ -163,12 +166,17 @@ KDA_API const char* kda_prof_kernel_name(int i);
  *
  * The array is KDA_NOALLOC_SCRATCH_BYTES (32 MiB) of device memory, reserved
  * on every GPU that loads this library for as long as the process lives.  A
- * problem whose forward scratch (kda_workspace_size(p, 0)) exceeds it is
- * rejected with KDA_ERR_WORKSPACE before anything is launched.  With bf16 io
- * at dk=32/dv=64 the forward only needs its chunk table (about 12 bytes per
- * 64 tokens), so any realistic problem fits; the other shapes keep fp32
- * intra-chunk factors (about 56 KB per chunk and head at dk=32/dv=64 fp32,
- * i.e. roughly 600 chunk-heads).  Nothing is saved for kda_bwd.
+ * problem whose scratch does not fit is rejected with KDA_ERR_WORKSPACE
+ * before anything is launched.  The scratch is:
+ *  - bf16 io at dk=32/dv=64: the chunk table only (a single-kernel forward
+ *    carries each document's state itself), about 12 bytes per 64-token
+ *    chunk plus 4 per document -- up to about 2.8 million chunks, far more
+ *    than kda_workspace_size(p, 0), which counts the two-kernel forward's
+ *    per-chunk products, would suggest;
+ *  - every other shape or fp32 io: exactly kda_workspace_size(p, 0) (fp32
+ *    intra-chunk factors, about 56 KB per chunk and head at 32/64 fp32,
+ *    roughly 600 chunk-heads).
+ * Nothing is saved for kda_bwd.
  *
  * The first call on a device looks up the array's device address on that
  * device (the device must be current); make that first call before any
@@ -176,13 +184,24 @@ KDA_API const char* kda_prof_kernel_name(int i);
  * its contents behind (nothing in it needs to start zeroed: each call writes
  * everything it later reads).  Calls whose work overlaps on the GPU -- on
  * different streams, or from different host threads -- race on the array
- * and give wrong results: serialise them.  Arguments and statuses are those
- * of kda_fwd with save_for_backward = 0. */
+ * and give wrong results: serialise them.  Arguments and host-side statuses
+ * are those of kda_fwd with save_for_backward = 0.  Offsets that exist only
+ * on the device (cu_seqlens without cu_seqlens_host) are checked by the
+ * device; a rejection leaves o and h_final unwritten and is reported by
+ * kda_noalloc_status(), not by the return value. */
 #define KDA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 KDA_API kda_status kda_fwd_noalloc(const kda_problem* p,
                    const void* q, const void* k, const void* v, const void* f, const void* b,
                    const float* A_log, const float* dt_bias, const float* h0,
                    void* o, float* h_final, cudaStream_t stream);
+
+/* Synchronises `stream` and returns the device-side status of the last
+ * kda_fwd_noalloc() on the current device (KDA_OK, or e.g.
+ * KDA_ERR_BAD_SEQLENS for offsets that were only on the device); the error
+ * word lives in the same fixed array, so the call must follow the forward it
+ * checks before any other kda_fwd_noalloc() on that device.  Allocates
+ * nothing. */
+KDA_API kda_status kda_noalloc_status(cudaStream_t stream);
 
 /* Single-token recurrent step (decode): one token for each of n_seq
  * independent sequences, applied to their states in place.  Per sequence and

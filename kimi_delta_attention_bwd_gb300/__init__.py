@@ -88,9 +88,10 @@ def _gate_of(f, dt_bias, qshape):
 def kda_forward(q, k, v, f, b, A_log, dt_bias, scale: Optional[float] = None, h0=None,
                 cu_seqlens=None, cu_seqlens_host=None, save_for_backward: bool = True,
                 workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
-                want_final_state: bool = True):
+                want_final_state: bool = True, final_state: Optional[torch.Tensor] = None):
     """Forward pass.  Returns (o, h_final or None, ctx); ctx feeds kda_backward
-    when save_for_backward is set."""
+    when save_for_backward is set.  out / final_state: optional preallocated
+    outputs (final_state is written when want_final_state is set)."""
     _dims(q, "q", 4)
     _dims(v, "v", 4)
     B, T, H, dk = q.shape
@@ -109,6 +110,8 @@ def kda_forward(q, k, v, f, b, A_log, dt_bias, scale: Optional[float] = None, h0
         _shape(h0, "h0", (n_docs, H, dk, dv))
     if out is not None:
         _shape(out, "out", (B, T, H, dv))
+    if final_state is not None:
+        _shape(final_state, "final_state", (n_docs, H, dk, dv))
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (f, "f"), (b, "b")):
         _check(t, n, q.dtype)
     _check(A_log, "A_log", torch.float32)
@@ -119,11 +122,16 @@ def kda_forward(q, k, v, f, b, A_log, dt_bias, scale: Optional[float] = None, h0
         _check(h0, "h0", torch.float32)
     if out is not None:
         _check(out, "out", q.dtype)
+    if final_state is not None:
+        _check(final_state, "final_state", torch.float32)
     prob = _lib.make_problem(B, T, H, dk, dv, q.dtype, scale, cu_seqlens, cu_seqlens_host, gate)
     if workspace is None:
         workspace = _lib.alloc_workspace(prob, save_for_backward, q.device)
     o = out if out is not None else torch.empty(B, T, H, dv, dtype=q.dtype, device=q.device)
-    hf = torch.empty(n_docs, H, dk, dv, dtype=torch.float32, device=q.device) if want_final_state else None
+    hf = None
+    if want_final_state:
+        hf = final_state if final_state is not None else torch.empty(n_docs, H, dk, dv, dtype=torch.float32,
+                                                                     device=q.device)
     _lib.kda_fwd(prob, q, k, v, f, b, A_log, dt_bias, h0, o, hf, save_for_backward, workspace)
     ctx = KdaContext(prob, q, k, v, f, b, A_log, dt_bias, h0, cu_seqlens, cu_seqlens_host, workspace, n_docs)
     return o, hf, ctx

@@ -67,6 +67,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.kda_bwd.restype = I
         lib.kda_device_status.argtypes = [P, P]
         lib.kda_device_status.restype = I
+        lib.kda_fwd_noalloc.argtypes = [PP] + [P] * 10 + [P]
+        lib.kda_fwd_noalloc.restype = I
+        lib.kda_noalloc_status.argtypes = [P]
+        lib.kda_noalloc_status.restype = I
         lib.kda_strerror.argtypes = [I]
         lib.kda_strerror.restype = ctypes.c_char_p
         lib.kda_prof_start.restype = I

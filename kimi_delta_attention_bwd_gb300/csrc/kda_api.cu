@@ -473,3 +473,11 @@ extern "C" kda_status kda_fwd_noalloc(const kda_problem* p, const void* q, const
   FwdIO io{q, k, v, f, b, A_log, dt_bias, h0, o, h_final, 0};
   return run_forward(p, d, io, w, stream, true) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
+
+// The error word of the fixed array sits at its byte 0, like a workspace's.
+extern "C" kda_status kda_noalloc_status(cudaStream_t stream) {
+  void* scratch = nullptr;
+  const kda_status s = noalloc_scratch(&scratch);
+  if (s != KDA_OK) return s;
+  return kda_device_status(scratch, stream);
+}

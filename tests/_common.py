@@ -137,3 +137,28 @@ def compare(gpu, ref, backward: bool, rows=None, states=None, params_heads=None,
             bad[n] = (e, lim)
     assert not bad, f"parity failures {bad}; all errors {errs}"
     return errs
+
+
+def block_spans(inp, chunk=64, block=16):
+    """Decay span in nats of every 16-token block of every 64-token chunk
+    (chunks restart at each document): for channel i, minus the sum of the
+    log-decays g of the block's rows after its first, i.e. G_first - G_last
+    of the in-chunk cumulative gate.  Returns the per-block maximum over the
+    channels and heads.  The tensor-core kernels evaluate a diagonal block
+    pairwise and exactly when this exceeds 80."""
+    x = numpy_f64(inp)
+    f, dtb, A = x["f"], x["dt_bias"], x["A_log"]
+    N, H = x["q"].shape[:2]
+    if f.ndim == 2:  # scalar gate: one value per token and head
+        f = f[..., None]
+        dtb = dtb[:, None]
+    g = -np.exp(A)[None, :, None] * np.logaddexp(0.0, f + dtb[None])
+    cu = x["cu_seqlens"]
+    spans = []
+    for d in range(len(cu) - 1):
+        for c0 in range(int(cu[d]), int(cu[d + 1]), chunk):
+            c1 = min(c0 + chunk, int(cu[d + 1]))
+            for b0 in range(c0, c1, block):
+                b1 = min(b0 + block, c1)
+                spans.append(float(-g[b0 + 1:b1].sum(axis=0).min()) if b1 - b0 > 1 else 0.0)
+    return np.array(spans)

@@ -17,7 +17,7 @@ import pytest
 import torch
 
 from kimi_delta_attention_bwd_gb300.inputs import WORKLOADS, custom, make_inputs
-from _common import compare, run_gpu, run_oracle
+from _common import block_spans, compare, run_gpu, run_oracle
 
 pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -149,10 +149,8 @@ def test_head_shapes_fp32_io(dk, dv):
     _report(f"{dk}/{dv} f32", compare(gpu, ref, True, bf16=False))
 
 
-@pytest.mark.parametrize("mode", ["beta0", "beta1", "fast_decay", "no_decay"])
-def test_degenerate_gates(mode):
-    w = custom(2, 192, 2, 32, 64, dtype="f32", h0=True, dh_final=True)
-    inp = make_inputs(w, seed=13)
+def degenerate(inp, mode):
+    """Sets the gate inputs of a drawn problem to one of the hard cases."""
     if mode == "beta0":
         inp["b"].fill_(-30.0)
     elif mode == "beta1":
@@ -161,13 +159,56 @@ def test_degenerate_gates(mode):
         # per-token log-decay down to about -60: in-chunk spans far beyond fp32's exp range
         inp["A_log"].fill_(3.0)
         inp["f"].mul_(3.0).add_(1.0)
+    elif mode == "mixed_span":
+        # 16-token decay spans around the 80-nat guard: some diagonal blocks factorised,
+        # some evaluated pairwise, in the same chunks
+        inp["A_log"].fill_(2.0)
+        inp["f"].add_(2.0)
     elif mode == "no_decay":
         inp["A_log"].fill_(-30.0)
+    return inp
+
+
+def check_spans(inp, mode):
+    """The span cases must really put blocks past the 80-nat guard (so that the
+    tensor-core kernels' exact pairwise fallback runs); mixed_span must keep
+    others inside it.  Returns the widest span."""
+    sp = block_spans(inp)
+    wide = float((sp > 80.0).mean())
+    if mode == "fast_decay":
+        assert wide > 0.5, wide
+    elif mode == "mixed_span":
+        assert 0.05 < wide < 0.95, wide
+    print(f"\n[spans] {mode}: widest {sp.max():.1f} nats, {100 * wide:.0f}% of blocks past 80")
+    return float(sp.max())
+
+
+@pytest.mark.parametrize("mode", ["beta0", "beta1", "fast_decay", "mixed_span", "no_decay"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_degenerate_gates(mode, dtype):
+    """Saturated beta, extreme and absent decay, fwd+bwd against the oracle.
+    bf16 at 32/64 runs the tensor-core kernels (fwd_chunk, fwd_state,
+    bwd_scan, bwd_grad, bwd_gate); fp32 runs the general kernels."""
+    w = custom(2, 192, 2, 32, 64, dtype=dtype, h0=True, dh_final=True)
+    inp = degenerate(make_inputs(w, seed=13), mode)
+    check_spans(inp, mode)
     gpu = run_gpu(inp, True)
     for n, v in gpu.items():
         assert np.isfinite(v).all(), n
     ref = run_oracle(inp, True)
-    _report(mode, compare(gpu, ref, True, bf16=False))
+    _report(f"{mode}/{dtype}", compare(gpu, ref, True, bf16=dtype == "bf16"))
+
+
+@pytest.mark.parametrize("mode", ["fast_decay", "mixed_span"])
+def test_span_fallback_packed_documents(mode):
+    """The guarded factorisation and its exact pairwise fallback on packed
+    documents with one-token, empty and partial chunks (bf16, 32/64)."""
+    w = custom(1, 400, 3, 32, 64, dtype="bf16", h0=True, dh_final=True)
+    inp = degenerate(make_inputs(w, seed=17, lengths=[1, 0, 70, 17, 64, 1, 200, 47]), mode)
+    check_spans(inp, mode)
+    gpu = run_gpu(inp, True)
+    ref = run_oracle(inp, True)
+    _report(f"packed {mode}", compare(gpu, ref, True))
 
 
 def test_device_only_bad_offsets_flagged():
