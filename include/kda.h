@@ -108,7 +108,8 @@ typedef struct kda_problem {
 
 /* Bytes of device workspace kda_fwd / kda_bwd need for this problem
  * (for_backward = 0: forward only; 1: forward that saves for the backward,
- * and the backward).  Returns 0 for an invalid problem. */
+ * and the backward; 2: kda_fwd_norm_gate saving for kda_bwd_norm_gate, and
+ * that backward).  Returns 0 for an invalid problem. */
 KDA_API size_t kda_workspace_size(const kda_problem* p, int for_backward);
 
 /* Forward.  Writes o and, when non-NULL, h_final.  h0 may be NULL (zero
@@ -132,6 +133,55 @@ KDA_API kda_status kda_bwd(const kda_problem* p,
                    const void* q, const void* k, const void* v, const void* f, const void* b,
                    const float* A_log, const float* dt_bias, const float* h0,
                    const void* dO, const float* dh_final,
+                   void* dq, void* dk, void* dv, void* df, void* db,
+                   float* dA_log, float* ddt_bias, float* dh0,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Forward with the gated RMSNorm output epilogue fused in ("Pure KDA 300M"
+ * guide, Overview: per-head output gate and RMSNorm with eps 1e-6; openkimi
+ * README, "What is implemented": fused RMSNorm plus sigmoid gate on the KDA
+ * output).  Per token and head, over the value dim dv:
+ *   y_j = o_j r w_j sigmoid(g_j),   r = 1 / sqrt(mean_k o_k^2 + eps)
+ * where o is the KDA output of kda_fwd.  g, y : [B, T, H, dv] in dtype; w :
+ * [dv] fp32, shared by the heads; eps <= 0 selects 1e-6.  o (the pre-norm
+ * output, dtype) is written when non-NULL and may be NULL, except on the
+ * composed path below without save_for_backward (there it is the
+ * intermediate).  With save_for_backward the workspace must hold
+ * kda_workspace_size(p, 2) bytes: it keeps o in fp32 for kda_bwd_norm_gate, so
+ * that the backward does not depend on a rounding of o.  Other arguments and
+ * statuses are those of kda_fwd.
+ * bf16 io at dk=32/dv=64: the norm runs inside the state chain's output stage
+ * (the two column halves of a row exchange their sums of squares between the
+ * two CTAs of a thread-block cluster), so o need not round-trip through
+ * memory.  fp32 io, any supported (dk, dv): kda_fwd then the
+ * kda_norm_gate_fwd kernel inside the same call.  bf16 io at other head
+ * shapes: KDA_ERR_UNSUPPORTED (compose kda_fwd and kda_norm_gate_fwd). */
+KDA_API kda_status kda_fwd_norm_gate(const kda_problem* p,
+                   const void* q, const void* k, const void* v, const void* f, const void* b,
+                   const float* A_log, const float* dt_bias, const float* h0,
+                   const void* g, const float* w, float eps,
+                   void* o, void* y, float* h_final,
+                   int save_for_backward, void* workspace, size_t workspace_bytes,
+                   cudaStream_t stream);
+
+/* Backward of the loss sum(y * dy) + sum(h_final * dh_final) through the
+ * fused forward above: writes dO (the gradient of the pre-norm output o,
+ * [B, T, H, dv] in dtype; an output, also read by the later kernels of this
+ * call), dg ([B, T, H, dv] in dtype), dw ([dv] fp32, summed in a fixed order)
+ * and every output of kda_bwd.  g, w, eps are the forward's; o comes from the
+ * workspace, which must be the one kda_fwd_norm_gate(save_for_backward = 1)
+ * filled on the same inputs (kda_workspace_size(p, 2) bytes; a workspace
+ * saved by kda_fwd is refused by the device, see kda_device_status).
+ * bf16 io at dk=32/dv=64: the norm's backward runs inside the reverse state
+ * chain, which forms dO on chip for its own products.  fp32 io, other head
+ * shapes: the kda_norm_gate_bwd kernel, then the kda_bwd kernels.  bf16 io at
+ * other head shapes: KDA_ERR_UNSUPPORTED. */
+KDA_API kda_status kda_bwd_norm_gate(const kda_problem* p,
+                   const void* q, const void* k, const void* v, const void* f, const void* b,
+                   const float* A_log, const float* dt_bias, const float* h0,
+                   const void* g, const float* w, float eps,
+                   const void* dy, const float* dh_final,
+                   void* dO, void* dg, float* dw,
                    void* dq, void* dk, void* dv, void* df, void* db,
                    float* dA_log, float* ddt_bias, float* dh0,
                    void* workspace, size_t workspace_bytes, cudaStream_t stream);

@@ -8,6 +8,8 @@ libkda_gb300.so through its C ABI, include/kda.h):
   o = kda_decode_step(q, k, v, f, b, A_log, dt_bias, state)   # one token, state in place
   qkv = kda_short_conv(qkv_raw, conv_w, cu_seqlens)            # short causal conv (k=4) + silu
   y = kda_norm_gate(o, gate, weight)                           # gated RMSNorm epilogue
+  y, o, h_final, ctx = kda_forward_norm_gate(q, ..., gate, weight)  # KDA with the epilogue fused
+  grads = kda_backward_norm_gate(ctx, dy)                      # dq .. dh0, dO, dgate, dweight
   do, dgate, dweight = kda_norm_gate_backward(o, gate, weight, dy)
   o = kda_attention(q, k, v, f, b, A_log, dt_bias)             # the same as a torch.autograd op
   x = short_conv(x_raw, conv_w); y = gated_norm(o, gate, weight)  # likewise
@@ -26,7 +28,7 @@ import torch
 from . import _lib
 from ._lib import KdaError, kda_device_status, kda_strerror_text  # noqa: F401
 
-__all__ = ["kda_forward", "kda_backward", "kda_decode_step", "kda_norm_gate", "kda_norm_gate_backward",
+__all__ = ["kda_forward", "kda_backward", "kda_forward_norm_gate", "kda_backward_norm_gate", "kda_decode_step", "kda_norm_gate", "kda_norm_gate_backward",
            "kda_short_conv", "kda_short_conv_backward", "KdaContext", "KdaError", "kda_device_status",
            "kda_attention", "short_conv", "gated_norm"]
 
@@ -172,6 +174,90 @@ def kda_backward(ctx: KdaContext, dO, dh_final=None, want_dh0: bool = True, grad
                  grads["dq"], grads["dk"], grads["dv"], grads["df"], grads["db"], grads["dA_log"],
                  grads["ddt_bias"], grads.get("dh0"), ctx.workspace)
     return grads
+
+
+@dataclass
+class KdaNormContext:
+    """What kda_backward_norm_gate needs from kda_forward_norm_gate (the
+    workspace inside kda holds o in fp32)."""
+    kda: KdaContext
+    g: torch.Tensor
+    w: torch.Tensor
+    eps: float
+    saved: bool
+
+
+def kda_forward_norm_gate(q, k, v, f, b, A_log, dt_bias, g, w, eps: Optional[float] = None,
+                          scale: Optional[float] = None, h0=None, cu_seqlens=None, cu_seqlens_host=None,
+                          save_for_backward: bool = True, workspace: Optional[torch.Tensor] = None,
+                          want_final_state: bool = True, want_o: bool = False):
+    """KDA forward with the gated RMSNorm epilogue y = o r w sigmoid(g) fused in
+    (g [B, T, H, dv] in the io dtype, w [dv] fp32).  Returns (y, o or None,
+    h_final or None, ctx); o (the pre-norm output, io dtype) is returned when
+    asked for (want_o), or when it is the intermediate of the composed path
+    (head shapes other than 32/64, fp32 io, without saving)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    _shape(g, "g", (B, T, H, dv))
+    _shape(w, "w", (dv,))
+    _check(g, "g", q.dtype)
+    _check(w, "w", torch.float32)
+    _shape(k, "k", q.shape)
+    _shape(v, "v", (B, T, H, dv))
+    _shape(b, "b", (B, T, H))
+    _shape(A_log, "A_log", (H,))
+    gate = _gate_of(f, dt_bias, (B, T, H, dk))
+    n_docs = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if h0 is not None:
+        _shape(h0, "h0", (n_docs, H, dk, dv))
+        _check(h0, "h0", torch.float32)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (f, "f"), (b, "b")):
+        _check(t, n, q.dtype)
+    _check(A_log, "A_log", torch.float32)
+    _check(dt_bias, "dt_bias", torch.float32)
+    if cu_seqlens is not None:
+        _check(cu_seqlens, "cu_seqlens", torch.int32)
+    prob = _lib.make_problem(B, T, H, dk, dv, q.dtype, scale, cu_seqlens, cu_seqlens_host, gate)
+    if workspace is None:
+        workspace = _lib.alloc_workspace(prob, 2 if save_for_backward else 0, q.device)
+    y = torch.empty(B, T, H, dv, dtype=q.dtype, device=q.device)
+    composed_intermediate = not save_for_backward and not (q.dtype == torch.bfloat16 and (dk, dv) == (32, 64))
+    o = torch.empty_like(y) if (want_o or composed_intermediate) else None
+    hf = torch.empty(n_docs, H, dk, dv, dtype=torch.float32, device=q.device) if want_final_state else None
+    _lib.kda_fwd_norm_gate(prob, q, k, v, f, b, A_log, dt_bias, h0, g, w, eps, o, y, hf, save_for_backward,
+                           workspace)
+    ctx = KdaNormContext(KdaContext(prob, q, k, v, f, b, A_log, dt_bias, h0, cu_seqlens, cu_seqlens_host, workspace,
+                                    n_docs), g, w, float(eps or 0.0), bool(save_for_backward))
+    return y, o, hf, ctx
+
+
+def kda_backward_norm_gate(ctx: KdaNormContext, dy, dh_final=None, want_dh0: bool = True):
+    """Backward of sum(y * dy) + sum(h_final * dh_final) through the fused
+    epilogue.  Returns kda_backward's gradients plus dO (of the pre-norm
+    output), dg and dw."""
+    c = ctx.kda
+    q = c.q
+    B, T, H, dk = q.shape
+    dv = c.v.shape[-1]
+    if not ctx.saved:
+        raise ValueError("the forward saved nothing: call kda_forward_norm_gate with save_for_backward=True")
+    _shape(dy, "dy", (B, T, H, dv))
+    _check(dy, "dy", q.dtype)
+    if dh_final is not None:
+        _shape(dh_final, "dh_final", (c.n_docs, H, dk, dv))
+        _check(dh_final, "dh_final", torch.float32)
+    gr = {
+        "dq": torch.empty_like(q), "dk": torch.empty_like(c.k), "dv": torch.empty_like(c.v),
+        "df": torch.empty_like(c.f), "db": torch.empty_like(c.b),
+        "dA_log": torch.empty(H, dtype=torch.float32, device=q.device), "ddt_bias": torch.empty_like(c.dt_bias),
+        "dh0": torch.empty(c.n_docs, H, dk, dv, dtype=torch.float32, device=q.device) if want_dh0 else None,
+        "dO": torch.empty_like(dy), "dg": torch.empty_like(dy),
+        "dw": torch.empty(dv, dtype=torch.float32, device=q.device),
+    }
+    _lib.kda_bwd_norm_gate(c.problem, c.q, c.k, c.v, c.f, c.b, c.A_log, c.dt_bias, c.h0, ctx.g, ctx.w, ctx.eps,
+                           dy, dh_final, gr["dO"], gr["dg"], gr["dw"], gr["dq"], gr["dk"], gr["dv"], gr["df"],
+                           gr["db"], gr["dA_log"], gr["ddt_bias"], gr["dh0"], c.workspace)
+    return gr
 
 
 def kda_decode_step(q, k, v, f, b, A_log, dt_bias, state, scale: Optional[float] = None,

@@ -67,6 +67,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.kda_bwd.restype = I
         lib.kda_device_status.argtypes = [P, P]
         lib.kda_device_status.restype = I
+        F = ctypes.c_float
+        lib.kda_fwd_norm_gate.argtypes = [PP] + [P] * 10 + [F] + [P] * 3 + [I, P, SZ, P]
+        lib.kda_fwd_norm_gate.restype = I
+        lib.kda_bwd_norm_gate.argtypes = [PP] + [P] * 10 + [F] + [P] * 13 + [P, SZ, P]
+        lib.kda_bwd_norm_gate.restype = I
         lib.kda_fwd_noalloc.argtypes = [PP] + [P] * 10 + [P]
         lib.kda_fwd_noalloc.restype = I
         lib.kda_noalloc_status.argtypes = [P]
@@ -132,11 +137,14 @@ def make_problem(B, T, H, dk, dv, dtype, scale=None, cu_seqlens=None, cu_seqlens
     return p
 
 
-def kda_workspace_size(problem: kda_problem, for_backward: bool) -> int:
-    return int(load().kda_workspace_size(ctypes.byref(problem), 1 if for_backward else 0))
+def kda_workspace_size(problem: kda_problem, for_backward) -> int:
+    """for_backward: False / 0 (forward only), True / 1 (saving for kda_bwd), 2
+    (saving for kda_bwd_norm_gate)."""
+    kind = 2 if for_backward == 2 else 1 if for_backward else 0
+    return int(load().kda_workspace_size(ctypes.byref(problem), kind))
 
 
-def alloc_workspace(problem: kda_problem, for_backward: bool, device="cuda") -> torch.Tensor:
+def alloc_workspace(problem: kda_problem, for_backward, device="cuda") -> torch.Tensor:
     n = kda_workspace_size(problem, for_backward)
     if n == 0:
         raise KdaError(-1, "kda_workspace_size")
@@ -161,6 +169,29 @@ def kda_bwd(problem, q, k, v, f, b, A_log, dt_bias, h0, dO, dh_final, dq, dk, dv
                         _stream())
     if st != 0:
         raise KdaError(st, "kda_bwd")
+
+
+def kda_fwd_norm_gate(problem, q, k, v, f, b, A_log, dt_bias, h0, g, w, eps, o, y, h_final, save_for_backward,
+                      workspace):
+    """Raw forward with the fused gated RMSNorm epilogue."""
+    st = load().kda_fwd_norm_gate(ctypes.byref(problem), _p(q), _p(k), _p(v), _p(f), _p(b), _p(A_log), _p(dt_bias),
+                                  _p(h0), _p(g), _p(w), float(eps or 0.0), _p(o), _p(y), _p(h_final),
+                                  1 if save_for_backward else 0, _p(workspace),
+                                  workspace.numel() if workspace is not None else 0, _stream())
+    if st != 0:
+        raise KdaError(st, "kda_fwd_norm_gate")
+
+
+def kda_bwd_norm_gate(problem, q, k, v, f, b, A_log, dt_bias, h0, g, w, eps, dy, dh_final, dO, dg, dw,
+                      dq, dk, dv, df, db, dA_log, ddt_bias, dh0, workspace):
+    """Raw backward through the fused gated RMSNorm epilogue."""
+    st = load().kda_bwd_norm_gate(ctypes.byref(problem), _p(q), _p(k), _p(v), _p(f), _p(b), _p(A_log), _p(dt_bias),
+                                  _p(h0), _p(g), _p(w), float(eps or 0.0), _p(dy), _p(dh_final), _p(dO),
+                                  _p(dg), _p(dw), _p(dq), _p(dk), _p(dv), _p(df), _p(db), _p(dA_log), _p(ddt_bias),
+                                  _p(dh0), _p(workspace), workspace.numel() if workspace is not None else 0,
+                                  _stream())
+    if st != 0:
+        raise KdaError(st, "kda_bwd_norm_gate")
 
 
 def kda_decode(n_seq, H, dk, dv, dtype, scale, q, k, v, f, b, A_log, dt_bias, state, o, gate=KDA_GATE_CHANNEL):

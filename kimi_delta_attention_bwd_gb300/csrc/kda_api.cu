@@ -128,7 +128,7 @@ struct Layout {
   size_t off_err, off_nch, off_dc0, off_ct0, off_cl, off_cd;
   size_t off_W, off_U, off_P, off_QG, off_KD, off_gam, off_Sent, off_CH;
   size_t off_sT, off_sP, off_sW, off_sU, off_sA, off_gDP, off_gMA, off_gQG, off_gKD, off_gKG, off_gdg;
-  size_t off_dE, off_dSn, off_pA, off_pdt, off_scr;
+  size_t off_dE, off_dSn, off_pA, off_pdt, off_scr, off_nO, off_pdw, off_nrm;
 };
 
 // Workspace layout.  Both paths start with the error word, the saved-problem
@@ -169,6 +169,10 @@ static Layout layout(const Dims& d, int for_bwd, bool fused = false) {
       L.off_gKG = take(4 * nch * C * d.dk);
       L.off_gdg = take(4 * nch * d.dk);
     }
+    if (for_bwd == 2) {  // kda_fwd_norm_gate saving for kda_bwd_norm_gate
+      L.off_nO = take(4 * (size_t)d.Ntok * d.H * d.dv);
+      L.off_pdw = take(4 * (size_t)d.n_docs * d.H * d.dv);
+    }
     L.total = o;
     return L;
   }
@@ -185,6 +189,10 @@ static Layout layout(const Dims& d, int for_bwd, bool fused = false) {
     L.off_pA = take(4 * nch);
     L.off_pdt = take(4 * nch * d.dk);
     L.off_scr = take(4 * nch * (size_t)bwd_scratch_floats(d.dk, d.dv));
+  }
+  if (for_bwd == 2) {  // kda_fwd_norm_gate saving for kda_bwd_norm_gate: o, the norm kernels' partials
+    L.off_nO = take(4 * (size_t)d.Ntok * d.H * d.dv);
+    L.off_nrm = take(kda_norm_gate_workspace_size((int64_t)d.Ntok * d.H, d.dv));
   }
   L.total = o;
   return L;
@@ -229,6 +237,9 @@ static Ws bind(void* ws, const Layout& L, const Dims& d, int for_bwd) {
   w.gKD = at(L.off_gKD);
   w.gKG = at(L.off_gKG);
   w.gdg = at(L.off_gdg);
+  w.nO = at(L.off_nO);
+  w.pdw = at(L.off_pdw);
+  w.nrm = at(L.off_nrm);
   return w;
 }
 
@@ -295,6 +306,7 @@ static kda_status check_problem(const kda_problem* p, Dims* d) {
   d->fast = fast_path(p->dtype, p->dk, p->dv) ? 1 : 0;
   d->ahead = 0;
   d->gate = p->gate;
+  d->norm = 0;
   return KDA_OK;
 }
 
@@ -307,32 +319,130 @@ extern "C" {
 size_t kda_workspace_size(const kda_problem* p, int for_backward) {
   Dims d;
   if (check_problem(p, &d) != KDA_OK) return 0;
-  return layout(d, for_backward ? 1 : 0).total;
+  return layout(d, for_backward == 2 ? 2 : for_backward ? 1 : 0).total;
 }
 
 static kda_status status_of(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+}  // extern "C"
+
+namespace {
+// The gated RMSNorm epilogue's arguments of the fused entry points.
+struct NormArgs {
+  const void* g;
+  const float* w;
+  float eps;
+};
+
+kda_status fwd_impl(const kda_problem* p, const void* q, const void* k, const void* v, const void* f, const void* b,
+                    const float* A_log, const float* dt_bias, const float* h0, void* o, float* h_final,
+                    int save_for_backward, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                    const NormArgs* nm, void* y) {
+  Dims d;
+  kda_status s = check_problem(p, &d);
+  if (s != KDA_OK) return s;
+  if (nm && !d.fast && p->dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;  // bf16 needs the fused kernels
+  const int fb = save_for_backward ? (nm ? 2 : 1) : 0;
+  // o may be omitted with the norm, except as the composed path's intermediate when nothing is saved
+  const bool need_o = !nm || (!d.fast && !fb);
+  if (!q || !k || !v || !f || !b || !A_log || !dt_bias || (need_o && !o)) return KDA_ERR_INVALID_ARG;
+  if (nm && (!nm->g || !nm->w || !y)) return KDA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, f, b, A_log, dt_bias};
+  for (const void* x : ptrs)
+    if (!aligned(x, 16)) return KDA_ERR_ALIGNMENT;
+  if ((o && !aligned(o, 16)) || (h0 && !aligned(h0, 16)) || (h_final && !aligned(h_final, 16))) return KDA_ERR_ALIGNMENT;
+  if (nm && (!aligned(nm->g, 16) || !aligned(nm->w, 16) || !aligned(y, 16))) return KDA_ERR_ALIGNMENT;
+  if (!workspace) return KDA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return KDA_ERR_ALIGNMENT;
+  Layout L = layout(d, fb);
+  if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
+  Ws w = bind(workspace, L, d, fb ? 1 : 0);
+  d.save = fb ? 1 : 0;
+  if (nm) d.tag ^= 2;  // a workspace saved with the norm serves kda_bwd_norm_gate only
+  const float eps = nm && nm->eps > 0.f ? nm->eps : 1e-6f;
+  FwdIO io{q, k, v, f, b, A_log, dt_bias, h0, o, h_final, d.save, nullptr, nullptr, 0.f, nullptr};
+  if (nm && d.fast) {  // fused into the forward chain's output warps
+    d.norm = 1;
+    io.ng = nm->g;
+    io.nw = nm->w;
+    io.neps = eps;
+    io.y = y;
+  }
+  if (nm && !d.fast && fb) io.o = w.nO;  // fp32 io: the saved copy of o is the KDA output itself
+  if (run_forward(p, d, io, w, stream) != cudaSuccess) return KDA_ERR_CUDA;
+  if (nm && !d.fast) {  // other head shapes (fp32 io): the standalone epilogue kernel on o
+    const int64_t rows = (int64_t)d.Ntok * d.H;
+    s = kda_norm_gate_fwd(rows, d.dv, p->dtype, eps, io.o, nm->g, nm->w, y, stream);
+    if (s != KDA_OK) return s;
+    if (fb && o && cudaMemcpyAsync(o, w.nO, (size_t)rows * d.dv * 4, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+      return KDA_ERR_CUDA;
+  }
+  return KDA_OK;
+}
+
+kda_status bwd_impl(const kda_problem* p, const void* q, const void* k, const void* v, const void* f, const void* b,
+                    const float* A_log, const float* dt_bias, const void* dO, const float* dh_final, void* dq,
+                    void* dk, void* dv, void* df, void* db, float* dA_log, float* ddt_bias, float* dh0,
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream, const NormArgs* nm,
+                    const void* dy, void* dg, float* dw) {
+  Dims d;
+  kda_status s = check_problem(p, &d);
+  if (s != KDA_OK) return s;
+  if (nm && !d.fast && p->dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !f || !b || !A_log || !dt_bias || !dO || !dq || !dk || !dv || !df || !db ||
+      !dA_log || !ddt_bias)
+    return KDA_ERR_INVALID_ARG;
+  if (nm && (!nm->g || !nm->w || !dy || !dg || !dw)) return KDA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, f, b, A_log, dt_bias, dO, dq, dk, dv, df, db, dA_log, ddt_bias};
+  for (const void* x : ptrs)
+    if (!aligned(x, 16)) return KDA_ERR_ALIGNMENT;
+  if ((dh_final && !aligned(dh_final, 16)) || (dh0 && !aligned(dh0, 16))) return KDA_ERR_ALIGNMENT;
+  if (nm) {
+    const void* np[] = {nm->g, nm->w, dy, dg, dw};
+    for (const void* x : np)
+      if (!aligned(x, 16)) return KDA_ERR_ALIGNMENT;
+  }
+  if (!workspace) return KDA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return KDA_ERR_ALIGNMENT;
+  Layout L = layout(d, nm ? 2 : 1);
+  if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
+  Ws w = bind(workspace, L, d, 1);
+  if (nm) d.tag ^= 2;
+  const float eps = nm && nm->eps > 0.f ? nm->eps : 1e-6f;
+  BwdIO io{q, k, v, f, b, A_log, dt_bias, dO, dh_final, dq, dk, dv, df, db, dA_log, ddt_bias, dh0,
+           nullptr, nullptr, 0.f, nullptr, nullptr, nullptr, nullptr};
+  if (nm && d.fast) {  // fused into the reverse chain, which writes dO for the per-chunk kernels
+    d.norm = 1;
+    io.ng = nm->g;
+    io.nw = nm->w;
+    io.neps = eps;
+    io.dy = dy;
+    io.dOw = const_cast<void*>(dO);
+    io.dg = dg;
+    io.dw = dw;
+  }
+  if (nm && !d.fast) {  // other head shapes (fp32 io): the standalone epilogue backward writes dO first
+    const int64_t rows = (int64_t)d.Ntok * d.H;
+    s = kda_norm_gate_bwd(rows, d.dv, p->dtype, eps, w.nO, nm->g, nm->w, dy, const_cast<void*>(dO), dg, dw, w.nrm,
+                          kda_norm_gate_workspace_size(rows, d.dv), stream);
+    if (s != KDA_OK) return s;
+  }
+  if (d.fast) return status_of(launch_fast_bwd(d, io, w, stream));
+  cudaError_t e = launch_bwd_scan(p->dtype, d, io, w, stream);
+  if (e == cudaSuccess) e = launch_bwd_intra(p->dtype, d, io, w, stream);
+  if (e == cudaSuccess) e = launch_bwd_reduce(d, io, w, stream);
+  return status_of(e);
+}
+}  // namespace
+
+extern "C" {
 
 kda_status kda_fwd(const kda_problem* p, const void* q, const void* k, const void* v, const void* f,
                    const void* b, const float* A_log, const float* dt_bias, const float* h0, void* o,
                    float* h_final, int save_for_backward, void* workspace, size_t workspace_bytes,
                    cudaStream_t stream) {
-  Dims d;
-  kda_status s = check_problem(p, &d);
-  if (s != KDA_OK) return s;
-  if (!q || !k || !v || !f || !b || !A_log || !dt_bias || !o) return KDA_ERR_INVALID_ARG;
-  const void* ptrs[] = {q, k, v, f, b, A_log, dt_bias, o};
-  for (const void* x : ptrs)
-    if (!aligned(x, 16)) return KDA_ERR_ALIGNMENT;
-  if ((h0 && !aligned(h0, 16)) || (h_final && !aligned(h_final, 16))) return KDA_ERR_ALIGNMENT;
-  if (!workspace) return KDA_ERR_WORKSPACE;
-  if (!aligned(workspace, 256)) return KDA_ERR_ALIGNMENT;
-  const int fb = save_for_backward ? 1 : 0;
-  Layout L = layout(d, fb);
-  if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
-  Ws w = bind(workspace, L, d, fb);
-  d.save = fb;
-  FwdIO io{q, k, v, f, b, A_log, dt_bias, h0, o, h_final, fb};
-  return status_of(run_forward(p, d, io, w, stream));
+  return fwd_impl(p, q, k, v, f, b, A_log, dt_bias, h0, o, h_final, save_for_backward, workspace, workspace_bytes,
+                  stream, nullptr, nullptr);
 }
 
 kda_status kda_bwd(const kda_problem* p, const void* q, const void* k, const void* v, const void* f,
@@ -341,27 +451,29 @@ kda_status kda_bwd(const kda_problem* p, const void* q, const void* k, const voi
                    void* db, float* dA_log, float* ddt_bias, float* dh0, void* workspace,
                    size_t workspace_bytes, cudaStream_t stream) {
   (void)h0;  // the entry states were saved by kda_fwd
-  Dims d;
-  kda_status s = check_problem(p, &d);
-  if (s != KDA_OK) return s;
-  if (!q || !k || !v || !f || !b || !A_log || !dt_bias || !dO || !dq || !dk || !dv || !df || !db ||
-      !dA_log || !ddt_bias)
-    return KDA_ERR_INVALID_ARG;
-  const void* ptrs[] = {q, k, v, f, b, A_log, dt_bias, dO, dq, dk, dv, df, db, dA_log, ddt_bias};
-  for (const void* x : ptrs)
-    if (!aligned(x, 16)) return KDA_ERR_ALIGNMENT;
-  if ((dh_final && !aligned(dh_final, 16)) || (dh0 && !aligned(dh0, 16))) return KDA_ERR_ALIGNMENT;
-  if (!workspace) return KDA_ERR_WORKSPACE;
-  if (!aligned(workspace, 256)) return KDA_ERR_ALIGNMENT;
-  Layout L = layout(d, 1);
-  if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
-  Ws w = bind(workspace, L, d, 1);
-  BwdIO io{q, k, v, f, b, A_log, dt_bias, dO, dh_final, dq, dk, dv, df, db, dA_log, ddt_bias, dh0};
-  if (d.fast) return status_of(launch_fast_bwd(d, io, w, stream));
-  cudaError_t e = launch_bwd_scan(p->dtype, d, io, w, stream);
-  if (e == cudaSuccess) e = launch_bwd_intra(p->dtype, d, io, w, stream);
-  if (e == cudaSuccess) e = launch_bwd_reduce(d, io, w, stream);
-  return status_of(e);
+  return bwd_impl(p, q, k, v, f, b, A_log, dt_bias, dO, dh_final, dq, dk, dv, df, db, dA_log, ddt_bias, dh0,
+                  workspace, workspace_bytes, stream, nullptr, nullptr, nullptr, nullptr);
+}
+
+kda_status kda_fwd_norm_gate(const kda_problem* p, const void* q, const void* k, const void* v, const void* f,
+                             const void* b, const float* A_log, const float* dt_bias, const float* h0,
+                             const void* g, const float* w, float eps, void* o, void* y, float* h_final,
+                             int save_for_backward, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  const NormArgs nm{g, w, eps};
+  return fwd_impl(p, q, k, v, f, b, A_log, dt_bias, h0, o, h_final, save_for_backward, workspace, workspace_bytes,
+                  stream, &nm, y);
+}
+
+kda_status kda_bwd_norm_gate(const kda_problem* p, const void* q, const void* k, const void* v, const void* f,
+                             const void* b, const float* A_log, const float* dt_bias, const float* h0,
+                             const void* g, const float* w, float eps, const void* dy, const float* dh_final,
+                             void* dO, void* dg, float* dw, void* dq, void* dk, void* dv, void* df, void* db,
+                             float* dA_log, float* ddt_bias, float* dh0, void* workspace, size_t workspace_bytes,
+                             cudaStream_t stream) {
+  (void)h0;
+  const NormArgs nm{g, w, eps};
+  return bwd_impl(p, q, k, v, f, b, A_log, dt_bias, dO, dh_final, dq, dk, dv, df, db, dA_log, ddt_bias, dh0,
+                  workspace, workspace_bytes, stream, &nm, dy, dg, dw);
 }
 
 kda_status kda_device_status(const void* workspace, cudaStream_t stream) {
@@ -390,7 +502,8 @@ static const char* const k_names[K_COUNT] = {"chunk_table", "fwd_intra", "fwd_sc
                                              "bwd_intra", "bwd_reduce", "fwd_chain", "fwd_chunk",
                                              "fwd_state", "bwd_grad",  "bwd_gate",   "decode",
                                              "norm_gate_fwd", "norm_gate_bwd", "norm_gate_reduce",
-                                             "conv_fwd",  "conv_bwd",  "conv_reduce"};
+                                             "conv_fwd",  "conv_bwd",  "conv_reduce",
+                                             "fwd_state_norm", "bwd_scan_norm", "norm_dw_reduce"};
 
 const char* kda_prof_kernel_name(int i) { return (i >= 0 && i < K_COUNT) ? k_names[i] : nullptr; }
 

@@ -32,6 +32,8 @@
 #include "kda_mma.cuh"
 #include "kda_tc.cuh"
 
+#include <type_traits>
+
 namespace kda {
 namespace fast {
 using namespace mma;
@@ -1137,25 +1139,49 @@ __device__ __forceinline__ void slice_to_global(bf16* g, const bf16* s, int col0
 struct FChainStage {  // one copy of this half's part of the chain block: KU, PU, M, QW (half 0)
   __align__(16) unsigned char raw[CB_STAGE];  // or M, QW, KU, PU (half 1)
 };
+// Row partials exchanged by the two column-half CTAs of a (document, head)
+// when the gated RMSNorm is fused into a chain: the peer CTA stores its
+// partials of step s into part[s & 1] of this CTA's shared memory and arrives
+// on bar[s & 1] (one arrival per storing thread).  A CTA can run at most one
+// step ahead of its peer (each step waits for the peer's partials of that
+// step), so two slots suffice.
+struct Xchg {
+  float2 part[2][C];
+  uint64_t bar[2];
+};
 struct FChainSm {
   FChainStage st[NSTG];
   bf16 S[2][2 * DK * NSC];  // the carried state (split), double-buffered
   uint64_t bar[NSTG];       // stage completion
+  Xchg x;                   // fused norm only
 };
 static_assert(sizeof(FChainStage) % 16 == 0, "bulk-copy targets need 16-byte alignment");
 
 // fwd_state: warps 0..3 carry the state (S' = M S + KU into the other buffer
 // of the double-buffered tile), warps 4..7 write the output O = QW S + PU and
 // store the entering state, both on the step's state; one barrier per step.
+// NORM: the gated RMSNorm epilogue ("Pure KDA 300M" guide, Overview: per-head
+// output gate and RMSNorm, eps 1e-6), y = o r w sigmoid(g) with
+// r = 1 / sqrt(mean_j o_j^2 + eps) over the dv columns of a row, is fused into
+// the output warps.  A row's 64 columns are split over the two CTAs of the
+// (document, head); launched as a cluster of those two CTAs, each output warp
+// stores its rows' partial sums of o^2 into the peer's shared memory, arrives
+// on the peer's barrier and waits (bounded) for the peer's partials.  y is
+// written, o (io dtype) when io.o is set, and with io.save o in fp32 for the
+// fused backward (a bf16 copy would make its dg depend on a rounding).  A
+// CTA of a cluster never leaves before the final cluster barrier: errors skip
+// the remaining steps instead of returning.
+template <bool NORM>
 __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws w) {
   extern __shared__ __align__(16) unsigned char smraw[];
   FChainSm& sm = *reinterpret_cast<FChainSm*>(smraw);
   const int doc = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * NSC, tid = threadIdx.x, warp = tid >> 5;
   const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
   pdl_wait();  // fwd_chunk's products
-  if (*w.err != 0) return;
+  const int err0 = *w.err;
+  if (!NORM && err0 != 0) return;
   const int H = d.H;
-  const int cb = w.doc_chunk0[doc], n = w.doc_chunk0[doc + 1] - cb;
+  const int cb = w.doc_chunk0[doc], n = err0 != 0 ? 0 : w.doc_chunk0[doc + 1] - cb;
   const int64_t dh = ((int64_t)doc * H + h) * DK * DV;
   const Op S0{sm.S[0], sm.S[0] + DK * NSC, NSC}, S1{sm.S[1], sm.S[1] + DK * NSC, NSC};
   for (int idx = tid; idx < DK * NSC / 2; idx += 2 * CTH) {
@@ -1166,9 +1192,27 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
   }
   if (tid == 0) {
     for (int s2 = 0; s2 < NSTG; s2++) mbar_init(&sm.bar[s2], 1);
+    if (NORM) {
+      mbar_init(&sm.x.bar[0], 32);  // the peer's 4 output warps x 8 row-owning lanes
+      mbar_init(&sm.x.bar[1], 32);
+    }
     mbar_init_fence();
   }
   __syncthreads();  // the barriers are initialised before any thread waits on them
+  uint32_t xpart = 0, xbar = 0;  // the peer's exchange slots, mapped into the cluster window
+  float nwv[4][2];               // (output warps, NORM) the norm weight of this thread's columns
+  if constexpr (NORM) {
+    cluster_sync();  // ... and before the peer arrives on them
+    const uint32_t peer = cluster_rank() ^ 1u;
+    xpart = cluster_map(&sm.x.part[0][0], peer);
+    xbar = cluster_map(&sm.x.bar[0], peer);
+#pragma unroll
+    for (int jj = 0; jj < 4; jj++)
+#pragma unroll
+      for (int c1 = 0; c1 < 2; c1++) nwv[jj][c1] = io.nw[col0 + 8 * jj + 2 * tq + c1];
+  }
+  bool xfail = false;  // (output warps) the peer's partials did not arrive in bound
+  bool bad = false;
   // the stage of `step`: one copy, issued by a side-group thread (not on the carry warps' path)
   const int oKU = blockIdx.z ? CB_KU1 - CB_M : 0, oPU = oKU + (CB_PU0 - CB_KU0);
   const int oM = blockIdx.z ? 0 : CB_M - CB_KU0, oQW = oM + (CB_QW - CB_M);
@@ -1189,10 +1233,11 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
   for (int step = 0; step < n; step++) {
     const FChainStage& s = sm.st[step % NSTG];
     const int ci = cb + step;
-    if (__syncthreads_or(!mbar_wait(&sm.bar[step % NSTG], (step / NSTG) & 1))) {  // a stage did not arrive in bound
+    if (__syncthreads_or(!mbar_wait(&sm.bar[step % NSTG], (step / NSTG) & 1) || xfail)) {  // a wait ran out
       for (int k2 = step; k2 < n && k2 < step + NSTG - 1; k2++) mbar_wait(&sm.bar[k2 % NSTG], (k2 / NSTG) & 1);
       if (tid == 0) atomicExch(w.err, -7);
-      return;
+      bad = true;
+      break;
     }  // this step's stage and state are visible; the other state buffer is free
     prefetch(step + NSTG - 1);
     bf16* smp = reinterpret_cast<bf16*>(const_cast<unsigned char*>(s.raw) + oM);
@@ -1226,20 +1271,93 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
       gemm3<2, false, true>(oo, QWo, 16 * wq, 0, Sc, 0, 0, DK / 16);
       slice_to_global(w.sS + ((int64_t)ci * H + h) * 2 * DK * DV, Sc.hi, col0, tid - CTH);
       const float4* pup = reinterpret_cast<const float4*>(spu) + 4 * wq * 32 + lane;  // fragment order
+      if constexpr (!NORM) {
 #pragma unroll
-      for (int jj = 0; jj < 4; jj++) {
-        const float4 p4 = pup[32 * jj];
-        const int r = 16 * wq + gq, c = 8 * jj + 2 * tq;
-        if (r < L)
-          *reinterpret_cast<__nv_bfloat162*>(o + ((size_t)(t0 + r) * H + h) * DV + col0 + c) =
-              __floats2bfloat162_rn(oo[jj][0] + p4.x, oo[jj][1] + p4.y);
-        if (r + 8 < L)
-          *reinterpret_cast<__nv_bfloat162*>(o + ((size_t)(t0 + r + 8) * H + h) * DV + col0 + c) =
-              __floats2bfloat162_rn(oo[jj][2] + p4.z, oo[jj][3] + p4.w);
+        for (int jj = 0; jj < 4; jj++) {
+          const float4 p4 = pup[32 * jj];
+          const int r = 16 * wq + gq, c = 8 * jj + 2 * tq;
+          if (r < L)
+            *reinterpret_cast<__nv_bfloat162*>(o + ((size_t)(t0 + r) * H + h) * DV + col0 + c) =
+                __floats2bfloat162_rn(oo[jj][0] + p4.x, oo[jj][1] + p4.y);
+          if (r + 8 < L)
+            *reinterpret_cast<__nv_bfloat162*>(o + ((size_t)(t0 + r + 8) * H + h) * DV + col0 + c) =
+                __floats2bfloat162_rn(oo[jj][2] + p4.z, oo[jj][3] + p4.w);
+        }
+      } else {
+        // o of rows r = 16 wq + gq and r + 8 (columns 8 jj + 2 tq + {0, 1}); rows past the
+        // chunk end are zero (their QW and PU rows are)
+        const int r = 16 * wq + gq, slot = step & 1;
+        const bf16* gp = (const bf16*)io.ng;
+        float gv[4][4];
+#pragma unroll
+        for (int jj = 0; jj < 4; jj++) {
+          const float4 p4 = pup[32 * jj];
+          oo[jj][0] += p4.x;
+          oo[jj][1] += p4.y;
+          oo[jj][2] += p4.z;
+          oo[jj][3] += p4.w;
+          const int c = col0 + 8 * jj + 2 * tq;
+          const float2 g0 = r < L ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(
+                                        gp + ((size_t)(t0 + r) * H + h) * DV + c))
+                                  : make_float2(0.f, 0.f);
+          const float2 g1 = r + 8 < L ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(
+                                            gp + ((size_t)(t0 + r + 8) * H + h) * DV + c))
+                                      : make_float2(0.f, 0.f);
+          gv[jj][0] = g0.x;
+          gv[jj][1] = g0.y;
+          gv[jj][2] = g1.x;
+          gv[jj][3] = g1.y;
+        }
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 4; jj++) {
+          s0 += oo[jj][0] * oo[jj][0] + oo[jj][1] * oo[jj][1];
+          s1 += oo[jj][2] * oo[jj][2] + oo[jj][3] * oo[jj][3];
+        }
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+        if (tq == 0) {  // rows r and r + 8 into the peer's slot, then one arrival
+          st_cluster_f32x2(xpart + (uint32_t)((slot * C + r) * 8), s0, 0.f);
+          st_cluster_f32x2(xpart + (uint32_t)((slot * C + r + 8) * 8), s1, 0.f);
+          mbar_arrive_remote(xbar + (uint32_t)(slot * 8));
+        }
+        if (!mbar_wait_cluster(&sm.x.bar[slot], (step >> 1) & 1)) {
+          xfail = true;  // bails at the next step's barrier (or skips the end state)
+        } else {
+          const float t0s = s0 + sm.x.part[slot][r].x, t1s = s1 + sm.x.part[slot][r + 8].x;
+          const float r0 = 1.0f / sqrtf(t0s * (1.0f / DV) + io.neps), r1 = 1.0f / sqrtf(t1s * (1.0f / DV) + io.neps);
+          bf16* yp = (bf16*)io.y;
+#pragma unroll
+          for (int jj = 0; jj < 4; jj++) {
+            const int c = col0 + 8 * jj + 2 * tq;
+            if (r < L) {
+              const size_t i = ((size_t)(t0 + r) * H + h) * DV + c;
+              *reinterpret_cast<__nv_bfloat162*>(yp + i) =
+                  __floats2bfloat162_rn(oo[jj][0] * r0 * nwv[jj][0] * sigmoid_fast(gv[jj][0]),
+                                        oo[jj][1] * r0 * nwv[jj][1] * sigmoid_fast(gv[jj][1]));
+              if (o) *reinterpret_cast<__nv_bfloat162*>(o + i) = __floats2bfloat162_rn(oo[jj][0], oo[jj][1]);
+              if (io.save) *reinterpret_cast<float2*>(w.nO + i) = make_float2(oo[jj][0], oo[jj][1]);
+            }
+            if (r + 8 < L) {
+              const size_t i = ((size_t)(t0 + r + 8) * H + h) * DV + c;
+              *reinterpret_cast<__nv_bfloat162*>(yp + i) =
+                  __floats2bfloat162_rn(oo[jj][2] * r1 * nwv[jj][0] * sigmoid_fast(gv[jj][2]),
+                                        oo[jj][3] * r1 * nwv[jj][1] * sigmoid_fast(gv[jj][3]));
+              if (o) *reinterpret_cast<__nv_bfloat162*>(o + i) = __floats2bfloat162_rn(oo[jj][2], oo[jj][3]);
+              if (io.save) *reinterpret_cast<float2*>(w.nO + i) = make_float2(oo[jj][2], oo[jj][3]);
+            }
+          }
+        }
       }
     }
   }
-  if (io.h_final) {
+  if (NORM && __syncthreads_or(xfail) && !bad) {  // the last step's exchange ran out
+    if (tid == 0) atomicExch(w.err, -7);
+    bad = true;
+  }
+  if (io.h_final && !bad && err0 == 0) {
     if (n > 0) {
       if (carry)
 #pragma unroll
@@ -1257,6 +1375,7 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
       }
     }
   }
+  if constexpr (NORM) cluster_sync();  // the peer no longer touches this CTA's shared memory
 }
 
 struct BChainStage {
@@ -1264,23 +1383,48 @@ struct BChainStage {
   bf16 QW[2 * C * DK];  // QW (split)
   bf16 dO[C * NSC];     // columns col0.. of dO (exact bf16, operand layout)
 };
+// With the fused gated-norm backward the stage also holds this CTA's columns
+// of dy, g (bf16) and of the forward's fp32 o, row-major ([C][NSC]), from
+// which the chain forms dO.
+struct BChainStageN : BChainStage {
+  bf16 dy[C * NSC], g[C * NSC];
+  float o[C * NSC];
+};
+template <bool NORM>
 struct BChainSm {
-  BChainStage st[NSTG];
+  typename std::conditional<NORM, BChainStageN, BChainStage>::type st[NSTG];
   bf16 dS[2 * DK * NSC];  // the carried state gradient (split)
   uint64_t bar[NSTG];     // completion of the stage's M and QW
+  Xchg x;                 // fused norm only
 };
-static_assert(sizeof(BChainStage) % 16 == 0 && offsetof(BChainStage, QW) == 4 * DK * DK && offsetof(BChainStage, dO) == CB_KU1 - CB_M,
+static_assert(sizeof(BChainStage) % 16 == 0 && sizeof(BChainStageN) % 16 == 0 &&
+                  offsetof(BChainStage, QW) == 4 * DK * DK && offsetof(BChainStage, dO) == CB_KU1 - CB_M,
               "M | QW arrive in one copy");
 
+// bwd_scan: the reverse chain dS = M^T dS' + QW^T dO, one CTA of four warps
+// per (document, head, 32 value columns).
+// NORM: the gated RMSNorm's backward is fused in front of the chain's dO (o is
+// the forward's fp32 copy in the workspace).  With
+// y = o r w s (s = sigmoid(g), r = 1 / sqrt(mean_j o_j^2 + eps)) and dy given,
+//   dO_j = r a_j - o_j r^3 (sum_k a_k o_k) / dv,   a_j = dy_j w_j s_j
+//   dg_j = dy_j o_j r w_j s_j (1 - s_j),           dw_j = sum over rows of dy_j o_j r s_j
+// (the chain rule through the norm).  The two row sums (of o^2 and of a o) need
+// all dv columns: the two column-half CTAs of a (document, head) run as a
+// cluster and exchange their partials through distributed shared memory, the
+// exchange overlapping the step's M^T dS product.  dO (bf16, also written for
+// the per-chunk kernels) replaces the loaded dO tile; dg is written; the dw
+// partials are summed over the (document, head)'s rows in a fixed order.
+template <bool NORM>
 __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
   extern __shared__ __align__(16) unsigned char smraw[];
-  BChainSm& sm = *reinterpret_cast<BChainSm*>(smraw);
+  BChainSm<NORM>& sm = *reinterpret_cast<BChainSm<NORM>*>(smraw);
   const int doc = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * NSC, tid = threadIdx.x, warp = tid >> 5;
   const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
   pdl_release();  // bwd_grad may launch: it waits for this grid before reading dS
-  if (!saved_ok(d, w.tag, w.err)) return;
+  const bool ok0 = saved_ok(d, w.tag, w.err);
+  if (!NORM && !ok0) return;
   const int H = d.H;
-  const int cb = w.doc_chunk0[doc], ce = w.doc_chunk0[doc + 1], n = ce - cb;
+  const int cb = w.doc_chunk0[doc], ce = w.doc_chunk0[doc + 1], n = ok0 ? ce - cb : 0;
   const int64_t dh = ((int64_t)doc * H + h) * DK * DV;
   const Op dS{sm.dS, sm.dS + DK * NSC, NSC};
   for (int idx = tid; idx < DK * NSC / 2; idx += CTH) {
@@ -1292,24 +1436,59 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
   const bf16* dOg = (const bf16*)io.dO;
   if (tid == 0) {
     for (int s2 = 0; s2 < NSTG; s2++) mbar_init(&sm.bar[s2], 1);
+    if (NORM) {
+      mbar_init(&sm.x.bar[0], C);  // one arrival per row from the peer
+      mbar_init(&sm.x.bar[1], C);
+    }
     mbar_init_fence();
   }
   __syncthreads();  // the barriers are initialised before any thread waits on them
+  // (NORM) thread t owns row t / 2, columns 16 (t % 2) .. of the CTA's 32
+  const int nr = tid >> 1, nh = tid & 1;
+  uint32_t xpart = 0, xbar = 0;
+  float nwv[16], dwacc[16];
+  if constexpr (NORM) {
+    cluster_sync();  // ... and before the peer arrives on them
+    const uint32_t peer = cluster_rank() ^ 1u;
+    xpart = cluster_map(&sm.x.part[0][0], peer);
+    xbar = cluster_map(&sm.x.bar[0], peer);
+#pragma unroll
+    for (int j = 0; j < 16; j++) {
+      nwv[j] = io.nw[col0 + 16 * nh + j];
+      dwacc[j] = 0.f;
+    }
+  }
   auto prefetch = [&](int step) {  // always commits a cp.async group (empty past the end)
     if (step < n) {
       const int slot = step % NSTG;
-      BChainStage& s = sm.st[slot];
+      auto& s = sm.st[slot];
       const int ci = ce - 1 - step, L = w.chunk_len[ci], t0 = w.chunk_tok0[ci];
       const int64_t ch = (int64_t)ci * H + h;
       if (tid == 0) {  // M | QW, adjacent in the chain block and in the stage
         mbar_expect_tx(&sm.bar[slot], CB_KU1 - CB_M);
         bulk_g2s(s.M, chblk(w, ch) + CB_M, CB_KU1 - CB_M, &sm.bar[slot]);
       }
-      for (int idx = tid; idx < C * NSC / 8; idx += CTH) {
-        const int r = idx / (NSC / 8), p = idx % (NSC / 8);
-        bf16* dst = s.dO + opix(r, 8 * p, NSC);
-        if (r < L) cp16(dst, dOg + ((size_t)(t0 + r) * H + h) * DV + col0 + 8 * p);
-        else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (!NORM) {
+        for (int idx = tid; idx < C * NSC / 8; idx += CTH) {
+          const int r = idx / (NSC / 8), p = idx % (NSC / 8);
+          bf16* dst = s.dO + opix(r, 8 * p, NSC);
+          if (r < L) cp16(dst, dOg + ((size_t)(t0 + r) * H + h) * DV + col0 + 8 * p);
+          else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      } else {  // dy, g (bf16) and o (fp32) rows of this CTA's columns, zero past the chunk end
+        for (int idx = tid; idx < 2 * C * NSC / 8; idx += CTH) {
+          const int t2 = idx / (C * NSC / 8), rem = idx % (C * NSC / 8), r = rem / (NSC / 8), p = rem % (NSC / 8);
+          bf16* dst = (t2 == 0 ? s.dy : s.g) + r * NSC + 8 * p;
+          const bf16* src = (const bf16*)(t2 == 0 ? io.dy : io.ng);
+          if (r < L) cp16(dst, src + ((size_t)(t0 + r) * H + h) * DV + col0 + 8 * p);
+          else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        for (int idx = tid; idx < C * NSC / 4; idx += CTH) {
+          const int r = idx / (NSC / 4), p = idx % (NSC / 4);
+          float* dst = s.o + r * NSC + 4 * p;
+          if (r < L) cp16(dst, w.nO + ((size_t)(t0 + r) * H + h) * DV + col0 + 4 * p);
+          else *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
     }
     cp_commit();
@@ -1318,15 +1497,17 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
   float acc[2][4];  // this warp's tile of the carried gradient: rows 16 (warp & 1) .., columns 16 (warp >> 1) ..
   zero(acc);
   const int mI = warp & 1, jn = warp >> 1;
+  bool xfail = false, bad = false;
   for (int step = 0; step < n; step++) {
-    const BChainStage& s = sm.st[step % NSTG];
+    auto& s = sm.st[step % NSTG];
     const int ci = ce - 1 - step;
     asm volatile("cp.async.wait_group %0;\n" ::"n"(NSTG - 2));
-    if (__syncthreads_or(!mbar_wait(&sm.bar[step % NSTG], (step / NSTG) & 1))) {  // a stage did not arrive in bound
+    if (__syncthreads_or(!mbar_wait(&sm.bar[step % NSTG], (step / NSTG) & 1) || xfail)) {  // a wait ran out
       for (int k2 = step; k2 < n && k2 < step + NSTG - 1; k2++) mbar_wait(&sm.bar[k2 % NSTG], (k2 / NSTG) & 1);
       cp_wait_all();
       if (tid == 0) atomicExch(w.err, -7);
-      return;
+      bad = true;
+      break;
     }  // this step's stage and the last state update are visible
     prefetch(step + NSTG - 1);
     const Op Mo{const_cast<bf16*>(s.M), const_cast<bf16*>(s.M) + DK * DK, DK};
@@ -1335,14 +1516,93 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
     float ax[2][4];
     zero(acc);
     zero(ax);
-    gemm3<1, true, true>(ax, QWo, 16 * mI, 0, dOo, 16 * jn, 0, C / 16);
-    gemm3<1, true, true>(acc, Mo, 16 * mI, 0, dS, 16 * jn, 0, DK / 16);
-    slice_to_global(w.sdS + ((int64_t)ci * H + h) * 2 * DK * DV, sm.dS, col0, threadIdx.x);
+    if constexpr (!NORM) {
+      gemm3<1, true, true>(ax, QWo, 16 * mI, 0, dOo, 16 * jn, 0, C / 16);
+      gemm3<1, true, true>(acc, Mo, 16 * mI, 0, dS, 16 * jn, 0, DK / 16);
+      slice_to_global(w.sdS + ((int64_t)ci * H + h) * 2 * DK * DV, sm.dS, col0, threadIdx.x);
 #pragma unroll
-    for (int jj = 0; jj < 2; jj++)
+      for (int jj = 0; jj < 2; jj++)
 #pragma unroll
-      for (int e = 0; e < 4; e++) acc[jj][e] += ax[jj][e];
-    __syncthreads();  // every read of the state tile is done
+        for (int e = 0; e < 4; e++) acc[jj][e] += ax[jj][e];
+      __syncthreads();  // every read of the state tile is done
+    } else {
+      const int slot = step & 1, L = w.chunk_len[ci], t0 = w.chunk_tok0[ci];
+      float dyv[16], ov[16], gv[16];
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++) {
+        const int o8 = nr * NSC + 16 * nh + 8 * hh;
+        unpack8(*reinterpret_cast<const uint4*>(s.dy + o8), dyv + 8 * hh);
+        unpack8(*reinterpret_cast<const uint4*>(s.g + o8), gv + 8 * hh);
+        const float4 a = *reinterpret_cast<const float4*>(s.o + o8), b = *reinterpret_cast<const float4*>(s.o + o8 + 4);
+        ov[8 * hh] = a.x; ov[8 * hh + 1] = a.y; ov[8 * hh + 2] = a.z; ov[8 * hh + 3] = a.w;
+        ov[8 * hh + 4] = b.x; ov[8 * hh + 5] = b.y; ov[8 * hh + 6] = b.z; ov[8 * hh + 7] = b.w;
+      }
+      float po = 0.f, pa = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; j++) {
+        gv[j] = sigmoid_fast(gv[j]);           // s_j
+        const float a = dyv[j] * nwv[j] * gv[j];  // a_j
+        po += ov[j] * ov[j];
+        pa += a * ov[j];
+      }
+      po += __shfl_xor_sync(0xffffffffu, po, 1);
+      pa += __shfl_xor_sync(0xffffffffu, pa, 1);
+      if (nh == 0) {
+        st_cluster_f32x2(xpart + (uint32_t)((slot * C + nr) * 8), po, pa);
+        mbar_arrive_remote(xbar + (uint32_t)(slot * 8));
+      }
+      gemm3<1, true, true>(acc, Mo, 16 * mI, 0, dS, 16 * jn, 0, DK / 16);  // overlaps the exchange
+      slice_to_global(w.sdS + ((int64_t)ci * H + h) * 2 * DK * DV, sm.dS, col0, threadIdx.x);
+      float dOv[16];
+      if (!mbar_wait_cluster(&sm.x.bar[slot], (step >> 1) & 1)) {
+        xfail = true;  // bails at the next step's barrier
+#pragma unroll
+        for (int j = 0; j < 16; j++) dOv[j] = 0.f;
+      } else {
+        const float2 pp = sm.x.part[slot][nr];
+        const float To = po + pp.x, Ta = pa + pp.y;
+        const float rr = 1.0f / sqrtf(To * (1.0f / DV) + io.neps);
+        const float cc = rr * rr * rr * Ta * (1.0f / DV);
+        float dgv[16];
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+          const float sg = gv[j], or_ = ov[j] * rr;
+          dOv[j] = rr * dyv[j] * nwv[j] * sg - ov[j] * cc;
+          dgv[j] = dyv[j] * or_ * nwv[j] * sg * (1.f - sg);
+          dwacc[j] += dyv[j] * or_ * sg;
+        }
+        if (nr < L) {
+          const size_t gi = ((size_t)(t0 + nr) * H + h) * DV + col0 + 16 * nh;
+#pragma unroll
+          for (int hh = 0; hh < 2; hh++) {
+            uint4 ud, ug;
+            __nv_bfloat162* d2 = reinterpret_cast<__nv_bfloat162*>(&ud);
+            __nv_bfloat162* g2 = reinterpret_cast<__nv_bfloat162*>(&ug);
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+              d2[e] = __floats2bfloat162_rn(dOv[8 * hh + 2 * e], dOv[8 * hh + 2 * e + 1]);
+              g2[e] = __floats2bfloat162_rn(dgv[8 * hh + 2 * e], dgv[8 * hh + 2 * e + 1]);
+            }
+            *reinterpret_cast<uint4*>((bf16*)io.dOw + gi + 8 * hh) = ud;
+            *reinterpret_cast<uint4*>((bf16*)io.dg + gi + 8 * hh) = ug;
+          }
+        }
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++) {  // the dO operand tile (bf16, as stored for the per-chunk kernels)
+        uint4 u;
+        __nv_bfloat162* u2 = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; e++) u2[e] = __floats2bfloat162_rn(dOv[8 * hh + 2 * e], dOv[8 * hh + 2 * e + 1]);
+        *reinterpret_cast<uint4*>(const_cast<bf16*>(s.dO) + opix(nr, 16 * nh + 8 * hh, NSC)) = u;
+      }
+      __syncthreads();  // the dO tile is complete; every read of the state tile is done
+      gemm3<1, true, true>(ax, QWo, 16 * mI, 0, dOo, 16 * jn, 0, C / 16);
+#pragma unroll
+      for (int jj = 0; jj < 2; jj++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) acc[jj][e] += ax[jj][e];
+    }
 #pragma unroll
     for (int jj = 0; jj < 2; jj++)
 #pragma unroll
@@ -1350,7 +1610,11 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
         op_store2(dS, 16 * mI + gq + 8 * hh, 16 * jn + 8 * jj + 2 * tq, acc[jj][2 * hh], acc[jj][2 * hh + 1]);
   }
   cp_wait_all();
-  if (io.dh0) {
+  if (NORM && __syncthreads_or(xfail) && !bad) {  // the last step's exchange ran out
+    if (tid == 0) atomicExch(w.err, -7);
+    bad = true;
+  }
+  if (io.dh0 && !bad && ok0) {
     if (n > 0) {
 #pragma unroll
       for (int jj = 0; jj < 2; jj++)
@@ -1365,6 +1629,22 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
         io.dh0[dh + i * DV + col0 + jc] = io.dh_final ? io.dh_final[dh + i * DV + col0 + jc] : 0.f;
       }
     }
+  }
+  if constexpr (NORM) {
+    // dw partial of this (document, head): column sums over the 64 row-owning
+    // threads of each half, in a fixed order, through the (now idle) stages
+    float* red = reinterpret_cast<float*>(&sm.st[0]);  // [CTH][16]
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 16; j++) red[tid * 16 + j] = dwacc[j];
+    __syncthreads();
+    if (tid < NSC && !bad && ok0) {
+      const int hf = tid >> 4, j = tid & 15;
+      float a = 0.f;
+      for (int r = 0; r < C; r++) a += red[(2 * r + hf) * 16 + j];
+      w.pdw[((int64_t)doc * H + h) * DV + col0 + tid] = a;
+    }
+    cluster_sync();  // the peer no longer touches this CTA's shared memory
   }
 }
 
@@ -1472,6 +1752,7 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
     }
   }
   cp_commit();
+  if (d.norm) pdl_wait();  // dO is then written by the fused-norm bwd_scan, the kernel before
   for (int idx = tid; idx < C * 8; idx += NTH) {
     const int r = idx >> 3, p = idx & 7;
     bf16* dst = wk + opix(r, 8 * p, DV);
@@ -2217,6 +2498,7 @@ static_assert(sizeof(fast::FwdSm) <= 232448, "fused forward shared memory exceed
 static_assert(sizeof(fast::ChunkSm) <= 113 * 1024, "per-chunk forward must fit two CTAs per SM");
 
 static_assert(sizeof(fast::GradSm) <= 112 * 1024, "chunk-gradient kernel must fit two CTAs per SM");
+static_assert(sizeof(fast::BChainSm<true>) <= 113 * 1024, "fused-norm reverse chain must fit two CTAs per SM");
 static_assert(sizeof(fast::GateSm) <= 75 * 1024, "gate kernel must fit three CTAs per SM");
 
 bool fast_path(int dtype, int dk, int dv) { return dtype == 0 && dk == fast::DK && dv == fast::DV; }
@@ -2250,34 +2532,53 @@ cudaError_t launch_fast_fwd(const Dims& d0, const FwdIO& io, const Ws& w, cudaSt
   const size_t s1 = sizeof(fast::ChunkSm), s2 = sizeof(fast::FChainSm);
   e = cudaFuncSetAttribute(fast::fwd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(fast::fwd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
+    e = cudaFuncSetAttribute(fast::fwd_state_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fast::fwd_state_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
   if (e != cudaSuccess) return e;
   prof_begin(K_FWD_CHUNK, st);
   e = launch_pdl(fast::fwd_chunk_kernel, dim3(d.nc_max * d.H), dim3(fast::NTH), s1, st, d, io, w);
   prof_end(K_FWD_CHUNK, st);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  prof_begin(K_FWD_STATE, st);
-  e = launch_pdl(fast::fwd_state_kernel, dim3(d.n_docs, d.H, fast::DV / fast::NSC), dim3(2 * fast::CTH), s2, st, d,
-                 io, w);
-  prof_end(K_FWD_STATE, st);
+  const dim3 grid(d.n_docs, d.H, fast::DV / fast::NSC);
+  if (d.norm) {  // the two column halves of a (document, head) as one cluster
+    prof_begin(K_FWD_STATE_NORM, st);
+    e = launch_cluster(fast::fwd_state_kernel<true>, grid, dim3(2 * fast::CTH), s2, st, 2, true, d, io, w);
+    prof_end(K_FWD_STATE_NORM, st);
+  } else {
+    prof_begin(K_FWD_STATE, st);
+    e = launch_pdl(fast::fwd_state_kernel<false>, grid, dim3(2 * fast::CTH), s2, st, d, io, w);
+    prof_end(K_FWD_STATE, st);
+  }
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_fast_bwd(const Dims& d0, const BwdIO& io, const Ws& w, cudaStream_t st) {
   Dims d = d0;
   d.ahead = 0;  // the backward's chunk kernels prefetch nothing (measured: the L2 prefetch of the next wave slowed them)
-  const size_t sc = sizeof(fast::BChainSm), s1 = sizeof(fast::GradSm), s2 = sizeof(fast::GateSm);
-  cudaError_t e = cudaFuncSetAttribute(fast::bwd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
+  const size_t sc = sizeof(fast::BChainSm<false>), scn = sizeof(fast::BChainSm<true>), s1 = sizeof(fast::GradSm),
+               s2 = sizeof(fast::GateSm);
+  cudaError_t e =
+      cudaFuncSetAttribute(fast::bwd_scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fast::bwd_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scn);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(fast::bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(fast::bwd_gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
   if (e != cudaSuccess) return e;
-  prof_begin(K_BWD_SCAN, st);
-  fast::bwd_scan_kernel<<<dim3(d.n_docs, d.H, fast::DV / fast::NSC), fast::CTH, sc, st>>>(d, io, w);
-  prof_end(K_BWD_SCAN, st);
-  e = cudaGetLastError();
+  const dim3 grid(d.n_docs, d.H, fast::DV / fast::NSC);
+  if (d.norm) {  // the two column halves of a (document, head) as one cluster
+    prof_begin(K_BWD_SCAN_NORM, st);
+    e = launch_cluster(fast::bwd_scan_kernel<true>, grid, dim3(fast::CTH), scn, st, 2, false, d, io, w);
+    prof_end(K_BWD_SCAN_NORM, st);
+  } else {
+    prof_begin(K_BWD_SCAN, st);
+    fast::bwd_scan_kernel<false><<<grid, fast::CTH, sc, st>>>(d, io, w);
+    prof_end(K_BWD_SCAN, st);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) return e;
   prof_begin(K_BWD_GRAD, st);
   e = launch_pdl(fast::bwd_grad_kernel, dim3(d.nc_max * d.H), dim3(fast::NTH), s1, st, d, io, w);
@@ -2289,7 +2590,12 @@ cudaError_t launch_fast_bwd(const Dims& d0, const BwdIO& io, const Ws& w, cudaSt
   prof_end(K_BWD_GATE, st);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_bwd_reduce(d, io, w, st);
+  e = launch_bwd_reduce(d, io, w, st);
+  if (e != cudaSuccess || !d.norm) return e;
+  prof_begin(K_NORM_DW, st);  // dw: the (document, head) partials summed in a fixed order
+  e = launch_sum_rows(w.pdw, d.n_docs * d.H, fast::DV, io.dw, st);
+  prof_end(K_NORM_DW, st);
+  return e;
 }
 
 }  // namespace kda

@@ -31,6 +31,9 @@ enum KernelId {
   K_CONV_FWD,
   K_CONV_BWD,
   K_CONV_RED,
+  K_FWD_STATE_NORM,
+  K_BWD_SCAN_NORM,
+  K_NORM_DW,
   K_COUNT
 };
 
@@ -71,6 +74,10 @@ struct Ws {
   float* dSn;  // [ch][dk][dv] gradient of the state leaving the chunk
   float* pA;   // [ch]         per chunk-head partial of dA_log
   float* pdt;  // [ch][dk]     per chunk-head partial of ddt_bias
+  // saved by kda_fwd_norm_gate for kda_bwd_norm_gate (workspace for_backward = 2)
+  float* nO;   // [Ntok][H][dv] the pre-norm KDA output o in fp32
+  float* pdw;  // [n_docs * H][dv] per (document, head) partial of the gated norm's dw (fused backward)
+  float* nrm;  // other head shapes: the standalone norm backward's per-CTA dw partials
   float* scr;  // [ch][scr_per_ch] backward scratch
   int64_t scr_per_ch;
 };
@@ -83,6 +90,7 @@ struct Dims {
   int32_t fast;  // bf16 io with dk = 32, dv = 64: tensor-core kernels
   int32_t ahead; // CTAs in flight (one wave) of the per-chunk tensor-core kernels: their L2 prefetch distance
   int32_t gate;  // 0: per key channel (KDA); 1: scalar per head (GDN), f [Ntok, H], dt_bias [H]
+  int32_t norm;  // the gated RMSNorm epilogue is fused into the chains (tensor-core path)
 };
 
 // Backward kernels refuse a workspace that no saving forward of the same
@@ -101,6 +109,11 @@ struct FwdIO {
   void* o;
   float* h_final;
   int save;
+  // fused gated RMSNorm epilogue (Dims::norm): y = o r w sigmoid(g) per row
+  const void* ng;   // gate g [Ntok, H, dv]
+  const float* nw;  // weight w [dv]
+  float neps;
+  void* y;          // [Ntok, H, dv]
 };
 
 struct BwdIO {
@@ -110,6 +123,17 @@ struct BwdIO {
   const float* dh_final;
   void *dq, *dk, *dv, *df, *db;
   float *dA_log, *ddt_bias, *dh0;
+  // fused gated RMSNorm backward (Dims::norm): from dy, g, w and the fp32 o the
+  // forward saved (Ws::nO) the reverse chain forms dO itself and writes it to
+  // dOw (dO above then names the same buffer for the per-chunk kernels), dg and
+  // the dw partials
+  const void* ng;
+  const float* nw;
+  float neps;
+  const void* dy;
+  void* dOw;
+  void* dg;
+  float* dw;
 };
 
 // Launch wrappers (return cudaGetLastError of their launches).
@@ -126,6 +150,28 @@ inline cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, args...);
+}
+// Launches kernel k in thread-block clusters of cz CTAs along z (the grid's z
+// extent a multiple of cz), with the programmatic-stream-serialization
+// attribute when pdl is set.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_cluster(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, int cz,
+                                  bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[1].id = cudaLaunchAttributeClusterDimension;
+  at[1].val.clusterDim.x = 1;
+  at[1].val.clusterDim.y = 1;
+  at[1].val.clusterDim.z = cz;
+  cfg.attrs = pdl ? at : at + 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, k, args...);
 }
 cudaError_t launch_chunk_table(const int32_t* cu, const Dims& d, const Ws& w, cudaStream_t st);

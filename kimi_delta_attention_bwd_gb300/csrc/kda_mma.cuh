@@ -320,5 +320,47 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) 
 // Orders this thread's generic-proxy shared-memory accesses before later bulk copies.
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
+// ------------------------------------------------------------ thread-block clusters
+// Distributed shared memory between the CTAs of a cluster: an address of this
+// CTA's shared memory mapped to the same variable in CTA `rank` of the
+// cluster, remote stores and remote mbarrier arrivals through it, and the
+// cluster-wide barrier.  A CTA must not exit while a peer may still access
+// its shared memory: kernels that exchange end with cluster_sync().
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};\n" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+// Arrives on an mbarrier of another CTA of the cluster; release at cluster
+// scope orders this thread's earlier (remote) stores before the arrival.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(bar_addr) : "memory");
+}
+// mbar_wait with acquire at cluster scope: the arrivals came from a peer CTA,
+// whose stores before them are visible afterwards.  Bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t done = 0;
+  for (int it = 0; it < (1 << 20) && !done; it++)
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, "
+        "p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+  return done != 0;
+}
+// Every thread of every CTA of the cluster (warp-convergent).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
 }  // namespace mma
 }  // namespace kda
