@@ -417,6 +417,130 @@ def short_conv_bench(args, dev, flush, world, stream, hbm, rank):
                                  "frac": bb / (bwd_ms / 1e3) / 1e9 / hbm, "algorithmic_bytes_per_launch": bb}}}
 
 
+def fused_norm_bench(args, dev, flush, world, stream, hbm, rank):
+    """KDA with the gated RMSNorm epilogue at the 300M layer shape: the fused
+    entry points (kda_fwd_norm_gate + kda_bwd_norm_gate) against the same work
+    composed of four calls (kda_fwd, kda_norm_gate_fwd, kda_norm_gate_bwd,
+    kda_bwd), forward + backward, and the fused forward alone (inference: no
+    save, o never written)."""
+    from kimi_delta_attention_bwd_gb300 import (kda_backward, kda_backward_norm_gate, kda_forward,
+                                                kda_forward_norm_gate, kda_norm_gate, kda_norm_gate_backward, _lib)
+    from kimi_delta_attention_bwd_gb300.inputs import norm_gate_inputs
+    w = WORKLOADS[STEP_WORKLOAD]
+    inp = make_inputs(w, seed=BASE_SEED + STEP_WORKLOAD + 1000 * rank)
+    d = {k: (t.to(dev) if isinstance(t, torch.Tensor) else t) for k, t in inp.items()}
+    shape = (w.B, w.T, w.H, w.dv)
+    ng = norm_gate_inputs(w.B * w.T * w.H, w.dv, "bf16", seed=BASE_SEED + 80 + 1000 * rank)
+    g, wn, dy = ng["g"].reshape(shape).to(dev), ng["w"].to(dev), ng["dy"].reshape(shape).to(dev)
+    prob = _lib.make_problem(w.B, w.T, w.H, w.dk, w.dv, w.torch_dtype, d["scale"])
+    ws2 = _lib.alloc_workspace(prob, 2, dev)
+    ws1 = _lib.alloc_workspace(prob, 1, dev)
+    ws0 = _lib.alloc_workspace(prob, 0, dev)
+    nws = torch.empty(_lib.kda_norm_gate_workspace_size(w.B * w.T * w.H, w.dv), dtype=torch.uint8, device=dev)
+    x = (d["q"], d["k"], d["v"], d["f"], d["b"], d["A_log"], d["dt_bias"])
+
+    def fused():
+        _, _, _, ctx = kda_forward_norm_gate(*x, g, wn, scale=d["scale"], workspace=ws2, want_final_state=False)
+        kda_backward_norm_gate(ctx, dy, want_dh0=False)
+
+    def composed():
+        o, _, ctx = kda_forward(*x, scale=d["scale"], workspace=ws1, want_final_state=False)
+        kda_norm_gate(o, g, wn)
+        do, _, _ = kda_norm_gate_backward(o, g, wn, dy, workspace=nws)
+        kda_backward(ctx, do, want_dh0=False)
+
+    def fused_fwd():
+        kda_forward_norm_gate(*x, g, wn, scale=d["scale"], workspace=ws0, save_for_backward=False,
+                              want_final_state=False)
+
+    def composed_fwd():
+        o, _, _ = kda_forward(*x, scale=d["scale"], workspace=ws0, save_for_backward=False, want_final_state=False)
+        kda_norm_gate(o, g, wn)
+
+    res = {}
+    for name, fn, back in (("fused_step", fused, True), ("composed_step", composed, True),
+                           ("fused_fwd", fused_fwd, False), ("composed_fwd", composed_fwd, False)):
+        ms = max_over_ranks(time_steps(fn, args.steps, args.warmup, flush, world, stream), world, dev)
+        # algorithmic bytes: the KDA step's, plus g read and y written (and, backward, g and dy read, dg written)
+        nb = step_bytes(w, back) + w.B * w.T * w.H * w.dv * 2 * (2 + (3 if back else 0))
+        res[name] = {"value": world * w.tokens / (ms / 1e3), "ms_per_step": ms,
+                     "roofline": {"bound": "hbm", "algorithmic_bytes": nb, "achieved": nb / (ms / 1e3) / 1e9,
+                                  "peak": hbm, "unit": "GB/s", "frac": nb / (ms / 1e3) / 1e9 / hbm}}
+    _lib.prof_start()
+    time_steps(fused, args.steps, 0, flush, world, stream)
+    prof = _lib.prof_stop()
+    res["fused_kernels_ms_per_step"] = {k: v[0] / args.steps for k, v in prof.items() if v[1]}
+    res["workload"] = f"{w.name} with the gated RMSNorm epilogue (g, dy ~ N(0,1) bf16, w ~ 1 + 0.1 N(0,1))"
+    res["unit"] = "tokens/s"
+    del ws0, ws1, ws2
+    torch.cuda.empty_cache()
+    return res
+
+
+def fused_conv_bench(args, dev, flush, world, stream, hbm, rank):
+    """The layer at the 300M shape: short conv (width 4, silu) on the q | k | v
+    projection, KDA, gated RMSNorm, forward + backward.  Fused: kda_fwd_conv +
+    kda_bwd_conv (the convolution applied to the rows the per-chunk kernels
+    load, the norm inside the chains).  Composed: the standalone convolution
+    on each of the q, k, v blocks, kda_fwd, kda_norm_gate_fwd; then
+    kda_norm_gate_bwd, kda_bwd and the convolution's backward."""
+    from kimi_delta_attention_bwd_gb300 import (kda_backward, kda_backward_conv, kda_forward, kda_forward_conv,
+                                                kda_norm_gate, kda_norm_gate_backward, kda_short_conv,
+                                                kda_short_conv_backward, _lib)
+    from kimi_delta_attention_bwd_gb300.inputs import norm_gate_inputs, short_conv_inputs
+    w = WORKLOADS[STEP_WORKLOAD]
+    inp = make_inputs(w, seed=BASE_SEED + STEP_WORKLOAD + 1000 * rank)
+    d = {k: (t.to(dev) if isinstance(t, torch.Tensor) else t) for k, t in inp.items()}
+    N, H, dk, dv = w.B * w.T, w.H, w.dk, w.dv
+    C = H * (2 * dk + dv)
+    cv = short_conv_inputs(N, C, "bf16", seed=BASE_SEED + 81 + 1000 * rank)
+    x, cw = cv["x"].reshape(w.B, w.T, C).to(dev), cv["w"].to(dev)
+    xq, xk, xv = (x[..., a:b].contiguous() for a, b in ((0, H * dk), (H * dk, 2 * H * dk), (2 * H * dk, C)))
+    cwq, cwk, cwv = cw[:H * dk].contiguous(), cw[H * dk:2 * H * dk].contiguous(), cw[2 * H * dk:].contiguous()
+    shape = (w.B, w.T, H, dv)
+    ng = norm_gate_inputs(N * H, dv, "bf16", seed=BASE_SEED + 82 + 1000 * rank)
+    g, wn, dy = ng["g"].reshape(shape).to(dev), ng["w"].to(dev), ng["dy"].reshape(shape).to(dev)
+    prob = _lib.make_problem(w.B, w.T, H, dk, dv, w.torch_dtype, d["scale"])
+    ws3 = _lib.alloc_workspace(prob, 3, dev)
+    ws1 = _lib.alloc_workspace(prob, 1, dev)
+    cu_rows = torch.arange(0, (w.B + 1) * w.T, w.T, dtype=torch.int32, device=dev)  # the rows are the documents
+
+    def fused():
+        _, _, ctx = kda_forward_conv(x, cw, d["f"], d["b"], d["A_log"], d["dt_bias"], dk, dv, g=g, w=wn,
+                                     scale=d["scale"], workspace=ws3, want_final_state=False)
+        kda_backward_conv(ctx, dy, want_dh0=False)
+
+    def composed():
+        q = kda_short_conv(xq.view(N, -1), cwq, cu_rows).view(w.B, w.T, H, dk)
+        k = kda_short_conv(xk.view(N, -1), cwk, cu_rows).view(w.B, w.T, H, dk)
+        v = kda_short_conv(xv.view(N, -1), cwv, cu_rows).view(w.B, w.T, H, dv)
+        o, _, ctx = kda_forward(q, k, v, d["f"], d["b"], d["A_log"], d["dt_bias"], scale=d["scale"], workspace=ws1,
+                                want_final_state=False)
+        kda_norm_gate(o, g, wn)
+        do, _, _ = kda_norm_gate_backward(o, g, wn, dy)
+        gr = kda_backward(ctx, do, want_dh0=False)
+        kda_short_conv_backward(xq.view(N, -1), cwq, gr["dq"].view(N, -1), cu_rows)
+        kda_short_conv_backward(xk.view(N, -1), cwk, gr["dk"].view(N, -1), cu_rows)
+        kda_short_conv_backward(xv.view(N, -1), cwv, gr["dv"].view(N, -1), cu_rows)
+
+    res = {}
+    nb = step_bytes(w, True) + N * H * dv * 2 * 5  # the KDA step's bytes, x counted as q | k | v; g, y, dy, dg
+    for name, fn in (("fused_step", fused), ("composed_step", composed)):
+        ms = max_over_ranks(time_steps(fn, args.steps, args.warmup, flush, world, stream), world, dev)
+        res[name] = {"value": world * w.tokens / (ms / 1e3), "ms_per_step": ms,
+                     "roofline": {"bound": "hbm", "algorithmic_bytes": nb, "achieved": nb / (ms / 1e3) / 1e9,
+                                  "peak": hbm, "unit": "GB/s", "frac": nb / (ms / 1e3) / 1e9 / hbm}}
+    _lib.prof_start()
+    time_steps(fused, args.steps, 0, flush, world, stream)
+    prof = _lib.prof_stop()
+    res["fused_kernels_ms_per_step"] = {k: v[0] / args.steps for k, v in prof.items() if v[1]}
+    res["workload"] = f"{w.name}: short conv (x [{N}, {C}] bf16, taps ~ N(0, 0.25)) -> KDA -> gated RMSNorm"
+    res["unit"] = "tokens/s"
+    del ws1, ws3
+    torch.cuda.empty_cache()
+    return res
+
+
 def time_steps(step, steps, warmup, flush, world, stream):
     for _ in range(warmup):
         step()
@@ -536,6 +660,8 @@ def run_ours(args, rank, world, local):
     torch.cuda.empty_cache()
     sconv = short_conv_bench(args, dev, flush, world, stream, hbm, rank)
     torch.cuda.empty_cache()
+    fnorm = fused_norm_bench(args, dev, flush, world, stream, hbm, rank)
+    fconv = fused_conv_bench(args, dev, flush, world, stream, hbm, rank)
 
     # the training step (timed region with per-kernel event brackets and clock sampling)
     w = WORKLOADS[STEP_WORKLOAD]
@@ -605,6 +731,8 @@ def run_ours(args, rank, world, local):
             "large_head_step": large,
             "decode": dec,
             "norm_gate": ngate,
+            "norm_gate_fused": fnorm,
+            "conv_norm_layer": fconv,
             "short_conv": sconv,
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": traffic, "peak_kind": peak_kind,

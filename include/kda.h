@@ -109,7 +109,8 @@ typedef struct kda_problem {
 /* Bytes of device workspace kda_fwd / kda_bwd need for this problem
  * (for_backward = 0: forward only; 1: forward that saves for the backward,
  * and the backward; 2: kda_fwd_norm_gate saving for kda_bwd_norm_gate, and
- * that backward).  Returns 0 for an invalid problem. */
+ * that backward; 3: kda_fwd_conv saving for kda_bwd_conv, and that
+ * backward).  Returns 0 for an invalid problem. */
 KDA_API size_t kda_workspace_size(const kda_problem* p, int for_backward);
 
 /* Forward.  Writes o and, when non-NULL, h_final.  h0 may be NULL (zero
@@ -186,10 +187,63 @@ KDA_API kda_status kda_bwd_norm_gate(const kda_problem* p,
                    float* dA_log, float* ddt_bias, float* dh0,
                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* The layer around the KDA path in one call each way: the varlen short causal
+ * convolution (width 4, silu) on the concatenated q | k | v projection, KDA,
+ * and optionally the gated RMSNorm epilogue ("Pure KDA 300M" guide,
+ * Overview: short-conv kernel size 4, depthwise on the concatenated QKV, then
+ * the KDA recurrence, per-head output gate and RMSNorm; torchtitan PR "[kimi
+ * k3] Support sample packing in KDA": the convolution window and the state
+ * both reset at document starts):
+ *   q | k | v = silu(conv4(x)),   o = KDA(q, k, v, f, b, ...),   y = o r w sigmoid(g)
+ * x : [B, T, H (2 dk + dv)] in dtype, the q channels (h dk + i) first, then k,
+ * then v (h dv + j); conv_w : [H (2 dk + dv), 4] fp32, tap j multiplying
+ * x_{t-3+j}; tokens before the document start read as 0 (documents are the
+ * rows, or cu_seqlens).  g == NULL: no norm (o is written, y unused); else as
+ * kda_fwd_norm_gate (o optional).  bf16 io at dk=32/dv=64 only (other shapes:
+ * KDA_ERR_UNSUPPORTED): the per-chunk kernels apply the convolution and silu
+ * to the rows they load (with the three tokens before the chunk), so q, k, v
+ * never exist in memory.  Saving for the backward needs
+ * kda_workspace_size(p, 3) bytes. */
+KDA_API kda_status kda_fwd_conv(const kda_problem* p, const void* x, const float* conv_w,
+                   const void* f, const void* b, const float* A_log, const float* dt_bias, const float* h0,
+                   const void* g, const float* w, float eps,
+                   void* o, void* y, float* h_final,
+                   int save_for_backward, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Backward of kda_fwd_conv: the loss sum(y * dy) (with the norm; dy then
+ * [B, T, H, dv], and dO, dg, dw are written as in kda_bwd_norm_gate) or
+ * sum(o * dy) (g == NULL; dO, dg, dw unused), plus sum(h_final * dh_final).
+ * Writes dx [B, T, H (2 dk + dv)] (dtype), dconv_w [H (2 dk + dv), 4] (fp32,
+ * summed in a fixed order), df, db, dA_log, ddt_bias and dh0 (NULL: not
+ * returned).  The per-chunk kernels recompute q, k, v from x and write the
+ * fp32 gradients of the convolution's outputs into the workspace; one
+ * streaming kernel then forms dx and the tap gradients (its window crosses
+ * chunk boundaries).  The workspace must come from kda_fwd_conv with
+ * save_for_backward = 1 on the same inputs. */
+KDA_API kda_status kda_bwd_conv(const kda_problem* p, const void* x, const float* conv_w,
+                   const void* f, const void* b, const float* A_log, const float* dt_bias, const float* h0,
+                   const void* g, const float* w, float eps,
+                   const void* dy, const float* dh_final,
+                   void* dO, void* dg, float* dw,
+                   void* dx, float* dconv_w, void* df, void* db,
+                   float* dA_log, float* ddt_bias, float* dh0,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Synchronises `stream` and reads the device-side error word kept in the
  * workspace (KDA_OK, or the status the device flagged, e.g.
  * KDA_ERR_BAD_SEQLENS for offsets that were only on the device). */
 KDA_API kda_status kda_device_status(const void* workspace, cudaStream_t stream);
+
+/* Failure-detection test hook.  Every wait of the library's kernels on an
+ * mbarrier (bulk-copy completion, a cluster peer's data) gives up after a
+ * quarter of a second; the kernel then flags KDA_ERR_DEVICE in the workspace's
+ * error word, skips its remaining work and returns, leaving the context
+ * usable.  While enable != 0, later tensor-core forwards (bf16, dk=32/dv=64)
+ * make the state chain's stage barriers expect 16 bytes more than each copy
+ * delivers, so those waits run out (every copy issued still completes):
+ * kda_device_status() then reports KDA_ERR_DEVICE, and the outputs are not
+ * valid.  Off by default; process-wide, not thread-safe; for tests only. */
+KDA_API kda_status kda_test_stage_timeout(int enable);
 
 /* Human-readable text for a status. */
 KDA_API const char* kda_strerror(kda_status s);

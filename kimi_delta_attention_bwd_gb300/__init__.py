@@ -10,6 +10,8 @@ libkda_gb300.so through its C ABI, include/kda.h):
   y = kda_norm_gate(o, gate, weight)                           # gated RMSNorm epilogue
   y, o, h_final, ctx = kda_forward_norm_gate(q, ..., gate, weight)  # KDA with the epilogue fused
   grads = kda_backward_norm_gate(ctx, dy)                      # dq .. dh0, dO, dgate, dweight
+  out, h_final, ctx = kda_forward_conv(x, conv_w, f, ...)      # short conv -> KDA (-> gated norm), fused
+  grads = kda_backward_conv(ctx, dy)                           # dx, dconv_w, df, db, ...
   do, dgate, dweight = kda_norm_gate_backward(o, gate, weight, dy)
   o = kda_attention(q, k, v, f, b, A_log, dt_bias)             # the same as a torch.autograd op
   x = short_conv(x_raw, conv_w); y = gated_norm(o, gate, weight)  # likewise
@@ -28,7 +30,8 @@ import torch
 from . import _lib
 from ._lib import KdaError, kda_device_status, kda_strerror_text  # noqa: F401
 
-__all__ = ["kda_forward", "kda_backward", "kda_forward_norm_gate", "kda_backward_norm_gate", "kda_decode_step", "kda_norm_gate", "kda_norm_gate_backward",
+__all__ = ["kda_forward", "kda_backward", "kda_forward_norm_gate", "kda_backward_norm_gate", "kda_forward_conv",
+           "kda_backward_conv", "kda_decode_step", "kda_norm_gate", "kda_norm_gate_backward",
            "kda_short_conv", "kda_short_conv_backward", "KdaContext", "KdaError", "kda_device_status",
            "kda_attention", "short_conv", "gated_norm"]
 
@@ -257,6 +260,103 @@ def kda_backward_norm_gate(ctx: KdaNormContext, dy, dh_final=None, want_dh0: boo
     _lib.kda_bwd_norm_gate(c.problem, c.q, c.k, c.v, c.f, c.b, c.A_log, c.dt_bias, c.h0, ctx.g, ctx.w, ctx.eps,
                            dy, dh_final, gr["dO"], gr["dg"], gr["dw"], gr["dq"], gr["dk"], gr["dv"], gr["df"],
                            gr["db"], gr["dA_log"], gr["ddt_bias"], gr["dh0"], c.workspace)
+    return gr
+
+
+@dataclass
+class KdaConvContext:
+    """What kda_backward_conv needs from kda_forward_conv."""
+    problem: object
+    x: torch.Tensor
+    conv_w: torch.Tensor
+    f: torch.Tensor
+    b: torch.Tensor
+    A_log: torch.Tensor
+    dt_bias: torch.Tensor
+    h0: Optional[torch.Tensor]
+    g: Optional[torch.Tensor]
+    w: Optional[torch.Tensor]
+    eps: float
+    cu_seqlens: Optional[torch.Tensor]
+    cu_seqlens_host: object
+    workspace: torch.Tensor
+    n_docs: int
+    dk: int
+    dv: int
+    saved: bool
+
+
+def kda_forward_conv(x, conv_w, f, b, A_log, dt_bias, dk: int, dv: int, g=None, w=None, eps: Optional[float] = None,
+                     scale: Optional[float] = None, h0=None, cu_seqlens=None, cu_seqlens_host=None,
+                     save_for_backward: bool = True, workspace: Optional[torch.Tensor] = None,
+                     want_final_state: bool = True):
+    """The layer in one call: q | k | v = silu(conv4(x)) per document, KDA, and
+    (g, w given) the gated RMSNorm.  x [B, T, H (2 dk + dv)] (q channels, then
+    k, then v), conv_w [H (2 dk + dv), 4] fp32.  Returns (out, h_final or None,
+    ctx): out is y with the norm, o without."""
+    _dims(x, "x", 3)
+    B, T, Cx = x.shape
+    H = A_log.shape[0]
+    if Cx != H * (2 * dk + dv):
+        raise ValueError(f"x has {Cx} channels; H (2 dk + dv) = {H * (2 * dk + dv)}")
+    _shape(conv_w, "conv_w", (Cx, 4))
+    _shape(b, "b", (B, T, H))
+    _shape(A_log, "A_log", (H,))
+    gate = _gate_of(f, dt_bias, (B, T, H, dk))
+    n_docs = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if h0 is not None:
+        _shape(h0, "h0", (n_docs, H, dk, dv))
+        _check(h0, "h0", torch.float32)
+    for t, n in ((x, "x"), (f, "f"), (b, "b")):
+        _check(t, n, x.dtype)
+    _check(conv_w, "conv_w", torch.float32)
+    _check(A_log, "A_log", torch.float32)
+    _check(dt_bias, "dt_bias", torch.float32)
+    if cu_seqlens is not None:
+        _check(cu_seqlens, "cu_seqlens", torch.int32)
+    if g is not None:
+        _shape(g, "g", (B, T, H, dv))
+        _shape(w, "w", (dv,))
+        _check(g, "g", x.dtype)
+        _check(w, "w", torch.float32)
+    prob = _lib.make_problem(B, T, H, dk, dv, x.dtype, scale, cu_seqlens, cu_seqlens_host, gate)
+    if workspace is None:
+        workspace = _lib.alloc_workspace(prob, 3 if save_for_backward else 0, x.device)
+    out = torch.empty(B, T, H, dv, dtype=x.dtype, device=x.device)
+    o, y = (out, None) if g is None else (None, out)
+    hf = torch.empty(n_docs, H, dk, dv, dtype=torch.float32, device=x.device) if want_final_state else None
+    _lib.kda_fwd_conv(prob, x, conv_w, f, b, A_log, dt_bias, h0, g, w, eps, o, y, hf, save_for_backward, workspace)
+    ctx = KdaConvContext(prob, x, conv_w, f, b, A_log, dt_bias, h0, g, w, float(eps or 0.0), cu_seqlens,
+                         cu_seqlens_host, workspace, n_docs, dk, dv, bool(save_for_backward))
+    return out, hf, ctx
+
+
+def kda_backward_conv(ctx: KdaConvContext, dy, dh_final=None, want_dh0: bool = True):
+    """Backward of the layer: dy is the gradient of its output (y with the
+    norm, o without).  Returns dx, dconv_w, df, db, dA_log, ddt_bias, dh0 and,
+    with the norm, dO, dg, dw."""
+    if not ctx.saved:
+        raise ValueError("the forward saved nothing: call kda_forward_conv with save_for_backward=True")
+    x = ctx.x
+    B, T, _ = x.shape
+    H, dk, dv = ctx.A_log.shape[0], ctx.dk, ctx.dv
+    _shape(dy, "dy", (B, T, H, dv))
+    _check(dy, "dy", x.dtype)
+    if dh_final is not None:
+        _shape(dh_final, "dh_final", (ctx.n_docs, H, dk, dv))
+        _check(dh_final, "dh_final", torch.float32)
+    norm = ctx.g is not None
+    gr = {
+        "dx": torch.empty_like(x), "dconv_w": torch.empty_like(ctx.conv_w), "df": torch.empty_like(ctx.f),
+        "db": torch.empty_like(ctx.b), "dA_log": torch.empty(H, dtype=torch.float32, device=x.device),
+        "ddt_bias": torch.empty_like(ctx.dt_bias),
+        "dh0": torch.empty(ctx.n_docs, H, dk, dv, dtype=torch.float32, device=x.device) if want_dh0 else None,
+        "dO": torch.empty_like(dy) if norm else None, "dg": torch.empty_like(dy) if norm else None,
+        "dw": torch.empty(dv, dtype=torch.float32, device=x.device) if norm else None,
+    }
+    _lib.kda_bwd_conv(ctx.problem, x, ctx.conv_w, ctx.f, ctx.b, ctx.A_log, ctx.dt_bias, ctx.h0, ctx.g, ctx.w, ctx.eps,
+                      dy, dh_final, gr["dO"], gr["dg"], gr["dw"], gr["dx"], gr["dconv_w"], gr["df"], gr["db"],
+                      gr["dA_log"], gr["ddt_bias"], gr["dh0"], ctx.workspace)
     return gr
 
 

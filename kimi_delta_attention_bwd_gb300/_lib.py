@@ -72,8 +72,14 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.kda_fwd_norm_gate.restype = I
         lib.kda_bwd_norm_gate.argtypes = [PP] + [P] * 10 + [F] + [P] * 13 + [P, SZ, P]
         lib.kda_bwd_norm_gate.restype = I
+        lib.kda_fwd_conv.argtypes = [PP] + [P] * 9 + [F] + [P] * 3 + [I, P, SZ, P]
+        lib.kda_fwd_conv.restype = I
+        lib.kda_bwd_conv.argtypes = [PP] + [P] * 9 + [F] + [P] * 12 + [P, SZ, P]
+        lib.kda_bwd_conv.restype = I
         lib.kda_fwd_noalloc.argtypes = [PP] + [P] * 10 + [P]
         lib.kda_fwd_noalloc.restype = I
+        lib.kda_test_stage_timeout.argtypes = [I]
+        lib.kda_test_stage_timeout.restype = I
         lib.kda_noalloc_status.argtypes = [P]
         lib.kda_noalloc_status.restype = I
         lib.kda_strerror.argtypes = [I]
@@ -139,8 +145,8 @@ def make_problem(B, T, H, dk, dv, dtype, scale=None, cu_seqlens=None, cu_seqlens
 
 def kda_workspace_size(problem: kda_problem, for_backward) -> int:
     """for_backward: False / 0 (forward only), True / 1 (saving for kda_bwd), 2
-    (saving for kda_bwd_norm_gate)."""
-    kind = 2 if for_backward == 2 else 1 if for_backward else 0
+    (saving for kda_bwd_norm_gate), 3 (saving for kda_bwd_conv)."""
+    kind = int(for_backward) if for_backward in (2, 3) else 1 if for_backward else 0
     return int(load().kda_workspace_size(ctypes.byref(problem), kind))
 
 
@@ -192,6 +198,28 @@ def kda_bwd_norm_gate(problem, q, k, v, f, b, A_log, dt_bias, h0, g, w, eps, dy,
                                   _stream())
     if st != 0:
         raise KdaError(st, "kda_bwd_norm_gate")
+
+
+def kda_fwd_conv(problem, x, conv_w, f, b, A_log, dt_bias, h0, g, w, eps, o, y, h_final, save_for_backward,
+                 workspace):
+    """Raw forward of the layer: short convolution, KDA, optional gated norm."""
+    st = load().kda_fwd_conv(ctypes.byref(problem), _p(x), _p(conv_w), _p(f), _p(b), _p(A_log), _p(dt_bias), _p(h0),
+                             _p(g), _p(w), float(eps or 0.0), _p(o), _p(y), _p(h_final),
+                             1 if save_for_backward else 0, _p(workspace),
+                             workspace.numel() if workspace is not None else 0, _stream())
+    if st != 0:
+        raise KdaError(st, "kda_fwd_conv")
+
+
+def kda_bwd_conv(problem, x, conv_w, f, b, A_log, dt_bias, h0, g, w, eps, dy, dh_final, dO, dg, dw, dx, dconv_w,
+                 df, db, dA_log, ddt_bias, dh0, workspace):
+    """Raw backward of the layer."""
+    st = load().kda_bwd_conv(ctypes.byref(problem), _p(x), _p(conv_w), _p(f), _p(b), _p(A_log), _p(dt_bias), _p(h0),
+                             _p(g), _p(w), float(eps or 0.0), _p(dy), _p(dh_final), _p(dO), _p(dg), _p(dw), _p(dx),
+                             _p(dconv_w), _p(df), _p(db), _p(dA_log), _p(ddt_bias), _p(dh0), _p(workspace),
+                             workspace.numel() if workspace is not None else 0, _stream())
+    if st != 0:
+        raise KdaError(st, "kda_bwd_conv")
 
 
 def kda_decode(n_seq, H, dk, dv, dtype, scale, q, k, v, f, b, A_log, dt_bias, state, o, gate=KDA_GATE_CHANNEL):

@@ -128,7 +128,7 @@ struct Layout {
   size_t off_err, off_nch, off_dc0, off_ct0, off_cl, off_cd;
   size_t off_W, off_U, off_P, off_QG, off_KD, off_gam, off_Sent, off_CH;
   size_t off_sT, off_sP, off_sW, off_sU, off_sA, off_gDP, off_gMA, off_gQG, off_gKD, off_gKG, off_gdg;
-  size_t off_dE, off_dSn, off_pA, off_pdt, off_scr, off_nO, off_pdw, off_nrm;
+  size_t off_dE, off_dSn, off_pA, off_pdt, off_scr, off_nO, off_pdw, off_nrm, off_cg, off_cpart;
 };
 
 // Workspace layout.  Both paths start with the error word, the saved-problem
@@ -169,9 +169,14 @@ static Layout layout(const Dims& d, int for_bwd, bool fused = false) {
       L.off_gKG = take(4 * nch * C * d.dk);
       L.off_gdg = take(4 * nch * d.dk);
     }
-    if (for_bwd == 2) {  // kda_fwd_norm_gate saving for kda_bwd_norm_gate
+    if (for_bwd >= 2) {  // kda_fwd_norm_gate / kda_fwd_conv saving for their backward
       L.off_nO = take(4 * (size_t)d.Ntok * d.H * d.dv);
       L.off_pdw = take(4 * (size_t)d.n_docs * d.H * d.dv);
+    }
+    if (for_bwd == 3) {  // the fused convolution's backward
+      const int64_t Cc = (int64_t)d.H * (2 * d.dk + d.dv);
+      L.off_cg = take(4 * (size_t)d.Ntok * Cc);
+      L.off_cpart = take(kda_short_conv_workspace_size(d.Ntok, (int)Cc));
     }
     L.total = o;
     return L;
@@ -238,14 +243,20 @@ static Ws bind(void* ws, const Layout& L, const Dims& d, int for_bwd) {
   w.gKG = at(L.off_gKG);
   w.gdg = at(L.off_gdg);
   w.nO = at(L.off_nO);
+  w.cg = at(L.off_cg);
+  w.cpart = at(L.off_cpart);
   w.pdw = at(L.off_pdw);
   w.nrm = at(L.off_nrm);
   return w;
 }
 
+// Failure-detection test hook (kda_test_stage_timeout); 0 in normal use.
+static int g_test_tx_extra = 0;
+
 // The forward launch sequence shared by kda_fwd and kda_fwd_noalloc.
 static cudaError_t run_forward(const kda_problem* p, Dims d, const FwdIO& io, const Ws& w, cudaStream_t stream,
                                bool fused = false) {
+  d.tx_extra = g_test_tx_extra;
   cudaError_t e = launch_chunk_table(p->cu_seqlens, d, w, stream);
   if (e != cudaSuccess) return e;
   if (d.fast) return launch_fast_fwd(d, io, w, stream, fused);
@@ -307,6 +318,8 @@ static kda_status check_problem(const kda_problem* p, Dims* d) {
   d->ahead = 0;
   d->gate = p->gate;
   d->norm = 0;
+  d->conv = 0;
+  d->tx_extra = 0;
   return KDA_OK;
 }
 
@@ -319,7 +332,7 @@ extern "C" {
 size_t kda_workspace_size(const kda_problem* p, int for_backward) {
   Dims d;
   if (check_problem(p, &d) != KDA_OK) return 0;
-  return layout(d, for_backward == 2 ? 2 : for_backward ? 1 : 0).total;
+  return layout(d, (for_backward == 2 || for_backward == 3) ? for_backward : for_backward ? 1 : 0).total;
 }
 
 static kda_status status_of(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
@@ -333,16 +346,41 @@ struct NormArgs {
   const float* w;
   float eps;
 };
+// The short convolution's arguments: x [Ntok, H (2 dk + dv)] (the q | k | v
+// blocks before the convolution) and its taps [H (2 dk + dv), 4].
+struct ConvArgs {
+  const void* x;
+  const float* w;
+};
+// Points the q, k, v inputs (and the convolution taps) of io at the blocks of x.
+template <class IO>
+void bind_conv(IO& io, const Dims& d, const ConvArgs& cv) {
+  const size_t qk = (size_t)d.H * d.dk;
+  const __nv_bfloat16* x = (const __nv_bfloat16*)cv.x;
+  io.q = x;
+  io.k = x + qk;
+  io.v = x + 2 * qk;
+  io.ld = d.H * (2 * d.dk + d.dv);
+  io.cwq = cv.w;
+  io.cwk = cv.w + 4 * qk;
+  io.cwv = cv.w + 8 * qk;
+}
 
 kda_status fwd_impl(const kda_problem* p, const void* q, const void* k, const void* v, const void* f, const void* b,
                     const float* A_log, const float* dt_bias, const float* h0, void* o, float* h_final,
                     int save_for_backward, void* workspace, size_t workspace_bytes, cudaStream_t stream,
-                    const NormArgs* nm, void* y) {
+                    const NormArgs* nm, void* y, const ConvArgs* cv = nullptr) {
   Dims d;
   kda_status s = check_problem(p, &d);
   if (s != KDA_OK) return s;
   if (nm && !d.fast && p->dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;  // bf16 needs the fused kernels
-  const int fb = save_for_backward ? (nm ? 2 : 1) : 0;
+  if (cv && !d.fast) return KDA_ERR_UNSUPPORTED;                         // the convolution is fused only there
+  if (cv) {
+    if (!cv->x || !cv->w) return KDA_ERR_INVALID_ARG;
+    if (!aligned(cv->x, 16) || !aligned(cv->w, 16)) return KDA_ERR_ALIGNMENT;
+    q = k = v = cv->x;  // checked below; bound to the blocks of x after the checks
+  }
+  const int fb = save_for_backward ? (cv ? 3 : nm ? 2 : 1) : 0;
   // o may be omitted with the norm, except as the composed path's intermediate when nothing is saved
   const bool need_o = !nm || (!d.fast && !fb);
   if (!q || !k || !v || !f || !b || !A_log || !dt_bias || (need_o && !o)) return KDA_ERR_INVALID_ARG;
@@ -358,9 +396,15 @@ kda_status fwd_impl(const kda_problem* p, const void* q, const void* k, const vo
   if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
   Ws w = bind(workspace, L, d, fb ? 1 : 0);
   d.save = fb ? 1 : 0;
-  if (nm) d.tag ^= 2;  // a workspace saved with the norm serves kda_bwd_norm_gate only
+  if (nm) d.tag ^= 2;  // a workspace saved with the norm (or the convolution) serves that backward only
+  if (cv) d.tag ^= 4;
   const float eps = nm && nm->eps > 0.f ? nm->eps : 1e-6f;
-  FwdIO io{q, k, v, f, b, A_log, dt_bias, h0, o, h_final, d.save, nullptr, nullptr, 0.f, nullptr};
+  FwdIO io{q, k, v, f, b, A_log, dt_bias, h0, o, h_final, d.save, nullptr, nullptr, 0.f, nullptr,
+           d.H * d.dk, nullptr, nullptr, nullptr};
+  if (cv) {
+    d.conv = 1;
+    bind_conv(io, d, *cv);
+  }
   if (nm && d.fast) {  // fused into the forward chain's output warps
     d.norm = 1;
     io.ng = nm->g;
@@ -384,11 +428,19 @@ kda_status bwd_impl(const kda_problem* p, const void* q, const void* k, const vo
                     const float* A_log, const float* dt_bias, const void* dO, const float* dh_final, void* dq,
                     void* dk, void* dv, void* df, void* db, float* dA_log, float* ddt_bias, float* dh0,
                     void* workspace, size_t workspace_bytes, cudaStream_t stream, const NormArgs* nm,
-                    const void* dy, void* dg, float* dw) {
+                    const void* dy, void* dg, float* dw, const ConvArgs* cv = nullptr, void* dx = nullptr,
+                    float* dcw = nullptr) {
   Dims d;
   kda_status s = check_problem(p, &d);
   if (s != KDA_OK) return s;
   if (nm && !d.fast && p->dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
+  if (cv && !d.fast) return KDA_ERR_UNSUPPORTED;
+  if (cv) {
+    if (!cv->x || !cv->w || !dx || !dcw) return KDA_ERR_INVALID_ARG;
+    if (!aligned(cv->x, 16) || !aligned(cv->w, 16) || !aligned(dx, 16) || !aligned(dcw, 16)) return KDA_ERR_ALIGNMENT;
+    q = k = v = cv->x;  // bound to the blocks of x below
+  }
+  if (cv) dq = dk = dv = dx;  // the gradients of the convolution's outputs go to the workspace (below)
   if (!q || !k || !v || !f || !b || !A_log || !dt_bias || !dO || !dq || !dk || !dv || !df || !db ||
       !dA_log || !ddt_bias)
     return KDA_ERR_INVALID_ARG;
@@ -404,13 +456,22 @@ kda_status bwd_impl(const kda_problem* p, const void* q, const void* k, const vo
   }
   if (!workspace) return KDA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return KDA_ERR_ALIGNMENT;
-  Layout L = layout(d, nm ? 2 : 1);
+  Layout L = layout(d, cv ? 3 : nm ? 2 : 1);
   if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
   Ws w = bind(workspace, L, d, 1);
   if (nm) d.tag ^= 2;
+  if (cv) d.tag ^= 4;
   const float eps = nm && nm->eps > 0.f ? nm->eps : 1e-6f;
   BwdIO io{q, k, v, f, b, A_log, dt_bias, dO, dh_final, dq, dk, dv, df, db, dA_log, ddt_bias, dh0,
-           nullptr, nullptr, 0.f, nullptr, nullptr, nullptr, nullptr};
+           nullptr, nullptr, 0.f, nullptr, nullptr, nullptr, nullptr, d.H * d.dk, nullptr, nullptr, nullptr};
+  if (cv) {  // q, k, v from x; dq, dk, dv the fp32 gradients of the convolution's outputs
+    d.conv = 1;
+    bind_conv(io, d, *cv);
+    const size_t qk = (size_t)d.H * d.dk;
+    io.dq = w.cg;
+    io.dk = w.cg + qk;
+    io.dv = w.cg + 2 * qk;
+  }
   if (nm && d.fast) {  // fused into the reverse chain, which writes dO for the per-chunk kernels
     d.norm = 1;
     io.ng = nm->g;
@@ -427,7 +488,15 @@ kda_status bwd_impl(const kda_problem* p, const void* q, const void* k, const vo
                           kda_norm_gate_workspace_size(rows, d.dv), stream);
     if (s != KDA_OK) return s;
   }
-  if (d.fast) return status_of(launch_fast_bwd(d, io, w, stream));
+  if (d.fast) {
+    cudaError_t e = launch_fast_bwd(d, io, w, stream);
+    if (e == cudaSuccess && cv) {  // dx, dw of the convolution from its outputs' gradients
+      const int Cc = d.H * (2 * d.dk + d.dv);
+      e = launch_conv_bwd_fused(d.Ntok, Cc, p->cu_seqlens, d.n_docs, p->cu_seqlens ? (int64_t)d.Ntok : (int64_t)d.T,
+                                (const __nv_bfloat16*)cv->x, cv->w, w.cg, (__nv_bfloat16*)dx, w.cpart, dcw, stream);
+    }
+    return status_of(e);
+  }
   cudaError_t e = launch_bwd_scan(p->dtype, d, io, w, stream);
   if (e == cudaSuccess) e = launch_bwd_intra(p->dtype, d, io, w, stream);
   if (e == cudaSuccess) e = launch_bwd_reduce(d, io, w, stream);
@@ -464,6 +533,30 @@ kda_status kda_fwd_norm_gate(const kda_problem* p, const void* q, const void* k,
                   stream, &nm, y);
 }
 
+kda_status kda_fwd_conv(const kda_problem* p, const void* x, const float* conv_w, const void* f, const void* b,
+                        const float* A_log, const float* dt_bias, const float* h0, const void* g, const float* w,
+                        float eps, void* o, void* y, float* h_final, int save_for_backward, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+  const ConvArgs cv{x, conv_w};
+  const NormArgs nm{g, w, eps};
+  return fwd_impl(p, nullptr, nullptr, nullptr, f, b, A_log, dt_bias, h0, o, h_final, save_for_backward, workspace,
+                  workspace_bytes, stream, g ? &nm : nullptr, y, &cv);
+}
+
+kda_status kda_bwd_conv(const kda_problem* p, const void* x, const float* conv_w, const void* f, const void* b,
+                        const float* A_log, const float* dt_bias, const float* h0, const void* g, const float* w,
+                        float eps, const void* dy, const float* dh_final, void* dO, void* dg, float* dw, void* dx,
+                        float* dconv_w, void* df, void* db, float* dA_log, float* ddt_bias, float* dh0,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  (void)h0;
+  const ConvArgs cv{x, conv_w};
+  const NormArgs nm{g, w, eps};
+  // without the norm, dy is the gradient of o itself
+  return bwd_impl(p, nullptr, nullptr, nullptr, f, b, A_log, dt_bias, g ? dO : dy, dh_final, nullptr, nullptr,
+                  nullptr, df, db, dA_log, ddt_bias, dh0, workspace, workspace_bytes, stream, g ? &nm : nullptr,
+                  dy, dg, dw, &cv, dx, dconv_w);
+}
+
 kda_status kda_bwd_norm_gate(const kda_problem* p, const void* q, const void* k, const void* v, const void* f,
                              const void* b, const float* A_log, const float* dt_bias, const float* h0,
                              const void* g, const float* w, float eps, const void* dy, const float* dh_final,
@@ -474,6 +567,11 @@ kda_status kda_bwd_norm_gate(const kda_problem* p, const void* q, const void* k,
   const NormArgs nm{g, w, eps};
   return bwd_impl(p, q, k, v, f, b, A_log, dt_bias, dO, dh_final, dq, dk, dv, df, db, dA_log, ddt_bias, dh0,
                   workspace, workspace_bytes, stream, &nm, dy, dg, dw);
+}
+
+kda_status kda_test_stage_timeout(int enable) {
+  g_test_tx_extra = enable ? 16 : 0;
+  return KDA_OK;
 }
 
 kda_status kda_device_status(const void* workspace, cudaStream_t stream) {

@@ -91,13 +91,15 @@ template <> struct Raw4<float> {
 constexpr int LB = 4;  // rows per load batch
 
 // Document of token t: the largest d < n_docs with cu[d] <= t (cu non-decreasing
-// from 0; without cu one document).  Returns its start, and its end in *end.
+// from 0; without cu, rows of row_len tokens).  Returns its start, and its end
+// in *end.
 __device__ __forceinline__ int64_t doc_of(const int32_t* cu, int n_docs, int64_t n_tok, int64_t t, int& d,
-                                          int64_t& end) {
+                                          int64_t& end, int64_t row_len) {
   if (!cu) {
-    d = 0;
-    end = n_tok;
-    return 0;
+    d = (int)(t / row_len);
+    const int64_t st = (int64_t)d * row_len;
+    end = st + row_len < n_tok ? st + row_len : n_tok;
+    return st;
   }
   int lo = 0, hi = n_docs - 1;
   while (lo < hi) {
@@ -111,7 +113,11 @@ __device__ __forceinline__ int64_t doc_of(const int32_t* cu, int n_docs, int64_t
 }
 // Advance (d, start, end) to the document of token t >= end.
 __device__ __forceinline__ void next_doc(const int32_t* cu, int n_docs, int64_t n_tok, int64_t t, int& d,
-                                         int64_t& start, int64_t& end) {
+                                         int64_t& start, int64_t& end, int64_t row_len) {
+  if (!cu) {
+    start = doc_of(cu, n_docs, n_tok, t, d, end, row_len);
+    return;
+  }
   while (d + 1 < n_docs && cu[d + 1] <= t) d++;
   start = cu[d];
   end = d + 1 <= n_docs ? cu[d + 1] : n_tok;
@@ -159,7 +165,7 @@ __global__ void __launch_bounds__(CTHR) conv_fwd_kernel(int64_t n_tok, int C, in
   }
   int d;
   int64_t end;
-  int64_t start = doc_of(cu, n_docs, n_tok, t0, d, end);
+  int64_t start = doc_of(cu, n_docs, n_tok, t0, d, end, n_tok);
   const bool staged = mbar_wait(bar, 0);
   auto row = [&](int64_t p) -> uint4 {  // this thread's 16 bytes of token p
     return staged ? *reinterpret_cast<const uint4*>(csm + (p - rb) * CTHR * 16 + cv * 16) : raw16(x + p * C + c0);
@@ -177,7 +183,7 @@ __global__ void __launch_bounds__(CTHR) conv_fwd_kernel(int64_t n_tok, int C, in
     }
     for (int64_t t = t0; t < t1; t++) {
       if (t >= end) {  // a new document: the window restarts from zero
-        next_doc(cu, n_docs, n_tok, t, d, start, end);
+        next_doc(cu, n_docs, n_tok, t, d, start, end, n_tok);
 #pragma unroll
         for (int k2 = 0; k2 < KW - 1; k2++)
 #pragma unroll
@@ -204,10 +210,12 @@ __global__ void __launch_bounds__(CTHR) conv_fwd_kernel(int64_t n_tok, int C, in
 // four positions so that no window reaches across a document boundary.
 constexpr int NB = 4;  // channels per thread in the backward
 
-template <typename T>
+// T: the type of x and dx; TY: the type of dy (the fused KDA backward hands
+// over fp32 gradients).  Without cu, documents are rows of row_len tokens.
+template <typename T, typename TY = T>
 __global__ void __launch_bounds__(CTHR) conv_bwd_kernel(int64_t n_tok, int C, int act, const int32_t* __restrict__ cu,
-                                                       int n_docs, const T* __restrict__ x,
-                                                       const float* __restrict__ w, const T* __restrict__ dy,
+                                                       int n_docs, int64_t row_len, const T* __restrict__ x,
+                                                       const float* __restrict__ w, const TY* __restrict__ dy,
                                                        T* __restrict__ dx, float* __restrict__ part) {
   constexpr int N = NB;
   const int cv = blockIdx.x * CTHR + threadIdx.x;
@@ -224,7 +232,7 @@ __global__ void __launch_bounds__(CTHR) conv_bwd_kernel(int64_t n_tok, int C, in
   }
   int d;
   int64_t end;
-  int64_t start = doc_of(cu, n_docs, n_tok, t0, d, end);
+  int64_t start = doc_of(cu, n_docs, n_tok, t0, d, end, row_len);
   float xw[KW - 1][N];  // x_{u-3..u-1}
   float dzw[KW - 1][N];  // dz_{u-3..u-1}
   int64_t dsw[KW];       // document starts of u-3 .. u
@@ -241,15 +249,18 @@ __global__ void __launch_bounds__(CTHR) conv_bwd_kernel(int64_t n_tok, int C, in
     dsw[k] = start;  // positions before t0 only pair with dz of tokens >= t0 through dx_{< t0}: never emitted
   }
   using R = typename Raw4<T>::type;
+  using RY = typename Raw4<TY>::type;
   const int64_t u1 = t1 + (KW - 1);  // dx of the last token needs dz up to t1 + 2
   for (int64_t ub = t0; ub < u1; ub += LB) {
-  R rx[LB], rdy[LB];  // the batch's rows of x and dy, loaded before any is used
+  R rx[LB];  // the batch's rows of x and dy, loaded before any is used
+  RY rdy[LB];
 #pragma unroll
   for (int k = 0; k < LB; k++) {
-    rx[k] = rdy[k] = R{};
+    rx[k] = R{};
+    rdy[k] = RY{};
     if (ub + k < u1 && ub + k < n_tok) {
       rx[k] = Raw4<T>::ld(x + (ub + k) * C + c0);
-      rdy[k] = Raw4<T>::ld(dy + (ub + k) * C + c0);
+      rdy[k] = Raw4<TY>::ld(dy + (ub + k) * C + c0);
     }
   }
 #pragma unroll
@@ -260,7 +271,7 @@ __global__ void __launch_bounds__(CTHR) conv_bwd_kernel(int64_t n_tok, int C, in
     const bool live = u < n_tok;
     if (live) {
       if (u >= end) {
-        next_doc(cu, n_docs, n_tok, u, d, start, end);
+        next_doc(cu, n_docs, n_tok, u, d, start, end, row_len);
 #pragma unroll
         for (int k = 0; k < KW - 1; k++)
 #pragma unroll
@@ -379,12 +390,12 @@ extern "C" KDA_API kda_status kda_short_conv_bwd(int64_t n_tok, int C, int dtype
   float* part = (float*)workspace;
   prof_begin(K_CONV_BWD, st);
   if (dtype == KDA_BF16)
-    conv_bwd_kernel<__nv_bfloat16><<<grid, CTHR, 0, st>>>(n_tok, C, activation, cu_seqlens, n_docs,
+    conv_bwd_kernel<__nv_bfloat16><<<grid, CTHR, 0, st>>>(n_tok, C, activation, cu_seqlens, n_docs, n_tok,
                                                            (const __nv_bfloat16*)x, w, (const __nv_bfloat16*)dy,
                                                            (__nv_bfloat16*)dx, part);
   else
-    conv_bwd_kernel<float><<<grid, CTHR, 0, st>>>(n_tok, C, activation, cu_seqlens, n_docs, (const float*)x, w,
-                                                   (const float*)dy, (float*)dx, part);
+    conv_bwd_kernel<float><<<grid, CTHR, 0, st>>>(n_tok, C, activation, cu_seqlens, n_docs, n_tok, (const float*)x,
+                                                   w, (const float*)dy, (float*)dx, part);
   prof_end(K_CONV_BWD, st);
   if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
   prof_begin(K_CONV_RED, st);
@@ -392,3 +403,25 @@ extern "C" KDA_API kda_status kda_short_conv_bwd(int64_t n_tok, int C, int dtype
   prof_end(K_CONV_RED, st);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
+
+namespace kda {
+// The fused convolution's backward (kda_bwd_conv): dx (bf16) and dw from x
+// (bf16) and the fp32 gradients of the convolution's silu outputs that the
+// KDA backward kernels wrote; documents are cu's, or rows of row_len tokens.
+// part: kda_short_conv_workspace_size(n_tok, C) bytes.
+cudaError_t launch_conv_bwd_fused(int64_t n_tok, int C, const int32_t* cu, int n_docs, int64_t row_len,
+                                  const __nv_bfloat16* x, const float* w, const float* dy, __nv_bfloat16* dx,
+                                  float* part, float* dw, cudaStream_t st) {
+  const int n_tiles = (int)((n_tok + TBB - 1) / TBB);
+  const dim3 grid((C / NB + CTHR - 1) / CTHR, (unsigned)n_tiles);
+  prof_begin(K_CONV_BWD, st);
+  conv_bwd_kernel<__nv_bfloat16, float><<<grid, CTHR, 0, st>>>(n_tok, C, 1, cu, n_docs, row_len, x, w, dy, dx, part);
+  prof_end(K_CONV_BWD, st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  prof_begin(K_CONV_RED, st);
+  e = launch_sum_rows(part, n_tiles, C * KW, dw, st);
+  prof_end(K_CONV_RED, st);
+  return e;
+}
+}  // namespace kda

@@ -32,6 +32,8 @@
 #include "kda_mma.cuh"
 #include "kda_tc.cuh"
 
+#include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled
+
 #include <type_traits>
 
 namespace kda {
@@ -377,7 +379,7 @@ struct FwdSm {
 };
 
 __global__ void __launch_bounds__(NTH, 1) fwd_chain_kernel(Dims d, FwdIO io, Ws w) {
-  extern __shared__ __align__(16) unsigned char smraw[];
+  extern __shared__ __align__(128) unsigned char smraw[];
   FwdSm& sm = *reinterpret_cast<FwdSm*>(smraw);
   const int doc = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
   const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
@@ -520,6 +522,7 @@ __global__ void __launch_bounds__(NTH, 1) fwd_chain_kernel(Dims d, FwdIO io, Ws 
       }
     __syncthreads();
   }
+  __syncthreads();  // other threads wrote ss (for an empty document: the initial state just above)
   if (io.h_final)
     for (int idx = tid; idx < DK * DV; idx += NTH) {
       int i = idx / DV, j = idx % DV;
@@ -675,6 +678,7 @@ struct ChunkSm {
   float tot[NW * DK];
   int spanok[4];
   uint64_t bar;    // tensor-core rounds
+  uint64_t tbar;   // the raw inputs' tensor-map copies
   uint32_t tslot;  // TMEM base address
 };
 
@@ -768,12 +772,79 @@ __device__ __forceinline__ void store_acc(const float (&acc)[NT][4], float* g, i
     }
 }
 
+// ---- the short convolution fused into the prologues ("Pure KDA 300M" guide,
+// Overview: short-conv kernel size 4, depthwise on the concatenated QKV;
+// torchtitan PR "[kimi k3] Support sample packing in KDA": the window resets
+// at each document start):  u_t,c = silu(sum_j w_c,j x_{t-3+j,c}), with x of
+// tokens before the document start taken as 0.  Every kernel that needs q, k
+// or v recomputes them from x with these helpers, in the same order of
+// operations, so the forward and the backward see the same bits.
+__device__ __forceinline__ float silu_f(float z) { return z * sigmoid_fast(z); }
+// N consecutive channels (N a multiple of 8) of token t: x points at channel 0
+// of them in token 0's row, rows ld elements apart; wc at their taps [N][4];
+// tokens below tmin read as zero.
+template <int N>
+__device__ __forceinline__ void conv_load(float* out, const bf16* x, int ld, int t, int tmin, const float* wc) {
+#pragma unroll
+  for (int e8 = 0; e8 < N; e8 += 8) {
+    uint4 raw[4];  // the window's four rows, issued together; rows before tmin read as 0
+#pragma unroll
+    for (int jt = 0; jt < 4; jt++) {
+      const int tt = t - 3 + jt;
+      raw[jt] = tt >= tmin ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)tt * ld + e8)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    // element e of a row's 8 bf16 (exact widening: the bf16 bits are the fp32's top half)
+    auto xe = [&](int jt, int e) {
+      const uint32_t wd = e < 2 ? raw[jt].x : e < 4 ? raw[jt].y : e < 6 ? raw[jt].z : raw[jt].w;
+      return __uint_as_float((e & 1) ? (wd & 0xffff0000u) : (wd << 16));
+    };
+#pragma unroll
+    for (int e = 0; e < 8; e++) {
+      const float4 w4 = __ldg(reinterpret_cast<const float4*>(wc + 4 * (e8 + e)));  // taps of one channel
+      float z = fmaf(w4.x, xe(0, e), 0.f);
+      z = fmaf(w4.y, xe(1, e), z);
+      z = fmaf(w4.z, xe(2, e), z);
+      z = fmaf(w4.w, xe(3, e), z);
+      out[e8 + e] = silu_f(z);
+    }
+  }
+}
+// One channel (the exact wide-span fallback's operands): conv_load's value,
+// with the same operations in the same order (a token before tmin gives a
+// zero term, which leaves z unchanged exactly as the skipped row does).
+__device__ __forceinline__ float conv_one(const bf16* x, int ld, int t, int tmin, const float* wc) {
+  const float4 w4 = __ldg(reinterpret_cast<const float4*>(wc));
+  auto xa = [&](int jt) { const int tt = t - 3 + jt; return tt >= tmin ? bfl(x[(size_t)tt * ld]) : 0.f; };
+  float z = fmaf(w4.x, xa(0), 0.f);
+  z = fmaf(w4.y, xa(1), z);
+  z = fmaf(w4.z, xa(2), z);
+  z = fmaf(w4.w, xa(3), z);
+  return silu_f(z);
+}
+// The exact diagonal-block value of pair_exact2 with q / k recomputed through
+// the convolution (X: the q or k block, Kx: the k block, channel 0 of head h).
+__device__ __forceinline__ float pair_exact2_conv(const bf16* X, const float* wX, float ix, const bf16* Kx,
+                                                  const float* wK, float ik, int ld, int tr, int ts, int tmin,
+                                                  const float* Gr, const float* Gs) {
+  float acc = 0.f;
+  for (int i = 0; i < DK; i++)
+    acc += (conv_one(X + i, ld, tr, tmin, wX + 4 * i) * ix) * (conv_one(Kx + i, ld, ts, tmin, wK + 4 * i) * ik) *
+           ex2(Gr[i] - Gs[i]);
+  return acc;
+}
+// First token whose x is read for chunk j starting at t0: the 3 tokens before
+// t0 belong to the chunk's document when the chunk before it does.
+__device__ __forceinline__ int conv_tmin(const Ws& w, int j, int t0) {
+  return (j > 0 && w.chunk_doc[j - 1] == w.chunk_doc[j]) ? t0 - 3 : t0;
+}
+
 static_assert(offsetof(ChunkSm, x) % 16 == 0 && offsetof(ChunkSm, am) % 16 == 0 && offsetof(ChunkSm, op) % 16 == 0 &&
                   offsetof(ChunkSm, y) % 16 == 0,
               "operand tiles need 16-byte rows");
 
-__global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws w) {
-  extern __shared__ __align__(16) unsigned char smraw[];
+template <bool CONV>
+__global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws w, const __grid_constant__ TMaps tmap) {
+  extern __shared__ __align__(128) unsigned char smraw[];
   ChunkSm& sm = *reinterpret_cast<ChunkSm*>(smraw);
   const int j = (int)(blockIdx.x / (unsigned)d.H), h = (int)(blockIdx.x % (unsigned)d.H), tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_wait();     // the chunk table of the kernel before
@@ -791,16 +862,52 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
   const bf16* qraw = (const bf16*)io.q;
   const bf16* kraw = (const bf16*)io.k;
   if (warp == 0) tc::tmem_alloc(&sm.tslot, TCOLS);  // published by the first barrier below
+  // (not CONV) the chunk's raw q, k, f [C][DK] and v [C][DV] tiles arrive by tensor-map copies
+  // into the x region, which the factors overwrite only after the prologue has read them
+  bf16* const stq = sm.x;
+  bf16* const stk = sm.x + C * DK;
+  bf16* const stf = sm.x + 2 * C * DK;
+  bf16* const stv = sm.x + 3 * C * DK;
   if (tid == 0) {
     mbar_init(&sm.bar, 1);
+    if (!CONV) mbar_init(&sm.tbar, 1);
     mbar_init_fence();
+    if (!CONV) {
+      mbar_expect_tx(&sm.tbar, (uint32_t)(2 * (gdn ? 2 : 3) * C * DK + 2 * C * DV));
+      tma_load_2d(stq, &tmap.q, h * DK, t0, &sm.tbar);
+      tma_load_2d(stk, &tmap.k, h * DK, t0, &sm.tbar);
+      if (!gdn) tma_load_2d(stf, &tmap.f, h * DK, t0, &sm.tbar);
+      tma_load_2d(stv, &tmap.v, h * DV, t0, &sm.tbar);
+    }
   }
   if (L2 > 0) {
-    prefetch_rows(io.q, DK, t2, L2, H, h2);
-    prefetch_rows(io.k, DK, t2, L2, H, h2);
+    if constexpr (CONV) {  // rows of the q, k, v blocks of x
+      if ((int)threadIdx.x < L2) {
+        const size_t o2 = (size_t)(t2 + threadIdx.x) * io.ld;
+        prefetch_l2(qraw + o2 + h2 * DK);
+        prefetch_l2(kraw + o2 + h2 * DK);
+        prefetch_l2((const bf16*)io.v + o2 + h2 * DV);
+      }
+    } else {
+      prefetch_rows(io.q, DK, t2, L2, H, h2);
+      prefetch_rows(io.k, DK, t2, L2, H, h2);
+      prefetch_rows(io.v, DV, t2, L2, H, h2);
+    }
     prefetch_rows(io.f, gdn ? 1 : DK, t2, L2, H, h2);
-    prefetch_rows(io.v, DV, t2, L2, H, h2);
     prefetch_rows(io.b, 1, t2, L2, H, h2);
+  }
+  const int tmin = CONV ? conv_tmin(w, j, t0) : t0;
+  if constexpr (!CONV) {
+    __syncthreads();  // the copies' barrier is initialised before anyone waits on it
+    if (__syncthreads_or(!mbar_wait(&sm.tbar, 0))) {  // a copy did not land in bound
+      mbar_wait(&sm.tbar, 0);
+      tc::fence_before();
+      __syncthreads();
+      tc::fence_after();
+      if (warp == 0) tc::tmem_dealloc(sm.tslot, TCOLS);
+      if (tid == 0) atomicExch(w.err, -7);
+      return;
+    }
   }
 
   const Op LQ{sm.x, sm.x + 2048, DK}, LK{sm.x + 4096, sm.x + 6144, DK}, R{sm.x + 8192, sm.x + 13312, DK};
@@ -823,12 +930,20 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
   float qv[8], kv[8], gv[8], vv[16], braw = 0.f;
   if (in) {
     const size_t row = (size_t)(t0 + r) * H + h;
-    unpack8(__ldg(reinterpret_cast<const uint4*>(qraw + row * DK + 8 * q4)), qv);
-    unpack8(__ldg(reinterpret_cast<const uint4*>(kraw + row * DK + 8 * q4)), kv);
-    if (!gdn) unpack8(__ldg(reinterpret_cast<const uint4*>((const bf16*)io.f + row * DK + 8 * q4)), gv);
-    const uint4* vp = reinterpret_cast<const uint4*>((const bf16*)io.v + row * DV + 16 * q4);
-    unpack8(__ldg(vp), vv);
-    unpack8(__ldg(vp + 1), vv + 8);
+    if constexpr (CONV) {  // (v is convolved where beta v is stored, below)
+      conv_load<8>(qv, qraw + h * DK + 8 * q4, io.ld, t0 + r, tmin, io.cwq + 4 * (h * DK + 8 * q4));
+      conv_load<8>(kv, kraw + h * DK + 8 * q4, io.ld, t0 + r, tmin, io.cwk + 4 * (h * DK + 8 * q4));
+    } else {
+      unpack8(*reinterpret_cast<const uint4*>(stq + r * DK + 8 * q4), qv);
+      unpack8(*reinterpret_cast<const uint4*>(stk + r * DK + 8 * q4), kv);
+      const uint4* vp = reinterpret_cast<const uint4*>(stv + r * DV + 16 * q4);
+      unpack8(vp[0], vv);
+      unpack8(vp[1], vv + 8);
+    }
+    if (!gdn) {
+      if constexpr (CONV) unpack8(__ldg(reinterpret_cast<const uint4*>((const bf16*)io.f + row * DK + 8 * q4)), gv);
+      else unpack8(*reinterpret_cast<const uint4*>(stf + r * DK + 8 * q4), gv);
+    }
     braw = bfl(((const bf16*)io.b)[row]);
     if (gdn) {
       const float g = -a * LOG2E * softplus_fast(bfl(((const bf16*)io.f)[row]) + dtb[0]);
@@ -862,8 +977,16 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
 #pragma unroll
   for (int hv = 0; hv < 2; hv++) {  // XV = beta v (its region is free from the start)
     float xv[8];
+    if constexpr (CONV) {
+      if (in)
+        conv_load<8>(xv, (const bf16*)io.v + h * DV + 16 * q4 + 8 * hv, io.ld, t0 + r, tmin,
+                     io.cwv + 4 * (h * DV + 16 * q4 + 8 * hv));
 #pragma unroll
-    for (int e = 0; e < 8; e++) xv[e] = beta * vv[8 * hv + e];
+      for (int e = 0; e < 8; e++) xv[e] = in ? beta * xv[e] : 0.f;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; e++) xv[e] = beta * vv[8 * hv + e];
+    }
     rot_pairs(xv, q4);
     store8_rot(XKV, r, DK + 16 * q4 + 8 * hv, xv, q4);
   }
@@ -959,9 +1082,15 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
       each(acc, [&](int m, int n, float& v) {
         const int rr = 16 * bI + m, s = 16 * bI + n;
         if (s <= rr && rr < L) {
-          const bf16* xr = (isP ? qraw : kraw) + ((size_t)(t0 + rr) * H + h) * DK;
-          const bf16* ks = kraw + ((size_t)(t0 + s) * H + h) * DK;
-          v = pair_exact2(xr, isP ? sm.inq[rr] : sm.ink[rr], ks, sm.ink[s], sm.gg + rr * SQ, sm.gg + s * SQ);
+          if constexpr (CONV) {
+            v = pair_exact2_conv((isP ? qraw : kraw) + h * DK, (isP ? io.cwq : io.cwk) + 4 * h * DK,
+                                 isP ? sm.inq[rr] : sm.ink[rr], kraw + h * DK, io.cwk + 4 * h * DK, sm.ink[s], io.ld,
+                                 t0 + rr, t0 + s, tmin, sm.gg + rr * SQ, sm.gg + s * SQ);
+          } else {
+            const bf16* xr = (isP ? qraw : kraw) + ((size_t)(t0 + rr) * H + h) * DK;
+            const bf16* ks = kraw + ((size_t)(t0 + s) * H + h) * DK;
+            v = pair_exact2(xr, isP ? sm.inq[rr] : sm.ink[rr], ks, sm.ink[s], sm.gg + rr * SQ, sm.gg + s * SQ);
+          }
         }
       });
     }
@@ -1141,13 +1270,16 @@ struct FChainStage {  // one copy of this half's part of the chain block: KU, PU
 };
 // Row partials exchanged by the two column-half CTAs of a (document, head)
 // when the gated RMSNorm is fused into a chain: the peer CTA stores its
-// partials of step s into part[s & 1] of this CTA's shared memory and arrives
-// on bar[s & 1] (one arrival per storing thread).  A CTA can run at most one
-// step ahead of its peer (each step waits for the peer's partials of that
-// step), so two slots suffice.
+// partials for step s into part[s % NX] of this CTA's shared memory and
+// arrives on bar[s % NX] (one arrival per storing thread).  The forward sends
+// step s's partials before it reads step s - 1's, and a CTA's send of step m
+// only waits (through its own barrier) for the peer's partials of step m - 2:
+// while this CTA has not read step j's, the peer may have sent up to j + 3,
+// so four slots.  (The backward sends and reads the same step's.)
+constexpr int NX = 4;
 struct Xchg {
-  float2 part[2][C];
-  uint64_t bar[2];
+  float2 part[NX][C];
+  uint64_t bar[NX];
 };
 struct FChainSm {
   FChainStage st[NSTG];
@@ -1173,7 +1305,7 @@ static_assert(sizeof(FChainStage) % 16 == 0, "bulk-copy targets need 16-byte ali
 // the remaining steps instead of returning.
 template <bool NORM>
 __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws w) {
-  extern __shared__ __align__(16) unsigned char smraw[];
+  extern __shared__ __align__(128) unsigned char smraw[];
   FChainSm& sm = *reinterpret_cast<FChainSm*>(smraw);
   const int doc = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * NSC, tid = threadIdx.x, warp = tid >> 5;
   const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
@@ -1193,8 +1325,7 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
   if (tid == 0) {
     for (int s2 = 0; s2 < NSTG; s2++) mbar_init(&sm.bar[s2], 1);
     if (NORM) {
-      mbar_init(&sm.x.bar[0], 32);  // the peer's 4 output warps x 8 row-owning lanes
-      mbar_init(&sm.x.bar[1], 32);
+      for (int x2 = 0; x2 < NX; x2++) mbar_init(&sm.x.bar[x2], 32);  // the peer's 4 output warps x 8 row lanes
     }
     mbar_init_fence();
   }
@@ -1213,6 +1344,40 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
   }
   bool xfail = false;  // (output warps) the peer's partials did not arrive in bound
   bool bad = false;
+  // (NORM, output warps) the previous step's rows, finished one step late
+  float lo[4][4], lg[4][4], ls0 = 0.f, ls1 = 0.f;
+  int lL = 0, lt0 = 0, lstep = 0;
+  auto finish_prev = [&]() {
+    const int r = 16 * (warp & 3) + gq, slot = lstep % NX;
+    if (!mbar_wait_cluster(&sm.x.bar[slot], (lstep / NX) & 1)) {
+      xfail = true;  // bails at the next step's barrier (or skips the end state)
+      return;
+    }
+    const float t0s = ls0 + sm.x.part[slot][r].x, t1s = ls1 + sm.x.part[slot][r + 8].x;
+    const float r0 = 1.0f / sqrtf(t0s * (1.0f / DV) + io.neps), r1 = 1.0f / sqrtf(t1s * (1.0f / DV) + io.neps);
+    bf16* yp = (bf16*)io.y;
+    bf16* op = (bf16*)io.o;
+#pragma unroll
+    for (int jj = 0; jj < 4; jj++) {
+      const int c = col0 + 8 * jj + 2 * tq;
+      if (r < lL) {
+        const size_t i = ((size_t)(lt0 + r) * d.H + h) * DV + c;
+        *reinterpret_cast<__nv_bfloat162*>(yp + i) =
+            __floats2bfloat162_rn(lo[jj][0] * r0 * nwv[jj][0] * sigmoid_fast(lg[jj][0]),
+                                  lo[jj][1] * r0 * nwv[jj][1] * sigmoid_fast(lg[jj][1]));
+        if (op) *reinterpret_cast<__nv_bfloat162*>(op + i) = __floats2bfloat162_rn(lo[jj][0], lo[jj][1]);
+        if (io.save) *reinterpret_cast<float2*>(w.nO + i) = make_float2(lo[jj][0], lo[jj][1]);
+      }
+      if (r + 8 < lL) {
+        const size_t i = ((size_t)(lt0 + r + 8) * d.H + h) * DV + c;
+        *reinterpret_cast<__nv_bfloat162*>(yp + i) =
+            __floats2bfloat162_rn(lo[jj][2] * r1 * nwv[jj][0] * sigmoid_fast(lg[jj][2]),
+                                  lo[jj][3] * r1 * nwv[jj][1] * sigmoid_fast(lg[jj][3]));
+        if (op) *reinterpret_cast<__nv_bfloat162*>(op + i) = __floats2bfloat162_rn(lo[jj][2], lo[jj][3]);
+        if (io.save) *reinterpret_cast<float2*>(w.nO + i) = make_float2(lo[jj][2], lo[jj][3]);
+      }
+    }
+  };
   // the stage of `step`: one copy, issued by a side-group thread (not on the carry warps' path)
   const int oKU = blockIdx.z ? CB_KU1 - CB_M : 0, oPU = oKU + (CB_PU0 - CB_KU0);
   const int oM = blockIdx.z ? 0 : CB_M - CB_KU0, oQW = oM + (CB_QW - CB_M);
@@ -1220,7 +1385,7 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
     if (step < n && tid == CTH) {
       const int slot = step % NSTG;
       const int64_t ch = (int64_t)(cb + step) * H + h;
-      mbar_expect_tx(&sm.bar[slot], (uint32_t)CB_STAGE);
+      mbar_expect_tx(&sm.bar[slot], (uint32_t)(CB_STAGE + d.tx_extra));
       bulk_g2s(sm.st[slot].raw, chblk(w, ch) + (blockIdx.z ? CB_M : CB_KU0), CB_STAGE, &sm.bar[slot]);
     }
   };
@@ -1285,9 +1450,15 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
         }
       } else {
         // o of rows r = 16 wq + gq and r + 8 (columns 8 jj + 2 tq + {0, 1}); rows past the
-        // chunk end are zero (their QW and PU rows are)
-        const int r = 16 * wq + gq, slot = step & 1;
+        // chunk end are zero (their QW and PU rows are).  This step's row partials go to the
+        // peer now; the rows are finished one step later (finish_prev), when the peer's
+        // partials have had a step's time to arrive.
+        const int r = 16 * wq + gq, slot = step % NX;
         const bf16* gp = (const bf16*)io.ng;
+        if (step + 2 < n) {  // the gate rows two steps ahead into L2 (one 64-byte row segment per thread)
+          const int c2 = ci + 2, t2 = w.chunk_tok0[c2], r2 = tid - CTH;
+          if (r2 < w.chunk_len[c2]) prefetch_l2(gp + ((size_t)(t2 + r2) * H + h) * DV + col0);
+        }
         float gv[4][4];
 #pragma unroll
         for (int jj = 0; jj < 4; jj++) {
@@ -1323,36 +1494,23 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
           st_cluster_f32x2(xpart + (uint32_t)((slot * C + r + 8) * 8), s1, 0.f);
           mbar_arrive_remote(xbar + (uint32_t)(slot * 8));
         }
-        if (!mbar_wait_cluster(&sm.x.bar[slot], (step >> 1) & 1)) {
-          xfail = true;  // bails at the next step's barrier (or skips the end state)
-        } else {
-          const float t0s = s0 + sm.x.part[slot][r].x, t1s = s1 + sm.x.part[slot][r + 8].x;
-          const float r0 = 1.0f / sqrtf(t0s * (1.0f / DV) + io.neps), r1 = 1.0f / sqrtf(t1s * (1.0f / DV) + io.neps);
-          bf16* yp = (bf16*)io.y;
+        if (step > 0) finish_prev();
 #pragma unroll
-          for (int jj = 0; jj < 4; jj++) {
-            const int c = col0 + 8 * jj + 2 * tq;
-            if (r < L) {
-              const size_t i = ((size_t)(t0 + r) * H + h) * DV + c;
-              *reinterpret_cast<__nv_bfloat162*>(yp + i) =
-                  __floats2bfloat162_rn(oo[jj][0] * r0 * nwv[jj][0] * sigmoid_fast(gv[jj][0]),
-                                        oo[jj][1] * r0 * nwv[jj][1] * sigmoid_fast(gv[jj][1]));
-              if (o) *reinterpret_cast<__nv_bfloat162*>(o + i) = __floats2bfloat162_rn(oo[jj][0], oo[jj][1]);
-              if (io.save) *reinterpret_cast<float2*>(w.nO + i) = make_float2(oo[jj][0], oo[jj][1]);
-            }
-            if (r + 8 < L) {
-              const size_t i = ((size_t)(t0 + r + 8) * H + h) * DV + c;
-              *reinterpret_cast<__nv_bfloat162*>(yp + i) =
-                  __floats2bfloat162_rn(oo[jj][2] * r1 * nwv[jj][0] * sigmoid_fast(gv[jj][2]),
-                                        oo[jj][3] * r1 * nwv[jj][1] * sigmoid_fast(gv[jj][3]));
-              if (o) *reinterpret_cast<__nv_bfloat162*>(o + i) = __floats2bfloat162_rn(oo[jj][2], oo[jj][3]);
-              if (io.save) *reinterpret_cast<float2*>(w.nO + i) = make_float2(oo[jj][2], oo[jj][3]);
-            }
+        for (int jj = 0; jj < 4; jj++)
+#pragma unroll
+          for (int e = 0; e < 4; e++) {
+            lo[jj][e] = oo[jj][e];
+            lg[jj][e] = gv[jj][e];
           }
-        }
+        ls0 = s0;
+        ls1 = s1;
+        lL = L;
+        lt0 = t0;
+        lstep = step;
       }
     }
   }
+  if (NORM && !bad && n > 0 && !carry) finish_prev();  // the last step's rows
   if (NORM && __syncthreads_or(xfail) && !bad) {  // the last step's exchange ran out
     if (tid == 0) atomicExch(w.err, -7);
     bad = true;
@@ -1416,7 +1574,7 @@ static_assert(sizeof(BChainStage) % 16 == 0 && sizeof(BChainStageN) % 16 == 0 &&
 // partials are summed over the (document, head)'s rows in a fixed order.
 template <bool NORM>
 __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
-  extern __shared__ __align__(16) unsigned char smraw[];
+  extern __shared__ __align__(128) unsigned char smraw[];
   BChainSm<NORM>& sm = *reinterpret_cast<BChainSm<NORM>*>(smraw);
   const int doc = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * NSC, tid = threadIdx.x, warp = tid >> 5;
   const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
@@ -1437,8 +1595,7 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
   if (tid == 0) {
     for (int s2 = 0; s2 < NSTG; s2++) mbar_init(&sm.bar[s2], 1);
     if (NORM) {
-      mbar_init(&sm.x.bar[0], C);  // one arrival per row from the peer
-      mbar_init(&sm.x.bar[1], C);
+      for (int x2 = 0; x2 < NX; x2++) mbar_init(&sm.x.bar[x2], C);  // one arrival per row from the peer
     }
     mbar_init_fence();
   }
@@ -1498,111 +1655,140 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
   zero(acc);
   const int mI = warp & 1, jn = warp >> 1;
   bool xfail = false, bad = false;
+  // (NORM) the norm's backward for the stage of step k, in two halves around the
+  // chain's products of the step before: send sends this CTA's row partials
+  // (sum o^2, sum a o over its columns) to the peer; recv waits for the peer's
+  // and writes dO (the stage's operand tile, and global memory), dg and dw.
+  float po = 0.f, pa = 0.f;
+  // (generic lambdas: instantiated only where called, i.e. for NORM)
+  auto norm_vals = [&](auto& s, float* dyv, float* ov, float* sgv) {
+#pragma unroll
+    for (int hh = 0; hh < 2; hh++) {
+      const int o8 = nr * NSC + 16 * nh + 8 * hh;
+      unpack8(*reinterpret_cast<const uint4*>(s.dy + o8), dyv + 8 * hh);
+      unpack8(*reinterpret_cast<const uint4*>(s.g + o8), sgv + 8 * hh);
+      const float4 a = *reinterpret_cast<const float4*>(s.o + o8), b = *reinterpret_cast<const float4*>(s.o + o8 + 4);
+      ov[8 * hh] = a.x; ov[8 * hh + 1] = a.y; ov[8 * hh + 2] = a.z; ov[8 * hh + 3] = a.w;
+      ov[8 * hh + 4] = b.x; ov[8 * hh + 5] = b.y; ov[8 * hh + 6] = b.z; ov[8 * hh + 7] = b.w;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; j++) sgv[j] = sigmoid_fast(sgv[j]);  // s_j
+  };
+  auto norm_send = [&](auto k) {
+    float dyv[16], ov[16], sgv[16];
+    norm_vals(sm.st[k % NSTG], dyv, ov, sgv);
+    po = pa = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; j++) {
+      po += ov[j] * ov[j];
+      pa += dyv[j] * nwv[j] * sgv[j] * ov[j];  // a_j o_j
+    }
+    po += __shfl_xor_sync(0xffffffffu, po, 1);
+    pa += __shfl_xor_sync(0xffffffffu, pa, 1);
+    const int slot = k % NX;
+    if (nh == 0) {
+      st_cluster_f32x2(xpart + (uint32_t)((slot * C + nr) * 8), po, pa);
+      mbar_arrive_remote(xbar + (uint32_t)(slot * 8));
+    }
+  };
+  auto norm_recv = [&](auto k) {
+    auto& s = sm.st[k % NSTG];
+    const int ci = ce - 1 - k, L = w.chunk_len[ci], t0 = w.chunk_tok0[ci], slot = k % NX;
+    float dOv[16];
+    if (!mbar_wait_cluster(&sm.x.bar[slot], (k / NX) & 1)) {
+      xfail = true;  // bails at the next step's barrier
+#pragma unroll
+      for (int j = 0; j < 16; j++) dOv[j] = 0.f;
+    } else {
+      float dyv[16], ov[16], sgv[16], dgv[16];
+      norm_vals(s, dyv, ov, sgv);
+      const float2 pp = sm.x.part[slot][nr];
+      const float To = po + pp.x, Ta = pa + pp.y;
+      const float rr = 1.0f / sqrtf(To * (1.0f / DV) + io.neps);
+      const float cc = rr * rr * rr * Ta * (1.0f / DV);
+#pragma unroll
+      for (int j = 0; j < 16; j++) {
+        const float sg = sgv[j], or_ = ov[j] * rr;
+        dOv[j] = rr * dyv[j] * nwv[j] * sg - ov[j] * cc;
+        dgv[j] = dyv[j] * or_ * nwv[j] * sg * (1.f - sg);
+        dwacc[j] += dyv[j] * or_ * sg;
+      }
+      if (nr < L) {
+        const size_t gi = ((size_t)(t0 + nr) * H + h) * DV + col0 + 16 * nh;
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+          uint4 ud, ug;
+          __nv_bfloat162* d2 = reinterpret_cast<__nv_bfloat162*>(&ud);
+          __nv_bfloat162* g2 = reinterpret_cast<__nv_bfloat162*>(&ug);
+#pragma unroll
+          for (int e = 0; e < 4; e++) {
+            d2[e] = __floats2bfloat162_rn(dOv[8 * hh + 2 * e], dOv[8 * hh + 2 * e + 1]);
+            g2[e] = __floats2bfloat162_rn(dgv[8 * hh + 2 * e], dgv[8 * hh + 2 * e + 1]);
+          }
+          *reinterpret_cast<uint4*>((bf16*)io.dOw + gi + 8 * hh) = ud;
+          *reinterpret_cast<uint4*>((bf16*)io.dg + gi + 8 * hh) = ug;
+        }
+      }
+    }
+#pragma unroll
+    for (int hh = 0; hh < 2; hh++) {  // the dO operand tile (bf16, as stored for the per-chunk kernels)
+      uint4 u;
+      __nv_bfloat162* u2 = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+      for (int e = 0; e < 4; e++) u2[e] = __floats2bfloat162_rn(dOv[8 * hh + 2 * e], dOv[8 * hh + 2 * e + 1]);
+      *reinterpret_cast<uint4*>(const_cast<bf16*>(s.dO) + opix(nr, 16 * nh + 8 * hh, NSC)) = u;
+    }
+  };
+  if constexpr (NORM) {
+    if (n > 0) {  // stage 0's dO before the chain starts
+      cp_wait_all();
+      __syncthreads();
+      norm_send(0);
+      norm_recv(0);
+    }
+  }
   for (int step = 0; step < n; step++) {
     auto& s = sm.st[step % NSTG];
     const int ci = ce - 1 - step;
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(NSTG - 2));
+    if (NORM) asm volatile("cp.async.wait_group 0;\n" ::);  // the next stage's dy, g, o too
+    else asm volatile("cp.async.wait_group %0;\n" ::"n"(NSTG - 2));
     if (__syncthreads_or(!mbar_wait(&sm.bar[step % NSTG], (step / NSTG) & 1) || xfail)) {  // a wait ran out
       for (int k2 = step; k2 < n && k2 < step + NSTG - 1; k2++) mbar_wait(&sm.bar[k2 % NSTG], (k2 / NSTG) & 1);
       cp_wait_all();
       if (tid == 0) atomicExch(w.err, -7);
       bad = true;
       break;
-    }  // this step's stage and the last state update are visible
+    }  // this step's stage (and dO tile) and the last state update are visible
     prefetch(step + NSTG - 1);
+    if constexpr (NORM) {
+      if (step + NSTG < n && tid < C) {  // the rows of the stage after the one just issued, into L2
+        const int c3 = ce - 1 - (step + NSTG), t3 = w.chunk_tok0[c3];
+        if (tid < w.chunk_len[c3]) {
+          const size_t gi = ((size_t)(t3 + tid) * H + h) * DV + col0;
+          prefetch_l2((const bf16*)io.dy + gi);
+          prefetch_l2((const bf16*)io.ng + gi);
+          prefetch_l2(w.nO + gi);
+        }
+      }
+      if (step + 1 < n) norm_send(step + 1);
+    }
     const Op Mo{const_cast<bf16*>(s.M), const_cast<bf16*>(s.M) + DK * DK, DK};
     const Op QWo{const_cast<bf16*>(s.QW), const_cast<bf16*>(s.QW) + C * DK, DK};
     const Op dOo{const_cast<bf16*>(s.dO), nullptr, NSC};
     float ax[2][4];
     zero(acc);
     zero(ax);
-    if constexpr (!NORM) {
-      gemm3<1, true, true>(ax, QWo, 16 * mI, 0, dOo, 16 * jn, 0, C / 16);
-      gemm3<1, true, true>(acc, Mo, 16 * mI, 0, dS, 16 * jn, 0, DK / 16);
-      slice_to_global(w.sdS + ((int64_t)ci * H + h) * 2 * DK * DV, sm.dS, col0, threadIdx.x);
+    gemm3<1, true, true>(ax, QWo, 16 * mI, 0, dOo, 16 * jn, 0, C / 16);
+    gemm3<1, true, true>(acc, Mo, 16 * mI, 0, dS, 16 * jn, 0, DK / 16);
+    slice_to_global(w.sdS + ((int64_t)ci * H + h) * 2 * DK * DV, sm.dS, col0, threadIdx.x);
 #pragma unroll
-      for (int jj = 0; jj < 2; jj++)
+    for (int jj = 0; jj < 2; jj++)
 #pragma unroll
-        for (int e = 0; e < 4; e++) acc[jj][e] += ax[jj][e];
-      __syncthreads();  // every read of the state tile is done
-    } else {
-      const int slot = step & 1, L = w.chunk_len[ci], t0 = w.chunk_tok0[ci];
-      float dyv[16], ov[16], gv[16];
-#pragma unroll
-      for (int hh = 0; hh < 2; hh++) {
-        const int o8 = nr * NSC + 16 * nh + 8 * hh;
-        unpack8(*reinterpret_cast<const uint4*>(s.dy + o8), dyv + 8 * hh);
-        unpack8(*reinterpret_cast<const uint4*>(s.g + o8), gv + 8 * hh);
-        const float4 a = *reinterpret_cast<const float4*>(s.o + o8), b = *reinterpret_cast<const float4*>(s.o + o8 + 4);
-        ov[8 * hh] = a.x; ov[8 * hh + 1] = a.y; ov[8 * hh + 2] = a.z; ov[8 * hh + 3] = a.w;
-        ov[8 * hh + 4] = b.x; ov[8 * hh + 5] = b.y; ov[8 * hh + 6] = b.z; ov[8 * hh + 7] = b.w;
-      }
-      float po = 0.f, pa = 0.f;
-#pragma unroll
-      for (int j = 0; j < 16; j++) {
-        gv[j] = sigmoid_fast(gv[j]);           // s_j
-        const float a = dyv[j] * nwv[j] * gv[j];  // a_j
-        po += ov[j] * ov[j];
-        pa += a * ov[j];
-      }
-      po += __shfl_xor_sync(0xffffffffu, po, 1);
-      pa += __shfl_xor_sync(0xffffffffu, pa, 1);
-      if (nh == 0) {
-        st_cluster_f32x2(xpart + (uint32_t)((slot * C + nr) * 8), po, pa);
-        mbar_arrive_remote(xbar + (uint32_t)(slot * 8));
-      }
-      gemm3<1, true, true>(acc, Mo, 16 * mI, 0, dS, 16 * jn, 0, DK / 16);  // overlaps the exchange
-      slice_to_global(w.sdS + ((int64_t)ci * H + h) * 2 * DK * DV, sm.dS, col0, threadIdx.x);
-      float dOv[16];
-      if (!mbar_wait_cluster(&sm.x.bar[slot], (step >> 1) & 1)) {
-        xfail = true;  // bails at the next step's barrier
-#pragma unroll
-        for (int j = 0; j < 16; j++) dOv[j] = 0.f;
-      } else {
-        const float2 pp = sm.x.part[slot][nr];
-        const float To = po + pp.x, Ta = pa + pp.y;
-        const float rr = 1.0f / sqrtf(To * (1.0f / DV) + io.neps);
-        const float cc = rr * rr * rr * Ta * (1.0f / DV);
-        float dgv[16];
-#pragma unroll
-        for (int j = 0; j < 16; j++) {
-          const float sg = gv[j], or_ = ov[j] * rr;
-          dOv[j] = rr * dyv[j] * nwv[j] * sg - ov[j] * cc;
-          dgv[j] = dyv[j] * or_ * nwv[j] * sg * (1.f - sg);
-          dwacc[j] += dyv[j] * or_ * sg;
-        }
-        if (nr < L) {
-          const size_t gi = ((size_t)(t0 + nr) * H + h) * DV + col0 + 16 * nh;
-#pragma unroll
-          for (int hh = 0; hh < 2; hh++) {
-            uint4 ud, ug;
-            __nv_bfloat162* d2 = reinterpret_cast<__nv_bfloat162*>(&ud);
-            __nv_bfloat162* g2 = reinterpret_cast<__nv_bfloat162*>(&ug);
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-              d2[e] = __floats2bfloat162_rn(dOv[8 * hh + 2 * e], dOv[8 * hh + 2 * e + 1]);
-              g2[e] = __floats2bfloat162_rn(dgv[8 * hh + 2 * e], dgv[8 * hh + 2 * e + 1]);
-            }
-            *reinterpret_cast<uint4*>((bf16*)io.dOw + gi + 8 * hh) = ud;
-            *reinterpret_cast<uint4*>((bf16*)io.dg + gi + 8 * hh) = ug;
-          }
-        }
-      }
-#pragma unroll
-      for (int hh = 0; hh < 2; hh++) {  // the dO operand tile (bf16, as stored for the per-chunk kernels)
-        uint4 u;
-        __nv_bfloat162* u2 = reinterpret_cast<__nv_bfloat162*>(&u);
-#pragma unroll
-        for (int e = 0; e < 4; e++) u2[e] = __floats2bfloat162_rn(dOv[8 * hh + 2 * e], dOv[8 * hh + 2 * e + 1]);
-        *reinterpret_cast<uint4*>(const_cast<bf16*>(s.dO) + opix(nr, 16 * nh + 8 * hh, NSC)) = u;
-      }
-      __syncthreads();  // the dO tile is complete; every read of the state tile is done
-      gemm3<1, true, true>(ax, QWo, 16 * mI, 0, dOo, 16 * jn, 0, C / 16);
-#pragma unroll
-      for (int jj = 0; jj < 2; jj++)
-#pragma unroll
-        for (int e = 0; e < 4; e++) acc[jj][e] += ax[jj][e];
+      for (int e = 0; e < 4; e++) acc[jj][e] += ax[jj][e];
+    if constexpr (NORM) {
+      if (step + 1 < n) norm_recv(step + 1);  // the exchange overlapped the products above
     }
+    __syncthreads();  // every read of the state tile is done (and the next stage's dO tile written)
 #pragma unroll
     for (int jj = 0; jj < 2; jj++)
 #pragma unroll
@@ -1709,8 +1895,9 @@ struct GradSm {
 };
 static_assert(offsetof(GradSm, rk) % 16 == 0 && offsetof(GradSm, gg) % 16 == 0, "vector-accessed arrays");
 
+template <bool CONV>
 __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w) {
-  extern __shared__ __align__(16) unsigned char smraw[];
+  extern __shared__ __align__(128) unsigned char smraw[];
   GradSm& sm = *reinterpret_cast<GradSm*>(smraw);
   const int j = (int)(blockIdx.x / (unsigned)d.H), h = (int)(blockIdx.x % (unsigned)d.H), tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
@@ -1742,12 +1929,12 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   const Op U2{wk, wk + 4096, DV}, W2{wk + 8192, wk + 10240, DK};
   bf16* fst = wk + 32768;
 
-  // ---- group 1: raw k, f;  group 2: dO, S, dS', P, W, U, T
+  // ---- group 1: raw k, f;  group 2: dO, S, dS', P, W, U, T  (CONV: k comes from the convolution below)
   for (int idx = tid; idx < C * 4; idx += NTH) {
     const int r = idx >> 2, p = idx & 3;
     if (r < L) {
       const size_t g = ((size_t)(t0 + r) * H + h) * DK + 8 * p;
-      cp16(sm.rk + r * DK + 8 * p, (const bf16*)io.k + g);
+      if (!CONV) cp16(sm.rk + r * DK + 8 * p, (const bf16*)io.k + g);
       if (!gdn) cp16(fst + r * DK + 8 * p, (const bf16*)io.f + g);
     }
   }
@@ -1781,14 +1968,27 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   const int r = tid >> 2, q4 = tid & 3;
   const bool in = r < L;
   uint4 vraw[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+  float vcv[CONV ? 16 : 1];  // CONV: this thread's v after the convolution
+  float kcv[CONV ? 8 : 1];   // and its k
   float braw = 0.f, fs = 0.f;  // fs: the scalar gate input of this row
   if (in) {
     const size_t row = (size_t)(t0 + r) * H + h;
-    const uint4* vp = reinterpret_cast<const uint4*>((const bf16*)io.v + row * DV + 16 * q4);
-    vraw[0] = __ldg(vp);
-    vraw[1] = __ldg(vp + 1);
+    if constexpr (CONV) {
+      const int tmin = conv_tmin(w, j, t0);
+      conv_load<16>(vcv, (const bf16*)io.v + h * DV + 16 * q4, io.ld, t0 + r, tmin, io.cwv + 4 * (h * DV + 16 * q4));
+      conv_load<8>(kcv, (const bf16*)io.k + h * DK + 8 * q4, io.ld, t0 + r, tmin, io.cwk + 4 * (h * DK + 8 * q4));
+    } else {
+      const uint4* vp = reinterpret_cast<const uint4*>((const bf16*)io.v + row * DV + 16 * q4);
+      vraw[0] = __ldg(vp);
+      vraw[1] = __ldg(vp + 1);
+    }
     braw = bfl(((const bf16*)io.b)[row]);
     if (gdn) fs = bfl(((const bf16*)io.f)[row]);
+  } else if constexpr (CONV) {
+#pragma unroll
+    for (int e = 0; e < 16; e++) vcv[e] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; e++) kcv[e] = 0.f;
   }
   asm volatile("cp.async.wait_group 1;\n" ::);
   tc::fence_before();
@@ -1797,7 +1997,12 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   const uint32_t tb = sm.tslot;
   float kv[8], gv[8];
   if (in) {
-    unpack8(*reinterpret_cast<const uint4*>(sm.rk + r * DK + 8 * q4), kv);
+    if constexpr (CONV) {
+#pragma unroll
+      for (int e = 0; e < 8; e++) kv[e] = kcv[e];
+    } else {
+      unpack8(*reinterpret_cast<const uint4*>(sm.rk + r * DK + 8 * q4), kv);
+    }
     if (gdn) {
       const float g = -a * LOG2E * softplus_fast(fs + dtv[0]);
 #pragma unroll
@@ -1997,9 +2202,14 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
       for (int hh = 0; hh < 2; hh++) {
         const int rr = 16 * I + gq + 8 * hh, col = 32 * hk + 8 * jt + 2 * tq;
         op_store2(YU, rr, col, yu[jt][2 * hh], yu[jt][2 * hh + 1]);
-        if (rr < L)
-          *reinterpret_cast<__nv_bfloat162*>(dvo + ((size_t)(t0 + rr) * H + h) * DV + col) =
-              __floats2bfloat162_rn(sm.bet[rr] * yu[jt][2 * hh], sm.bet[rr] * yu[jt][2 * hh + 1]);
+        if (rr < L) {
+          if constexpr (CONV)  // fp32 gradient of the convolution's v output
+            *reinterpret_cast<float2*>((float*)io.dv + (size_t)(t0 + rr) * io.ld + h * DV + col) =
+                make_float2(sm.bet[rr] * yu[jt][2 * hh], sm.bet[rr] * yu[jt][2 * hh + 1]);
+          else
+            *reinterpret_cast<__nv_bfloat162*>(dvo + ((size_t)(t0 + rr) * H + h) * DV + col) =
+                __floats2bfloat162_rn(sm.bet[rr] * yu[jt][2 * hh], sm.bet[rr] * yu[jt][2 * hh + 1]);
+        }
       }
 #pragma unroll
     for (int jt = 0; jt < 2; jt++)
@@ -2031,8 +2241,16 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
   });
   {  // bf16 pairs read in the rotated order of store8_rot: the 32 lanes hit 32 banks
     float va[8], vb[8];
-    unpack8(vraw[0], va);
-    unpack8(vraw[1], vb);
+    if constexpr (CONV) {
+#pragma unroll
+      for (int e = 0; e < 8; e++) {
+        va[e] = vcv[e];
+        vb[e] = vcv[8 + e];
+      }
+    } else {
+      unpack8(vraw[0], va);
+      unpack8(vraw[1], vb);
+    }
     rot_pairs(va, q4);
     rot_pairs(vb, q4);
     rot_pairs(xkg, q4);
@@ -2107,11 +2325,16 @@ __global__ void __launch_bounds__(NTH, 2) bwd_grad_kernel(Dims d, BwdIO io, Ws w
 // dq^ / dk^ / dG terms, the reverse cumulative sum over the chunk into dg,
 // the gate backward (df and the per-chunk partials of dA_log and dt_bias)
 // and the L2-norm backward (dq, dk).
+// CONV: q and k are the convolution's fp32 outputs (recomputed from x as the
+// forward computed them), kept in fp32 so that the backward sees their bits.
+template <bool CONV>
 struct GateSm {
+  typedef typename std::conditional<CONV, float, bf16>::type QK;
   float gg[C * SQ];           // G2 = G log2(e); then dq^
   float dp[NBLK * 16 * PB];   // dP' lower blocks; then dk^
   float ma[NBLK * 16 * PB];   // MA lower blocks; then dG - kdt and its suffix sums
-  bf16 rq[C * DK], rk[C * DK], rf[C * DK];
+  QK rq[C * DK], rk[C * DK];
+  bf16 rf[C * DK];
   float inq[C], ink[C];
   float gam[DK], dgam[DK];
   float tot[NW * DK], ks[4 * DK], part[NW * DK], red[NW];
@@ -2120,20 +2343,35 @@ struct GateSm {
   // row's 16-row block I (each at most |q^|, |k^|)
   float kl[C * DK], qf[C * DK], kf[C * DK];
   int spanok[4];
-  uint64_t bar;  // bulk-load completion of dP' and MA
+  uint64_t bar;   // bulk-load completion of dP' and MA
+  uint64_t tbar;  // (not CONV) the raw q, k, f tiles' tensor-map copies
 };
 // Element (r, c) of a swizzled [C][DK] tile: the four rows r = 0..3 (mod 4) of
 // a fragment load put their eight columns in different bank groups.
 __device__ __forceinline__ int tix(int r, int c) { return r * DK + (c ^ ((r & 3) << 3)); }
 
-static_assert(offsetof(GateSm, rq) % 16 == 0 && offsetof(GateSm, rk) % 16 == 0 && offsetof(GateSm, rf) % 16 == 0 &&
-                  offsetof(GateSm, dp) % 16 == 0 && offsetof(GateSm, ma) % 16 == 0 && offsetof(GateSm, kl) % 16 == 0 &&
-                  offsetof(GateSm, qf) % 16 == 0 && offsetof(GateSm, kf) % 16 == 0,
+static_assert(offsetof(GateSm<false>, rq) % 16 == 0 && offsetof(GateSm<false>, rk) % 16 == 0 &&
+                  offsetof(GateSm<false>, rf) % 16 == 0 && offsetof(GateSm<false>, dp) % 16 == 0 &&
+                  offsetof(GateSm<false>, ma) % 16 == 0 && offsetof(GateSm<false>, kl) % 16 == 0 &&
+                  offsetof(GateSm<false>, qf) % 16 == 0 && offsetof(GateSm<false>, kf) % 16 == 0 &&
+                  offsetof(GateSm<true>, rk) % 16 == 0 && offsetof(GateSm<true>, rf) % 16 == 0 &&
+                  offsetof(GateSm<true>, kl) % 16 == 0 && offsetof(GateSm<true>, qf) % 16 == 0 &&
+                  offsetof(GateSm<true>, kf) % 16 == 0,
               "vector-accessed arrays");
+__device__ __forceinline__ float fl(float x) { return x; }
+__device__ __forceinline__ float fl(bf16 x) { return bfl(x); }
+__device__ __forceinline__ void load8(const bf16* p, float* v) { unpack8(*reinterpret_cast<const uint4*>(p), v); }
+__device__ __forceinline__ void load8(const float* p, float* v) {
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
 
-__global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w) {
-  extern __shared__ __align__(16) unsigned char smraw[];
-  GateSm& sm = *reinterpret_cast<GateSm*>(smraw);
+template <bool CONV>
+__global__ void __launch_bounds__(NTH, CONV ? 2 : 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w,
+                                                                    const __grid_constant__ TMaps tmap) {
+  extern __shared__ __align__(128) unsigned char smraw[];
+  GateSm<CONV>& sm = *reinterpret_cast<GateSm<CONV>*>(smraw);
   const int j = (int)(blockIdx.x / (unsigned)d.H), h = (int)(blockIdx.x % (unsigned)d.H), tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
   const bool gdn = d.gate != 0;
@@ -2156,21 +2394,43 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
   const bf16* fsc = (const bf16*)io.f + h;  // scalar gate: f of this head, stride H
 
   // ---- group 1: raw q, k, f (rows past the chunk end zeroed);  group 2: dP', MA
+  //      (CONV: q and k from the convolution, each thread its own row r = tid / 4, channels 8 (tid % 4) ..)
   for (int idx = tid; idx < C * 4; idx += NTH) {
     const int r = idx >> 2, p = idx & 3, o = r * DK + 8 * p;
     if (r < L) {
       const size_t g = ((size_t)(t0 + r) * H + h) * DK + 8 * p;
-      cp16(sm.rq + o, (const bf16*)io.q + g);
-      cp16(sm.rk + o, (const bf16*)io.k + g);
-      if (!gdn) cp16(sm.rf + o, (const bf16*)io.f + g);
-    } else {
+      if constexpr (CONV) {
+        const int tmin = conv_tmin(w, j, t0);
+        float cq[8], ck[8];
+        conv_load<8>(cq, (const bf16*)io.q + h * DK + 8 * p, io.ld, t0 + r, tmin, io.cwq + 4 * (h * DK + 8 * p));
+        conv_load<8>(ck, (const bf16*)io.k + h * DK + 8 * p, io.ld, t0 + r, tmin, io.cwk + 4 * (h * DK + 8 * p));
+        float4* q4p = reinterpret_cast<float4*>(reinterpret_cast<float*>(sm.rq) + o);
+        float4* k4p = reinterpret_cast<float4*>(reinterpret_cast<float*>(sm.rk) + o);
+        q4p[0] = make_float4(cq[0], cq[1], cq[2], cq[3]);
+        q4p[1] = make_float4(cq[4], cq[5], cq[6], cq[7]);
+        k4p[0] = make_float4(ck[0], ck[1], ck[2], ck[3]);
+        k4p[1] = make_float4(ck[4], ck[5], ck[6], ck[7]);
+        if (!gdn) cp16(sm.rf + o, (const bf16*)io.f + g);
+      }  // (not CONV: tensor-map copies below)
+    } else if (CONV) {
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      *reinterpret_cast<uint4*>(sm.rq + o) = z;
-      *reinterpret_cast<uint4*>(sm.rk + o) = z;
+#pragma unroll
+      for (int u = 0; u < (CONV ? 2 : 1); u++) {
+        reinterpret_cast<uint4*>(sm.rq + o)[u] = z;
+        reinterpret_cast<uint4*>(sm.rk + o)[u] = z;
+      }
       *reinterpret_cast<uint4*>(sm.rf + o) = z;
     }
   }
   cp_commit();
+  if (!CONV && tid == 0) {  // the raw q, k (and f) tiles [C][DK], rows past the chunk end zeroed below
+    mbar_init(&sm.tbar, 1);
+    mbar_init_fence();
+    mbar_expect_tx(&sm.tbar, (uint32_t)(2 * (gdn ? 2 : 3) * C * DK));
+    tma_load_2d(sm.rq, &tmap.q, h * DK, t0, &sm.tbar);
+    tma_load_2d(sm.rk, &tmap.k, h * DK, t0, &sm.tbar);
+    if (!gdn) tma_load_2d(sm.rf, &tmap.f, h * DK, t0, &sm.tbar);
+  }
   pdl_wait();  // every read below of bwd_grad's hand-over (the kernel before) follows this
   if (tid == 0) {
     mbar_init(&sm.bar, 1);
@@ -2183,13 +2443,29 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
   if (tid < 4) sm.spanok[tid] = 1;
   cp_wait_all();
   __syncthreads();
+  if constexpr (!CONV) {
+    if (__syncthreads_or(!mbar_wait(&sm.tbar, 0))) {  // a copy did not land in bound
+      mbar_wait(&sm.tbar, 0);
+      mbar_wait(&sm.bar, 0);
+      if (tid == 0) atomicExch(w.err, -7);
+      return;
+    }
+    const int r = tid >> 2, o = r * DK + 8 * (tid & 3);  // rows past the chunk end: another document's, or zero
+    if (r >= L) {
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(sm.rq + o) = z;
+      *reinterpret_cast<uint4*>(sm.rk + o) = z;
+      *reinterpret_cast<uint4*>(sm.rf + o) = z;
+    }
+    __syncthreads();
+  }
 
   // ---- q^, k^ norms and G (thread: row tid / 4, key channels 8 (tid % 4) ..)
   {
     const int r = tid >> 2, q4 = tid & 3;
     float qv[8], kv[8], gv[8];
-    unpack8(*reinterpret_cast<const uint4*>(sm.rq + r * DK + 8 * q4), qv);
-    unpack8(*reinterpret_cast<const uint4*>(sm.rk + r * DK + 8 * q4), kv);
+    load8(sm.rq + r * DK + 8 * q4, qv);
+    load8(sm.rk + r * DK + 8 * q4, kv);
     unpack8(*reinterpret_cast<const uint4*>(sm.rf + r * DK + 8 * q4), gv);
     const bool in = r < L;
     float sq = 0.f, sk = 0.f;
@@ -2336,7 +2612,7 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
         if (!ok) {  // exact diagonal-block terms (rows past the chunk end are zero)
           for (int s = 16 * I; s < 16 * I + 16 && s < L; s++) {
             const int n = s - 16 * I;
-            const float ks = bfl(sm.rk[s * DK + i]) * sm.ink[s], qs = bfl(sm.rq[s * DK + i]) * sm.inq[s];
+            const float ks = fl(sm.rk[s * DK + i]) * sm.ink[s], qs = fl(sm.rq[s * DK + i]) * sm.inq[s];
             if (s <= rr) {
               const float ex = ex2(G - sm.gg[s * SQ + i]);
               pr += DPd[m * PB + n] * ks * ex;
@@ -2348,7 +2624,7 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
             }
           }
         }
-        const float q = bfl(sm.rq[rr * DK + i]) * sm.inq[rr], k = bfl(sm.rk[rr * DK + i]) * sm.ink[rr];
+        const float q = fl(sm.rq[rr * DK + i]) * sm.inq[rr], k = fl(sm.rk[rr * DK + i]) * sm.ink[rr];
         const float Gm = ex2(G), kdf = ex2(sm.gg[(L - 1) * SQ + i] - G);
         const float kdt = dKD[jj][e] * k * kdf;
         dqh[jj][e] = pr + dQG[jj][e] * Gm;
@@ -2460,8 +2736,8 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
   {
     const int r = tid >> 2, q4 = tid & 3;
     float qv[8], kv[8], dqv[8], dkv[8], pq = 0.f, pk = 0.f;
-    unpack8(*reinterpret_cast<const uint4*>(sm.rq + r * DK + 8 * q4), qv);
-    unpack8(*reinterpret_cast<const uint4*>(sm.rk + r * DK + 8 * q4), kv);
+    load8(sm.rq + r * DK + 8 * q4, qv);
+    load8(sm.rk + r * DK + 8 * q4, kv);
     const float iq = sm.inq[r], ik = sm.ink[r];
 #pragma unroll
     for (int e = 0; e < 8; e++) {
@@ -2477,17 +2753,35 @@ __global__ void __launch_bounds__(NTH, 3) bwd_gate_kernel(Dims d, BwdIO io, Ws w
     pk += __shfl_xor_sync(0xffffffffu, pk, 1);
     pk += __shfl_xor_sync(0xffffffffu, pk, 2);
     if (r < L) {
-      uint4 uq, uk;
-      __nv_bfloat162* pq2 = reinterpret_cast<__nv_bfloat162*>(&uq);
-      __nv_bfloat162* pk2 = reinterpret_cast<__nv_bfloat162*>(&uk);
+      if constexpr (CONV) {  // fp32 gradients of the convolution's q and k outputs
+        float oq[8], ok[8];
 #pragma unroll
-      for (int e = 0; e < 4; e++) {
-        pq2[e] = __floats2bfloat162_rn((dqv[2 * e] - qv[2 * e] * pq) * iq, (dqv[2 * e + 1] - qv[2 * e + 1] * pq) * iq);
-        pk2[e] = __floats2bfloat162_rn((dkv[2 * e] - kv[2 * e] * pk) * ik, (dkv[2 * e + 1] - kv[2 * e + 1] * pk) * ik);
+        for (int e = 0; e < 8; e++) {
+          oq[e] = (dqv[e] - qv[e] * pq) * iq;
+          ok[e] = (dkv[e] - kv[e] * pk) * ik;
+        }
+        const size_t off = (size_t)(t0 + r) * io.ld + h * DK + 8 * q4;
+        float4* pq4 = reinterpret_cast<float4*>((float*)io.dq + off);
+        float4* pk4 = reinterpret_cast<float4*>((float*)io.dk + off);
+        pq4[0] = make_float4(oq[0], oq[1], oq[2], oq[3]);
+        pq4[1] = make_float4(oq[4], oq[5], oq[6], oq[7]);
+        pk4[0] = make_float4(ok[0], ok[1], ok[2], ok[3]);
+        pk4[1] = make_float4(ok[4], ok[5], ok[6], ok[7]);
+      } else {
+        uint4 uq, uk;
+        __nv_bfloat162* pq2 = reinterpret_cast<__nv_bfloat162*>(&uq);
+        __nv_bfloat162* pk2 = reinterpret_cast<__nv_bfloat162*>(&uk);
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          pq2[e] =
+              __floats2bfloat162_rn((dqv[2 * e] - qv[2 * e] * pq) * iq, (dqv[2 * e + 1] - qv[2 * e + 1] * pq) * iq);
+          pk2[e] =
+              __floats2bfloat162_rn((dkv[2 * e] - kv[2 * e] * pk) * ik, (dkv[2 * e + 1] - kv[2 * e + 1] * pk) * ik);
+        }
+        const size_t off = ((size_t)(t0 + r) * H + h) * DK + 8 * q4;
+        *reinterpret_cast<uint4*>((bf16*)io.dq + off) = uq;
+        *reinterpret_cast<uint4*>((bf16*)io.dk + off) = uk;
       }
-      const size_t off = ((size_t)(t0 + r) * H + h) * DK + 8 * q4;
-      *reinterpret_cast<uint4*>((bf16*)io.dq + off) = uq;
-      *reinterpret_cast<uint4*>((bf16*)io.dk + off) = uk;
     }
   }
 }
@@ -2499,9 +2793,35 @@ static_assert(sizeof(fast::ChunkSm) <= 113 * 1024, "per-chunk forward must fit t
 
 static_assert(sizeof(fast::GradSm) <= 112 * 1024, "chunk-gradient kernel must fit two CTAs per SM");
 static_assert(sizeof(fast::BChainSm<true>) <= 113 * 1024, "fused-norm reverse chain must fit two CTAs per SM");
-static_assert(sizeof(fast::GateSm) <= 75 * 1024, "gate kernel must fit three CTAs per SM");
+static_assert(sizeof(fast::GateSm<false>) <= 75 * 1024, "gate kernel must fit three CTAs per SM");
+static_assert(sizeof(fast::GateSm<true>) <= 113 * 1024, "gate kernel (fused convolution) must fit two CTAs per SM");
 
 bool fast_path(int dtype, int dk, int dv) { return dtype == 0 && dk == fast::DK && dv == fast::DV; }
+
+bool encode_tmaps(TMaps* tm, const void* q, const void* k, const void* v, const void* f, int Ntok, int H, int dk,
+                  int dv, bool channel_gate) {
+  static PFN_cuTensorMapEncodeTiled_v12000 enc = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr) !=
+            cudaSuccess ||
+        qr != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }();
+  if (!enc) return false;
+  auto one = [&](CUtensorMap* m, const void* base, int dh) {  // [Ntok][H dh] bf16, box dh x C
+    const cuuint64_t dims[2] = {(cuuint64_t)H * dh, (cuuint64_t)Ntok};
+    const cuuint64_t strides[1] = {(cuuint64_t)H * dh * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)dh, (cuuint32_t)C};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  *tm = TMaps{};
+  return one(&tm->q, q, dk) && one(&tm->k, k, dk) && one(&tm->v, v, dv) && (!channel_gate || one(&tm->f, f, dk));
+}
 
 // CTAs of the per-chunk kernels in flight on the current device (two per SM).
 static int wave_ctas() {
@@ -2530,14 +2850,22 @@ cudaError_t launch_fast_fwd(const Dims& d0, const FwdIO& io, const Ws& w, cudaSt
     return cudaGetLastError();
   }
   const size_t s1 = sizeof(fast::ChunkSm), s2 = sizeof(fast::FChainSm);
-  e = cudaFuncSetAttribute(fast::fwd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
+  e = cudaFuncSetAttribute(fast::fwd_chunk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fast::fwd_chunk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(fast::fwd_state_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(fast::fwd_state_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
   if (e != cudaSuccess) return e;
+  TMaps tm = {};
+  if (!d.conv && !encode_tmaps(&tm, io.q, io.k, io.v, io.f, d.Ntok, d.H, fast::DK, fast::DV, d.gate == 0))
+    return cudaErrorInvalidValue;
   prof_begin(K_FWD_CHUNK, st);
-  e = launch_pdl(fast::fwd_chunk_kernel, dim3(d.nc_max * d.H), dim3(fast::NTH), s1, st, d, io, w);
+  if (d.conv)
+    e = launch_pdl(fast::fwd_chunk_kernel<true>, dim3(d.nc_max * d.H), dim3(fast::NTH), s1, st, d, io, w, tm);
+  else
+    e = launch_pdl(fast::fwd_chunk_kernel<false>, dim3(d.nc_max * d.H), dim3(fast::NTH), s1, st, d, io, w, tm);
   prof_end(K_FWD_CHUNK, st);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -2558,15 +2886,21 @@ cudaError_t launch_fast_bwd(const Dims& d0, const BwdIO& io, const Ws& w, cudaSt
   Dims d = d0;
   d.ahead = 0;  // the backward's chunk kernels prefetch nothing (measured: the L2 prefetch of the next wave slowed them)
   const size_t sc = sizeof(fast::BChainSm<false>), scn = sizeof(fast::BChainSm<true>), s1 = sizeof(fast::GradSm),
-               s2 = sizeof(fast::GateSm);
+               s2 = d.conv ? sizeof(fast::GateSm<true>) : sizeof(fast::GateSm<false>);
   cudaError_t e =
       cudaFuncSetAttribute(fast::bwd_scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(fast::bwd_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scn);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(fast::bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
+    e = cudaFuncSetAttribute(fast::bwd_grad_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(fast::bwd_gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
+    e = cudaFuncSetAttribute(fast::bwd_grad_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fast::bwd_gate_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(fast::GateSm<false>));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fast::bwd_gate_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(fast::GateSm<true>));
   if (e != cudaSuccess) return e;
   const dim3 grid(d.n_docs, d.H, fast::DV / fast::NSC);
   if (d.norm) {  // the two column halves of a (document, head) as one cluster
@@ -2581,12 +2915,17 @@ cudaError_t launch_fast_bwd(const Dims& d0, const BwdIO& io, const Ws& w, cudaSt
   }
   if (e != cudaSuccess) return e;
   prof_begin(K_BWD_GRAD, st);
-  e = launch_pdl(fast::bwd_grad_kernel, dim3(d.nc_max * d.H), dim3(fast::NTH), s1, st, d, io, w);
+  e = d.conv ? launch_pdl(fast::bwd_grad_kernel<true>, dim3(d.nc_max * d.H), dim3(fast::NTH), s1, st, d, io, w)
+             : launch_pdl(fast::bwd_grad_kernel<false>, dim3(d.nc_max * d.H), dim3(fast::NTH), s1, st, d, io, w);
   prof_end(K_BWD_GRAD, st);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prof_begin(K_BWD_GATE, st);
-  e = launch_pdl(fast::bwd_gate_kernel, dim3(d.nc_max * d.H), dim3(fast::NTH), s2, st, d, io, w);
+  TMaps tm = {};
+  if (!d.conv && !encode_tmaps(&tm, io.q, io.k, io.v, io.f, d.Ntok, d.H, fast::DK, fast::DV, d.gate == 0))
+    return cudaErrorInvalidValue;
+  e = d.conv ? launch_pdl(fast::bwd_gate_kernel<true>, dim3(d.nc_max * d.H), dim3(fast::NTH), s2, st, d, io, w, tm)
+             : launch_pdl(fast::bwd_gate_kernel<false>, dim3(d.nc_max * d.H), dim3(fast::NTH), s2, st, d, io, w, tm);
   prof_end(K_BWD_GATE, st);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -1,6 +1,7 @@
 // Internal declarations shared by the CUDA translation units of the KDA
 // library (not part of the C ABI).
 #pragma once
+#include <cuda.h>  // CUtensorMap (the maps are encoded through the runtime's driver entry point)
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -78,6 +79,9 @@ struct Ws {
   float* nO;   // [Ntok][H][dv] the pre-norm KDA output o in fp32
   float* pdw;  // [n_docs * H][dv] per (document, head) partial of the gated norm's dw (fused backward)
   float* nrm;  // other head shapes: the standalone norm backward's per-CTA dw partials
+  // the fused convolution's backward (workspace for_backward = 3)
+  float* cg;     // [Ntok][C] fp32 gradients of the convolution's outputs (q | k | v blocks)
+  float* cpart;  // its weight-gradient partials
   float* scr;  // [ch][scr_per_ch] backward scratch
   int64_t scr_per_ch;
 };
@@ -91,6 +95,9 @@ struct Dims {
   int32_t ahead; // CTAs in flight (one wave) of the per-chunk tensor-core kernels: their L2 prefetch distance
   int32_t gate;  // 0: per key channel (KDA); 1: scalar per head (GDN), f [Ntok, H], dt_bias [H]
   int32_t norm;  // the gated RMSNorm epilogue is fused into the chains (tensor-core path)
+  int32_t conv;  // the short convolution is fused into the per-chunk kernels' prologue (tensor-core path)
+  int32_t tx_extra;  // failure-detection test hook (kda_test_stage_timeout): bytes the forward chain's stage
+                     // barriers expect beyond what their copies deliver; 0 outside that test
 };
 
 // Backward kernels refuse a workspace that no saving forward of the same
@@ -114,6 +121,12 @@ struct FwdIO {
   const float* nw;  // weight w [dv]
   float neps;
   void* y;          // [Ntok, H, dv]
+  // fused short convolution (Dims::conv): q, k, v point at the q, k, v channel
+  // blocks of the pre-convolution projection x [Ntok, C] (C = H (2 dk + dv)),
+  // whose rows are ld elements apart, and cwq / cwk / cwv at the blocks' taps
+  // ([channels][4] fp32); the kernels apply the convolution and silu on load
+  int ld;
+  const float *cwq, *cwk, *cwv;
 };
 
 struct BwdIO {
@@ -134,7 +147,23 @@ struct BwdIO {
   void* dOw;
   void* dg;
   float* dw;
+  // fused short convolution (Dims::conv): inputs as in FwdIO; dq, dk, dv are
+  // then the fp32 gradients of the convolution's outputs, rows ld apart (the
+  // q, k, v blocks of a [Ntok, C] buffer the convolution's backward reads)
+  int ld;
+  const float *cwq, *cwk, *cwv;
 };
+
+// TMA tensor maps of the raw per-token inputs, each viewed as a 2-D [Ntok][H d]
+// bf16 tensor with a box of one head's d channels x C tokens (encoded on the
+// host per call; unused fields are zero).
+struct TMaps {
+  CUtensorMap q, k, v, f;
+};
+// Encodes the maps for bf16 q, k, f [Ntok, H, dk] and v [Ntok, H, dv]
+// (f only for the per-channel gate); false if the driver refuses.
+bool encode_tmaps(TMaps* tm, const void* q, const void* k, const void* v, const void* f, int Ntok, int H, int dk,
+                  int dv, bool channel_gate);
 
 // Launch wrappers (return cudaGetLastError of their launches).
 // Launches kernel k with the programmatic-stream-serialization attribute (see pdl_wait).
@@ -185,6 +214,12 @@ bool fast_path(int dtype, int dk, int dv);
 // kda_fwd_noalloc); else the per-chunk kernel and the state chain.
 cudaError_t launch_fast_fwd(const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st, bool fused);
 cudaError_t launch_fast_bwd(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st);
+
+// The fused convolution's backward: dx and dw from x and the fp32 gradients of
+// the convolution's outputs (documents: cu, or rows of row_len tokens).
+cudaError_t launch_conv_bwd_fused(int64_t n_tok, int C, const int32_t* cu, int n_docs, int64_t row_len,
+                                  const __nv_bfloat16* x, const float* w, const float* dy, __nv_bfloat16* dx,
+                                  float* part, float* dw, cudaStream_t st);
 
 // out[c] = sum over the rows of a [nrows][ncols] fp32 array, in a fixed order.
 cudaError_t launch_sum_rows(const float* part, int nrows, int ncols, float* out, cudaStream_t st);

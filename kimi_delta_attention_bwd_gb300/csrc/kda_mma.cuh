@@ -291,17 +291,35 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
-// Polls phase `parity` of the barrier; gives up after a bounded number of
-// polls and returns false (the caller flags the error).
+// The GPU's nanosecond clock.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+  return t;
+}
+// Bound of every wait on an mbarrier: a phase that has not completed this long
+// after the wait began never will (the copies and arrivals it waits for take
+// microseconds), so the wait gives up and the kernel flags the error.
+constexpr uint64_t WAIT_LIMIT_NS = 250000000ull;  // 0.25 s
+__device__ __forceinline__ uint32_t mbar_try(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done;
+}
+// Polls phase `parity` of the barrier; gives up WAIT_LIMIT_NS after the first
+// unsuccessful poll and returns false (the caller flags the error).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t done = 0;
-  for (int it = 0; it < (1 << 20) && !done; it++)
-    asm volatile(
-        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-  return done != 0;
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    for (int it = 0; it < 32; it++)
+      if (mbar_try(bar, parity)) return true;
+    if (global_ns() - t0 > WAIT_LIMIT_NS) return false;
+  }
 }
 __device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(smem_u32(src)),
@@ -316,6 +334,17 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p)); }
 __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
+}
+// A 2-D tile of a tensor map (TMA, cp.async.bulk.tensor) into shared memory,
+// completing on an mbarrier: box element (x0 + i, y0 + j) of the map lands at
+// dst + (j * box_x + i) elements.  x0 times the element size must be a multiple
+// of 16 bytes; coordinates past the tensor read as zero.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x0, int y0, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x0), "r"(y0), "r"(smem_u32(bar))
+      : "memory");
 }
 // Orders this thread's generic-proxy shared-memory accesses before later bulk copies.
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
@@ -346,16 +375,24 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_addr) {
 }
 // mbar_wait with acquire at cluster scope: the arrivals came from a peer CTA,
 // whose stores before them are visible afterwards.  Bounded like mbar_wait.
+__device__ __forceinline__ uint32_t mbar_try_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, "
+      "p;\n}\n"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done;
+}
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t done = 0;
-  for (int it = 0; it < (1 << 20) && !done; it++)
-    asm volatile(
-        "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, "
-        "p;\n}\n"
-        : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-  return done != 0;
+  if (mbar_try_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    for (int it = 0; it < 32; it++)
+      if (mbar_try_cluster(bar, parity)) return true;
+    if (global_ns() - t0 > WAIT_LIMIT_NS) return false;
+  }
 }
 // Every thread of every CTA of the cluster (warp-convergent).
 __device__ __forceinline__ void cluster_sync() {
