@@ -9,6 +9,8 @@ next, normal call on the same context gives correct results.  Covered: the
 plain state chain and the clustered one with the gated norm fused in (whose
 two CTAs must both reach their final cluster barrier).
 """
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -44,10 +46,16 @@ def test_stage_wait_runs_out_and_context_survives(norm):
     lib = _lib.load()
     lib.kda_test_stage_timeout(1)
     try:
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
         _, ws, _ = _run(norm)
+        torch.cuda.synchronize()
+        elapsed = time.perf_counter() - t0
         assert kda_device_status(ws) == -7
     finally:
         lib.kda_test_stage_timeout(0)
+    print(f"\n[wait run-out] norm={norm}: the forward returned after {elapsed:.2f} s")
+    assert elapsed < 60.0
     out, ws, inp = _run(norm)  # the same context, normal waits
     assert kda_device_status(ws) == 0
     if not norm:
