@@ -757,16 +757,24 @@ def run_ours(args, rank, world, local):
     return 0
 
 
-def ncu_pass():
+def ncu_pass(rows: int = 16):
     """One untimed pass for profiler captures (select launches with ncu's -k /
     -s / -c): a warm-up forward+backward of the bench step's workload, the same
     forward+backward again, then one decode step, the gated norm forward and
-    backward and the short convolution forward and backward, in that order."""
-    from kimi_delta_attention_bwd_gb300 import (kda_backward, kda_decode_step, kda_forward, kda_norm_gate,
-                                                kda_norm_gate_backward, kda_short_conv, kda_short_conv_backward)
+    backward, the short convolution forward and backward, one forward+backward
+    with the gated norm fused into the chains (kda_fwd_norm_gate /
+    kda_bwd_norm_gate) and one of the fused layer (kda_fwd_conv / kda_bwd_conv
+    with the norm), in that order.  rows < 16 runs the step workloads on that
+    many 2048-token rows (a smaller case for multi-pass captures)."""
+    from kimi_delta_attention_bwd_gb300 import (kda_backward, kda_backward_conv, kda_backward_norm_gate,
+                                                kda_decode_step, kda_forward, kda_forward_conv,
+                                                kda_forward_norm_gate, kda_norm_gate, kda_norm_gate_backward,
+                                                kda_short_conv, kda_short_conv_backward)
     from kimi_delta_attention_bwd_gb300.inputs import norm_gate_inputs, short_conv_inputs
     dev = torch.device("cuda", 0)
     w = WORKLOADS[STEP_WORKLOAD]
+    if rows != w.B:
+        w = custom(rows, w.T, w.H, w.dk, w.dv, dtype=w.dtype, name=f"{rows}x{w.T} rows of the 300M layer")
     d = {k: (t.to(dev) if isinstance(t, torch.Tensor) else t) for k, t in make_inputs(w).items()}
     for _ in range(2):
         o, hf, ctx = kda_forward(d["q"], d["k"], d["v"], d["f"], d["b"], d["A_log"], d["dt_bias"], scale=d["scale"])
@@ -783,6 +791,13 @@ def ncu_pass():
     sc = {k: t.to(dev) for k, t in short_conv_inputs(w.B * w.T, 1024).items()}
     kda_short_conv(sc["x"], sc["w"])
     kda_short_conv_backward(sc["x"], sc["w"], sc["dy"])
+    shape = (w.B, w.T, w.H, w.dv)
+    _, _, _, nctx = kda_forward_norm_gate(d["q"], d["k"], d["v"], d["f"], d["b"], d["A_log"], d["dt_bias"],
+                                          ng["g"].reshape(shape), ng["w"], scale=d["scale"])
+    kda_backward_norm_gate(nctx, ng["dy"].reshape(shape))
+    _, _, cctx = kda_forward_conv(sc["x"].reshape(w.B, w.T, -1), sc["w"], d["f"], d["b"], d["A_log"], d["dt_bias"],
+                                  w.dk, w.dv, g=ng["g"].reshape(shape), w=ng["w"], scale=d["scale"])
+    kda_backward_conv(cctx, ng["dy"].reshape(shape))
     torch.cuda.synchronize()
     print("ncu pass done")
     return 0
@@ -819,11 +834,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ncu-pass", action="store_true", help="one untimed pass of every kernel, for ncu captures")
+    ap.add_argument("--ncu-rows", type=int, default=16, help="rows of the --ncu-pass step workloads (16: full size)")
     ap.add_argument("--ncu-large-heads", action="store_true",
                     help="one untimed pass of the large-head (128/128) kernels, for ncu captures")
     args = ap.parse_args()
     if args.ncu_pass:
-        return ncu_pass()
+        return ncu_pass(args.ncu_rows)
     if args.ncu_large_heads:
         return ncu_large_heads()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup

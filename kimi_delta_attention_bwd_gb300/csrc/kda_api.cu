@@ -149,11 +149,9 @@ static Layout layout(const Dims& d, int for_bwd, bool fused = false) {
   L.off_cl = take(4 * (size_t)d.nc_max);
   L.off_cd = take(4 * (size_t)d.nc_max);
   if (d.fast) {
-    if (!fused) {
-      L.off_CH = take(4 * nch * (d.dk * d.dk + C * d.dk + d.dk * d.dv + C * d.dv));  // M, QW, KU, PU
-      L.off_Sent = take(4 * nch * d.dk * d.dv);  // split-bf16 tiles: 4 bytes per element
-    }
+    if (!fused) L.off_CH = take(4 * nch * (d.dk * d.dk + C * d.dk + d.dk * d.dv + C * d.dv));  // M, QW, KU, PU
     if (for_bwd) {
+      L.off_Sent = take(4 * nch * d.dk * d.dv);  // entry states for the backward (split-bf16 tiles)
       L.off_dSn = take(4 * nch * d.dk * d.dv);
       L.off_pA = take(4 * nch);
       L.off_pdt = take(4 * nch * d.dk);

@@ -1407,7 +1407,7 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
       float oo[4][4];
       zero(oo);
       gemm3<2, false, true>(oo, QWo, 16 * wq, 0, Sc, 0, 0, DK / 16);
-      slice_to_global(w.sS + ((int64_t)ci * H + h) * 2 * DK * DV, Sc.hi, col0, tid - CTH);
+      if (io.save) slice_to_global(w.sS + ((int64_t)ci * H + h) * 2 * DK * DV, Sc.hi, col0, tid - CTH);  // for bwd_grad
       const float4* pup = reinterpret_cast<const float4*>(spu) + 4 * wq * 32 + lane;  // fragment order
       if constexpr (!NORM) {
 #pragma unroll
