@@ -1223,8 +1223,29 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
 // per-chunk kernels.  The fp32 state rounds to ~16 bits only as an operand;
 // h_final and dh0 are the fp32 accumulators.
 constexpr int NSC = 32;   // value columns per chain CTA
-constexpr int NSTG = 3;
+constexpr int NSTG = 3;   // stages of the fused-norm chains
+constexpr int FSTG = 4;   // stages of fwd_state (plain)
+constexpr int BSTG = 4;   // stages of bwd_scan (plain)
 constexpr int CTH = 128;  // chain threads
+
+// A document's chunks are consecutive C-token pieces from its first token
+// (how the chunk table is built), so a chain derives chunk c's first token and
+// length from the document's first token and length, loaded once, instead of
+// loading table rows inside its step loop (a dependent global load on the
+// step's path).
+struct DocSpan {
+  int tok0 = 0, len = 0;
+  __device__ int t0(int c) const { return tok0 + C * c; }
+  __device__ int L(int c) const { return min(C, len - C * c); }
+};
+__device__ __forceinline__ DocSpan doc_span(const Ws& w, int cb, int n) {
+  DocSpan sp;
+  if (n > 0) {
+    sp.tok0 = w.chunk_tok0[cb];
+    sp.len = w.chunk_tok0[cb + n - 1] + w.chunk_len[cb + n - 1] - sp.tok0;
+  }
+  return sp;
+}
 
 // Copies the 32 x NSC slice tile (K = NSC) into columns col0.. of the chunk's
 // full 32 x dv state tile (K = dv) in global memory: whole 8 x 8 core matrices.
@@ -1238,48 +1259,75 @@ __device__ __forceinline__ void slice_to_global(bf16* g, const bf16* s, int col0
   }
 }
 
+template <bool NORM>
 struct FChainStage {  // one copy of this half's part of the chain block: KU, PU, M, QW (half 0)
-  __align__(16) unsigned char raw[CB_STAGE];  // or M, QW, KU, PU (half 1)
+  __align__(128) unsigned char raw[CB_STAGE];  // or M, QW, KU, PU (half 1)
+  bf16 g[NORM ? C * NSC : 8];  // (NORM) the gate's columns of this half for the step's chunk, [C][NSC], by TMA
 };
 // Row partials exchanged by the two column-half CTAs of a (document, head)
 // when the gated RMSNorm is fused into a chain: the peer CTA stores its
-// partials for step s into part[s % NX] of this CTA's shared memory and
-// arrives on bar[s % NX] (one arrival per storing thread).  The forward sends
+// partials for step s into part[s % NX] of this CTA's shared memory by
+// asynchronous stores, each completing its 8 bytes of bar[s % NX]'s
+// transaction count.  One thread of this CTA arms each phase (one arrival
+// expecting the slot's XBYTES): for steps 0 .. NX - 1 at the start, for step
+// s + NX right after its own wait for step s succeeded.  The forward sends
 // step s's partials before it reads step s - 1's, and a CTA's send of step m
 // only waits (through its own barrier) for the peer's partials of step m - 2:
 // while this CTA has not read step j's, the peer may have sent up to j + 3,
-// so four slots.  (The backward sends and reads the same step's.)
+// so four slots, and the peer cannot send step s + NX before every thread
+// here has passed its wait for step s (so an early arming never completes a
+// phase under a thread still waiting).  (The backward sends and reads the
+// same step's.)
 constexpr int NX = 4;
+constexpr uint32_t XBYTES = C * 8;  // one slot: a float2 per row
 struct Xchg {
   float2 part[NX][C];
   uint64_t bar[NX];
 };
-struct FChainSm {
-  FChainStage st[NSTG];
-  bf16 S[2][2 * DK * NSC];  // the carried state (split), double-buffered
-  uint64_t bar[NSTG];       // stage completion
-  Xchg x;                   // fused norm only
+struct __align__(16) FChainNorm {  // (fused norm) one step's rows handed from the output to the carry warps
+  float u[2][C * NSC];         // u = o w sigmoid(g), [C][NSC] with 8-column groups swizzled by row
+  float own[2][C];             // this CTA's half of each row's sum of o^2
 };
-static_assert(sizeof(FChainStage) % 16 == 0, "bulk-copy targets need 16-byte alignment");
+template <bool NORM>
+struct FChainSm {
+  FChainStage<NORM> st[NORM ? NSTG : FSTG];
+  bf16 S[2][2 * DK * NSC];          // the carried state (split), double-buffered
+  uint64_t bar[NORM ? NSTG : FSTG];  // stage completion
+  Xchg x;                           // fused norm only
+  FChainNorm nr[NORM ? 1 : 0];
+};
+static_assert(offsetof(FChainSm<true>, nr) % 16 == 0, "the u tiles are read as float4");
+// Column c of row r of a u tile: 8-column groups XOR-permuted by r % 4, so the
+// output warps' fragment stores (8 rows x 4 column pairs per instruction) and
+// the carry warps' 8-column reads spread over the banks.
+__device__ __forceinline__ int uswz(int r, int c) { return r * NSC + (c ^ (8 * (r & 3))); }
+static_assert(sizeof(FChainStage<false>) % 128 == 0 && sizeof(FChainStage<true>) % 128 == 0 &&
+                  offsetof(FChainStage<true>, g) % 128 == 0,
+              "bulk and tensor copy targets need 128-byte alignment");
 
 // fwd_state: warps 0..3 carry the state (S' = M S + KU into the other buffer
-// of the double-buffered tile), warps 4..7 write the output O = QW S + PU and
-// store the entering state, both on the step's state; one barrier per step.
+// of the double-buffered tile), then store the entering state and issue the
+// stage copy of a later step; warps 4..7 write the output O = QW S + PU, on
+// the same step's state; one barrier per step.
 // NORM: the gated RMSNorm epilogue ("Pure KDA 300M" guide, Overview: per-head
 // output gate and RMSNorm, eps 1e-6), y = o r w sigmoid(g) with
 // r = 1 / sqrt(mean_j o_j^2 + eps) over the dv columns of a row, is fused into
-// the output warps.  A row's 64 columns are split over the two CTAs of the
-// (document, head); launched as a cluster of those two CTAs, each output warp
-// stores its rows' partial sums of o^2 into the peer's shared memory, arrives
-// on the peer's barrier and waits (bounded) for the peer's partials.  y is
-// written, o (io dtype) when io.o is set, and with io.save o in fp32 for the
-// fused backward (a bf16 copy would make its dg depend on a rounding).  A
-// CTA of a cluster never leaves before the final cluster barrier: errors skip
-// the remaining steps instead of returning.
+// the chain.  A row's 64 columns are split over the two CTAs of the
+// (document, head); launched as a cluster of those two CTAs.  At step s the
+// output warps send their rows' partial sums of o^2 into the peer's shared
+// memory, write o (io dtype) when io.o is set and, with io.save, o in fp32 for
+// the fused backward (a bf16 copy would make its dg depend on a rounding), and
+// hand u = o w sigmoid(g) and their own partials to the carry warps, which at
+// step s + 1, after their state update, wait (bounded) for the peer's
+// partials of step s and write y = u r.  (The carry warps' part of a step is
+// the shorter one; the output warps' product and stores set the step time.)
+// A CTA of a cluster never leaves before the final cluster barrier: errors
+// skip the remaining steps instead of returning.
 template <bool NORM>
-__global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws w) {
+__global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws w, const __grid_constant__ NMaps nmap) {
   extern __shared__ __align__(128) unsigned char smraw[];
-  FChainSm& sm = *reinterpret_cast<FChainSm*>(smraw);
+  FChainSm<NORM>& sm = *reinterpret_cast<FChainSm<NORM>*>(smraw);
+  constexpr int NS = NORM ? NSTG : FSTG;
   const int doc = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * NSC, tid = threadIdx.x, warp = tid >> 5;
   const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
   pdl_wait();  // fwd_chunk's products
@@ -1287,6 +1335,7 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
   if (!NORM && err0 != 0) return;
   const int H = d.H;
   const int cb = w.doc_chunk0[doc], n = err0 != 0 ? 0 : w.doc_chunk0[doc + 1] - cb;
+  const DocSpan sp = doc_span(w, cb, n);
   const int64_t dh = ((int64_t)doc * H + h) * DK * DV;
   const Op S0{sm.S[0], sm.S[0] + DK * NSC, NSC}, S1{sm.S[1], sm.S[1] + DK * NSC, NSC};
   for (int idx = tid; idx < DK * NSC / 2; idx += 2 * CTH) {
@@ -1296,11 +1345,13 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
     op_store2(S0, i, jc, v.x, v.y);
   }
   if (tid == 0) {
-    for (int s2 = 0; s2 < NSTG; s2++) mbar_init(&sm.bar[s2], 1);
+    for (int s2 = 0; s2 < NS; s2++) mbar_init(&sm.bar[s2], 1);
     if (NORM) {
-      for (int x2 = 0; x2 < NX; x2++) mbar_init(&sm.x.bar[x2], 32);  // the peer's 4 output warps x 8 row lanes
+      for (int x2 = 0; x2 < NX; x2++) mbar_init(&sm.x.bar[x2], 1);  // one local arming per phase + the peer's bytes
     }
     mbar_init_fence();
+    if (NORM)
+      for (int x2 = 0; x2 < NX; x2++) mbar_expect_tx(&sm.x.bar[x2], XBYTES);  // steps 0 .. NX - 1
   }
   __syncthreads();  // the barriers are initialised before any thread waits on them
   uint32_t xpart = 0, xbar = 0;  // the peer's exchange slots, mapped into the cluster window
@@ -1315,69 +1366,64 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
 #pragma unroll
       for (int c1 = 0; c1 < 2; c1++) nwv[jj][c1] = io.nw[col0 + 8 * jj + 2 * tq + c1];
   }
-  bool xfail = false;  // (output warps) the peer's partials did not arrive in bound
+  bool xfail = false;  // (carry warps) the peer's partials did not arrive in bound
   bool bad = false;
-  // (NORM, output warps) the previous step's rows, finished one step late
-  float lo[4][4], lg[4][4], ls0 = 0.f, ls1 = 0.f;
-  int lL = 0, lt0 = 0, lstep = 0;
-  auto finish_prev = [&]() {
-    const int r = 16 * (warp & 3) + gq, slot = lstep % NX;
-    if (!mbar_wait_cluster(&sm.x.bar[slot], (lstep / NX) & 1)) {
+  // (NORM, carry warps) the rows of step k: thread = row tid / 2, columns 16 (tid % 2) ..
+  auto finish_rows = [&](int k) {
+    const int row = tid >> 1, hf = tid & 1, slot = k % NX, ub = k & 1;
+    if (!mbar_wait_cluster(&sm.x.bar[slot], (k / NX) & 1)) {
       xfail = true;  // bails at the next step's barrier (or skips the end state)
       return;
     }
-    const float t0s = ls0 + sm.x.part[slot][r].x, t1s = ls1 + sm.x.part[slot][r + 8].x;
-    const float r0 = 1.0f / sqrtf(t0s * (1.0f / DV) + io.neps), r1 = 1.0f / sqrtf(t1s * (1.0f / DV) + io.neps);
-    bf16* yp = (bf16*)io.y;
-    bf16* op = (bf16*)io.o;
+    if (tid == 0) mbar_expect_tx(&sm.x.bar[slot], XBYTES);  // armed for step k + NX
+    const int L = sp.L(k), t0 = sp.t0(k);
+    if (row < L) {
+      const float tot = sm.nr[0].own[ub][row] + sm.x.part[slot][row].x;
+      const float rr = 1.0f / sqrtf(tot * (1.0f / DV) + io.neps);
+      bf16* yp = (bf16*)io.y + ((size_t)(t0 + row) * d.H + h) * DV + col0 + 16 * hf;
 #pragma unroll
-    for (int jj = 0; jj < 4; jj++) {
-      const int c = col0 + 8 * jj + 2 * tq;
-      if (r < lL) {
-        const size_t i = ((size_t)(lt0 + r) * d.H + h) * DV + c;
-        *reinterpret_cast<__nv_bfloat162*>(yp + i) =
-            __floats2bfloat162_rn(lo[jj][0] * r0 * nwv[jj][0] * sigmoid_fast(lg[jj][0]),
-                                  lo[jj][1] * r0 * nwv[jj][1] * sigmoid_fast(lg[jj][1]));
-        if (op) *reinterpret_cast<__nv_bfloat162*>(op + i) = __floats2bfloat162_rn(lo[jj][0], lo[jj][1]);
-        if (io.save) *reinterpret_cast<float2*>(w.nO + i) = make_float2(lo[jj][0], lo[jj][1]);
-      }
-      if (r + 8 < lL) {
-        const size_t i = ((size_t)(lt0 + r + 8) * d.H + h) * DV + c;
-        *reinterpret_cast<__nv_bfloat162*>(yp + i) =
-            __floats2bfloat162_rn(lo[jj][2] * r1 * nwv[jj][0] * sigmoid_fast(lg[jj][2]),
-                                  lo[jj][3] * r1 * nwv[jj][1] * sigmoid_fast(lg[jj][3]));
-        if (op) *reinterpret_cast<__nv_bfloat162*>(op + i) = __floats2bfloat162_rn(lo[jj][2], lo[jj][3]);
-        if (io.save) *reinterpret_cast<float2*>(w.nO + i) = make_float2(lo[jj][2], lo[jj][3]);
+      for (int lg = 0; lg < 2; lg++) {
+        const float4* up = reinterpret_cast<const float4*>(sm.nr[0].u[ub] + uswz(row, 16 * hf + 8 * lg));
+        const float4 a = up[0], b = up[1];
+        uint4 o4;
+        __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o4);
+        o2[0] = __floats2bfloat162_rn(a.x * rr, a.y * rr);
+        o2[1] = __floats2bfloat162_rn(a.z * rr, a.w * rr);
+        o2[2] = __floats2bfloat162_rn(b.x * rr, b.y * rr);
+        o2[3] = __floats2bfloat162_rn(b.z * rr, b.w * rr);
+        *reinterpret_cast<uint4*>(yp + 8 * lg) = o4;
       }
     }
   };
-  // the stage of `step`: one copy, issued by a side-group thread (not on the carry warps' path)
+  // the stage of `step`: one copy (with the gate tile: two), issued by carry thread 0 once its part of
+  // the step before is done (the output warps' part is the longer one)
   const int oKU = blockIdx.z ? CB_KU1 - CB_M : 0, oPU = oKU + (CB_PU0 - CB_KU0);
   const int oM = blockIdx.z ? 0 : CB_M - CB_KU0, oQW = oM + (CB_QW - CB_M);
   auto prefetch = [&](int step) {
-    if (step < n && tid == CTH) {
-      const int slot = step % NSTG;
+    if (step < n && tid == 0) {
+      const int slot = step % NS;
       const int64_t ch = (int64_t)(cb + step) * H + h;
-      mbar_expect_tx(&sm.bar[slot], (uint32_t)(CB_STAGE + d.tx_extra));
+      mbar_expect_tx(&sm.bar[slot], (uint32_t)(CB_STAGE + (NORM ? 2 * C * NSC : 0) + d.tx_extra));
       bulk_g2s(sm.st[slot].raw, chblk(w, ch) + (blockIdx.z ? CB_M : CB_KU0), CB_STAGE, &sm.bar[slot]);
+      if (NORM)  // the gate rows of the chunk (rows past its end are not used)
+        tma_load_2d(sm.st[slot].g, &nmap.g, h * DV + col0, sp.t0(step), &sm.bar[slot]);
     }
   };
-  for (int s = 0; s < NSTG - 1; s++) prefetch(s);
+  for (int s = 0; s < NS - 1; s++) prefetch(s);
   const bool carry = warp < 4;
   const int wq = warp & 3, mI = wq & 1, jn = wq >> 1;
   float snew[2][4];  // (carry warps) tile of the updated state: rows 16 mI .., columns 16 jn ..
   zero(snew);
   bf16* o = (bf16*)io.o;
   for (int step = 0; step < n; step++) {
-    const FChainStage& s = sm.st[step % NSTG];
+    const FChainStage<NORM>& s = sm.st[step % NS];
     const int ci = cb + step;
-    if (__syncthreads_or(!mbar_wait(&sm.bar[step % NSTG], (step / NSTG) & 1) || xfail)) {  // a wait ran out
-      for (int k2 = step; k2 < n && k2 < step + NSTG - 1; k2++) mbar_wait(&sm.bar[k2 % NSTG], (k2 / NSTG) & 1);
+    if (__syncthreads_or(!mbar_wait(&sm.bar[step % NS], (step / NS) & 1) || xfail)) {  // a wait ran out
+      for (int k2 = step; k2 < n && k2 < step + NS - 1; k2++) mbar_wait(&sm.bar[k2 % NS], (k2 / NS) & 1);
       if (tid == 0) atomicExch(w.err, -7);
       bad = true;
       break;
     }  // this step's stage and state are visible; the other state buffer is free
-    prefetch(step + NSTG - 1);
     bf16* smp = reinterpret_cast<bf16*>(const_cast<unsigned char*>(s.raw) + oM);
     bf16* sqp = reinterpret_cast<bf16*>(const_cast<unsigned char*>(s.raw) + oQW);
     const float* sku = reinterpret_cast<const float*>(s.raw + oKU);
@@ -1402,12 +1448,15 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
         for (int hh = 0; hh < 2; hh++)
           op_store2(Sn, 16 * mI + gq + 8 * hh, 16 * jn + 8 * jj + 2 * tq, snew[jj][2 * hh], snew[jj][2 * hh + 1]);
       }
+      if (io.save) slice_to_global(w.sS + ((int64_t)ci * H + h) * 2 * DK * DV, Sc.hi, col0, tid);  // for bwd_grad
+      if constexpr (NORM)
+        if (step > 0) finish_rows(step - 1);  // the previous step's y, off the state's path
+      prefetch(step + NS - 1);  // into the slot of step - 1, free since the barrier
     } else {
-      const int L = w.chunk_len[ci], t0 = w.chunk_tok0[ci];
+      const int L = sp.L(step), t0 = sp.t0(step);
       float oo[4][4];
       zero(oo);
       gemm3<2, false, true>(oo, QWo, 16 * wq, 0, Sc, 0, 0, DK / 16);
-      if (io.save) slice_to_global(w.sS + ((int64_t)ci * H + h) * 2 * DK * DV, Sc.hi, col0, tid - CTH);  // for bwd_grad
       const float4* pup = reinterpret_cast<const float4*>(spu) + 4 * wq * 32 + lane;  // fragment order
       if constexpr (!NORM) {
 #pragma unroll
@@ -1423,16 +1472,8 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
         }
       } else {
         // o of rows r = 16 wq + gq and r + 8 (columns 8 jj + 2 tq + {0, 1}); rows past the
-        // chunk end are zero (their QW and PU rows are).  This step's row partials go to the
-        // peer now; the rows are finished one step later (finish_prev), when the peer's
-        // partials have had a step's time to arrive.
-        const int r = 16 * wq + gq, slot = step % NX;
-        const bf16* gp = (const bf16*)io.ng;
-        if (step + 2 < n) {  // the gate rows two steps ahead into L2 (one 64-byte row segment per thread)
-          const int c2 = ci + 2, t2 = w.chunk_tok0[c2], r2 = tid - CTH;
-          if (r2 < w.chunk_len[c2]) prefetch_l2(gp + ((size_t)(t2 + r2) * H + h) * DV + col0);
-        }
-        float gv[4][4];
+        // chunk end are zero (their QW and PU rows are).  The row partials go to the peer now.
+        const int r = 16 * wq + gq, slot = step % NX, ub = step & 1;
 #pragma unroll
         for (int jj = 0; jj < 4; jj++) {
           const float4 p4 = pup[32 * jj];
@@ -1440,17 +1481,6 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
           oo[jj][1] += p4.y;
           oo[jj][2] += p4.z;
           oo[jj][3] += p4.w;
-          const int c = col0 + 8 * jj + 2 * tq;
-          const float2 g0 = r < L ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(
-                                        gp + ((size_t)(t0 + r) * H + h) * DV + c))
-                                  : make_float2(0.f, 0.f);
-          const float2 g1 = r + 8 < L ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(
-                                            gp + ((size_t)(t0 + r + 8) * H + h) * DV + c))
-                                      : make_float2(0.f, 0.f);
-          gv[jj][0] = g0.x;
-          gv[jj][1] = g0.y;
-          gv[jj][2] = g1.x;
-          gv[jj][3] = g1.y;
         }
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -1462,28 +1492,41 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
         s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
         s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
         s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
-        if (tq == 0) {  // rows r and r + 8 into the peer's slot, then one arrival
-          st_cluster_f32x2(xpart + (uint32_t)((slot * C + r) * 8), s0, 0.f);
-          st_cluster_f32x2(xpart + (uint32_t)((slot * C + r + 8) * 8), s1, 0.f);
-          mbar_arrive_remote(xbar + (uint32_t)(slot * 8));
+        if (tq == 0) {  // rows r and r + 8 into the peer's slot, each completing 8 of its barrier's bytes
+          st_async_f32x2(xpart + (uint32_t)((slot * C + r) * 8), s0, 0.f, xbar + (uint32_t)(slot * 8));
+          st_async_f32x2(xpart + (uint32_t)((slot * C + r + 8) * 8), s1, 0.f, xbar + (uint32_t)(slot * 8));
+          sm.nr[0].own[ub][r] = s0;
+          sm.nr[0].own[ub][r + 8] = s1;
         }
-        if (step > 0) finish_prev();
+        float* ut = sm.nr[0].u[ub];
 #pragma unroll
-        for (int jj = 0; jj < 4; jj++)
-#pragma unroll
-          for (int e = 0; e < 4; e++) {
-            lo[jj][e] = oo[jj][e];
-            lg[jj][e] = gv[jj][e];
+        for (int jj = 0; jj < 4; jj++) {
+          const int c = 8 * jj + 2 * tq;  // the gate tile arrived with the stage
+          const float2 g0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(s.g + r * NSC + c));
+          const float2 g1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(s.g + (r + 8) * NSC + c));
+          *reinterpret_cast<float2*>(ut + uswz(r, c)) =
+              make_float2(oo[jj][0] * nwv[jj][0] * sigmoid_fast(g0.x), oo[jj][1] * nwv[jj][1] * sigmoid_fast(g0.y));
+          *reinterpret_cast<float2*>(ut + uswz(r + 8, c)) =
+              make_float2(oo[jj][2] * nwv[jj][0] * sigmoid_fast(g1.x), oo[jj][3] * nwv[jj][1] * sigmoid_fast(g1.y));
+          bf16* op = (bf16*)io.o;
+          if (r < L) {
+            const size_t i = ((size_t)(t0 + r) * H + h) * DV + col0 + c;
+            if (op) *reinterpret_cast<__nv_bfloat162*>(op + i) = __floats2bfloat162_rn(oo[jj][0], oo[jj][1]);
+            if (io.save) *reinterpret_cast<float2*>(w.nO + i) = make_float2(oo[jj][0], oo[jj][1]);
           }
-        ls0 = s0;
-        ls1 = s1;
-        lL = L;
-        lt0 = t0;
-        lstep = step;
+          if (r + 8 < L) {
+            const size_t i = ((size_t)(t0 + r + 8) * H + h) * DV + col0 + c;
+            if (op) *reinterpret_cast<__nv_bfloat162*>(op + i) = __floats2bfloat162_rn(oo[jj][2], oo[jj][3]);
+            if (io.save) *reinterpret_cast<float2*>(w.nO + i) = make_float2(oo[jj][2], oo[jj][3]);
+          }
+        }
       }
     }
   }
-  if (NORM && !bad && n > 0 && !carry) finish_prev();  // the last step's rows
+  if constexpr (NORM) {
+    __syncthreads();  // the output warps' last u tile and partials are written
+    if (!bad && n > 0 && carry) finish_rows(n - 1);  // the last step's rows
+  }
   if (NORM && __syncthreads_or(xfail) && !bad) {  // the last step's exchange ran out
     if (tid == 0) atomicExch(w.err, -7);
     bad = true;
@@ -1514,48 +1557,27 @@ struct BChainStage {
   bf16 QW[2 * C * DK];  // QW (split)
   bf16 dO[C * NSC];     // columns col0.. of dO (exact bf16, operand layout)
 };
-// With the fused gated-norm backward the stage also holds this CTA's columns
-// of dy, g (bf16) and of the forward's fp32 o, row-major ([C][NSC]), from
-// which the chain forms dO.
-struct BChainStageN : BChainStage {
-  bf16 dy[C * NSC], g[C * NSC];
-  float o[C * NSC];
-};
-template <bool NORM>
 struct BChainSm {
-  typename std::conditional<NORM, BChainStageN, BChainStage>::type st[NSTG];
+  BChainStage st[BSTG];
   bf16 dS[2 * DK * NSC];  // the carried state gradient (split)
-  uint64_t bar[NSTG];     // completion of the stage's M and QW
-  Xchg x;                 // fused norm only
+  uint64_t bar[BSTG];     // completion of the stage's M and QW
 };
-static_assert(sizeof(BChainStage) % 16 == 0 && sizeof(BChainStageN) % 16 == 0 &&
-                  offsetof(BChainStage, QW) == 4 * DK * DK && offsetof(BChainStage, dO) == CB_KU1 - CB_M,
+static_assert(sizeof(BChainStage) % 16 == 0 && offsetof(BChainStage, QW) == 4 * DK * DK &&
+                  offsetof(BChainStage, dO) == CB_KU1 - CB_M,
               "M | QW arrive in one copy");
 
 // bwd_scan: the reverse chain dS = M^T dS' + QW^T dO, one CTA of four warps
 // per (document, head, 32 value columns).
-// NORM: the gated RMSNorm's backward is fused in front of the chain's dO (o is
-// the forward's fp32 copy in the workspace).  With
-// y = o r w s (s = sigmoid(g), r = 1 / sqrt(mean_j o_j^2 + eps)) and dy given,
-//   dO_j = r a_j - o_j r^3 (sum_k a_k o_k) / dv,   a_j = dy_j w_j s_j
-//   dg_j = dy_j o_j r w_j s_j (1 - s_j),           dw_j = sum over rows of dy_j o_j r s_j
-// (the chain rule through the norm).  The two row sums (of o^2 and of a o) need
-// all dv columns: the two column-half CTAs of a (document, head) run as a
-// cluster and exchange their partials through distributed shared memory, the
-// exchange overlapping the step's M^T dS product.  dO (bf16, also written for
-// the per-chunk kernels) replaces the loaded dO tile; dg is written; the dw
-// partials are summed over the (document, head)'s rows in a fixed order.
-template <bool NORM>
 __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
   extern __shared__ __align__(128) unsigned char smraw[];
-  BChainSm<NORM>& sm = *reinterpret_cast<BChainSm<NORM>*>(smraw);
+  BChainSm& sm = *reinterpret_cast<BChainSm*>(smraw);
   const int doc = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * NSC, tid = threadIdx.x, warp = tid >> 5;
   const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
   pdl_release();  // bwd_grad may launch: it waits for this grid before reading dS
-  const bool ok0 = saved_ok(d, w.tag, w.err);
-  if (!NORM && !ok0) return;
+  if (!saved_ok(d, w.tag, w.err)) return;
   const int H = d.H;
-  const int cb = w.doc_chunk0[doc], ce = w.doc_chunk0[doc + 1], n = ok0 ? ce - cb : 0;
+  const int cb = w.doc_chunk0[doc], ce = w.doc_chunk0[doc + 1], n = ce - cb;
+  const DocSpan sp = doc_span(w, cb, n);
   const int64_t dh = ((int64_t)doc * H + h) * DK * DV;
   const Op dS{sm.dS, sm.dS + DK * NSC, NSC};
   for (int idx = tid; idx < DK * NSC / 2; idx += CTH) {
@@ -1566,75 +1588,172 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
   }
   const bf16* dOg = (const bf16*)io.dO;
   if (tid == 0) {
-    for (int s2 = 0; s2 < NSTG; s2++) mbar_init(&sm.bar[s2], 1);
-    if (NORM) {
-      for (int x2 = 0; x2 < NX; x2++) mbar_init(&sm.x.bar[x2], C);  // one arrival per row from the peer
-    }
+    for (int s2 = 0; s2 < BSTG; s2++) mbar_init(&sm.bar[s2], 1);
     mbar_init_fence();
   }
   __syncthreads();  // the barriers are initialised before any thread waits on them
-  // (NORM) thread t owns row t / 2, columns 16 (t % 2) .. of the CTA's 32
-  const int nr = tid >> 1, nh = tid & 1;
-  uint32_t xpart = 0, xbar = 0;
-  float nwv[16], dwacc[16];
-  if constexpr (NORM) {
-    cluster_sync();  // ... and before the peer arrives on them
-    const uint32_t peer = cluster_rank() ^ 1u;
-    xpart = cluster_map(&sm.x.part[0][0], peer);
-    xbar = cluster_map(&sm.x.bar[0], peer);
-#pragma unroll
-    for (int j = 0; j < 16; j++) {
-      nwv[j] = io.nw[col0 + 16 * nh + j];
-      dwacc[j] = 0.f;
-    }
-  }
   auto prefetch = [&](int step) {  // always commits a cp.async group (empty past the end)
     if (step < n) {
-      const int slot = step % NSTG;
-      auto& s = sm.st[slot];
-      const int ci = ce - 1 - step, L = w.chunk_len[ci], t0 = w.chunk_tok0[ci];
+      const int slot = step % BSTG;
+      BChainStage& s = sm.st[slot];
+      const int ci = ce - 1 - step, L = sp.L(n - 1 - step), t0 = sp.t0(n - 1 - step);
       const int64_t ch = (int64_t)ci * H + h;
       if (tid == 0) {  // M | QW, adjacent in the chain block and in the stage
         mbar_expect_tx(&sm.bar[slot], CB_KU1 - CB_M);
         bulk_g2s(s.M, chblk(w, ch) + CB_M, CB_KU1 - CB_M, &sm.bar[slot]);
       }
-      if constexpr (!NORM) {
-        for (int idx = tid; idx < C * NSC / 8; idx += CTH) {
-          const int r = idx / (NSC / 8), p = idx % (NSC / 8);
-          bf16* dst = s.dO + opix(r, 8 * p, NSC);
-          if (r < L) cp16(dst, dOg + ((size_t)(t0 + r) * H + h) * DV + col0 + 8 * p);
-          else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-        }
-      } else {  // dy, g (bf16) and o (fp32) rows of this CTA's columns, zero past the chunk end
-        for (int idx = tid; idx < 2 * C * NSC / 8; idx += CTH) {
-          const int t2 = idx / (C * NSC / 8), rem = idx % (C * NSC / 8), r = rem / (NSC / 8), p = rem % (NSC / 8);
-          bf16* dst = (t2 == 0 ? s.dy : s.g) + r * NSC + 8 * p;
-          const bf16* src = (const bf16*)(t2 == 0 ? io.dy : io.ng);
-          if (r < L) cp16(dst, src + ((size_t)(t0 + r) * H + h) * DV + col0 + 8 * p);
-          else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        for (int idx = tid; idx < C * NSC / 4; idx += CTH) {
-          const int r = idx / (NSC / 4), p = idx % (NSC / 4);
-          float* dst = s.o + r * NSC + 4 * p;
-          if (r < L) cp16(dst, w.nO + ((size_t)(t0 + r) * H + h) * DV + col0 + 4 * p);
-          else *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+      for (int idx = tid; idx < C * NSC / 8; idx += CTH) {
+        const int r = idx / (NSC / 8), p = idx % (NSC / 8);
+        bf16* dst = s.dO + opix(r, 8 * p, NSC);
+        if (r < L) cp16(dst, dOg + ((size_t)(t0 + r) * H + h) * DV + col0 + 8 * p);
+        else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
     cp_commit();
   };
-  for (int s = 0; s < NSTG - 1; s++) prefetch(s);
+  for (int s = 0; s < BSTG - 1; s++) prefetch(s);
   float acc[2][4];  // this warp's tile of the carried gradient: rows 16 (warp & 1) .., columns 16 (warp >> 1) ..
   zero(acc);
   const int mI = warp & 1, jn = warp >> 1;
-  bool xfail = false, bad = false;
-  // (NORM) the norm's backward for the stage of step k, in two halves around the
-  // chain's products of the step before: send sends this CTA's row partials
-  // (sum o^2, sum a o over its columns) to the peer; recv waits for the peer's
-  // and writes dO (the stage's operand tile, and global memory), dg and dw.
-  float po = 0.f, pa = 0.f;
-  // (generic lambdas: instantiated only where called, i.e. for NORM)
-  auto norm_vals = [&](auto& s, float* dyv, float* ov, float* sgv) {
+  for (int step = 0; step < n; step++) {
+    const BChainStage& s = sm.st[step % BSTG];
+    const int ci = ce - 1 - step;
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(BSTG - 2));
+    if (__syncthreads_or(!mbar_wait(&sm.bar[step % BSTG], (step / BSTG) & 1))) {  // a stage did not arrive in bound
+      for (int k2 = step; k2 < n && k2 < step + BSTG - 1; k2++) mbar_wait(&sm.bar[k2 % BSTG], (k2 / BSTG) & 1);
+      cp_wait_all();
+      if (tid == 0) atomicExch(w.err, -7);
+      return;
+    }  // this step's stage and the last state update are visible
+    prefetch(step + BSTG - 1);
+    const Op Mo{const_cast<bf16*>(s.M), const_cast<bf16*>(s.M) + DK * DK, DK};
+    const Op QWo{const_cast<bf16*>(s.QW), const_cast<bf16*>(s.QW) + C * DK, DK};
+    const Op dOo{const_cast<bf16*>(s.dO), nullptr, NSC};
+    float ax[2][4];
+    zero(acc);
+    zero(ax);
+    gemm3<1, true, true>(ax, QWo, 16 * mI, 0, dOo, 16 * jn, 0, C / 16);
+    gemm3<1, true, true>(acc, Mo, 16 * mI, 0, dS, 16 * jn, 0, DK / 16);
+    slice_to_global(w.sdS + ((int64_t)ci * H + h) * 2 * DK * DV, sm.dS, col0, threadIdx.x);
+#pragma unroll
+    for (int jj = 0; jj < 2; jj++)
+#pragma unroll
+      for (int e = 0; e < 4; e++) acc[jj][e] += ax[jj][e];
+    __syncthreads();  // every read of the state tile is done
+#pragma unroll
+    for (int jj = 0; jj < 2; jj++)
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++)
+        op_store2(dS, 16 * mI + gq + 8 * hh, 16 * jn + 8 * jj + 2 * tq, acc[jj][2 * hh], acc[jj][2 * hh + 1]);
+  }
+  cp_wait_all();
+  if (io.dh0) {
+    if (n > 0) {
+#pragma unroll
+      for (int jj = 0; jj < 2; jj++)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+          const int i = 16 * mI + gq + 8 * hh, c = 16 * jn + 8 * jj + 2 * tq;
+          *reinterpret_cast<float2*>(io.dh0 + dh + i * DV + col0 + c) = make_float2(acc[jj][2 * hh], acc[jj][2 * hh + 1]);
+        }
+    } else {
+      for (int idx = tid; idx < DK * NSC; idx += CTH) {
+        const int i = idx / NSC, jc = idx % NSC;
+        io.dh0[dh + i * DV + col0 + jc] = io.dh_final ? io.dh_final[dh + i * DV + col0 + jc] : 0.f;
+      }
+    }
+  }
+}
+
+// bwd_scan_norm: the reverse chain with the gated RMSNorm's backward fused in
+// front of its dO.  With y = o r w s (s = sigmoid(g), r = 1 / sqrt(mean_j o_j^2
+// + eps)) and dy given, by the chain rule through the norm:
+//   dO_j = r a_j - o_j r^3 (sum_k a_k o_k) / dv,   a_j = dy_j w_j s_j
+//   dg_j = dy_j o_j r w_j s_j (1 - s_j),           dw_j = sum over rows of dy_j o_j r s_j
+// The two row sums need all dv columns; the two column-half CTAs of a
+// (document, head) run as a cluster and exchange their halves' partials
+// through distributed shared memory.  Warp-specialised: warps 0-3 carry the
+// chain exactly as bwd_scan does (their own named barrier between reading and
+// writing the state tile); warps 4-7 form, during step s, the next stage's dO
+// (its operand tile, dO in global memory for bwd_grad, dg, and the dw partials),
+// so the norm's work and the exchange stay off the chain's critical path.  Each
+// stage brings M | QW (one bulk copy) and this half's dy, g (bf16) and the
+// forward's fp32 o (tensor-map copies) on one barrier, two steps ahead.  No
+// early return after the first cluster barrier (errors skip the remaining
+// steps) and a final cluster barrier: no CTA exits while its peer may still
+// address its shared memory.
+struct BChainStageN {
+  bf16 M[2 * DK * DK];
+  bf16 QW[2 * C * DK];
+  bf16 dO[C * NSC];              // formed here by the norm warps
+  bf16 dy[C * NSC], g[C * NSC];  // [C][NSC], rows past the chunk end masked when used
+  float o[C * NSC];
+};
+struct BChainSmN {
+  BChainStageN st[NSTG];
+  bf16 dS[2 * DK * NSC];
+  uint64_t bar[NSTG];
+  Xchg x;
+};
+static_assert(sizeof(BChainStageN) % 128 == 0 && offsetof(BChainStageN, QW) == 4 * DK * DK &&
+                  offsetof(BChainStageN, dy) % 128 == 0 &&
+                  offsetof(BChainStageN, g) % 128 == 0 && offsetof(BChainStageN, o) % 128 == 0,
+              "tensor-copy targets need 128-byte alignment");
+constexpr uint32_t BSTAGE_N_TX = (CB_KU1 - CB_M) + 2 * 2 * C * NSC + 4 * C * NSC;
+
+__global__ void __launch_bounds__(2 * CTH, 2) bwd_scan_norm_kernel(Dims d, BwdIO io, Ws w,
+                                                                const __grid_constant__ NMaps nmap) {
+  extern __shared__ __align__(128) unsigned char smraw[];
+  BChainSmN& sm = *reinterpret_cast<BChainSmN*>(smraw);
+  const int doc = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * NSC, tid = threadIdx.x, warp = tid >> 5;
+  const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+  const bool chain = warp < 4;
+  pdl_release();  // bwd_grad may launch: it waits for this grid before reading dS and dO
+  const bool ok0 = saved_ok(d, w.tag, w.err);
+  const int H = d.H;
+  const int cb = w.doc_chunk0[doc], ce = w.doc_chunk0[doc + 1], n = ok0 ? ce - cb : 0;
+  const DocSpan sp = doc_span(w, cb, n);
+  const int64_t dh = ((int64_t)doc * H + h) * DK * DV;
+  const Op dS{sm.dS, sm.dS + DK * NSC, NSC};
+  for (int idx = tid; idx < DK * NSC / 2; idx += 2 * CTH) {
+    const int i = idx / (NSC / 2), jc = 2 * (idx % (NSC / 2));
+    float2 v = make_float2(0.f, 0.f);
+    if (io.dh_final && ok0) v = *reinterpret_cast<const float2*>(io.dh_final + dh + i * DV + col0 + jc);
+    op_store2(dS, i, jc, v.x, v.y);
+  }
+  if (tid == 0) {
+    for (int s2 = 0; s2 < NSTG; s2++) mbar_init(&sm.bar[s2], 1);
+    for (int x2 = 0; x2 < NX; x2++) mbar_init(&sm.x.bar[x2], 1);  // one local arming per phase + the peer's bytes
+    mbar_init_fence();
+    for (int x2 = 0; x2 < NX; x2++) mbar_expect_tx(&sm.x.bar[x2], XBYTES);  // stages 0 .. NX - 1
+  }
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before any remote arrival
+  const uint32_t peer = cluster_rank() ^ 1u;
+  const uint32_t xpart = cluster_map(&sm.x.part[0][0], peer), xbar = cluster_map(&sm.x.bar[0], peer);
+  // (norm warps) thread nt owns row nt / 2, columns 16 (nt % 2) .. of the CTA's 32
+  const int nt = tid - CTH, nr = nt >> 1, nh = nt & 1;
+  float nwv[16], dwacc[16];
+#pragma unroll
+  for (int j = 0; j < 16; j++) {
+    nwv[j] = chain ? 0.f : io.nw[col0 + 16 * nh + j];
+    dwacc[j] = 0.f;
+  }
+  auto prefetch = [&](int step) {  // one thread: M | QW (bulk) and dy, g, o (tensor maps) on one barrier
+    if (step < n && tid == 0) {
+      const int slot = step % NSTG;
+      BChainStageN& s = sm.st[slot];
+      const int ci = ce - 1 - step, t0 = sp.t0(n - 1 - step);
+      const int64_t ch = (int64_t)ci * H + h;
+      mbar_expect_tx(&sm.bar[slot], BSTAGE_N_TX);
+      bulk_g2s(s.M, chblk(w, ch) + CB_M, CB_KU1 - CB_M, &sm.bar[slot]);
+      tma_load_2d(s.dy, &nmap.dy, h * DV + col0, t0, &sm.bar[slot]);
+      tma_load_2d(s.g, &nmap.g, h * DV + col0, t0, &sm.bar[slot]);
+      tma_load_2d(s.o, &nmap.o, h * DV + col0, t0, &sm.bar[slot]);
+    }
+  };
+  // (norm warps) this thread's 16 values of stage k's row nr, rows past the chunk end as zero
+  auto norm_vals = [&](const BChainStageN& s, int L, float* dyv, float* ov, float* sgv) {
 #pragma unroll
     for (int hh = 0; hh < 2; hh++) {
       const int o8 = nr * NSC + 16 * nh + 8 * hh;
@@ -1644,13 +1763,26 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
       ov[8 * hh] = a.x; ov[8 * hh + 1] = a.y; ov[8 * hh + 2] = a.z; ov[8 * hh + 3] = a.w;
       ov[8 * hh + 4] = b.x; ov[8 * hh + 5] = b.y; ov[8 * hh + 6] = b.z; ov[8 * hh + 7] = b.w;
     }
+    const bool live = nr < L;
 #pragma unroll
-    for (int j = 0; j < 16; j++) sgv[j] = sigmoid_fast(sgv[j]);  // s_j
+    for (int j = 0; j < 16; j++) {
+      sgv[j] = live ? sigmoid_fast(sgv[j]) : 0.f;  // s_j
+      if (!live) dyv[j] = ov[j] = 0.f;
+    }
   };
-  auto norm_send = [&](auto k) {
+  bool xfail = false, bad = false;
+  // (norm warps) stage k's dO: wait for the stage, send the row partials, receive the peer's,
+  // write the dO operand tile, dO and dg to global memory, and accumulate dw
+  auto norm_stage = [&](int k) {
+    BChainStageN& s = sm.st[k % NSTG];
+    if (!mbar_wait(&sm.bar[k % NSTG], (k / NSTG) & 1)) {
+      xfail = true;
+      return;
+    }
+    const int L = sp.L(n - 1 - k), t0 = sp.t0(n - 1 - k), slot = k % NX;
     float dyv[16], ov[16], sgv[16];
-    norm_vals(sm.st[k % NSTG], dyv, ov, sgv);
-    po = pa = 0.f;
+    norm_vals(s, L, dyv, ov, sgv);
+    float po = 0.f, pa = 0.f;
 #pragma unroll
     for (int j = 0; j < 16; j++) {
       po += ov[j] * ov[j];
@@ -1658,27 +1790,19 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
     }
     po += __shfl_xor_sync(0xffffffffu, po, 1);
     pa += __shfl_xor_sync(0xffffffffu, pa, 1);
-    const int slot = k % NX;
-    if (nh == 0) {
-      st_cluster_f32x2(xpart + (uint32_t)((slot * C + nr) * 8), po, pa);
-      mbar_arrive_remote(xbar + (uint32_t)(slot * 8));
-    }
-  };
-  auto norm_recv = [&](auto k) {
-    auto& s = sm.st[k % NSTG];
-    const int ci = ce - 1 - k, L = w.chunk_len[ci], t0 = w.chunk_tok0[ci], slot = k % NX;
+    if (nh == 0) st_async_f32x2(xpart + (uint32_t)((slot * C + nr) * 8), po, pa, xbar + (uint32_t)(slot * 8));
     float dOv[16];
     if (!mbar_wait_cluster(&sm.x.bar[slot], (k / NX) & 1)) {
-      xfail = true;  // bails at the next step's barrier
+      xfail = true;
 #pragma unroll
       for (int j = 0; j < 16; j++) dOv[j] = 0.f;
     } else {
-      float dyv[16], ov[16], sgv[16], dgv[16];
-      norm_vals(s, dyv, ov, sgv);
+      if (nt == 0) mbar_expect_tx(&sm.x.bar[slot], XBYTES);  // armed for stage k + NX
       const float2 pp = sm.x.part[slot][nr];
       const float To = po + pp.x, Ta = pa + pp.y;
       const float rr = 1.0f / sqrtf(To * (1.0f / DV) + io.neps);
       const float cc = rr * rr * rr * Ta * (1.0f / DV);
+      float dgv[16];
 #pragma unroll
       for (int j = 0; j < 16; j++) {
         const float sg = sgv[j], or_ = ov[j] * rr;
@@ -1709,102 +1833,85 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
       __nv_bfloat162* u2 = reinterpret_cast<__nv_bfloat162*>(&u);
 #pragma unroll
       for (int e = 0; e < 4; e++) u2[e] = __floats2bfloat162_rn(dOv[8 * hh + 2 * e], dOv[8 * hh + 2 * e + 1]);
-      *reinterpret_cast<uint4*>(const_cast<bf16*>(s.dO) + opix(nr, 16 * nh + 8 * hh, NSC)) = u;
+      *reinterpret_cast<uint4*>(s.dO + opix(nr, 16 * nh + 8 * hh, NSC)) = u;
     }
   };
-  if constexpr (NORM) {
-    if (n > 0) {  // stage 0's dO before the chain starts
-      cp_wait_all();
-      __syncthreads();
-      norm_send(0);
-      norm_recv(0);
-    }
-  }
+  for (int s = 0; s < NSTG - 1; s++) prefetch(s);
+  if (!chain && n > 0) norm_stage(0);  // stage 0's dO before the chain starts
+  float acc[2][4];
+  zero(acc);
+  const int mI = warp & 1, jn = (warp >> 1) & 1;
   for (int step = 0; step < n; step++) {
-    auto& s = sm.st[step % NSTG];
+    const BChainStageN& s = sm.st[step % NSTG];
     const int ci = ce - 1 - step;
-    if (NORM) asm volatile("cp.async.wait_group 0;\n" ::);  // the next stage's dy, g, o too
-    else asm volatile("cp.async.wait_group %0;\n" ::"n"(NSTG - 2));
     if (__syncthreads_or(!mbar_wait(&sm.bar[step % NSTG], (step / NSTG) & 1) || xfail)) {  // a wait ran out
       for (int k2 = step; k2 < n && k2 < step + NSTG - 1; k2++) mbar_wait(&sm.bar[k2 % NSTG], (k2 / NSTG) & 1);
-      cp_wait_all();
       if (tid == 0) atomicExch(w.err, -7);
       bad = true;
       break;
-    }  // this step's stage (and dO tile) and the last state update are visible
+    }  // this step's stage, its dO tile and the last state update are visible
     prefetch(step + NSTG - 1);
-    if constexpr (NORM) {
-      if (step + NSTG < n && tid < C) {  // the rows of the stage after the one just issued, into L2
-        const int c3 = ce - 1 - (step + NSTG), t3 = w.chunk_tok0[c3];
-        if (tid < w.chunk_len[c3]) {
-          const size_t gi = ((size_t)(t3 + tid) * H + h) * DV + col0;
-          prefetch_l2((const bf16*)io.dy + gi);
-          prefetch_l2((const bf16*)io.ng + gi);
-          prefetch_l2(w.nO + gi);
-        }
-      }
-      if (step + 1 < n) norm_send(step + 1);
+    if (chain) {
+      const Op Mo{const_cast<bf16*>(s.M), const_cast<bf16*>(s.M) + DK * DK, DK};
+      const Op QWo{const_cast<bf16*>(s.QW), const_cast<bf16*>(s.QW) + C * DK, DK};
+      const Op dOo{const_cast<bf16*>(s.dO), nullptr, NSC};
+      float ax[2][4];
+      zero(acc);
+      zero(ax);
+      gemm3<1, true, true>(ax, QWo, 16 * mI, 0, dOo, 16 * jn, 0, C / 16);
+      gemm3<1, true, true>(acc, Mo, 16 * mI, 0, dS, 16 * jn, 0, DK / 16);
+      slice_to_global(w.sdS + ((int64_t)ci * H + h) * 2 * DK * DV, sm.dS, col0, tid);
+#pragma unroll
+      for (int jj = 0; jj < 2; jj++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) acc[jj][e] += ax[jj][e];
+      asm volatile("bar.sync 1, %0;\n" ::"n"(CTH) : "memory");  // the chain warps' reads of the state tile are done
+#pragma unroll
+      for (int jj = 0; jj < 2; jj++)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++)
+          op_store2(dS, 16 * mI + gq + 8 * hh, 16 * jn + 8 * jj + 2 * tq, acc[jj][2 * hh], acc[jj][2 * hh + 1]);
+    } else if (step + 1 < n) {
+      norm_stage(step + 1);  // the next stage's dO, while the chain works on this one
     }
-    const Op Mo{const_cast<bf16*>(s.M), const_cast<bf16*>(s.M) + DK * DK, DK};
-    const Op QWo{const_cast<bf16*>(s.QW), const_cast<bf16*>(s.QW) + C * DK, DK};
-    const Op dOo{const_cast<bf16*>(s.dO), nullptr, NSC};
-    float ax[2][4];
-    zero(acc);
-    zero(ax);
-    gemm3<1, true, true>(ax, QWo, 16 * mI, 0, dOo, 16 * jn, 0, C / 16);
-    gemm3<1, true, true>(acc, Mo, 16 * mI, 0, dS, 16 * jn, 0, DK / 16);
-    slice_to_global(w.sdS + ((int64_t)ci * H + h) * 2 * DK * DV, sm.dS, col0, threadIdx.x);
-#pragma unroll
-    for (int jj = 0; jj < 2; jj++)
-#pragma unroll
-      for (int e = 0; e < 4; e++) acc[jj][e] += ax[jj][e];
-    if constexpr (NORM) {
-      if (step + 1 < n) norm_recv(step + 1);  // the exchange overlapped the products above
-    }
-    __syncthreads();  // every read of the state tile is done (and the next stage's dO tile written)
-#pragma unroll
-    for (int jj = 0; jj < 2; jj++)
-#pragma unroll
-      for (int hh = 0; hh < 2; hh++)
-        op_store2(dS, 16 * mI + gq + 8 * hh, 16 * jn + 8 * jj + 2 * tq, acc[jj][2 * hh], acc[jj][2 * hh + 1]);
   }
-  cp_wait_all();
-  if (NORM && __syncthreads_or(xfail) && !bad) {  // the last step's exchange ran out
+  if (__syncthreads_or(xfail) && !bad) {  // the last exchange ran out
     if (tid == 0) atomicExch(w.err, -7);
     bad = true;
   }
   if (io.dh0 && !bad && ok0) {
     if (n > 0) {
+      if (chain)
 #pragma unroll
-      for (int jj = 0; jj < 2; jj++)
+        for (int jj = 0; jj < 2; jj++)
 #pragma unroll
-        for (int hh = 0; hh < 2; hh++) {
-          const int i = 16 * mI + gq + 8 * hh, c = 16 * jn + 8 * jj + 2 * tq;
-          *reinterpret_cast<float2*>(io.dh0 + dh + i * DV + col0 + c) = make_float2(acc[jj][2 * hh], acc[jj][2 * hh + 1]);
-        }
+          for (int hh = 0; hh < 2; hh++) {
+            const int i = 16 * mI + gq + 8 * hh, c = 16 * jn + 8 * jj + 2 * tq;
+            *reinterpret_cast<float2*>(io.dh0 + dh + i * DV + col0 + c) =
+                make_float2(acc[jj][2 * hh], acc[jj][2 * hh + 1]);
+          }
     } else {
-      for (int idx = tid; idx < DK * NSC; idx += CTH) {
+      for (int idx = tid; idx < DK * NSC; idx += 2 * CTH) {
         const int i = idx / NSC, jc = idx % NSC;
         io.dh0[dh + i * DV + col0 + jc] = io.dh_final ? io.dh_final[dh + i * DV + col0 + jc] : 0.f;
       }
     }
   }
-  if constexpr (NORM) {
-    // dw partial of this (document, head): column sums over the 64 row-owning
-    // threads of each half, in a fixed order, through the (now idle) stages
-    float* red = reinterpret_cast<float*>(&sm.st[0]);  // [CTH][16]
-    __syncthreads();
+  // dw partial of this (document, head): column sums over the 64 rows (the norm
+  // threads of each half), in a fixed order, through the idle stage 0
+  float* red = reinterpret_cast<float*>(&sm.st[0]);  // [CTH][16]
+  __syncthreads();
+  if (!chain)
 #pragma unroll
-    for (int j = 0; j < 16; j++) red[tid * 16 + j] = dwacc[j];
-    __syncthreads();
-    if (tid < NSC && !bad && ok0) {
-      const int hf = tid >> 4, j = tid & 15;
-      float a = 0.f;
-      for (int r = 0; r < C; r++) a += red[(2 * r + hf) * 16 + j];
-      w.pdw[((int64_t)doc * H + h) * DV + col0 + tid] = a;
-    }
-    cluster_sync();  // the peer no longer touches this CTA's shared memory
+    for (int j = 0; j < 16; j++) red[nt * 16 + j] = dwacc[j];
+  __syncthreads();
+  if (tid < NSC && !bad && ok0) {
+    const int hf = tid >> 4, j = tid & 15;
+    float a = 0.f;
+    for (int r = 0; r < C; r++) a += red[(2 * r + hf) * 16 + j];
+    w.pdw[((int64_t)doc * H + h) * DV + col0 + tid] = a;
   }
+  cluster_sync();  // the peer no longer touches this CTA's shared memory
 }
 
 // ------------------------------------------------------------ backward chunk kernels
@@ -2765,14 +2872,16 @@ static_assert(sizeof(fast::FwdSm) <= 232448, "fused forward shared memory exceed
 static_assert(sizeof(fast::ChunkSm) <= 113 * 1024, "per-chunk forward must fit two CTAs per SM");
 
 static_assert(sizeof(fast::GradSm) <= 112 * 1024, "chunk-gradient kernel must fit two CTAs per SM");
-static_assert(sizeof(fast::BChainSm<true>) <= 113 * 1024, "fused-norm reverse chain must fit two CTAs per SM");
+static_assert(sizeof(fast::BChainSmN) <= 113 * 1024, "fused-norm reverse chain must fit two CTAs per SM");
+static_assert(sizeof(fast::FChainSm<true>) <= 113 * 1024, "fused-norm forward chain must fit two CTAs per SM");
+static_assert(sizeof(fast::FChainSm<false>) <= 113 * 1024 && sizeof(fast::BChainSm) <= 113 * 1024,
+              "the chains must fit two CTAs per SM");
 static_assert(sizeof(fast::GateSm<false>) <= 75 * 1024, "gate kernel must fit three CTAs per SM");
 static_assert(sizeof(fast::GateSm<true>) <= 113 * 1024, "gate kernel (fused convolution) must fit two CTAs per SM");
 
 bool fast_path(int dtype, int dk, int dv) { return dtype == 0 && dk == fast::DK && dv == fast::DV; }
 
-bool encode_tmaps(TMaps* tm, const void* q, const void* k, const void* v, const void* f, int Ntok, int H, int dk,
-                  int dv, bool channel_gate) {
+static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 enc = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult qr;
@@ -2782,6 +2891,32 @@ bool encode_tmaps(TMaps* tm, const void* q, const void* k, const void* v, const 
       return nullptr;
     return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }();
+  return enc;
+}
+
+// One 2-D map over [Ntok][H dh] elements (esz bytes each) with a box of bx columns x C tokens.
+static bool encode_rows(CUtensorMap* m, const void* base, int Ntok, int H, int dh, int bx, bool fp32) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
+  if (!enc) return false;
+  const int esz = fp32 ? 4 : 2;
+  const cuuint64_t dims[2] = {(cuuint64_t)H * dh, (cuuint64_t)Ntok};
+  const cuuint64_t strides[1] = {(cuuint64_t)H * dh * esz};
+  const cuuint32_t box[2] = {(cuuint32_t)bx, (cuuint32_t)C};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_nmaps(NMaps* nm, const void* g, const void* dy, const float* o, int Ntok, int H, int dv) {
+  *nm = NMaps{};
+  return encode_rows(&nm->g, g, Ntok, H, dv, fast::NSC, false) && (!dy || encode_rows(&nm->dy, dy, Ntok, H, dv, fast::NSC, false)) &&
+         (!o || encode_rows(&nm->o, o, Ntok, H, dv, fast::NSC, true));
+}
+
+bool encode_tmaps(TMaps* tm, const void* q, const void* k, const void* v, const void* f, int Ntok, int H, int dk,
+                  int dv, bool channel_gate) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
   if (!enc) return false;
   auto one = [&](CUtensorMap* m, const void* base, int dh) {  // [Ntok][H dh] bf16, box dh x C
     const cuuint64_t dims[2] = {(cuuint64_t)H * dh, (cuuint64_t)Ntok};
@@ -2822,14 +2957,14 @@ cudaError_t launch_fast_fwd(const Dims& d0, const FwdIO& io, const Ws& w, cudaSt
     prof_end(K_FWD_CHAIN, st);
     return cudaGetLastError();
   }
-  const size_t s1 = sizeof(fast::ChunkSm), s2 = sizeof(fast::FChainSm);
+  const size_t s1 = sizeof(fast::ChunkSm), s2 = sizeof(fast::FChainSm<false>), s2n = sizeof(fast::FChainSm<true>);
   e = cudaFuncSetAttribute(fast::fwd_chunk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(fast::fwd_chunk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(fast::fwd_state_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(fast::fwd_state_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
+    e = cudaFuncSetAttribute(fast::fwd_state_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2n);
   if (e != cudaSuccess) return e;
   prof_begin(K_FWD_CHUNK, st);
   if (d.conv)
@@ -2840,13 +2975,15 @@ cudaError_t launch_fast_fwd(const Dims& d0, const FwdIO& io, const Ws& w, cudaSt
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const dim3 grid(d.n_docs, d.H, fast::DV / fast::NSC);
+  NMaps nm = {};
   if (d.norm) {  // the two column halves of a (document, head) as one cluster
+    if (!encode_nmaps(&nm, io.ng, nullptr, nullptr, d.Ntok, d.H, fast::DV)) return cudaErrorInvalidValue;
     prof_begin(K_FWD_STATE_NORM, st);
-    e = launch_cluster(fast::fwd_state_kernel<true>, grid, dim3(2 * fast::CTH), s2, st, 2, true, d, io, w);
+    e = launch_cluster(fast::fwd_state_kernel<true>, grid, dim3(2 * fast::CTH), s2n, st, 2, true, d, io, w, nm);
     prof_end(K_FWD_STATE_NORM, st);
   } else {
     prof_begin(K_FWD_STATE, st);
-    e = launch_pdl(fast::fwd_state_kernel<false>, grid, dim3(2 * fast::CTH), s2, st, d, io, w);
+    e = launch_pdl(fast::fwd_state_kernel<false>, grid, dim3(2 * fast::CTH), s2, st, d, io, w, nm);
     prof_end(K_FWD_STATE, st);
   }
   return e != cudaSuccess ? e : cudaGetLastError();
@@ -2855,12 +2992,11 @@ cudaError_t launch_fast_fwd(const Dims& d0, const FwdIO& io, const Ws& w, cudaSt
 cudaError_t launch_fast_bwd(const Dims& d0, const BwdIO& io, const Ws& w, cudaStream_t st) {
   Dims d = d0;
   d.ahead = 0;  // the backward's chunk kernels prefetch nothing (measured: the L2 prefetch of the next wave slowed them)
-  const size_t sc = sizeof(fast::BChainSm<false>), scn = sizeof(fast::BChainSm<true>), s1 = sizeof(fast::GradSm),
+  const size_t sc = sizeof(fast::BChainSm), scn = sizeof(fast::BChainSmN), s1 = sizeof(fast::GradSm),
                s2 = d.conv ? sizeof(fast::GateSm<true>) : sizeof(fast::GateSm<false>);
-  cudaError_t e =
-      cudaFuncSetAttribute(fast::bwd_scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
+  cudaError_t e = cudaFuncSetAttribute(fast::bwd_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(fast::bwd_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scn);
+    e = cudaFuncSetAttribute(fast::bwd_scan_norm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scn);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(fast::bwd_grad_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
   if (e == cudaSuccess)
@@ -2874,12 +3010,14 @@ cudaError_t launch_fast_bwd(const Dims& d0, const BwdIO& io, const Ws& w, cudaSt
   if (e != cudaSuccess) return e;
   const dim3 grid(d.n_docs, d.H, fast::DV / fast::NSC);
   if (d.norm) {  // the two column halves of a (document, head) as one cluster
+    NMaps nm;
+    if (!encode_nmaps(&nm, io.ng, io.dy, w.nO, d.Ntok, d.H, fast::DV)) return cudaErrorInvalidValue;
     prof_begin(K_BWD_SCAN_NORM, st);
-    e = launch_cluster(fast::bwd_scan_kernel<true>, grid, dim3(fast::CTH), scn, st, 2, false, d, io, w);
+    e = launch_cluster(fast::bwd_scan_norm_kernel, grid, dim3(2 * fast::CTH), scn, st, 2, false, d, io, w, nm);
     prof_end(K_BWD_SCAN_NORM, st);
   } else {
     prof_begin(K_BWD_SCAN, st);
-    fast::bwd_scan_kernel<false><<<grid, fast::CTH, sc, st>>>(d, io, w);
+    fast::bwd_scan_kernel<<<grid, fast::CTH, sc, st>>>(d, io, w);
     prof_end(K_BWD_SCAN, st);
     e = cudaGetLastError();
   }

@@ -164,6 +164,12 @@ struct TMaps {
 // (f only for the per-channel gate); false if the driver refuses.
 bool encode_tmaps(TMaps* tm, const void* q, const void* k, const void* v, const void* f, int Ntok, int H, int dk,
                   int dv, bool channel_gate);
+// The fused gated norm's per-row tensors, [Ntok][H dv] with a box of 32 value
+// columns x C tokens: the gate g and dy (bf16) and the saved fp32 o.
+struct NMaps {
+  CUtensorMap g, dy, o;
+};
+bool encode_nmaps(NMaps* nm, const void* g, const void* dy, const float* o, int Ntok, int H, int dv);
 
 // Launch wrappers (return cudaGetLastError of their launches).
 // Launches kernel k with the programmatic-stream-serialization attribute (see pdl_wait).

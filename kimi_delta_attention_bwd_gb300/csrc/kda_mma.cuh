@@ -344,7 +344,7 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 // ------------------------------------------------------------ thread-block clusters
 // Distributed shared memory between the CTAs of a cluster: an address of this
 // CTA's shared memory mapped to the same variable in CTA `rank` of the
-// cluster, remote stores and remote mbarrier arrivals through it, and the
+// cluster, asynchronous remote stores that signal the peer's mbarrier, and the
 // cluster-wide barrier.  A CTA must not exit while a peer may still access
 // its shared memory: kernels that exchange end with cluster_sync().
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -357,16 +357,20 @@ __device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, float a, float b) {
-  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};\n" ::"r"(addr), "f"(a), "f"(b) : "memory");
+// Asynchronous store of two floats into a peer CTA's shared memory that
+// completes 8 bytes of the transaction count of the peer's mbarrier `bar_addr`
+// when the data has landed: the receiver's barrier phase (armed with
+// mbar_expect_tx for the bytes it expects) completes with the data visible,
+// and the sender needs no release fence.  (A release-ordered remote arrival
+// would first wait for every global store the sending thread still has in
+// flight, about a microsecond under load.)
+__device__ __forceinline__ void st_async_f32x2(uint32_t addr, float a, float b, uint32_t bar_addr) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];\n" ::"r"(addr),
+               "f"(a), "f"(b), "r"(bar_addr)
+               : "memory");
 }
-// Arrives on an mbarrier of another CTA of the cluster; release at cluster
-// scope orders this thread's earlier (remote) stores before the arrival.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(bar_addr) : "memory");
-}
-// mbar_wait with acquire at cluster scope: the arrivals came from a peer CTA,
-// whose stores before them are visible afterwards.  Bounded like mbar_wait.
+// mbar_wait with acquire at cluster scope, for phases completed by a peer
+// CTA's asynchronous stores.  Bounded like mbar_wait.
 __device__ __forceinline__ uint32_t mbar_try_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
