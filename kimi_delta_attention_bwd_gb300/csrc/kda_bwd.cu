@@ -230,17 +230,20 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   __syncthreads();
   // T = (I + A)^-1, held transposed (Tt[c][r] = T[r][c])
   unit_lower_inverse_t<GTH>(dAm, Tt, slab);
+  // the products below on the tensor cores: the accumulator in TMEM, the slab
+  // buffers over the inverse's scratch (done: the inverse ends with a barrier)
+  constexpr int NX = (DK > DV ? DK : DV) > C ? (DK > DV ? DK : DV) : C;
+  __shared__ uint32_t t5slot;
+  __shared__ uint64_t t5bar[2];
+  Tc5 t5 = tc5_setup(&t5slot, t5bar, slab, w.err);
 
   // ---- E = U - W S (scratch), dgamma; then with the value columns as k:
   //      dQG = scale dO S^T, dW = -dE S^T, dKd = E dS'^T (products staged
-  //      through shared memory, every global read coalesced)
-  {
-    TcAcc<C, DV, GTH> acc;
-    tc_zero<C, DV, GTH>(acc);
-    cta_mma<C, DV, DK, GTH, true, true>(acc, slab, [&](int m, int k) { return Wg[m * DK + k]; },
-                                    [&](int k, int n) { return Sg[k * DV + n]; });
-    tc_out<C, DV, GTH>(acc, [&](int m, int n, float v) { E[m * DV + n] = Ug[m * DV + n] - v; });
-  }
+  //      through shared memory, every global read coalesced; each product's
+  //      operands were written before a barrier of an earlier product)
+  cta_tc<DV, DK, GTH, NX, true, true>(t5, false, [&](int m, int k) { return Wg[m * DK + k]; },
+                                      [&](int k, int n) { return Sg[k * DV + n]; });
+  tc5_out<DV, GTH>(t5, [&](int m, int n, float v) { E[m * DV + n] = Ug[m * DV + n] - v; });
   for (int i = warp; i < DK; i += nw) {
     float acc = 0.f;
     for (int jj = lane; jj < DV; jj += 32) acc += dSg[i * DV + jj] * Sg[i * DV + jj];
@@ -249,42 +252,24 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
   }
   const TI* dOc = dO + ((int64_t)t0 * H + h) * DV;  // row r of the chunk at dOc + r H dv
   auto fdO = [&](int m, int k) { return m < L ? ldf(dOc + (int64_t)m * H * DV + k) : 0.f; };
-  {
-    TcAcc<C, DK, GTH> acc;
-    tc_zero<C, DK, GTH>(acc);
-    cta_mma<C, DK, DV, GTH, true, false>(acc, slab, fdO, [&](int k, int n) { return Sg[n * DV + k]; });
-    tc_out<C, DK, GTH>(acc, [&](int m, int n, float v) { dQG[m * DK + n] = scale * v; });
-    tc_zero<C, DK, GTH>(acc);
-    cta_mma<C, DK, DV, GTH, true, false>(acc, slab, [&](int m, int k) { return dEg[m * DV + k]; },
-                                     [&](int k, int n) { return Sg[n * DV + k]; });
-    tc_out<C, DK, GTH>(acc, [&](int m, int n, float v) { dW[m * DK + n] = -v; });
-    tc_zero<C, DK, GTH>(acc);
-    cta_mma<C, DK, DV, GTH, true, false>(acc, slab, [&](int m, int k) { return E[m * DV + k]; },
-                                     [&](int k, int n) { return dSg[n * DV + k]; });
-    tc_out<C, DK, GTH>(acc, [&](int m, int n, float v) { dKd[m * DK + n] = v; });
-  }
+  cta_tc<DK, DV, GTH, NX, true, false>(t5, false, fdO, [&](int k, int n) { return Sg[n * DV + k]; });
+  tc5_out<DK, GTH>(t5, [&](int m, int n, float v) { dQG[m * DK + n] = scale * v; });
+  cta_tc<DK, DV, GTH, NX, true, false>(t5, false, [&](int m, int k) { return dEg[m * DV + k]; },
+                                       [&](int k, int n) { return Sg[n * DV + k]; });
+  tc5_out<DK, GTH>(t5, [&](int m, int n, float v) { dW[m * DK + n] = -v; });
+  cta_tc<DK, DV, GTH, NX, true, false>(t5, false, [&](int m, int k) { return E[m * DV + k]; },
+                                       [&](int k, int n) { return dSg[n * DV + k]; });
+  tc5_out<DK, GTH>(t5, [&](int m, int n, float v) { dKd[m * DK + n] = v; });
 
   // ---- dP = scale dO E^T (inclusive lower, rows < L), YW = T^T dW, YU = T^T dE
-  {
-    TcAcc<C, C, GTH> acc;
-    tc_zero<C, C, GTH>(acc);
-    cta_mma<C, C, DV, GTH, true, false>(acc, slab, fdO, [&](int k, int n) { return E[n * DV + k]; });
-    tc_out<C, C, GTH>(acc, [&](int m, int n, float v) { dPm[m * C + n] = n <= m && m < L ? scale * v : 0.f; });
-  }
-  {
-    TcAcc<C, DK, GTH> acc;
-    tc_zero<C, DK, GTH>(acc);
-    cta_mma<C, DK, C, GTH, true, true>(acc, slab, [&](int m, int k) { return Tt[m * C + k]; },
-                                    [&](int k, int n) { return dW[k * DK + n]; });
-    tc_out<C, DK, GTH>(acc, [&](int m, int n, float v) { YW[m * DK + n] = v; });
-  }
-  {
-    TcAcc<C, DV, GTH> acc;
-    tc_zero<C, DV, GTH>(acc);
-    cta_mma<C, DV, C, GTH, true, true>(acc, slab, [&](int m, int k) { return Tt[m * C + k]; },
-                                    [&](int k, int n) { return dEg[k * DV + n]; });
-    tc_out<C, DV, GTH>(acc, [&](int m, int n, float v) { YU[m * DV + n] = v; });
-  }
+  cta_tc<C, DV, GTH, NX, true, false>(t5, false, fdO, [&](int k, int n) { return E[n * DV + k]; });
+  tc5_out<C, GTH>(t5, [&](int m, int n, float v) { dPm[m * C + n] = n <= m && m < L ? scale * v : 0.f; });
+  cta_tc<DK, C, GTH, NX, true, true>(t5, false, [&](int m, int k) { return Tt[m * C + k]; },
+                                     [&](int k, int n) { return dW[k * DK + n]; });
+  tc5_out<DK, GTH>(t5, [&](int m, int n, float v) { YW[m * DK + n] = v; });
+  cta_tc<DV, C, GTH, NX, true, true>(t5, false, [&](int m, int k) { return Tt[m * C + k]; },
+                                     [&](int k, int n) { return dEg[k * DV + n]; });
+  tc5_out<DV, GTH>(t5, [&](int m, int n, float v) { YU[m * DV + n] = v; });
   __syncthreads();
 
   // ---- dv = beta YU;  dbeta from U and W;  dA = -(YU U^T + YW W^T) strict lower
@@ -300,15 +285,12 @@ __global__ void __launch_bounds__(GTH) bwd_intra_kernel(Dims d, BwdIO io, Ws w) 
     acc = warp_sum(acc);
     if (lane == 0) dbet[r] += acc;
   }
-  {
-    TcAcc<C, C, GTH> acc;
-    tc_zero<C, C, GTH>(acc);
-    cta_mma<C, C, DV, GTH, true, false>(acc, slab, [&](int m, int k) { return YU[m * DV + k]; },
-                                    [&](int k, int n) { return Ug[n * DV + k]; });
-    cta_mma<C, C, DK, GTH, true, false>(acc, slab, [&](int m, int k) { return YW[m * DK + k]; },
-                                    [&](int k, int n) { return Wg[n * DK + k]; });
-    tc_out<C, C, GTH>(acc, [&](int m, int n, float v) { dAm[m * C + n] = n < m ? -v : 0.f; });
-  }
+  cta_tc<C, DV, GTH, NX, true, false>(t5, false, [&](int m, int k) { return YU[m * DV + k]; },
+                                      [&](int k, int n) { return Ug[n * DV + k]; });
+  cta_tc<C, DK, GTH, NX, true, false>(t5, true, [&](int m, int k) { return YW[m * DK + k]; },
+                                      [&](int k, int n) { return Wg[n * DK + k]; });
+  tc5_out<C, GTH>(t5, [&](int m, int n, float v) { dAm[m * C + n] = n < m ? -v : 0.f; });
+  tc5_release(t5);
   __syncthreads();
   for (int r = warp; r < L; r += nw) {
     float acc = 0.f;
@@ -496,7 +478,7 @@ static cudaError_t bwd_scan_launch(const Dims& d, const BwdIO& io, const Ws& w, 
 template <typename TI, int DK, int DV>
 static cudaError_t bwd_intra_launch(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st) {
   constexpr int NMAX = DK > DV ? DK : DV;
-  size_t smem = sizeof(float) * (3 * C * DK + 4 * C * C + 5 * C + DK + 32 + tc_slab_floats(C, NMAX > C ? NMAX : C));
+  size_t smem = sizeof(float) * (3 * C * DK + 4 * C * C + 5 * C + DK + 32 + tc5_slab_floats(NMAX > C ? NMAX : C));
   cudaError_t e = cudaFuncSetAttribute(bwd_intra_kernel<TI, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(d.nc_max, d.H);

@@ -127,22 +127,22 @@ __global__ void __launch_bounds__(GTH) fwd_intra_kernel(Dims d, FwdIO io, Ws w) 
     xk[idx] = bet[r] * kh[idx] * eG;
   }
   for (int i = tid; i < DK; i += blockDim.x) w.gam[ch * DK + i] = ex2(Glast[i]);
-  // W = T XK and U = T diag(beta) V (T unit lower, its upper part zero)
-  {
-    TcAcc<C, DK, GTH> acc;
-    tc_zero<C, DK, GTH>(acc);
-    cta_mma<C, DK, C, GTH, false, true>(acc, slab, [&](int m, int k) { return Tt[k * C + m]; },
-                                   [&](int k, int n) { return xk[k * DK + n]; });
-    tc_out<C, DK, GTH>(acc, [&](int m, int n, float v) { Wg[m * DK + n] = v; });
-  }
+  // W = T XK and U = T diag(beta) V (T unit lower, its upper part zero) on the
+  // tensor cores: the accumulator in TMEM, the slab buffers over the inverse's
+  // scratch; tc5_setup's barrier also orders the XK writes above before the
+  // product reads them
+  constexpr int NX = (DK > DV ? DK : DV) > C ? (DK > DV ? DK : DV) : C;
+  __shared__ uint32_t t5slot;
+  __shared__ uint64_t t5bar[2];
+  Tc5 t5 = tc5_setup(&t5slot, t5bar, slab, w.err);
+  cta_tc<DK, C, GTH, NX, false, true>(t5, false, [&](int m, int k) { return Tt[k * C + m]; },
+                                      [&](int k, int n) { return xk[k * DK + n]; });
+  tc5_out<DK, GTH>(t5, [&](int m, int n, float v) { Wg[m * DK + n] = v; });
   float* Ug = w.U + ch * C * DV;
-  {
-    TcAcc<C, DV, GTH> acc;
-    tc_zero<C, DV, GTH>(acc);
-    cta_mma<C, DV, C, GTH, false, true>(acc, slab, [&](int m, int k) { return Tt[k * C + m]; },
-                                   [&](int k, int n) { return bet[k] * vv[k * DV + n]; });
-    tc_out<C, DV, GTH>(acc, [&](int m, int n, float v) { Ug[m * DV + n] = v; });
-  }
+  cta_tc<DV, C, GTH, NX, false, true>(t5, false, [&](int m, int k) { return Tt[k * C + m]; },
+                                      [&](int k, int n) { return bet[k] * vv[k * DV + n]; });
+  tc5_out<DV, GTH>(t5, [&](int m, int n, float v) { Ug[m * DV + n] = v; });
+  tc5_release(t5);
 }
 
 
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(STH) fwd_scan_kernel(Dims d, FwdIO io, Ws w) {
 template <typename TI, int DK, int DV>
 static cudaError_t fwd_intra_launch(const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st) {
   constexpr int NMAX = DK > DV ? DK : DV;
-  size_t smem = sizeof(float) * (3 * C * DK + C * DV + 2 * C * C + C + tc_slab_floats(C, NMAX > C ? NMAX : C));
+  size_t smem = sizeof(float) * (3 * C * DK + C * DV + 2 * C * C + C + tc5_slab_floats(NMAX > C ? NMAX : C));
   cudaError_t e = cudaFuncSetAttribute(fwd_intra_kernel<TI, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(d.nc_max, d.H);

@@ -1,12 +1,14 @@
 // CTA-wide fp32-accurate products of the general kernels: M x N outputs of
 // sum_k A(m, k) B(k, n), with the operands staged through shared memory in
 // KS-wide slabs so that every global read is coalesced and every shared
-// read is a broadcast or conflict-free; on the tensor cores (split tf32) for
-// the per-chunk kernels, fp32 FMA for the scans.  Also the blocked inverse
-// of the unit lower chunk factor and an L2 prefetch helper.
+// read is a broadcast or conflict-free; on the 5th-generation tensor cores
+// (split bf16, tcgen05) for the per-chunk kernels, fp32 FMA for the scans.
+// Also the blocked inverse of the unit lower chunk factor and an L2 prefetch
+// helper.
 #pragma once
 #include "kda_internal.cuh"
 #include "kda_mma.cuh"
+#include "kda_tc.cuh"
 
 namespace kda {
 
@@ -142,132 +144,153 @@ __device__ __forceinline__ void prefetch_span(const float* p, int n) {
   for (int o = threadIdx.x * 32; o < n; o += NTH * 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(p + o));
 }
 
-// ---- the same products on the tensor cores (mma.sync m16n8k8, tf32 operands
-// split into a head and a remainder, hi*hi + hi*lo + lo*hi: about 21
-// significant bits, the accuracy of the fp32 loop above).  Warp w owns the
-// 16 x 8 output tiles w, w + NW, ...; the slabs hold each operand's head and
-// remainder with rows padded to 8 (mod 32) words, so that fragment loads
-// are conflict-free.
-template <int M, int N, int NTH>
-struct TcShape {
-  static constexpr int NW = NTH / 32, TN = N / 8, T = (M / 16) * TN, TPW = (T + NW - 1) / NW;
-  static constexpr int AP = M + 8, BP = N + 8;
-  static_assert(M % 16 == 0 && N % 8 == 0 && AP % 32 == 8 && BP % 32 == 8, "tile shape");
+// ---- the per-chunk products on the 5th-generation tensor cores.  Each KS-wide
+// slab of both operands is staged as bf16 head and remainder tiles (x = hi +
+// lo, hi*hi + hi*lo + lo*hi: the neglected lo*lo term is below 2^-16 of the
+// product) in the core-matrix layout of kda_mma.cuh, A with rows m and B with
+// rows n (both K-major); one thread issues the slab's tcgen05 MMAs into a TMEM
+// accumulator of M = 64 rows and N fp32 columns and commits them to the
+// slab buffer's mbarrier, while every thread loads the next slab into
+// registers.  Two slab buffers; a buffer is restaged once the MMAs that read it
+// have completed.
+struct Tc5 {
+  uint32_t tmem;          // accumulator base: 64 rows, TC5_COLS columns
+  uint64_t* bar;          // [2] MMA completion of each slab buffer
+  __nv_bfloat16* buf;     // [2][(64 + NMAX) * KS * 2] slab buffers, 128-byte aligned
+  int* err;               // set to -7 when a wait on the tensor core runs out
+  uint32_t ph[2];         // phase of each buffer's barrier
+  bool busy[2];           // MMAs issued on the buffer and not yet waited for
+  int next;               // buffer of the next slab
 };
-template <int M, int N, int NTH>
-using TcAcc = float[TcShape<M, N, NTH>::TPW][4];
-
-// Words of shared memory the tensor-core slabs of products with up to mmax
-// rows and nmax columns take.
-constexpr int tc_slab_floats(int mmax, int nmax) { return 2 * KS * (mmax + 8) + 2 * KS * (nmax + 8); }
-
-// Index (k, x) of element e < KS X of a slab: for an operand whose k index
-// is contiguous in memory, lanes take 4 consecutive k of 8 consecutive x
-// (16-byte global runs, and stores to distinct banks of the 8 (mod 32)
-// padded rows); otherwise lanes take consecutive x.
-template <int X, bool KC>
-__device__ __forceinline__ void slab_index(int e, int& k, int& x) {
-  if (KC) {
-    const int q = e >> 5, ln = e & 31;
-    k = (ln & 3) + 4 * (q % (KS / 4));
-    x = (ln >> 2) + 8 * (q / (KS / 4));
-  } else {
-    k = e / X;
-    x = e % X;
+constexpr int TC5_COLS = 128;  // N <= 128
+// Shared words the slab buffers of products with up to nmax columns take (with
+// the slack that aligns them).
+constexpr int tc5_slab_floats(int nmax) { return (64 + nmax) * KS * 2 + 32; }
+__device__ __forceinline__ __nv_bfloat16* tc5_align(float* p) {
+  return reinterpret_cast<__nv_bfloat16*>((reinterpret_cast<uintptr_t>(p) + 127) & ~(uintptr_t)127);
+}
+__device__ __forceinline__ void tc5_wait(Tc5& t, int bi) {
+  if (t.busy[bi]) {
+    if (!mma::mbar_wait(&t.bar[bi], t.ph[bi]) && threadIdx.x == 0) atomicExch(t.err, -7);
+    t.ph[bi] ^= 1u;
+    t.busy[bi] = false;
   }
 }
-
-// acc += sum over k < K of fa(m, k) fb(k, n) on the tensor cores, both
-// operands staged; AK / BN: A's k / B's n index is contiguous in memory.
-// Slab k0 + KS is loaded into registers while slab k0 is multiplied.  slab:
-// tc_slab_floats(M, N) words.  Every thread of the CTA must call it; it
-// starts with a barrier (the slab's previous readers, and the operands'
-// writers, are done) and ends without one.
-template <int M, int N, int K, int NTH, bool AK, bool BN, class FA, class FB>
-__device__ __forceinline__ void cta_mma(TcAcc<M, N, NTH>& acc, float* slab, FA fa, FB fb) {
-  using S = TcShape<M, N, NTH>;
-  static_assert(K % KS == 0 && (M * KS) % NTH == 0 && (N * KS) % NTH == 0, "k a multiple of the slab, slabs of the threads");
-  static_assert(!AK || M % 8 == 0, "row groups");
-  constexpr int PA = M * KS / NTH, PB = N * KS / NTH;
-  uint32_t* ah = reinterpret_cast<uint32_t*>(slab);
-  uint32_t* al = ah + KS * S::AP;
-  uint32_t* bh = al + KS * S::AP;
-  uint32_t* bl = bh + KS * S::BP;
-  float ra[PA], rb[PB];
+// D (TMEM) = (or +=, when accumulate) sum over k < K of fa(m, k) fb(k, n), M = 64.
+// AK / BN: A's k / B's n index is contiguous in memory (pairs of k are read
+// together).  Every thread of the CTA must call it; it ends with the MMAs
+// complete (tc5_out may read the accumulator) and without a barrier.  The
+// operands' writers must be separated from the call by a barrier.
+template <int N, int K, int NTH, int NMAX, bool AK, bool BN, class FA, class FB>
+__device__ __forceinline__ void cta_tc(Tc5& t, bool accumulate, FA fa, FB fb) {
+  constexpr int M = 64, NS = K / KS, QA = M * KS / 2, QB = N * KS / 2;  // bf16 pairs of a slab
+  constexpr int PA = (QA + NTH - 1) / NTH, PB = (QB + NTH - 1) / NTH, BUF = (64 + NMAX) * KS * 2;
+  static_assert(N % 8 == 0 && N <= NMAX && NMAX <= TC5_COLS && K % KS == 0 && KS % 16 == 0, "product shape");
+  float2 ra[PA], rb[PB];
+  auto ia = [](int p, int& m, int& k) {
+    if (AK) { m = p / (KS / 2); k = 2 * (p % (KS / 2)); } else { m = p % M; k = 2 * (p / M); }
+  };
+  auto ib = [](int p, int& n, int& k) {
+    if (BN) { n = p % N; k = 2 * (p / N); } else { n = p / (KS / 2); k = 2 * (p % (KS / 2)); }
+  };
   auto load = [&](int k0) {
 #pragma unroll
     for (int u = 0; u < PA; u++) {
-      int k, m;
-      slab_index<M, AK>(threadIdx.x + u * NTH, k, m);
-      ra[u] = fa(m, k0 + k);
+      const int p = threadIdx.x + u * NTH;
+      int m, k;
+      ia(p, m, k);
+      if (p < QA) ra[u] = make_float2(fa(m, k0 + k), fa(m, k0 + k + 1));
     }
 #pragma unroll
     for (int u = 0; u < PB; u++) {
-      int k, n;
-      slab_index<N, !BN>(threadIdx.x + u * NTH, k, n);
-      rb[u] = fb(k0 + k, n);
+      const int p = threadIdx.x + u * NTH;
+      int n, k;
+      ib(p, n, k);
+      if (p < QB) rb[u] = make_float2(fb(k0 + k, n), fb(k0 + k + 1, n));
     }
   };
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   load(0);
-  for (int k0 = 0; k0 < K; k0 += KS) {
-    __syncthreads();
+  for (int s = 0; s < NS; s++) {
+    const int bi = t.next;
+    t.next ^= 1;
+    tc5_wait(t, bi);  // the MMAs that last read this buffer are done
+    __nv_bfloat16* A = t.buf + bi * BUF;
+    __nv_bfloat16* B = A + 2 * M * KS;
+    const mma::Op OA{A, A + M * KS, KS}, OB{B, B + N * KS, KS};
 #pragma unroll
     for (int u = 0; u < PA; u++) {
-      int k, m;
-      slab_index<M, AK>(threadIdx.x + u * NTH, k, m);
-      mma::split_tf32(ra[u], ah[k * S::AP + m], al[k * S::AP + m]);
+      const int p = threadIdx.x + u * NTH;
+      int m, k;
+      ia(p, m, k);
+      if (p < QA) mma::op_store2(OA, m, k, ra[u].x, ra[u].y);
     }
 #pragma unroll
     for (int u = 0; u < PB; u++) {
-      int k, n;
-      slab_index<N, !BN>(threadIdx.x + u * NTH, k, n);
-      mma::split_tf32(rb[u], bh[k * S::BP + n], bl[k * S::BP + n]);
+      const int p = threadIdx.x + u * NTH;
+      int n, k;
+      ib(p, n, k);
+      if (p < QB) mma::op_store2(OB, n, k, rb[u].x, rb[u].y);
     }
+    mma::fence_async_smem();  // the staged tiles are visible to the tensor core
+    tc::fence_before();
     __syncthreads();
-    if (k0 + KS < K) load(k0 + KS);
-#pragma unroll
-    for (int k8 = 0; k8 < KS; k8 += 8) {
-#pragma unroll
-      for (int j = 0; j < S::TPW; j++) {
-        const int tile = warp + j * S::NW;
-        if (tile < S::T) {
-          const int m0 = 16 * (tile / S::TN) + g, n0 = 8 * (tile % S::TN) + g;
-          const int r0 = (k8 + t) * S::AP + m0, r1 = r0 + 4 * S::AP;
-          const int c0 = (k8 + t) * S::BP + n0, c1 = c0 + 4 * S::BP;
-          const uint32_t a0 = ah[r0], a1 = ah[r0 + 8], a2 = ah[r1], a3 = ah[r1 + 8];
-          const uint32_t b0 = bh[c0], b1 = bh[c1];
-          mma::mma_tf32(acc[j], a0, a1, a2, a3, b0, b1);
-          mma::mma_tf32(acc[j], a0, a1, a2, a3, bl[c0], bl[c1]);
-          mma::mma_tf32(acc[j], al[r0], al[r0 + 8], al[r1], al[r1 + 8], b0, b1);
-        }
-      }
+    if (threadIdx.x == 0) {
+      tc::fence_after();
+      tc::gemm_split(t.tmem, tc::kmaj(OA), tc::kmaj(OB), N, KS / 16, accumulate || s > 0);
+      tc::commit(&t.bar[bi]);
     }
+    t.busy[bi] = true;
+    if (s + 1 < NS) load((s + 1) * KS);
   }
+  tc5_wait(t, 0);
+  tc5_wait(t, 1);
+  tc::fence_after();
 }
-
-// Calls out(m, n, v) for every output of the warp's tiles held by this lane.
-template <int M, int N, int NTH, class F>
-__device__ __forceinline__ void tc_out(const TcAcc<M, N, NTH>& acc, F out) {
-  using S = TcShape<M, N, NTH>;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-#pragma unroll
-  for (int j = 0; j < S::TPW; j++) {
-    const int tile = warp + j * S::NW;
-    if (tile < S::T) {
-      const int m0 = 16 * (tile / S::TN) + g, n0 = 8 * (tile % S::TN) + 2 * t;
-      out(m0, n0, acc[j][0]);
-      out(m0, n0 + 1, acc[j][1]);
-      out(m0 + 8, n0, acc[j][2]);
-      out(m0 + 8, n0 + 1, acc[j][3]);
-    }
+// Calls out(m, n, v) for every accumulator element: warp w reads rows
+// 16 (w % 4) .. (its TMEM lane quarter) of the 8-column groups w / 4,
+// w / 4 + NTH / 128, ...  Ends with the reads complete (the next cta_tc may
+// overwrite the accumulator after its barrier).
+template <int N, int NTH, class F>
+__device__ __forceinline__ void tc5_out(const Tc5& t, F out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, gq = lane >> 2, tq = lane & 3;
+  for (int g = warp >> 2; g < N / 8; g += NTH / 128) {
+    float v[1][4];
+    tc::ld_frag<1>(t.tmem, 8 * g, v);
+    const int m0 = 16 * q + gq, n0 = 8 * g + 2 * tq;
+    out(m0, n0, v[0][0]);
+    out(m0, n0 + 1, v[0][1]);
+    out(m0 + 8, n0, v[0][2]);
+    out(m0 + 8, n0 + 1, v[0][3]);
   }
+  tc::fence_before();
 }
-
-template <int M, int N, int NTH>
-__device__ __forceinline__ void tc_zero(TcAcc<M, N, NTH>& acc) {
-#pragma unroll
-  for (int j = 0; j < TcShape<M, N, NTH>::TPW; j++) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+// Allocates the accumulator and initialises the barriers (every thread; warp 0
+// allocates).  slot / bar: shared memory.
+__device__ __forceinline__ Tc5 tc5_setup(uint32_t* slot, uint64_t* bar, float* slab, int* err) {
+  if (threadIdx.x < 32) tc::tmem_alloc(slot, TC5_COLS);
+  if (threadIdx.x == 0) {
+    mma::mbar_init(&bar[0], 1);
+    mma::mbar_init(&bar[1], 1);
+    mma::mbar_init_fence();
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  Tc5 t;
+  t.tmem = *slot;
+  t.bar = bar;
+  t.buf = tc5_align(slab);
+  t.err = err;
+  t.ph[0] = t.ph[1] = 0u;
+  t.busy[0] = t.busy[1] = false;
+  t.next = 0;
+  return t;
+}
+// Frees the accumulator (every thread; after the last tc5_out).
+__device__ __forceinline__ void tc5_release(const Tc5& t) {
+  tc::fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) tc::tmem_dealloc(t.tmem, TC5_COLS);
 }
 
 // Calls out(m, n, acc[q][e]) for every output this thread holds.

@@ -120,6 +120,17 @@ __device__ __forceinline__ void commit(uint64_t* bar) {
 template <int NT>
 __device__ __forceinline__ void ld_frag(uint32_t tbase, int c0, float (&v)[NT][4]);
 template <>
+__device__ __forceinline__ void ld_frag<1>(uint32_t tbase, int c0, float (&v)[1][4]) {
+  const uint32_t a = tbase + ((uint32_t)(32 * ((threadIdx.x >> 5) & 3)) << 16) + (uint32_t)c0;
+  uint32_t r[4];
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+  for (int e = 0; e < 4; e++) v[0][e] = __uint_as_float(r[e]);
+}
+template <>
 __device__ __forceinline__ void ld_frag<2>(uint32_t tbase, int c0, float (&v)[2][4]) {
   const uint32_t a = tbase + ((uint32_t)(32 * ((threadIdx.x >> 5) & 3)) << 16) + (uint32_t)c0;
   uint32_t r[8];
