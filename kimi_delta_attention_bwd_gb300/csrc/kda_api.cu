@@ -16,6 +16,7 @@ namespace kda {
 // start at a document start, so a state never crosses a document boundary
 // (torchtitan PR "[kimi k3] Support sample packing in KDA", Verification).
 // Equal-length rows use the same table with offsets b * T.
+constexpr int ORD_BUCKETS = 2048;  // document chunk counts the dispatch order sorts
 __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* cu, Dims d, Ws w) {
   __shared__ int s_bad;
   __shared__ int s_carry;
@@ -84,6 +85,57 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* cu, Di
     }
   }
   for (int j = s_carry + tid; j < d.nc_max; j += blockDim.x) w.chunk_len[j] = 0;
+  // The documents by decreasing chunk count: the general scans run one CTA per
+  // (document, head, column slice) in this order, longest first, so that a grid
+  // of more chains than resident CTAs ends about when its longest chain does
+  // instead of when a long chain dispatched last does.  A counting sort over the
+  // counts in shared memory; documents of equal count in any order (a chain's
+  // result does not depend on when it runs).  Counts past the buckets keep the
+  // index order.
+  if (d.fast) return;  // (the tensor-core chains keep the grid order)
+  __shared__ int s_cnt[ORD_BUCKETS];
+  __shared__ int s_max;
+  if (tid == 0) s_max = 0;
+  __syncthreads();  // doc_chunk0 (written above by other threads) is visible
+  int mx = 0;
+  for (int i = tid; i < n; i += blockDim.x) mx = max(mx, w.doc_chunk0[i + 1] - w.doc_chunk0[i]);
+  atomicMax(&s_max, mx);
+  for (int b = tid; b < ORD_BUCKETS; b += blockDim.x) s_cnt[b] = 0;
+  __syncthreads();
+  if (s_max >= ORD_BUCKETS) {
+    for (int i = tid; i < n; i += blockDim.x) w.doc_order[i] = i;
+    return;
+  }
+  for (int i = tid; i < n; i += blockDim.x) atomicAdd(&s_cnt[w.doc_chunk0[i + 1] - w.doc_chunk0[i]], 1);
+  __syncthreads();
+  {  // s_cnt[b] <- documents with more than b chunks: thread t owns buckets 2 (N - 1 - t) + {1, 0}
+    static_assert(ORD_BUCKETS == 2048, "two buckets per thread of a 1024-thread block");
+    const int lane = tid & 31, warp = tid >> 5, b0 = ORD_BUCKETS - 2 * (tid + 1);
+    const int c1 = s_cnt[b0 + 1], c0 = s_cnt[b0];
+    int x = c1 + c0;  // inclusive scan over the threads
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int y = s_wsum[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int z = __shfl_up_sync(0xffffffffu, y, o);
+        if (lane >= o) y += z;
+      }
+      s_wsum[lane] = y;
+    }
+    __syncthreads();
+    const int ex = x - (c1 + c0) + (warp > 0 ? s_wsum[warp - 1] : 0);
+    s_cnt[b0 + 1] = ex;
+    s_cnt[b0] = ex + c1;
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += blockDim.x) w.doc_order[atomicAdd(&s_cnt[w.doc_chunk0[i + 1] - w.doc_chunk0[i]], 1)] = i;
 }
 
 cudaError_t launch_chunk_table(const int32_t* cu, const Dims& d, const Ws& w, cudaStream_t st) {
@@ -125,7 +177,7 @@ static size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
   size_t total;
-  size_t off_err, off_nch, off_dc0, off_ct0, off_cl, off_cd;
+  size_t off_err, off_nch, off_dc0, off_ct0, off_cl, off_cd, off_ord;
   size_t off_W, off_U, off_P, off_QG, off_KD, off_gam, off_Sent, off_CH;
   size_t off_sT, off_sP, off_sW, off_sU, off_sA, off_gDP, off_gMA, off_gQG, off_gKD, off_gKG, off_gdg;
   size_t off_dE, off_dSn, off_pA, off_pdt, off_scr, off_nO, off_pdw, off_nrm, off_cg, off_cpart;
@@ -148,6 +200,7 @@ static Layout layout(const Dims& d, int for_bwd, bool fused = false) {
   L.off_ct0 = take(4 * (size_t)d.nc_max);
   L.off_cl = take(4 * (size_t)d.nc_max);
   L.off_cd = take(4 * (size_t)d.nc_max);
+  L.off_ord = take(4 * (size_t)d.n_docs);
   if (d.fast) {
     if (!fused) L.off_CH = take(4 * nch * (d.dk * d.dk + C * d.dk + d.dk * d.dv + C * d.dv));  // M, QW, KU, PU
     if (for_bwd) {
@@ -213,6 +266,7 @@ static Ws bind(void* ws, const Layout& L, const Dims& d, int for_bwd) {
   w.chunk_tok0 = (int32_t*)(p + L.off_ct0);
   w.chunk_len = (int32_t*)(p + L.off_cl);
   w.chunk_doc = (int32_t*)(p + L.off_cd);
+  w.doc_order = (int32_t*)(p + L.off_ord);
   w.W = at(L.off_W);
   w.U = at(L.off_U);
   w.P = at(L.off_P);

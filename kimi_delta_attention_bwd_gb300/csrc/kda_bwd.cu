@@ -26,7 +26,11 @@ constexpr int STH = 256;      // threads of the scan kernels
 // slab.
 template <typename TI, int DK, int DV>
 __global__ void __launch_bounds__(STH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
-  const int doc = blockIdx.x, h = blockIdx.y, c0col = blockIdx.z * NT, tid = threadIdx.x;
+  // one CTA per (document, head, column slice), slices fastest, then heads,
+  // then the documents in the chunk table's longest-first order
+  constexpr int NSL = DV / NT;
+  const int lin = blockIdx.x, c0col = (lin % NSL) * NT, h = (lin / NSL) % d.H, tid = threadIdx.x;
+  const int doc = w.doc_order[lin / (NSL * d.H)];
   if (!saved_ok(d, w.tag, w.err)) return;
   const int H = d.H;
   extern __shared__ __align__(16) float sm[];
@@ -468,7 +472,7 @@ static cudaError_t bwd_scan_launch(const Dims& d, const BwdIO& io, const Ws& w, 
   size_t smem = sizeof(float) * ((DK + 2 * C) * LDS + KS * ((DK > C ? DK : C) + 1));
   cudaError_t e = cudaFuncSetAttribute(bwd_scan_kernel<TI, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(d.n_docs, d.H, DV / NT);
+  dim3 grid((unsigned)d.n_docs * d.H * (DV / NT));
   prof_begin(K_BWD_SCAN, st);
   bwd_scan_kernel<TI, DK, DV><<<grid, STH, smem, st>>>(d, io, w);
   prof_end(K_BWD_SCAN, st);

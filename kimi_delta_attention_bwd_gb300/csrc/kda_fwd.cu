@@ -151,7 +151,11 @@ __global__ void __launch_bounds__(GTH) fwd_intra_kernel(Dims d, FwdIO io, Ws w) 
 // each step's products read the chunk's factors through the staged slab.
 template <typename TI, int DK, int DV>
 __global__ void __launch_bounds__(STH) fwd_scan_kernel(Dims d, FwdIO io, Ws w) {
-  const int doc = blockIdx.x, h = blockIdx.y, c0col = blockIdx.z * NT, tid = threadIdx.x;
+  // one CTA per (document, head, column slice), slices fastest, then heads,
+  // then the documents in the chunk table's longest-first order
+  constexpr int NSL = DV / NT;
+  const int lin = blockIdx.x, c0col = (lin % NSL) * NT, h = (lin / NSL) % d.H, tid = threadIdx.x;
+  const int doc = w.doc_order[lin / (NSL * d.H)];
   if (*w.err != 0) return;
   const int H = d.H;
   extern __shared__ __align__(16) float sm[];
@@ -236,7 +240,7 @@ static cudaError_t fwd_scan_launch(const Dims& d, const FwdIO& io, const Ws& w, 
   size_t smem = sizeof(float) * ((DK + C) * LDS + KS * ((DK > C ? DK : C) + 1));
   cudaError_t e = cudaFuncSetAttribute(fwd_scan_kernel<TI, DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(d.n_docs, d.H, DV / NT);
+  dim3 grid((unsigned)d.n_docs * d.H * (DV / NT));
   prof_begin(K_FWD_SCAN, st);
   fwd_scan_kernel<TI, DK, DV><<<grid, STH, smem, st>>>(d, io, w);
   prof_end(K_FWD_SCAN, st);

@@ -48,6 +48,7 @@ struct Ws {
   int32_t* chunk_tok0;  // [nc_max] first flattened token of each chunk
   int32_t* chunk_len;   // [nc_max] tokens in the chunk (1..C), 0 = unused
   int32_t* chunk_doc;   // [nc_max]
+  int32_t* doc_order;   // [n_docs] documents by decreasing chunk count (the general scans' dispatch order)
   // forward intermediates, per chunk-head ch = chunk * H + h
   float* W;    // [ch][C][dk]  T diag(beta) (K^ * Gamma)
   float* U;    // [ch][C][dv]  T diag(beta) V
