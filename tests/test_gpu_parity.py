@@ -140,8 +140,8 @@ def test_head_shapes_hard_cases(dk, dv, mode):
 
 @pytest.mark.parametrize("dk,dv", [(64, 128), (128, 128)])
 def test_head_shapes_fp32_io(dk, dv):
-    """fp32 inputs and outputs on the large-head kernels (split-tf32 products),
-    packed documents with partial chunks."""
+    """fp32 inputs and outputs on the large-head kernels (split-bf16 tensor-core
+    products), packed documents with partial chunks."""
     w = custom(1, 230, 2, dk, dv, dtype="f32", h0=True, dh_final=True)
     inp = make_inputs(w, seed=16, lengths=[100, 1, 129])
     gpu = run_gpu(inp, True)
