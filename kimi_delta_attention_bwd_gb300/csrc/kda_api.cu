@@ -653,7 +653,7 @@ static const char* const k_names[K_COUNT] = {"chunk_table", "fwd_intra", "fwd_sc
                                              "fwd_state", "bwd_grad",  "bwd_gate",   "decode",
                                              "norm_gate_fwd", "norm_gate_bwd", "norm_gate_reduce",
                                              "conv_fwd",  "conv_bwd",  "conv_reduce",
-                                             "fwd_state_norm", "bwd_scan_norm", "norm_dw_reduce"};
+                                             "fwd_state_norm", "bwd_scan_norm"};
 
 const char* kda_prof_kernel_name(int i) { return (i >= 0 && i < K_COUNT) ? k_names[i] : nullptr; }
 

@@ -424,6 +424,20 @@ __global__ void __launch_bounds__(RTH) bwd_reduce_kernel(Dims d, BwdIO io, Ws w)
   __shared__ float red[RTH];
   pdl_wait();  // the per-chunk partials of the kernel before
   if (!saved_ok(d, w.tag, w.err)) return;
+  if (h == H) {  // (fused gated norm, dv = 64) dw: the (document, head) partials in a fixed order
+    constexpr int NG = RTH / 64;
+    const int j = tid % 64, g = tid / 64, rows = d.n_docs * H;
+    float acc = 0.f;
+    for (int r = g; r < rows; r += NG) acc += w.pdw[(int64_t)r * 64 + j];
+    red[tid] = acc;
+    __syncthreads();
+    if (tid < 64) {
+      float t = 0.f;
+      for (int g2 = 0; g2 < NG; g2++) t += red[g2 * 64 + tid];
+      io.dw[tid] = t;
+    }
+    return;
+  }
   const int nc = *w.n_chunks;
   {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -516,7 +530,8 @@ cudaError_t launch_bwd_intra(int dtype, const Dims& d, const BwdIO& io, const Ws
 }
 cudaError_t launch_bwd_reduce(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st) {
   prof_begin(K_BWD_REDUCE, st);
-  const cudaError_t e = launch_pdl(bwd_reduce_kernel, dim3(d.H), dim3(RTH), 0, st, d, io, w);
+  const bool dw = d.fast && d.norm;  // one more block sums the fused norm's dw partials
+  const cudaError_t e = launch_pdl(bwd_reduce_kernel, dim3(d.H + (dw ? 1 : 0)), dim3(RTH), 0, st, d, io, w);
   prof_end(K_BWD_REDUCE, st);
   return e;
 }

@@ -3037,12 +3037,7 @@ cudaError_t launch_fast_bwd(const Dims& d0, const BwdIO& io, const Ws& w, cudaSt
   prof_end(K_BWD_GATE, st);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = launch_bwd_reduce(d, io, w, st);
-  if (e != cudaSuccess || !d.norm) return e;
-  prof_begin(K_NORM_DW, st);  // dw: the (document, head) partials summed in a fixed order
-  e = launch_sum_rows(w.pdw, d.n_docs * d.H, fast::DV, io.dw, st);
-  prof_end(K_NORM_DW, st);
-  return e;
+  return launch_bwd_reduce(d, io, w, st);  // (with the fused norm also dw, in one more block)
 }
 
 }  // namespace kda

@@ -34,7 +34,6 @@ enum KernelId {
   K_CONV_RED,
   K_FWD_STATE_NORM,
   K_BWD_SCAN_NORM,
-  K_NORM_DW,
   K_COUNT
 };
 
