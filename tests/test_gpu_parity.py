@@ -72,6 +72,33 @@ def test_packed_equals_separate_bitwise_torchtitan_fixture():
     assert not np.allclose(j["o"][96:], packed["o"][96:], atol=1e-3)
 
 
+def test_general_path_packed_equals_separate_bitwise():
+    """The general (large-head) kernels on a packed row of seven documents at
+    H 16, 128/128: 448 scan CTAs, more than one wave, dispatched longest
+    document first.  Every document's outputs and gradients equal its separate
+    run bit for bit, with its own h0 and dS_final."""
+    lens = [300, 1, 0, 250, 64, 585, 2]
+    w = custom(1, sum(lens), 16, 128, 128, dtype="bf16", h0=True, dh_final=True)
+    inp = make_inputs(w, seed=18, lengths=lens)
+    packed = run_gpu(inp, True)
+    cu = inp["cu_seqlens"].numpy()
+    for s in range(len(lens)):
+        t0, t1 = int(cu[s]), int(cu[s + 1])
+        if t1 == t0:
+            assert np.array_equal(packed["h_final"][s], inp["h0"][s].double().numpy()), s
+            assert np.array_equal(packed["dh0"][s], inp["dh_final"][s].double().numpy()), s
+            continue
+        sub = {k: (v[:, t0:t1].contiguous() if k in ("q", "k", "v", "f", "b", "dO") else v) for k, v in inp.items()}
+        sub["cu_seqlens"] = None
+        sub["h0"] = inp["h0"][s:s + 1].contiguous()
+        sub["dh_final"] = inp["dh_final"][s:s + 1].contiguous()
+        one = run_gpu(sub, True)
+        for n in ("o", "dq", "dk", "dv", "df", "db"):
+            assert np.array_equal(one[n], packed[n][t0:t1]), (s, n)
+        assert np.array_equal(one["h_final"][0], packed["h_final"][s]), s
+        assert np.array_equal(one["dh0"][0], packed["dh0"][s]), s
+
+
 def test_varlen_workload_segmentation_bitwise():
     """Every document of the packed varlen workload equals its separate run."""
     w = WORKLOADS[2]
