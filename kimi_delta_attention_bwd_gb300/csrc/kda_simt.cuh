@@ -150,9 +150,9 @@ __device__ __forceinline__ void prefetch_span(const float* p, int n) {
 // product) in the core-matrix layout of kda_mma.cuh, A with rows m and B with
 // rows n (both K-major); one thread issues the slab's tcgen05 MMAs into a TMEM
 // accumulator of M = 64 rows and N fp32 columns and commits them to the
-// slab buffer's mbarrier, while every thread loads the next slab into
-// registers.  Two slab buffers; a buffer is restaged once the MMAs that read it
-// have completed.
+// slab buffer's mbarrier.  All of a product's operand loads are issued before
+// its first slab is stored.  Two slab buffers; a buffer is restaged once the
+// MMAs that read it have completed.
 struct Tc5 {
   uint32_t tmem;          // accumulator base: 64 rows, TC5_COLS columns
   uint64_t* bar;          // [2] MMA completion of each slab buffer
@@ -186,30 +186,33 @@ __device__ __forceinline__ void cta_tc(Tc5& t, bool accumulate, FA fa, FB fb) {
   constexpr int M = 64, NS = K / KS, QA = M * KS / 2, QB = N * KS / 2;  // bf16 pairs of a slab
   constexpr int PA = (QA + NTH - 1) / NTH, PB = (QB + NTH - 1) / NTH, BUF = (64 + NMAX) * KS * 2;
   static_assert(N % 8 == 0 && N <= NMAX && NMAX <= TC5_COLS && K % KS == 0 && KS % 16 == 0, "product shape");
-  float2 ra[PA], rb[PB];
   auto ia = [](int p, int& m, int& k) {
     if (AK) { m = p / (KS / 2); k = 2 * (p % (KS / 2)); } else { m = p % M; k = 2 * (p / M); }
   };
   auto ib = [](int p, int& n, int& k) {
     if (BN) { n = p % N; k = 2 * (p / N); } else { n = p / (KS / 2); k = 2 * (p % (KS / 2)); }
   };
-  auto load = [&](int k0) {
+  // every slab's operands are loaded into registers first, so that the product
+  // waits for one memory latency rather than one per slab
+  float2 ra[NS][PA], rb[NS][PB];
+#pragma unroll
+  for (int s = 0; s < NS; s++) {
 #pragma unroll
     for (int u = 0; u < PA; u++) {
       const int p = threadIdx.x + u * NTH;
       int m, k;
       ia(p, m, k);
-      if (p < QA) ra[u] = make_float2(fa(m, k0 + k), fa(m, k0 + k + 1));
+      if (p < QA) ra[s][u] = make_float2(fa(m, s * KS + k), fa(m, s * KS + k + 1));
     }
 #pragma unroll
     for (int u = 0; u < PB; u++) {
       const int p = threadIdx.x + u * NTH;
       int n, k;
       ib(p, n, k);
-      if (p < QB) rb[u] = make_float2(fb(k0 + k, n), fb(k0 + k + 1, n));
+      if (p < QB) rb[s][u] = make_float2(fb(s * KS + k, n), fb(s * KS + k + 1, n));
     }
-  };
-  load(0);
+  }
+#pragma unroll
   for (int s = 0; s < NS; s++) {
     const int bi = t.next;
     t.next ^= 1;
@@ -222,14 +225,14 @@ __device__ __forceinline__ void cta_tc(Tc5& t, bool accumulate, FA fa, FB fb) {
       const int p = threadIdx.x + u * NTH;
       int m, k;
       ia(p, m, k);
-      if (p < QA) mma::op_store2(OA, m, k, ra[u].x, ra[u].y);
+      if (p < QA) mma::op_store2(OA, m, k, ra[s][u].x, ra[s][u].y);
     }
 #pragma unroll
     for (int u = 0; u < PB; u++) {
       const int p = threadIdx.x + u * NTH;
       int n, k;
       ib(p, n, k);
-      if (p < QB) mma::op_store2(OB, n, k, rb[u].x, rb[u].y);
+      if (p < QB) mma::op_store2(OB, n, k, rb[s][u].x, rb[s][u].y);
     }
     mma::fence_async_smem();  // the staged tiles are visible to the tensor core
     tc::fence_before();
@@ -240,7 +243,6 @@ __device__ __forceinline__ void cta_tc(Tc5& t, bool accumulate, FA fa, FB fb) {
       tc::commit(&t.bar[bi]);
     }
     t.busy[bi] = true;
-    if (s + 1 < NS) load((s + 1) * KS);
   }
   tc5_wait(t, 0);
   tc5_wait(t, 1);
