@@ -439,20 +439,21 @@ __global__ void __launch_bounds__(RTH) bwd_reduce_kernel(Dims d, BwdIO io, Ws w)
     return;
   }
   const int nc = *w.n_chunks;
-  {
+  {  // per thread, then a fixed shuffle tree per warp, then the warps in order
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     int c = tid;
     for (; c + 3 * RTH < nc; c += 4 * RTH)
 #pragma unroll
       for (int u = 0; u < 4; u++) acc[u] += w.pA[(int64_t)(c + u * RTH) * H + h];
     for (; c < nc; c += RTH) acc[0] += w.pA[(int64_t)c * H + h];
-    red[tid] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    const float x = warp_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
+    if (lane == 0) red[grp] = x;
     __syncthreads();
-    for (int s2 = RTH / 2; s2 > 0; s2 >>= 1) {
-      if (tid < s2) red[tid] += red[tid + s2];
-      __syncthreads();
+    if (tid == 0) {
+      float t = 0.f;
+      for (int g = 0; g < RG; g++) t += red[g];
+      io.dA_log[h] = t;
     }
-    if (tid == 0) io.dA_log[h] = red[0];
   }
   float gsum = 0.f;
   for (int i0 = 0; i0 < dk; i0 += 32) {
