@@ -6,7 +6,9 @@ backwards in reverse.
 
 As in the fused-norm test, the one tensor the fused backward stores in the io
 dtype between the steps, dO (with the norm), enters the KDA oracle's backward
-rounded to that dtype.  q, k, v are never rounded: the kernels apply the
+rounded to that dtype; the gradients downstream of it (dx, df, db) then take
+the max-norm limit widened by the oracle's own sensitivity to that rounding
+(dO_rounding_tol).  q, k, v are never rounded: the kernels apply the
 convolution to the rows they load and keep its fp32 outputs, so the KDA
 oracle takes the convolution oracle's exact outputs.
 
@@ -23,7 +25,7 @@ from kimi_delta_attention_bwd_gb300 import kda_backward_conv, kda_forward_conv
 from kimi_delta_attention_bwd_gb300.inputs import custom, make_inputs, norm_gate_inputs, short_conv_inputs
 from oracle import norm_gate as ong
 from oracle import short_conv as osc
-from _common import TOL_IO, TOL_STATE, block_spans, rel_fro, rel_max, rel_rms, run_oracle
+from _common import TOL_IO, TOL_STATE, block_spans, dO_rounding_tol, rel_fro, rel_max, rel_rms, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -34,6 +36,8 @@ CASES = {
     "scalar_gate_norm": (custom(2, 200, 3, 32, 64, gate="scalar"), 43, None, True, None),
     "wide_spans_packed": (custom(1, 400, 2, 32, 64, h0=True, dh_final=True), 44, [1, 0, 70, 17, 64, 1, 200, 47], False,
                           "fast"),
+    # the 300M layer shape the bench times (16 x 2048, H 8), with the norm and states
+    "full_300M_16x2048_norm": (custom(16, 2048, 8, 32, 64, h0=True, dh_final=True), 45, None, True, None),
 }
 
 
@@ -92,18 +96,29 @@ def test_fused_conv_layer_matches_composed_oracles(name):
         errs["dw"] = rel_max(host(gr["dw"]), dw_ref)
         assert errs["dw"] <= TOL_IO, errs
         dO_kda = torch.from_numpy(dO_ref.reshape(w.B, w.T, H, dv)).to(torch.bfloat16)
+        dO_exact = torch.from_numpy(dO_ref.reshape(w.B, w.T, H, dv))
     else:
         errs["o"] = rel_max(host(out).reshape(N, H, dv), ref["o"], bf16=True)
         assert errs["o"] <= TOL_IO and rel_rms(host(out).reshape(N, H, dv), ref["o"]) <= 5e-3, errs
         dO_kda = dy
     inp_b = dict(inp_k, dO=dO_kda)
     refb = run_oracle(inp_b, True)
-    dqkv = np.concatenate([refb["dq"].reshape(N, -1), refb["dk"].reshape(N, -1), refb["dv"].reshape(N, -1)], axis=1)
-    dx_ref, dcw_ref = osc.backward(x64, cw64, dqkv, cu)
+
+    def conv_back(r):
+        dqkv = np.concatenate([r["dq"].reshape(N, -1), r["dk"].reshape(N, -1), r["dv"].reshape(N, -1)], axis=1)
+        return osc.backward(x64, cw64, dqkv, cu)
+    dx_ref, dcw_ref = conv_back(refb)
+    refb["dx"] = dx_ref
+    tol_grad = {"dx": TOL_IO, "df": TOL_IO, "db": TOL_IO}
+    if g is not None:  # the path's dO is its own bf16 rounding: allow the oracle's sensitivity to one rounding
+        refx = run_oracle(dict(inp_k, dO=dO_exact), True)
+        refx["dx"] = conv_back(refx)[0]
+        tol_grad = dO_rounding_tol(refb, refx, ("dx", "df", "db"))
+        errs.update({"tol:" + k: v for k, v in tol_grad.items()})
     errs["dx"] = rel_max(host(gr["dx"]).reshape(N, C), dx_ref, bf16=True)
     errs["dx:rms"] = rel_rms(host(gr["dx"]).reshape(N, C), dx_ref)
     errs["dconv_w"] = rel_max(host(gr["dconv_w"]), dcw_ref)
-    assert errs["dx"] <= TOL_IO and errs["dx:rms"] <= 5e-3 and errs["dconv_w"] <= TOL_IO, errs
+    assert errs["dx"] <= tol_grad["dx"] and errs["dx:rms"] <= 5e-3 and errs["dconv_w"] <= TOL_IO, errs
     errs["h_final"] = rel_fro(host(hf), ref["h_final"])
     errs["dh0"] = rel_fro(host(gr["dh0"]), refb["dh0"])
     assert errs["h_final"] <= TOL_STATE and errs["dh0"] <= TOL_STATE, errs
@@ -112,7 +127,7 @@ def test_fused_conv_layer_matches_composed_oracles(name):
         t = t.reshape(N, H, *t.shape[3:]) if t.ndim == 4 else t.reshape(N, H)
         errs[k2] = rel_max(t, refb[k2], bf16=True)
         errs[k2 + ":rms"] = rel_rms(t, refb[k2])
-        assert errs[k2] <= TOL_IO and errs[k2 + ":rms"] <= 5e-3, errs
+        assert errs[k2] <= tol_grad[k2] and errs[k2 + ":rms"] <= 5e-3, errs
     for k2 in ("dA_log", "ddt_bias"):
         errs[k2] = rel_max(host(gr[k2]), refb[k2])
         assert errs[k2] <= TOL_IO, errs

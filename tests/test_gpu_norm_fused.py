@@ -9,7 +9,11 @@ output, which the backward reads) and dO (an output, read back by the
 per-chunk kernels).  The forward keeps o in fp32 for the backward, so the
 norm oracle's backward takes the exact o; the KDA oracle's backward takes its
 dO rounded to the io dtype, the tensor the fused path hands to its per-chunk
-kernels.
+kernels.  The path rounds its own dO, which can sit one bf16 step from the
+oracle's rounded dO; with bf16 io the token gradients' max-norm limit adds
+twice the oracle's own sensitivity to that rounding (dO_rounding_tol), which
+matters at the full 16 x 2048 size where some large dO element always lands on
+a rounding boundary.  The rms limit stays.
 
 
 bf16 at dk=32/dv=64 runs the fused chains (a cluster of two CTAs per document
@@ -23,7 +27,7 @@ import torch
 from kimi_delta_attention_bwd_gb300 import kda_backward_norm_gate, kda_forward_norm_gate
 from kimi_delta_attention_bwd_gb300.inputs import custom, make_inputs, norm_gate_inputs
 from oracle import norm_gate as ong
-from _common import TOL_IO, compare, rel_max, rel_rms, run_oracle
+from _common import TOL_IO, compare, dO_rounding_tol, rel_max, rel_rms, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -35,6 +39,8 @@ CASES = {
     "composed_fp32_128_128_packed": (custom(1, 300, 2, 128, 128, dtype="f32", h0=True, dh_final=True), 34,
                                      [100, 1, 199]),
     "composed_fp32": (custom(1, 192, 2, 32, 64, dtype="f32", h0=True, dh_final=True), 35, None),
+    # the 300M layer shape the bench times (16 x 2048, H 8), with states
+    "full_300M_16x2048": (custom(16, 2048, 8, 32, 64, h0=True, dh_final=True), 38, None),
 }
 
 
@@ -82,13 +88,18 @@ def test_fused_norm_matches_composed_oracles(name):
     inp_b = dict(inp)
     inp_b["dO"] = torch.from_numpy(dO_ref.reshape(w.B, w.T, H, dv)).to(inp["q"].dtype)
     refb = run_oracle(inp_b, True)
+    tol_grad = None
+    if bf:  # the path's dO is its own bf16 rounding: allow the oracle's sensitivity to one rounding
+        refx = run_oracle(dict(inp, dO=torch.from_numpy(dO_ref.reshape(w.B, w.T, H, dv))), True)
+        tol_grad = dO_rounding_tol(refb, refx)
+        errs.update({"tol:" + k: v for k, v in tol_grad.items()})
     gpu = {"o": host(o).reshape(N, H, dv), "h_final": host(hf)}
     for k2 in ("dq", "dk", "dv", "df", "db"):
         t = host(gr[k2])
         gpu[k2] = t.reshape(N, H, *t.shape[3:]) if t.ndim == 4 else t.reshape(N, H)
     for k2 in ("dA_log", "ddt_bias", "dh0"):
         gpu[k2] = host(gr[k2])
-    errs.update(compare(gpu, refb, True, bf16=bf))
+    errs.update(compare(gpu, refb, True, bf16=bf, tol_grad=tol_grad))
     print(f"\n[fused norm] {name}: " + ", ".join(f"{k}={v:.2e}" for k, v in errs.items()))
 
 
