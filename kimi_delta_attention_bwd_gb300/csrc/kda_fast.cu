@@ -576,29 +576,39 @@ __device__ __forceinline__ void diag_inverse(const float* am, float* td, int I) 
     for (int r = 0; r < 16; r++) td[r * SC + cidx] = tc[r];
 }
 
-// acc (a 16 x 8 m16n8 fragment) = sum over k < 8 KS of fl(m, k) fr(k, n) in
-// split tf32 (hi*hi + hi*lo + lo*hi, about 21 bits); all operand loads are
+// (x0, x1) as bf16 pairs: hi = bf16(x), lo = bf16(x - hi).
+__device__ __forceinline__ void split_bf2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// acc (a 16 x 8 m16n8 fragment) = sum over k < 16 KS of fl(m, k) fr(k, n) in
+// split bf16 (hi*hi + hi*lo + lo*hi, about 16 bits, the precision of the
+// split tiles the products' results are stored in); all operand loads are
 // issued before the products.
 template <int KS, class FL, class FR>
-__device__ __forceinline__ void tile_tf32(float (&acc)[4], FL fl, FR fr) {
+__device__ __forceinline__ void tile_bf16s(float (&acc)[4], FL fl, FR fr) {
   const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
   uint32_t ah[KS][4], al[KS][4], bh[KS][2], bl[KS][2];
 #pragma unroll
   for (int ks = 0; ks < KS; ks++) {
-    const int kk = 8 * ks + tq;
-    split_tf32(fl(gq, kk), ah[ks][0], al[ks][0]);
-    split_tf32(fl(gq + 8, kk), ah[ks][1], al[ks][1]);
-    split_tf32(fl(gq, kk + 4), ah[ks][2], al[ks][2]);
-    split_tf32(fl(gq + 8, kk + 4), ah[ks][3], al[ks][3]);
-    split_tf32(fr(kk, gq), bh[ks][0], bl[ks][0]);
-    split_tf32(fr(kk + 4, gq), bh[ks][1], bl[ks][1]);
+    const int k0 = 16 * ks + 2 * tq;
+    split_bf2(fl(gq, k0), fl(gq, k0 + 1), ah[ks][0], al[ks][0]);
+    split_bf2(fl(gq + 8, k0), fl(gq + 8, k0 + 1), ah[ks][1], al[ks][1]);
+    split_bf2(fl(gq, k0 + 8), fl(gq, k0 + 9), ah[ks][2], al[ks][2]);
+    split_bf2(fl(gq + 8, k0 + 8), fl(gq + 8, k0 + 9), ah[ks][3], al[ks][3]);
+    split_bf2(fr(k0, gq), fr(k0 + 1, gq), bh[ks][0], bl[ks][0]);
+    split_bf2(fr(k0 + 8, gq), fr(k0 + 9, gq), bh[ks][1], bl[ks][1]);
   }
   acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
 #pragma unroll
   for (int ks = 0; ks < KS; ks++) {
-    mma_tf32(acc, ah[ks][0], ah[ks][1], ah[ks][2], ah[ks][3], bh[ks][0], bh[ks][1]);
-    mma_tf32(acc, ah[ks][0], ah[ks][1], ah[ks][2], ah[ks][3], bl[ks][0], bl[ks][1]);
-    mma_tf32(acc, al[ks][0], al[ks][1], al[ks][2], al[ks][3], bh[ks][0], bh[ks][1]);
+    mma_bf16(acc, ah[ks], bh[ks][0], bh[ks][1]);
+    mma_bf16(acc, ah[ks], bl[ks][0], bl[ks][1]);
+    mma_bf16(acc, al[ks], bh[ks][0], bh[ks][1]);
   }
 }
 template <class F>
@@ -621,7 +631,7 @@ __device__ void solve_merge(const float* am, float* tm, float* yy) {
     const float* Al = am + (16 + 32 * p) * SC + 32 * p;
     const float* Tr = am + tdoff(2 * p) + n0;
     float acc[4];
-    tile_tf32<2>(acc, [&](int m, int k) { return Al[m * SC + k]; }, [&](int k, int n) { return Tr[k * SC + n]; });
+    tile_bf16s<1>(acc, [&](int m, int k) { return Al[m * SC + k]; }, [&](int k, int n) { return Tr[k * SC + n]; });
     tile_store(acc, [&](int m, int n, float v) { yy[(16 * p + m) * YS + n0 + n] = v; });
   } else {  // the diagonal inverses into T
     for (int idx = tid - 128; idx < 4 * 256; idx += 128) {
@@ -634,7 +644,7 @@ __device__ void solve_merge(const float* am, float* tm, float* yy) {
     const int p = warp >> 1, n0 = 8 * (warp & 1);
     const float* Tl = am + tdoff(2 * p + 1);
     float acc[4];
-    tile_tf32<2>(acc, [&](int m, int k) { return Tl[m * SC + k]; },
+    tile_bf16s<1>(acc, [&](int m, int k) { return Tl[m * SC + k]; },
                  [&](int k, int n) { return yy[(16 * p + k) * YS + n0 + n]; });
     float* out = tm + (16 + 32 * p) * SC + 32 * p + n0;
     tile_store(acc, [&](int m, int n, float v) { out[m * SC + n] = -v; });
@@ -645,9 +655,9 @@ __device__ void solve_merge(const float* am, float* tm, float* yy) {
     const float* Al = am + (32 + 16 * rb) * SC;
     float acc[4];
     if (n0 < 16)
-      tile_tf32<4>(acc, [&](int m, int k) { return Al[m * SC + k]; }, [&](int k, int n) { return tm[k * SC + n0 + n]; });
+      tile_bf16s<2>(acc, [&](int m, int k) { return Al[m * SC + k]; }, [&](int k, int n) { return tm[k * SC + n0 + n]; });
     else
-      tile_tf32<2>(acc, [&](int m, int k) { return Al[m * SC + 16 + k]; },
+      tile_bf16s<1>(acc, [&](int m, int k) { return Al[m * SC + 16 + k]; },
                    [&](int k, int n) { return tm[(16 + k) * SC + n0 + n]; });
     tile_store(acc, [&](int m, int n, float v) { yy[(16 * rb + m) * YS + n0 + n] = v; });
   }
@@ -656,9 +666,9 @@ __device__ void solve_merge(const float* am, float* tm, float* yy) {
     const float* Tl = tm + (32 + 16 * rb) * SC + 32;
     float acc[4];
     if (rb == 0)
-      tile_tf32<2>(acc, [&](int m, int k) { return Tl[m * SC + k]; }, [&](int k, int n) { return yy[k * YS + n0 + n]; });
+      tile_bf16s<1>(acc, [&](int m, int k) { return Tl[m * SC + k]; }, [&](int k, int n) { return yy[k * YS + n0 + n]; });
     else
-      tile_tf32<4>(acc, [&](int m, int k) { return Tl[m * SC + k]; }, [&](int k, int n) { return yy[k * YS + n0 + n]; });
+      tile_bf16s<2>(acc, [&](int m, int k) { return Tl[m * SC + k]; }, [&](int k, int n) { return yy[k * YS + n0 + n]; });
     float* out = tm + (32 + 16 * rb) * SC + n0;
     tile_store(acc, [&](int m, int n, float v) { out[m * SC + n] = -v; });
   }
