@@ -17,8 +17,60 @@ namespace kda {
 // (torchtitan PR "[kimi k3] Support sample packing in KDA", Verification).
 // Equal-length rows use the same table with offsets b * T.
 constexpr int ORD_BUCKETS = 2048;  // document chunk counts the dispatch order sorts
+// Inclusive scan of x over the block (a multiple of 32 threads, at most
+// 1024), with the block's sum in *total; every thread calls it.
+__device__ int block_incl_scan(int x, int* s_wsum, int* total) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = (int)(blockDim.x >> 5);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_wsum[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int y = lane < nw ? s_wsum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int z = __shfl_up_sync(0xffffffffu, y, o);
+      if (lane >= o) y += z;
+    }
+    s_wsum[lane] = y;
+  }
+  __syncthreads();
+  const int incl = x + (warp > 0 ? s_wsum[warp - 1] : 0);
+  *total = s_wsum[nw - 1];
+  __syncthreads();  // s_wsum is free again
+  return incl;
+}
+
+// order[0 .. n) <- 0 .. n - 1 by decreasing key(i) >= 0, keys at or past
+// ORD_BUCKETS sharing the top bucket; equal keys in any order (a chain's result
+// does not depend on when it runs).  A counting sort in shared memory: every
+// thread of the 1024-thread block calls it.
+template <class K>
+__device__ void order_desc(int n, K key, int32_t* order, int* s_cnt, int* s_wsum) {
+  const int tid = threadIdx.x;
+  for (int b = tid; b < ORD_BUCKETS; b += blockDim.x) s_cnt[b] = 0;
+  __syncthreads();
+  for (int i = tid; i < n; i += blockDim.x) atomicAdd(&s_cnt[min(key(i), ORD_BUCKETS - 1)], 1);
+  __syncthreads();
+  {  // s_cnt[b] <- items of larger keys: thread t owns buckets 2 (N - 1 - t) + {1, 0}
+    static_assert(ORD_BUCKETS == 2048, "two buckets per thread of a 1024-thread block");
+    const int b0 = ORD_BUCKETS - 2 * (tid + 1);
+    const int c1 = s_cnt[b0 + 1], c0 = s_cnt[b0];
+    int total;
+    const int ex = block_incl_scan(c1 + c0, s_wsum, &total) - (c1 + c0);
+    s_cnt[b0 + 1] = ex;
+    s_cnt[b0] = ex + c1;
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += blockDim.x) order[atomicAdd(&s_cnt[min(key(i), ORD_BUCKETS - 1)], 1)] = i;
+}
+
 __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* cu, Dims d, Ws w) {
   __shared__ int s_bad;
+  __shared__ int s_cnt[ORD_BUCKETS];
   __shared__ int s_carry;
   __shared__ int s_wsum[32];
   pdl_release();  // fwd_chunk may launch; it waits for this table before reading it
@@ -34,30 +86,11 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* cu, Di
   __syncthreads();
   if (!s_bad) {
     for (int base = 0; base < n; base += blockDim.x) {
-      int i = base + tid;
-      int nc = i < n ? (off(i + 1) - off(i) + C - 1) / C : 0;
-      int x = nc;  // inclusive scan over the block
-      const int lane = tid & 31, warp = tid >> 5;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-      }
-      if (lane == 31) s_wsum[warp] = x;
-      __syncthreads();
-      if (warp == 0) {
-        int y = lane < (int)(blockDim.x >> 5) ? s_wsum[lane] : 0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          int z = __shfl_up_sync(0xffffffffu, y, o);
-          if (lane >= o) y += z;
-        }
-        s_wsum[lane] = y;
-      }
-      __syncthreads();
-      int incl = x + (warp > 0 ? s_wsum[warp - 1] : 0);
+      const int i = base + tid;
+      const int nc = i < n ? (off(i + 1) - off(i) + C - 1) / C : 0;
+      int total;
+      const int incl = block_incl_scan(nc, s_wsum, &total);
       if (i < n) w.doc_chunk0[i] = s_carry + incl - nc;
-      int total = s_wsum[(blockDim.x >> 5) - 1];
       __syncthreads();
       if (tid == 0) s_carry += total;
       __syncthreads();
@@ -85,57 +118,47 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* cu, Di
     }
   }
   for (int j = s_carry + tid; j < d.nc_max; j += blockDim.x) w.chunk_len[j] = 0;
+  if (d.seg) {  // the segment table of the tensor-core forward chains (seg_split, seg_count)
+    __shared__ int s_nmax, s_ucarry;
+    if (tid == 0) { s_nmax = 0; s_ucarry = 0; }
+    __syncthreads();  // doc_chunk0 (written above by other threads) is visible
+    int mx = 0;
+    for (int i = tid; i < n; i += blockDim.x) mx = max(mx, w.doc_chunk0[i + 1] - w.doc_chunk0[i]);
+    atomicMax(&s_nmax, mx);
+    __syncthreads();
+    const bool split = seg_split(s_nmax, s_carry, d.H, d.slots);
+    const int len = seg_len(s_nmax);
+    for (int base = 0; base < n; base += blockDim.x) {
+      const int i = base + tid;
+      const int nc = i < n ? w.doc_chunk0[i + 1] - w.doc_chunk0[i] : 0;
+      const int ns = i < n ? seg_count(nc, split, len) : 0;
+      int total;
+      const int u0 = s_ucarry + block_incl_scan(ns, s_wsum, &total) - ns;
+      for (int sg = 0; sg < ns; sg++) {
+        const int c0 = sg * len;
+        if (u0 + sg < d.nu) w.useg[u0 + sg] = make_int4(i, c0, ns > 1 ? min(len, nc - c0) : nc, sg);
+      }
+      __syncthreads();
+      if (tid == 0) s_ucarry += total;
+      __syncthreads();
+    }
+    if (tid == 0) {  // d.nu bounds the count (the host's own count or seg_units_max); past it, refuse
+      *w.n_units = min(s_ucarry, d.nu);
+      if (s_ucarry > d.nu) *w.err = KDA_ERR_INVALID_ARG;
+    }
+    __syncthreads();  // the table (written by every thread) and the count are visible
+    // the chain grids take the heaviest units first: a later segment folds one composite per
+    // earlier segment before its chunks
+    order_desc(min(s_ucarry, d.nu), [&](int u) { const int4 un = w.useg[u]; return un.z + un.w; }, w.uorder,
+               s_cnt, s_wsum);
+  }
   // The documents by decreasing chunk count: the general scans run one CTA per
   // (document, head, column slice) in this order, longest first, so that a grid
   // of more chains than resident CTAs ends about when its longest chain does
-  // instead of when a long chain dispatched last does.  A counting sort over the
-  // counts in shared memory; documents of equal count in any order (a chain's
-  // result does not depend on when it runs).  Counts past the buckets keep the
-  // index order.
-  if (d.fast) return;  // (the tensor-core chains keep the grid order)
-  __shared__ int s_cnt[ORD_BUCKETS];
-  __shared__ int s_max;
-  if (tid == 0) s_max = 0;
+  // instead of when a long chain dispatched last does.
+  if (d.fast) return;  // (the tensor-core chains order their units above, when split)
   __syncthreads();  // doc_chunk0 (written above by other threads) is visible
-  int mx = 0;
-  for (int i = tid; i < n; i += blockDim.x) mx = max(mx, w.doc_chunk0[i + 1] - w.doc_chunk0[i]);
-  atomicMax(&s_max, mx);
-  for (int b = tid; b < ORD_BUCKETS; b += blockDim.x) s_cnt[b] = 0;
-  __syncthreads();
-  if (s_max >= ORD_BUCKETS) {
-    for (int i = tid; i < n; i += blockDim.x) w.doc_order[i] = i;
-    return;
-  }
-  for (int i = tid; i < n; i += blockDim.x) atomicAdd(&s_cnt[w.doc_chunk0[i + 1] - w.doc_chunk0[i]], 1);
-  __syncthreads();
-  {  // s_cnt[b] <- documents with more than b chunks: thread t owns buckets 2 (N - 1 - t) + {1, 0}
-    static_assert(ORD_BUCKETS == 2048, "two buckets per thread of a 1024-thread block");
-    const int lane = tid & 31, warp = tid >> 5, b0 = ORD_BUCKETS - 2 * (tid + 1);
-    const int c1 = s_cnt[b0 + 1], c0 = s_cnt[b0];
-    int x = c1 + c0;  // inclusive scan over the threads
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) s_wsum[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-      int y = s_wsum[lane];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int z = __shfl_up_sync(0xffffffffu, y, o);
-        if (lane >= o) y += z;
-      }
-      s_wsum[lane] = y;
-    }
-    __syncthreads();
-    const int ex = x - (c1 + c0) + (warp > 0 ? s_wsum[warp - 1] : 0);
-    s_cnt[b0 + 1] = ex;
-    s_cnt[b0] = ex + c1;
-  }
-  __syncthreads();
-  for (int i = tid; i < n; i += blockDim.x) w.doc_order[atomicAdd(&s_cnt[w.doc_chunk0[i + 1] - w.doc_chunk0[i]], 1)] = i;
+  order_desc(n, [&](int i) { return w.doc_chunk0[i + 1] - w.doc_chunk0[i]; }, w.doc_order, s_cnt, s_wsum);
 }
 
 cudaError_t launch_chunk_table(const int32_t* cu, const Dims& d, const Ws& w, cudaStream_t st) {
@@ -181,7 +204,12 @@ struct Layout {
   size_t off_W, off_U, off_P, off_QG, off_KD, off_gam, off_Sent, off_CH;
   size_t off_sT, off_sP, off_sW, off_sU, off_sA, off_gDP, off_gMA, off_gQG, off_gKD, off_gKG, off_gdg;
   size_t off_dE, off_dSn, off_pA, off_pdt, off_scr, off_nO, off_pdw, off_nrm, off_cg, off_cpart;
+  size_t off_useg, off_uord, off_nu, off_segc;
 };
+
+// Upper bound on the segment units of a split forward chain: a document of n
+// chunks has at most n / SEG + 1 segments (segments have at least SEG chunks).
+static int64_t seg_units_max(const Dims& d) { return (int64_t)d.n_docs + (d.nc_max + SEG - 1) / SEG; }
 
 // Workspace layout.  Both paths start with the error word, the saved-problem
 // tag and the chunk table.  The tensor-core path (d.fast) keeps per chunk and
@@ -202,7 +230,14 @@ static Layout layout(const Dims& d, int for_bwd, bool fused = false) {
   L.off_cd = take(4 * (size_t)d.nc_max);
   L.off_ord = take(4 * (size_t)d.n_docs);
   if (d.fast) {
-    if (!fused) L.off_CH = take(4 * nch * (d.dk * d.dk + C * d.dk + d.dk * d.dv + C * d.dv));  // M, QW, KU, PU
+    if (!fused) {
+      L.off_CH = take(4 * nch * (d.dk * d.dk + C * d.dk + d.dk * d.dv + C * d.dv));  // M, QW, KU, PU
+      const size_t nu = (size_t)seg_units_max(d);
+      L.off_useg = take(16 * nu);  // the segment table of split forward chains
+      L.off_uord = take(4 * nu);
+      L.off_nu = take(4);
+      L.off_segc = take(4 * nu * d.H * d.dk * (d.dk + d.dv));  // and the segments' composites
+    }
     if (for_bwd) {
       L.off_Sent = take(4 * nch * d.dk * d.dv);  // entry states for the backward (split-bf16 tiles)
       L.off_dSn = take(4 * nch * d.dk * d.dv);
@@ -267,6 +302,10 @@ static Ws bind(void* ws, const Layout& L, const Dims& d, int for_bwd) {
   w.chunk_len = (int32_t*)(p + L.off_cl);
   w.chunk_doc = (int32_t*)(p + L.off_cd);
   w.doc_order = (int32_t*)(p + L.off_ord);
+  w.useg = L.off_useg ? (int4*)(p + L.off_useg) : nullptr;
+  w.uorder = L.off_uord ? (int32_t*)(p + L.off_uord) : nullptr;
+  w.n_units = L.off_nu ? (int32_t*)(p + L.off_nu) : nullptr;
+  w.segc = at(L.off_segc);
   w.W = at(L.off_W);
   w.U = at(L.off_U);
   w.P = at(L.off_P);
@@ -305,10 +344,48 @@ static Ws bind(void* ws, const Layout& L, const Dims& d, int for_bwd) {
 // Failure-detection test hook (kda_test_stage_timeout); 0 in normal use.
 static int g_test_tx_extra = 0;
 
+// The tensor-core forward chain's grid (without the fused norm, whose chains
+// stay whole): whether long chains may be split into segments (Dims::seg) and
+// how many units the grid covers (Dims::nu).  With the lengths known on the
+// host (equal rows, or a host copy of cu_seqlens) the rule of seg_split is
+// applied here and the grid is exact; with device-only offsets the chunk
+// table applies it and the grid covers the most units any offsets can give.
+static void plan_chain_split(const kda_problem* p, Dims& d) {
+  d.seg = 0;
+  d.nu = d.n_docs;
+  if (!d.fast || d.norm) return;
+  d.slots = fast_chain_slots();
+  if (d.slots <= 0) return;
+  const long long grid_max = 2147483647LL / (2LL * d.H);  // the split grids are one-dimensional
+  if (p->cu_seqlens && !p->cu_seqlens_host) {
+    if (seg_units_max(d) > grid_max) return;
+    d.seg = 1;
+    d.nu = (int)seg_units_max(d);
+    return;
+  }
+  const int32_t* c = p->cu_seqlens_host;
+  auto chunks = [&](int i) { return c ? (c[i + 1] - c[i] + C - 1) / C : (d.T + C - 1) / C; };
+  int n_max = 0;
+  long long total = 0;
+  for (int i = 0; i < d.n_docs; i++) {
+    const int n = chunks(i);
+    n_max = n > n_max ? n : n_max;
+    total += n;
+  }
+  if (!seg_split(n_max, total, d.H, d.slots)) return;
+  const int len = seg_len(n_max);
+  long long units = 0;
+  for (int i = 0; i < d.n_docs; i++) units += seg_count(chunks(i), true, len);
+  if (units > grid_max) return;
+  d.seg = 1;
+  d.nu = (int)units;
+}
+
 // The forward launch sequence shared by kda_fwd and kda_fwd_noalloc.
 static cudaError_t run_forward(const kda_problem* p, Dims d, const FwdIO& io, const Ws& w, cudaStream_t stream,
                                bool fused = false) {
   d.tx_extra = g_test_tx_extra;
+  if (!fused) plan_chain_split(p, d);
   cudaError_t e = launch_chunk_table(p->cu_seqlens, d, w, stream);
   if (e != cudaSuccess) return e;
   if (d.fast) return launch_fast_fwd(d, io, w, stream, fused);
@@ -372,6 +449,9 @@ static kda_status check_problem(const kda_problem* p, Dims* d) {
   d->norm = 0;
   d->conv = 0;
   d->tx_extra = 0;
+  d->seg = 0;
+  d->nu = n_docs;
+  d->slots = 0;
   return KDA_OK;
 }
 
@@ -653,7 +733,7 @@ static const char* const k_names[K_COUNT] = {"chunk_table", "fwd_intra", "fwd_sc
                                              "fwd_state", "bwd_grad",  "bwd_gate",   "decode",
                                              "norm_gate_fwd", "norm_gate_bwd", "norm_gate_reduce",
                                              "conv_fwd",  "conv_bwd",  "conv_reduce",
-                                             "fwd_state_norm", "bwd_scan_norm"};
+                                             "fwd_state_norm", "bwd_scan_norm", "fwd_seg"};
 
 const char* kda_prof_kernel_name(int i) { return (i >= 0 && i < K_COUNT) ? k_names[i] : nullptr; }
 

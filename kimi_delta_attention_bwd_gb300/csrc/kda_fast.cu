@@ -1269,6 +1269,24 @@ __device__ __forceinline__ void slice_to_global(bf16* g, const bf16* s, int col0
   }
 }
 
+// The forward chain grids with split chains (Dims::seg): one dimension, CTA
+// i = (rank, head, column half) with the half fastest (the two halves of a
+// chunk read the same M and QW), ranks in the segment table's dispatch order
+// (heaviest units first).  Without seg: (document, head, half) as blockIdx.
+struct ChainCta {
+  int unit, h, half;
+};
+__device__ __forceinline__ ChainCta chain_cta(const Dims& d, const Ws& w) {
+  ChainCta c{(int)blockIdx.x, (int)blockIdx.y, (int)blockIdx.z};
+  if (d.seg) {
+    const int i = (int)blockIdx.x, rank = i / (2 * d.H);
+    c.half = i & 1;
+    c.h = (i >> 1) % d.H;
+    c.unit = rank < *w.n_units ? w.uorder[rank] : -1;
+  }
+  return c;
+}
+
 template <bool NORM>
 struct FChainStage {  // one copy of this half's part of the chain block: KU, PU, M, QW (half 0)
   __align__(128) unsigned char raw[CB_STAGE];  // or M, QW, KU, PU (half 1)
@@ -1338,17 +1356,34 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
   extern __shared__ __align__(128) unsigned char smraw[];
   FChainSm<NORM>& sm = *reinterpret_cast<FChainSm<NORM>*>(smraw);
   constexpr int NS = NORM ? NSTG : FSTG;
-  const int doc = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * NSC, tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
-  pdl_wait();  // fwd_chunk's products
+  pdl_wait();  // fwd_chunk's products (and with d.seg, fwd_seg's composites)
   const int err0 = *w.err;
   if (!NORM && err0 != 0) return;
   const int H = d.H;
-  const int cb = w.doc_chunk0[doc], n = err0 != 0 ? 0 : w.doc_chunk0[doc + 1] - cb;
+  const ChainCta cc = chain_cta(d, w);  // (NORM runs without d.seg)
+  const int h = cc.h, zc = cc.half, col0 = zc * NSC;
+  // this CTA's run of chunks: a whole document, or with d.seg one unit of the segment table
+  // (segment sg of its document, chunks c0 ..; `last`: the run ends the document)
+  int doc = cc.unit, cb, n, sg = 0;
+  bool last = true;
+  if (!NORM && d.seg) {
+    if (cc.unit < 0) return;
+    const int4 un = w.useg[cc.unit];
+    doc = un.x;
+    sg = un.w;
+    cb = w.doc_chunk0[doc] + un.y;
+    n = un.z;
+    last = un.y + n == w.doc_chunk0[doc + 1] - w.doc_chunk0[doc];
+  } else {
+    cb = w.doc_chunk0[doc];
+    n = err0 != 0 ? 0 : w.doc_chunk0[doc + 1] - cb;
+  }
   const DocSpan sp = doc_span(w, cb, n);
   const int64_t dh = ((int64_t)doc * H + h) * DK * DV;
   const Op S0{sm.S[0], sm.S[0] + DK * NSC, NSC}, S1{sm.S[1], sm.S[1] + DK * NSC, NSC};
-  for (int idx = tid; idx < DK * NSC / 2; idx += 2 * CTH) {
+  for (int idx = tid; sg == 0 && idx < DK * NSC / 2; idx += 2 * CTH) {  // (a later segment's is folded below)
     const int i = idx / (NSC / 2), jc = 2 * (idx % (NSC / 2));
     float2 v = make_float2(0.f, 0.f);
     if (io.h0) v = *reinterpret_cast<const float2*>(io.h0 + dh + i * DV + col0 + jc);
@@ -1407,19 +1442,62 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
   };
   // the stage of `step`: one copy (with the gate tile: two), issued by carry thread 0 once its part of
   // the step before is done (the output warps' part is the longer one)
-  const int oKU = blockIdx.z ? CB_KU1 - CB_M : 0, oPU = oKU + (CB_PU0 - CB_KU0);
-  const int oM = blockIdx.z ? 0 : CB_M - CB_KU0, oQW = oM + (CB_QW - CB_M);
+  const int oKU = zc ? CB_KU1 - CB_M : 0, oPU = oKU + (CB_PU0 - CB_KU0);
+  const int oM = zc ? 0 : CB_M - CB_KU0, oQW = oM + (CB_QW - CB_M);
   auto prefetch = [&](int step) {
     if (step < n && tid == 0) {
       const int slot = step % NS;
       const int64_t ch = (int64_t)(cb + step) * H + h;
       mbar_expect_tx(&sm.bar[slot], (uint32_t)(CB_STAGE + (NORM ? 2 * C * NSC : 0) + d.tx_extra));
-      bulk_g2s(sm.st[slot].raw, chblk(w, ch) + (blockIdx.z ? CB_M : CB_KU0), CB_STAGE, &sm.bar[slot]);
+      bulk_g2s(sm.st[slot].raw, chblk(w, ch) + (zc ? CB_M : CB_KU0), CB_STAGE, &sm.bar[slot]);
       if (NORM)  // the gate rows of the chunk (rows past its end are not used)
         tma_load_2d(sm.st[slot].g, &nmap.g, h * DV + col0, sp.t0(step), &sm.bar[slot]);
     }
   };
   for (int s = 0; s < NS - 1; s++) prefetch(s);
+  if (!NORM && sg > 0) {
+    // entry state of segment sg: S <- Phi_t S + B_t over the composites of the document's earlier
+    // segments (the units cc.unit - sg ..), from the initial state, in fp32.  Scratch: the ring's
+    // last slot, whose first copy is issued in step 0 (after this).  Thread: row i, columns c4 ..
+    float* fs = reinterpret_cast<float*>(sm.st[NS - 1].raw);  // S [DK][NSC]
+    float* fp = fs + DK * NSC;                                 // Phi_t [DK][DK]
+    float* fb = fp + DK * DK;                                  // B_t, this half's columns [DK][NSC]
+    const int i = tid >> 3, c4 = 4 * (tid & 7);
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(fs + i * NSC + c4) =
+        io.h0 ? *reinterpret_cast<const float4*>(io.h0 + dh + i * DV + col0 + c4) : z4;
+    const int64_t cstride = (int64_t)H * DK * (DK + DV);
+    const float* comp = w.segc + ((int64_t)(cc.unit - sg) * H + h) * DK * (DK + DV);
+    float4 pv = *reinterpret_cast<const float4*>(comp + 4 * tid);
+    float4 bv = *reinterpret_cast<const float4*>(comp + DK * DK + i * DV + col0 + c4);
+    for (int t = 0; t < sg; t++) {
+      *reinterpret_cast<float4*>(fp + 4 * tid) = pv;
+      *reinterpret_cast<float4*>(fb + i * NSC + c4) = bv;
+      __syncthreads();  // S, Phi_t and B_t are visible
+      if (t + 1 < sg) {  // the next composite's loads in flight during this product
+        comp += cstride;
+        pv = *reinterpret_cast<const float4*>(comp + 4 * tid);
+        bv = *reinterpret_cast<const float4*>(comp + DK * DK + i * DV + col0 + c4);
+      }
+      float4 a = *reinterpret_cast<const float4*>(fb + i * NSC + c4);
+#pragma unroll 8
+      for (int k = 0; k < DK; k++) {
+        const float pk = fp[i * DK + k];
+        const float4 s4 = *reinterpret_cast<const float4*>(fs + k * NSC + c4);
+        a.x = fmaf(pk, s4.x, a.x);
+        a.y = fmaf(pk, s4.y, a.y);
+        a.z = fmaf(pk, s4.z, a.z);
+        a.w = fmaf(pk, s4.w, a.w);
+      }
+      __syncthreads();  // every read of S, Phi_t and B_t is done
+      *reinterpret_cast<float4*>(fs + i * NSC + c4) = a;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < DK * NSC / 2; idx += 2 * CTH) {
+      const int r = idx / (NSC / 2), jc = 2 * (idx % (NSC / 2));
+      op_store2(S0, r, jc, fs[r * NSC + jc], fs[r * NSC + jc + 1]);
+    }
+  }
   const bool carry = warp < 4;
   const int wq = warp & 3, mI = wq & 1, jn = wq >> 1;
   float snew[2][4];  // (carry warps) tile of the updated state: rows 16 mI .., columns 16 jn ..
@@ -1541,7 +1619,7 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
     if (tid == 0) atomicExch(w.err, -7);
     bad = true;
   }
-  if (io.h_final && !bad && err0 == 0) {
+  if (io.h_final && !bad && err0 == 0 && last) {
     if (n > 0) {
       if (carry)
 #pragma unroll
@@ -1560,6 +1638,108 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
     }
   }
   if constexpr (NORM) cluster_sync();  // the peer no longer touches this CTA's shared memory
+}
+
+// fwd_seg: the composites of split forward chains (Dims::seg).  One CTA of
+// four warps per (unit, head, 32 value columns) whose unit is a segment before
+// its document's last: X = [Phi | B] (32 x 64; Phi the product of the
+// segment's M_c, B the state it reaches from zero) by X <- M_c X + [0 | KU_c]
+// from [I | 0], with fwd_state's split-bf16 products and double-buffered split
+// tile, and a four-stage ring of M and this half's KU (bulk copies, bounded
+// waits).  Phi is the same for both halves; half 0 stores it.
+constexpr int SSTG = 4;
+struct SegStage {
+  bf16 M[2 * DK * DK];  // M (split)
+  float ku[DK * NSC];   // KU of this half, in fragment order
+};
+struct SegSm {
+  SegStage st[SSTG];
+  bf16 X[2][2 * DK * 2 * NSC];  // [Phi | B] (split), double-buffered
+  uint64_t bar[SSTG];
+};
+static_assert(sizeof(SegStage) % 16 == 0 && offsetof(SegStage, ku) % 16 == 0 && offsetof(SegSm, X) % 16 == 0,
+              "bulk copy targets and operand tiles need 16-byte alignment");
+
+__global__ void __launch_bounds__(CTH) fwd_seg_kernel(Dims d, FwdIO io, Ws w) {
+  (void)io;
+  extern __shared__ __align__(128) unsigned char smraw[];
+  SegSm& sm = *reinterpret_cast<SegSm*>(smraw);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+  pdl_wait();     // fwd_chunk's chain operands
+  pdl_release();  // fwd_state may launch: it waits for this grid before reading the composites
+  if (*w.err != 0) return;
+  const ChainCta cc = chain_cta(d, w);
+  const int u = cc.unit, h = cc.h, half = cc.half;
+  if (u < 0) return;
+  const int4 un = w.useg[u];  // (document, first chunk in it, chunks, segment)
+  const int c0d = w.doc_chunk0[un.x], n = un.z;
+  if (un.y + n == w.doc_chunk0[un.x + 1] - c0d) return;  // the document's last segment is not composed
+  const int H = d.H, cb = c0d + un.y;
+  constexpr int XK = 2 * NSC;  // columns of X
+  const Op X0{sm.X[0], sm.X[0] + DK * XK, XK}, X1{sm.X[1], sm.X[1] + DK * XK, XK};
+  for (int idx = tid; idx < DK * XK / 2; idx += CTH) {  // [I | 0]
+    const int i = idx / (XK / 2), jc = 2 * (idx % (XK / 2));
+    op_store2(X0, i, jc, i == jc ? 1.f : 0.f, i == jc + 1 ? 1.f : 0.f);
+  }
+  if (tid == 0) {
+    for (int s2 = 0; s2 < SSTG; s2++) mbar_init(&sm.bar[s2], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();  // the barriers are initialised before any thread waits on them
+  auto prefetch = [&](int step) {
+    if (step < n && tid == 0) {
+      const int slot = step % SSTG;
+      const int64_t ch = (int64_t)(cb + step) * H + h;
+      mbar_expect_tx(&sm.bar[slot], (uint32_t)(4 * DK * DK + 4 * DK * NSC + d.tx_extra));
+      bulk_g2s(sm.st[slot].M, chblk(w, ch) + CB_M, 4 * DK * DK, &sm.bar[slot]);
+      bulk_g2s(sm.st[slot].ku, chblk(w, ch) + (half ? CB_KU1 : CB_KU0), 4 * DK * NSC, &sm.bar[slot]);
+    }
+  };
+  for (int s = 0; s < SSTG - 1; s++) prefetch(s);
+  const int mI = warp & 1, jn = warp >> 1;  // this warp's tile of X: rows 16 mI .., columns 32 jn ..
+  float xn[4][4];
+  zero(xn);
+  for (int step = 0; step < n; step++) {
+    const SegStage& st = sm.st[step % SSTG];
+    if (__syncthreads_or(!mbar_wait(&sm.bar[step % SSTG], (step / SSTG) & 1))) {  // a wait ran out
+      for (int k2 = step; k2 < n && k2 < step + SSTG - 1; k2++) mbar_wait(&sm.bar[k2 % SSTG], (k2 / SSTG) & 1);
+      if (tid == 0) atomicExch(w.err, -7);
+      return;
+    }  // this step's stage and X are visible; the other X buffer and the slot of step - 1 are free
+    prefetch(step + SSTG - 1);
+    const Op Mo{const_cast<bf16*>(st.M), const_cast<bf16*>(st.M) + DK * DK, DK};
+    const Op& Xc = (step & 1) ? X1 : X0;
+    const Op& Xn = (step & 1) ? X0 : X1;
+    zero(xn);
+    gemm3<2, false, true>(xn, Mo, 16 * mI, 0, Xc, 32 * jn, 0, DK / 16);
+    if (jn == 1) {  // + KU: fragment jt of this lane's row block in KU's fragment order
+      const float4* kup = reinterpret_cast<const float4*>(st.ku) + 4 * mI * 32 + lane;
+#pragma unroll
+      for (int jt = 0; jt < 4; jt++) {
+        const float4 k4 = kup[32 * jt];
+        xn[jt][0] += k4.x;
+        xn[jt][1] += k4.y;
+        xn[jt][2] += k4.z;
+        xn[jt][3] += k4.w;
+      }
+    }
+#pragma unroll
+    for (int jt = 0; jt < 4; jt++)
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++)
+        op_store2(Xn, 16 * mI + gq + 8 * hh, 32 * jn + 8 * jt + 2 * tq, xn[jt][2 * hh], xn[jt][2 * hh + 1]);
+  }
+  float* out = w.segc + ((int64_t)u * H + h) * DK * (DK + DV);  // Phi [DK][DK], then B [DK][DV]
+  if (jn == 0 && half != 0) return;
+#pragma unroll
+  for (int jt = 0; jt < 4; jt++)
+#pragma unroll
+    for (int hh = 0; hh < 2; hh++) {
+      const int r = 16 * mI + gq + 8 * hh, c = 8 * jt + 2 * tq;
+      float* dst = jn == 0 ? out + r * DK + c : out + DK * DK + r * DV + half * NSC + c;
+      *reinterpret_cast<float2*>(dst) = make_float2(xn[jt][2 * hh], xn[jt][2 * hh + 1]);
+    }
 }
 
 struct BChainStage {
@@ -2954,6 +3134,8 @@ static int wave_ctas() {
   return cached[dev];
 }
 
+int fast_chain_slots() { return wave_ctas(); }  // fwd_state: two CTAs per SM, like the per-chunk kernels
+
 cudaError_t launch_fast_fwd(const Dims& d0, const FwdIO& io, const Ws& w, cudaStream_t st, bool fused) {
   Dims d = d0;
   d.ahead = wave_ctas() / 2;  // fwd_chunk's L2 prefetch: the CTA half a wave later
@@ -2975,6 +3157,9 @@ cudaError_t launch_fast_fwd(const Dims& d0, const FwdIO& io, const Ws& w, cudaSt
     e = cudaFuncSetAttribute(fast::fwd_state_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(fast::fwd_state_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2n);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fast::fwd_seg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(fast::SegSm));
   if (e != cudaSuccess) return e;
   prof_begin(K_FWD_CHUNK, st);
   if (d.conv)
@@ -2984,7 +3169,10 @@ cudaError_t launch_fast_fwd(const Dims& d0, const FwdIO& io, const Ws& w, cudaSt
   prof_end(K_FWD_CHUNK, st);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const dim3 grid(d.n_docs, d.H, fast::DV / fast::NSC);
+  // one CTA per (document, head, column half); with split chains one per (segment unit, head,
+  // half) on a 1-D grid (chain_cta)
+  static_assert(fast::DV / fast::NSC == 2, "two column halves");
+  const dim3 grid = d.seg ? dim3((unsigned)d.nu * d.H * 2) : dim3(d.n_docs, d.H, 2);
   NMaps nm = {};
   if (d.norm) {  // the two column halves of a (document, head) as one cluster
     if (!encode_nmaps(&nm, io.ng, nullptr, nullptr, d.Ntok, d.H, fast::DV)) return cudaErrorInvalidValue;
@@ -2992,6 +3180,13 @@ cudaError_t launch_fast_fwd(const Dims& d0, const FwdIO& io, const Ws& w, cudaSt
     e = launch_cluster(fast::fwd_state_kernel<true>, grid, dim3(2 * fast::CTH), s2n, st, 2, true, d, io, w, nm);
     prof_end(K_FWD_STATE_NORM, st);
   } else {
+    if (d.seg) {  // the segments' composites first
+      prof_begin(K_FWD_SEG, st);
+      e = launch_pdl(fast::fwd_seg_kernel, grid, dim3(fast::CTH), sizeof(fast::SegSm), st, d, io, w);
+      prof_end(K_FWD_SEG, st);
+      if (e == cudaSuccess) e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
     prof_begin(K_FWD_STATE, st);
     e = launch_pdl(fast::fwd_state_kernel<false>, grid, dim3(2 * fast::CTH), s2, st, d, io, w, nm);
     prof_end(K_FWD_STATE, st);

@@ -34,8 +34,38 @@ enum KernelId {
   K_CONV_RED,
   K_FWD_STATE_NORM,
   K_BWD_SCAN_NORM,
+  K_FWD_SEG,
   K_COUNT
 };
+
+// Splitting long forward chains (tensor-core path).  The forward state chain
+// is affine, S_{c+1} = M_c S_c + KU_c, so a run of chunks composes into one map
+// S -> Phi S + B.  When a workload's longest document has more than SPLIT_MIN
+// chunks and more than twice the average chain length per resident chain CTA
+// (a chain-bound workload: a few long chains finish long after the rest),
+// every document of more than SPLIT_MIN chunks is cut into segments of
+// seg_len(n_max) chunks.  One kernel composes each segment but a document's
+// last; the chain kernel starts every later segment from its predecessors'
+// composites folded onto the document's initial state (one small product per
+// earlier segment, so segments grow with the longest document: about
+// sqrt(n_max) chunks, at least SEG).  The same rule runs on the host (to size
+// the launch) and in the chunk-table kernel (to build the segment table).
+constexpr int SEG = 16, SPLIT_MIN = 32;
+__host__ __device__ inline bool seg_split(int n_max, long long total_chunks, int H, int slots) {
+  if (n_max <= SPLIT_MIN || slots <= 0) return false;
+  const long long avg = (total_chunks * H * 2 + slots - 1) / slots;  // chain steps per resident chain CTA
+  return n_max > 2 * avg;
+}
+// Chunks per segment: the least multiple of SEG whose square covers n_max.
+__host__ __device__ inline int seg_len(int n_max) {
+  int s = SEG;
+  while ((long long)s * s < n_max) s += SEG;
+  return s;
+}
+// Segments of a document of n chunks.
+__host__ __device__ inline int seg_count(int n, bool split, int len) {
+  return split && n > SPLIT_MIN ? (n + len - 1) / len : 1;
+}
 
 // Device-side view of the caller's workspace.  Offsets are fixed by
 // layout_workspace() from the problem sizes; the error word sits at byte 0.
@@ -48,6 +78,14 @@ struct Ws {
   int32_t* chunk_len;   // [nc_max] tokens in the chunk (1..C), 0 = unused
   int32_t* chunk_doc;   // [nc_max]
   int32_t* doc_order;   // [n_docs] documents by decreasing chunk count (the general scans' dispatch order)
+  // tensor-core forward chains split into segments (Dims::seg): per unit (document, first chunk
+  // within it, chunks, segment index), a document's segments consecutive; the unit count; and
+  // per unit and head the composite [Phi | B] ([dk][dk] then [dk][dv], fp32) of every
+  // segment but a document's last
+  int4* useg;
+  int32_t* uorder;  // units by decreasing work (chunks plus folded segments): the chain grids' dispatch order
+  int32_t* n_units;
+  float* segc;
   // forward intermediates, per chunk-head ch = chunk * H + h
   float* W;    // [ch][C][dk]  T diag(beta) (K^ * Gamma)
   float* U;    // [ch][C][dv]  T diag(beta) V
@@ -98,6 +136,9 @@ struct Dims {
   int32_t conv;  // the short convolution is fused into the per-chunk kernels' prologue (tensor-core path)
   int32_t tx_extra;  // failure-detection test hook (kda_test_stage_timeout): bytes the forward chain's stage
                      // barriers expect beyond what their copies deliver; 0 outside that test
+  int32_t seg;    // (tensor-core forward) the chunk table decides whether to split long chains (seg_split)
+  int32_t nu;     // units of the forward chain grid: documents, or with seg an upper bound on the segments
+  int32_t slots;  // resident forward chain CTAs on the device (the split rule's denominator)
 };
 
 // Backward kernels refuse a workspace that no saving forward of the same
@@ -219,6 +260,8 @@ bool fast_path(int dtype, int dk, int dv);
 // fused: the single-kernel forward that needs only the chunk table (used by
 // kda_fwd_noalloc); else the per-chunk kernel and the state chain.
 cudaError_t launch_fast_fwd(const Dims& d, const FwdIO& io, const Ws& w, cudaStream_t st, bool fused);
+// Resident forward-chain CTAs of the tensor-core path on the current device (two per SM).
+int fast_chain_slots();
 cudaError_t launch_fast_bwd(const Dims& d, const BwdIO& io, const Ws& w, cudaStream_t st);
 
 // The fused convolution's backward: dx and dw from x and the fp32 gradients of
