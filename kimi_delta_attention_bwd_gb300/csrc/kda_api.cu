@@ -350,7 +350,14 @@ static int g_test_tx_extra = 0;
 // host (equal rows, or a host copy of cu_seqlens) the rule of seg_split is
 // applied here and the grid is exact; with device-only offsets the chunk
 // table applies it and the grid covers the most units any offsets can give.
+static void plan_chain_split_(const kda_problem* p, Dims& d);
 static void plan_chain_split(const kda_problem* p, Dims& d) {
+  plan_chain_split_(p, d);
+  // the backward reads the forward's segment table: a plan that differs (another device's SM
+  // count) makes a different saved-problem tag, so that the backward refuses the workspace
+  if (d.seg) d.tag ^= (int32_t)(((uint32_t)d.nu * 2654435761u) << 4 | 8u);
+}
+static void plan_chain_split_(const kda_problem* p, Dims& d) {
   d.seg = 0;
   d.nu = d.n_docs;
   if (!d.fast || d.norm) return;
@@ -621,6 +628,7 @@ kda_status bwd_impl(const kda_problem* p, const void* q, const void* k, const vo
     if (s != KDA_OK) return s;
   }
   if (d.fast) {
+    plan_chain_split(p, d);  // the forward's plan (its segment table is in the workspace)
     cudaError_t e = launch_fast_bwd(d, io, w, stream);
     if (e == cudaSuccess && cv) {  // dx, dw of the convolution from its outputs' gradients
       const int Cc = d.H * (2 * d.dk + d.dv);
@@ -733,7 +741,7 @@ static const char* const k_names[K_COUNT] = {"chunk_table", "fwd_intra", "fwd_sc
                                              "fwd_state", "bwd_grad",  "bwd_gate",   "decode",
                                              "norm_gate_fwd", "norm_gate_bwd", "norm_gate_reduce",
                                              "conv_fwd",  "conv_bwd",  "conv_reduce",
-                                             "fwd_state_norm", "bwd_scan_norm", "fwd_seg"};
+                                             "fwd_state_norm", "bwd_scan_norm", "fwd_seg", "bwd_seg"};
 
 const char* kda_prof_kernel_name(int i) { return (i >= 0 && i < K_COUNT) ? k_names[i] : nullptr; }
 

@@ -1287,6 +1287,51 @@ __device__ __forceinline__ ChainCta chain_cta(const Dims& d, const Ws& w) {
   return c;
 }
 
+// S <- Phi_t S + B_t for t = 0 .. count - 1 in fp32, composite t at comp + t
+// cstride (Phi [DK][DK], then B [DK][DV] of which columns col0 .. are this
+// CTA's).  fs: S [DK][NSC], holding the initial state and then the result;
+// fp, fb: scratch of DK x DK and DK x NSC floats (shared memory).  NT threads,
+// each owning E consecutive entries of a row of S; composite t + 1's loads
+// are in flight during product t.  Ends with a barrier.
+template <int NT>
+__device__ void fold_composites(float* fs, float* fp, float* fb, const float* comp, int64_t cstride, int count,
+                                int col0) {
+  constexpr int E = DK * NSC / NT, Q = E / 4;
+  static_assert(E % 4 == 0 && NSC % E == 0, "whole float4s of one row per thread");
+  const int tid = threadIdx.x, i = tid / (NSC / E), c = E * (tid % (NSC / E));
+  float4 pv[Q], bv[Q];
+  auto load = [&](const float* cp) {
+#pragma unroll
+    for (int q = 0; q < Q; q++) {
+      pv[q] = reinterpret_cast<const float4*>(cp + E * tid)[q];
+      bv[q] = reinterpret_cast<const float4*>(cp + DK * DK + i * DV + col0 + c)[q];
+    }
+  };
+  load(comp);
+  for (int t = 0; t < count; t++) {
+#pragma unroll
+    for (int q = 0; q < Q; q++) {
+      reinterpret_cast<float4*>(fp + E * tid)[q] = pv[q];
+      reinterpret_cast<float4*>(fb + i * NSC + c)[q] = bv[q];
+    }
+    __syncthreads();  // S, Phi_t and B_t are visible
+    if (t + 1 < count) load(comp + (t + 1) * cstride);
+    float a[E];
+#pragma unroll
+    for (int e = 0; e < E; e++) a[e] = fb[i * NSC + c + e];
+#pragma unroll 4
+    for (int k = 0; k < DK; k++) {
+      const float pk = fp[i * DK + k];
+#pragma unroll
+      for (int e = 0; e < E; e++) a[e] = fmaf(pk, fs[k * NSC + c + e], a[e]);
+    }
+    __syncthreads();  // every read of S, Phi_t and B_t is done
+#pragma unroll
+    for (int e = 0; e < E; e++) fs[i * NSC + c + e] = a[e];
+  }
+  __syncthreads();
+}
+
 template <bool NORM>
 struct FChainStage {  // one copy of this half's part of the chain block: KU, PU, M, QW (half 0)
   __align__(128) unsigned char raw[CB_STAGE];  // or M, QW, KU, PU (half 1)
@@ -1456,43 +1501,18 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
   };
   for (int s = 0; s < NS - 1; s++) prefetch(s);
   if (!NORM && sg > 0) {
-    // entry state of segment sg: S <- Phi_t S + B_t over the composites of the document's earlier
-    // segments (the units cc.unit - sg ..), from the initial state, in fp32.  Scratch: the ring's
-    // last slot, whose first copy is issued in step 0 (after this).  Thread: row i, columns c4 ..
-    float* fs = reinterpret_cast<float*>(sm.st[NS - 1].raw);  // S [DK][NSC]
-    float* fp = fs + DK * NSC;                                 // Phi_t [DK][DK]
-    float* fb = fp + DK * DK;                                  // B_t, this half's columns [DK][NSC]
-    const int i = tid >> 3, c4 = 4 * (tid & 7);
-    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    *reinterpret_cast<float4*>(fs + i * NSC + c4) =
-        io.h0 ? *reinterpret_cast<const float4*>(io.h0 + dh + i * DV + col0 + c4) : z4;
-    const int64_t cstride = (int64_t)H * DK * (DK + DV);
-    const float* comp = w.segc + ((int64_t)(cc.unit - sg) * H + h) * DK * (DK + DV);
-    float4 pv = *reinterpret_cast<const float4*>(comp + 4 * tid);
-    float4 bv = *reinterpret_cast<const float4*>(comp + DK * DK + i * DV + col0 + c4);
-    for (int t = 0; t < sg; t++) {
-      *reinterpret_cast<float4*>(fp + 4 * tid) = pv;
-      *reinterpret_cast<float4*>(fb + i * NSC + c4) = bv;
-      __syncthreads();  // S, Phi_t and B_t are visible
-      if (t + 1 < sg) {  // the next composite's loads in flight during this product
-        comp += cstride;
-        pv = *reinterpret_cast<const float4*>(comp + 4 * tid);
-        bv = *reinterpret_cast<const float4*>(comp + DK * DK + i * DV + col0 + c4);
-      }
-      float4 a = *reinterpret_cast<const float4*>(fb + i * NSC + c4);
-#pragma unroll 8
-      for (int k = 0; k < DK; k++) {
-        const float pk = fp[i * DK + k];
-        const float4 s4 = *reinterpret_cast<const float4*>(fs + k * NSC + c4);
-        a.x = fmaf(pk, s4.x, a.x);
-        a.y = fmaf(pk, s4.y, a.y);
-        a.z = fmaf(pk, s4.z, a.z);
-        a.w = fmaf(pk, s4.w, a.w);
-      }
-      __syncthreads();  // every read of S, Phi_t and B_t is done
-      *reinterpret_cast<float4*>(fs + i * NSC + c4) = a;
+    // entry state of segment sg: the composites of the document's earlier segments (the units
+    // cc.unit - sg ..) folded onto the initial state.  Scratch: the ring's last slot, whose first
+    // copy is issued in step 0 (after this).
+    float* fs = reinterpret_cast<float*>(sm.st[NS - 1].raw);
+    float* fp = fs + DK * NSC;
+    float* fb = fp + DK * DK;
+    for (int idx = tid; idx < DK * NSC; idx += 2 * CTH) {
+      const int r = idx / NSC, c = idx % NSC;
+      fs[idx] = io.h0 ? io.h0[dh + r * DV + col0 + c] : 0.f;
     }
-    __syncthreads();
+    fold_composites<2 * CTH>(fs, fp, fb, w.segc + ((int64_t)(cc.unit - sg) * H + h) * DK * (DK + DV),
+                             (int64_t)H * DK * (DK + DV), sg, col0);
     for (int idx = tid; idx < DK * NSC / 2; idx += 2 * CTH) {
       const int r = idx / (NSC / 2), jc = 2 * (idx % (NSC / 2));
       op_store2(S0, r, jc, fs[r * NSC + jc], fs[r * NSC + jc + 1]);
@@ -1761,16 +1781,35 @@ static_assert(sizeof(BChainStage) % 16 == 0 && offsetof(BChainStage, QW) == 4 * 
 __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
   extern __shared__ __align__(128) unsigned char smraw[];
   BChainSm& sm = *reinterpret_cast<BChainSm*>(smraw);
-  const int doc = blockIdx.x, h = blockIdx.y, col0 = blockIdx.z * NSC, tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
   pdl_release();  // bwd_grad may launch: it waits for this grid before reading dS
   if (!saved_ok(d, w.tag, w.err)) return;
   const int H = d.H;
-  const int cb = w.doc_chunk0[doc], ce = w.doc_chunk0[doc + 1], n = ce - cb;
+  const ChainCta cc = chain_cta(d, w);
+  if (cc.unit < 0) return;
+  const int h = cc.h, col0 = cc.half * NSC;
+  // this CTA's run of chunks, taken from the last: a whole document, or with d.seg one unit of the
+  // segment table (segment sg; `later` segments of the document follow it, all of n chunks but
+  // the document's last)
+  int doc = cc.unit, cb, n, sg = 0, later = 0;
+  if (d.seg) {
+    const int4 un = w.useg[cc.unit];
+    doc = un.x;
+    sg = un.w;
+    n = un.z;
+    cb = w.doc_chunk0[doc] + un.y;
+    const int rest = w.doc_chunk0[doc + 1] - cb - n;
+    later = rest > 0 ? (rest + n - 1) / n : 0;
+  } else {
+    cb = w.doc_chunk0[doc];
+    n = w.doc_chunk0[doc + 1] - cb;
+  }
+  const int ce = cb + n;
   const DocSpan sp = doc_span(w, cb, n);
   const int64_t dh = ((int64_t)doc * H + h) * DK * DV;
   const Op dS{sm.dS, sm.dS + DK * NSC, NSC};
-  for (int idx = tid; idx < DK * NSC / 2; idx += CTH) {
+  for (int idx = tid; later == 0 && idx < DK * NSC / 2; idx += CTH) {  // (an earlier segment's is folded below)
     const int i = idx / (NSC / 2), jc = 2 * (idx % (NSC / 2));
     float2 v = make_float2(0.f, 0.f);
     if (io.dh_final) v = *reinterpret_cast<const float2*>(io.dh_final + dh + i * DV + col0 + jc);
@@ -1802,6 +1841,24 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
     cp_commit();
   };
   for (int s = 0; s < BSTG - 1; s++) prefetch(s);
+  if (later > 0) {
+    // the gradient leaving segment sg: the composites of the document's later segments (the units
+    // cc.unit + later down to cc.unit + 1) folded onto dS_final.  Scratch: the ring's last slot,
+    // whose first copies are issued in step 0 (after this).
+    float* fs = reinterpret_cast<float*>(&sm.st[BSTG - 1]);
+    float* fp = fs + DK * NSC;
+    float* fb = fp + DK * DK;
+    for (int idx = tid; idx < DK * NSC; idx += CTH) {
+      const int r = idx / NSC, c = idx % NSC;
+      fs[idx] = io.dh_final ? io.dh_final[dh + r * DV + col0 + c] : 0.f;
+    }
+    fold_composites<CTH>(fs, fp, fb, w.segc + ((int64_t)(cc.unit + later) * H + h) * DK * (DK + DV),
+                         -(int64_t)H * DK * (DK + DV), later, col0);
+    for (int idx = tid; idx < DK * NSC / 2; idx += CTH) {
+      const int r = idx / (NSC / 2), jc = 2 * (idx % (NSC / 2));
+      op_store2(dS, r, jc, fs[r * NSC + jc], fs[r * NSC + jc + 1]);
+    }
+  }
   float acc[2][4];  // this warp's tile of the carried gradient: rows 16 (warp & 1) .., columns 16 (warp >> 1) ..
   zero(acc);
   const int mI = warp & 1, jn = warp >> 1;
@@ -1837,7 +1894,7 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
         op_store2(dS, 16 * mI + gq + 8 * hh, 16 * jn + 8 * jj + 2 * tq, acc[jj][2 * hh], acc[jj][2 * hh + 1]);
   }
   cp_wait_all();
-  if (io.dh0) {
+  if (io.dh0 && sg == 0) {  // the document's first chunks end its reverse chain
     if (n > 0) {
 #pragma unroll
       for (int jj = 0; jj < 2; jj++)
@@ -1853,6 +1910,106 @@ __global__ void __launch_bounds__(CTH) bwd_scan_kernel(Dims d, BwdIO io, Ws w) {
       }
     }
   }
+}
+
+// bwd_seg: the composites of split backward chains (Dims::seg; the forward's
+// segment table).  One CTA of four warps per (unit, head, 32 value columns)
+// whose unit is a segment after its document's first: Y = [Psi | D] (32 x 64;
+// Psi the product of the segment's M_c^T, D the gradient its reverse chain
+// reaches from zero) by Y <- M_c^T Y + [0 | QW_c^T dO_c] over its chunks from
+// the last, from [I | 0], with bwd_scan's products and four-stage ring (M | QW
+// by bulk copy, dO rows by cp.async).  Psi is the same for both halves; half 0
+// stores it (over the forward's composites, consumed by then).
+struct BSegSm {
+  BChainStage st[BSTG];
+  bf16 Y[2][2 * DK * 2 * NSC];  // [Psi | D] (split), double-buffered
+  uint64_t bar[BSTG];
+};
+static_assert(offsetof(BSegSm, Y) % 16 == 0, "operand tiles need 16-byte alignment");
+
+__global__ void __launch_bounds__(CTH) bwd_seg_kernel(Dims d, BwdIO io, Ws w) {
+  extern __shared__ __align__(128) unsigned char smraw[];
+  BSegSm& sm = *reinterpret_cast<BSegSm*>(smraw);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+  if (!saved_ok(d, w.tag, w.err)) return;
+  const ChainCta cc = chain_cta(d, w);
+  const int u = cc.unit, h = cc.h, half = cc.half, col0 = half * NSC;
+  if (u < 0) return;
+  const int4 un = w.useg[u];  // (document, first chunk in it, chunks, segment)
+  if (un.w == 0) return;      // a document's first segment is not composed
+  const int H = d.H, n = un.z, cb = w.doc_chunk0[un.x] + un.y, ce = cb + n;
+  const DocSpan sp = doc_span(w, cb, n);
+  constexpr int YK = 2 * NSC;  // columns of Y
+  const Op Y0{sm.Y[0], sm.Y[0] + DK * YK, YK}, Y1{sm.Y[1], sm.Y[1] + DK * YK, YK};
+  for (int idx = tid; idx < DK * YK / 2; idx += CTH) {  // [I | 0]
+    const int i = idx / (YK / 2), jc = 2 * (idx % (YK / 2));
+    op_store2(Y0, i, jc, i == jc ? 1.f : 0.f, i == jc + 1 ? 1.f : 0.f);
+  }
+  const bf16* dOg = (const bf16*)io.dO;
+  if (tid == 0) {
+    for (int s2 = 0; s2 < BSTG; s2++) mbar_init(&sm.bar[s2], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();  // the barriers are initialised before any thread waits on them
+  auto prefetch = [&](int step) {  // always commits a cp.async group (empty past the end)
+    if (step < n) {
+      const int slot = step % BSTG;
+      BChainStage& s = sm.st[slot];
+      const int ci = ce - 1 - step, L = sp.L(n - 1 - step), t0 = sp.t0(n - 1 - step);
+      const int64_t ch = (int64_t)ci * H + h;
+      if (tid == 0) {  // M | QW, adjacent in the chain block and in the stage
+        mbar_expect_tx(&sm.bar[slot], CB_KU1 - CB_M);
+        bulk_g2s(s.M, chblk(w, ch) + CB_M, CB_KU1 - CB_M, &sm.bar[slot]);
+      }
+      for (int idx = tid; idx < C * NSC / 8; idx += CTH) {
+        const int r = idx / (NSC / 8), p = idx % (NSC / 8);
+        bf16* dst = s.dO + opix(r, 8 * p, NSC);
+        if (r < L) cp16(dst, dOg + ((size_t)(t0 + r) * H + h) * DV + col0 + 8 * p);
+        else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    cp_commit();
+  };
+  for (int s = 0; s < BSTG - 1; s++) prefetch(s);
+  const int mI = warp & 1, jn = warp >> 1;  // this warp's tile of Y: rows 16 mI .., columns 32 jn ..
+  float yn[4][4];
+  zero(yn);
+  for (int step = 0; step < n; step++) {
+    const BChainStage& s = sm.st[step % BSTG];
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(BSTG - 2));
+    if (__syncthreads_or(!mbar_wait(&sm.bar[step % BSTG], (step / BSTG) & 1))) {  // a stage did not arrive in bound
+      for (int k2 = step; k2 < n && k2 < step + BSTG - 1; k2++) mbar_wait(&sm.bar[k2 % BSTG], (k2 / BSTG) & 1);
+      cp_wait_all();
+      if (tid == 0) atomicExch(w.err, -7);
+      return;
+    }  // this step's stage and Y are visible; the other Y buffer and the slot of step - 1 are free
+    prefetch(step + BSTG - 1);
+    const Op Mo{const_cast<bf16*>(s.M), const_cast<bf16*>(s.M) + DK * DK, DK};
+    const Op QWo{const_cast<bf16*>(s.QW), const_cast<bf16*>(s.QW) + C * DK, DK};
+    const Op dOo{const_cast<bf16*>(s.dO), nullptr, NSC};
+    const Op& Yc = (step & 1) ? Y1 : Y0;
+    const Op& Yn = (step & 1) ? Y0 : Y1;
+    zero(yn);
+    gemm3<2, true, true>(yn, Mo, 16 * mI, 0, Yc, 32 * jn, 0, DK / 16);        // M^T Y
+    if (jn == 1) gemm3<2, true, true>(yn, QWo, 16 * mI, 0, dOo, 0, 0, C / 16);  // + QW^T dO
+#pragma unroll
+    for (int jt = 0; jt < 4; jt++)
+#pragma unroll
+      for (int hh = 0; hh < 2; hh++)
+        op_store2(Yn, 16 * mI + gq + 8 * hh, 32 * jn + 8 * jt + 2 * tq, yn[jt][2 * hh], yn[jt][2 * hh + 1]);
+  }
+  cp_wait_all();
+  float* out = w.segc + ((int64_t)u * H + h) * DK * (DK + DV);  // Psi [DK][DK], then D [DK][DV]
+  if (jn == 0 && half != 0) return;
+#pragma unroll
+  for (int jt = 0; jt < 4; jt++)
+#pragma unroll
+    for (int hh = 0; hh < 2; hh++) {
+      const int r = 16 * mI + gq + 8 * hh, c = 8 * jt + 2 * tq;
+      float* dst = jn == 0 ? out + r * DK + c : out + DK * DK + r * DV + col0 + c;
+      *reinterpret_cast<float2*>(dst) = make_float2(yn[jt][2 * hh], yn[jt][2 * hh + 1]);
+    }
 }
 
 // bwd_scan_norm: the reverse chain with the gated RMSNorm's backward fused in
@@ -3212,8 +3369,11 @@ cudaError_t launch_fast_bwd(const Dims& d0, const BwdIO& io, const Ws& w, cudaSt
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(fast::bwd_gate_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sizeof(fast::GateSm<true>));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fast::bwd_seg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(fast::BSegSm));
   if (e != cudaSuccess) return e;
-  const dim3 grid(d.n_docs, d.H, fast::DV / fast::NSC);
+  const dim3 grid = d.seg && !d.norm ? dim3((unsigned)d.nu * d.H * 2) : dim3(d.n_docs, d.H, 2);  // (chain_cta)
   if (d.norm) {  // the two column halves of a (document, head) as one cluster
     NMaps nm;
     if (!encode_nmaps(&nm, io.ng, io.dy, w.nO, d.Ntok, d.H, fast::DV)) return cudaErrorInvalidValue;
@@ -3221,6 +3381,13 @@ cudaError_t launch_fast_bwd(const Dims& d0, const BwdIO& io, const Ws& w, cudaSt
     e = launch_cluster(fast::bwd_scan_norm_kernel, grid, dim3(2 * fast::CTH), scn, st, 2, false, d, io, w, nm);
     prof_end(K_BWD_SCAN_NORM, st);
   } else {
+    if (d.seg) {  // the later segments' composites first
+      prof_begin(K_BWD_SEG, st);
+      fast::bwd_seg_kernel<<<grid, fast::CTH, sizeof(fast::BSegSm), st>>>(d, io, w);
+      prof_end(K_BWD_SEG, st);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
     prof_begin(K_BWD_SCAN, st);
     fast::bwd_scan_kernel<<<grid, fast::CTH, sc, st>>>(d, io, w);
     prof_end(K_BWD_SCAN, st);

@@ -35,6 +35,7 @@ enum KernelId {
   K_FWD_STATE_NORM,
   K_BWD_SCAN_NORM,
   K_FWD_SEG,
+  K_BWD_SEG,
   K_COUNT
 };
 
@@ -136,7 +137,7 @@ struct Dims {
   int32_t conv;  // the short convolution is fused into the per-chunk kernels' prologue (tensor-core path)
   int32_t tx_extra;  // failure-detection test hook (kda_test_stage_timeout): bytes the forward chain's stage
                      // barriers expect beyond what their copies deliver; 0 outside that test
-  int32_t seg;    // (tensor-core forward) the chunk table decides whether to split long chains (seg_split)
+  int32_t seg;    // (tensor-core chains) the chunk table decides whether to split long chains (seg_split)
   int32_t nu;     // units of the forward chain grid: documents, or with seg an upper bound on the segments
   int32_t slots;  // resident forward chain CTAs on the device (the split rule's denominator)
 };

@@ -1,15 +1,17 @@
-"""Split forward chains of the tensor-core path against the oracle.
+"""Split state chains of the tensor-core path against the oracle.
 
 The forward state chain S_{c+1} = M_c S_c + KU_c is affine, so a run of chunks
-composes into one map S -> Phi S + B.  When a workload's longest document has
-more than 32 chunks and more than twice the average chain length per resident
-chain CTA (a chain-bound workload, such as one long document packed with
-short ones), every document over 32 chunks runs as segments of 16 chunks:
-one kernel composes each segment but a document's last, and the chain kernel
-starts every later segment from its predecessors' composites folded onto the
-initial state.  The torchtitan PR "[kimi k3] Support sample packing in KDA"
-(description: the recurrent state resets at document boundaries) fixes what a
-packed document must equal: the same document run alone.
+composes into one map S -> Phi S + B; so is the backward's reverse chain
+dS_c = M_c^T dS_{c+1} + QW_c^T dO_c (dS -> Psi dS + D).  When a workload's
+longest document has more than 32 chunks and more than twice the average
+chain length per resident chain CTA (a chain-bound workload, such as one long
+document packed with short ones), every document over 32 chunks runs as
+segments of 16 chunks: one kernel per direction composes each segment but the
+one its chain starts in, and the chain kernels start every other segment from
+the composites before it (after it, in the backward) folded onto h0
+(dS_final).  The torchtitan PR "[kimi k3] Support sample packing in KDA"
+(description: the recurrent state resets at document boundaries) fixes what
+a packed document must equal: the same document run alone.
 
 Cases force the split at H = 2 (a few chains on the whole GPU): a long
 document packed with one-token, empty and short ones; long equal rows;
@@ -78,7 +80,7 @@ def test_split_chain_matches_oracle(name):
     w, seed, lens = CASES[name]
     inp = make_inputs(w, seed=seed, lengths=lens)
     n = _launches(lambda: _run(inp))
-    assert n.get("fwd_seg", 0) == 1, n  # the case is split
+    assert n.get("fwd_seg", 0) == 1 and n.get("bwd_seg", 0) == 1, n  # the case is split
     gpu = _run(inp)
     ref = run_oracle(inp, True)
     errs = compare(gpu, ref, True)
@@ -116,5 +118,5 @@ def test_split_boundary(chunks, split):
     w = custom(1, 64 * chunks, 2, 32, 64, h0=True)
     inp = make_inputs(w, seed=65, with_grad_inputs=True)
     n = _launches(lambda: _run(inp))
-    assert (n.get("fwd_seg", 0) == 1) == split, n
-    assert n.get("fwd_state", 0) == 1, n
+    assert (n.get("fwd_seg", 0) == 1) == split and (n.get("bwd_seg", 0) == 1) == split, n
+    assert n.get("fwd_state", 0) == 1 and n.get("bwd_scan", 0) == 1, n
