@@ -20,6 +20,7 @@ of the method here) on the host cores, one full workload per step.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -314,12 +315,13 @@ def make_step(w, inp, dev):
     return step, d, grads
 
 
-def workload_bench(wi, args, dev, flush, world, stream, hbm, rank):
+def workload_bench(wi, args, dev, flush, world, stream, hbm, rank, w=None):
     """One workload's step (forward, or forward + backward) timed as launched,
     then a second pass with per-kernel event brackets for the split and the
-    dominant kernel's roofline."""
+    dominant kernel's roofline.  w: a variant of workload wi (its inputs drawn
+    with wi's seed)."""
     from kimi_delta_attention_bwd_gb300 import _lib
-    w = WORKLOADS[wi]
+    w = WORKLOADS[wi] if w is None else w
     inp = make_inputs(w, seed=BASE_SEED + wi + 1000 * rank)
     n_docs = w.B if inp.get("cu_seqlens") is None else int(inp["cu_seqlens"].numel()) - 1
     step, _, _ = make_step(w, inp, dev)
@@ -653,6 +655,10 @@ def run_ours(args, rank, world, local):
     # forward-only at the same shape, the packed varlen forward and the large-head training step
     fwd = workload_bench(FWD_WORKLOAD, args, dev, flush, world, stream, hbm, rank)
     varlen = workload_bench(VARLEN_WORKLOAD, args, dev, flush, world, stream, hbm, rank)
+    # the same packed row as a training step (with dO): both chains split on its long document
+    vw = dataclasses.replace(WORKLOADS[VARLEN_WORKLOAD], backward=True,
+                             name="varlen fwd+bwd, 1x32768 packed, H8, 32/64, bf16")
+    varlen_step = workload_bench(VARLEN_WORKLOAD, args, dev, flush, world, stream, hbm, rank, w=vw)
     large = workload_bench(LARGE_WORKLOAD, args, dev, flush, world, stream, hbm, rank)
     dec = decode_bench(args, dev, flush, world, stream, hbm, rank)
     torch.cuda.empty_cache()
@@ -728,6 +734,7 @@ def run_ours(args, rank, world, local):
             "fwd_value": fwd["value"], "fwd_roofline_frac": fwd["roofline"]["frac"],
             "fwd": fwd,
             "varlen_fwd": varlen,
+            "varlen_step": varlen_step,
             "large_head_step": large,
             "decode": dec,
             "norm_gate": ngate,
@@ -763,9 +770,11 @@ def ncu_pass(rows: int = 16):
     forward+backward again, then one decode step, the gated norm forward and
     backward, the short convolution forward and backward, one forward+backward
     with the gated norm fused into the chains (kda_fwd_norm_gate /
-    kda_bwd_norm_gate) and one of the fused layer (kda_fwd_conv / kda_bwd_conv
-    with the norm), in that order.  rows < 16 runs the step workloads on that
-    many 2048-token rows (a smaller case for multi-pass captures)."""
+    kda_bwd_norm_gate), one of the fused layer (kda_fwd_conv / kda_bwd_conv
+    with the norm) and one forward+backward of the packed varlen row (1 x 32768
+    tokens, whose long document splits both chains: fwd_seg, bwd_seg), in that
+    order.  rows < 16 runs the 300M step workloads on that many 2048-token rows
+    (a smaller case for multi-pass captures); the varlen row stays whole."""
     from kimi_delta_attention_bwd_gb300 import (kda_backward, kda_backward_conv, kda_backward_norm_gate,
                                                 kda_decode_step, kda_forward, kda_forward_conv,
                                                 kda_forward_norm_gate, kda_norm_gate, kda_norm_gate_backward,
@@ -798,6 +807,13 @@ def ncu_pass(rows: int = 16):
     _, _, cctx = kda_forward_conv(sc["x"].reshape(w.B, w.T, -1), sc["w"], d["f"], d["b"], d["A_log"], d["dt_bias"],
                                   w.dk, w.dv, g=ng["g"].reshape(shape), w=ng["w"], scale=d["scale"])
     kda_backward_conv(cctx, ng["dy"].reshape(shape))
+    vw = dataclasses.replace(WORKLOADS[VARLEN_WORKLOAD], backward=True)
+    vi = make_inputs(vw, seed=BASE_SEED + VARLEN_WORKLOAD)
+    dv_ = {k: (t.to(dev) if isinstance(t, torch.Tensor) else t) for k, t in vi.items()}
+    _, _, vctx = kda_forward(dv_["q"], dv_["k"], dv_["v"], dv_["f"], dv_["b"], dv_["A_log"], dv_["dt_bias"],
+                             scale=dv_["scale"], cu_seqlens=dv_["cu_seqlens"],
+                             cu_seqlens_host=vi["cu_seqlens"].numpy())
+    kda_backward(vctx, dv_["dO"])
     torch.cuda.synchronize()
     print("ncu pass done")
     return 0
