@@ -15,7 +15,8 @@ oracle takes the convolution oracle's exact outputs.
 Cases: rows, packed documents with one-token and empty ones (the window and
 the state reset at each document), the scalar gate, gates whose 16-token
 spans pass the 80-nat guard (the exact fallback recomputes q and k through
-the convolution), and the norm.
+the convolution), the norm, and a long packed document on which both state
+chains run split into composed segments.
 """
 import numpy as np
 import pytest
@@ -38,6 +39,10 @@ CASES = {
                           "fast"),
     # the 300M layer shape the bench times (16 x 2048, H 8), with the norm and states
     "full_300M_16x2048_norm": (custom(16, 2048, 8, 32, 64, h0=True, dh_final=True), 45, None, True, None),
+    # a 41-chunk document packed with a short one, few heads: without the norm both state chains
+    # run split into composed segments (the fused-norm chains never split)
+    "long_doc_split_chains": (custom(1, 64 * 40 + 17 + 13, 2, 32, 64, h0=True, dh_final=True), 46,
+                              [64 * 40 + 17, 13], False, None),
 }
 
 
@@ -72,6 +77,16 @@ def test_fused_conv_layer_matches_composed_oracles(name):
                                     cu_seqlens_host=cu_host)
     gr = kda_backward_conv(ctx, dy.to(dev), d.get("dh_final"))
     torch.cuda.synchronize()
+    if name == "long_doc_split_chains":  # the case does split both chains
+        from kimi_delta_attention_bwd_gb300 import _lib
+        _lib.prof_start()
+        _, _, c2 = kda_forward_conv(x.to(dev), cw.to(dev), d["f"], d["b"], d["A_log"], d["dt_bias"], w.dk, w.dv,
+                                    scale=d["scale"], h0=d.get("h0"), cu_seqlens=d.get("cu_seqlens"),
+                                    cu_seqlens_host=cu_host)
+        kda_backward_conv(c2, dy.to(dev), d.get("dh_final"))
+        torch.cuda.synchronize()
+        launched = {k for k, v in _lib.prof_stop().items() if v[1]}
+        assert {"fwd_seg", "bwd_seg"} <= launched, launched
     N, H, dk, dv = w.B * w.T, w.H, w.dk, w.dv
     C = H * (2 * dk + dv)
 
