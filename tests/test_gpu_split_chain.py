@@ -13,9 +13,10 @@ the composites before it (after it, in the backward) folded onto h0
 (description: the recurrent state resets at document boundaries) fixes what
 a packed document must equal: the same document run alone.
 
-Cases force the split at H = 2 (a few chains on the whole GPU): a long
+Cases force the split at H = 2 or 1 (a few chains on the whole GPU): a long
 document packed with one-token, empty and short ones; long equal rows;
-exactly 33 chunks (segments of 16, 16 and 1); the scalar gate.  Forward and
+exactly 33 chunks (segments of 16, 16 and 1); the scalar gate; no states; a
+301-chunk document (segments of 32 chunks, folds of up to nine).  Forward and
 backward (with h0 and dS_final) are compared with the oracle at the parity
 tolerances; the grid planned on the host (host copy of cu_seqlens) and on the
 device (device-only offsets) give the same bits; a packed long document equals
@@ -39,6 +40,11 @@ CASES = {
     "rows_51_chunks": (custom(2, 64 * 50 + 5, 2, 32, 64, h0=True, dh_final=True), 62, None),
     "exactly_33_chunks": (custom(1, 64 * 32 + 1, 2, 32, 64, h0=True, dh_final=True), 63, None),
     "scalar_gate_long": (custom(1, 64 * 40 + 30, 2, 32, 64, gate="scalar", h0=True, dh_final=True), 64, None),
+    # no initial state and no final-state gradient: the folds start from zero
+    "packed_no_states": (custom(1, 64 * 45 + 200, 2, 32, 64), 66, [64 * 45, 150, 50]),
+    # 301 chunks: segments of 32 chunks (the least multiple of 16 whose square covers 301), ten of
+    # them, folds of up to nine composites
+    "very_long_doc": (custom(1, 64 * 300 + 7, 1, 32, 64, h0=True, dh_final=True), 67, None),
 }
 
 
