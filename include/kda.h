@@ -117,7 +117,16 @@ KDA_API size_t kda_workspace_size(const kda_problem* p, int for_backward);
  * initial state).  With save_for_backward = 1 the workspace (sized with
  * for_backward = 1) keeps what kda_bwd needs; it must then be passed to
  * kda_bwd unmodified, with the same inputs.  Streams: stream 0 is the legacy
- * default stream. */
+ * default stream.
+ * bf16 io at dk=32/dv=64: when the batch is chain-bound (its longest document
+ * has more than 32 chunks of 64 tokens and more than twice the average chain
+ * length per resident chain CTA of the device), documents of more than 32
+ * chunks run their state chains as segments composed in parallel and folded
+ * onto h0 (the same map, a different rounding order: such a document's last
+ * bits can differ from its run in a batch that is not chain-bound).  The plan
+ * depends on the device's SM count; kda_bwd on a device that plans
+ * differently refuses the workspace (KDA_ERR_WORKSPACE from
+ * kda_device_status). */
 KDA_API kda_status kda_fwd(const kda_problem* p,
                    const void* q, const void* k, const void* v, const void* f, const void* b,
                    const float* A_log, const float* dt_bias, const float* h0,
@@ -126,7 +135,8 @@ KDA_API kda_status kda_fwd(const kda_problem* p,
                    cudaStream_t stream);
 
 /* Backward of the loss sum(o * dO) + sum(h_final * dh_final).  Requires the
- * workspace filled by kda_fwd(save_for_backward = 1) on the same inputs.
+ * workspace filled by kda_fwd(save_for_backward = 1) on the same inputs (and
+ * a device of the same SM count, see kda_fwd).
  * dh_final may be NULL (zero); dh0 may be NULL (not returned).  Writes dq,
  * dk, dv, df, db (dtype), dA_log [H] and ddt_bias [H, dk] (fp32, summed over
  * all tokens in a fixed order: deterministic). */
