@@ -344,20 +344,13 @@ static Ws bind(void* ws, const Layout& L, const Dims& d, int for_bwd) {
 // Failure-detection test hook (kda_test_stage_timeout); 0 in normal use.
 static int g_test_tx_extra = 0;
 
-// The tensor-core forward chain's grid (without the fused norm, whose chains
+// The tensor-core state chains' grids (without the fused norm, whose chains
 // stay whole): whether long chains may be split into segments (Dims::seg) and
-// how many units the grid covers (Dims::nu).  With the lengths known on the
+// how many units the grids cover (Dims::nu).  With the lengths known on the
 // host (equal rows, or a host copy of cu_seqlens) the rule of seg_split is
 // applied here and the grid is exact; with device-only offsets the chunk
 // table applies it and the grid covers the most units any offsets can give.
-static void plan_chain_split_(const kda_problem* p, Dims& d);
-static void plan_chain_split(const kda_problem* p, Dims& d) {
-  plan_chain_split_(p, d);
-  // the backward reads the forward's segment table: a plan that differs (another device's SM
-  // count) makes a different saved-problem tag, so that the backward refuses the workspace
-  if (d.seg) d.tag ^= (int32_t)(((uint32_t)d.nu * 2654435761u) << 4 | 8u);
-}
-static void plan_chain_split_(const kda_problem* p, Dims& d) {
+static void chain_split_rule(const kda_problem* p, Dims& d) {
   d.seg = 0;
   d.nu = d.n_docs;
   if (!d.fast || d.norm) return;
@@ -386,6 +379,15 @@ static void plan_chain_split_(const kda_problem* p, Dims& d) {
   if (units > grid_max) return;
   d.seg = 1;
   d.nu = (int)units;
+}
+
+// The plan of chain_split_rule, for the forward and again for its backward,
+// which reads the forward's segment table: a plan that differs (another
+// device's SM count) makes a different saved-problem tag, so that the
+// backward refuses the workspace.
+static void plan_chain_split(const kda_problem* p, Dims& d) {
+  chain_split_rule(p, d);
+  if (d.seg) d.tag ^= (int32_t)(((uint32_t)d.nu * 2654435761u) << 4 | 8u);
 }
 
 // The forward launch sequence shared by kda_fwd and kda_fwd_noalloc.

@@ -1269,10 +1269,11 @@ __device__ __forceinline__ void slice_to_global(bf16* g, const bf16* s, int col0
   }
 }
 
-// The forward chain grids with split chains (Dims::seg): one dimension, CTA
-// i = (rank, head, column half) with the half fastest (the two halves of a
-// chunk read the same M and QW), ranks in the segment table's dispatch order
-// (heaviest units first).  Without seg: (document, head, half) as blockIdx.
+// The state chains' grids (fwd_seg, fwd_state, bwd_seg, bwd_scan) with split
+// chains (Dims::seg): one dimension, CTA i = (rank, head, column half) with
+// the half fastest (the two halves of a chunk read the same M and QW), ranks
+// in the segment table's dispatch order (heaviest units first).  Without seg:
+// (document, head, half) as blockIdx.
 struct ChainCta {
   int unit, h, half;
 };

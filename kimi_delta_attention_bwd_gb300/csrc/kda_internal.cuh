@@ -39,17 +39,18 @@ enum KernelId {
   K_COUNT
 };
 
-// Splitting long forward chains (tensor-core path).  The forward state chain
-// is affine, S_{c+1} = M_c S_c + KU_c, so a run of chunks composes into one map
-// S -> Phi S + B.  When a workload's longest document has more than SPLIT_MIN
-// chunks and more than twice the average chain length per resident chain CTA
-// (a chain-bound workload: a few long chains finish long after the rest),
-// every document of more than SPLIT_MIN chunks is cut into segments of
-// seg_len(n_max) chunks.  One kernel composes each segment but a document's
-// last; the chain kernel starts every later segment from its predecessors'
-// composites folded onto the document's initial state (one small product per
-// earlier segment, so segments grow with the longest document: about
-// sqrt(n_max) chunks, at least SEG).  The same rule runs on the host (to size
+// Splitting long state chains (tensor-core path).  The forward state chain is
+// affine, S_{c+1} = M_c S_c + KU_c, so a run of chunks composes into one map
+// S -> Phi S + B; so is the backward's reverse chain (dS -> Psi dS + D).  When
+// a workload's longest document has more than SPLIT_MIN chunks and more than
+// twice the average chain length per resident chain CTA (a chain-bound
+// workload: a few long chains finish long after the rest), every document of
+// more than SPLIT_MIN chunks is cut into segments of seg_len(n_max) chunks.
+// Per direction one kernel composes each segment but the one its chain starts
+// in; the chain kernel starts every other segment from the composites on its
+// way folded onto the document's initial state (final-state gradient): one
+// small product per segment, so segments grow with the longest document, about
+// sqrt(n_max) chunks and at least SEG.  The same rule runs on the host (to size
 // the launch) and in the chunk-table kernel (to build the segment table).
 constexpr int SEG = 16, SPLIT_MIN = 32;
 __host__ __device__ inline bool seg_split(int n_max, long long total_chunks, int H, int slots) {
@@ -79,10 +80,10 @@ struct Ws {
   int32_t* chunk_len;   // [nc_max] tokens in the chunk (1..C), 0 = unused
   int32_t* chunk_doc;   // [nc_max]
   int32_t* doc_order;   // [n_docs] documents by decreasing chunk count (the general scans' dispatch order)
-  // tensor-core forward chains split into segments (Dims::seg): per unit (document, first chunk
+  // tensor-core state chains split into segments (Dims::seg): per unit (document, first chunk
   // within it, chunks, segment index), a document's segments consecutive; the unit count; and
-  // per unit and head the composite [Phi | B] ([dk][dk] then [dk][dv], fp32) of every
-  // segment but a document's last
+  // per unit and head a composite ([dk][dk] then [dk][dv], fp32): in the forward [Phi | B] of
+  // every segment but a document's last, in the backward [Psi | D] of every segment but its first
   int4* useg;
   int32_t* uorder;  // units by decreasing work (chunks plus folded segments): the chain grids' dispatch order
   int32_t* n_units;
