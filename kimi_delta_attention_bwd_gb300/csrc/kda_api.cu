@@ -73,6 +73,9 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* cu, Di
   __shared__ int s_cnt[ORD_BUCKETS];
   __shared__ int s_carry;
   __shared__ int s_wsum[32];
+  // With equal rows the tensor-core fwd_chunk reads no table and runs alongside this kernel (it
+  // waits for this grid only before it ends): the error word is reset before it may launch.
+  if (d.rows && threadIdx.x == 0) *w.err = KDA_OK;
   pdl_release();  // fwd_chunk may launch; it waits for this table before reading it
   const int tid = threadIdx.x, n = d.n_docs;
   auto off = [&](int i) -> int { return cu ? cu[i] : i * d.T; };
@@ -106,7 +109,7 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t* cu, Di
   if (tid == 0) {
     w.doc_chunk0[n] = s_carry;
     *w.n_chunks = s_carry;
-    *w.err = KDA_OK;
+    if (!d.rows) *w.err = KDA_OK;  // (equal rows: reset above)
     *w.tag = d.save ? d.tag : 0;
   }
   for (int i = tid; i < n; i += blockDim.x) {
@@ -458,6 +461,7 @@ static kda_status check_problem(const kda_problem* p, Dims* d) {
   d->norm = 0;
   d->conv = 0;
   d->tx_extra = 0;
+  d->rows = p->cu_seqlens ? 0 : 1;
   d->seg = 0;
   d->nu = n_docs;
   d->slots = 0;

@@ -856,12 +856,37 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
   extern __shared__ __align__(128) unsigned char smraw[];
   ChunkSm& sm = *reinterpret_cast<ChunkSm*>(smraw);
   const int j = (int)(blockIdx.x / (unsigned)d.H), h = (int)(blockIdx.x % (unsigned)d.H), tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  pdl_wait();     // the chunk table of the kernel before
-  pdl_release();  // fwd_state may launch (it waits for this grid)
+  // Equal rows (d.rows): chunk j is chunk j % nr of row j / nr, so this kernel reads no table and
+  // runs alongside the chunk-table kernel; it waits for that grid before it ends, so that the
+  // kernels after it find the table complete.  Otherwise it waits for the table first.
+  const bool rows = d.rows != 0;
+  if (!rows) pdl_wait();  // the chunk table of the kernel before
+  pdl_release();          // fwd_state may launch (it waits for this grid)
   int j2, h2;
   const bool pf = ahead_of(d, j, h, j2, h2);
-  const int err = *w.err, L = w.chunk_len[j], t0 = w.chunk_tok0[j];  // one round trip
-  const int L2 = pf ? w.chunk_len[j2] : 0, t2 = pf ? w.chunk_tok0[j2] : 0;
+  int err = 0, L, t0, L2 = 0, t2 = 0;
+  if (rows) {
+    const int nr = (d.T + C - 1) / C;
+    auto at = [&](int jj, int& len, int& tok) {
+      const int c = jj % nr;
+      tok = (jj / nr) * d.T + c * C;
+      len = min(C, d.T - c * C);
+    };
+    at(j, L, t0);
+    if (pf) at(j2, L2, t2);
+  } else {
+    err = *w.err;
+    L = w.chunk_len[j];
+    t0 = w.chunk_tok0[j];  // one round trip
+    L2 = pf ? w.chunk_len[j2] : 0;
+    t2 = pf ? w.chunk_tok0[j2] : 0;
+  }
+  struct TableWait {  // (equal rows) wait for the chunk-table grid on every way out
+    bool on;
+    __device__ ~TableWait() {
+      if (on) pdl_wait();
+    }
+  } table_wait{rows};
   if (err != 0 || L <= 0) return;
   const int H = d.H;
   const int64_t ch = (int64_t)j * H + h;
@@ -894,7 +919,7 @@ __global__ void __launch_bounds__(NTH, 2) fwd_chunk_kernel(Dims d, FwdIO io, Ws 
     prefetch_rows(io.f, gdn ? 1 : DK, t2, L2, H, h2);
     prefetch_rows(io.b, 1, t2, L2, H, h2);
   }
-  const int tmin = CONV ? conv_tmin(w, j, t0) : t0;
+  const int tmin = !CONV ? t0 : rows ? (j % ((d.T + C - 1) / C) > 0 ? t0 - 3 : t0) : conv_tmin(w, j, t0);
 
   const Op LQ{sm.x, sm.x + 2048, DK}, LK{sm.x + 4096, sm.x + 6144, DK}, R{sm.x + 8192, sm.x + 13312, DK};
   // [XK | XV] and [W | U] are single 96-column tiles (one tensor-core operand

@@ -138,6 +138,7 @@ struct Dims {
   int32_t conv;  // the short convolution is fused into the per-chunk kernels' prologue (tensor-core path)
   int32_t tx_extra;  // failure-detection test hook (kda_test_stage_timeout): bytes the forward chain's stage
                      // barriers expect beyond what their copies deliver; 0 outside that test
+  int32_t rows;   // no cu_seqlens: the documents are the B rows of T tokens (chunk j's tokens follow from j)
   int32_t seg;    // (tensor-core chains) the chunk table decides whether to split long chains (seg_split)
   int32_t nu;     // units of the forward chain grid: documents, or with seg an upper bound on the segments
   int32_t slots;  // resident forward chain CTAs on the device (the split rule's denominator)
