@@ -347,16 +347,17 @@ static Ws bind(void* ws, const Layout& L, const Dims& d, int for_bwd) {
 // Failure-detection test hook (kda_test_stage_timeout); 0 in normal use.
 static int g_test_tx_extra = 0;
 
-// The tensor-core state chains' grids (without the fused norm, whose chains
-// stay whole): whether long chains may be split into segments (Dims::seg) and
-// how many units the grids cover (Dims::nu).  With the lengths known on the
+// The tensor-core state chains' grids: whether long chains may be split into
+// segments (Dims::seg) and how many units the grids cover (Dims::nu).  (With
+// the fused norm only the forward chain splits: the reverse chain forms dO
+// itself, which the backward's composites would need beforehand.)  With the lengths known on the
 // host (equal rows, or a host copy of cu_seqlens) the rule of seg_split is
 // applied here and the grid is exact; with device-only offsets the chunk
 // table applies it and the grid covers the most units any offsets can give.
 static void chain_split_rule(const kda_problem* p, Dims& d) {
   d.seg = 0;
   d.nu = d.n_docs;
-  if (!d.fast || d.norm) return;
+  if (!d.fast) return;
   d.slots = fast_chain_slots();
   if (d.slots <= 0) return;
   const long long grid_max = 2147483647LL / (2LL * d.H);  // the split grids are one-dimensional

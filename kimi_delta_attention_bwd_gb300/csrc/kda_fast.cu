@@ -1433,14 +1433,17 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
   const int err0 = *w.err;
   if (!NORM && err0 != 0) return;
   const int H = d.H;
-  const ChainCta cc = chain_cta(d, w);  // (NORM runs without d.seg)
+  const ChainCta cc = chain_cta(d, w);
   const int h = cc.h, zc = cc.half, col0 = zc * NSC;
   // this CTA's run of chunks: a whole document, or with d.seg one unit of the segment table
   // (segment sg of its document, chunks c0 ..; `last`: the run ends the document)
   int doc = cc.unit, cb, n, sg = 0;
   bool last = true;
-  if (!NORM && d.seg) {
-    if (cc.unit < 0) return;
+  if (d.seg && err0 != 0) {  // (NORM) the table may be stale: no steps, to the cluster barriers
+    doc = 0;
+    cb = n = 0;
+  } else if (d.seg) {
+    if (cc.unit < 0) return;  // (NORM: both CTAs of the cluster, the same rank)
     const int4 un = w.useg[cc.unit];
     doc = un.x;
     sg = un.w;
@@ -1526,7 +1529,7 @@ __global__ void __launch_bounds__(2 * CTH) fwd_state_kernel(Dims d, FwdIO io, Ws
     }
   };
   for (int s = 0; s < NS - 1; s++) prefetch(s);
-  if (!NORM && sg > 0) {
+  if (sg > 0) {
     // entry state of segment sg: the composites of the document's earlier segments (the units
     // cc.unit - sg ..) folded onto the initial state.  Scratch: the ring's last slot, whose first
     // copy is issued in step 0 (after this).
@@ -3357,19 +3360,19 @@ cudaError_t launch_fast_fwd(const Dims& d0, const FwdIO& io, const Ws& w, cudaSt
   static_assert(fast::DV / fast::NSC == 2, "two column halves");
   const dim3 grid = d.seg ? dim3((unsigned)d.nu * d.H * 2) : dim3(d.n_docs, d.H, 2);
   NMaps nm = {};
-  if (d.norm) {  // the two column halves of a (document, head) as one cluster
+  if (d.seg) {  // the segments' composites first
+    prof_begin(K_FWD_SEG, st);
+    e = launch_pdl(fast::fwd_seg_kernel, grid, dim3(fast::CTH), sizeof(fast::SegSm), st, d, io, w);
+    prof_end(K_FWD_SEG, st);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (d.norm) {  // the two column halves of a (document, head, or segment) as one cluster
     if (!encode_nmaps(&nm, io.ng, nullptr, nullptr, d.Ntok, d.H, fast::DV)) return cudaErrorInvalidValue;
     prof_begin(K_FWD_STATE_NORM, st);
     e = launch_cluster(fast::fwd_state_kernel<true>, grid, dim3(2 * fast::CTH), s2n, st, 2, true, d, io, w, nm);
     prof_end(K_FWD_STATE_NORM, st);
   } else {
-    if (d.seg) {  // the segments' composites first
-      prof_begin(K_FWD_SEG, st);
-      e = launch_pdl(fast::fwd_seg_kernel, grid, dim3(fast::CTH), sizeof(fast::SegSm), st, d, io, w);
-      prof_end(K_FWD_SEG, st);
-      if (e == cudaSuccess) e = cudaGetLastError();
-      if (e != cudaSuccess) return e;
-    }
     prof_begin(K_FWD_STATE, st);
     e = launch_pdl(fast::fwd_state_kernel<false>, grid, dim3(2 * fast::CTH), s2, st, d, io, w, nm);
     prof_end(K_FWD_STATE, st);

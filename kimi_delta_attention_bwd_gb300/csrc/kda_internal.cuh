@@ -245,10 +245,11 @@ inline cudaError_t launch_cluster(void (*k)(KArgs...), dim3 grid, dim3 block, si
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
-  at[1].id = cudaLaunchAttributeClusterDimension;
-  at[1].val.clusterDim.x = 1;
+  at[1].id = cudaLaunchAttributeClusterDimension;  // cz CTAs along z, or along x for a 1-D grid
+  const bool along_x = grid.y == 1 && grid.z == 1;
+  at[1].val.clusterDim.x = along_x ? cz : 1;
   at[1].val.clusterDim.y = 1;
-  at[1].val.clusterDim.z = cz;
+  at[1].val.clusterDim.z = along_x ? 1 : cz;
   cfg.attrs = pdl ? at : at + 1;
   cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, k, args...);

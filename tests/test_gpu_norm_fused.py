@@ -41,6 +41,10 @@ CASES = {
     "composed_fp32": (custom(1, 192, 2, 32, 64, dtype="f32", h0=True, dh_final=True), 35, None),
     # the 300M layer shape the bench times (16 x 2048, H 8), with states
     "full_300M_16x2048": (custom(16, 2048, 8, 32, 64, h0=True, dh_final=True), 38, None),
+    # a 41-chunk document packed with short ones, two heads: the forward chain runs it as composed
+    # segments (the reverse chain, which forms dO itself, stays whole)
+    "long_doc_split_forward": (custom(1, 64 * 40 + 17 + 150, 2, 32, 64, h0=True, dh_final=True), 39,
+                               [64 * 40 + 17, 1, 0, 149]),
 }
 
 
@@ -64,6 +68,16 @@ def test_fused_norm_matches_composed_oracles(name):
                                           cu_seqlens=d.get("cu_seqlens"), cu_seqlens_host=cu_host, want_o=True)
     gr = kda_backward_norm_gate(ctx, dy.to(dev), d.get("dh_final"))
     torch.cuda.synchronize()
+    if name == "long_doc_split_forward":  # the forward chain splits, the reverse chain does not
+        from kimi_delta_attention_bwd_gb300 import _lib
+        _lib.prof_start()
+        _, _, _, c2 = kda_forward_norm_gate(d["q"], d["k"], d["v"], d["f"], d["b"], d["A_log"], d["dt_bias"],
+                                            g.to(dev), wn.to(dev), scale=d["scale"], h0=d.get("h0"),
+                                            cu_seqlens=d.get("cu_seqlens"), cu_seqlens_host=cu_host, want_o=True)
+        kda_backward_norm_gate(c2, dy.to(dev), d.get("dh_final"))
+        torch.cuda.synchronize()
+        launched = {k for k, v in _lib.prof_stop().items() if v[1]}
+        assert "fwd_seg" in launched and "bwd_seg" not in launched, launched
     N, H, dv = w.B * w.T, w.H, w.dv
 
     def host(t):
