@@ -43,6 +43,9 @@ CASES = {
     # run split into composed segments (the fused-norm chains never split)
     "long_doc_split_chains": (custom(1, 64 * 40 + 17 + 13, 2, 32, 64, h0=True, dh_final=True), 46,
                               [64 * 40 + 17, 13], False, None),
+    # the same with the norm: the forward chain (fused norm) splits, the reverse chain stays whole
+    "long_doc_split_norm": (custom(1, 64 * 36 + 40 + 1, 2, 32, 64, h0=True, dh_final=True), 47,
+                            [64 * 36 + 40, 1], True, None),
 }
 
 
@@ -77,16 +80,17 @@ def test_fused_conv_layer_matches_composed_oracles(name):
                                     cu_seqlens_host=cu_host)
     gr = kda_backward_conv(ctx, dy.to(dev), d.get("dh_final"))
     torch.cuda.synchronize()
-    if name == "long_doc_split_chains":  # the case does split both chains
+    if name.startswith("long_doc_split"):  # the case does split (the reverse chain only without the norm)
         from kimi_delta_attention_bwd_gb300 import _lib
         _lib.prof_start()
         _, _, c2 = kda_forward_conv(x.to(dev), cw.to(dev), d["f"], d["b"], d["A_log"], d["dt_bias"], w.dk, w.dv,
+                                    g=None if g is None else g.to(dev), w=None if wn is None else wn.to(dev),
                                     scale=d["scale"], h0=d.get("h0"), cu_seqlens=d.get("cu_seqlens"),
                                     cu_seqlens_host=cu_host)
         kda_backward_conv(c2, dy.to(dev), d.get("dh_final"))
         torch.cuda.synchronize()
         launched = {k for k, v in _lib.prof_stop().items() if v[1]}
-        assert {"fwd_seg", "bwd_seg"} <= launched, launched
+        assert "fwd_seg" in launched and ("bwd_seg" in launched) == (g is None), launched
     N, H, dk, dv = w.B * w.T, w.H, w.dk, w.dv
     C = H * (2 * dk + dv)
 

@@ -78,6 +78,16 @@ def test_fused_norm_matches_composed_oracles(name):
         torch.cuda.synchronize()
         launched = {k for k, v in _lib.prof_stop().items() if v[1]}
         assert "fwd_seg" in launched and "bwd_seg" not in launched, launched
+        # offsets on the device only: the device plans the split on the grid of the most units any
+        # offsets could give (the clusters past the last unit exit together); the same bits
+        y3, o3, hf3, c3 = kda_forward_norm_gate(d["q"], d["k"], d["v"], d["f"], d["b"], d["A_log"], d["dt_bias"],
+                                                g.to(dev), wn.to(dev), scale=d["scale"], h0=d.get("h0"),
+                                                cu_seqlens=d.get("cu_seqlens"), want_o=True)
+        gr3 = kda_backward_norm_gate(c3, dy.to(dev), d.get("dh_final"))
+        torch.cuda.synchronize()
+        assert torch.equal(y3, y) and torch.equal(o3, o) and torch.equal(hf3, hf)
+        for k2 in ("dO", "dg", "dw", "dq", "dk", "dv", "df", "db", "dA_log", "ddt_bias", "dh0"):
+            assert torch.equal(gr3[k2], gr[k2]), k2
     N, H, dv = w.B * w.T, w.H, w.dv
 
     def host(t):
