@@ -9,6 +9,7 @@ exact value, with rms(err)/rms(ref) <= 5e-3 as well), relative Frobenius
 error <= 2e-3 for the fp32 final state and dS0; the cu_seqlens segmentation
 itself is bit-exact.
 """
+import dataclasses
 import json
 import os
 
@@ -34,6 +35,18 @@ def test_workload_full_size(wi):
     gpu = run_gpu(inp, w.backward)
     ref = run_oracle(inp, w.backward)
     _report(w.name, compare(gpu, ref, w.backward, bf16=w.dtype == "bf16"))
+
+
+def test_varlen_workload_training_step_full_size():
+    """The packed varlen row (1 x 32768 tokens, H 8, 32/64, bf16) as a training
+    step, with dO: its 128-chunk document makes the batch chain-bound, so both
+    state chains run its long documents as composed segments.  Forward and
+    backward at full size against the oracle."""
+    w = dataclasses.replace(WORKLOADS[2], backward=True)
+    inp = make_inputs(w)
+    gpu = run_gpu(inp, True)
+    ref = run_oracle(inp, True)
+    _report(w.name + " (fwd+bwd)", compare(gpu, ref, True))
 
 
 def test_workload4_sampled_heads():
@@ -100,19 +113,22 @@ def test_general_path_packed_equals_separate_bitwise():
 
 
 def test_varlen_workload_segmentation_bitwise():
-    """Every document of the packed varlen workload equals its separate run."""
-    w = WORKLOADS[2]
+    """Every document of the packed varlen workload equals its separate run,
+    forward and backward (the long documents run as composed segments in both:
+    the packed row is chain-bound, and so is a lone document over 32 chunks)."""
+    w = dataclasses.replace(WORKLOADS[2], backward=True)
     inp = make_inputs(w)
-    packed = run_gpu(inp, False)
+    packed = run_gpu(inp, True)
     cu = inp["cu_seqlens"].numpy()
     for s in range(len(cu) - 1):
         t0, t1 = int(cu[s]), int(cu[s + 1])
         if t1 == t0:
             continue
-        sub = {k: (v[:, t0:t1].contiguous() if k in ("q", "k", "v", "f", "b") else v) for k, v in inp.items()}
+        sub = {k: (v[:, t0:t1].contiguous() if k in ("q", "k", "v", "f", "b", "dO") else v) for k, v in inp.items()}
         sub["cu_seqlens"] = None
-        one = run_gpu(sub, False)
-        assert np.array_equal(one["o"], packed["o"][t0:t1]), s
+        one = run_gpu(sub, True)
+        for n in ("o", "dq", "dk", "dv", "df", "db"):
+            assert np.array_equal(one[n], packed[n][t0:t1]), (s, n)
         assert np.array_equal(one["h_final"][0], packed["h_final"][s]), s
 
 
