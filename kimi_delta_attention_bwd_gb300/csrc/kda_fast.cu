@@ -2798,6 +2798,9 @@ struct GateSm {
   // kl = k^ 2^(G_last(I) - G), qf / kf = q^ / k^ 2^(G - G_first(I)) over the
   // row's 16-row block I (each at most |q^|, |k^|)
   float kl[C * DK], qf[C * DK], kf[C * DK];
+  // the pairwise terms' block-boundary factors, per key channel: 2^(G_last(J) - G_last(J - 1)) for
+  // J = 1..3, then 2^(G_first(I2 + 1) - G_first(I2)) for I2 = 0..2
+  float bfac[6][DK];
   int spanok[4];
   uint64_t bar;   // bulk-load completion of dP' and MA
   uint64_t tbar;  // (not CONV) the raw q, k, f tiles' tensor-map copies
@@ -2958,6 +2961,12 @@ __global__ void __launch_bounds__(NTH, CONV ? 2 : 3) bwd_gate_kernel(Dims d, Bwd
     add_warp_prefix(gv, sm.tot, warp, lane, q4);
     store_row8(sm.gg, r, q4, gv);
     __syncthreads();
+    if (tid < 6 * DK) {  // once per CTA instead of in every warp's block loop
+      const int f = tid / DK, i = tid % DK;
+      const float* ga = sm.gg + (f < 3 ? 16 * f + 31 : 16 * (f - 3) + 16) * SQ;
+      const float* gb = sm.gg + (f < 3 ? 16 * f + 15 : 16 * (f - 3)) * SQ;
+      sm.bfac[f][i] = ex2(ga[i] - gb[i]);
+    }
     const int I0 = r >> 4;
 #pragma unroll
     for (int e = 0; e < 8; e++) {
@@ -3017,14 +3026,23 @@ __global__ void __launch_bounds__(NTH, CONV ? 2 : 3) bwd_gate_kernel(Dims d, Bwd
         x[jj][2 + c1] *= f;
       }
   };
+  auto scalef = [&](float (&x)[2][4], const float* fac) {  // x *= fac per column
+#pragma unroll
+    for (int jj = 0; jj < 2; jj++)
+#pragma unroll
+      for (int c1 = 0; c1 < 2; c1++) {
+        const float f = fac[16 * hk + 8 * jj + 2 * tq + c1];
+        x[jj][c1] *= f;
+        x[jj][2 + c1] *= f;
+      }
+  };
   const int Jl = ok ? I : I - 1;  // the last block J of prow / arow
   for (int J = 0; J <= Jl; J++) {
     const float* DPb = sm.dp + blk_of(I, J) * 16 * PB;
     const float* MAb = sm.ma + blk_of(I, J) * 16 * PB;
-    if (J > 0) {
-      const float* geJ = sm.gg + (16 * J + 15) * SQ;
-      scale(prow, geJ, geJ - 16 * SQ);
-      scale(arow, geJ, geJ - 16 * SQ);
+    if (J > 0) {  // 2^(G_last(J) - G_last(J - 1))
+      scalef(prow, sm.bfac[J - 1]);
+      scalef(arow, sm.bfac[J - 1]);
     }
     rows16_2a<2>(prow, arow, 2, [&](int m, int k) { return DPb[m * PB + k]; },
                  [&](int m, int k) { return MAb[m * PB + k]; },
@@ -3038,7 +3056,7 @@ __global__ void __launch_bounds__(NTH, CONV ? 2 : 3) bwd_gate_kernel(Dims d, Bwd
   for (int I2 = 3; I2 >= Il; I2--) {
     const float* DPb = sm.dp + blk_of(I2, I) * 16 * PB;
     const float* MAb = sm.ma + blk_of(I2, I) * 16 * PB;
-    if (I2 < 3) scale(col, sm.gg + (16 * I2 + 16) * SQ, sm.gg + (16 * I2) * SQ);
+    if (I2 < 3) scalef(col, sm.bfac[3 + I2]);  // 2^(G_first(I2 + 1) - G_first(I2))
     rows16_ab<2>(col, 2, [&](int m, int k) { return DPb[k * PB + m]; },
                  [&](int m, int k) { return MAb[k * PB + m]; },
                  [&](int k, int jj, int n) {
