@@ -245,11 +245,12 @@ KDA_API kda_status kda_bwd_conv(const kda_problem* p, const void* x, const float
 KDA_API kda_status kda_device_status(const void* workspace, cudaStream_t stream);
 
 /* Failure-detection test hook.  Every wait of the library's kernels on an
- * mbarrier (bulk-copy completion, a cluster peer's data) gives up after a
- * quarter of a second; the kernel then flags KDA_ERR_DEVICE in the workspace's
+ * mbarrier (bulk-copy completion, a cluster peer's data) gives up after about
+ * a second; the kernel then flags KDA_ERR_DEVICE in the workspace's
  * error word, skips its remaining work and returns, leaving the context
  * usable.  While enable != 0, later tensor-core forwards (bf16, dk=32/dv=64)
- * make the state chain's stage barriers expect 16 bytes more than each copy
+ * make the forward state chain's stage barriers (and those of its composing
+ * kernel, when the chain runs split) expect 16 bytes more than each copy
  * delivers, so those waits run out (every copy issued still completes):
  * kda_device_status() then reports KDA_ERR_DEVICE, and the outputs are not
  * valid.  Off by default; process-wide, not thread-safe; for tests only. */
